@@ -1,0 +1,189 @@
+/*
+ * gbthist: level-batched (gradient, hessian) histogram construction for
+ * histogram gradient-boosted trees on one GB300 (sm_103a).
+ *
+ * C ABI. Plain pointers and sizes; no C++ or framework types cross it. Every
+ * call returns a gbt_status; nothing throws or aborts. Work is enqueued
+ * asynchronously on the stream given to gbt_create; device-side faults (a bin
+ * or row out of range, a quantisation overflow, a bounded wait that ran out,
+ * an inconsistent subtraction) set bits in a device error word that
+ * gbt_sync() reads and clears. There is no CPU fallback: every step of the
+ * path runs in this library's CUDA kernels.
+ *
+ * Pointer kinds. Arguments documented "host or device" are inspected with
+ * cudaPointerGetAttributes: device (or managed) memory is read in place, host
+ * memory is copied on the context stream first (pinned host memory keeps that
+ * copy asynchronous; pageable host memory makes it synchronous). Arguments
+ * documented "device" must be device memory.
+ *
+ * Histogram layout (the one global contiguous bin array of "GBDT engine
+ * engineering deep-dive" (ybb.press), section 1): int64
+ * hist[node][feature][slot][2] = (G, H), slot in [0, n_bins] where slot n_bins
+ * holds the rows whose bin is the missing sentinel. B = n_bins + 1 slots per
+ * feature. G and H are exact sums of fixed-point values (bonsai "9.
+ * Parallelism & determinism", "The idea": int64 cells give one integer in any
+ * order), so results are bit-identical run to run and to the serial oracle.
+ */
+#ifndef GBTHIST_H
+#define GBTHIST_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct gbt_ctx gbt_ctx;
+
+typedef enum {
+  GBT_OK = 0,
+  GBT_ERR_INVALID_ARG = 1,    /* a NULL, negative size, misaligned pointer or wrong pointer kind */
+  GBT_ERR_STATE = 2,          /* call out of order (no bins uploaded, no tree begun, sizes mismatch) */
+  GBT_ERR_OOM = 3,            /* a device or pinned allocation failed */
+  GBT_ERR_CUDA = 4,           /* a CUDA runtime call failed; gbt_last_error has the text */
+  GBT_ERR_BIN_RANGE = 5,      /* device: a bin value was neither < n_bins nor the sentinel */
+  GBT_ERR_ROW_RANGE = 6,      /* device: a row index was outside [0, n_rows), or offsets not ascending */
+  GBT_ERR_QUANT_OVERFLOW = 7, /* device: |g*scale| or |h*scale| >= 2^31, or not finite */
+  GBT_ERR_UNSUPPORTED = 8,    /* a size beyond this build's limits */
+  GBT_ERR_TIMEOUT = 9,        /* device: a bounded wait ran out */
+  GBT_ERR_INCONSISTENT = 10   /* device: subtraction produced a negative hessian cell */
+} gbt_status;
+
+/* The best split of one node. feature = -1 (and gain = -inf, sums 0) when no
+ * candidate is valid. Rows with slot <= bin go left; the missing slot goes
+ * left iff default_left = 1. Sums are the fixed-point left/right totals. */
+typedef struct {
+  int32_t feature;
+  int32_t bin;
+  uint8_t default_left;
+  uint8_t pad[7];
+  double gain;
+  int64_t g_left, h_left, g_right, h_right;
+} gbt_split; /* 56 bytes */
+
+/* lambda: L2 regulariser; gamma: per-split penalty; min_child_weight: minimum
+ * converted hessian on each side (0 disables). */
+typedef struct {
+  double lambda, gamma, min_child_weight;
+} gbt_params;
+
+/* Create a context on `device`, enqueuing on `cuda_stream` (a cudaStream_t;
+ * NULL = the legacy default stream). The context owns the binned-matrix
+ * mirror, the quantised gradients and scratch; the caller owns every input,
+ * output and histogram buffer. */
+gbt_status gbt_create(int device, void *cuda_stream, gbt_ctx **out);
+
+/* Synchronise the stream and free everything the context owns. NULL is a no-op. */
+gbt_status gbt_destroy(gbt_ctx *ctx);
+
+/* Text of the last host-side error on this context ("" if none). The pointer
+ * stays valid until the next call on the same context. Not thread-safe. */
+const char *gbt_last_error(const gbt_ctx *ctx);
+
+/* Wait for all enqueued work, then read and clear the device error word.
+ * Returns the first device error (in the order of the enum) or GBT_OK. */
+gbt_status gbt_sync(gbt_ctx *ctx);
+
+/* Upload the binned matrix once per dataset [bonsai "10: CUDA histogram
+ * backend", "The kernel": feature-major, uint8 when every feature fits 256
+ * bins, uint16 otherwise].
+ *   bins: host or device, feature-major [n_features][n_rows], bin_bytes each.
+ *   bin_bytes: 1 (then n_bins <= 255) or 2 (then n_bins <= 65535).
+ *   n_bins: real bins per feature; the histogram has n_bins + 1 slots.
+ *   missing_sentinel: the width's missing value [hessboost PR #163, "Change"]
+ *     (0xFF / 0xFFFF usually); must be >= n_bins and fit the width.
+ * The library copies the data into its own tiled row-major mirror (64-byte
+ * row strips per tile of features), validating every value on the device
+ * (GBT_ERR_BIN_RANGE). The caller may free `bins` after the call returns
+ * (device pointer) or after gbt_sync (host pointer).
+ * Limits: n_rows < 2^31, n_features < 2^24. */
+gbt_status gbt_upload_bins(gbt_ctx *ctx, const void *bins, int bin_bytes, int64_t n_rows, int32_t n_features,
+                           int32_t n_bins, uint32_t missing_sentinel);
+
+/* Begin a tree [bonsai "10: CUDA histogram backend", "The device context
+ * lifecycle": begin_tree takes the tree's gradients; "GBDT engine engineering
+ * deep-dive", section 7: gradients are quantised to fixed point for integer
+ * atomics].
+ *   gpair: host or device, packed float32 (g, h) pairs [n_rows][2].
+ *   scale_g, scale_h: fixed-point scales; q = round-half-even(float32(x * s)),
+ *     |q| < 2^31 (else GBT_ERR_QUANT_OVERFLOW on the device word).
+ * Read only during the call's stream work. */
+gbt_status gbt_begin_tree(gbt_ctx *ctx, const float *gpair, float scale_g, float scale_h);
+
+/* Suggest power-of-two scales such that `rows_per_partial` rows of the
+ * largest |g| (|h|) sum below 2^31 (the width of the kernels' per-chunk
+ * partial sums); rows_per_partial <= 0 means 65536. A larger scale is always
+ * correct; it only makes the build split nodes into more row chunks. */
+gbt_status gbt_suggest_scales(int64_t rows_per_partial, float max_abs_g, float max_abs_h, float *scale_g,
+                              float *scale_h);
+
+/* Build the histograms of a batch of nodes in one pass [bonsai "10: CUDA
+ * histogram backend", "Level batching": every smaller sibling of a level in
+ * one pass; "GBDT engine engineering deep-dive", section 1: for each row add
+ * (g, h) into its bin of every feature].
+ *   rows: host or device int32 [node_offsets[n_nodes]] row ids of the batch,
+ *     node segments concatenated; rows within a node are unique, any order.
+ *     NULL = the identity list (position k is row k).
+ *   node_offsets: host or device int64 [n_nodes + 1], ascending, offsets[0] = 0.
+ *   hist_out: device, 16-byte aligned, [n_nodes][n_features][B][2] int64,
+ *     overwritten.
+ * Limits: n_nodes <= 65535; total rows < 2^31. */
+gbt_status gbt_build_level(gbt_ctx *ctx, const int32_t *rows, const int64_t *node_offsets, int32_t n_nodes,
+                           int64_t *hist_out);
+
+/* Sibling subtraction ["GBDT engine engineering deep-dive", section 3:
+ * hist(right) = hist(parent) - hist(left)]: large[p] = parent[parent_of[p]] -
+ * small[p] cell by cell, exact in int64. A negative hessian cell (impossible
+ * for consistent inputs) sets GBT_ERR_INCONSISTENT instead of being clamped.
+ *   parent_hist, small_hist, large_hist: device [..][n_features][B][2] int64,
+ *     16-byte aligned; large_hist may not alias the others.
+ *   parent_of: host or device int32 [n_pairs]; NULL = identity. */
+gbt_status gbt_subtract_siblings(gbt_ctx *ctx, const int64_t *parent_hist, const int32_t *parent_of,
+                                 const int64_t *small_hist, int64_t *large_hist, int32_t n_pairs);
+
+/* Best split per node ["GBDT engine engineering deep-dive", section 1: gain
+ * = 1/2 [GL^2/(HL+lambda) + GR^2/(HR+lambda) - (GL+GR)^2/(HL+HR+lambda)] -
+ * gamma, cuts on bin boundaries; section 4: missing goes wholly left or right,
+ * the larger gain wins; bonsai "9. Parallelism & determinism", "In bonsai":
+ * ties break as a serial scan in feature order].
+ * Candidates: cut t in [0, n_bins-1] (slots <= t left) x {missing right,
+ * missing left}; valid iff both sides' quantised H > 0 and both converted
+ * H >= min_child_weight; values convert as (double)x * (1/(double)scale);
+ * the first strictly larger gain in (feature, t, right-before-left) order wins.
+ *   hist: device [n_nodes][n_features][B][2] int64.
+ *   out: host or device gbt_split [n_nodes] (host: valid after gbt_sync). */
+gbt_status gbt_find_splits(gbt_ctx *ctx, const int64_t *hist, int32_t n_nodes, const gbt_params *params,
+                           gbt_split *out);
+
+/* gbt_subtract_siblings and gbt_find_splits for both siblings in one pass
+ * over the parent and small histograms: small_out[p] is the split of
+ * small_hist[p], large_out[p] of large_hist[p]. Outputs as above. */
+gbt_status gbt_subtract_and_find(gbt_ctx *ctx, const int64_t *parent_hist, const int32_t *parent_of,
+                                 const int64_t *small_hist, int64_t *large_hist, int32_t n_pairs,
+                                 const gbt_params *params, gbt_split *small_out, gbt_split *large_out);
+
+/* Route each node's rows to its children [bonsai "10: CUDA histogram
+ * backend", "The device context lifecycle": partition_level routes each parent
+ * segment into stable left and right child segments]. Node i's rows go to
+ * child 2i (slot(bin[feature][row]) <= bin, or missing with default_left) or
+ * 2i+1 (otherwise), keeping their order; a node with feature = -1 sends every
+ * row left.
+ *   rows: host or device int32 [node_offsets[n_nodes]]; NULL = identity.
+ *   node_offsets: host or device int64 [n_nodes + 1], offsets[0] = 0.
+ *   splits: host or device gbt_split [n_nodes].
+ *   out_rows: device int32 [node_offsets[n_nodes]]; must not alias rows.
+ *   out_offsets: device int64 [2 * n_nodes + 1]. */
+gbt_status gbt_partition_level(gbt_ctx *ctx, const int32_t *rows, const int64_t *node_offsets, int32_t n_nodes,
+                               const gbt_split *splits, int32_t *out_rows, int64_t *out_offsets);
+
+/* B = n_bins + 1 of the uploaded matrix, or -1 before gbt_upload_bins. */
+int32_t gbt_slots_per_feature(const gbt_ctx *ctx);
+
+/* Number of CUDA kernels this context has launched (for launch accounting). */
+int64_t gbt_kernel_launches(const gbt_ctx *ctx);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GBTHIST_H */

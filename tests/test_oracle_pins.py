@@ -1,0 +1,287 @@
+"""Pins of the CPU oracle against what the pages and mathematics fix (no GPU).
+
+Each test checks the oracle against something other than itself: hand-worked
+golden cases, numpy brute force on tiny inputs, closed forms, invariants, the
+exact-greedy special case, IEEE rounding facts, and the pages' printed sizes.
+"""
+import json
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+import synth
+
+GOLD = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _load(name):
+    with open(os.path.join(GOLD, name)) as f:
+        return json.load(f)
+
+
+# --------------------------------------------------------------------------- quantisation
+@pytest.mark.parametrize(
+    "x,s,q",
+    [
+        (0.5, 1.0, 0), (1.5, 1.0, 2), (2.5, 1.0, 2), (-0.5, 1.0, 0), (-1.5, 1.0, -2), (-2.5, 1.0, -2),
+        (3.25, 4.0, 13), (0.1, 1024.0, 102), (-0.1, 1024.0, -102),
+        (2147483520.0, 1.0, 2147483520),  # largest float below 2^31
+        (-2147483520.0, 1.0, -2147483520),
+    ],
+)
+def test_quantise_round_half_even(oracle_mod, x, s, q):
+    """IEEE float32 product, then round-half-even to an integer (bonsai '9. Parallelism & determinism', 'The idea':
+    fixed-point cells; reading: ties to even)."""
+    out, st = oracle_mod.quantise(np.array([[x, x]], np.float32), s, s)
+    assert st == oracle_mod.OK
+    assert out[0, 0] == q and out[0, 1] == q
+
+
+@pytest.mark.parametrize("x", [2147483648.0, -2147483648.0, float("inf"), float("nan"), 3.0e9])
+def test_quantise_overflow_is_an_error(oracle_mod, x):
+    _, st = oracle_mod.quantise(np.array([[x, 0.0]], np.float32), 1.0, 1.0)
+    assert st == oracle_mod.ERR_QUANT
+
+
+def test_quantise_matches_numpy_rint(oracle_mod):
+    rng = np.random.default_rng(5)
+    gp = rng.standard_normal((4096, 2)).astype(np.float32)
+    s = np.float32(1000.0)
+    q, st = oracle_mod.quantise(gp, float(s), float(s))
+    assert st == oracle_mod.OK
+    ref = np.rint((gp * s).astype(np.float32)).astype(np.int32)  # numpy rint: half to even
+    np.testing.assert_array_equal(q, ref)
+
+
+# --------------------------------------------------------------------------- histogram build
+def _brute_hist(bins, n_bins, sentinel, q, rows, offs):
+    """int64 np.add.at per slot: the definition with a different library primitive."""
+    F, N = bins.shape
+    n_nodes = len(offs) - 1
+    out = np.zeros((n_nodes, F, n_bins + 1, 2), np.int64)
+    for n in range(n_nodes):
+        rr = np.arange(offs[n], offs[n + 1]) if rows is None else rows[offs[n]:offs[n + 1]]
+        for f in range(F):
+            b = bins[f, rr].astype(np.int64)
+            slot = np.where(b == sentinel, n_bins, b)
+            np.add.at(out[n, f, :, 0], slot, q[rr, 0].astype(np.int64))
+            np.add.at(out[n, f, :, 1], slot, q[rr, 1].astype(np.int64))
+    return out
+
+
+@pytest.mark.parametrize("width", [1, 2])
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_build_matches_brute_force(oracle_mod, width, seed):
+    rng = np.random.default_rng(100 + seed)
+    N, F, n_bins = 64, 4, 8
+    sentinel = 0xFF if width == 1 else 0xFFFF
+    dt = np.uint8 if width == 1 else np.uint16
+    bins = rng.integers(0, n_bins, size=(F, N)).astype(dt)
+    bins[rng.random((F, N)) < 0.2] = sentinel
+    q = rng.integers(-1000, 1000, size=(N, 2)).astype(np.int32)
+    perm = rng.permutation(N).astype(np.int32)
+    rows = perm[:50]
+    offs = np.array([0, 7, 7, 30, 50], np.int64)  # includes an empty node
+    got, st = oracle_mod.build_hist(bins, n_bins, sentinel, q, rows, offs)
+    assert st == oracle_mod.OK
+    np.testing.assert_array_equal(got, _brute_hist(bins, n_bins, sentinel, q, rows, offs))
+    got2, st = oracle_mod.build_hist(bins, n_bins, sentinel, q, None, np.array([0, 20, 64]))
+    assert st == oracle_mod.OK
+    np.testing.assert_array_equal(got2, _brute_hist(bins, n_bins, sentinel, q, None, np.array([0, 20, 64])))
+
+
+def test_build_feature_totals_equal_node_total(oracle_mod):
+    """Every row lands in exactly one slot of every feature: per-feature totals equal sum of q over the node."""
+    w = synth.make("u16miss", n_rows=3000, n_features=5, depth=3)
+    q, st = oracle_mod.quantise(w.gpair, 4096.0, 4096.0)
+    lv = w.levels[3]
+    hist, st = oracle_mod.build_hist(w.bins, w.n_bins, w.sentinel, q, lv.rows, lv.offsets)
+    assert st == oracle_mod.OK
+    for n in range(lv.n_nodes):
+        rr = lv.rows[lv.offsets[n]:lv.offsets[n + 1]]
+        tot = q[rr].astype(np.int64).sum(axis=0)
+        np.testing.assert_array_equal(hist[n].sum(axis=1), np.broadcast_to(tot, (w.n_features, 2)))
+
+
+def test_build_constant_hessian_is_count_times_q(oracle_mod):
+    """Constant h (0.25): every H cell is count x q(0.25) exactly, counts from an independent bincount."""
+    w = synth.make("dense", n_rows=5000, n_features=6, depth=2)
+    s_h = 1024.0
+    q, st = oracle_mod.quantise(w.gpair, 1024.0, s_h)
+    assert st == oracle_mod.OK and np.all(q[:, 1] == 256)
+    lv = w.levels[2]
+    hist, st = oracle_mod.build_hist(w.bins, w.n_bins, w.sentinel, q, lv.rows, lv.offsets)
+    for n in range(lv.n_nodes):
+        rr = lv.rows[lv.offsets[n]:lv.offsets[n + 1]]
+        for f in range(w.n_features):
+            cnt = np.bincount(w.bins[f, rr], minlength=w.n_bins + 1)
+            np.testing.assert_array_equal(hist[n, f, :, 1], cnt * 256)
+
+
+def test_build_reports_bad_bin_and_row(oracle_mod):
+    bins = np.array([[0, 1, 9]], np.uint8)  # 9 is neither < n_bins=4 nor the sentinel
+    q = np.ones((3, 2), np.int32)
+    _, st = oracle_mod.build_hist(bins, 4, 0xFF, q, None, np.array([0, 3]))
+    assert st == oracle_mod.ERR_BIN
+    _, st = oracle_mod.build_hist(bins[:, :2], 4, 0xFF, q[:2], np.array([0, 5], np.int32), np.array([0, 2]))
+    assert st == oracle_mod.ERR_ROW
+
+
+# --------------------------------------------------------------------------- subtraction
+def test_subtraction_parent_equals_small_plus_large(oracle_mod):
+    """'GBDT engine engineering deep-dive', section 3: hist(parent) = hist(left) + hist(right). Build the
+    parent, both children directly; subtraction of the smaller must give the larger exactly."""
+    w = synth.make("level5", n_rows=4000, n_features=7, depth=3)
+    q, _ = oracle_mod.quantise(w.gpair, 2048.0, 2048.0)
+    par, ch = w.levels[2], w.levels[3]
+    hp, _ = oracle_mod.build_hist(w.bins, w.n_bins, w.sentinel, q, par.rows, par.offsets)
+    hc, _ = oracle_mod.build_hist(w.bins, w.n_bins, w.sentinel, q, ch.rows, ch.offsets)
+    small = hc[ch.small]
+    large, st = oracle_mod.subtract(hp, None, small)
+    assert st == oracle_mod.OK
+    np.testing.assert_array_equal(large, hc[ch.large])
+    np.testing.assert_array_equal(small + large, hp)
+    # parent_of mapping: reversed pair order
+    po = np.arange(len(ch.small))[::-1].astype(np.int32)
+    large2, st = oracle_mod.subtract(hp, po, hc[ch.small[::-1]])
+    np.testing.assert_array_equal(large2, hc[ch.large[::-1]])
+
+
+def test_subtraction_flags_negative_hessian(oracle_mod):
+    parent = np.zeros((1, 1, 2, 2), np.int64)
+    small = np.zeros_like(parent)
+    small[0, 0, 1, 1] = 3
+    _, st = oracle_mod.subtract(parent, None, small)
+    assert st == oracle_mod.ERR_INCONSISTENT
+
+
+# --------------------------------------------------------------------------- gain and split find
+def _frac(s):
+    return Fraction(s)
+
+
+def test_gain_closed_form_cases(oracle_mod):
+    for gl, hl, gr, hr, lam, gam, exact, _work in _load("gain_cases.json")["cases"]:
+        got = oracle_mod.gain(gl, hl, gr, hr, gl + gr, hl + hr, lam, gam)
+        assert got == pytest.approx(float(Fraction(exact)), rel=1e-14, abs=1e-15), (gl, hl, gr, hr, exact)
+
+
+def test_split_golden_cases(oracle_mod):
+    for case in _load("split_cases.json")["cases"]:
+        hist = np.array(case["hist"], np.int64)[None]
+        out, st = oracle_mod.find_splits(hist, case["n_bins"], case["lambda"], case["gamma"],
+                                         case["min_child_weight"], 1.0, 1.0)
+        assert st == oracle_mod.OK
+        e = case["expect"]
+        s = out[0]
+        for k in ("feature", "bin", "default_left", "g_left", "h_left", "g_right", "h_right"):
+            assert int(s[k]) == e[k], (case["name"], k)
+        if e["gain"] == "-inf":
+            assert s["gain"] == -np.inf
+        else:
+            assert s["gain"] == pytest.approx(float(Fraction(e["gain"])), rel=1e-14), case["name"]
+
+
+def test_split_golden_rows_case_builds_its_histogram(oracle_mod):
+    case = _load("split_cases.json")["cases"][0]
+    gp = np.array(case["rows_gh"], np.float32)
+    q, st = oracle_mod.quantise(gp, 1.0, 1.0)
+    bins = np.array(case["bins_feature_major"], np.uint8)
+    hist, st = oracle_mod.build_hist(bins, case["n_bins"], 0xFF, q, None, np.array([0, len(gp)]))
+    assert st == oracle_mod.OK
+    np.testing.assert_array_equal(hist[0], np.array(case["hist"], np.int64))
+
+
+def _exact_gain(gl, hl, gr, hr, lam):
+    return Fraction(1, 2) * (gl * gl / (hl + lam) + gr * gr / (hr + lam) - (gl + gr) ** 2 / (hl + hr + lam))
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_split_equals_exact_greedy_on_rank_bins(oracle_mod, seed):
+    """When each row's bin is the rank of its distinct value, histogram split finding equals exact greedy
+    ('GBDT engine engineering deep-dive', section 1): try every cut between sorted values, in exact
+    rational arithmetic, with missing rows sent wholly left or right (section 4)."""
+    rng = np.random.default_rng(700 + seed)
+    N, F = 24, 3
+    vals = np.stack([rng.permutation(N) for _ in range(F)]).astype(np.float64) + rng.random((F, N))
+    miss = rng.random((F, N)) < (0.25 if seed % 2 else 0.0)
+    g = rng.integers(-50, 50, N)
+    h = rng.integers(1, 20, N)
+    lam = Fraction(1)
+    best = None  # (gain, f, t, dir) in exact arithmetic; first strictly larger wins
+    cands = []
+    for f in range(F):
+        present = np.where(~miss[f])[0]
+        order = present[np.argsort(vals[f, present])]
+        gm, hm = int(g[miss[f]].sum()), int(h[miss[f]].sum())
+        G, H = int(g.sum()), int(h.sum())
+        for t in range(len(order)):
+            pg, ph = int(g[order[:t + 1]].sum()), int(h[order[:t + 1]].sum())
+            for d in (0, 1):
+                gl, hl = pg + (gm if d else 0), ph + (hm if d else 0)
+                gr, hr = G - gl, H - hl
+                if hl > 0 and hr > 0:
+                    cands.append((_exact_gain(Fraction(gl), hl, Fraction(gr), hr, lam), f, t, d))
+    for c in cands:
+        if best is None or c[0] > best[0]:
+            best = c
+    gains = sorted({c[0] for c in cands}, reverse=True)
+    if len(gains) > 1 and gains[0] - gains[1] < Fraction(1, 10 ** 9):
+        pytest.skip("near-tie between distinct exact gains")
+    # bins = rank among present values; missing -> sentinel
+    n_bins = N
+    bins = np.zeros((F, N), np.uint8)
+    for f in range(F):
+        present = np.where(~miss[f])[0]
+        ranks = np.empty(N, np.int64)
+        ranks[present[np.argsort(vals[f, present])]] = np.arange(len(present))
+        bins[f] = np.where(miss[f], 0xFF, ranks)
+    q = np.stack([g, h], 1).astype(np.int32)
+    hist, st = oracle_mod.build_hist(bins, n_bins, 0xFF, q, None, np.array([0, N]))
+    out, st = oracle_mod.find_splits(hist, n_bins, 1.0, 0.0, 0.0, 1.0, 1.0)
+    s = out[0]
+    # exact greedy's best threshold in value space corresponds to rank t in bin space
+    assert (int(s["feature"]), int(s["bin"]), int(s["default_left"])) == best[1:], (s, best)
+    assert s["gain"] == pytest.approx(float(best[0]), rel=1e-12)
+
+
+# --------------------------------------------------------------------------- partition
+def test_partition_matches_python_loop(oracle_mod):
+    rng = np.random.default_rng(9)
+    N, F, n_bins = 200, 3, 10
+    bins = rng.integers(0, n_bins, size=(F, N)).astype(np.uint16)
+    bins[rng.random((F, N)) < 0.3] = 0xFFFF
+    rows = rng.permutation(N)[:150].astype(np.int32)
+    offs = np.array([0, 40, 100, 150], np.int64)
+    splits = np.zeros(3, oracle_mod.SPLIT_DTYPE)
+    splits["feature"] = [1, -1, 2]
+    splits["bin"] = [4, -1, 0]
+    splits["default_left"] = [1, 0, 0]
+    got_rows, got_offs, st = oracle_mod.partition(bins, n_bins, 0xFFFF, rows, offs, splits)
+    assert st == oracle_mod.OK
+    exp_rows, exp_offs = [], [0]
+    for n in range(3):
+        seg = rows[offs[n]:offs[n + 1]]
+        f, t, d = int(splits["feature"][n]), int(splits["bin"][n]), int(splits["default_left"][n])
+        if f < 0:
+            left = list(seg)
+            right = []
+        else:
+            left = [r for r in seg if (bins[f, r] == 0xFFFF and d) or (bins[f, r] != 0xFFFF and bins[f, r] <= t)]
+            right = [r for r in seg if r not in left]
+        exp_rows += left
+        exp_offs.append(len(exp_rows))
+        exp_rows += right
+        exp_offs.append(len(exp_rows))
+    np.testing.assert_array_equal(got_rows, np.array(exp_rows, np.int32))
+    np.testing.assert_array_equal(got_offs, np.array(exp_offs, np.int64))
+
+
+# --------------------------------------------------------------------------- determinism of the oracle inputs
+def test_synth_is_seeded():
+    a = synth.make("root", n_rows=500, n_features=3)
+    b = synth.make("root", n_rows=500, n_features=3)
+    np.testing.assert_array_equal(a.bins, b.bins)
+    np.testing.assert_array_equal(a.gpair, b.gpair)
