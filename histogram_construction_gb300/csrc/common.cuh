@@ -1,0 +1,81 @@
+// Shared device-side definitions of the gbthist CUDA library (sm_103a).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace gbt {
+
+// Device error word bits (read and cleared by gbt_sync).
+enum : uint32_t {
+  ERRBIT_BIN = 1u << 0,
+  ERRBIT_ROW = 1u << 1,
+  ERRBIT_QUANT = 1u << 2,
+  ERRBIT_TIMEOUT = 1u << 3,
+  ERRBIT_INCONSISTENT = 1u << 4,
+};
+
+// Small device-resident state shared by the kernels of one context.
+struct DevState {
+  uint32_t err;        // error bits
+  uint32_t qmax;       // max |q| over the current tree's rows, both components
+  uint32_t work_next;  // dynamic work counter of the histogram kernel
+  uint32_t plan_ok;    // 1 when the level plan is valid
+  int64_t chunk_rows;  // rows per work item chunk (level plan)
+  int32_t n_items;     // work items of the level
+  int32_t pad;
+};
+
+// Per-feature split candidate written by the scan kernels.
+struct Cand {
+  double gain;
+  int32_t t;    // cut (INT32_MAX when no valid candidate)
+  int32_t dir;  // 0 missing right, 1 missing left
+};
+
+constexpr int MIRROR_STRIP_BYTES = 64;  // bytes per row per mirror tile of features
+
+__device__ __forceinline__ void raise_err(DevState *st, uint32_t bit) { atomicOr(&st->err, bit); }
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// Make generic-proxy shared-memory writes visible to the async (bulk copy) proxy.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Bulk copy shared -> global (TMA engine, no tensor map): bytes % 16 == 0, both 16-B aligned.
+__device__ __forceinline__ void bulk_store(void *gdst, const void *ssrc, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst), "r"(smem_addr(ssrc)),
+               "r"(bytes)
+               : "memory");
+}
+
+// Bulk reduce-add shared -> global of 64-bit integers (two's complement add).
+__device__ __forceinline__ void bulk_reduce_add_u64(void *gdst, const void *ssrc, uint32_t bytes) {
+  asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.u64 [%0], [%1], %2;" ::"l"(gdst),
+               "r"(smem_addr(ssrc)), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+
+// Wait until the committed bulk groups have finished reading shared memory.
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+
+// Wait until the committed bulk groups have completed.
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+__device__ __forceinline__ uint4 ldg_nc_v4(const void *p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ int4 ldg_v4s(const int4 *p) { return __ldg(p); }
+
+}  // namespace gbt

@@ -1,0 +1,770 @@
+// gbthist C-ABI: context, uploads, level build, subtraction, split find and
+// row partition on one GB300 (sm_103a). See include/gbthist.h for the contract.
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <math.h>
+#include <stdio.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include <algorithm>
+#include <map>
+#include <string>
+#include <vector>
+
+#include "../../include/gbthist.h"
+#include "common.cuh"
+#include "k_hist.cuh"
+#include "k_partition.cuh"
+#include "k_prep.cuh"
+#include "k_split.cuh"
+
+using namespace gbt;
+
+static_assert(sizeof(gbt_split) == 56, "gbt_split layout");
+static_assert(sizeof(SplitOut) == sizeof(gbt_split), "device split layout");
+
+namespace {
+
+// ---------------------------------------------------------------------------- allocation with fault injection
+// GBT_FAULT_ALLOC_AT="k[:tag]" makes the k-th device or pinned allocation
+// counted from the moment the variable took its current value fail with
+// GBT_ERR_OOM (host-side fault injection for tests; changing the value, e.g.
+// its tag, restarts the count).
+std::string g_fault_env;
+long long g_alloc_count = 0;
+
+bool alloc_should_fail() {
+  const char *e = getenv("GBT_FAULT_ALLOC_AT");
+  const std::string v = e ? e : "";
+  if (v != g_fault_env) {
+    g_fault_env = v;
+    g_alloc_count = 0;
+  }
+  ++g_alloc_count;
+  const long long at = v.empty() ? 0 : atoll(v.c_str());
+  return at > 0 && g_alloc_count == at;
+}
+
+cudaError_t dev_alloc(void **p, size_t bytes, cudaStream_t s) {
+  if (alloc_should_fail()) {
+    *p = nullptr;
+    return cudaErrorMemoryAllocation;
+  }
+  return cudaMallocAsync(p, bytes, s);
+}
+
+}  // namespace
+
+struct Buf {
+  void *p = nullptr;
+  size_t cap = 0;
+};
+
+struct gbt_ctx {
+  int device = 0;
+  cudaStream_t stream = nullptr;
+  int n_sm = 0;
+  int smem_optin = 0;
+  // dataset
+  int bin_bytes = 0;
+  int64_t n_rows = 0;
+  int32_t n_features = 0;
+  int32_t n_bins = 0;
+  uint32_t sentinel = 0;
+  int32_t n_tiles = 0;     // mirror tiles of 64-byte strips
+  int32_t tile_feats = 0;  // features per mirror tile
+  int32_t ts16 = 0;        // features per u16 work item
+  Buf mirror;
+  // tree
+  bool tree_ready = false;
+  float sg = 1.f, sh = 1.f;
+  double inv_sg = 1.0, inv_sh = 1.0;
+  Buf q;
+  // state + scratch
+  DevState *st = nullptr;
+  uint32_t *err_host = nullptr;  // pinned
+  Buf rec, chunk_prefix, rows_in, offs_in, cand, splits_a, splits_b, parent_of_in, tile_counts, lrank, slab;
+  std::string last_error;
+  int64_t launches = 0;
+  // diagnostics: per-launch event pairs
+  bool prof = false;
+  struct ProfRec {
+    const char *name;
+    cudaEvent_t a, b;
+  };
+  std::vector<ProfRec> prof_pending;
+  std::vector<cudaEvent_t> prof_pool;
+  cudaEvent_t prof_open = nullptr;
+};
+
+namespace {
+
+gbt_status fail(gbt_ctx *c, gbt_status s, const std::string &msg) {
+  if (c) c->last_error = msg;
+  return s;
+}
+
+gbt_status cuda_fail(gbt_ctx *c, cudaError_t e, const char *what) {
+  std::string m = std::string(what) + ": " + cudaGetErrorString(e);
+  if (e == cudaErrorMemoryAllocation) return fail(c, GBT_ERR_OOM, m);
+  return fail(c, GBT_ERR_CUDA, m);
+}
+
+#define CUDA_TRY(c, expr, what)                 \
+  do {                                          \
+    cudaError_t e_ = (expr);                    \
+    if (e_ != cudaSuccess) return cuda_fail(c, e_, what); \
+  } while (0)
+
+cudaEvent_t prof_event(gbt_ctx *c) {
+  if (!c->prof_pool.empty()) {
+    cudaEvent_t e = c->prof_pool.back();
+    c->prof_pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  cudaEventCreate(&e);
+  return e;
+}
+
+// Record the start event of a launch (diagnostics only).
+void prof_begin(gbt_ctx *c) {
+  if (!c->prof) return;
+  c->prof_open = prof_event(c);
+  cudaEventRecord(c->prof_open, c->stream);
+}
+
+void prof_end(gbt_ctx *c, const char *name) {
+  if (!c->prof || !c->prof_open) return;
+  cudaEvent_t b = prof_event(c);
+  cudaEventRecord(b, c->stream);
+  c->prof_pending.push_back({name, c->prof_open, b});
+  c->prof_open = nullptr;
+}
+
+// After a kernel launch: count it, close its profiling record, check the launch.
+#define LAUNCH_CHECK(c, what)                            \
+  do {                                                   \
+    ++(c)->launches;                                     \
+    prof_end((c), what);                                 \
+    cudaError_t e_ = cudaGetLastError();                 \
+    if (e_ != cudaSuccess) return cuda_fail(c, e_, what); \
+  } while (0)
+
+gbt_status ensure(gbt_ctx *c, Buf &b, size_t bytes, const char *what) {
+  if (bytes == 0) bytes = 16;
+  if (b.cap >= bytes) return GBT_OK;
+  if (b.p) {
+    cudaError_t e = cudaFreeAsync(b.p, c->stream);
+    b.p = nullptr;
+    b.cap = 0;
+    if (e != cudaSuccess) return cuda_fail(c, e, what);
+  }
+  void *p = nullptr;
+  cudaError_t e = dev_alloc(&p, bytes, c->stream);
+  if (e != cudaSuccess) return cuda_fail(c, e, what);
+  b.p = p;
+  b.cap = bytes;
+  return GBT_OK;
+}
+
+void release(gbt_ctx *c, Buf &b) {
+  if (b.p) cudaFreeAsync(b.p, c->stream);
+  b.p = nullptr;
+  b.cap = 0;
+}
+
+// 1 device/managed, 0 host, -1 invalid
+int ptr_kind(const void *p) {
+  if (!p) return -1;
+  cudaPointerAttributes a;
+  cudaError_t e = cudaPointerGetAttributes(&a, p);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return (a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged) ? 1 : 0;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Return a device pointer holding `bytes` of `src` (copied into `stage` when src is host memory).
+gbt_status device_view(gbt_ctx *c, const void *src, size_t bytes, Buf &stage, const void **out, const char *what) {
+  const int k = ptr_kind(src);
+  if (k < 0) return fail(c, GBT_ERR_INVALID_ARG, std::string(what) + ": NULL");
+  if (k == 1) {
+    *out = src;
+    return GBT_OK;
+  }
+  gbt_status s = ensure(c, stage, bytes, what);
+  if (s != GBT_OK) return s;
+  CUDA_TRY(c, cudaMemcpyAsync(stage.p, src, bytes, cudaMemcpyHostToDevice, c->stream), what);
+  *out = stage.p;
+  return GBT_OK;
+}
+
+gbt_status check_ctx(gbt_ctx *c) {
+  if (!c) return GBT_ERR_INVALID_ARG;
+  cudaError_t e = cudaSetDevice(c->device);
+  if (e != cudaSuccess) return cuda_fail(c, e, "cudaSetDevice");
+  c->last_error.clear();
+  return GBT_OK;
+}
+
+int grid_for(gbt_ctx *c, int64_t work, int threads, int per_sm) {
+  int64_t g = (work + threads - 1) / threads;
+  g = std::max<int64_t>(1, std::min<int64_t>(g, (int64_t)c->n_sm * per_sm));
+  return (int)g;
+}
+
+int h16_ts_for(int B) {
+  for (int ts = 32; ts >= 2; ts >>= 1)
+    if ((int64_t)ts * B * 8 <= H16_HIST_MAX) return ts;
+  return 0;
+}
+
+SplitParams make_sp(const gbt_ctx *c, const gbt_params *prm) {
+  SplitParams sp;
+  sp.lambda = prm->lambda;
+  sp.gamma = prm->gamma;
+  sp.mcw = prm->min_child_weight;
+  sp.inv_sg = c->inv_sg;
+  sp.inv_sh = c->inv_sh;
+  return sp;
+}
+
+}  // namespace
+
+extern "C" {
+
+gbt_status gbt_create(int device, void *cuda_stream, gbt_ctx **out) {
+  if (!out) return GBT_ERR_INVALID_ARG;
+  *out = nullptr;
+  int ndev = 0;
+  cudaError_t e = cudaGetDeviceCount(&ndev);
+  if (e != cudaSuccess) return e == cudaErrorMemoryAllocation ? GBT_ERR_OOM : GBT_ERR_CUDA;
+  if (device < 0 || device >= ndev) return GBT_ERR_INVALID_ARG;
+  if (cudaSetDevice(device) != cudaSuccess) return GBT_ERR_CUDA;
+  gbt_ctx *c = new gbt_ctx();
+  c->device = device;
+  c->stream = reinterpret_cast<cudaStream_t>(cuda_stream);
+  cudaDeviceGetAttribute(&c->n_sm, cudaDevAttrMultiProcessorCount, device);
+  cudaDeviceGetAttribute(&c->smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device);
+  void *st = nullptr;
+  e = dev_alloc(&st, sizeof(DevState), c->stream);
+  if (e != cudaSuccess) {
+    delete c;
+    return e == cudaErrorMemoryAllocation ? GBT_ERR_OOM : GBT_ERR_CUDA;
+  }
+  c->st = reinterpret_cast<DevState *>(st);
+  cudaMemsetAsync(c->st, 0, sizeof(DevState), c->stream);
+  if (alloc_should_fail() || cudaMallocHost(&c->err_host, sizeof(uint32_t)) != cudaSuccess) {
+    cudaFreeAsync(c->st, c->stream);
+    cudaStreamSynchronize(c->stream);
+    delete c;
+    return GBT_ERR_OOM;
+  }
+  *c->err_host = 0;
+  if (cudaFuncSetAttribute(k_hist_u8, cudaFuncAttributeMaxDynamicSharedMemorySize, H8_SMEM) != cudaSuccess ||
+      cudaFuncSetAttribute(k_hist_u16<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, H16_HIST_MAX + H16_STAGE_BYTES + 128) != cudaSuccess ||
+      cudaFuncSetAttribute(k_hist_u16<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, H16_HIST_MAX + H16_STAGE_BYTES + 128) != cudaSuccess ||
+      cudaFuncSetAttribute(k_hist_u16<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, H16_HIST_MAX + H16_STAGE_BYTES + 128) != cudaSuccess ||
+      cudaFuncSetAttribute(k_hist_u16<16>, cudaFuncAttributeMaxDynamicSharedMemorySize, H16_HIST_MAX + H16_STAGE_BYTES + 128) != cudaSuccess ||
+      cudaFuncSetAttribute(k_hist_u16<32>, cudaFuncAttributeMaxDynamicSharedMemorySize, H16_HIST_MAX + H16_STAGE_BYTES + 128) != cudaSuccess) {
+    cudaGetLastError();
+    cudaFreeHost(c->err_host);
+    cudaFreeAsync(c->st, c->stream);
+    cudaStreamSynchronize(c->stream);
+    delete c;
+    return GBT_ERR_CUDA;
+  }
+  *out = c;
+  return GBT_OK;
+}
+
+gbt_status gbt_destroy(gbt_ctx *c) {
+  if (!c) return GBT_OK;
+  cudaSetDevice(c->device);
+  cudaStreamSynchronize(c->stream);
+  Buf *bufs[] = {&c->mirror, &c->q, &c->rec, &c->chunk_prefix, &c->rows_in, &c->offs_in, &c->cand,
+                 &c->splits_a, &c->splits_b, &c->parent_of_in, &c->tile_counts, &c->lrank, &c->slab};
+  for (Buf *b : bufs) release(c, *b);
+  if (c->st) cudaFreeAsync(c->st, c->stream);
+  cudaStreamSynchronize(c->stream);
+  if (c->err_host) cudaFreeHost(c->err_host);
+  for (auto &r : c->prof_pending) {
+    cudaEventDestroy(r.a);
+    cudaEventDestroy(r.b);
+  }
+  for (cudaEvent_t e : c->prof_pool) cudaEventDestroy(e);
+  delete c;
+  return GBT_OK;
+}
+
+const char *gbt_last_error(const gbt_ctx *c) { return c ? c->last_error.c_str() : "NULL context"; }
+
+gbt_status gbt_sync(gbt_ctx *c) {
+  gbt_status s = check_ctx(c);
+  if (s != GBT_OK) return s;
+  CUDA_TRY(c, cudaMemcpyAsync(c->err_host, &c->st->err, sizeof(uint32_t), cudaMemcpyDeviceToHost, c->stream),
+           "read error word");
+  CUDA_TRY(c, cudaMemsetAsync(&c->st->err, 0, sizeof(uint32_t), c->stream), "clear error word");
+  CUDA_TRY(c, cudaStreamSynchronize(c->stream), "stream synchronize");
+  const uint32_t e = *c->err_host;
+  if (e & ERRBIT_BIN) return fail(c, GBT_ERR_BIN_RANGE, "device: bin value out of range");
+  if (e & ERRBIT_ROW) return fail(c, GBT_ERR_ROW_RANGE, "device: row index or node offsets out of range");
+  if (e & ERRBIT_QUANT) return fail(c, GBT_ERR_QUANT_OVERFLOW, "device: quantised value out of int32 range");
+  if (e & ERRBIT_TIMEOUT) return fail(c, GBT_ERR_TIMEOUT, "device: bounded wait ran out");
+  if (e & ERRBIT_INCONSISTENT) return fail(c, GBT_ERR_INCONSISTENT, "device: negative hessian after subtraction");
+  return GBT_OK;
+}
+
+gbt_status gbt_upload_bins(gbt_ctx *c, const void *bins, int bin_bytes, int64_t n_rows, int32_t n_features,
+                           int32_t n_bins, uint32_t sentinel) {
+  gbt_status s = check_ctx(c);
+  if (s != GBT_OK) return s;
+  if (!bins) return fail(c, GBT_ERR_INVALID_ARG, "bins is NULL");
+  if (bin_bytes != 1 && bin_bytes != 2) return fail(c, GBT_ERR_INVALID_ARG, "bin_bytes must be 1 or 2");
+  if (n_rows <= 0 || n_rows >= (1LL << 31)) return fail(c, GBT_ERR_UNSUPPORTED, "n_rows must be in [1, 2^31)");
+  if (n_features <= 0 || n_features >= (1 << 24)) return fail(c, GBT_ERR_UNSUPPORTED, "n_features must be in [1, 2^24)");
+  const uint32_t wmax = bin_bytes == 1 ? 0xFFu : 0xFFFFu;
+  if (n_bins < 1 || (uint32_t)n_bins > wmax) return fail(c, GBT_ERR_INVALID_ARG, "n_bins must be in [1, width max]");
+  if (sentinel > wmax || sentinel < (uint32_t)n_bins)
+    return fail(c, GBT_ERR_INVALID_ARG, "missing_sentinel must fit the width and be >= n_bins");
+  const int B = n_bins + 1;
+  int ts16 = 0;
+  if (bin_bytes == 2) {
+    ts16 = h16_ts_for(B);
+    if (ts16 == 0) return fail(c, GBT_ERR_UNSUPPORTED, "u16 n_bins too large for the shared-memory histogram");
+  }
+  const int tf = MIRROR_STRIP_BYTES / bin_bytes;
+  const int n_tiles = (n_features + tf - 1) / tf;
+  const size_t mbytes = (size_t)n_tiles * (size_t)n_rows * MIRROR_STRIP_BYTES;
+  s = ensure(c, c->mirror, mbytes, "mirror allocation");
+  if (s != GBT_OK) return s;
+  // per-dataset scratch sized by n_rows
+  s = ensure(c, c->rec, (size_t)n_rows * sizeof(int4), "level record scratch");
+  if (s != GBT_OK) return s;
+  c->bin_bytes = bin_bytes;
+  c->n_rows = n_rows;
+  c->n_features = n_features;
+  c->n_bins = n_bins;
+  c->sentinel = sentinel;
+  c->n_tiles = n_tiles;
+  c->tile_feats = tf;
+  c->ts16 = ts16;
+  c->tree_ready = false;
+  const int k = ptr_kind(bins);
+  const dim3 block(256);
+  if (k == 1) {
+    const dim3 grid((unsigned)((n_rows + 63) / 64), (unsigned)n_tiles);
+    prof_begin(c);
+    if (bin_bytes == 1)
+      k_mirror<uint8_t><<<grid, block, 0, c->stream>>>((const uint8_t *)bins, n_rows, 0, n_rows, 0, n_features,
+                                                       n_bins, sentinel, n_rows, (uint8_t *)c->mirror.p, c->st);
+    else
+      k_mirror<uint16_t><<<grid, block, 0, c->stream>>>((const uint16_t *)bins, n_rows, 0, n_rows, 0, n_features,
+                                                        n_bins, sentinel, n_rows, (uint16_t *)c->mirror.p, c->st);
+    LAUNCH_CHECK(c, "k_mirror");
+  } else {
+    // host input: one feature tile (tf feature rows, contiguous) per copy + kernel
+    const size_t slab_bytes = (size_t)tf * n_rows * bin_bytes;
+    s = ensure(c, c->slab, slab_bytes, "upload slab");
+    if (s != GBT_OK) return s;
+    for (int t = 0; t < n_tiles; ++t) {
+      const int f0 = t * tf;
+      const int nf = std::min(tf, n_features - f0);
+      const unsigned char *src = (const unsigned char *)bins + (size_t)f0 * n_rows * bin_bytes;
+      CUDA_TRY(c, cudaMemcpyAsync(c->slab.p, src, (size_t)nf * n_rows * bin_bytes, cudaMemcpyHostToDevice, c->stream),
+               "bins upload");
+      const dim3 grid((unsigned)((n_rows + 63) / 64), 1u);
+      prof_begin(c);
+      if (bin_bytes == 1)
+        k_mirror<uint8_t><<<grid, block, 0, c->stream>>>((const uint8_t *)c->slab.p, n_rows, 0, n_rows, f0,
+                                                         n_features, n_bins, sentinel, n_rows,
+                                                         (uint8_t *)c->mirror.p, c->st);
+      else
+        k_mirror<uint16_t><<<grid, block, 0, c->stream>>>((const uint16_t *)c->slab.p, n_rows, 0, n_rows, f0,
+                                                          n_features, n_bins, sentinel, n_rows,
+                                                          (uint16_t *)c->mirror.p, c->st);
+      LAUNCH_CHECK(c, "k_mirror");
+    }
+    // the slab is only needed during the upload
+    release(c, c->slab);
+  }
+  return GBT_OK;
+}
+
+gbt_status gbt_begin_tree(gbt_ctx *c, const float *gpair, float scale_g, float scale_h) {
+  gbt_status s = check_ctx(c);
+  if (s != GBT_OK) return s;
+  if (c->n_rows == 0) return fail(c, GBT_ERR_STATE, "gbt_upload_bins first");
+  if (!(scale_g > 0.f) || !(scale_h > 0.f) || !isfinite(scale_g) || !isfinite(scale_h))
+    return fail(c, GBT_ERR_INVALID_ARG, "scales must be finite and > 0");
+  s = ensure(c, c->q, (size_t)c->n_rows * sizeof(int2), "quantised gpair");
+  if (s != GBT_OK) return s;
+  const void *gp = nullptr;
+  Buf &stage = c->rec;  // rec has n_rows * 16 >= n_rows * 8 bytes and is free between levels
+  s = device_view(c, gpair, (size_t)c->n_rows * 2 * sizeof(float), stage, &gp, "gpair");
+  if (s != GBT_OK) return s;
+  if (!aligned16(gp) && ((reinterpret_cast<uintptr_t>(gp) & 7u) != 0))
+    return fail(c, GBT_ERR_INVALID_ARG, "gpair must be 8-byte aligned");
+  CUDA_TRY(c, cudaMemsetAsync(&c->st->qmax, 0, sizeof(uint32_t), c->stream), "reset qmax");
+  const int grid = grid_for(c, c->n_rows, 256, 8);
+  prof_begin(c);
+  k_quantise<<<grid, 256, 0, c->stream>>>((const float2 *)gp, c->n_rows, scale_g, scale_h, (int2 *)c->q.p, c->st);
+  LAUNCH_CHECK(c, "k_quantise");
+  c->sg = scale_g;
+  c->sh = scale_h;
+  c->inv_sg = 1.0 / (double)scale_g;
+  c->inv_sh = 1.0 / (double)scale_h;
+  c->tree_ready = true;
+  return GBT_OK;
+}
+
+gbt_status gbt_suggest_scales(int64_t rows_per_partial, float max_abs_g, float max_abs_h, float *sg, float *sh) {
+  if (!sg || !sh) return GBT_ERR_INVALID_ARG;
+  if (!(max_abs_g >= 0.f) || !(max_abs_h >= 0.f) || !isfinite(max_abs_g) || !isfinite(max_abs_h))
+    return GBT_ERR_INVALID_ARG;
+  if (rows_per_partial <= 0) rows_per_partial = 65536;
+  const double lim = 2147483647.0 / (double)rows_per_partial;  // max |q| per row
+  auto pick = [&](float m) -> float {
+    if (m == 0.f) return 1.f;
+    // largest power of two s with m * s <= lim
+    int e = (int)floor(log2(lim / (double)m));
+    e = std::max(-126, std::min(e, 126));
+    double s = ldexp(1.0, e);
+    while (s > ldexp(1.0, -126) && (double)m * s > lim) s *= 0.5;
+    return (float)s;
+  };
+  *sg = pick(max_abs_g);
+  *sh = pick(max_abs_h);
+  return GBT_OK;
+}
+
+gbt_status gbt_build_level(gbt_ctx *c, const int32_t *rows, const int64_t *node_offsets, int32_t n_nodes,
+                           int64_t *hist_out) {
+  gbt_status s = check_ctx(c);
+  if (s != GBT_OK) return s;
+  if (!c->tree_ready) return fail(c, GBT_ERR_STATE, "gbt_begin_tree first");
+  if (n_nodes < 0 || n_nodes > 65535) return fail(c, GBT_ERR_UNSUPPORTED, "n_nodes must be in [0, 65535]");
+  if (!node_offsets || !hist_out) return fail(c, GBT_ERR_INVALID_ARG, "node_offsets and hist_out are required");
+  if (ptr_kind(hist_out) != 1 || !aligned16(hist_out))
+    return fail(c, GBT_ERR_INVALID_ARG, "hist_out must be 16-byte aligned device memory");
+  if (n_nodes == 0) return GBT_OK;
+  const int B = c->n_bins + 1;
+  // node offsets: host offsets are validated here and tell the row count
+  const void *offs_d = nullptr;
+  int64_t R_host = -1;
+  if (ptr_kind(node_offsets) == 0) {
+    if (node_offsets[0] != 0) return fail(c, GBT_ERR_INVALID_ARG, "node_offsets[0] must be 0");
+    for (int32_t i = 0; i < n_nodes; ++i)
+      if (node_offsets[i + 1] < node_offsets[i]) return fail(c, GBT_ERR_INVALID_ARG, "node_offsets must ascend");
+    R_host = node_offsets[n_nodes];
+    if (R_host > c->n_rows) return fail(c, GBT_ERR_INVALID_ARG, "more level rows than dataset rows");
+  }
+  s = device_view(c, node_offsets, (size_t)(n_nodes + 1) * sizeof(int64_t), c->offs_in, &offs_d, "node_offsets");
+  if (s != GBT_OK) return s;
+  const void *rows_d = nullptr;
+  if (rows) {
+    const int k = ptr_kind(rows);
+    if (k == 0 && R_host < 0) return fail(c, GBT_ERR_INVALID_ARG, "host rows need host node_offsets");
+    const size_t rb = (size_t)(k == 0 ? R_host : 0) * sizeof(int32_t);
+    if (k == 0) {
+      s = device_view(c, rows, rb, c->rows_in, &rows_d, "rows");
+      if (s != GBT_OK) return s;
+    } else {
+      rows_d = rows;
+    }
+  }
+  s = ensure(c, c->chunk_prefix, (size_t)(n_nodes + 1) * sizeof(int32_t), "chunk prefix");
+  if (s != GBT_OK) return s;
+
+  LevelParams lp;
+  lp.rows = (const int32_t *)rows_d;
+  lp.offs = (const int64_t *)offs_d;
+  lp.n_nodes = n_nodes;
+  const int hist_ctas = c->n_sm;  // one resident CTA per SM for both histogram kernels
+  if (c->bin_bytes == 1) {
+    lp.n_fgroups = c->n_tiles;
+  } else {
+    lp.n_fgroups = (c->n_features + c->ts16 - 1) / c->ts16;
+  }
+  lp.target_items = hist_ctas * 2;
+  lp.pad = 0;
+  lp.n_rows = c->n_rows;
+  lp.q = (const int2 *)c->q.p;
+  lp.rec = (int4 *)c->rec.p;
+  lp.chunk_prefix = (int32_t *)c->chunk_prefix.p;
+  lp.hist_out = hist_out;
+  lp.node_int64s = (int64_t)c->n_features * B * 2;
+  lp.st = c->st;
+  {
+    const int64_t work = R_host >= 0 ? R_host : c->n_rows;
+    const int grid = grid_for(c, std::max<int64_t>(work, 1), 1024, 2);
+    prof_begin(c);
+    k_level_prologue<<<grid, 1024, 0, c->stream>>>(lp);
+    LAUNCH_CHECK(c, "k_level_prologue");
+  }
+  if (c->bin_bytes == 1) {
+    Hist8Params hp;
+    hp.lv = lp;
+    hp.mirror = (const uint8_t *)c->mirror.p;
+    hp.n_features = c->n_features;
+    hp.n_slots = B;
+    prof_begin(c);
+    k_hist_u8<<<hist_ctas, H8_THREADS, H8_SMEM, c->stream>>>(hp);
+    LAUNCH_CHECK(c, "k_hist_u8");
+  } else {
+    Hist16Params hp;
+    hp.lv = lp;
+    hp.mirror = (const uint16_t *)c->mirror.p;
+    hp.n_features = c->n_features;
+    hp.n_slots = B;
+    hp.n_bins = c->n_bins;
+    hp.ts = c->ts16;
+    const int hist_bytes = ((B * c->ts16 * 8) + 127) & ~127;
+    const int smem = hist_bytes + H16_STAGE_BYTES;
+    prof_begin(c);
+    switch (c->ts16) {
+      case 32: k_hist_u16<32><<<hist_ctas, H16_THREADS, smem, c->stream>>>(hp); break;
+      case 16: k_hist_u16<16><<<hist_ctas, H16_THREADS, smem, c->stream>>>(hp); break;
+      case 8: k_hist_u16<8><<<hist_ctas, H16_THREADS, smem, c->stream>>>(hp); break;
+      case 4: k_hist_u16<4><<<hist_ctas, H16_THREADS, smem, c->stream>>>(hp); break;
+      default: k_hist_u16<2><<<hist_ctas, H16_THREADS, smem, c->stream>>>(hp); break;
+    }
+    LAUNCH_CHECK(c, "k_hist_u16");
+  }
+  return GBT_OK;
+}
+
+static gbt_status parent_of_view(gbt_ctx *c, const int32_t *parent_of, int32_t n_pairs, const int32_t **out) {
+  *out = nullptr;
+  if (!parent_of) return GBT_OK;
+  const void *d = nullptr;
+  gbt_status s = device_view(c, parent_of, (size_t)n_pairs * sizeof(int32_t), c->parent_of_in, &d, "parent_of");
+  *out = (const int32_t *)d;
+  return s;
+}
+
+gbt_status gbt_subtract_siblings(gbt_ctx *c, const int64_t *parent_hist, const int32_t *parent_of,
+                                 const int64_t *small_hist, int64_t *large_hist, int32_t n_pairs) {
+  gbt_status s = check_ctx(c);
+  if (s != GBT_OK) return s;
+  if (c->n_rows == 0) return fail(c, GBT_ERR_STATE, "gbt_upload_bins first");
+  if (n_pairs < 0) return fail(c, GBT_ERR_INVALID_ARG, "n_pairs < 0");
+  if (n_pairs == 0) return GBT_OK;
+  for (const void *p : {(const void *)parent_hist, (const void *)small_hist, (const void *)large_hist})
+    if (ptr_kind(p) != 1 || !aligned16(p)) return fail(c, GBT_ERR_INVALID_ARG, "histograms must be 16-byte aligned device memory");
+  const int32_t *po = nullptr;
+  s = parent_of_view(c, parent_of, n_pairs, &po);
+  if (s != GBT_OK) return s;
+  const int64_t upn = (int64_t)c->n_features * (c->n_bins + 1);
+  const int grid = grid_for(c, (int64_t)n_pairs * upn, 256, 8);
+  prof_begin(c);
+  k_subtract<<<grid, 256, 0, c->stream>>>(parent_hist, po, small_hist, large_hist, n_pairs, upn, c->st);
+  LAUNCH_CHECK(c, "k_subtract");
+  return GBT_OK;
+}
+
+static gbt_status split_out_view(gbt_ctx *c, gbt_split *out, int32_t n, Buf &stage, SplitOut **dev, bool *host) {
+  const int k = ptr_kind(out);
+  if (k < 0) return fail(c, GBT_ERR_INVALID_ARG, "split output is NULL");
+  *host = (k == 0);
+  if (k == 1) {
+    *dev = reinterpret_cast<SplitOut *>(out);
+    return GBT_OK;
+  }
+  gbt_status s = ensure(c, stage, (size_t)n * sizeof(SplitOut), "split staging");
+  if (s != GBT_OK) return s;
+  *dev = reinterpret_cast<SplitOut *>(stage.p);
+  return GBT_OK;
+}
+
+gbt_status gbt_find_splits(gbt_ctx *c, const int64_t *hist, int32_t n_nodes, const gbt_params *params,
+                           gbt_split *out) {
+  gbt_status s = check_ctx(c);
+  if (s != GBT_OK) return s;
+  if (!c->tree_ready) return fail(c, GBT_ERR_STATE, "gbt_begin_tree first (scales)");
+  if (!params || n_nodes < 0) return fail(c, GBT_ERR_INVALID_ARG, "params NULL or n_nodes < 0");
+  if (n_nodes == 0) return GBT_OK;
+  if (ptr_kind(hist) != 1 || !aligned16(hist)) return fail(c, GBT_ERR_INVALID_ARG, "hist must be 16-byte aligned device memory");
+  SplitOut *dout = nullptr;
+  bool host = false;
+  s = split_out_view(c, out, n_nodes, c->splits_a, &dout, &host);
+  if (s != GBT_OK) return s;
+  s = ensure(c, c->cand, (size_t)n_nodes * c->n_features * sizeof(Cand), "candidates");
+  if (s != GBT_OK) return s;
+  const SplitParams sp = make_sp(c, params);
+  const int64_t units = (int64_t)n_nodes * c->n_features;
+  const int grid = grid_for(c, units * 32, SCAN_THREADS, 8);
+  prof_begin(c);
+  k_find<<<grid, SCAN_THREADS, 0, c->stream>>>(hist, n_nodes, c->n_features, c->n_bins, sp, (Cand *)c->cand.p);
+  LAUNCH_CHECK(c, "k_find");
+  prof_begin(c);
+  k_reduce_splits<<<n_nodes, 256, 0, c->stream>>>((const Cand *)c->cand.p, n_nodes, c->n_features, c->n_bins, 0, hist,
+                                                  nullptr, dout, nullptr);
+  LAUNCH_CHECK(c, "k_reduce_splits");
+  if (host)
+    CUDA_TRY(c, cudaMemcpyAsync(out, dout, (size_t)n_nodes * sizeof(gbt_split), cudaMemcpyDeviceToHost, c->stream),
+             "splits to host");
+  return GBT_OK;
+}
+
+gbt_status gbt_subtract_and_find(gbt_ctx *c, const int64_t *parent_hist, const int32_t *parent_of,
+                                 const int64_t *small_hist, int64_t *large_hist, int32_t n_pairs,
+                                 const gbt_params *params, gbt_split *small_out, gbt_split *large_out) {
+  gbt_status s = check_ctx(c);
+  if (s != GBT_OK) return s;
+  if (!c->tree_ready) return fail(c, GBT_ERR_STATE, "gbt_begin_tree first (scales)");
+  if (!params || n_pairs < 0) return fail(c, GBT_ERR_INVALID_ARG, "params NULL or n_pairs < 0");
+  if (n_pairs == 0) return GBT_OK;
+  if (n_pairs > 32767) return fail(c, GBT_ERR_UNSUPPORTED, "n_pairs must be <= 32767");
+  for (const void *p : {(const void *)parent_hist, (const void *)small_hist, (const void *)large_hist})
+    if (ptr_kind(p) != 1 || !aligned16(p)) return fail(c, GBT_ERR_INVALID_ARG, "histograms must be 16-byte aligned device memory");
+  const int32_t *po = nullptr;
+  s = parent_of_view(c, parent_of, n_pairs, &po);
+  if (s != GBT_OK) return s;
+  SplitOut *da = nullptr, *db = nullptr;
+  bool ha = false, hb = false;
+  s = split_out_view(c, small_out, n_pairs, c->splits_a, &da, &ha);
+  if (s != GBT_OK) return s;
+  s = split_out_view(c, large_out, n_pairs, c->splits_b, &db, &hb);
+  if (s != GBT_OK) return s;
+  s = ensure(c, c->cand, (size_t)2 * n_pairs * c->n_features * sizeof(Cand), "candidates");
+  if (s != GBT_OK) return s;
+  const SplitParams sp = make_sp(c, params);
+  const int64_t units = (int64_t)n_pairs * c->n_features;
+  const int grid = grid_for(c, units * 32, SCAN_THREADS, 8);
+  prof_begin(c);
+  k_subtract_find<<<grid, SCAN_THREADS, 0, c->stream>>>(parent_hist, po, small_hist, large_hist, n_pairs,
+                                                       c->n_features, c->n_bins, sp, (Cand *)c->cand.p, c->st);
+  LAUNCH_CHECK(c, "k_subtract_find");
+  prof_begin(c);
+  k_reduce_splits<<<2 * n_pairs, 256, 0, c->stream>>>((const Cand *)c->cand.p, 2 * n_pairs, c->n_features, c->n_bins,
+                                                      1, small_hist, large_hist, da, db);
+  LAUNCH_CHECK(c, "k_reduce_splits");
+  if (ha)
+    CUDA_TRY(c, cudaMemcpyAsync(small_out, da, (size_t)n_pairs * sizeof(gbt_split), cudaMemcpyDeviceToHost, c->stream),
+             "splits to host");
+  if (hb)
+    CUDA_TRY(c, cudaMemcpyAsync(large_out, db, (size_t)n_pairs * sizeof(gbt_split), cudaMemcpyDeviceToHost, c->stream),
+             "splits to host");
+  return GBT_OK;
+}
+
+gbt_status gbt_partition_level(gbt_ctx *c, const int32_t *rows, const int64_t *node_offsets, int32_t n_nodes,
+                               const gbt_split *splits, int32_t *out_rows, int64_t *out_offsets) {
+  gbt_status s = check_ctx(c);
+  if (s != GBT_OK) return s;
+  if (c->n_rows == 0) return fail(c, GBT_ERR_STATE, "gbt_upload_bins first");
+  if (n_nodes < 0 || n_nodes > 65535) return fail(c, GBT_ERR_UNSUPPORTED, "n_nodes must be in [0, 65535]");
+  if (n_nodes == 0) return GBT_OK;
+  if (!node_offsets || !splits || !out_rows || !out_offsets) return fail(c, GBT_ERR_INVALID_ARG, "NULL argument");
+  if (ptr_kind(out_rows) != 1 || ptr_kind(out_offsets) != 1)
+    return fail(c, GBT_ERR_INVALID_ARG, "out_rows and out_offsets must be device memory");
+  int64_t R_host = -1;
+  if (ptr_kind(node_offsets) == 0) {
+    if (node_offsets[0] != 0) return fail(c, GBT_ERR_INVALID_ARG, "node_offsets[0] must be 0");
+    for (int32_t i = 0; i < n_nodes; ++i)
+      if (node_offsets[i + 1] < node_offsets[i]) return fail(c, GBT_ERR_INVALID_ARG, "node_offsets must ascend");
+    R_host = node_offsets[n_nodes];
+    if (R_host > c->n_rows) return fail(c, GBT_ERR_INVALID_ARG, "more level rows than dataset rows");
+  }
+  const void *offs_d = nullptr;
+  s = device_view(c, node_offsets, (size_t)(n_nodes + 1) * sizeof(int64_t), c->offs_in, &offs_d, "node_offsets");
+  if (s != GBT_OK) return s;
+  const void *rows_d = nullptr;
+  if (rows) {
+    const int k = ptr_kind(rows);
+    if (k == 0 && R_host < 0) return fail(c, GBT_ERR_INVALID_ARG, "host rows need host node_offsets");
+    if (k == 0) {
+      s = device_view(c, rows, (size_t)R_host * sizeof(int32_t), c->rows_in, &rows_d, "rows");
+      if (s != GBT_OK) return s;
+    } else {
+      rows_d = rows;
+    }
+  }
+  const void *sp_d = nullptr;
+  s = device_view(c, splits, (size_t)n_nodes * sizeof(gbt_split), c->splits_b, &sp_d, "splits");
+  if (s != GBT_OK) return s;
+  const int64_t bound = R_host >= 0 ? R_host : c->n_rows;
+  const int64_t n_tiles = std::max<int64_t>(1, (bound + PART_TILE - 1) / PART_TILE);
+  s = ensure(c, c->tile_counts, (size_t)(n_tiles + 1) * sizeof(int64_t), "partition tile counts");
+  if (s != GBT_OK) return s;
+  s = ensure(c, c->lrank, (size_t)(n_nodes + 1) * sizeof(int64_t), "partition node ranks");
+  if (s != GBT_OK) return s;
+  PartParams pp;
+  pp.rows = (const int32_t *)rows_d;
+  pp.offs = (const int64_t *)offs_d;
+  pp.n_nodes = n_nodes;
+  pp.tile_feats = c->tile_feats;
+  pp.bin_bytes = c->bin_bytes;
+  pp.n_bins = c->n_bins;
+  pp.n_features = c->n_features;
+  pp.pad = 0;
+  pp.n_rows = c->n_rows;
+  pp.mirror = (const unsigned char *)c->mirror.p;
+  pp.splits = (const SplitOut *)sp_d;
+  pp.tile_counts = (int64_t *)c->tile_counts.p;
+  pp.out_rows = out_rows;
+  pp.out_offs = out_offsets;
+  pp.st = c->st;
+  int64_t *lrank = (int64_t *)c->lrank.p;
+  prof_begin(c);
+  k_part_count<<<(unsigned)n_tiles, PART_THREADS, 0, c->stream>>>(pp);
+  LAUNCH_CHECK(c, "k_part_count");
+  prof_begin(c);
+  k_part_scan<<<1, 1024, 0, c->stream>>>(pp, n_tiles);
+  LAUNCH_CHECK(c, "k_part_scan");
+  prof_begin(c);
+  k_part_rank<<<(unsigned)n_tiles, PART_THREADS, 0, c->stream>>>(pp, lrank);
+  LAUNCH_CHECK(c, "k_part_rank");
+  prof_begin(c);
+  k_part_offsets<<<1, 32, 0, c->stream>>>(pp, lrank, n_tiles);
+  LAUNCH_CHECK(c, "k_part_offsets");
+  prof_begin(c);
+  k_part_scatter<<<(unsigned)n_tiles, PART_THREADS, 0, c->stream>>>(pp, lrank);
+  LAUNCH_CHECK(c, "k_part_scatter");
+  return GBT_OK;
+}
+
+gbt_status gbt_profile_enable(gbt_ctx *c, int on) {
+  gbt_status s = check_ctx(c);
+  if (s != GBT_OK) return s;
+  c->prof = on != 0;
+  return GBT_OK;
+}
+
+gbt_status gbt_profile_read(gbt_ctx *c, const char *kernel, double *total_ms, int64_t *launches) {
+  gbt_status s = check_ctx(c);
+  if (s != GBT_OK) return s;
+  if (!total_ms || !launches) return fail(c, GBT_ERR_INVALID_ARG, "NULL output");
+  CUDA_TRY(c, cudaStreamSynchronize(c->stream), "stream synchronize");
+  double ms = 0.0;
+  int64_t n = 0;
+  for (const auto &r : c->prof_pending) {
+    if (!kernel || strcmp(kernel, r.name) == 0) {
+      float t = 0.f;
+      if (cudaEventElapsedTime(&t, r.a, r.b) == cudaSuccess) {
+        ms += t;
+        ++n;
+      } else {
+        cudaGetLastError();
+      }
+    }
+    c->prof_pool.push_back(r.a);
+    c->prof_pool.push_back(r.b);
+  }
+  c->prof_pending.clear();
+  *total_ms = ms;
+  *launches = n;
+  return GBT_OK;
+}
+
+int32_t gbt_slots_per_feature(const gbt_ctx *c) { return (c && c->n_rows > 0) ? c->n_bins + 1 : -1; }
+
+int64_t gbt_kernel_launches(const gbt_ctx *c) { return c ? c->launches : 0; }
+
+}  // extern "C"

@@ -1,0 +1,91 @@
+// Dataset and tree preparation kernels: the tiled row-major bin mirror and the
+// fixed-point quantisation of (g, h).
+#pragma once
+
+#include "common.cuh"
+
+namespace gbt {
+
+// Feature-major [F][N] bins -> tiled row-major mirror [n_tiles][N][64 bytes]
+// holding histogram slots (bin, or n_bins for the missing sentinel).
+// The mirror is the column tiling of bonsai "E6. The wide-data wall",
+// "Epilogue": each row of a feature tile is one contiguous strip, so a node's
+// gathered rows read whole 64-byte strips instead of one byte per feature.
+// grid (ceil(rows/64), n_tiles), block 256. Validates every value.
+template <typename T>
+__global__ void __launch_bounds__(256) k_mirror(const T *__restrict__ bins, int64_t n_rows, int64_t row0,
+                                                int64_t rows_in_slab, int32_t f_base, int32_t n_features,
+                                                int32_t n_bins, uint32_t sentinel, int64_t bins_stride,
+                                                T *__restrict__ mirror, DevState *st) {
+  constexpr int TF = MIRROR_STRIP_BYTES / sizeof(T);  // features per tile
+  __shared__ T sm[TF][64 + 2];
+  const int tile = blockIdx.y;
+  const int64_t rl0 = (int64_t)blockIdx.x * 64;  // row within slab
+  const int f0 = tile * TF;                      // feature within slab
+  uint32_t bad = 0;
+  for (int i = threadIdx.x; i < TF * 64; i += blockDim.x) {
+    const int fl = i >> 6, rl = i & 63;
+    const int f = f0 + fl;
+    const int64_t r = rl0 + rl;
+    T v = 0;
+    if (f_base + f < n_features && r < rows_in_slab) {
+      const uint32_t b = bins[(int64_t)f * bins_stride + r];
+      uint32_t slot;
+      if (b == sentinel) {
+        slot = (uint32_t)n_bins;
+      } else if (b < (uint32_t)n_bins) {
+        slot = b;
+      } else {
+        slot = (uint32_t)n_bins;
+        bad = 1;
+      }
+      v = (T)slot;
+    }
+    sm[fl][rl] = v;
+  }
+  __syncthreads();
+  const int64_t gtile = (int64_t)(f_base / TF) + tile;
+  for (int i = threadIdx.x; i < TF * 64; i += blockDim.x) {
+    const int rl = i / TF, fl = i % TF;
+    const int64_t r = rl0 + rl;
+    if (r < rows_in_slab) mirror[(gtile * n_rows + row0 + r) * TF + fl] = sm[fl][rl];
+  }
+  if (bad) raise_err(st, ERRBIT_BIN);
+}
+
+// (g, h) float32 pairs -> int32 fixed-point pairs, q = round-half-even(fl32(x * s)).
+// "GBDT engine engineering deep-dive" (ybb.press), section 7: gradients are
+// quantised to fixed point before integer atomics; bonsai "9. Parallelism &
+// determinism", "The idea": int64 cells are exact in any order.
+// Also reduces max |q| into st->qmax (zeroed by the caller).
+__global__ void __launch_bounds__(256) k_quantise(const float2 *__restrict__ gp, int64_t n, float sg, float sh,
+                                                  int2 *__restrict__ q, DevState *st) {
+  uint32_t mx = 0, bad = 0;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+    const float2 v = gp[i];
+    const float pg = __fmul_rn(v.x, sg);
+    const float ph = __fmul_rn(v.y, sh);
+    int qg = 0, qh = 0;
+    if (fabsf(pg) < 2147483648.0f) {
+      const long long t = __float2ll_rn(pg);
+      if (t > -2147483648LL && t < 2147483648LL) qg = (int)t; else bad = 1;
+    } else {
+      bad = 1;
+    }
+    if (fabsf(ph) < 2147483648.0f) {
+      const long long t = __float2ll_rn(ph);
+      if (t > -2147483648LL && t < 2147483648LL) qh = (int)t; else bad = 1;
+    } else {
+      bad = 1;
+    }
+    q[i] = make_int2(qg, qh);
+    const uint32_t ag = qg < 0 ? (uint32_t)(-(int64_t)qg) : (uint32_t)qg;
+    const uint32_t ah = qh < 0 ? (uint32_t)(-(int64_t)qh) : (uint32_t)qh;
+    mx = max(mx, max(ag, ah));
+  }
+  for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  if ((threadIdx.x & 31) == 0 && mx) atomicMax(&st->qmax, mx);
+  if (bad) raise_err(st, ERRBIT_QUANT);
+}
+
+}  // namespace gbt

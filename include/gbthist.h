@@ -176,6 +176,15 @@ gbt_status gbt_subtract_and_find(gbt_ctx *ctx, const int64_t *parent_hist, const
 gbt_status gbt_partition_level(gbt_ctx *ctx, const int32_t *rows, const int64_t *node_offsets, int32_t n_nodes,
                                const gbt_split *splits, int32_t *out_rows, int64_t *out_offsets);
 
+/* Per-kernel device-time accounting for diagnostics. When enabled, every
+ * kernel this context launches is bracketed by a pair of CUDA events on the
+ * context stream. gbt_profile_read synchronises the stream, adds up the
+ * elapsed times of the completed launches of `kernel` (a kernel name such as
+ * "k_hist_u8"; NULL = all kernels) since the last read, returns them in
+ * total_ms / launches, and forgets every recorded launch. */
+gbt_status gbt_profile_enable(gbt_ctx *ctx, int on);
+gbt_status gbt_profile_read(gbt_ctx *ctx, const char *kernel, double *total_ms, int64_t *launches);
+
 /* B = n_bins + 1 of the uploaded matrix, or -1 before gbt_upload_bins. */
 int32_t gbt_slots_per_feature(const gbt_ctx *ctx);
 
