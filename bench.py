@@ -1,0 +1,459 @@
+#!/usr/bin/env python
+"""Benchmark of the level histogram path: binned entries per second per level on GB300.
+
+One step = one tree level of the workload: gbt_build_level over the smaller
+siblings (level prologue + histogram kernel) and gbt_subtract_and_find (sibling
+subtraction + split find for both siblings of every pair). Inputs are resident
+in HBM when the timed region starts; L2 is flushed (a write larger than L2)
+before every step, outside the step's CUDA events.
+
+Prints one JSON line (rank 0). ``--impl reference`` times the serial CPU oracle
+on the same workload instead (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "binned entries/sec per level histogram build (1 GB300); % of HBM roofline"
+UNIT = "entries/s"
+WORKLOAD_TEXT = {
+    "level5": "level5: 1,000,000 rows x 100 features u8 (per-feature Zipf s=1.1 over 255 bins), level 5 of a tree "
+              "grown by random seeded partitions: 16 smaller siblings built, 16 derived by subtraction, split find "
+              "for all 32",
+    "wide": "wide: 131,072 rows x 16,384 features u8 uniform, level 3 with 8 nodes of geometric sizes: 4 built, "
+            "4 derived, split find for all 8",
+    "u16miss": "u16miss: 2,000,000 rows x 64 features u16 (4096 bins, 40% missing), level 7: 64 built, 64 derived, "
+               "split find for all 128",
+    "root": "root: 10,000 rows x 28 features u8 uniform, one node (identity rows), build + split find",
+}
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def _kernel_source_hash():
+    h = hashlib.sha256()
+    for name in ("k_hist.cuh", "common.cuh"):
+        with open(os.path.join(ROOT, "histogram_construction_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def _profile_traffic(workload):
+    """DRAM bytes per launch of the histogram kernel from a committed ncu summary, if it matches the source."""
+    path = os.path.join(ROOT, "profiles", f"k_hist_u8_{workload}.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        if d.get("source_hash") == _kernel_source_hash():
+            return float(d["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks/throttle reasons sampled while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.12)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = []
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append(dict(sm=float(parts[1]), smax=float(parts[2]), hw=parts[5], hwt=parts[6], swt=parts[7],
+                                 pcap=parts[8]))
+            except ValueError:
+                continue
+        if not rows:
+            return None
+        reasons = set()
+        for r in rows:
+            for k, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"), ("swt", "sw_thermal_slowdown"),
+                            ("pcap", "sw_power_cap")):
+                if r[k].lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in rows), "sm_max_mhz": max(r["smax"] for r in rows),
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+# ----------------------------------------------------------------------------- workload setup
+def level_plan(w: synth.Workload):
+    """(parent level, target level) row lists for the bench level of a workload."""
+    L = w.target_depth
+    if L == 0:
+        return None, w.levels[0]
+    return w.levels[L - 1], w.levels[L]
+
+
+def entries_and_bytes(w, lv, B):
+    """Units of one step and the algorithmic HBM bytes (per level and for the histogram kernel alone)."""
+    F, wb = w.n_features, w.width
+    if lv.depth == 0:
+        R = int(lv.offsets[-1])
+        n_b, n_p = 1, 0
+    else:
+        R = int(lv.built_offsets[-1])
+        n_b = n_p = len(lv.small)
+    entries = R * F
+    hist_bytes = n_b * F * B * 16
+    kernel_bytes = R * F * wb + R * 12 + hist_bytes
+    level_bytes = kernel_bytes + 3 * n_p * F * B * 16
+    return entries, R, n_b, n_p, kernel_bytes, level_bytes
+
+
+def scales_for(w):
+    import histogram_construction_gb300 as g
+    _, sg, sh = g.gbt_suggest_scales(0, float(np.abs(w.gpair[:, 0]).max()), float(np.abs(w.gpair[:, 1]).max()))
+    return sg, sh
+
+
+# ----------------------------------------------------------------------------- CPU oracle leg
+def oracle_level(oracle, w, q, lv, parent_hist, sg, sh, node_slice=None):
+    """Serial oracle for one step: build the smaller siblings, subtract, find splits for both.
+    node_slice restricts the step to a prefix of the built nodes (bounded sample)."""
+    if lv.depth == 0:
+        h, _ = oracle.build_hist(w.bins, w.n_bins, w.sentinel, q, None, lv.offsets)
+        oracle.find_splits(h, w.n_bins, 1.0, 0.0, 0.0, sg, sh)
+        return int(lv.offsets[-1]) * w.n_features
+    k = len(lv.small) if node_slice is None else node_slice
+    offs = lv.built_offsets[:k + 1]
+    rows = lv.built_rows[:int(offs[-1])]
+    hs, _ = oracle.build_hist(w.bins, w.n_bins, w.sentinel, q, rows, offs)
+    large, _ = oracle.subtract(parent_hist[:k], None, hs)
+    oracle.find_splits(hs, w.n_bins, 1.0, 0.0, 0.0, sg, sh)
+    oracle.find_splits(large, w.n_bins, 1.0, 0.0, 0.0, sg, sh)
+    return int(offs[-1]) * w.n_features
+
+
+def cpu_oracle_timing(w, budget_s=10.0, steps=None, warmup=0):
+    """Time the oracle as it stands (1 thread). Returns (entries/s, sample text, per-step seconds)."""
+    import oracle
+    sg, sh = scales_for(w)
+    q, _ = oracle.quantise(w.gpair, sg, sh)
+    par, lv = level_plan(w)
+    parent_hist = None
+    if par is not None:
+        parent_hist, _ = oracle.build_hist(w.bins, w.n_bins, w.sentinel, q, par.rows, par.offsets)
+    # calibrate one full step
+    t0 = time.perf_counter()
+    e_full = oracle_level(oracle, w, q, lv, parent_hist, sg, sh)
+    t_full = time.perf_counter() - t0
+    node_slice = None
+    if steps is not None:
+        n_total = steps + warmup
+        if lv.depth > 0 and n_total * t_full > budget_s:
+            frac = budget_s / (n_total * t_full)
+            node_slice = max(1, int(len(lv.small) * frac))
+        for _ in range(warmup):
+            oracle_level(oracle, w, q, lv, parent_hist, sg, sh, node_slice)
+        ent, t0 = 0, time.perf_counter()
+        per = []
+        for _ in range(steps):
+            ts = time.perf_counter()
+            ent += oracle_level(oracle, w, q, lv, parent_hist, sg, sh, node_slice)
+            per.append(time.perf_counter() - ts)
+        dt = time.perf_counter() - t0
+        n_nodes = len(lv.small) if lv.depth > 0 else 1
+        sample = (f"{steps} steps of {'the full level' if node_slice is None else f'the first {node_slice} of {n_nodes} built nodes'}"
+                  f" ({ent // steps} entries per step)")
+        return ent / dt, sample, per
+    reps, ent, dt = 1, e_full, t_full
+    while dt < budget_s:
+        t0 = time.perf_counter()
+        ent += oracle_level(oracle, w, q, lv, parent_hist, sg, sh)
+        dt += time.perf_counter() - t0
+        reps += 1
+    return ent / dt, f"the full level ({e_full} entries: build, subtract, split find) x {reps} repetitions", None
+
+
+# ----------------------------------------------------------------------------- GPU leg
+def run_gpu(args, rank, world, local_rank):
+    import torch
+
+    import histogram_construction_gb300 as g
+    from histogram_construction_gb300.session import Session
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    w = synth.make(args.workload)
+    sg, sh = scales_for(w)
+    par, lv = level_plan(w)
+    B = w.n_bins + 1
+    entries, R, n_b, n_p, kernel_bytes, level_bytes = entries_and_bytes(w, lv, B)
+    stream = torch.cuda.Stream(dev)
+    prop = torch.cuda.get_device_properties(dev)
+    l2 = int(getattr(prop, "L2_cache_size", 0) or 0) or (129 << 20)
+    hist_kernel = "k_hist_u8" if w.width == 1 else "k_hist_u16"
+    with torch.cuda.stream(stream):
+        sess = Session(local_rank, stream=stream)
+        sess.upload_bins(torch.from_numpy(w.bins).to(dev), w.n_bins, w.sentinel)
+        gp_d = torch.from_numpy(w.gpair).to(dev)
+        sess.begin_tree(gp_d, sg, sh)
+        if lv.depth > 0:
+            hp = sess.build_level(torch.from_numpy(par.rows).to(dev), torch.from_numpy(par.offsets).to(dev))
+            rows_d = torch.from_numpy(lv.built_rows).to(dev)
+            offs_d = torch.from_numpy(lv.built_offsets).to(dev)
+            hs = sess.hist_tensor(n_b)
+            large = torch.empty_like(hs)
+            so = torch.empty((n_p, g.SPLIT_BYTES), dtype=torch.uint8, device=dev)
+            lo = torch.empty_like(so)
+            prm = g.params(1.0, 0.0, 0.0)
+        else:
+            rows_d = None
+            offs_d = torch.from_numpy(lv.offsets).to(dev)
+            hs = sess.hist_tensor(1)
+            so = torch.empty((1, g.SPLIT_BYTES), dtype=torch.uint8, device=dev)
+            prm = g.params(1.0, 0.0, 0.0)
+        flush_buf = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
+        ctx = sess.ctx
+
+        def step():
+            if lv.depth > 0:
+                sess.check(g.gbt_build_level(ctx, rows_d, offs_d, n_b, hs))
+                sess.check(g.gbt_subtract_and_find(ctx, hp, None, hs, large, n_p, prm, so, lo))
+            else:
+                sess.check(g.gbt_build_level(ctx, None, offs_d, 1, hs))
+                sess.check(g.gbt_find_splits(ctx, hs, 1, prm, so))
+
+        def flush(i):
+            flush_buf.fill_(i & 0xFF)
+
+        for i in range(args.warmup):
+            flush(i)
+            step()
+        assert sess.sync() == 0
+        barrier()
+
+        kernel_names = [hist_kernel, "k_level_prologue", "k_subtract_find", "k_reduce_splits", "k_find"]
+
+        def timed_pass(profile, flush_l2=True):
+            """K steps, each bracketed by CUDA events on the launching stream (flush outside the events)."""
+            g.gbt_profile_enable(ctx, profile)
+            g.gbt_profile_read(ctx)  # forget earlier records
+            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                  for _ in range(args.steps)]
+            l0 = g.gbt_kernel_launches(ctx)
+            barrier()
+            t0 = time.perf_counter()
+            for i in range(args.steps):
+                if flush_l2:
+                    flush(i)
+                ev[i][0].record(stream)
+                step()
+                ev[i][1].record(stream)
+            barrier()
+            wall = time.perf_counter() - t0
+            launches = g.gbt_kernel_launches(ctx) - l0
+            ms = [a.elapsed_time(b) for a, b in ev]
+            snap = {}
+            if profile:
+                for name in kernel_names:
+                    _, t, n = g.gbt_profile_read(ctx, name)
+                    snap[name] = (t, n)
+                g.gbt_profile_enable(ctx, False)
+            return ms, wall, launches, snap
+
+        clocks = ClockSampler(local_rank).start() if rank == 0 else None
+        ms, wall, launches, _ = timed_pass(False)
+        # second pass with per-kernel events: device time of each kernel over K steps
+        ms_prof, _, _, snap = timed_pass(True)
+        clk = clocks.stop() if clocks is not None else None
+        # warm-L2 pass (reported second)
+        ms_warm, _, _, _ = timed_pass(False, flush_l2=False)
+        assert sess.sync() == 0
+
+        # ---------------------------------------------------------------- e2e through host buffers
+        e2e = None
+        if lv.depth > 0:
+            rows_h = torch.from_numpy(lv.built_rows).pin_memory()
+            offs_h = torch.from_numpy(lv.built_offsets).pin_memory()
+            so_h = torch.empty((n_p, g.SPLIT_BYTES), dtype=torch.uint8).pin_memory()
+            lo_h = torch.empty_like(so_h).pin_memory()
+            h2d = rows_h.numel() * 4 + offs_h.numel() * 8
+            d2h = 2 * n_p * g.SPLIT_BYTES
+
+            def step_e2e():
+                sess.check(g.gbt_build_level(ctx, rows_h, offs_h, n_b, hs))
+                sess.check(g.gbt_subtract_and_find(ctx, hp, None, hs, large, n_p, prm, so_h, lo_h))
+        else:
+            gp_h = torch.from_numpy(w.gpair).pin_memory()
+            offs_h = torch.from_numpy(lv.offsets).pin_memory()
+            so_h = torch.empty((1, g.SPLIT_BYTES), dtype=torch.uint8).pin_memory()
+            h2d = gp_h.numel() * 4 + offs_h.numel() * 8
+            d2h = g.SPLIT_BYTES
+
+            def step_e2e():
+                sess.check(g.gbt_begin_tree(ctx, gp_h, sg, sh))
+                sess.check(g.gbt_build_level(ctx, None, offs_h, 1, hs))
+                sess.check(g.gbt_find_splits(ctx, hs, 1, prm, so_h))
+        for i in range(3):
+            flush(i)
+            step_e2e()
+            sess.check(sess.sync())
+        e2e_ms = []
+        for i in range(args.steps):
+            flush(i)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            step_e2e()
+            b.record(stream)
+            b.synchronize()  # the host reads the step's result
+            e2e_ms.append(a.elapsed_time(b))
+        assert sess.sync() == 0
+        e2e = {"value": entries / (statistics.mean(e2e_ms) / 1e3) * world, "unit": UNIT,
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+        sess.close()
+
+    total_ms = sum(ms)
+    if dist is not None:
+        t = torch.tensor([total_ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+        e = torch.tensor([e2e["value"] / world], device=dev, dtype=torch.float64)
+        dist.all_reduce(e, op=dist.ReduceOp.MIN)
+        e2e["value"] = float(e.item()) * world
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return
+    peak, peak_kind = _peaks()
+    value = world * args.steps * entries / (total_ms / 1e3)
+    hk_ms, hk_n = snap[hist_kernel]
+    hk_avg = hk_ms / max(hk_n, 1)
+    achieved = kernel_bytes / (hk_avg / 1e3) / 1e9 if hk_n else None
+    traffic = _profile_traffic(args.workload) if w.width == 1 else None
+    step_ms = total_ms / args.steps
+    level_gbs = level_bytes / (step_ms / 1e3) / 1e9
+    cpu_v, cpu_sample, _ = cpu_oracle_timing(w, budget_s=args.cpu_budget)
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "int64", "data": "synthetic",
+        "config": {"workload": WORKLOAD_TEXT[args.workload], "rows_built": R, "features": w.n_features,
+                   "bin_bytes": w.width, "slots_per_feature": B, "nodes_built": n_b, "nodes_derived": n_p,
+                   "entries_per_step": entries, "l2": f"flushed before every step ({2 * l2 >> 20} MiB write)",
+                   "parallelism": f"replicas{world}"},
+        "roofline": {"bound": "hbm", "kernel": hist_kernel, "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": (achieved / peak) if achieved else None, "traffic": traffic,
+                     "algorithmic_bytes_per_launch": kernel_bytes, "avg_launch_ms": hk_avg,
+                     "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"},
+        "level_roofline": {"algorithmic_bytes_per_step": level_bytes, "achieved_gbs": level_gbs,
+                           "frac": level_gbs / peak, "peak": peak},
+        "kernels_ms_per_launch": {k: (v[0] / max(v[1], 1)) for k, v in snap.items() if v[1]},
+        "profiled_pass_ms_per_step": sum(ms_prof) / len(ms_prof),
+        "warm_l2": {"ms_per_step": sum(ms_warm) / len(ms_warm),
+                    "value": world * entries / (sum(ms_warm) / len(ms_warm) / 1e3)},
+        "e2e": e2e,
+        "gpu_launches": int(launches),
+        "clocks": clk,
+        "cpu_baseline": {"value": cpu_v, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": cpu_sample},
+        "wall_s_timed": wall,
+    }
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    w = synth.make(args.workload)
+    par, lv = level_plan(w)
+    B = w.n_bins + 1
+    entries, R, n_b, n_p, kernel_bytes, level_bytes = entries_and_bytes(w, lv, B)
+    v, sample, per = cpu_oracle_timing(w, budget_s=args.ref_budget, steps=args.steps, warmup=args.warmup)
+    line = {
+        "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * statistics.mean(per), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "int64", "data": "synthetic",
+        "config": {"workload": WORKLOAD_TEXT[args.workload], "rows_built": R, "features": w.n_features,
+                   "bin_bytes": w.width, "slots_per_feature": B, "nodes_built": n_b, "nodes_derived": n_p,
+                   "entries_per_step": entries, "parallelism": "serial CPU oracle"},
+        "impl": "reference",
+        "cpu_baseline": {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOAD_TEXT), default="level5")
+    ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle time for cpu_baseline")
+    ap.add_argument("--ref-budget", type=float, default=90.0, help="seconds of oracle time for --impl reference")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_gpu(args, rank, world, local_rank)
+
+
+if __name__ == "__main__":
+    main()

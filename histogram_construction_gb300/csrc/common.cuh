@@ -26,13 +26,6 @@ struct DevState {
   int32_t pad;
 };
 
-// Per-feature split candidate written by the scan kernels.
-struct Cand {
-  double gain;
-  int32_t t;    // cut (INT32_MAX when no valid candidate)
-  int32_t dir;  // 0 missing right, 1 missing left
-};
-
 constexpr int MIRROR_STRIP_BYTES = 64;  // bytes per row per mirror tile of features
 
 __device__ __forceinline__ void raise_err(DevState *st, uint32_t bit) { atomicOr(&st->err, bit); }

@@ -84,7 +84,8 @@ struct gbt_ctx {
   // state + scratch
   DevState *st = nullptr;
   uint32_t *err_host = nullptr;  // pinned
-  Buf rec, chunk_prefix, rows_in, offs_in, cand, splits_a, splits_b, parent_of_in, tile_counts, lrank, slab;
+  Buf rec, chunk_prefix, rows_in, offs_in, cand, splits_a, splits_b, parent_of_in, tile_counts, lrank, slab,
+      counters;
   std::string last_error;
   int64_t launches = 0;
   // diagnostics: per-launch event pairs
@@ -224,13 +225,60 @@ int h16_ts_for(int B) {
   return 0;
 }
 
+// Completion counters of the split kernels: zero when allocated, and every
+// launch leaves them zero again (the last CTA of a group resets its counter).
+gbt_status ensure_counters(gbt_ctx *c, size_t n) {
+  const size_t bytes = std::max<size_t>(n, 1) * sizeof(uint32_t);
+  if (c->counters.cap >= bytes) return GBT_OK;
+  gbt_status s = ensure(c, c->counters, bytes, "split counters");
+  if (s != GBT_OK) return s;
+  CUDA_TRY(c, cudaMemsetAsync(c->counters.p, 0, c->counters.cap, c->stream), "zero split counters");
+  return GBT_OK;
+}
+
+// Rounds of 32 slots held in registers by the split kernels (0: streaming).
+int scan_rounds(int B) {
+  const int r = (B + 31) / 32;
+  if (r <= 1) return 1;
+  if (r <= 2) return 2;
+  if (r <= 4) return 4;
+  if (r <= 8) return 8;
+  return 0;
+}
+
 SplitParams make_sp(const gbt_ctx *c, const gbt_params *prm) {
   SplitParams sp;
   sp.lambda = prm->lambda;
   sp.gamma = prm->gamma;
-  sp.mcw = prm->min_child_weight;
   sp.inv_sg = c->inv_sg;
   sp.inv_sh = c->inv_sh;
+  // smallest H >= 1 with (double)H * inv_sh >= min_child_weight; the map
+  // H -> fl(fl(H) * inv_sh) is non-decreasing, so validity is H >= h_min
+  const double mcw = prm->min_child_weight;
+  auto ok = [&](int64_t h) { return (double)h * c->inv_sh >= mcw; };
+  const int64_t top = (int64_t)1 << 62;
+  if (!ok(top)) {
+    sp.h_min = INT64_MAX;
+  } else if (ok(1)) {
+    sp.h_min = 1;
+  } else {
+    int64_t lo = 1, hi = top;  // ok(lo) false, ok(hi) true
+    while (hi - lo > 1) {
+      const int64_t mid = lo + (hi - lo) / 2;
+      if (ok(mid)) hi = mid; else lo = mid;
+    }
+    sp.h_min = hi;
+  }
+  sp.lambda_f = (float)prm->lambda;
+  sp.gamma_f = (float)prm->gamma;
+  sp.gamma_abs_f = fabsf((float)prm->gamma);
+  sp.inv_sg_f = (float)c->inv_sg;
+  sp.inv_sh_f = (float)c->inv_sh;
+  sp.filter = (prm->lambda >= 0.0 && isfinite(prm->lambda) && isfinite(prm->gamma) && fabs(prm->gamma) < 1e30 &&
+               prm->lambda < 1e30 && isfinite(sp.inv_sg_f) && isfinite(sp.inv_sh_f) && sp.inv_sg_f > 0.f &&
+               sp.inv_sh_f > 0.f)
+                  ? 1
+                  : 0;
   return sp;
 }
 
@@ -288,7 +336,8 @@ gbt_status gbt_destroy(gbt_ctx *c) {
   cudaSetDevice(c->device);
   cudaStreamSynchronize(c->stream);
   Buf *bufs[] = {&c->mirror, &c->q, &c->rec, &c->chunk_prefix, &c->rows_in, &c->offs_in, &c->cand,
-                 &c->splits_a, &c->splits_b, &c->parent_of_in, &c->tile_counts, &c->lrank, &c->slab};
+                 &c->splits_a, &c->splits_b, &c->parent_of_in, &c->tile_counts, &c->lrank, &c->slab,
+                 &c->counters};
   for (Buf *b : bufs) release(c, *b);
   if (c->st) cudaFreeAsync(c->st, c->stream);
   cudaStreamSynchronize(c->stream);
@@ -411,9 +460,9 @@ gbt_status gbt_begin_tree(gbt_ctx *c, const float *gpair, float scale_g, float s
   if (!aligned16(gp) && ((reinterpret_cast<uintptr_t>(gp) & 7u) != 0))
     return fail(c, GBT_ERR_INVALID_ARG, "gpair must be 8-byte aligned");
   CUDA_TRY(c, cudaMemsetAsync(&c->st->qmax, 0, sizeof(uint32_t), c->stream), "reset qmax");
-  const int grid = grid_for(c, c->n_rows, 256, 8);
+  const int grid = grid_for(c, c->n_rows, 1024, 2);
   prof_begin(c);
-  k_quantise<<<grid, 256, 0, c->stream>>>((const float2 *)gp, c->n_rows, scale_g, scale_h, (int2 *)c->q.p, c->st);
+  k_quantise<<<grid, 1024, 0, c->stream>>>((const float2 *)gp, c->n_rows, scale_g, scale_h, (int2 *)c->q.p, c->st);
   LAUNCH_CHECK(c, "k_quantise");
   c->sg = scale_g;
   c->sh = scale_h;
@@ -589,23 +638,30 @@ gbt_status gbt_find_splits(gbt_ctx *c, const int64_t *hist, int32_t n_nodes, con
   if (!c->tree_ready) return fail(c, GBT_ERR_STATE, "gbt_begin_tree first (scales)");
   if (!params || n_nodes < 0) return fail(c, GBT_ERR_INVALID_ARG, "params NULL or n_nodes < 0");
   if (n_nodes == 0) return GBT_OK;
+  if (n_nodes > 65535) return fail(c, GBT_ERR_UNSUPPORTED, "n_nodes must be <= 65535");
   if (ptr_kind(hist) != 1 || !aligned16(hist)) return fail(c, GBT_ERR_INVALID_ARG, "hist must be 16-byte aligned device memory");
   SplitOut *dout = nullptr;
   bool host = false;
   s = split_out_view(c, out, n_nodes, c->splits_a, &dout, &host);
   if (s != GBT_OK) return s;
-  s = ensure(c, c->cand, (size_t)n_nodes * c->n_features * sizeof(Cand), "candidates");
+  const int nfb = (c->n_features + SCAN_FEATS - 1) / SCAN_FEATS;
+  s = ensure(c, c->cand, (size_t)n_nodes * nfb * sizeof(Cand), "candidates");
+  if (s != GBT_OK) return s;
+  s = ensure_counters(c, (size_t)n_nodes);
   if (s != GBT_OK) return s;
   const SplitParams sp = make_sp(c, params);
-  const int64_t units = (int64_t)n_nodes * c->n_features;
-  const int grid = grid_for(c, units * 32, SCAN_THREADS, 8);
+  const dim3 grid(nfb, n_nodes);
+  Cand *cd = (Cand *)c->cand.p;
+  uint32_t *cnt = (uint32_t *)c->counters.p;
   prof_begin(c);
-  k_find<<<grid, SCAN_THREADS, 0, c->stream>>>(hist, n_nodes, c->n_features, c->n_bins, sp, (Cand *)c->cand.p);
+  switch (scan_rounds(c->n_bins + 1)) {
+    case 1: k_find<1><<<grid, SCAN_THREADS, 0, c->stream>>>(hist, c->n_features, c->n_bins, sp, cd, cnt, dout); break;
+    case 2: k_find<2><<<grid, SCAN_THREADS, 0, c->stream>>>(hist, c->n_features, c->n_bins, sp, cd, cnt, dout); break;
+    case 4: k_find<4><<<grid, SCAN_THREADS, 0, c->stream>>>(hist, c->n_features, c->n_bins, sp, cd, cnt, dout); break;
+    case 8: k_find<8><<<grid, SCAN_THREADS, 0, c->stream>>>(hist, c->n_features, c->n_bins, sp, cd, cnt, dout); break;
+    default: k_find<0><<<grid, SCAN_THREADS, 0, c->stream>>>(hist, c->n_features, c->n_bins, sp, cd, cnt, dout); break;
+  }
   LAUNCH_CHECK(c, "k_find");
-  prof_begin(c);
-  k_reduce_splits<<<n_nodes, 256, 0, c->stream>>>((const Cand *)c->cand.p, n_nodes, c->n_features, c->n_bins, 0, hist,
-                                                  nullptr, dout, nullptr);
-  LAUNCH_CHECK(c, "k_reduce_splits");
   if (host)
     CUDA_TRY(c, cudaMemcpyAsync(out, dout, (size_t)n_nodes * sizeof(gbt_split), cudaMemcpyDeviceToHost, c->stream),
              "splits to host");
@@ -632,19 +688,28 @@ gbt_status gbt_subtract_and_find(gbt_ctx *c, const int64_t *parent_hist, const i
   if (s != GBT_OK) return s;
   s = split_out_view(c, large_out, n_pairs, c->splits_b, &db, &hb);
   if (s != GBT_OK) return s;
-  s = ensure(c, c->cand, (size_t)2 * n_pairs * c->n_features * sizeof(Cand), "candidates");
+  const int nfb = (c->n_features + SCAN_FEATS - 1) / SCAN_FEATS;
+  s = ensure(c, c->cand, (size_t)2 * n_pairs * nfb * sizeof(Cand), "candidates");
+  if (s != GBT_OK) return s;
+  s = ensure_counters(c, (size_t)n_pairs);
   if (s != GBT_OK) return s;
   const SplitParams sp = make_sp(c, params);
-  const int64_t units = (int64_t)n_pairs * c->n_features;
-  const int grid = grid_for(c, units * 32, SCAN_THREADS, 8);
+  const dim3 grid(nfb, n_pairs);
+  Cand *cd = (Cand *)c->cand.p;
+  uint32_t *cnt = (uint32_t *)c->counters.p;
   prof_begin(c);
-  k_subtract_find<<<grid, SCAN_THREADS, 0, c->stream>>>(parent_hist, po, small_hist, large_hist, n_pairs,
-                                                       c->n_features, c->n_bins, sp, (Cand *)c->cand.p, c->st);
+#define GBT_SUBFIND(NR)                                                                                         \
+  k_subtract_find<NR><<<grid, SCAN_THREADS, 0, c->stream>>>(parent_hist, po, small_hist, large_hist, c->n_features, \
+                                                            c->n_bins, sp, cd, cnt, da, db, c->st)
+  switch (scan_rounds(c->n_bins + 1)) {
+    case 1: GBT_SUBFIND(1); break;
+    case 2: GBT_SUBFIND(2); break;
+    case 4: GBT_SUBFIND(4); break;
+    case 8: GBT_SUBFIND(8); break;
+    default: GBT_SUBFIND(0); break;
+  }
+#undef GBT_SUBFIND
   LAUNCH_CHECK(c, "k_subtract_find");
-  prof_begin(c);
-  k_reduce_splits<<<2 * n_pairs, 256, 0, c->stream>>>((const Cand *)c->cand.p, 2 * n_pairs, c->n_features, c->n_bins,
-                                                      1, small_hist, large_hist, da, db);
-  LAUNCH_CHECK(c, "k_reduce_splits");
   if (ha)
     CUDA_TRY(c, cudaMemcpyAsync(small_out, da, (size_t)n_pairs * sizeof(gbt_split), cudaMemcpyDeviceToHost, c->stream),
              "splits to host");
@@ -744,20 +809,23 @@ gbt_status gbt_profile_read(gbt_ctx *c, const char *kernel, double *total_ms, in
   CUDA_TRY(c, cudaStreamSynchronize(c->stream), "stream synchronize");
   double ms = 0.0;
   int64_t n = 0;
+  std::vector<gbt_ctx::ProfRec> keep;
   for (const auto &r : c->prof_pending) {
-    if (!kernel || strcmp(kernel, r.name) == 0) {
-      float t = 0.f;
-      if (cudaEventElapsedTime(&t, r.a, r.b) == cudaSuccess) {
-        ms += t;
-        ++n;
-      } else {
-        cudaGetLastError();
-      }
+    if (kernel && strcmp(kernel, r.name) != 0) {
+      keep.push_back(r);
+      continue;
+    }
+    float t = 0.f;
+    if (cudaEventElapsedTime(&t, r.a, r.b) == cudaSuccess) {
+      ms += t;
+      ++n;
+    } else {
+      cudaGetLastError();
     }
     c->prof_pool.push_back(r.a);
     c->prof_pool.push_back(r.b);
   }
-  c->prof_pending.clear();
+  c->prof_pending.swap(keep);
   *total_ms = ms;
   *launches = n;
   return GBT_OK;

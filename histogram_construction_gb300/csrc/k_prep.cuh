@@ -58,7 +58,7 @@ __global__ void __launch_bounds__(256) k_mirror(const T *__restrict__ bins, int6
 // quantised to fixed point before integer atomics; bonsai "9. Parallelism &
 // determinism", "The idea": int64 cells are exact in any order.
 // Also reduces max |q| into st->qmax (zeroed by the caller).
-__global__ void __launch_bounds__(256) k_quantise(const float2 *__restrict__ gp, int64_t n, float sg, float sh,
+__global__ void __launch_bounds__(1024) k_quantise(const float2 *__restrict__ gp, int64_t n, float sg, float sh,
                                                   int2 *__restrict__ q, DevState *st) {
   uint32_t mx = 0, bad = 0;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
@@ -83,9 +83,21 @@ __global__ void __launch_bounds__(256) k_quantise(const float2 *__restrict__ gp,
     const uint32_t ah = qh < 0 ? (uint32_t)(-(int64_t)qh) : (uint32_t)qh;
     mx = max(mx, max(ag, ah));
   }
+  // one atomic per block: same-address atomics serialise in L2
+  __shared__ uint32_t s_mx[32];
+  __shared__ uint32_t s_bad;
+  if (threadIdx.x == 0) s_bad = 0;
   for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-  if ((threadIdx.x & 31) == 0 && mx) atomicMax(&st->qmax, mx);
-  if (bad) raise_err(st, ERRBIT_QUANT);
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) s_mx[threadIdx.x >> 5] = mx;
+  if (bad) s_bad = 1;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    uint32_t m = 0;
+    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) m = max(m, s_mx[w]);
+    if (m) atomicMax(&st->qmax, m);
+    if (s_bad) raise_err(st, ERRBIT_QUANT);
+  }
 }
 
 }  // namespace gbt

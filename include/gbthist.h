@@ -179,9 +179,9 @@ gbt_status gbt_partition_level(gbt_ctx *ctx, const int32_t *rows, const int64_t 
 /* Per-kernel device-time accounting for diagnostics. When enabled, every
  * kernel this context launches is bracketed by a pair of CUDA events on the
  * context stream. gbt_profile_read synchronises the stream, adds up the
- * elapsed times of the completed launches of `kernel` (a kernel name such as
- * "k_hist_u8"; NULL = all kernels) since the last read, returns them in
- * total_ms / launches, and forgets every recorded launch. */
+ * elapsed times of the recorded launches of `kernel` (a kernel name such as
+ * "k_hist_u8"; NULL = all kernels), returns them in total_ms / launches and
+ * forgets those launches (records of other kernels are kept). */
 gbt_status gbt_profile_enable(gbt_ctx *ctx, int on);
 gbt_status gbt_profile_read(gbt_ctx *ctx, const char *kernel, double *total_ms, int64_t *launches);
 

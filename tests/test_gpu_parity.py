@@ -352,3 +352,73 @@ def test_error_alloc_fault_injection(gb, monkeypatch):
         h = s.build_level(None, np.array([0, 5000], np.int64))
         assert s.sync() == 0
         assert int(h[0, 0, :, 1].sum()) == 5000
+
+
+# --------------------------------------------------------------------------- split find: golden cases and adversarial ties
+def _dummy_session(Session, n_bins, n_features, scale_g=1.0, scale_h=1.0):
+    """A context whose dataset shape (features, bins) matches histograms passed in directly."""
+    s = Session()
+    bins = np.zeros((n_features, 8), np.uint8 if n_bins < 255 else np.uint16)
+    s.upload_bins(bins, n_bins, 0xFF if n_bins < 255 else 0xFFFF)
+    s.begin_tree(np.zeros((8, 2), np.float32), scale_g, scale_h)
+    return s
+
+
+def test_golden_split_cases_on_gpu(gb):
+    """The hand-worked cases of tests/golden/split_cases.json through gbt_find_splits."""
+    import json
+    import os
+    from fractions import Fraction
+    g, Session, s2n = gb
+    with open(os.path.join(os.path.dirname(__file__), "golden", "split_cases.json")) as f:
+        cases = json.load(f)["cases"]
+    for case in cases:
+        hist = torch.tensor(np.array(case["hist"], np.int64)[None]).cuda()
+        s = _dummy_session(Session, case["n_bins"], hist.shape[1])
+        try:
+            out = s2n(s.find_splits(hist, lam=case["lambda"], gamma=case["gamma"], mcw=case["min_child_weight"]))
+            assert s.sync() == 0
+        finally:
+            s.close()
+        e = case["expect"]
+        for k in ("feature", "bin", "default_left", "g_left", "h_left", "g_right", "h_right"):
+            assert int(out[k][0]) == e[k], (case["name"], k)
+        if e["gain"] == "-inf":
+            assert out["gain"][0] == -np.inf
+        else:
+            assert out["gain"][0] == pytest.approx(float(Fraction(e["gain"])), rel=1e-14), case["name"]
+
+
+@pytest.mark.parametrize("seed,lam,gamma,mcw,sg,sh", [
+    (0, 1.0, 0.0, 0.0, 1.0, 1.0),
+    (1, 0.0, 0.5, 0.0, 1024.0, 4096.0),
+    (2, 3.0, -2.0, 1.5, 2.0 ** 20, 2.0 ** 18),
+    (3, 1e-3, 1e3, 0.0, 2.0 ** -20, 2.0 ** -10),   # tiny scales: huge converted values
+    (4, 0.0, 0.0, 0.0, 2.0 ** 40, 2.0 ** 40),        # huge scales: tiny converted values (double path)
+])
+def test_split_find_adversarial_ties_and_ranges(gb, oracle_mod, seed, lam, gamma, mcw, sg, sh):
+    """Random histograms with duplicated features (exact ties), magnitudes over many binades, cuts with
+    equal gains in both directions; the GPU must match the all-double oracle bit for bit."""
+    g, Session, s2n = gb
+    rng = np.random.default_rng(900 + seed)
+    n_nodes, F, n_bins = 6, 23, 61
+    B = n_bins + 1
+    hist = np.zeros((n_nodes, F, B, 2), np.int64)
+    for n in range(n_nodes):
+        for f in range(F):
+            scale = 2.0 ** rng.integers(0, 40)
+            hist[n, f, :, 0] = (rng.standard_normal(B) * scale).astype(np.int64)
+            hist[n, f, :, 1] = (rng.random(B) * scale).astype(np.int64) + 1
+            if rng.random() < 0.3:
+                hist[n, f, -1] = 0  # no missing mass: both directions tie
+        hist[n, 5] = hist[n, 2]        # duplicated features: exact ties across features
+        hist[n, 11] = hist[n, 2]
+        hist[n, 7, 3:] = 0             # mass concentrated at the start
+    out_ref, st = oracle_mod.find_splits(hist, n_bins, lam, gamma, mcw, sg, sh)
+    s = _dummy_session(Session, n_bins, F, sg, sh)
+    try:
+        got = s2n(s.find_splits(torch.from_numpy(hist).cuda(), lam=lam, gamma=gamma, mcw=mcw))
+        assert s.sync() == 0
+    finally:
+        s.close()
+    assert_splits_equal(got, out_ref, f"seed {seed}")
