@@ -236,16 +236,6 @@ gbt_status ensure_counters(gbt_ctx *c, size_t n) {
   return GBT_OK;
 }
 
-// Rounds of 32 slots held in registers by the split kernels (0: streaming).
-int scan_rounds(int B) {
-  const int r = (B + 31) / 32;
-  if (r <= 1) return 1;
-  if (r <= 2) return 2;
-  if (r <= 4) return 4;
-  if (r <= 8) return 8;
-  return 0;
-}
-
 SplitParams make_sp(const gbt_ctx *c, const gbt_params *prm) {
   SplitParams sp;
   sp.lambda = prm->lambda;
@@ -644,23 +634,15 @@ gbt_status gbt_find_splits(gbt_ctx *c, const int64_t *hist, int32_t n_nodes, con
   bool host = false;
   s = split_out_view(c, out, n_nodes, c->splits_a, &dout, &host);
   if (s != GBT_OK) return s;
-  const int nfb = (c->n_features + SCAN_FEATS - 1) / SCAN_FEATS;
+  const int nfb = (c->n_features + SCAN_WARPS - 1) / SCAN_WARPS;
   s = ensure(c, c->cand, (size_t)n_nodes * nfb * sizeof(Cand), "candidates");
   if (s != GBT_OK) return s;
   s = ensure_counters(c, (size_t)n_nodes);
   if (s != GBT_OK) return s;
   const SplitParams sp = make_sp(c, params);
-  const dim3 grid(nfb, n_nodes);
-  Cand *cd = (Cand *)c->cand.p;
-  uint32_t *cnt = (uint32_t *)c->counters.p;
   prof_begin(c);
-  switch (scan_rounds(c->n_bins + 1)) {
-    case 1: k_find<1><<<grid, SCAN_THREADS, 0, c->stream>>>(hist, c->n_features, c->n_bins, sp, cd, cnt, dout); break;
-    case 2: k_find<2><<<grid, SCAN_THREADS, 0, c->stream>>>(hist, c->n_features, c->n_bins, sp, cd, cnt, dout); break;
-    case 4: k_find<4><<<grid, SCAN_THREADS, 0, c->stream>>>(hist, c->n_features, c->n_bins, sp, cd, cnt, dout); break;
-    case 8: k_find<8><<<grid, SCAN_THREADS, 0, c->stream>>>(hist, c->n_features, c->n_bins, sp, cd, cnt, dout); break;
-    default: k_find<0><<<grid, SCAN_THREADS, 0, c->stream>>>(hist, c->n_features, c->n_bins, sp, cd, cnt, dout); break;
-  }
+  k_find<<<dim3(nfb, n_nodes), SCAN_THREADS, 0, c->stream>>>(hist, c->n_features, c->n_bins, sp, (Cand *)c->cand.p,
+                                                             (uint32_t *)c->counters.p, dout);
   LAUNCH_CHECK(c, "k_find");
   if (host)
     CUDA_TRY(c, cudaMemcpyAsync(out, dout, (size_t)n_nodes * sizeof(gbt_split), cudaMemcpyDeviceToHost, c->stream),
@@ -688,27 +670,16 @@ gbt_status gbt_subtract_and_find(gbt_ctx *c, const int64_t *parent_hist, const i
   if (s != GBT_OK) return s;
   s = split_out_view(c, large_out, n_pairs, c->splits_b, &db, &hb);
   if (s != GBT_OK) return s;
-  const int nfb = (c->n_features + SCAN_FEATS - 1) / SCAN_FEATS;
+  const int nfb = (c->n_features + SCAN_WARPS / 2 - 1) / (SCAN_WARPS / 2);
   s = ensure(c, c->cand, (size_t)2 * n_pairs * nfb * sizeof(Cand), "candidates");
   if (s != GBT_OK) return s;
   s = ensure_counters(c, (size_t)n_pairs);
   if (s != GBT_OK) return s;
   const SplitParams sp = make_sp(c, params);
-  const dim3 grid(nfb, n_pairs);
-  Cand *cd = (Cand *)c->cand.p;
-  uint32_t *cnt = (uint32_t *)c->counters.p;
   prof_begin(c);
-#define GBT_SUBFIND(NR)                                                                                         \
-  k_subtract_find<NR><<<grid, SCAN_THREADS, 0, c->stream>>>(parent_hist, po, small_hist, large_hist, c->n_features, \
-                                                            c->n_bins, sp, cd, cnt, da, db, c->st)
-  switch (scan_rounds(c->n_bins + 1)) {
-    case 1: GBT_SUBFIND(1); break;
-    case 2: GBT_SUBFIND(2); break;
-    case 4: GBT_SUBFIND(4); break;
-    case 8: GBT_SUBFIND(8); break;
-    default: GBT_SUBFIND(0); break;
-  }
-#undef GBT_SUBFIND
+  k_subtract_find<<<dim3(nfb, n_pairs), SCAN_THREADS, 0, c->stream>>>(
+      parent_hist, po, small_hist, large_hist, c->n_features, c->n_bins, sp, (Cand *)c->cand.p,
+      (uint32_t *)c->counters.p, da, db, c->st);
   LAUNCH_CHECK(c, "k_subtract_find");
   if (ha)
     CUDA_TRY(c, cudaMemcpyAsync(small_out, da, (size_t)n_pairs * sizeof(gbt_split), cudaMemcpyDeviceToHost, c->stream),
