@@ -88,6 +88,9 @@ struct gbt_ctx {
       counters;
   std::string last_error;
   int64_t launches = 0;
+  // tuning (defaults; GBT_TARGET_ITEMS / GBT_U8_CTAS_PER_SM override them for sweeps)
+  int target_items = 0;
+  int u8_ctas_per_sm = 4;
   // diagnostics: per-launch event pairs
   bool prof = false;
   struct ProfRec {
@@ -289,6 +292,8 @@ gbt_status gbt_create(int device, void *cuda_stream, gbt_ctx **out) {
   c->stream = reinterpret_cast<cudaStream_t>(cuda_stream);
   cudaDeviceGetAttribute(&c->n_sm, cudaDevAttrMultiProcessorCount, device);
   cudaDeviceGetAttribute(&c->smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device);
+  if (const char *e = getenv("GBT_TARGET_ITEMS")) c->target_items = std::max(0, atoi(e));
+  if (const char *e = getenv("GBT_U8_CTAS_PER_SM")) c->u8_ctas_per_sm = std::min(4, std::max(1, atoi(e)));
   void *st = nullptr;
   e = dev_alloc(&st, sizeof(DevState), c->stream);
   if (e != cudaSuccess) {
@@ -524,13 +529,14 @@ gbt_status gbt_build_level(gbt_ctx *c, const int32_t *rows, const int64_t *node_
   lp.rows = (const int32_t *)rows_d;
   lp.offs = (const int64_t *)offs_d;
   lp.n_nodes = n_nodes;
-  const int hist_ctas = c->n_sm;  // one resident CTA per SM for both histogram kernels
+  // persistent grids: 4 CTAs per SM (u8, 49 KB shared each), 1 per SM (u16)
+  const int hist_ctas = c->bin_bytes == 1 ? c->n_sm * c->u8_ctas_per_sm : c->n_sm;
   if (c->bin_bytes == 1) {
-    lp.n_fgroups = c->n_tiles;
+    lp.n_fgroups = (c->n_features + H8_TS - 1) / H8_TS;
   } else {
     lp.n_fgroups = (c->n_features + c->ts16 - 1) / c->ts16;
   }
-  lp.target_items = hist_ctas * 2;
+  lp.target_items = c->target_items > 0 ? c->target_items : c->n_sm * 2;
   lp.pad = 0;
   lp.n_rows = c->n_rows;
   lp.q = (const int2 *)c->q.p;
@@ -541,9 +547,9 @@ gbt_status gbt_build_level(gbt_ctx *c, const int32_t *rows, const int64_t *node_
   lp.st = c->st;
   {
     const int64_t work = R_host >= 0 ? R_host : c->n_rows;
-    const int grid = grid_for(c, std::max<int64_t>(work, 1), 1024, 2);
+    const int grid = grid_for(c, std::max<int64_t>(work, 1) / 4 + 1, 512, 1);
     prof_begin(c);
-    k_level_prologue<<<grid, 1024, 0, c->stream>>>(lp);
+    k_level_prologue<<<grid, 512, 0, c->stream>>>(lp);
     LAUNCH_CHECK(c, "k_level_prologue");
   }
   if (c->bin_bytes == 1) {

@@ -9,25 +9,26 @@
 //
 // GB300 design (differs from the pages' (feature, node, row-chunk) grid with
 // float shared cells):
-//  * work items (node, feature group, row chunk) handed out to a persistent
-//    grid by an atomic counter;
-//  * one CTA holds a 64-feature x 256-slot histogram of int32 (G, H) pairs in
-//    shared memory (128 KB); each lane adds (qg, qh) with two 32-bit shared
-//    atomics, and the column order of the features is permuted so that the 32
-//    lanes of every atomic instruction hit 32 different banks whatever the bin
-//    values (no bank conflicts, no same-address conflicts);
+//  * work items (node, 16-feature group, row chunk) handed out to a persistent
+//    grid of several CTAs per SM by an atomic counter;
+//  * a CTA holds a 16-feature x 256-slot histogram of int32 (G, H) pairs in
+//    shared memory (32 KB); each lane adds (qg, qh) with two 32-bit shared
+//    atomics, and lanes are assigned to (row, feature, component) so that the
+//    32 lanes of every atomic instruction hit 32 different banks whatever the
+//    bin values (no bank conflicts, no same-address conflicts);
 //  * a chunk never holds more rows than keep every int32 partial exact
 //    (rows * max|q| < 2^31), so the int64 result is exact;
-//  * the flush converts to int64 in a padded staging buffer and writes each
-//    feature's slot strip with one TMA bulk copy (single-chunk node) or one
-//    bulk reduce-add into the zeroed output (multi-chunk node).
+//  * the flush transposes the cells to int64 through a small padded staging
+//    buffer and writes each feature's slot range with one TMA bulk copy
+//    (node built by one item) or one bulk reduce-add into the zeroed output
+//    (node split into several chunks).
 #pragma once
 
 #include "common.cuh"
 
 namespace gbt {
 
-constexpr int CHUNK_MIN_ROWS = 4096;
+constexpr int CHUNK_MIN_ROWS = 2048;
 
 struct LevelParams {
   const int32_t *rows;   // level row list or nullptr (identity)
@@ -57,7 +58,7 @@ __device__ __forceinline__ int64_t level_chunk_rows(const LevelParams &p) {
 // Level prologue: block 0 plans the work items; all blocks gather the level
 // records (row id and its quantised pair, in level order) and zero the
 // outputs of nodes that will be reduced from several chunks.
-__global__ void __launch_bounds__(1024) k_level_prologue(LevelParams p) {
+__global__ void __launch_bounds__(512) k_level_prologue(LevelParams p) {
   const int64_t chunk = level_chunk_rows(p);
   const int64_t R = p.offs[p.n_nodes] - p.offs[0];
   if (blockIdx.x == 0) {
@@ -114,30 +115,41 @@ __global__ void __launch_bounds__(1024) k_level_prologue(LevelParams p) {
   }
   // gather level records (bounded by n_rows whatever the offsets say)
   const int64_t Rg = min(max(R, (int64_t)0), p.n_rows);
+  const int64_t nthr = (int64_t)gridDim.x * blockDim.x;
+  const int64_t gtid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (p.rows != nullptr) {
     uint32_t bad = 0;
-    for (int64_t k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; k < Rg; k += (int64_t)gridDim.x * blockDim.x) {
-      const int32_t r = p.rows[k];
-      int4 rec;
-      if (r >= 0 && r < p.n_rows) {
-        const int2 qq = p.q[r];
-        rec = make_int4(r, qq.x, qq.y, 0);
-      } else {
-        rec = make_int4(-1, 0, 0, 0);
-        bad = 1;
+    for (int64_t k0 = gtid; k0 < Rg; k0 += 4 * nthr) {
+      int32_t r[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int64_t k = k0 + u * nthr;
+        r[u] = k < Rg ? __ldg(p.rows + k) : -1;
       }
-      p.rec[k] = rec;
+      int2 qq[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const bool ok = r[u] >= 0 && r[u] < p.n_rows;
+        qq[u] = ok ? __ldg(p.q + r[u]) : make_int2(0, 0);
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int64_t k = k0 + u * nthr;
+        if (k >= Rg) break;
+        const bool ok = r[u] >= 0 && r[u] < p.n_rows;
+        if (!ok) bad = 1;
+        p.rec[k] = ok ? make_int4(r[u], qq[u].x, qq[u].y, 0) : make_int4(-1, 0, 0, 0);
+      }
     }
     if (bad) raise_err(p.st, ERRBIT_ROW);
   }
   // zero the outputs of multi-chunk nodes (they are reduced into)
+  const int64_t units = p.node_int64s / 2;
   for (int n = 0; n < p.n_nodes; ++n) {
-    const int64_t rows_n = p.offs[n + 1] - p.offs[n];
+    const int64_t rows_n = __ldg(p.offs + n + 1) - __ldg(p.offs + n);
     if (rows_n <= chunk) continue;
     int4 *dst = reinterpret_cast<int4 *>(p.hist_out + (int64_t)n * p.node_int64s);
-    const int64_t units = p.node_int64s / 2;
-    for (int64_t u = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; u < units; u += (int64_t)gridDim.x * blockDim.x)
-      dst[u] = make_int4(0, 0, 0, 0);
+    for (int64_t u = gtid; u < units; u += nthr) dst[u] = make_int4(0, 0, 0, 0);
   }
 }
 
@@ -167,27 +179,22 @@ __device__ __forceinline__ Item decode_item(int32_t id, const LevelParams &p, in
 }
 
 // ----------------------------------------------------------------------------
-// u8 kernel: 64 features per item, conflict-free column permutation.
+// u8 kernel: 16 features per item (one quarter of a 64-byte mirror strip).
 //
-// Lane l of a warp takes row rho = l/4 of an 8-row group and the 16-byte
-// quarter qq = l%4 of the row's 64-byte strip (words 4qq..4qq+3). For atomic
-// instruction (e, j, c) the lane uses word w = 4qq + ((e + rho/2) & 3), byte j,
-// and component (c ^ (rho & 1)) (0 = G, 1 = H). Feature f = 4w + j lives in
-// column col(f) = 16 j + ((w + 4 j) & 15) of a 64-cell slot row; the word
-// index of the component is 2 (slot * 64 + col) + comp, whose bank is
-// 2 ((w + 4 j) & 15) + comp = 2 (4 ((qq + j) & 3) + ((e + rho/2) & 3)) + comp:
-// distinct for the 32 lanes.
-constexpr int H8_THREADS = 1024;
-constexpr int H8_HIST_BYTES = 256 * 64 * 8;          // slots x columns x (G,H) int32
-constexpr int H8_STAGE_ROW = 256 * 16 + 16;          // one feature's int64 strip + 16 B pad
-constexpr int H8_STAGE_FEATS = 16;
-constexpr int H8_SMEM = H8_HIST_BYTES + H8_STAGE_FEATS * H8_STAGE_ROW;
-constexpr int H8_UNROLL = 4;
-
-__device__ __forceinline__ int h8_col(int f) {
-  const int w = f >> 2, j = f & 3;
-  return 16 * j + ((w + 4 * j) & 15);
-}
+// Lane l of a warp takes row rho = l/4 of an 8-row group and byte word
+// w = l%4 of the row's 16-byte quarter (one 32-bit load). In atomic
+// instruction (j, c) the lane adds byte jj = (j + rho/2) & 3 of its word,
+// i.e. feature f = 4w + jj, component (c ^ (rho & 1)) (0 = G, 1 = H). Cells
+// are [slot][16 features][G, H]; a slot row is 128 bytes = 32 banks, so the
+// bank of a lane is 2f + comp: distinct for the 32 lanes of every
+// instruction (f covers 16 values over (w, rho/2), comp separates rho&1).
+constexpr int H8_THREADS = 256;
+constexpr int H8_TS = 16;                                  // features per item
+constexpr int H8_HIST_BYTES = 256 * H8_TS * 8;             // 32 KB
+constexpr int H8_STAGE_SLOTS = 64;                         // slots per flush round
+constexpr int H8_STAGE_ROW = (H8_STAGE_SLOTS + 1) * 16;    // one feature's int64 pairs + pad
+constexpr int H8_SMEM = H8_HIST_BYTES + H8_TS * H8_STAGE_ROW;
+constexpr int H8_UNROLL = 8;
 
 struct Hist8Params {
   LevelParams lv;
@@ -196,7 +203,7 @@ struct Hist8Params {
   int32_t n_slots;        // B
 };
 
-__global__ void __launch_bounds__(H8_THREADS, 1) k_hist_u8(Hist8Params P) {
+__global__ void __launch_bounds__(H8_THREADS, 4) k_hist_u8(Hist8Params P) {
   extern __shared__ __align__(128) unsigned char smem[];
   uint32_t *hist = reinterpret_cast<uint32_t *>(smem);
   unsigned char *stage = smem + H8_HIST_BYTES;
@@ -211,19 +218,17 @@ __global__ void __launch_bounds__(H8_THREADS, 1) k_hist_u8(Hist8Params P) {
   const bool ident = (p.rows == nullptr);
 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
-  const int rho = lane >> 2, qq = lane & 3;
+  const int rho = lane >> 2, w = lane & 3;
   const int pr = rho >> 1, par = rho & 1;
-  // per-lane byte offsets of (e, j) columns, without the slot term
-  int colbyte[4][4];
+  // per-lane byte shift and column byte offset of instruction j
+  uint32_t shift[4], colb[4];
 #pragma unroll
-  for (int e = 0; e < 4; ++e)
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int w = 4 * qq + ((e + pr) & 3);
-      colbyte[e][j] = (16 * j + ((w + 4 * j) & 15)) * 8;
-    }
-  const int off0 = par ? 4 : 0;  // instruction c=0 component byte offset
-  const int off1 = par ? 0 : 4;
+  for (int j = 0; j < 4; ++j) {
+    const int jj = (j + pr) & 3;
+    shift[j] = 8u * jj;
+    colb[j] = (uint32_t)(4 * w + jj) * 8u;
+  }
+  const uint32_t off0 = par ? 4u : 0u, off1 = par ? 0u : 4u;
   const uint32_t hist_base = smem_addr(hist);
 
   for (;;) {
@@ -232,15 +237,14 @@ __global__ void __launch_bounds__(H8_THREADS, 1) k_hist_u8(Hist8Params P) {
     const int32_t id = s_item;
     if (id >= n_items) break;
     const Item it = decode_item(id, p, chunk);
-    // zero the shared histogram (B slot rows)
     {
       uint4 *h4 = reinterpret_cast<uint4 *>(hist);
-      const int n4 = B * 64 * 8 / 16;
+      const int n4 = B * H8_TS * 8 / 16;
       for (int i = threadIdx.x; i < n4; i += blockDim.x) h4[i] = make_uint4(0, 0, 0, 0);
     }
     __syncthreads();
-    // accumulate
-    const unsigned char *strip = P.mirror + (int64_t)it.fgroup * N * MIRROR_STRIP_BYTES + qq * 16;
+    const int tile = it.fgroup >> 2, sub = it.fgroup & 3;
+    const unsigned char *strip = P.mirror + (int64_t)tile * N * MIRROR_STRIP_BYTES + sub * 16 + w * 4;
     const int64_t step = (int64_t)8 * nwarps;
     for (int64_t g0 = it.k0 + 8 * warp; g0 < it.k1; g0 += step * H8_UNROLL) {
       int32_t rr[H8_UNROLL], vg[H8_UNROLL], vh[H8_UNROLL];
@@ -264,62 +268,50 @@ __global__ void __launch_bounds__(H8_THREADS, 1) k_hist_u8(Hist8Params P) {
           }
         }
       }
-      uint4 bv[H8_UNROLL];
+      uint32_t bw[H8_UNROLL];
 #pragma unroll
-      for (int u = 0; u < H8_UNROLL; ++u) {
-        bv[u] = make_uint4(0, 0, 0, 0);
-        if (rr[u] >= 0) bv[u] = ldg_nc_v4(strip + (int64_t)rr[u] * MIRROR_STRIP_BYTES);
-      }
+      for (int u = 0; u < H8_UNROLL; ++u)
+        bw[u] = rr[u] >= 0 ? __ldg(reinterpret_cast<const uint32_t *>(strip + (int64_t)rr[u] * MIRROR_STRIP_BYTES))
+                           : 0u;
 #pragma unroll
       for (int u = 0; u < H8_UNROLL; ++u) {
         if (rr[u] < 0) continue;
         const uint32_t v0 = par ? (uint32_t)vh[u] : (uint32_t)vg[u];
         const uint32_t v1 = par ? (uint32_t)vg[u] : (uint32_t)vh[u];
-        // rotate the 4 words by pr so that word index e of the rotated set is (e + pr) & 3
-        uint32_t wd[4];
-        {
-          const uint32_t a0 = bv[u].x, a1 = bv[u].y, a2 = bv[u].z, a3 = bv[u].w;
-          wd[0] = pr == 0 ? a0 : pr == 1 ? a1 : pr == 2 ? a2 : a3;
-          wd[1] = pr == 0 ? a1 : pr == 1 ? a2 : pr == 2 ? a3 : a0;
-          wd[2] = pr == 0 ? a2 : pr == 1 ? a3 : pr == 2 ? a0 : a1;
-          wd[3] = pr == 0 ? a3 : pr == 1 ? a0 : pr == 2 ? a1 : a2;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint32_t slot = (bw[u] >> shift[j]) & 0xffu;
+          const uint32_t a = hist_base + slot * (H8_TS * 8) + colb[j];
+          asm volatile("red.shared.add.u32 [%0], %1;" ::"r"(a + off0), "r"(v0) : "memory");
+          asm volatile("red.shared.add.u32 [%0], %1;" ::"r"(a + off1), "r"(v1) : "memory");
         }
-#pragma unroll
-        for (int e = 0; e < 4; ++e)
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const uint32_t slot = (wd[e] >> (8 * j)) & 0xffu;
-            const uint32_t a = hist_base + slot * 512u + (uint32_t)colbyte[e][j];
-            asm volatile("red.shared.add.u32 [%0], %1;" ::"r"(a + off0), "r"(v0) : "memory");
-            asm volatile("red.shared.add.u32 [%0], %1;" ::"r"(a + off1), "r"(v1) : "memory");
-          }
       }
     }
     __syncthreads();
-    // flush: 4 rounds of 16 features
-    const int f_tile0 = it.fgroup * 64;
+    // flush: rounds of 64 slots; lanes over features for conflict-free reads,
+    // staging rows padded by 16 bytes for conflict-free 16-byte writes
+    const int f0 = it.fgroup * H8_TS;
     int64_t *node_out = p.hist_out + (int64_t)it.node * p.node_int64s;
-    for (int r = 0; r < 4; ++r) {
-      const int f_first = f_tile0 + 16 * r;
-      if (f_first >= P.n_features) break;
-      // convert: lane -> (fi = lane & 15, slot = 2*warp + (lane >> 4) + 2*nwarps*i)
-      const int fi = lane & 15;
-      const int col = h8_col(16 * r + fi);
-      for (int s = 2 * warp + (lane >> 4); s < B; s += 2 * nwarps) {
-        const uint2 gh = *reinterpret_cast<const uint2 *>(hist + 2 * (s * 64 + col));
-        longlong2 v;
-        v.x = (long long)(int32_t)gh.x;
-        v.y = (long long)(int32_t)gh.y;
-        *reinterpret_cast<longlong2 *>(stage + fi * H8_STAGE_ROW + s * 16) = v;
+    for (int s0 = 0; s0 < B; s0 += H8_STAGE_SLOTS) {
+      const int ns = min(H8_STAGE_SLOTS, B - s0);
+      for (int idx = threadIdx.x; idx < H8_TS * H8_STAGE_SLOTS; idx += blockDim.x) {
+        const int fl = idx & (H8_TS - 1), sl = idx >> 4;
+        if (sl < ns) {
+          const uint2 gh = *reinterpret_cast<const uint2 *>(hist + 2 * ((s0 + sl) * H8_TS + fl));
+          longlong2 v;
+          v.x = (long long)(int32_t)gh.x;
+          v.y = (long long)(int32_t)gh.y;
+          *reinterpret_cast<longlong2 *>(stage + fl * H8_STAGE_ROW + sl * 16) = v;
+        }
       }
       fence_proxy_async_smem();
       __syncthreads();
       if (threadIdx.x == 0) {
-        const uint32_t bytes = (uint32_t)B * 16u;
-        for (int k = 0; k < 16; ++k) {
-          const int f = f_first + k;
+        const uint32_t bytes = (uint32_t)ns * 16u;
+        for (int k = 0; k < H8_TS; ++k) {
+          const int f = f0 + k;
           if (f >= P.n_features) break;
-          int64_t *dst = node_out + (int64_t)f * B * 2;
+          int64_t *dst = node_out + ((int64_t)f * B + s0) * 2;
           if (it.multi) bulk_reduce_add_u64(dst, stage + k * H8_STAGE_ROW, bytes);
           else bulk_store(dst, stage + k * H8_STAGE_ROW, bytes);
         }
