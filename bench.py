@@ -1,11 +1,13 @@
 #!/usr/bin/env python
 """Benchmark of the level histogram path: binned entries per second per level on GB300.
 
-One step = one tree level of the workload: gbt_build_level over the smaller
-siblings (level prologue + histogram kernel) and gbt_subtract_and_find (sibling
-subtraction + split find for both siblings of every pair). Inputs are resident
-in HBM when the timed region starts; L2 is flushed (a write larger than L2)
-before every step, outside the step's CUDA events.
+One step = one tree level of the workload through gbt_level_step: the
+histograms of the smaller siblings (level plan + histogram kernel), sibling
+subtraction and split find for both siblings of every pair (level-finish
+kernel). ``--path unfused`` times gbt_build_level + gbt_subtract_and_find
+instead. Inputs are resident in HBM when the timed region starts; L2 is
+flushed (a write larger than L2) before every step, outside the step's CUDA
+events.
 
 Prints one JSON line (rank 0). ``--impl reference`` times the serial CPU oracle
 on the same workload instead (rank 0 only).
@@ -143,9 +145,11 @@ def entries_and_bytes(w, lv, B):
         R = int(lv.built_offsets[-1])
         n_b = n_p = len(lv.small)
     entries = R * F
-    hist_bytes = n_b * F * B * 16
-    kernel_bytes = R * F * wb + R * 12 + hist_bytes
-    level_bytes = kernel_bytes + 3 * n_p * F * B * 16
+    # histogram kernel: read the bins and (row id, qg, qh) of every built row, write each
+    # built node's exact 32-bit partial (the least it can hand on)
+    kernel_bytes = R * F * wb + R * 12 + n_b * F * B * 8
+    # whole level (fused path): bins + row ids/gradients, read parents, write small and large
+    level_bytes = R * F * wb + R * 12 + 3 * n_p * F * B * 16 if n_p else R * F * wb + R * 8 + n_b * F * B * 16
     return entries, R, n_b, n_p, kernel_bytes, level_bytes
 
 
@@ -267,8 +271,11 @@ def run_gpu(args, rank, world, local_rank):
 
         def step():
             if lv.depth > 0:
-                sess.check(g.gbt_build_level(ctx, rows_d, offs_d, n_b, hs))
-                sess.check(g.gbt_subtract_and_find(ctx, hp, None, hs, large, n_p, prm, so, lo))
+                if args.path == "fused":
+                    sess.check(g.gbt_level_step(ctx, rows_d, offs_d, n_p, hp, None, hs, large, prm, so, lo))
+                else:
+                    sess.check(g.gbt_build_level(ctx, rows_d, offs_d, n_b, hs))
+                    sess.check(g.gbt_subtract_and_find(ctx, hp, None, hs, large, n_p, prm, so, lo))
             else:
                 sess.check(g.gbt_build_level(ctx, None, offs_d, 1, hs))
                 sess.check(g.gbt_find_splits(ctx, hs, 1, prm, so))
@@ -282,7 +289,7 @@ def run_gpu(args, rank, world, local_rank):
         assert sess.sync() == 0
         barrier()
 
-        kernel_names = [hist_kernel, "k_level_prologue", "k_subtract_find", "k_reduce_splits", "k_find"]
+        kernel_names = [hist_kernel, "k_level_plan", "k_subtract_find", "k_level_finish", "k_finalize", "k_find"]
 
         def timed_pass(profile, flush_l2=True):
             """K steps, each bracketed by CUDA events on the launching stream (flush outside the events)."""
@@ -331,8 +338,7 @@ def run_gpu(args, rank, world, local_rank):
             d2h = 2 * n_p * g.SPLIT_BYTES
 
             def step_e2e():
-                sess.check(g.gbt_build_level(ctx, rows_h, offs_h, n_b, hs))
-                sess.check(g.gbt_subtract_and_find(ctx, hp, None, hs, large, n_p, prm, so_h, lo_h))
+                sess.check(g.gbt_level_step(ctx, rows_h, offs_h, n_p, hp, None, hs, large, prm, so_h, lo_h))
         else:
             gp_h = torch.from_numpy(w.gpair).pin_memory()
             offs_h = torch.from_numpy(lv.offsets).pin_memory()
@@ -390,6 +396,7 @@ def run_gpu(args, rank, world, local_rank):
         "config": {"workload": WORKLOAD_TEXT[args.workload], "rows_built": R, "features": w.n_features,
                    "bin_bytes": w.width, "slots_per_feature": B, "nodes_built": n_b, "nodes_derived": n_p,
                    "entries_per_step": entries, "l2": f"flushed before every step ({2 * l2 >> 20} MiB write)",
+                   "path": "gbt_level_step" if args.path == "fused" else "gbt_build_level + gbt_subtract_and_find",
                    "parallelism": f"replicas{world}"},
         "roofline": {"bound": "hbm", "kernel": hist_kernel, "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": (achieved / peak) if achieved else None, "traffic": traffic,
@@ -441,6 +448,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOAD_TEXT), default="level5")
+    ap.add_argument("--path", choices=["fused", "unfused"], default="fused")
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle time for cpu_baseline")
     ap.add_argument("--ref-budget", type=float, default=90.0, help="seconds of oracle time for --impl reference")
     args = ap.parse_args()

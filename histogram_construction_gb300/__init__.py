@@ -25,6 +25,7 @@ STATUS_NAMES = {
 EXPORTS = [
     "gbt_create", "gbt_destroy", "gbt_last_error", "gbt_sync", "gbt_upload_bins", "gbt_begin_tree",
     "gbt_suggest_scales", "gbt_build_level", "gbt_subtract_siblings", "gbt_find_splits", "gbt_subtract_and_find",
+    "gbt_level_step",
     "gbt_partition_level", "gbt_profile_enable", "gbt_profile_read", "gbt_slots_per_feature",
     "gbt_kernel_launches",
 ]
@@ -77,6 +78,7 @@ def lib(build_if_missing: bool = True):
         "gbt_subtract_siblings": (st, [vp, vp, vp, vp, vp, i32]),
         "gbt_find_splits": (st, [vp, vp, i32, ctypes.POINTER(GbtParams), vp]),
         "gbt_subtract_and_find": (st, [vp, vp, vp, vp, vp, i32, ctypes.POINTER(GbtParams), vp, vp]),
+        "gbt_level_step": (st, [vp, vp, vp, i32, vp, vp, vp, vp, ctypes.POINTER(GbtParams), vp, vp]),
         "gbt_partition_level": (st, [vp, vp, vp, i32, vp, vp, vp]),
         "gbt_profile_enable": (st, [vp, ctypes.c_int]),
         "gbt_profile_read": (st, [vp, ctypes.c_char_p, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(i64)]),
@@ -176,6 +178,12 @@ def gbt_find_splits(ctx, hist, n_nodes, prm, out):
 def gbt_subtract_and_find(ctx, parent_hist, parent_of, small_hist, large_hist, n_pairs, prm, small_out, large_out):
     return lib().gbt_subtract_and_find(ctx, ptr(parent_hist), ptr(parent_of), ptr(small_hist), ptr(large_hist),
                                        int(n_pairs), ctypes.byref(prm), ptr(small_out), ptr(large_out))
+
+
+def gbt_level_step(ctx, rows, node_offsets, n_pairs, parent_hist, parent_of, small_hist, large_hist, prm, small_out,
+                   large_out):
+    return lib().gbt_level_step(ctx, ptr(rows), ptr(node_offsets), int(n_pairs), ptr(parent_hist), ptr(parent_of),
+                                ptr(small_hist), ptr(large_hist), ctypes.byref(prm), ptr(small_out), ptr(large_out))
 
 
 def gbt_partition_level(ctx, rows, node_offsets, n_nodes, splits, out_rows, out_offsets):

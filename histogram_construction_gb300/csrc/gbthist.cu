@@ -8,6 +8,7 @@
 #include <string.h>
 
 #include <algorithm>
+#include <initializer_list>
 #include <map>
 #include <string>
 #include <vector>
@@ -81,16 +82,18 @@ struct gbt_ctx {
   float sg = 1.f, sh = 1.f;
   double inv_sg = 1.0, inv_sh = 1.0;
   Buf q;
+  uint32_t qmax = 0;             // max |q| of the current tree, known on the host after ev_q
+  bool qmax_known = false;
+  cudaEvent_t ev_q = nullptr;
   // state + scratch
   DevState *st = nullptr;
-  uint32_t *err_host = nullptr;  // pinned
-  Buf rec, chunk_prefix, rows_in, offs_in, cand, splits_a, splits_b, parent_of_in, tile_counts, lrank, slab,
-      counters;
+  uint32_t *err_host = nullptr;  // pinned: [0] error word copy, [1] max |q| copy
+  Buf gp_stage, chunk_prefix, partial, rows_in, offs_in, cand, splits_a, splits_b, parent_of_in, tile_counts, lrank,
+      slab, counters;
   std::string last_error;
   int64_t launches = 0;
-  // tuning (defaults; GBT_TARGET_ITEMS / GBT_U8_CTAS_PER_SM override them for sweeps)
+  // tuning: work items the level plan aims for (default 2 per SM; GBT_TARGET_ITEMS overrides it for sweeps)
   int target_items = 0;
-  int u8_ctas_per_sm = 4;
   // diagnostics: per-launch event pairs
   bool prof = false;
   struct ProfRec {
@@ -293,7 +296,6 @@ gbt_status gbt_create(int device, void *cuda_stream, gbt_ctx **out) {
   cudaDeviceGetAttribute(&c->n_sm, cudaDevAttrMultiProcessorCount, device);
   cudaDeviceGetAttribute(&c->smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device);
   if (const char *e = getenv("GBT_TARGET_ITEMS")) c->target_items = std::max(0, atoi(e));
-  if (const char *e = getenv("GBT_U8_CTAS_PER_SM")) c->u8_ctas_per_sm = std::min(4, std::max(1, atoi(e)));
   void *st = nullptr;
   e = dev_alloc(&st, sizeof(DevState), c->stream);
   if (e != cudaSuccess) {
@@ -302,20 +304,29 @@ gbt_status gbt_create(int device, void *cuda_stream, gbt_ctx **out) {
   }
   c->st = reinterpret_cast<DevState *>(st);
   cudaMemsetAsync(c->st, 0, sizeof(DevState), c->stream);
-  if (alloc_should_fail() || cudaMallocHost(&c->err_host, sizeof(uint32_t)) != cudaSuccess) {
+  if (alloc_should_fail() || cudaMallocHost(&c->err_host, 2 * sizeof(uint32_t)) != cudaSuccess) {
     cudaFreeAsync(c->st, c->stream);
     cudaStreamSynchronize(c->stream);
     delete c;
     return GBT_ERR_OOM;
   }
-  *c->err_host = 0;
+  c->err_host[0] = c->err_host[1] = 0;
+  if (cudaEventCreateWithFlags(&c->ev_q, cudaEventDisableTiming) != cudaSuccess) {
+    cudaFreeHost(c->err_host);
+    cudaFreeAsync(c->st, c->stream);
+    cudaStreamSynchronize(c->stream);
+    delete c;
+    return GBT_ERR_CUDA;
+  }
   if (cudaFuncSetAttribute(k_hist_u8, cudaFuncAttributeMaxDynamicSharedMemorySize, H8_SMEM) != cudaSuccess ||
+      cudaFuncSetAttribute(k_hist_u8, cudaFuncAttributePreferredSharedMemoryCarveout, 100) != cudaSuccess ||
       cudaFuncSetAttribute(k_hist_u16<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, H16_HIST_MAX + H16_STAGE_BYTES + 128) != cudaSuccess ||
       cudaFuncSetAttribute(k_hist_u16<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, H16_HIST_MAX + H16_STAGE_BYTES + 128) != cudaSuccess ||
       cudaFuncSetAttribute(k_hist_u16<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, H16_HIST_MAX + H16_STAGE_BYTES + 128) != cudaSuccess ||
       cudaFuncSetAttribute(k_hist_u16<16>, cudaFuncAttributeMaxDynamicSharedMemorySize, H16_HIST_MAX + H16_STAGE_BYTES + 128) != cudaSuccess ||
       cudaFuncSetAttribute(k_hist_u16<32>, cudaFuncAttributeMaxDynamicSharedMemorySize, H16_HIST_MAX + H16_STAGE_BYTES + 128) != cudaSuccess) {
     cudaGetLastError();
+    cudaEventDestroy(c->ev_q);
     cudaFreeHost(c->err_host);
     cudaFreeAsync(c->st, c->stream);
     cudaStreamSynchronize(c->stream);
@@ -330,13 +341,14 @@ gbt_status gbt_destroy(gbt_ctx *c) {
   if (!c) return GBT_OK;
   cudaSetDevice(c->device);
   cudaStreamSynchronize(c->stream);
-  Buf *bufs[] = {&c->mirror, &c->q, &c->rec, &c->chunk_prefix, &c->rows_in, &c->offs_in, &c->cand,
-                 &c->splits_a, &c->splits_b, &c->parent_of_in, &c->tile_counts, &c->lrank, &c->slab,
+  Buf *bufs[] = {&c->mirror, &c->q, &c->gp_stage, &c->chunk_prefix, &c->partial, &c->rows_in, &c->offs_in,
+                 &c->cand, &c->splits_a, &c->splits_b, &c->parent_of_in, &c->tile_counts, &c->lrank, &c->slab,
                  &c->counters};
   for (Buf *b : bufs) release(c, *b);
   if (c->st) cudaFreeAsync(c->st, c->stream);
   cudaStreamSynchronize(c->stream);
   if (c->err_host) cudaFreeHost(c->err_host);
+  if (c->ev_q) cudaEventDestroy(c->ev_q);
   for (auto &r : c->prof_pending) {
     cudaEventDestroy(r.a);
     cudaEventDestroy(r.b);
@@ -386,9 +398,6 @@ gbt_status gbt_upload_bins(gbt_ctx *c, const void *bins, int bin_bytes, int64_t 
   const int n_tiles = (n_features + tf - 1) / tf;
   const size_t mbytes = (size_t)n_tiles * (size_t)n_rows * MIRROR_STRIP_BYTES;
   s = ensure(c, c->mirror, mbytes, "mirror allocation");
-  if (s != GBT_OK) return s;
-  // per-dataset scratch sized by n_rows
-  s = ensure(c, c->rec, (size_t)n_rows * sizeof(int4), "level record scratch");
   if (s != GBT_OK) return s;
   c->bin_bytes = bin_bytes;
   c->n_rows = n_rows;
@@ -449,8 +458,7 @@ gbt_status gbt_begin_tree(gbt_ctx *c, const float *gpair, float scale_g, float s
   s = ensure(c, c->q, (size_t)c->n_rows * sizeof(int2), "quantised gpair");
   if (s != GBT_OK) return s;
   const void *gp = nullptr;
-  Buf &stage = c->rec;  // rec has n_rows * 16 >= n_rows * 8 bytes and is free between levels
-  s = device_view(c, gpair, (size_t)c->n_rows * 2 * sizeof(float), stage, &gp, "gpair");
+  s = device_view(c, gpair, (size_t)c->n_rows * 2 * sizeof(float), c->gp_stage, &gp, "gpair");
   if (s != GBT_OK) return s;
   if (!aligned16(gp) && ((reinterpret_cast<uintptr_t>(gp) & 7u) != 0))
     return fail(c, GBT_ERR_INVALID_ARG, "gpair must be 8-byte aligned");
@@ -459,6 +467,11 @@ gbt_status gbt_begin_tree(gbt_ctx *c, const float *gpair, float scale_g, float s
   prof_begin(c);
   k_quantise<<<grid, 1024, 0, c->stream>>>((const float2 *)gp, c->n_rows, scale_g, scale_h, (int2 *)c->q.p, c->st);
   LAUNCH_CHECK(c, "k_quantise");
+  // bring max|q| home asynchronously: the build sizes its partial scratch from it
+  CUDA_TRY(c, cudaMemcpyAsync(&c->err_host[1], &c->st->qmax, sizeof(uint32_t), cudaMemcpyDeviceToHost, c->stream),
+           "read max|q|");
+  CUDA_TRY(c, cudaEventRecord(c->ev_q, c->stream), "record max|q| event");
+  c->qmax_known = false;
   c->sg = scale_g;
   c->sh = scale_h;
   c->inv_sg = 1.0 / (double)scale_g;
@@ -472,6 +485,7 @@ gbt_status gbt_suggest_scales(int64_t rows_per_partial, float max_abs_g, float m
   if (!(max_abs_g >= 0.f) || !(max_abs_h >= 0.f) || !isfinite(max_abs_g) || !isfinite(max_abs_h))
     return GBT_ERR_INVALID_ARG;
   if (rows_per_partial <= 0) rows_per_partial = 65536;
+  rows_per_partial = std::max<int64_t>(rows_per_partial, 1024);
   const double lim = 2147483647.0 / (double)rows_per_partial;  // max |q| per row
   auto pick = [&](float m) -> float {
     if (m == 0.f) return 1.f;
@@ -487,18 +501,15 @@ gbt_status gbt_suggest_scales(int64_t rows_per_partial, float max_abs_g, float m
   return GBT_OK;
 }
 
-gbt_status gbt_build_level(gbt_ctx *c, const int32_t *rows, const int64_t *node_offsets, int32_t n_nodes,
-                           int64_t *hist_out) {
-  gbt_status s = check_ctx(c);
-  if (s != GBT_OK) return s;
-  if (!c->tree_ready) return fail(c, GBT_ERR_STATE, "gbt_begin_tree first");
-  if (n_nodes < 0 || n_nodes > 65535) return fail(c, GBT_ERR_UNSUPPORTED, "n_nodes must be in [0, 65535]");
-  if (!node_offsets || !hist_out) return fail(c, GBT_ERR_INVALID_ARG, "node_offsets and hist_out are required");
-  if (ptr_kind(hist_out) != 1 || !aligned16(hist_out))
-    return fail(c, GBT_ERR_INVALID_ARG, "hist_out must be 16-byte aligned device memory");
-  if (n_nodes == 0) return GBT_OK;
+}  // extern "C"
+
+namespace {
+
+// Validate the level inputs, plan the work items on the device and run the
+// histogram kernel, which leaves exact int32 partials per item in c->partial.
+gbt_status run_level_build(gbt_ctx *c, const int32_t *rows, const int64_t *node_offsets, int32_t n_nodes,
+                           LevelParams *out_lp) {
   const int B = c->n_bins + 1;
-  // node offsets: host offsets are validated here and tell the row count
   const void *offs_d = nullptr;
   int64_t R_host = -1;
   if (ptr_kind(node_offsets) == 0) {
@@ -508,15 +519,15 @@ gbt_status gbt_build_level(gbt_ctx *c, const int32_t *rows, const int64_t *node_
     R_host = node_offsets[n_nodes];
     if (R_host > c->n_rows) return fail(c, GBT_ERR_INVALID_ARG, "more level rows than dataset rows");
   }
-  s = device_view(c, node_offsets, (size_t)(n_nodes + 1) * sizeof(int64_t), c->offs_in, &offs_d, "node_offsets");
+  gbt_status s =
+      device_view(c, node_offsets, (size_t)(n_nodes + 1) * sizeof(int64_t), c->offs_in, &offs_d, "node_offsets");
   if (s != GBT_OK) return s;
   const void *rows_d = nullptr;
   if (rows) {
     const int k = ptr_kind(rows);
     if (k == 0 && R_host < 0) return fail(c, GBT_ERR_INVALID_ARG, "host rows need host node_offsets");
-    const size_t rb = (size_t)(k == 0 ? R_host : 0) * sizeof(int32_t);
     if (k == 0) {
-      s = device_view(c, rows, rb, c->rows_in, &rows_d, "rows");
+      s = device_view(c, rows, (size_t)R_host * sizeof(int32_t), c->rows_in, &rows_d, "rows");
       if (s != GBT_OK) return s;
     } else {
       rows_d = rows;
@@ -524,34 +535,42 @@ gbt_status gbt_build_level(gbt_ctx *c, const int32_t *rows, const int64_t *node_
   }
   s = ensure(c, c->chunk_prefix, (size_t)(n_nodes + 1) * sizeof(int32_t), "chunk prefix");
   if (s != GBT_OK) return s;
+  if (!c->qmax_known) {
+    CUDA_TRY(c, cudaEventSynchronize(c->ev_q), "wait for max|q|");
+    c->qmax = c->err_host[1];
+    c->qmax_known = true;
+  }
 
   LevelParams lp;
   lp.rows = (const int32_t *)rows_d;
   lp.offs = (const int64_t *)offs_d;
   lp.n_nodes = n_nodes;
-  // persistent grids: 4 CTAs per SM (u8, 49 KB shared each), 1 per SM (u16)
-  const int hist_ctas = c->bin_bytes == 1 ? c->n_sm * c->u8_ctas_per_sm : c->n_sm;
-  if (c->bin_bytes == 1) {
-    lp.n_fgroups = (c->n_features + H8_TS - 1) / H8_TS;
-  } else {
-    lp.n_fgroups = (c->n_features + c->ts16 - 1) / c->ts16;
-  }
+  lp.item_feats = c->bin_bytes == 1 ? 64 : c->ts16;
+  lp.n_fgroups = (c->n_features + lp.item_feats - 1) / lp.item_feats;
   lp.target_items = c->target_items > 0 ? c->target_items : c->n_sm * 2;
-  lp.pad = 0;
   lp.n_rows = c->n_rows;
   lp.q = (const int2 *)c->q.p;
-  lp.rec = (int4 *)c->rec.p;
   lp.chunk_prefix = (int32_t *)c->chunk_prefix.p;
-  lp.hist_out = hist_out;
-  lp.node_int64s = (int64_t)c->n_features * B * 2;
+  lp.sbw = c->bin_bytes == 1 ? 16 : c->ts16;
+  lp.nsb = c->bin_bytes == 1 ? H8_SB : 1;
   lp.st = c->st;
-  {
-    const int64_t work = R_host >= 0 ? R_host : c->n_rows;
-    const int grid = grid_for(c, std::max<int64_t>(work, 1) / 4 + 1, 512, 1);
-    prof_begin(c);
-    k_level_prologue<<<grid, 512, 0, c->stream>>>(lp);
-    LAUNCH_CHECK(c, "k_level_prologue");
-  }
+  // partial scratch for the largest item count the device plan can produce:
+  // items <= n_fgroups * n_nodes + max(target_items, n_fgroups * n_rows / rows_per_chunk_min)
+  const int64_t rc = 2147483647LL / std::max<int64_t>(c->qmax, 1);
+  const int64_t chunk_floor = std::max<int64_t>(1, std::min<int64_t>(rc, CHUNK_MIN_ROWS));
+  const int64_t items_max = (int64_t)lp.n_fgroups * n_nodes +
+                            std::max<int64_t>(lp.target_items, (int64_t)lp.n_fgroups *
+                                                                   ((c->n_rows + chunk_floor - 1) / chunk_floor)) +
+                            lp.n_fgroups;
+  if (items_max > INT32_MAX / 2) return fail(c, GBT_ERR_UNSUPPORTED, "level too large for the work-item plan");
+  s = ensure(c, c->partial, (size_t)items_max * lp.nsb * lp.sbw * B * 8, "level partial scratch");
+  if (s != GBT_OK) return s;
+  lp.partial = (int32_t *)c->partial.p;
+
+  prof_begin(c);
+  k_level_plan<<<1, 1024, 0, c->stream>>>(lp);
+  LAUNCH_CHECK(c, "k_level_plan");
+  const int hist_ctas = c->n_sm;  // persistent: one resident CTA per SM
   if (c->bin_bytes == 1) {
     Hist8Params hp;
     hp.lv = lp;
@@ -581,6 +600,42 @@ gbt_status gbt_build_level(gbt_ctx *c, const int32_t *rows, const int64_t *node_
     }
     LAUNCH_CHECK(c, "k_hist_u16");
   }
+  *out_lp = lp;
+  return GBT_OK;
+}
+
+PartialView partial_view(const LevelParams &lp, int B) {
+  PartialView v;
+  v.partial = lp.partial;
+  v.chunk_prefix = lp.chunk_prefix;
+  v.n_fgroups = lp.n_fgroups;
+  v.sbw = lp.sbw;
+  v.nsb = lp.nsb;
+  v.B = B;
+  return v;
+}
+
+}  // namespace
+
+extern "C" {
+
+gbt_status gbt_build_level(gbt_ctx *c, const int32_t *rows, const int64_t *node_offsets, int32_t n_nodes,
+                           int64_t *hist_out) {
+  gbt_status s = check_ctx(c);
+  if (s != GBT_OK) return s;
+  if (!c->tree_ready) return fail(c, GBT_ERR_STATE, "gbt_begin_tree first");
+  if (n_nodes < 0 || n_nodes > 65535) return fail(c, GBT_ERR_UNSUPPORTED, "n_nodes must be in [0, 65535]");
+  if (!node_offsets || !hist_out) return fail(c, GBT_ERR_INVALID_ARG, "node_offsets and hist_out are required");
+  if (ptr_kind(hist_out) != 1 || !aligned16(hist_out))
+    return fail(c, GBT_ERR_INVALID_ARG, "hist_out must be 16-byte aligned device memory");
+  if (n_nodes == 0) return GBT_OK;
+  LevelParams lp;
+  s = run_level_build(c, rows, node_offsets, n_nodes, &lp);
+  if (s != GBT_OK) return s;
+  prof_begin(c);
+  k_finalize<<<dim3((c->n_features + 7) / 8, n_nodes), 256, 0, c->stream>>>(
+      partial_view(lp, c->n_bins + 1), c->n_features, lp.item_feats, hist_out, c->st);
+  LAUNCH_CHECK(c, "k_finalize");
   return GBT_OK;
 }
 
@@ -656,19 +711,18 @@ gbt_status gbt_find_splits(gbt_ctx *c, const int64_t *hist, int32_t n_nodes, con
   return GBT_OK;
 }
 
-gbt_status gbt_subtract_and_find(gbt_ctx *c, const int64_t *parent_hist, const int32_t *parent_of,
-                                 const int64_t *small_hist, int64_t *large_hist, int32_t n_pairs,
-                                 const gbt_params *params, gbt_split *small_out, gbt_split *large_out) {
-  gbt_status s = check_ctx(c);
-  if (s != GBT_OK) return s;
-  if (!c->tree_ready) return fail(c, GBT_ERR_STATE, "gbt_begin_tree first (scales)");
-  if (!params || n_pairs < 0) return fail(c, GBT_ERR_INVALID_ARG, "params NULL or n_pairs < 0");
-  if (n_pairs == 0) return GBT_OK;
-  if (n_pairs > 32767) return fail(c, GBT_ERR_UNSUPPORTED, "n_pairs must be <= 32767");
-  for (const void *p : {(const void *)parent_hist, (const void *)small_hist, (const void *)large_hist})
-    if (ptr_kind(p) != 1 || !aligned16(p)) return fail(c, GBT_ERR_INVALID_ARG, "histograms must be 16-byte aligned device memory");
+}  // extern "C"
+
+namespace {
+
+// Shared tail of gbt_subtract_and_find and gbt_level_step: one launch of the
+// level-finish kernel (small strip from `src`, subtraction, split find).
+template <bool FROM_PARTIALS>
+gbt_status run_level_finish(gbt_ctx *c, const SmallSource &src, const int64_t *parent_hist, const int32_t *parent_of,
+                            int64_t *large_hist, int32_t n_pairs, const gbt_params *params, gbt_split *small_out,
+                            gbt_split *large_out) {
   const int32_t *po = nullptr;
-  s = parent_of_view(c, parent_of, n_pairs, &po);
+  gbt_status s = parent_of_view(c, parent_of, n_pairs, &po);
   if (s != GBT_OK) return s;
   SplitOut *da = nullptr, *db = nullptr;
   bool ha = false, hb = false;
@@ -676,17 +730,17 @@ gbt_status gbt_subtract_and_find(gbt_ctx *c, const int64_t *parent_hist, const i
   if (s != GBT_OK) return s;
   s = split_out_view(c, large_out, n_pairs, c->splits_b, &db, &hb);
   if (s != GBT_OK) return s;
-  const int nfb = (c->n_features + SCAN_WARPS / 2 - 1) / (SCAN_WARPS / 2);
+  const int nfb = (c->n_features + 3) / 4;
   s = ensure(c, c->cand, (size_t)2 * n_pairs * nfb * sizeof(Cand), "candidates");
   if (s != GBT_OK) return s;
   s = ensure_counters(c, (size_t)n_pairs);
   if (s != GBT_OK) return s;
   const SplitParams sp = make_sp(c, params);
   prof_begin(c);
-  k_subtract_find<<<dim3(nfb, n_pairs), SCAN_THREADS, 0, c->stream>>>(
-      parent_hist, po, small_hist, large_hist, c->n_features, c->n_bins, sp, (Cand *)c->cand.p,
-      (uint32_t *)c->counters.p, da, db, c->st);
-  LAUNCH_CHECK(c, "k_subtract_find");
+  k_level_finish<FROM_PARTIALS><<<dim3(nfb, n_pairs), SCAN_THREADS, 0, c->stream>>>(
+      src, parent_hist, po, large_hist, c->n_features, c->n_bins, sp, (Cand *)c->cand.p, (uint32_t *)c->counters.p,
+      da, db, c->st);
+  LAUNCH_CHECK(c, FROM_PARTIALS ? "k_level_finish" : "k_subtract_find");
   if (ha)
     CUDA_TRY(c, cudaMemcpyAsync(small_out, da, (size_t)n_pairs * sizeof(gbt_split), cudaMemcpyDeviceToHost, c->stream),
              "splits to host");
@@ -694,6 +748,54 @@ gbt_status gbt_subtract_and_find(gbt_ctx *c, const int64_t *parent_hist, const i
     CUDA_TRY(c, cudaMemcpyAsync(large_out, db, (size_t)n_pairs * sizeof(gbt_split), cudaMemcpyDeviceToHost, c->stream),
              "splits to host");
   return GBT_OK;
+}
+
+gbt_status check_pair_args(gbt_ctx *c, const gbt_params *params, int32_t n_pairs,
+                           std::initializer_list<const void *> hists) {
+  if (!c->tree_ready) return fail(c, GBT_ERR_STATE, "gbt_begin_tree first (scales)");
+  if (!params || n_pairs < 0) return fail(c, GBT_ERR_INVALID_ARG, "params NULL or n_pairs < 0");
+  if (n_pairs > 32767) return fail(c, GBT_ERR_UNSUPPORTED, "n_pairs must be <= 32767");
+  for (const void *p : hists)
+    if (ptr_kind(p) != 1 || !aligned16(p))
+      return fail(c, GBT_ERR_INVALID_ARG, "histograms must be 16-byte aligned device memory");
+  return GBT_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+gbt_status gbt_subtract_and_find(gbt_ctx *c, const int64_t *parent_hist, const int32_t *parent_of,
+                                 const int64_t *small_hist, int64_t *large_hist, int32_t n_pairs,
+                                 const gbt_params *params, gbt_split *small_out, gbt_split *large_out) {
+  gbt_status s = check_ctx(c);
+  if (s != GBT_OK) return s;
+  if (n_pairs == 0 && params) return GBT_OK;
+  s = check_pair_args(c, params, n_pairs, {parent_hist, small_hist, large_hist});
+  if (s != GBT_OK) return s;
+  SmallSource src{};
+  src.hist = small_hist;
+  return run_level_finish<false>(c, src, parent_hist, parent_of, large_hist, n_pairs, params, small_out, large_out);
+}
+
+gbt_status gbt_level_step(gbt_ctx *c, const int32_t *rows, const int64_t *node_offsets, int32_t n_pairs,
+                          const int64_t *parent_hist, const int32_t *parent_of, int64_t *small_hist,
+                          int64_t *large_hist, const gbt_params *params, gbt_split *small_out,
+                          gbt_split *large_out) {
+  gbt_status s = check_ctx(c);
+  if (s != GBT_OK) return s;
+  if (!node_offsets) return fail(c, GBT_ERR_INVALID_ARG, "node_offsets is required");
+  if (n_pairs == 0 && params) return GBT_OK;
+  s = check_pair_args(c, params, n_pairs, {parent_hist, small_hist, large_hist});
+  if (s != GBT_OK) return s;
+  LevelParams lp;
+  s = run_level_build(c, rows, node_offsets, n_pairs, &lp);
+  if (s != GBT_OK) return s;
+  SmallSource src{};
+  src.view = partial_view(lp, c->n_bins + 1);
+  src.item_feats = lp.item_feats;
+  src.hist_out = small_hist;
+  return run_level_finish<true>(c, src, parent_hist, parent_of, large_hist, n_pairs, params, small_out, large_out);
 }
 
 gbt_status gbt_partition_level(gbt_ctx *c, const int32_t *rows, const int64_t *node_offsets, int32_t n_nodes,

@@ -1,5 +1,6 @@
-// Level-batched histogram build: level prologue (plan, gather, zero) and the
-// persistent shared-memory histogram kernels.
+// Level-batched histogram build: level plan, the persistent shared-memory
+// histogram kernels (exact int32 partials per work item) and the finalize
+// kernel that adds the partials of each node into its int64 histogram.
 //
 // What is computed [bonsai "10: CUDA histogram backend", "Level batching" and
 // "The kernel"; "GBDT engine engineering deep-dive" (ybb.press), section 1
@@ -8,156 +9,113 @@
 //   Hist[n][f][s] = sum over rows k of node n with slot(bins[f][row_k]) == s of (qg, qh).
 //
 // GB300 design (differs from the pages' (feature, node, row-chunk) grid with
-// float shared cells):
-//  * work items (node, 16-feature group, row chunk) handed out to a persistent
-//    grid of several CTAs per SM by an atomic counter;
-//  * a CTA holds a 16-feature x 256-slot histogram of int32 (G, H) pairs in
-//    shared memory (32 KB); each lane adds (qg, qh) with two 32-bit shared
-//    atomics, and lanes are assigned to (row, feature, component) so that the
-//    32 lanes of every atomic instruction hit 32 different banks whatever the
-//    bin values (no bank conflicts, no same-address conflicts);
+// float shared cells and double global atomics):
+//  * work items (node, 64-feature tile, row chunk) go to a persistent grid
+//    (one 1024-thread CTA per SM) through an atomic counter;
+//  * a CTA holds the tile's histogram as int32 (G, H) pairs in shared memory,
+//    in 16-feature sub-blocks of [256 slots][16 features]; each lane adds
+//    (qg, qh) with two 32-bit shared atomics, and lanes are assigned to
+//    (row, feature, component) so that the 32 lanes of every atomic
+//    instruction hit 32 different banks whatever the bin values;
 //  * a chunk never holds more rows than keep every int32 partial exact
-//    (rows * max|q| < 2^31), so the int64 result is exact;
-//  * the flush transposes the cells to int64 through a small padded staging
-//    buffer and writes each feature's slot range with one TMA bulk copy
-//    (node built by one item) or one bulk reduce-add into the zeroed output
-//    (node split into several chunks).
+//    (rows * max|q| < 2^31);
+//  * the item's shared image leaves as is with TMA bulk stores (no
+//    transposition, no zeroing of global memory, no global atomics); the
+//    images of a node's chunks are added in int64 afterwards (finalize
+//    kernel, or the fused subtract + split-find kernel).
 #pragma once
 
 #include "common.cuh"
 
 namespace gbt {
 
-constexpr int CHUNK_MIN_ROWS = 2048;
+constexpr int CHUNK_MIN_ROWS = 1024;
 
 struct LevelParams {
-  const int32_t *rows;   // level row list or nullptr (identity)
-  const int64_t *offs;   // [n_nodes + 1]
+  const int32_t *rows;    // level row list or nullptr (identity)
+  const int64_t *offs;    // [n_nodes + 1]
   int32_t n_nodes;
-  int32_t n_fgroups;     // feature groups per node chunk (work items per chunk)
-  int32_t target_items;  // load-balance target for the item count
-  int32_t pad;
+  int32_t n_fgroups;      // feature groups per node chunk (work items per chunk)
+  int32_t target_items;   // load-balance target for the item count
+  int32_t item_feats;     // features per work item (64 for u8, TS for u16)
   int64_t n_rows;
-  const int2 *q;         // quantised gpair [n_rows]
-  int4 *rec;             // gathered level records {row, qg, qh, 0} [n_rows]
-  int32_t *chunk_prefix; // [n_nodes + 1]
-  int64_t *hist_out;     // [n_nodes][F][B][2]
-  int64_t node_int64s;   // F * B * 2
+  const int2 *q;          // quantised gpair [n_rows]
+  int32_t *chunk_prefix;  // [n_nodes + 1]
+  int32_t *partial;       // raw shared-memory images of the items (see PartialView)
+  int32_t sbw;            // features per sub-block of the image (16 for u8, TS for u16)
+  int32_t nsb;            // sub-blocks per item image (4 for u8, 1 for u16)
   DevState *st;
 };
 
-__device__ __forceinline__ int64_t level_chunk_rows(const LevelParams &p) {
-  const int64_t R = p.offs[p.n_nodes] - p.offs[0];
-  const uint32_t qm = max(p.st->qmax, 1u);
-  const int64_t rc = 2147483647LL / (int64_t)qm;  // rows whose int32 partials cannot overflow
-  int64_t tgt = (max(R, (int64_t)0) * p.n_fgroups + p.target_items - 1) / max(p.target_items, 1);
-  tgt = max(tgt, (int64_t)CHUNK_MIN_ROWS);
-  return max((int64_t)1, min(rc, tgt));
-}
-
-// Level prologue: block 0 plans the work items; all blocks gather the level
-// records (row id and its quantised pair, in level order) and zero the
-// outputs of nodes that will be reduced from several chunks.
-__global__ void __launch_bounds__(512) k_level_prologue(LevelParams p) {
-  const int64_t chunk = level_chunk_rows(p);
-  const int64_t R = p.offs[p.n_nodes] - p.offs[0];
-  if (blockIdx.x == 0) {
-    __shared__ int32_t s_carry;
-    __shared__ int32_t s_bad;
-    __shared__ int32_t s_warp[32];
-    if (threadIdx.x == 0) {
-      s_carry = 0;
-      s_bad = (p.offs[0] != 0 || R > p.n_rows || R < 0) ? 1 : 0;
+// Level plan (one block): rows per chunk (load balance, capped by the int32
+// exactness bound), chunk counts per node and their prefix, item count.
+// Offsets that do not start at 0, descend or exceed n_rows invalidate the
+// plan (no items; GBT_ERR_ROW_RANGE).
+__global__ void __launch_bounds__(1024) k_level_plan(LevelParams p) {
+  __shared__ int32_t s_carry;
+  __shared__ int32_t s_bad;
+  __shared__ int32_t s_warp[32];
+  __shared__ long long s_chunk;
+  if (threadIdx.x == 0) {
+    const int64_t R = p.offs[p.n_nodes] - p.offs[0];
+    const uint32_t qm = max(p.st->qmax, 1u);
+    const int64_t rc = 2147483647LL / (int64_t)qm;  // rows whose int32 partials cannot overflow
+    int64_t tgt = (max(R, (int64_t)0) * p.n_fgroups + p.target_items - 1) / max(p.target_items, 1);
+    tgt = max(tgt, (int64_t)CHUNK_MIN_ROWS);
+    s_chunk = max((int64_t)1, min(rc, tgt));
+    s_carry = 0;
+    s_bad = (p.offs[0] != 0 || R > p.n_rows || R < 0) ? 1 : 0;
+  }
+  __syncthreads();
+  const int64_t chunk = s_chunk;
+  for (int base = 0; base < p.n_nodes; base += blockDim.x) {
+    const int n = base + threadIdx.x;
+    int32_t c = 0;
+    if (n < p.n_nodes) {
+      const int64_t a = p.offs[n], b = p.offs[n + 1];
+      if (b < a) s_bad = 1;
+      const int64_t rows_n = max(b - a, (int64_t)0);
+      c = (int32_t)max((int64_t)1, (rows_n + chunk - 1) / chunk);
+    }
+    int32_t v = c;
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    for (int o = 1; o < 32; o <<= 1) {
+      const int32_t y = __shfl_up_sync(0xffffffffu, v, o);
+      if (lane >= o) v += y;
+    }
+    if (lane == 31) s_warp[w] = v;
+    __syncthreads();
+    if (w == 0) {
+      int32_t x = lane < (int)(blockDim.x >> 5) ? s_warp[lane] : 0;
+      for (int o = 1; o < 32; o <<= 1) {
+        const int32_t y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+      }
+      s_warp[lane] = x;
     }
     __syncthreads();
-    for (int base = 0; base < p.n_nodes; base += blockDim.x) {
-      const int n = base + threadIdx.x;
-      int32_t c = 0;
-      if (n < p.n_nodes) {
-        const int64_t a = p.offs[n], b = p.offs[n + 1];
-        if (b < a) s_bad = 1;
-        const int64_t rows_n = max(b - a, (int64_t)0);
-        c = (int32_t)max((int64_t)1, (rows_n + chunk - 1) / chunk);
-      }
-      // block inclusive scan of c
-      int32_t v = c;
-      const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-      for (int o = 1; o < 32; o <<= 1) {
-        const int32_t y = __shfl_up_sync(0xffffffffu, v, o);
-        if (lane >= o) v += y;
-      }
-      if (lane == 31) s_warp[w] = v;
-      __syncthreads();
-      if (w == 0) {
-        int32_t x = lane < (int)(blockDim.x >> 5) ? s_warp[lane] : 0;
-        for (int o = 1; o < 32; o <<= 1) {
-          const int32_t y = __shfl_up_sync(0xffffffffu, x, o);
-          if (lane >= o) x += y;
-        }
-        s_warp[lane] = x;
-      }
-      __syncthreads();
-      const int32_t incl = v + (w > 0 ? s_warp[w - 1] : 0) + s_carry;
-      if (n < p.n_nodes) p.chunk_prefix[n + 1] = incl;
-      __syncthreads();
-      if (threadIdx.x == blockDim.x - 1) s_carry = incl;
-      __syncthreads();
-    }
-    if (threadIdx.x == 0) {
-      p.chunk_prefix[0] = 0;
-      const int ok = !s_bad;
-      p.st->plan_ok = ok;
-      p.st->chunk_rows = chunk;
-      p.st->n_items = ok ? s_carry * p.n_fgroups : 0;
-      p.st->work_next = 0;
-      if (!ok) raise_err(p.st, ERRBIT_ROW);
-    }
+    const int32_t incl = v + (w > 0 ? s_warp[w - 1] : 0) + s_carry;
+    if (n < p.n_nodes) p.chunk_prefix[n + 1] = incl;
+    __syncthreads();
+    if (threadIdx.x == blockDim.x - 1) s_carry = incl;
+    __syncthreads();
   }
-  // gather level records (bounded by n_rows whatever the offsets say)
-  const int64_t Rg = min(max(R, (int64_t)0), p.n_rows);
-  const int64_t nthr = (int64_t)gridDim.x * blockDim.x;
-  const int64_t gtid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (p.rows != nullptr) {
-    uint32_t bad = 0;
-    for (int64_t k0 = gtid; k0 < Rg; k0 += 4 * nthr) {
-      int32_t r[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int64_t k = k0 + u * nthr;
-        r[u] = k < Rg ? __ldg(p.rows + k) : -1;
-      }
-      int2 qq[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const bool ok = r[u] >= 0 && r[u] < p.n_rows;
-        qq[u] = ok ? __ldg(p.q + r[u]) : make_int2(0, 0);
-      }
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int64_t k = k0 + u * nthr;
-        if (k >= Rg) break;
-        const bool ok = r[u] >= 0 && r[u] < p.n_rows;
-        if (!ok) bad = 1;
-        p.rec[k] = ok ? make_int4(r[u], qq[u].x, qq[u].y, 0) : make_int4(-1, 0, 0, 0);
-      }
-    }
-    if (bad) raise_err(p.st, ERRBIT_ROW);
-  }
-  // zero the outputs of multi-chunk nodes (they are reduced into)
-  const int64_t units = p.node_int64s / 2;
-  for (int n = 0; n < p.n_nodes; ++n) {
-    const int64_t rows_n = __ldg(p.offs + n + 1) - __ldg(p.offs + n);
-    if (rows_n <= chunk) continue;
-    int4 *dst = reinterpret_cast<int4 *>(p.hist_out + (int64_t)n * p.node_int64s);
-    for (int64_t u = gtid; u < units; u += nthr) dst[u] = make_int4(0, 0, 0, 0);
+  if (threadIdx.x == 0) {
+    p.chunk_prefix[0] = 0;
+    const int ok = !s_bad;
+    p.st->plan_ok = ok;
+    p.st->chunk_rows = chunk;
+    p.st->n_items = ok ? s_carry * p.n_fgroups : 0;
+    p.st->work_next = 0;
+    if (!ok) raise_err(p.st, ERRBIT_ROW);
   }
 }
 
-// Decode a work item id into node, feature group and row range.
+// Decode a work item id (chunk-major, feature group fastest) into node,
+// feature group and row range.
 struct Item {
   int32_t node, fgroup;
   int64_t k0, k1;
-  int32_t multi;
 };
 
 __device__ __forceinline__ Item decode_item(int32_t id, const LevelParams &p, int64_t chunk) {
@@ -174,27 +132,43 @@ __device__ __forceinline__ Item decode_item(int32_t id, const LevelParams &p, in
   const int64_t a = p.offs[lo], b = p.offs[lo + 1];
   it.k0 = a + (int64_t)c * chunk;
   it.k1 = min(b, it.k0 + chunk);
-  it.multi = (p.chunk_prefix[lo + 1] - p.chunk_prefix[lo]) > 1;
   return it;
 }
 
+// Loads (row id, qg, qh) of level position k; row -1 marks an invalid row.
+__device__ __forceinline__ void load_row(const LevelParams &p, bool ident, int64_t k, int64_t k1, int32_t &r,
+                                         int32_t &vg, int32_t &vh, uint32_t &bad) {
+  r = -1;
+  vg = 0;
+  vh = 0;
+  if (k >= k1) return;
+  const int32_t rr = ident ? (int32_t)k : __ldg(p.rows + k);
+  if (rr < 0 || rr >= p.n_rows) {
+    bad = 1;
+    return;
+  }
+  const int2 qv = __ldg(p.q + rr);
+  r = rr;
+  vg = qv.x;
+  vh = qv.y;
+}
+
 // ----------------------------------------------------------------------------
-// u8 kernel: 16 features per item (one quarter of a 64-byte mirror strip).
+// u8 kernel: items of one 64-feature mirror tile, 16-feature sub-blocks.
 //
 // Lane l of a warp takes row rho = l/4 of an 8-row group and byte word
-// w = l%4 of the row's 16-byte quarter (one 32-bit load). In atomic
-// instruction (j, c) the lane adds byte jj = (j + rho/2) & 3 of its word,
-// i.e. feature f = 4w + jj, component (c ^ (rho & 1)) (0 = G, 1 = H). Cells
-// are [slot][16 features][G, H]; a slot row is 128 bytes = 32 banks, so the
-// bank of a lane is 2f + comp: distinct for the 32 lanes of every
-// instruction (f covers 16 values over (w, rho/2), comp separates rho&1).
-constexpr int H8_THREADS = 256;
-constexpr int H8_TS = 16;                                  // features per item
-constexpr int H8_HIST_BYTES = 256 * H8_TS * 8;             // 32 KB
-constexpr int H8_STAGE_SLOTS = 64;                         // slots per flush round
-constexpr int H8_STAGE_ROW = (H8_STAGE_SLOTS + 1) * 16;    // one feature's int64 pairs + pad
-constexpr int H8_SMEM = H8_HIST_BYTES + H8_TS * H8_STAGE_ROW;
-constexpr int H8_UNROLL = 8;
+// w = l%4 of each 16-byte quarter of the row's strip (one 32-bit load per
+// sub-block). In atomic instruction (sb, j, c) the lane adds byte
+// jj = (j + rho/2) & 3 of its word of quarter sb, i.e. feature f = 4w + jj of
+// sub-block sb, component (c ^ (rho & 1)) (0 = G, 1 = H). Cells are
+// [slot][16][G, H]: a slot row is 128 bytes = 32 banks, so the bank of a lane
+// is 2f + comp, distinct for the 32 lanes of every instruction.
+constexpr int H8_THREADS = 1024;
+constexpr int H8_SB = 4;                                   // sub-blocks per tile
+constexpr int H8_SB_BYTES = 256 * 16 * 8;                  // 32 KB
+constexpr int H8_HIST_BYTES = H8_SB * H8_SB_BYTES;         // 128 KB
+constexpr int H8_SMEM = H8_HIST_BYTES;
+constexpr int H8_UNROLL = 4;
 
 struct Hist8Params {
   LevelParams lv;
@@ -203,10 +177,9 @@ struct Hist8Params {
   int32_t n_slots;        // B
 };
 
-__global__ void __launch_bounds__(H8_THREADS, 4) k_hist_u8(Hist8Params P) {
+__global__ void __launch_bounds__(H8_THREADS, 1) k_hist_u8(Hist8Params P) {
   extern __shared__ __align__(128) unsigned char smem[];
   uint32_t *hist = reinterpret_cast<uint32_t *>(smem);
-  unsigned char *stage = smem + H8_HIST_BYTES;
   __shared__ int32_t s_item;
 
   const LevelParams &p = P.lv;
@@ -220,7 +193,6 @@ __global__ void __launch_bounds__(H8_THREADS, 4) k_hist_u8(Hist8Params P) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
   const int rho = lane >> 2, w = lane & 3;
   const int pr = rho >> 1, par = rho & 1;
-  // per-lane byte shift and column byte offset of instruction j
   uint32_t shift[4], colb[4];
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
@@ -230,6 +202,7 @@ __global__ void __launch_bounds__(H8_THREADS, 4) k_hist_u8(Hist8Params P) {
   }
   const uint32_t off0 = par ? 4u : 0u, off1 = par ? 0u : 4u;
   const uint32_t hist_base = smem_addr(hist);
+  uint32_t bad = 0;
 
   for (;;) {
     if (threadIdx.x == 0) s_item = (int32_t)atomicAdd(&p.st->work_next, 1u);
@@ -237,90 +210,62 @@ __global__ void __launch_bounds__(H8_THREADS, 4) k_hist_u8(Hist8Params P) {
     const int32_t id = s_item;
     if (id >= n_items) break;
     const Item it = decode_item(id, p, chunk);
+    const int f_tile0 = it.fgroup * 64;
+    const int nsb = min(H8_SB, (P.n_features - f_tile0 + 15) >> 4);
     {
       uint4 *h4 = reinterpret_cast<uint4 *>(hist);
-      const int n4 = B * H8_TS * 8 / 16;
+      const int n4 = nsb * (H8_SB_BYTES / 16);  // (rows beyond B are never read back)
       for (int i = threadIdx.x; i < n4; i += blockDim.x) h4[i] = make_uint4(0, 0, 0, 0);
     }
     __syncthreads();
-    const int tile = it.fgroup >> 2, sub = it.fgroup & 3;
-    const unsigned char *strip = P.mirror + (int64_t)tile * N * MIRROR_STRIP_BYTES + sub * 16 + w * 4;
+    const unsigned char *strip = P.mirror + (int64_t)it.fgroup * N * MIRROR_STRIP_BYTES + w * 4;
     const int64_t step = (int64_t)8 * nwarps;
     for (int64_t g0 = it.k0 + 8 * warp; g0 < it.k1; g0 += step * H8_UNROLL) {
       int32_t rr[H8_UNROLL], vg[H8_UNROLL], vh[H8_UNROLL];
 #pragma unroll
-      for (int u = 0; u < H8_UNROLL; ++u) {
-        const int64_t k = g0 + u * step + rho;
-        rr[u] = -1;
-        vg[u] = 0;
-        vh[u] = 0;
-        if (k < it.k1) {
-          if (ident) {
-            const int2 qv = __ldg(&p.q[k]);
-            rr[u] = (int32_t)k;
-            vg[u] = qv.x;
-            vh[u] = qv.y;
-          } else {
-            const int4 rc = __ldg(&p.rec[k]);
-            rr[u] = rc.x;
-            vg[u] = rc.y;
-            vh[u] = rc.z;
-          }
-        }
-      }
-      uint32_t bw[H8_UNROLL];
+      for (int u = 0; u < H8_UNROLL; ++u) load_row(p, ident, g0 + u * step + rho, it.k1, rr[u], vg[u], vh[u], bad);
+      uint32_t bw[H8_UNROLL][H8_SB];
 #pragma unroll
       for (int u = 0; u < H8_UNROLL; ++u)
-        bw[u] = rr[u] >= 0 ? __ldg(reinterpret_cast<const uint32_t *>(strip + (int64_t)rr[u] * MIRROR_STRIP_BYTES))
-                           : 0u;
+#pragma unroll
+        for (int sb = 0; sb < H8_SB; ++sb)
+          bw[u][sb] = (rr[u] >= 0 && sb < nsb)
+                          ? __ldg(reinterpret_cast<const uint32_t *>(strip + (int64_t)rr[u] * MIRROR_STRIP_BYTES +
+                                                                     sb * 16))
+                          : 0u;
 #pragma unroll
       for (int u = 0; u < H8_UNROLL; ++u) {
         if (rr[u] < 0) continue;
         const uint32_t v0 = par ? (uint32_t)vh[u] : (uint32_t)vg[u];
         const uint32_t v1 = par ? (uint32_t)vg[u] : (uint32_t)vh[u];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const uint32_t slot = (bw[u] >> shift[j]) & 0xffu;
-          const uint32_t a = hist_base + slot * (H8_TS * 8) + colb[j];
-          asm volatile("red.shared.add.u32 [%0], %1;" ::"r"(a + off0), "r"(v0) : "memory");
-          asm volatile("red.shared.add.u32 [%0], %1;" ::"r"(a + off1), "r"(v1) : "memory");
+        for (int sb = 0; sb < H8_SB; ++sb) {
+          if (sb >= nsb) break;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const uint32_t slot = (bw[u][sb] >> shift[j]) & 0xffu;
+            const uint32_t a = hist_base + sb * H8_SB_BYTES + slot * 128u + colb[j];
+            asm volatile("red.shared.add.u32 [%0], %1;" ::"r"(a + off0), "r"(v0) : "memory");
+            asm volatile("red.shared.add.u32 [%0], %1;" ::"r"(a + off1), "r"(v1) : "memory");
+          }
         }
       }
     }
     __syncthreads();
-    // flush: rounds of 64 slots; lanes over features for conflict-free reads,
-    // staging rows padded by 16 bytes for conflict-free 16-byte writes
-    const int f0 = it.fgroup * H8_TS;
-    int64_t *node_out = p.hist_out + (int64_t)it.node * p.node_int64s;
-    for (int s0 = 0; s0 < B; s0 += H8_STAGE_SLOTS) {
-      const int ns = min(H8_STAGE_SLOTS, B - s0);
-      for (int idx = threadIdx.x; idx < H8_TS * H8_STAGE_SLOTS; idx += blockDim.x) {
-        const int fl = idx & (H8_TS - 1), sl = idx >> 4;
-        if (sl < ns) {
-          const uint2 gh = *reinterpret_cast<const uint2 *>(hist + 2 * ((s0 + sl) * H8_TS + fl));
-          longlong2 v;
-          v.x = (long long)(int32_t)gh.x;
-          v.y = (long long)(int32_t)gh.y;
-          *reinterpret_cast<longlong2 *>(stage + fl * H8_STAGE_ROW + sl * 16) = v;
-        }
-      }
-      fence_proxy_async_smem();
-      __syncthreads();
-      if (threadIdx.x == 0) {
-        const uint32_t bytes = (uint32_t)ns * 16u;
-        for (int k = 0; k < H8_TS; ++k) {
-          const int f = f0 + k;
-          if (f >= P.n_features) break;
-          int64_t *dst = node_out + ((int64_t)f * B + s0) * 2;
-          if (it.multi) bulk_reduce_add_u64(dst, stage + k * H8_STAGE_ROW, bytes);
-          else bulk_store(dst, stage + k * H8_STAGE_ROW, bytes);
-        }
-        bulk_commit();
-        bulk_wait_read_all();
-      }
-      __syncthreads();
+    // flush: the item's shared image ([sub-block][slot][16][G, H] int32) leaves
+    // with one TMA bulk store per sub-block; no transposition, no staging
+    fence_proxy_async_smem();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      int32_t *item_out = p.partial + (int64_t)id * H8_SB * B * 16 * 2;
+      for (int sb = 0; sb < nsb; ++sb)
+        bulk_store(item_out + (int64_t)sb * B * 16 * 2, hist + sb * (H8_SB_BYTES / 4), (uint32_t)B * 128u);
+      bulk_commit();
+      bulk_wait_read_all();
     }
+    __syncthreads();
   }
+  if (bad) raise_err(p.st, ERRBIT_ROW);
   if (threadIdx.x == 0) bulk_wait_all();
 }
 
@@ -331,7 +276,7 @@ __global__ void __launch_bounds__(H8_THREADS, 4) k_hist_u8(Hist8Params P) {
 constexpr int H16_THREADS = 512;
 constexpr int H16_HIST_MAX = 160 * 1024;
 constexpr int H16_STAGE_SLOTS = 2048;
-constexpr int H16_STAGE_BYTES = H16_STAGE_SLOTS * 16;
+constexpr int H16_STAGE_BYTES = H16_STAGE_SLOTS * 8;
 
 struct Hist16Params {
   LevelParams lv;
@@ -360,10 +305,12 @@ __global__ void __launch_bounds__(H16_THREADS, 1) k_hist_u16(Hist16Params P) {
   const int64_t N = p.n_rows;
   const bool ident = (p.rows == nullptr);
   const uint32_t miss_slot = (uint32_t)P.n_bins;
+  (void)stage;
 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
   const int rho = lane / W, wi = lane % W;
   constexpr int GROUPS_PER_TILE = 32 / TS;
+  uint32_t bad = 0;
 
   for (;;) {
     if (threadIdx.x == 0) s_item = (int32_t)atomicAdd(&p.st->work_next, 1u);
@@ -386,19 +333,7 @@ __global__ void __launch_bounds__(H16_THREADS, 1) k_hist_u16(Hist16Params P) {
     for (int64_t g0 = it.k0 + RPI * warp; g0 < it.k1; g0 += step * 4) {
       int32_t rr[4], vg[4], vh[4];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int64_t k = g0 + u * step + rho;
-        rr[u] = -1; vg[u] = 0; vh[u] = 0;
-        if (k < it.k1) {
-          if (ident) {
-            const int2 qv = __ldg(&p.q[k]);
-            rr[u] = (int32_t)k; vg[u] = qv.x; vh[u] = qv.y;
-          } else {
-            const int4 rc = __ldg(&p.rec[k]);
-            rr[u] = rc.x; vg[u] = rc.y; vh[u] = rc.z;
-          }
-        }
-      }
+      for (int u = 0; u < 4; ++u) load_row(p, ident, g0 + u * step + rho, it.k1, rr[u], vg[u], vh[u], bad);
       uint32_t bw[4];
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
@@ -440,35 +375,82 @@ __global__ void __launch_bounds__(H16_THREADS, 1) k_hist_u16(Hist16Params P) {
       atomicAdd(c1 + 1, (uint32_t)mh1);
     }
     __syncthreads();
-    // flush per feature in slot chunks
-    const int f_item0 = it.fgroup * TS;
-    int64_t *node_out = p.hist_out + (int64_t)it.node * p.node_int64s;
-    for (int fl = 0; fl < TS; ++fl) {
-      const int f = f_item0 + fl;
-      if (f >= P.n_features) break;
-      for (int s0 = 0; s0 < B; s0 += H16_STAGE_SLOTS) {
-        const int ns = min(H16_STAGE_SLOTS, B - s0);
-        for (int i = threadIdx.x; i < ns; i += blockDim.x) {
-          const uint2 gh = *reinterpret_cast<const uint2 *>(hist + 2 * ((s0 + i) * TS + fl));
-          longlong2 v;
-          v.x = (long long)(int32_t)gh.x;
-          v.y = (long long)(int32_t)gh.y;
-          *reinterpret_cast<longlong2 *>(stage + i * 16) = v;
-        }
-        fence_proxy_async_smem();
-        __syncthreads();
-        if (threadIdx.x == 0) {
-          int64_t *dst = node_out + ((int64_t)f * B + s0) * 2;
-          if (it.multi) bulk_reduce_add_u64(dst, stage, (uint32_t)ns * 16u);
-          else bulk_store(dst, stage, (uint32_t)ns * 16u);
-          bulk_commit();
-          bulk_wait_read_all();
-        }
-        __syncthreads();
-      }
+    // flush: the item's shared image ([slot][TS][G, H] int32) in bulk stores of <= 64 KB
+    fence_proxy_async_smem();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      int32_t *item_out = p.partial + (int64_t)id * B * TS * 2;
+      const uint32_t total = (uint32_t)B * TS * 8u;
+      for (uint32_t off = 0; off < total; off += 65536u)
+        bulk_store(reinterpret_cast<unsigned char *>(item_out) + off, reinterpret_cast<unsigned char *>(hist) + off,
+                   min(65536u, total - off));
+      bulk_commit();
+      bulk_wait_read_all();
+    }
+    __syncthreads();
+  }
+  if (bad) raise_err(p.st, ERRBIT_ROW);
+  if (threadIdx.x == 0) bulk_wait_all();
+}
+
+// ----------------------------------------------------------------------------
+// Partials -> int64 histogram of one (node, feature) strip.
+//
+// Item images are [item][sub-block][slot][sbw][G, H] int32 (nsb sub-blocks of
+// sbw features per item): feature fl of an item is cell ((fl / sbw) * B + s)
+// * sbw + fl % sbw. Items are numbered chunk-major (chunk_prefix[n] + c) *
+// n_fgroups + feature group.
+struct PartialView {
+  const int32_t *partial;
+  const int32_t *chunk_prefix;
+  int32_t n_fgroups, sbw, nsb, B;
+};
+
+__device__ __forceinline__ const int2 *partial_feature(const PartialView &v, int64_t item, int f_in_group) {
+  const int sb = f_in_group / v.sbw, fl = f_in_group - sb * v.sbw;
+  return reinterpret_cast<const int2 *>(v.partial) + (item * v.nsb + sb) * (int64_t)v.B * v.sbw + fl;
+}
+
+// Sum of slot s of one feature over the nc chunk images starting at item0
+// (items item0 + c * n_fgroups); loads are issued in groups of 4.
+__device__ __forceinline__ longlong2 sum_chunks(const PartialView &v, int64_t item0, int nc, int f_in_group, int s) {
+  int64_t g = 0, h = 0;
+  const int64_t stride_items = v.n_fgroups;
+  int c = 0;
+  for (; c + 4 <= nc; c += 4) {
+    int2 x[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      x[u] = __ldcg(partial_feature(v, item0 + (int64_t)(c + u) * stride_items, f_in_group) + (int64_t)s * v.sbw);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      g += x[u].x;
+      h += x[u].y;
     }
   }
-  if (threadIdx.x == 0) bulk_wait_all();
+  for (; c < nc; ++c) {
+    const int2 x = __ldcg(partial_feature(v, item0 + (int64_t)c * stride_items, f_in_group) + (int64_t)s * v.sbw);
+    g += x.x;
+    h += x.y;
+  }
+  return make_longlong2(g, h);
+}
+
+// Finalize: grid (ceil(F / 8), n_nodes), 256 threads; warp w adds the chunk
+// partials of feature blockIdx.x * 8 + w of node blockIdx.y in int64 and
+// writes the strip of hist_out.
+__global__ void __launch_bounds__(256) k_finalize(PartialView v, int32_t n_features, int32_t item_feats,
+                                                  int64_t *__restrict__ hist_out, const DevState *st) {
+  if (!st->plan_ok) return;
+  const int n = blockIdx.y;
+  const int f = blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (f >= n_features) return;
+  const int nc = v.chunk_prefix[n + 1] - v.chunk_prefix[n];
+  const int fg = f / item_feats;
+  const int64_t item0 = (int64_t)v.chunk_prefix[n] * v.n_fgroups + fg;
+  longlong2 *dst = reinterpret_cast<longlong2 *>(hist_out) + ((int64_t)n * n_features + f) * v.B;
+  for (int s = lane; s < v.B; s += 32) dst[s] = sum_chunks(v, item0, nc, f - fg * item_feats, s);
 }
 
 }  // namespace gbt

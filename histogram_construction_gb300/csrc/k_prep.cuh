@@ -53,7 +53,11 @@ __global__ void __launch_bounds__(256) k_mirror(const T *__restrict__ bins, int6
   if (bad) raise_err(st, ERRBIT_BIN);
 }
 
-// (g, h) float32 pairs -> int32 fixed-point pairs, q = round-half-even(fl32(x * s)).
+// Largest admissible |q|: any 1024 rows then sum exactly in 32 bits.
+constexpr int QMAX = (1 << 21) - 1;
+
+// (g, h) float32 pairs -> int32 fixed-point pairs, q = round-half-even(fl32(x * s)),
+// |q| <= QMAX (else the quantisation error bit).
 // "GBDT engine engineering deep-dive" (ybb.press), section 7: gradients are
 // quantised to fixed point before integer atomics; bonsai "9. Parallelism &
 // determinism", "The idea": int64 cells are exact in any order.
@@ -66,15 +70,15 @@ __global__ void __launch_bounds__(1024) k_quantise(const float2 *__restrict__ gp
     const float pg = __fmul_rn(v.x, sg);
     const float ph = __fmul_rn(v.y, sh);
     int qg = 0, qh = 0;
-    if (fabsf(pg) < 2147483648.0f) {
-      const long long t = __float2ll_rn(pg);
-      if (t > -2147483648LL && t < 2147483648LL) qg = (int)t; else bad = 1;
+    if (fabsf(pg) < 2097152.0f) {
+      const int t = __float2int_rn(pg);
+      if (t >= -QMAX && t <= QMAX) qg = t; else bad = 1;
     } else {
       bad = 1;
     }
-    if (fabsf(ph) < 2147483648.0f) {
-      const long long t = __float2ll_rn(ph);
-      if (t > -2147483648LL && t < 2147483648LL) qh = (int)t; else bad = 1;
+    if (fabsf(ph) < 2097152.0f) {
+      const int t = __float2int_rn(ph);
+      if (t >= -QMAX && t <= QMAX) qh = t; else bad = 1;
     } else {
       bad = 1;
     }

@@ -21,6 +21,7 @@
 #include <float.h>
 
 #include "common.cuh"
+#include "k_hist.cuh"
 
 namespace gbt {
 
@@ -529,46 +530,100 @@ __global__ void __launch_bounds__(SCAN_THREADS) k_find(const int64_t *__restrict
   }
 }
 
-// Subtract and find: grid (ceil(F / (SCAN_WARPS/2)), n_pairs). Warp w takes
-// feature blockIdx.x * 4 + w/2 of pair blockIdx.y; even warps scan the small
-// sibling's strip, odd warps form Large = Parent - Small (stored) and scan it.
-// The last CTA of pair p writes small_out[p] and large_out[p].
-__global__ void __launch_bounds__(SCAN_THREADS) k_subtract_find(
-    const int64_t *__restrict__ parent, const int32_t *__restrict__ parent_of, const int64_t *__restrict__ small,
+// Where the small sibling's histogram comes from in the level-finish kernel.
+struct SmallSource {
+  const int64_t *hist;  // complete small histograms [n_pairs][F][B][2] (FROM_PARTIALS = false)
+  // chunk images of the level build (FROM_PARTIALS = true); the summed small
+  // histogram is also written to `hist_out`
+  PartialView view;
+  int32_t item_feats;
+  int32_t pad;
+  int64_t *hist_out;
+};
+
+// Small sibling strip of feature f of pair p, slot s (int64 pair).
+template <bool FROM_PARTIALS>
+__device__ __forceinline__ longlong2 small_cell(const SmallSource &src, int p, int f, int s, int n_features, int B,
+                                                int nc, int64_t item0) {
+  if (!FROM_PARTIALS) {
+    return __ldg(reinterpret_cast<const longlong2 *>(src.hist) + ((int64_t)p * n_features + f) * B + s);
+  } else {
+    return sum_chunks(src.view, item0, nc, f % src.item_feats, s);
+  }
+}
+
+// Level finish: grid (ceil(F / 4), n_pairs), 8 warps. Warp w takes feature
+// blockIdx.x * 4 + (w & 3) of pair blockIdx.y; warps 0-3 form the small
+// sibling's strip (read, or summed from the build's chunk partials and
+// written out), warps 4-7 load the parent strip and form Large = Parent -
+// Small (written out). Every warp then scans its strip; the last CTA of pair
+// p writes small_out[p] and large_out[p].
+template <bool FROM_PARTIALS>
+__global__ void __launch_bounds__(SCAN_THREADS) k_level_finish(
+    SmallSource src, const int64_t *__restrict__ parent, const int32_t *__restrict__ parent_of,
     int64_t *__restrict__ large, int32_t n_features, int32_t n_bins, SplitParams sp, Cand *__restrict__ cand,
     uint32_t *__restrict__ counters, SplitOut *__restrict__ small_out, SplitOut *__restrict__ large_out,
     DevState *st) {
   __shared__ ScanShared sh;
+  if (FROM_PARTIALS && !st->plan_ok) return;
   const int p = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int side = warp & 1;
-  const int f = blockIdx.x * (SCAN_WARPS / 2) + (warp >> 1);
+  const int fo = warp & 3, side = warp >> 2;
+  const int f = blockIdx.x * 4 + fo;
   const int B = n_bins + 1;
   const bool staged = B <= STAGE_SLOTS;
   scan_init(sh);
   const int64_t pp = parent_of ? (int64_t)parent_of[p] : p;
   const longlong2 *P = reinterpret_cast<const longlong2 *>(parent) + (pp * n_features + f) * B;
-  const longlong2 *S = reinterpret_cast<const longlong2 *>(small) + ((int64_t)p * n_features + f) * B;
   longlong2 *L = reinterpret_cast<longlong2 *>(large) + ((int64_t)p * n_features + f) * B;
-  const longlong2 *cells = staged ? sh.cells[warp] : (side ? L : S);
-  int64_t tg = 0, th = 0;
-  if (f < n_features) {
+  longlong2 *Sout = FROM_PARTIALS ? reinterpret_cast<longlong2 *>(src.hist_out) + ((int64_t)p * n_features + f) * B
+                                  : nullptr;
+  const longlong2 *Sin = FROM_PARTIALS ? Sout
+                                       : reinterpret_cast<const longlong2 *>(src.hist) + ((int64_t)p * n_features + f) * B;
+  int nc = 0;
+  int64_t item0 = 0;
+  if (FROM_PARTIALS) {
+    nc = src.view.chunk_prefix[p + 1] - src.view.chunk_prefix[p];
+    item0 = (int64_t)src.view.chunk_prefix[p] * src.view.n_fgroups + f / src.item_feats;
+  }
+  const bool active = f < n_features;
+  // phase A: small strip (warps 0-3), parent strip (warps 4-7)
+  if (active) {
+    if (side == 0) {
+      for (int s = lane; s < B; s += 32) {
+        const longlong2 c = small_cell<FROM_PARTIALS>(src, p, f, s, n_features, B, nc, item0);
+        if (FROM_PARTIALS) Sout[s] = c;
+        if (staged) sh.cells[warp][s] = c;
+      }
+    } else if (staged) {
+      for (int s = lane; s < B; s += 32) sh.cells[warp][s] = __ldg(P + s);
+    }
+  }
+  __syncthreads();
+  // phase B: large = parent - small
+  if (active && side == 1) {
     bool neg = false;
     for (int s = lane; s < B; s += 32) {
-      longlong2 c = __ldg(S + s);
-      if (side) {
-        const longlong2 a = __ldg(P + s);
-        c = make_longlong2(a.x - c.x, a.y - c.y);
-        neg |= c.y < 0;
-        L[s] = c;
-      }
-      if (staged) sh.cells[warp][s] = c;
+      const longlong2 a = staged ? sh.cells[warp][s] : __ldg(P + s);
+      const longlong2 b = staged ? sh.cells[warp - 4][s] : (FROM_PARTIALS ? __ldcg(Sin + s) : __ldg(Sin + s));
+      const longlong2 d = make_longlong2(a.x - b.x, a.y - b.y);
+      neg |= d.y < 0;
+      L[s] = d;
+      if (staged) sh.cells[warp][s] = d;
+    }
+    if (neg) raise_err(st, ERRBIT_INCONSISTENT);
+  }
+  __syncwarp();
+  // phase C: scan
+  const longlong2 *cells = staged ? sh.cells[warp] : (side ? L : Sin);
+  int64_t tg = 0, th = 0;
+  if (active) {
+    for (int s = lane; s < B; s += 32) {
+      const longlong2 c = cells[s];
       tg += c.x;
       th += c.y;
     }
-    if (neg) raise_err(st, ERRBIT_INCONSISTENT);
     warp_sum2(tg, th);
-    __syncwarp();
     int ovf = 0;
     const float wlo = warp_scan_push(cells, n_bins, tg, th, sp, f, side, sh, ovf);
     ovf = __any_sync(0xffffffffu, ovf);
@@ -579,15 +634,15 @@ __global__ void __launch_bounds__(SCAN_THREADS) k_subtract_find(
   }
   __syncthreads();
   float thr[2] = {-INFINITY, -INFINITY};
-  for (int w = 0; w < SCAN_WARPS; ++w) thr[w & 1] = fmaxf(thr[w & 1], sh.warp_lo[w]);
-  if (f < n_features && sh.warp_overflow[warp]) {
+  for (int w = 0; w < SCAN_WARPS; ++w) thr[w >> 2] = fmaxf(thr[w >> 2], sh.warp_lo[w]);
+  if (active && sh.warp_overflow[warp]) {
     const Cand d = warp_direct_best(cells, n_bins, tg, th, sp, thr[side], f);
     if (lane == 0) sh.extra[warp] = d;
   }
   __syncthreads();
   int warp_node[SCAN_WARPS];
 #pragma unroll
-  for (int w = 0; w < SCAN_WARPS; ++w) warp_node[w] = w & 1;
+  for (int w = 0; w < SCAN_WARPS; ++w) warp_node[w] = w >> 2;
   pool_finish(sh, sp, 2, thr, warp_node);
   const int nfb = gridDim.x;
   Cand *cs_base = cand + (int64_t)(2 * p) * nfb;

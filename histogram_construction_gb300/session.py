@@ -9,7 +9,7 @@ from __future__ import annotations
 import numpy as np
 
 from . import (GBT_OK, SPLIT_BYTES, check, gbt_begin_tree, gbt_build_level, gbt_create, gbt_destroy,
-               gbt_find_splits, gbt_kernel_launches, gbt_partition_level, gbt_subtract_and_find,
+               gbt_find_splits, gbt_kernel_launches, gbt_level_step, gbt_partition_level, gbt_subtract_and_find,
                gbt_subtract_siblings, gbt_sync, gbt_upload_bins, lib, params)
 
 SPLIT_DTYPE = np.dtype([
@@ -134,6 +134,21 @@ class Session:
         lo = self.torch.empty((n_pairs, SPLIT_BYTES), dtype=self.torch.uint8, device=self.device)
         self.check(gbt_subtract_and_find(self.ctx, parent, po, small, large, n_pairs, params(lam, gamma, mcw), so, lo))
         return large, so, lo
+
+    def level_step(self, rows, offsets, parent, parent_of=None, small=None, large=None, lam=1.0, gamma=0.0, mcw=0.0):
+        """Build the smaller siblings (rows/offsets: one segment per pair), subtract, find splits of both."""
+        n_pairs = int(len(offsets) - 1)
+        if small is None:
+            small = self.hist_tensor(n_pairs)
+        if large is None:
+            large = self.torch.empty_like(small)
+        r = self.to_dev(rows, self.torch.int32)
+        o = self.to_dev(offsets, self.torch.int64)
+        po = self.to_dev(parent_of, self.torch.int32)
+        so = self.torch.empty((n_pairs, SPLIT_BYTES), dtype=self.torch.uint8, device=self.device)
+        lo = self.torch.empty((n_pairs, SPLIT_BYTES), dtype=self.torch.uint8, device=self.device)
+        self.check(gbt_level_step(self.ctx, r, o, n_pairs, parent, po, small, large, params(lam, gamma, mcw), so, lo))
+        return small, large, so, lo
 
     def partition(self, rows, offsets, splits):
         """splits: [n, 56] uint8 tensor or numpy SPLIT_DTYPE array. Returns (rows, offsets [2n+1]) tensors."""

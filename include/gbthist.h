@@ -43,7 +43,7 @@ typedef enum {
   GBT_ERR_CUDA = 4,           /* a CUDA runtime call failed; gbt_last_error has the text */
   GBT_ERR_BIN_RANGE = 5,      /* device: a bin value was neither < n_bins nor the sentinel */
   GBT_ERR_ROW_RANGE = 6,      /* device: a row index was outside [0, n_rows), or offsets not ascending */
-  GBT_ERR_QUANT_OVERFLOW = 7, /* device: |g*scale| or |h*scale| >= 2^31, or not finite */
+  GBT_ERR_QUANT_OVERFLOW = 7, /* device: a quantised value outside [-(2^21-1), 2^21-1], or not finite */
   GBT_ERR_UNSUPPORTED = 8,    /* a size beyond this build's limits */
   GBT_ERR_TIMEOUT = 9,        /* device: a bounded wait ran out */
   GBT_ERR_INCONSISTENT = 10   /* device: subtraction produced a negative hessian cell */
@@ -106,14 +106,18 @@ gbt_status gbt_upload_bins(gbt_ctx *ctx, const void *bins, int bin_bytes, int64_
  * atomics].
  *   gpair: host or device, packed float32 (g, h) pairs [n_rows][2].
  *   scale_g, scale_h: fixed-point scales; q = round-half-even(float32(x * s)),
- *     |q| < 2^31 (else GBT_ERR_QUANT_OVERFLOW on the device word).
- * Read only during the call's stream work. */
+ *     |q| <= 2^21 - 1 (else GBT_ERR_QUANT_OVERFLOW on the device word). The
+ *     limit lets the kernels sum any 1024 rows exactly in 32-bit partials;
+ *     histogram cells are exact int64 sums.
+ * Read only during the call's stream work. The call also brings max|q| back
+ * to the host (asynchronously) to size the build's scratch. */
 gbt_status gbt_begin_tree(gbt_ctx *ctx, const float *gpair, float scale_g, float scale_h);
 
 /* Suggest power-of-two scales such that `rows_per_partial` rows of the
  * largest |g| (|h|) sum below 2^31 (the width of the kernels' per-chunk
- * partial sums); rows_per_partial <= 0 means 65536. A larger scale is always
- * correct; it only makes the build split nodes into more row chunks. */
+ * partial sums); rows_per_partial <= 0 means 65536, values below 1024 are
+ * raised to 1024. A larger scale (up to |q| <= 2^21 - 1) is always correct; it
+ * only makes the build split nodes into more row chunks. */
 gbt_status gbt_suggest_scales(int64_t rows_per_partial, float max_abs_g, float max_abs_h, float *scale_g,
                               float *scale_h);
 
@@ -154,6 +158,25 @@ gbt_status gbt_subtract_siblings(gbt_ctx *ctx, const int64_t *parent_hist, const
  *   out: host or device gbt_split [n_nodes] (host: valid after gbt_sync). */
 gbt_status gbt_find_splits(gbt_ctx *ctx, const int64_t *hist, int32_t n_nodes, const gbt_params *params,
                            gbt_split *out);
+
+/* One level of a depth-wise grower in three kernels: build the histograms of
+ * the smaller siblings of every pair (as gbt_build_level), derive the larger
+ * siblings from their parents (as gbt_subtract_siblings) and find the best
+ * split of both (as gbt_find_splits) [bonsai "10: CUDA histogram backend",
+ * "The device context lifecycle": advance_level builds the smaller siblings
+ * in one pass and derives the larger by subtraction; "Level batching"].
+ * Pair p = the p-th node segment of `rows`/`node_offsets` (its smaller
+ * sibling) and parent parent_of[p] (NULL = p).
+ *   rows, node_offsets: as gbt_build_level, n_pairs segments.
+ *   parent_hist: device [..][F][B][2] int64.
+ *   small_hist, large_hist: device [n_pairs][F][B][2] int64, written.
+ *   small_out, large_out: host or device gbt_split [n_pairs].
+ * Results equal gbt_build_level + gbt_subtract_and_find; the partial sums of
+ * the build go straight into the subtraction, with no int64 round trip. */
+gbt_status gbt_level_step(gbt_ctx *ctx, const int32_t *rows, const int64_t *node_offsets, int32_t n_pairs,
+                          const int64_t *parent_hist, const int32_t *parent_of, int64_t *small_hist,
+                          int64_t *large_hist, const gbt_params *params, gbt_split *small_out,
+                          gbt_split *large_out);
 
 /* gbt_subtract_siblings and gbt_find_splits for both siblings in one pass
  * over the parent and small histograms: small_out[p] is the split of

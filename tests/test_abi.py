@@ -40,7 +40,7 @@ def test_suggest_scales_is_largest_power_of_two_within_bound(rows, mg, mh):
     import histogram_construction_gb300 as g
     st, sg, sh = g.gbt_suggest_scales(rows, mg, mh)
     assert st == 0
-    r = rows if rows > 0 else 65536
+    r = max(rows if rows > 0 else 65536, 1024)  # documented floor of 1024 rows per partial
     for m, s in ((mg, sg), (mh, sh)):
         assert math.log2(s) == int(math.log2(s))
         assert m * s * r <= 2 ** 31 - 1

@@ -69,6 +69,13 @@ def run_level(sess, oracle, w, depth, sg, sh, lam=1.0, gamma=0.0, mcw=0.0, host_
     from histogram_construction_gb300.session import splits_to_numpy
     assert_splits_equal(splits_to_numpy(so), ref_so, "small splits")
     assert_splits_equal(splits_to_numpy(lo), ref_lo, "large splits")
+    # the fused level step (build partials -> subtract -> find in one pass) gives the same bytes
+    hs2, large2, so2, lo2 = sess.level_step(lv.built_rows, offs_s, hp, lam=lam, gamma=gamma, mcw=mcw)
+    assert sess.sync() == 0
+    np.testing.assert_array_equal(hs2.cpu().numpy(), ref_hs, err_msg="level_step small hist")
+    np.testing.assert_array_equal(large2.cpu().numpy(), ref_large, err_msg="level_step large hist")
+    assert_splits_equal(splits_to_numpy(so2), ref_so, "level_step small splits")
+    assert_splits_equal(splits_to_numpy(lo2), ref_lo, "level_step large splits")
     return hp, hs, large, ref_hp, ref_hs, ref_large
 
 
@@ -243,22 +250,26 @@ def test_edge_all_rows_one_bin_and_all_missing(gb, oracle_mod):
         assert rs["feature"][0] == -1
 
 
-def test_edge_quantisation_limit_forces_single_row_chunks(gb, oracle_mod):
-    """|q| close to 2^31: every chunk holds one row, all nodes are reduced from many chunks."""
+def test_edge_quantisation_limit_forces_minimum_chunks(gb, oracle_mod):
+    """|q| at the limit 2^21 - 1: chunks of 1024 rows, nodes built from several chunks."""
     g, Session, s2n = gb
-    bins, gp, sentinel = _tiny(1, n_rows=3000, n_features=65, n_bins=40)
-    gp[0, 0] = 1.0
-    scale = 2147483520.0  # q = 2147483520 for g = 1.0 (largest float below 2^31)
+    bins, gp, sentinel = _tiny(1, n_rows=5000, n_features=65, n_bins=40)
     gp[:, 0] = np.clip(gp[:, 0], -1.0, 1.0)
+    gp[0, 0] = 1.0
+    scale = 2097151.0  # q = 2097151 for g = 1.0
     with Session() as s:
         s.upload_bins(bins, 40, sentinel).begin_tree(gp, scale, 1.0e6)
-        offs = np.array([0, 1700, 3000], np.int64)
+        offs = np.array([0, 3700, 5000], np.int64)
         h = s.build_level(None, offs)
         assert s.sync() == 0
         q, st = oracle_mod.quantise(gp, scale, 1.0e6)
-        assert st == oracle_mod.OK and oracle_mod.max_abs_q(q) >= 2 ** 30
+        assert st == oracle_mod.OK and oracle_mod.max_abs_q(q) == 2097151
         ref, _ = oracle_mod.build_hist(bins, 40, sentinel, q, None, offs)
         np.testing.assert_array_equal(h.cpu().numpy(), ref)
+        bad = gp.copy()
+        bad[3, 0] = 1.5  # 1.5 * (2^21 - 1) is beyond the limit
+        assert g.gbt_begin_tree(s.ctx, bad, scale, 1.0e6) == 0
+        assert s.sync() == g.GBT_ERR_QUANT_OVERFLOW
 
 
 def test_determinism_bytes_identical(gb):

@@ -27,8 +27,9 @@ def _load(name):
     [
         (0.5, 1.0, 0), (1.5, 1.0, 2), (2.5, 1.0, 2), (-0.5, 1.0, 0), (-1.5, 1.0, -2), (-2.5, 1.0, -2),
         (3.25, 4.0, 13), (0.1, 1024.0, 102), (-0.1, 1024.0, -102),
-        (2147483520.0, 1.0, 2147483520),  # largest float below 2^31
-        (-2147483520.0, 1.0, -2147483520),
+        (2097151.0, 1.0, 2097151),  # largest admissible |q| = 2^21 - 1
+        (-2097151.0, 1.0, -2097151),
+        (2097151.25, 1.0, 2097151),  # rounds down to the limit
     ],
 )
 def test_quantise_round_half_even(oracle_mod, x, s, q):
@@ -39,8 +40,9 @@ def test_quantise_round_half_even(oracle_mod, x, s, q):
     assert out[0, 0] == q and out[0, 1] == q
 
 
-@pytest.mark.parametrize("x", [2147483648.0, -2147483648.0, float("inf"), float("nan"), 3.0e9])
+@pytest.mark.parametrize("x", [2097152.0, -2097152.0, 2097151.75, float("inf"), float("nan"), 3.0e9])
 def test_quantise_overflow_is_an_error(oracle_mod, x):
+    """|q| must stay within 2^21 - 1 (2097151.75 rounds to 2^21: out of range)."""
     _, st = oracle_mod.quantise(np.array([[x, 0.0]], np.float32), 1.0, 1.0)
     assert st == oracle_mod.ERR_QUANT
 
