@@ -27,7 +27,7 @@ EXPORTS = [
     "gbt_suggest_scales", "gbt_build_level", "gbt_subtract_siblings", "gbt_find_splits", "gbt_subtract_and_find",
     "gbt_level_step",
     "gbt_partition_level", "gbt_profile_enable", "gbt_profile_read", "gbt_slots_per_feature",
-    "gbt_kernel_launches",
+    "gbt_kernel_launches", "gbt_find_splits_noalloc",
 ]
 
 
@@ -84,6 +84,7 @@ def lib(build_if_missing: bool = True):
         "gbt_profile_read": (st, [vp, ctypes.c_char_p, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(i64)]),
         "gbt_slots_per_feature": (i32, [vp]),
         "gbt_kernel_launches": (i64, [vp]),
+        "gbt_find_splits_noalloc": (st, [vp, i32, i32, i32, f32, f32, ctypes.POINTER(GbtParams), vp, vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(L, name)
@@ -173,6 +174,12 @@ def gbt_subtract_siblings(ctx, parent_hist, parent_of, small_hist, large_hist, n
 
 def gbt_find_splits(ctx, hist, n_nodes, prm, out):
     return lib().gbt_find_splits(ctx, ptr(hist), int(n_nodes), ctypes.byref(prm), ptr(out))
+
+
+def gbt_find_splits_noalloc(hist, n_nodes, n_features, n_bins, scale_g, scale_h, prm, out, stream=None):
+    """Context-free split find that allocates nothing (device hist and out; see the header for its limits)."""
+    return lib().gbt_find_splits_noalloc(ptr(hist), int(n_nodes), int(n_features), int(n_bins), float(scale_g),
+                                         float(scale_h), ctypes.byref(prm), ptr(out), stream)
 
 
 def gbt_subtract_and_find(ctx, parent_hist, parent_of, small_hist, large_hist, n_pairs, prm, small_out, large_out):

@@ -10,6 +10,7 @@
 #include <algorithm>
 #include <initializer_list>
 #include <map>
+#include <mutex>
 #include <string>
 #include <vector>
 
@@ -913,5 +914,81 @@ gbt_status gbt_profile_read(gbt_ctx *c, const char *kernel, double *total_ms, in
 int32_t gbt_slots_per_feature(const gbt_ctx *c) { return (c && c->n_rows > 0) ? c->n_bins + 1 : -1; }
 
 int64_t gbt_kernel_launches(const gbt_ctx *c) { return c ? c->launches : 0; }
+
+}  // extern "C"
+
+// ---------------------------------------------------------------------------- split find without allocation
+// For callers that may not allocate device memory at all: code running inside
+// a host that owns every allocation (a pool or arena it hands out itself), or
+// a stream-ordered pipeline where a cudaMalloc would synchronise the device
+// and stall other work. The split find's scratch (per-CTA candidates and the
+// per-node arrival counters) lives here in one fixed array that is part of the
+// loaded module; every GPU that loads the library keeps it until exit.
+
+namespace {
+constexpr int NOALLOC_MAX_NODES = 4096;    // nodes per call
+constexpr int NOALLOC_MAX_CANDS = 32768;   // nodes * ceil(n_features / 8) per call
+constexpr size_t NOALLOC_COUNTER_BYTES = (size_t)NOALLOC_MAX_NODES * sizeof(uint32_t);
+constexpr size_t NOALLOC_BYTES = NOALLOC_COUNTER_BYTES + (size_t)NOALLOC_MAX_CANDS * sizeof(Cand);  // 2 MiB + 16 KiB
+static_assert(NOALLOC_COUNTER_BYTES % 256 == 0, "candidate area alignment");
+constexpr int NOALLOC_MAX_DEVICES = 64;
+}  // namespace
+
+// Host code sees only a stand-in for this array; its device address comes from
+// cudaGetSymbolAddress, taken once per device below.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[NOALLOC_BYTES];
+
+namespace {
+std::mutex g_noalloc_mu;
+void *g_noalloc_addr[NOALLOC_MAX_DEVICES] = {};  // device address of g_noalloc_scratch per device, once known
+}  // namespace
+
+extern "C" {
+
+gbt_status gbt_find_splits_noalloc(const int64_t *hist, int32_t n_nodes, int32_t n_features, int32_t n_bins,
+                                   float scale_g, float scale_h, const gbt_params *params, gbt_split *out,
+                                   void *cuda_stream) {
+  if (!hist || !params || !out) return GBT_ERR_INVALID_ARG;
+  if (n_nodes < 0 || n_features < 1 || n_bins < 1 || n_bins > 65535) return GBT_ERR_INVALID_ARG;
+  if (!(scale_g > 0.f) || !(scale_h > 0.f) || !isfinite(scale_g) || !isfinite(scale_h)) return GBT_ERR_INVALID_ARG;
+  if (n_nodes == 0) return GBT_OK;
+  const int64_t nfb = (n_features + SCAN_WARPS - 1) / SCAN_WARPS;
+  if (n_nodes > NOALLOC_MAX_NODES || (int64_t)n_nodes * nfb > NOALLOC_MAX_CANDS) return GBT_ERR_UNSUPPORTED;
+  if (ptr_kind(hist) != 1 || !aligned16(hist) || ptr_kind(out) != 1) return GBT_ERR_INVALID_ARG;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return GBT_ERR_CUDA;
+  if (dev < 0 || dev >= NOALLOC_MAX_DEVICES) return GBT_ERR_UNSUPPORTED;
+  void *scratch = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_noalloc_addr[dev]) {
+      void *p = nullptr;
+      const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+      if (e != cudaSuccess || !p) {
+        cudaGetLastError();
+        return GBT_ERR_CUDA;
+      }
+      g_noalloc_addr[dev] = p;
+    }
+    scratch = g_noalloc_addr[dev];
+  }
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(cuda_stream);
+  uint32_t *counters = static_cast<uint32_t *>(scratch);
+  Cand *cand = reinterpret_cast<Cand *>(static_cast<unsigned char *>(scratch) + NOALLOC_COUNTER_BYTES);
+  // the arrival counters must start at zero whatever an earlier call left
+  if (cudaMemsetAsync(counters, 0, (size_t)n_nodes * sizeof(uint32_t), stream) != cudaSuccess) {
+    cudaGetLastError();
+    return GBT_ERR_CUDA;
+  }
+  // make_sp reads only the two inverse scales of the context
+  gbt_ctx scales;
+  scales.inv_sg = 1.0 / (double)scale_g;
+  scales.inv_sh = 1.0 / (double)scale_h;
+  const SplitParams sp = make_sp(&scales, params);
+  k_find<<<dim3((unsigned)nfb, n_nodes), SCAN_THREADS, 0, stream>>>(hist, n_features, n_bins, sp, cand, counters,
+                                                                     reinterpret_cast<SplitOut *>(out));
+  if (cudaGetLastError() != cudaSuccess) return GBT_ERR_CUDA;
+  return GBT_OK;
+}
 
 }  // extern "C"

@@ -159,6 +159,31 @@ gbt_status gbt_subtract_siblings(gbt_ctx *ctx, const int64_t *parent_hist, const
 gbt_status gbt_find_splits(gbt_ctx *ctx, const int64_t *hist, int32_t n_nodes, const gbt_params *params,
                            gbt_split *out);
 
+/* gbt_find_splits without a context and without any allocation. The paper
+ * has no counterpart: this exists for callers that may not allocate device
+ * memory themselves or through a library, e.g. a host application that hands
+ * out all device memory from its own pool, or code that must not let a
+ * cudaMalloc synchronise the device in the middle of stream-ordered work.
+ * Same candidates, tie-break and result as gbt_find_splits with a context
+ * whose tree began with these scales.
+ *   hist: device [n_nodes][n_features][n_bins + 1][2] int64, 16-byte aligned.
+ *   out: DEVICE gbt_split [n_nodes] (no host staging: that would allocate).
+ *   scale_g, scale_h: the scales the histogram was quantised with (> 0, finite).
+ *   cuda_stream: a cudaStream_t of the calling thread's current device.
+ * Scratch: one fixed 2 MiB + 16 KiB array inside the library, present on
+ * every device that loads it until the process exits. Limits per call:
+ * n_nodes <= 4096 and n_nodes * ceil(n_features / 8) <= 32768; beyond them
+ * the call returns GBT_ERR_UNSUPPORTED before touching the device. The first
+ * call on each device looks up that array's device address (make it before
+ * any stream capture). Every call uses the same array and clears only its
+ * arrival counters: calls whose work overlaps on the GPU (other streams,
+ * other threads) race on it, so order them on one stream or synchronise.
+ * Errors: GBT_ERR_INVALID_ARG (NULL, bad sizes or scales, host or misaligned
+ * buffers), GBT_ERR_UNSUPPORTED (limits), GBT_ERR_CUDA (launch failed). */
+gbt_status gbt_find_splits_noalloc(const int64_t *hist, int32_t n_nodes, int32_t n_features, int32_t n_bins,
+                                   float scale_g, float scale_h, const gbt_params *params, gbt_split *out,
+                                   void *cuda_stream);
+
 /* One level of a depth-wise grower in three kernels: build the histograms of
  * the smaller siblings of every pair (as gbt_build_level), derive the larger
  * siblings from their parents (as gbt_subtract_siblings) and find the best
