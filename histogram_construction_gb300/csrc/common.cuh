@@ -23,7 +23,7 @@ struct DevState {
   uint32_t plan_ok;    // 1 when the level plan is valid
   int64_t chunk_rows;  // rows per work item chunk (level plan)
   int32_t n_items;     // work items of the level
-  int32_t pad;
+  int32_t chunks_per_group;  // consecutive chunks of a node whose int32 sum stays exact (level plan)
 };
 
 constexpr int MIRROR_STRIP_BYTES = 64;  // bytes per row per mirror tile of features
@@ -49,6 +49,13 @@ __device__ __forceinline__ void bulk_store(void *gdst, const void *ssrc, uint32_
 // Bulk reduce-add shared -> global of 64-bit integers (two's complement add).
 __device__ __forceinline__ void bulk_reduce_add_u64(void *gdst, const void *ssrc, uint32_t bytes) {
   asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.u64 [%0], [%1], %2;" ::"l"(gdst),
+               "r"(smem_addr(ssrc)), "r"(bytes)
+               : "memory");
+}
+
+// Bulk reduce-add shared -> global of 32-bit integers (wraps modulo 2^32).
+__device__ __forceinline__ void bulk_reduce_add_u32(void *gdst, const void *ssrc, uint32_t bytes) {
+  asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.u32 [%0], [%1], %2;" ::"l"(gdst),
                "r"(smem_addr(ssrc)), "r"(bytes)
                : "memory");
 }

@@ -534,7 +534,7 @@ gbt_status run_level_build(gbt_ctx *c, const int32_t *rows, const int64_t *node_
       rows_d = rows;
     }
   }
-  s = ensure(c, c->chunk_prefix, (size_t)(n_nodes + 1) * sizeof(int32_t), "chunk prefix");
+  s = ensure(c, c->chunk_prefix, (size_t)2 * (n_nodes + 1) * sizeof(int32_t), "chunk and group prefixes");
   if (s != GBT_OK) return s;
   if (!c->qmax_known) {
     CUDA_TRY(c, cudaEventSynchronize(c->ev_q), "wait for max|q|");
@@ -552,10 +552,13 @@ gbt_status run_level_build(gbt_ctx *c, const int32_t *rows, const int64_t *node_
   lp.n_rows = c->n_rows;
   lp.q = (const int2 *)c->q.p;
   lp.chunk_prefix = (int32_t *)c->chunk_prefix.p;
+  lp.group_prefix = lp.chunk_prefix + (n_nodes + 1);
   lp.sbw = c->bin_bytes == 1 ? 16 : c->ts16;
   lp.nsb = c->bin_bytes == 1 ? H8_SB : 1;
+  lp.image_int4s = (int64_t)lp.nsb * lp.sbw * B / 2;  // nsb x B x sbw (G, H) int32 pairs
   lp.st = c->st;
-  // partial scratch for the largest item count the device plan can produce:
+  // image scratch for the largest item count the device plan can produce
+  // (there are never more group images than items):
   // items <= n_fgroups * n_nodes + max(target_items, n_fgroups * n_rows / rows_per_chunk_min)
   const int64_t rc = 2147483647LL / std::max<int64_t>(c->qmax, 1);
   const int64_t chunk_floor = std::max<int64_t>(1, std::min<int64_t>(rc, CHUNK_MIN_ROWS));
@@ -564,12 +567,12 @@ gbt_status run_level_build(gbt_ctx *c, const int32_t *rows, const int64_t *node_
                                                                    ((c->n_rows + chunk_floor - 1) / chunk_floor)) +
                             lp.n_fgroups;
   if (items_max > INT32_MAX / 2) return fail(c, GBT_ERR_UNSUPPORTED, "level too large for the work-item plan");
-  s = ensure(c, c->partial, (size_t)items_max * lp.nsb * lp.sbw * B * 8, "level partial scratch");
+  s = ensure(c, c->partial, (size_t)items_max * lp.image_int4s * 16, "level image scratch");
   if (s != GBT_OK) return s;
   lp.partial = (int32_t *)c->partial.p;
 
   prof_begin(c);
-  k_level_plan<<<1, 1024, 0, c->stream>>>(lp);
+  k_level_plan<<<c->n_sm, PLAN_THREADS, 0, c->stream>>>(lp);
   LAUNCH_CHECK(c, "k_level_plan");
   const int hist_ctas = c->n_sm;  // persistent: one resident CTA per SM
   if (c->bin_bytes == 1) {
@@ -608,7 +611,8 @@ gbt_status run_level_build(gbt_ctx *c, const int32_t *rows, const int64_t *node_
 PartialView partial_view(const LevelParams &lp, int B) {
   PartialView v;
   v.partial = lp.partial;
-  v.chunk_prefix = lp.chunk_prefix;
+  v.group_prefix = lp.group_prefix;
+  v.image_int4s = lp.image_int4s;
   v.n_fgroups = lp.n_fgroups;
   v.sbw = lp.sbw;
   v.nsb = lp.nsb;
@@ -634,8 +638,9 @@ gbt_status gbt_build_level(gbt_ctx *c, const int32_t *rows, const int64_t *node_
   s = run_level_build(c, rows, node_offsets, n_nodes, &lp);
   if (s != GBT_OK) return s;
   prof_begin(c);
-  k_finalize<<<dim3((c->n_features + 7) / 8, n_nodes), 256, 0, c->stream>>>(
-      partial_view(lp, c->n_bins + 1), c->n_features, lp.item_feats, hist_out, c->st);
+  const int64_t cells = (int64_t)n_nodes * ((c->n_features + 3) / 4) * 4 * (c->n_bins + 1);
+  k_finalize<<<grid_for(c, cells, 256, 8), 256, 0, c->stream>>>(partial_view(lp, c->n_bins + 1), n_nodes,
+                                                                 c->n_features, lp.item_feats, hist_out, c->st);
   LAUNCH_CHECK(c, "k_finalize");
   return GBT_OK;
 }

@@ -40,85 +40,147 @@ struct LevelParams {
   int32_t item_feats;     // features per work item (64 for u8, TS for u16)
   int64_t n_rows;
   const int2 *q;          // quantised gpair [n_rows]
-  int32_t *chunk_prefix;  // [n_nodes + 1]
-  int32_t *partial;       // raw shared-memory images of the items (see PartialView)
+  int32_t *chunk_prefix;  // [n_nodes + 1] chunks before each node
+  int32_t *group_prefix;  // [n_nodes + 1] exactness groups before each node
+  int32_t *partial;       // int32 group images (see PartialView)
+  int64_t image_int4s;    // 16-byte units per image
   int32_t sbw;            // features per sub-block of the image (16 for u8, TS for u16)
-  int32_t nsb;            // sub-blocks per item image (4 for u8, 1 for u16)
+  int32_t nsb;            // sub-blocks per image (4 for u8, 1 for u16)
   DevState *st;
 };
 
-// Level plan (one block): rows per chunk (load balance, capped by the int32
-// exactness bound), chunk counts per node and their prefix, item count.
-// Offsets that do not start at 0, descend or exceed n_rows invalidate the
-// plan (no items; GBT_ERR_ROW_RANGE).
-__global__ void __launch_bounds__(1024) k_level_plan(LevelParams p) {
-  __shared__ int32_t s_carry;
-  __shared__ int32_t s_bad;
-  __shared__ int32_t s_warp[32];
+// Block-wide inclusive scan of one int64 per thread (every thread calls it).
+__device__ __forceinline__ int64_t block_incl_scan(int64_t v, int64_t *s_warp) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int64_t y = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += y;
+  }
+  if (lane == 31) s_warp[w] = v;
+  __syncthreads();
+  if (w == 0) {
+    int64_t x = lane < nw ? s_warp[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int64_t y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    s_warp[lane] = x;
+  }
+  __syncthreads();
+  const int64_t r = v + (w > 0 ? s_warp[w - 1] : 0);
+  __syncthreads();
+  return r;
+}
+
+// Level plan. Rows per chunk come from the load-balance target, capped by
+// the int32 exactness bound rc = (2^31 - 1) / max|q|; consecutive chunks of
+// a node form exactness groups of floor(rc / chunk) chunks, whose int32 sum
+// cannot overflow either. Every work item (chunk, feature group) adds its
+// shared-memory image into its group's image; groups of more than one chunk
+// are zeroed here first (every block plans redundantly and zeroes a share;
+// block 0 publishes the plan). Offsets that do not start at 0, descend or
+// leave [0, n_rows] invalidate the plan (no items; GBT_ERR_ROW_RANGE).
+constexpr int PLAN_THREADS = 1024;
+
+__global__ void __launch_bounds__(PLAN_THREADS) k_level_plan(LevelParams p) {
+  __shared__ int64_t s_warp[32];
+  __shared__ int64_t s_zpre[PLAN_THREADS + 1];  // zero-unit prefix of the batch's nodes
+  __shared__ int64_t s_zbase[PLAN_THREADS];     // first zeroed unit of each node of the batch
+  __shared__ int64_t s_tot[2];
   __shared__ long long s_chunk;
-  if (threadIdx.x == 0) {
-    const int64_t R = p.offs[p.n_nodes] - p.offs[0];
+  __shared__ int32_t s_cpg;
+  const int tid = threadIdx.x;
+  const bool pub = blockIdx.x == 0;
+  bool bad = (tid == 0) && (p.offs[0] != 0);
+  for (int n = tid; n < p.n_nodes; n += blockDim.x) {
+    const int64_t a = p.offs[n], b = p.offs[n + 1];
+    bad |= (a < 0) || (b < a) || (b > p.n_rows);
+  }
+  if (__syncthreads_or(bad)) {
+    if (pub && tid == 0) {
+      p.st->plan_ok = 0;
+      p.st->n_items = 0;
+      p.st->work_next = 0;
+      raise_err(p.st, ERRBIT_ROW);
+    }
+    return;
+  }
+  if (tid == 0) {
+    const int64_t R = p.offs[p.n_nodes];
     const uint32_t qm = max(p.st->qmax, 1u);
     const int64_t rc = 2147483647LL / (int64_t)qm;  // rows whose int32 partials cannot overflow
-    int64_t tgt = (max(R, (int64_t)0) * p.n_fgroups + p.target_items - 1) / max(p.target_items, 1);
+    int64_t tgt = (R * p.n_fgroups + p.target_items - 1) / max(p.target_items, 1);
     tgt = max(tgt, (int64_t)CHUNK_MIN_ROWS);
-    s_chunk = max((int64_t)1, min(rc, tgt));
-    s_carry = 0;
-    s_bad = (p.offs[0] != 0 || R > p.n_rows || R < 0) ? 1 : 0;
+    const int64_t chunk = max((int64_t)1, min(rc, tgt));
+    s_chunk = chunk;
+    s_cpg = (int32_t)min(rc / chunk, (int64_t)0x3fffffff);
   }
   __syncthreads();
   const int64_t chunk = s_chunk;
+  const int32_t cpg = s_cpg;
+  const int64_t img_group = (int64_t)p.n_fgroups * p.image_int4s;  // units of one group's images
+  int4 *zdst = reinterpret_cast<int4 *>(p.partial);
+  int64_t carry_c = 0, carry_g = 0;
   for (int base = 0; base < p.n_nodes; base += blockDim.x) {
-    const int n = base + threadIdx.x;
-    int32_t c = 0;
+    const int n = base + tid;
+    int64_t c = 0, g = 0, m = 0;
     if (n < p.n_nodes) {
-      const int64_t a = p.offs[n], b = p.offs[n + 1];
-      if (b < a) s_bad = 1;
-      const int64_t rows_n = max(b - a, (int64_t)0);
-      c = (int32_t)max((int64_t)1, (rows_n + chunk - 1) / chunk);
+      const int64_t rows_n = p.offs[n + 1] - p.offs[n];
+      c = max((int64_t)1, (rows_n + chunk - 1) / chunk);
+      g = (c + cpg - 1) / cpg;
+      if (cpg > 1) m = c / cpg + ((c % cpg) >= 2 ? 1 : 0);  // groups of >= 2 chunks: the first m
     }
-    int32_t v = c;
-    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-    for (int o = 1; o < 32; o <<= 1) {
-      const int32_t y = __shfl_up_sync(0xffffffffu, v, o);
-      if (lane >= o) v += y;
+    const int64_t ic = block_incl_scan(c, s_warp);
+    const int64_t ig = block_incl_scan(g, s_warp);
+    const int64_t iz = block_incl_scan(m * img_group, s_warp);
+    if (n < p.n_nodes && pub) {
+      p.chunk_prefix[n + 1] = (int32_t)(carry_c + ic);
+      p.group_prefix[n + 1] = (int32_t)(carry_g + ig);
     }
-    if (lane == 31) s_warp[w] = v;
+    s_zpre[tid + 1] = iz;
+    s_zbase[tid] = (carry_g + ig - g) * img_group;
+    if (tid == 0) s_zpre[0] = 0;
+    if (tid == blockDim.x - 1) {
+      s_tot[0] = ic;
+      s_tot[1] = ig;
+    }
     __syncthreads();
-    if (w == 0) {
-      int32_t x = lane < (int)(blockDim.x >> 5) ? s_warp[lane] : 0;
-      for (int o = 1; o < 32; o <<= 1) {
-        const int32_t y = __shfl_up_sync(0xffffffffu, x, o);
-        if (lane >= o) x += y;
+    const int64_t total = s_zpre[blockDim.x];
+    for (int64_t u = (int64_t)blockIdx.x * blockDim.x + tid; u < total; u += (int64_t)gridDim.x * blockDim.x) {
+      int lo = 0, hi = blockDim.x - 1;  // largest j with s_zpre[j] <= u
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (s_zpre[mid] <= u) lo = mid; else hi = mid - 1;
       }
-      s_warp[lane] = x;
+      zdst[s_zbase[lo] + (u - s_zpre[lo])] = make_int4(0, 0, 0, 0);
     }
-    __syncthreads();
-    const int32_t incl = v + (w > 0 ? s_warp[w - 1] : 0) + s_carry;
-    if (n < p.n_nodes) p.chunk_prefix[n + 1] = incl;
-    __syncthreads();
-    if (threadIdx.x == blockDim.x - 1) s_carry = incl;
+    carry_c += s_tot[0];
+    carry_g += s_tot[1];
     __syncthreads();
   }
-  if (threadIdx.x == 0) {
+  if (pub && tid == 0) {
     p.chunk_prefix[0] = 0;
-    const int ok = !s_bad;
-    p.st->plan_ok = ok;
+    p.group_prefix[0] = 0;
+    p.st->plan_ok = 1;
     p.st->chunk_rows = chunk;
-    p.st->n_items = ok ? s_carry * p.n_fgroups : 0;
+    p.st->chunks_per_group = cpg;
+    p.st->n_items = (int32_t)(carry_c * p.n_fgroups);
     p.st->work_next = 0;
-    if (!ok) raise_err(p.st, ERRBIT_ROW);
   }
 }
 
 // Decode a work item id (chunk-major, feature group fastest) into node,
-// feature group and row range.
+// feature group, row range and the group image it adds into.
 struct Item {
   int32_t node, fgroup;
   int64_t k0, k1;
+  int64_t image;  // group image index
+  bool multi;     // the group has more than one chunk: reduce-add, else store
 };
 
-__device__ __forceinline__ Item decode_item(int32_t id, const LevelParams &p, int64_t chunk) {
+__device__ __forceinline__ Item decode_item(int32_t id, const LevelParams &p, int64_t chunk, int32_t cpg) {
   Item it;
   const int32_t kc = id / p.n_fgroups;
   it.fgroup = id - kc * p.n_fgroups;
@@ -129,9 +191,13 @@ __device__ __forceinline__ Item decode_item(int32_t id, const LevelParams &p, in
   }
   it.node = lo;
   const int32_t c = kc - p.chunk_prefix[lo];
+  const int32_t nc = p.chunk_prefix[lo + 1] - p.chunk_prefix[lo];
   const int64_t a = p.offs[lo], b = p.offs[lo + 1];
   it.k0 = a + (int64_t)c * chunk;
   it.k1 = min(b, it.k0 + chunk);
+  const int32_t g = c / cpg;
+  it.image = (int64_t)(p.group_prefix[lo] + g) * p.n_fgroups + it.fgroup;
+  it.multi = min(cpg, nc - g * cpg) > 1;
   return it;
 }
 
@@ -185,6 +251,7 @@ __global__ void __launch_bounds__(H8_THREADS, 1) k_hist_u8(Hist8Params P) {
   const LevelParams &p = P.lv;
   if (!p.st->plan_ok) return;
   const int64_t chunk = p.st->chunk_rows;
+  const int32_t cpg = p.st->chunks_per_group;
   const int32_t n_items = p.st->n_items;
   const int B = P.n_slots;
   const int64_t N = p.n_rows;
@@ -209,7 +276,7 @@ __global__ void __launch_bounds__(H8_THREADS, 1) k_hist_u8(Hist8Params P) {
     __syncthreads();
     const int32_t id = s_item;
     if (id >= n_items) break;
-    const Item it = decode_item(id, p, chunk);
+    const Item it = decode_item(id, p, chunk, cpg);
     const int f_tile0 = it.fgroup * 64;
     const int nsb = min(H8_SB, (P.n_features - f_tile0 + 15) >> 4);
     {
@@ -252,14 +319,20 @@ __global__ void __launch_bounds__(H8_THREADS, 1) k_hist_u8(Hist8Params P) {
       }
     }
     __syncthreads();
-    // flush: the item's shared image ([sub-block][slot][16][G, H] int32) leaves
-    // with one TMA bulk store per sub-block; no transposition, no staging
+    // flush: the item's shared image ([sub-block][slot][16][G, H] int32)
+    // leaves as is, one TMA bulk operation per sub-block: a store when the
+    // item is its group's only chunk, else a reduce-add into the zeroed
+    // group image (exact: the group's int32 sums cannot overflow)
     fence_proxy_async_smem();
     __syncthreads();
     if (threadIdx.x == 0) {
-      int32_t *item_out = p.partial + (int64_t)id * H8_SB * B * 16 * 2;
-      for (int sb = 0; sb < nsb; ++sb)
-        bulk_store(item_out + (int64_t)sb * B * 16 * 2, hist + sb * (H8_SB_BYTES / 4), (uint32_t)B * 128u);
+      int32_t *img_out = p.partial + it.image * p.image_int4s * 4;
+      for (int sb = 0; sb < nsb; ++sb) {
+        int32_t *dst = img_out + (int64_t)sb * B * 16 * 2;
+        const int32_t *src = reinterpret_cast<const int32_t *>(hist) + sb * (H8_SB_BYTES / 4);
+        if (it.multi) bulk_reduce_add_u32(dst, src, (uint32_t)B * 128u);
+        else bulk_store(dst, src, (uint32_t)B * 128u);
+      }
       bulk_commit();
       bulk_wait_read_all();
     }
@@ -301,6 +374,7 @@ __global__ void __launch_bounds__(H16_THREADS, 1) k_hist_u16(Hist16Params P) {
   const LevelParams &p = P.lv;
   if (!p.st->plan_ok) return;
   const int64_t chunk = p.st->chunk_rows;
+  const int32_t cpg = p.st->chunks_per_group;
   const int32_t n_items = p.st->n_items;
   const int64_t N = p.n_rows;
   const bool ident = (p.rows == nullptr);
@@ -317,7 +391,7 @@ __global__ void __launch_bounds__(H16_THREADS, 1) k_hist_u16(Hist16Params P) {
     __syncthreads();
     const int32_t id = s_item;
     if (id >= n_items) break;
-    const Item it = decode_item(id, p, chunk);
+    const Item it = decode_item(id, p, chunk, cpg);
     {
       uint4 *h4 = reinterpret_cast<uint4 *>(hist);
       const int n4 = (B * TS * 8) / 16;
@@ -375,15 +449,18 @@ __global__ void __launch_bounds__(H16_THREADS, 1) k_hist_u16(Hist16Params P) {
       atomicAdd(c1 + 1, (uint32_t)mh1);
     }
     __syncthreads();
-    // flush: the item's shared image ([slot][TS][G, H] int32) in bulk stores of <= 64 KB
+    // flush: the item's shared image ([slot][TS][G, H] int32) in bulk stores
+    // (or reduce-adds, for a group of several chunks) of <= 64 KB
     fence_proxy_async_smem();
     __syncthreads();
     if (threadIdx.x == 0) {
-      int32_t *item_out = p.partial + (int64_t)id * B * TS * 2;
+      unsigned char *img_out = reinterpret_cast<unsigned char *>(p.partial + it.image * p.image_int4s * 4);
+      const unsigned char *src = reinterpret_cast<const unsigned char *>(hist);
       const uint32_t total = (uint32_t)B * TS * 8u;
-      for (uint32_t off = 0; off < total; off += 65536u)
-        bulk_store(reinterpret_cast<unsigned char *>(item_out) + off, reinterpret_cast<unsigned char *>(hist) + off,
-                   min(65536u, total - off));
+      for (uint32_t off = 0; off < total; off += 65536u) {
+        if (it.multi) bulk_reduce_add_u32(img_out + off, src + off, min(65536u, total - off));
+        else bulk_store(img_out + off, src + off, min(65536u, total - off));
+      }
       bulk_commit();
       bulk_wait_read_all();
     }
@@ -394,63 +471,58 @@ __global__ void __launch_bounds__(H16_THREADS, 1) k_hist_u16(Hist16Params P) {
 }
 
 // ----------------------------------------------------------------------------
-// Partials -> int64 histogram of one (node, feature) strip.
+// Group images -> int64 histogram.
 //
-// Item images are [item][sub-block][slot][sbw][G, H] int32 (nsb sub-blocks of
-// sbw features per item): feature fl of an item is cell ((fl / sbw) * B + s)
-// * sbw + fl % sbw. Items are numbered chunk-major (chunk_prefix[n] + c) *
-// n_fgroups + feature group.
+// Images are [image][sub-block][slot][sbw][G, H] int32 (nsb sub-blocks of sbw
+// features): feature fl of an item's feature group is cell ((fl / sbw) * B +
+// s) * sbw + fl % sbw. The images of node n are groups group_prefix[n] ..
+// group_prefix[n+1]-1, image (group * n_fgroups + feature group).
 struct PartialView {
   const int32_t *partial;
-  const int32_t *chunk_prefix;
+  const int32_t *group_prefix;
+  int64_t image_int4s;
   int32_t n_fgroups, sbw, nsb, B;
 };
 
-__device__ __forceinline__ const int2 *partial_feature(const PartialView &v, int64_t item, int f_in_group) {
-  const int sb = f_in_group / v.sbw, fl = f_in_group - sb * v.sbw;
-  return reinterpret_cast<const int2 *>(v.partial) + (item * v.nsb + sb) * (int64_t)v.B * v.sbw + fl;
+// Cell (slot s) of feature f of the first group image of a node; the next
+// group's image is image_stride int2 further.
+__device__ __forceinline__ const int2 *image_cell(const PartialView &v, int32_t group, int f, int item_feats,
+                                                  int s) {
+  const int fg = f / item_feats, fl = f - fg * item_feats;
+  const int sb = fl / v.sbw, c = fl - sb * v.sbw;
+  const int64_t image = (int64_t)group * v.n_fgroups + fg;
+  return reinterpret_cast<const int2 *>(v.partial) + image * v.image_int4s * 2 + ((int64_t)sb * v.B + s) * v.sbw + c;
 }
 
-// Sum of slot s of one feature over the nc chunk images starting at item0
-// (items item0 + c * n_fgroups); loads are issued in groups of 4.
-__device__ __forceinline__ longlong2 sum_chunks(const PartialView &v, int64_t item0, int nc, int f_in_group, int s) {
-  int64_t g = 0, h = 0;
-  const int64_t stride_items = v.n_fgroups;
-  int c = 0;
-  for (; c + 4 <= nc; c += 4) {
-    int2 x[4];
-#pragma unroll
-    for (int u = 0; u < 4; ++u)
-      x[u] = __ldcg(partial_feature(v, item0 + (int64_t)(c + u) * stride_items, f_in_group) + (int64_t)s * v.sbw);
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      g += x[u].x;
-      h += x[u].y;
-    }
-  }
-  for (; c < nc; ++c) {
-    const int2 x = __ldcg(partial_feature(v, item0 + (int64_t)c * stride_items, f_in_group) + (int64_t)s * v.sbw);
-    g += x.x;
-    h += x.y;
-  }
-  return make_longlong2(g, h);
-}
-
-// Finalize: grid (ceil(F / 8), n_nodes), 256 threads; warp w adds the chunk
-// partials of feature blockIdx.x * 8 + w of node blockIdx.y in int64 and
-// writes the strip of hist_out.
-__global__ void __launch_bounds__(256) k_finalize(PartialView v, int32_t n_features, int32_t item_feats,
-                                                  int64_t *__restrict__ hist_out, const DevState *st) {
+// Finalize: the int64 histogram of every (node, feature, slot) is the sum of
+// the node's group images. One thread per cell; four consecutive threads take
+// four consecutive features of one slot (one 32-byte sector of an image row).
+__global__ void __launch_bounds__(256) k_finalize(PartialView v, int32_t n_nodes, int32_t n_features,
+                                                  int32_t item_feats, int64_t *__restrict__ hist_out,
+                                                  const DevState *st) {
   if (!st->plan_ok) return;
-  const int n = blockIdx.y;
-  const int f = blockIdx.x * 8 + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  if (f >= n_features) return;
-  const int nc = v.chunk_prefix[n + 1] - v.chunk_prefix[n];
-  const int fg = f / item_feats;
-  const int64_t item0 = (int64_t)v.chunk_prefix[n] * v.n_fgroups + fg;
-  longlong2 *dst = reinterpret_cast<longlong2 *>(hist_out) + ((int64_t)n * n_features + f) * v.B;
-  for (int s = lane; s < v.B; s += 32) dst[s] = sum_chunks(v, item0, nc, f - fg * item_feats, s);
+  const int nq = (n_features + 3) >> 2;
+  const int64_t units = (int64_t)n_nodes * nq * v.B * 4;
+  const int64_t image_stride = v.n_fgroups * v.image_int4s * 2;  // int2 between a node's group images
+  for (int64_t u = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; u < units; u += (int64_t)gridDim.x * blockDim.x) {
+    const int fi = (int)(u & 3);
+    int64_t r = u >> 2;
+    const int s = (int)(r % v.B);
+    r /= v.B;
+    const int qd = (int)(r % nq);
+    const int n = (int)(r / nq);
+    const int f = qd * 4 + fi;
+    if (f >= n_features) continue;
+    const int32_t g0 = v.group_prefix[n], g1 = v.group_prefix[n + 1];
+    const int2 *cell = image_cell(v, g0, f, item_feats, s);
+    int64_t g = 0, h = 0;
+    for (int32_t k = g0; k < g1; ++k, cell += image_stride) {
+      const int2 x = __ldcg(cell);
+      g += x.x;
+      h += x.y;
+    }
+    reinterpret_cast<longlong2 *>(hist_out)[((int64_t)n * n_features + f) * v.B + s] = make_longlong2(g, h);
+  }
 }
 
 }  // namespace gbt

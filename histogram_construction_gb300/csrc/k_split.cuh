@@ -533,24 +533,13 @@ __global__ void __launch_bounds__(SCAN_THREADS) k_find(const int64_t *__restrict
 // Where the small sibling's histogram comes from in the level-finish kernel.
 struct SmallSource {
   const int64_t *hist;  // complete small histograms [n_pairs][F][B][2] (FROM_PARTIALS = false)
-  // chunk images of the level build (FROM_PARTIALS = true); the summed small
+  // group images of the level build (FROM_PARTIALS = true); the summed small
   // histogram is also written to `hist_out`
   PartialView view;
   int32_t item_feats;
   int32_t pad;
   int64_t *hist_out;
 };
-
-// Small sibling strip of feature f of pair p, slot s (int64 pair).
-template <bool FROM_PARTIALS>
-__device__ __forceinline__ longlong2 small_cell(const SmallSource &src, int p, int f, int s, int n_features, int B,
-                                                int nc, int64_t item0) {
-  if (!FROM_PARTIALS) {
-    return __ldg(reinterpret_cast<const longlong2 *>(src.hist) + ((int64_t)p * n_features + f) * B + s);
-  } else {
-    return sum_chunks(src.view, item0, nc, f % src.item_feats, s);
-  }
-}
 
 // Level finish: grid (ceil(F / 4), n_pairs), 8 warps. Warp w takes feature
 // blockIdx.x * 4 + (w & 3) of pair blockIdx.y; warps 0-3 form the small
@@ -580,24 +569,52 @@ __global__ void __launch_bounds__(SCAN_THREADS) k_level_finish(
                                   : nullptr;
   const longlong2 *Sin = FROM_PARTIALS ? Sout
                                        : reinterpret_cast<const longlong2 *>(src.hist) + ((int64_t)p * n_features + f) * B;
-  int nc = 0;
-  int64_t item0 = 0;
-  if (FROM_PARTIALS) {
-    nc = src.view.chunk_prefix[p + 1] - src.view.chunk_prefix[p];
-    item0 = (int64_t)src.view.chunk_prefix[p] * src.view.n_fgroups + f / src.item_feats;
-  }
   const bool active = f < n_features;
-  // phase A: small strip (warps 0-3), parent strip (warps 4-7)
-  if (active) {
-    if (side == 0) {
-      for (int s = lane; s < B; s += 32) {
-        const longlong2 c = small_cell<FROM_PARTIALS>(src, p, f, s, n_features, B, nc, item0);
-        if (FROM_PARTIALS) Sout[s] = c;
-        if (staged) sh.cells[warp][s] = c;
+  // phase A: small strips (warps 0-3), parent strips (warps 4-7)
+  if (side == 0) {
+    if (FROM_PARTIALS) {
+      // the 128 threads sum the group images of all four features: thread t
+      // takes feature t & 3 and slots (t >> 2) + 32 i, so each warp load
+      // covers 8 slots x 4 features (whole 32-byte sectors)
+      const int t = threadIdx.x, fi = t & 3, ff = blockIdx.x * 4 + fi;
+      if (ff < n_features) {
+        const int32_t g0 = src.view.group_prefix[p], g1 = src.view.group_prefix[p + 1];
+        const int64_t stride = src.view.n_fgroups * src.view.image_int4s * 2;
+        const int2 *img0 = image_cell(src.view, g0, ff, src.item_feats, 0);
+        const int64_t sstride = src.view.sbw;  // int2 between slots
+        longlong2 *So = reinterpret_cast<longlong2 *>(src.hist_out) + ((int64_t)p * n_features + ff) * B;
+        for (int s0 = t >> 2; s0 < B; s0 += 128) {
+          int64_t ag[4] = {0, 0, 0, 0}, ah[4] = {0, 0, 0, 0};
+          const int2 *img = img0;
+          for (int32_t k = g0; k < g1; ++k, img += stride) {
+            int2 x[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const int s = s0 + 32 * u;
+              x[u] = s < B ? __ldcg(img + s * sstride) : make_int2(0, 0);
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              ag[u] += x[u].x;
+              ah[u] += x[u].y;
+            }
+          }
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int s = s0 + 32 * u;
+            if (s < B) {
+              const longlong2 c = make_longlong2(ag[u], ah[u]);
+              So[s] = c;
+              if (staged) sh.cells[fi][s] = c;
+            }
+          }
+        }
       }
-    } else if (staged) {
-      for (int s = lane; s < B; s += 32) sh.cells[warp][s] = __ldg(P + s);
+    } else if (active && staged) {
+      for (int s = lane; s < B; s += 32) sh.cells[warp][s] = __ldg(Sin + s);
     }
+  } else if (active && staged) {
+    for (int s = lane; s < B; s += 32) sh.cells[warp][s] = __ldg(P + s);
   }
   __syncthreads();
   // phase B: large = parent - small
