@@ -222,19 +222,28 @@ __device__ __forceinline__ void load_row(const LevelParams &p, bool ident, int64
 // ----------------------------------------------------------------------------
 // u8 kernel: items of one 64-feature mirror tile, 16-feature sub-blocks.
 //
-// Lane l of a warp takes row rho = l/4 of an 8-row group and byte word
-// w = l%4 of each 16-byte quarter of the row's strip (one 32-bit load per
-// sub-block). In atomic instruction (sb, j, c) the lane adds byte
-// jj = (j + rho/2) & 3 of its word of quarter sb, i.e. feature f = 4w + jj of
-// sub-block sb, component (c ^ (rho & 1)) (0 = G, 1 = H). Cells are
-// [slot][16][G, H]: a slot row is 128 bytes = 32 banks, so the bank of a lane
-// is 2f + comp, distinct for the 32 lanes of every instruction.
-constexpr int H8_THREADS = 1024;
+// Shared layout: sub-block sb (features 16 sb .. 16 sb + 15) is a [slot][16]
+// array of (G, H) int32 pairs (128-byte slot rows) starting at byte
+// sb * (32 KB + 32): consecutive sub-blocks are staggered by 8 banks.
+//
+// Lane l of a warp takes row rho = l/4 of an 8-row group and the 16-byte
+// quarter w = l%4 of the row's strip, i.e. sub-block w, with one 128-bit load.
+// In atomic instruction (e, j, c) the lane adds byte jj = (j + rho/2) & 3 of
+// word e of its quarter (feature f = 4e + jj of sub-block w) for component
+// c ^ (rho & 1) (0 = G, 1 = H). Its bank is (8w + 8e + 2jj + comp) mod 32:
+// distinct over the 32 lanes, whatever the bin values. Per entry the lane
+// spends one byte permute (slot), one multiply-add (cell address; 32e is an
+// immediate offset), one xor (the other component) and two shared reductions.
+//
+// The gathers of the next U row groups (row ids one step further ahead) are
+// in flight while the current groups' reductions issue. Rows past the chunk
+// end or with an invalid id add zeros to slot 0, so the loop has no branches.
 constexpr int H8_SB = 4;                                   // sub-blocks per tile
-constexpr int H8_SB_BYTES = 256 * 16 * 8;                  // 32 KB
-constexpr int H8_HIST_BYTES = H8_SB * H8_SB_BYTES;         // 128 KB
-constexpr int H8_SMEM = H8_HIST_BYTES;
-constexpr int H8_UNROLL = 4;
+constexpr int H8_SB_BYTES = 256 * 16 * 8;                  // 32 KB of cells per sub-block
+constexpr int H8_SB_STRIDE = H8_SB_BYTES + 32;             // shared bytes between sub-blocks
+constexpr int H8_SMEM = H8_SB * H8_SB_STRIDE;
+constexpr int H8_THREADS = 1024;
+constexpr int H8_U = 2;                                    // 8-row groups per warp step
 
 struct Hist8Params {
   LevelParams lv;
@@ -243,9 +252,64 @@ struct Hist8Params {
   int32_t n_slots;        // B
 };
 
+// Gathered operands of U row groups of one lane.
+template <int U>
+struct H8Stage {
+  uint4 bw[U];            // the lane's 16-byte quarter of each row's strip
+  uint32_t v0[U], v1[U];  // (qg, qh) in the lane's component order
+};
+
+template <int U>
+__device__ __forceinline__ void h8_rows(const LevelParams &p, bool ident, int64_t k, int64_t step, int64_t k1,
+                                        int32_t (&rid)[U]) {
+#pragma unroll
+  for (int u = 0; u < U; ++u) {
+    const int64_t kk = k + u * step;
+    rid[u] = kk < k1 ? (ident ? (int32_t)kk : __ldg(p.rows + kk)) : -1;
+  }
+}
+
+template <int U>
+__device__ __forceinline__ void h8_gather(const LevelParams &p, const unsigned char *strip, bool lane_on, int par,
+                                          const int32_t (&rid)[U], H8Stage<U> &st, uint32_t &bad) {
+#pragma unroll
+  for (int u = 0; u < U; ++u) {
+    const int32_t r = rid[u];
+    const bool valid = (uint32_t)r < (uint32_t)p.n_rows;
+    bad |= (r >= 0 && !valid) ? 1u : 0u;
+    int2 qv = make_int2(0, 0);
+    if (valid) qv = __ldg(p.q + r);
+    st.bw[u] = (valid && lane_on) ? ldg_nc_v4(strip + (int64_t)r * MIRROR_STRIP_BYTES) : make_uint4(0, 0, 0, 0);
+    st.v0[u] = (uint32_t)(par ? qv.y : qv.x);
+    st.v1[u] = (uint32_t)(par ? qv.x : qv.y);
+  }
+}
+
+template <int E>
+__device__ __forceinline__ void h8_word(uint32_t word, const uint32_t (&sel)[4], const uint32_t (&cj)[4], uint32_t v0,
+                                        uint32_t v1) {
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint32_t a = __byte_perm(word, 0u, sel[j]) * 128u + cj[j];
+    asm volatile("red.shared.add.u32 [%0+%2], %1;" ::"r"(a), "r"(v0), "n"(32 * E) : "memory");
+    asm volatile("red.shared.add.u32 [%0+%2], %1;" ::"r"(a ^ 4u), "r"(v1), "n"(32 * E) : "memory");
+  }
+}
+
+template <int U>
+__device__ __forceinline__ void h8_scatter(const H8Stage<U> &st, const uint32_t (&sel)[4], const uint32_t (&cj)[4]) {
+#pragma unroll
+  for (int u = 0; u < U; ++u) {
+    h8_word<0>(st.bw[u].x, sel, cj, st.v0[u], st.v1[u]);
+    h8_word<1>(st.bw[u].y, sel, cj, st.v0[u], st.v1[u]);
+    h8_word<2>(st.bw[u].z, sel, cj, st.v0[u], st.v1[u]);
+    h8_word<3>(st.bw[u].w, sel, cj, st.v0[u], st.v1[u]);
+  }
+}
+
 __global__ void __launch_bounds__(H8_THREADS, 1) k_hist_u8(Hist8Params P) {
+  constexpr int U = H8_U;
   extern __shared__ __align__(128) unsigned char smem[];
-  uint32_t *hist = reinterpret_cast<uint32_t *>(smem);
   __shared__ int32_t s_item;
 
   const LevelParams &p = P.lv;
@@ -260,15 +324,14 @@ __global__ void __launch_bounds__(H8_THREADS, 1) k_hist_u8(Hist8Params P) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
   const int rho = lane >> 2, w = lane & 3;
   const int pr = rho >> 1, par = rho & 1;
-  uint32_t shift[4], colb[4];
+  const uint32_t hist_base = smem_addr(smem);
+  uint32_t sel[4], cj[4];
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
     const int jj = (j + pr) & 3;
-    shift[j] = 8u * jj;
-    colb[j] = (uint32_t)(4 * w + jj) * 8u;
+    sel[j] = 0x4440u | (uint32_t)jj;  // byte jj, zero-extended
+    cj[j] = hist_base + (uint32_t)(w * H8_SB_STRIDE) + (uint32_t)jj * 8u + (par ? 4u : 0u);
   }
-  const uint32_t off0 = par ? 4u : 0u, off1 = par ? 0u : 4u;
-  const uint32_t hist_base = smem_addr(hist);
   uint32_t bad = 0;
 
   for (;;) {
@@ -279,47 +342,36 @@ __global__ void __launch_bounds__(H8_THREADS, 1) k_hist_u8(Hist8Params P) {
     const Item it = decode_item(id, p, chunk, cpg);
     const int f_tile0 = it.fgroup * 64;
     const int nsb = min(H8_SB, (P.n_features - f_tile0 + 15) >> 4);
-    {
-      uint4 *h4 = reinterpret_cast<uint4 *>(hist);
-      const int n4 = nsb * (H8_SB_BYTES / 16);  // (rows beyond B are never read back)
-      for (int i = threadIdx.x; i < n4; i += blockDim.x) h4[i] = make_uint4(0, 0, 0, 0);
+    // zero the slot rows that will be read back: B rows of each used sub-block
+    // (lanes of unused sub-blocks add into their own, never read, sub-block)
+    for (int sb = 0; sb < nsb; ++sb) {
+      uint4 *h4 = reinterpret_cast<uint4 *>(smem + sb * H8_SB_STRIDE);
+      for (int i = threadIdx.x; i < B * 8; i += blockDim.x) h4[i] = make_uint4(0, 0, 0, 0);
     }
     __syncthreads();
-    const unsigned char *strip = P.mirror + (int64_t)it.fgroup * N * MIRROR_STRIP_BYTES + w * 4;
-    const int64_t step = (int64_t)8 * nwarps;
-    for (int64_t g0 = it.k0 + 8 * warp; g0 < it.k1; g0 += step * H8_UNROLL) {
-      int32_t rr[H8_UNROLL], vg[H8_UNROLL], vh[H8_UNROLL];
-#pragma unroll
-      for (int u = 0; u < H8_UNROLL; ++u) load_row(p, ident, g0 + u * step + rho, it.k1, rr[u], vg[u], vh[u], bad);
-      uint32_t bw[H8_UNROLL][H8_SB];
-#pragma unroll
-      for (int u = 0; u < H8_UNROLL; ++u)
-#pragma unroll
-        for (int sb = 0; sb < H8_SB; ++sb)
-          bw[u][sb] = (rr[u] >= 0 && sb < nsb)
-                          ? __ldg(reinterpret_cast<const uint32_t *>(strip + (int64_t)rr[u] * MIRROR_STRIP_BYTES +
-                                                                     sb * 16))
-                          : 0u;
-#pragma unroll
-      for (int u = 0; u < H8_UNROLL; ++u) {
-        if (rr[u] < 0) continue;
-        const uint32_t v0 = par ? (uint32_t)vh[u] : (uint32_t)vg[u];
-        const uint32_t v1 = par ? (uint32_t)vg[u] : (uint32_t)vh[u];
-#pragma unroll
-        for (int sb = 0; sb < H8_SB; ++sb) {
-          if (sb >= nsb) break;
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const uint32_t slot = (bw[u][sb] >> shift[j]) & 0xffu;
-            const uint32_t a = hist_base + sb * H8_SB_BYTES + slot * 128u + colb[j];
-            asm volatile("red.shared.add.u32 [%0], %1;" ::"r"(a + off0), "r"(v0) : "memory");
-            asm volatile("red.shared.add.u32 [%0], %1;" ::"r"(a + off1), "r"(v1) : "memory");
-          }
-        }
+    const bool lane_on = w < nsb;
+    const unsigned char *strip = P.mirror + (int64_t)it.fgroup * N * MIRROR_STRIP_BYTES + w * 16;
+    const int64_t step = (int64_t)8 * nwarps;  // rows between a warp's consecutive groups
+    const int64_t adv = step * U;              // rows per warp step
+    int64_t g0 = it.k0 + 8 * warp + rho;
+    int32_t rid[U];
+    H8Stage<U> cur, nxt;
+    h8_rows<U>(p, ident, g0, step, it.k1, rid);
+    h8_gather<U>(p, strip, lane_on, par, rid, cur, bad);
+    h8_rows<U>(p, ident, g0 + adv, step, it.k1, rid);
+    // lanes of a warp run out of rows within one group of each other; any
+    // lane with work keeps the warp going (the others add zeros)
+    while (__any_sync(0xffffffffu, g0 < it.k1)) {
+      if (__any_sync(0xffffffffu, g0 + adv < it.k1)) {
+        h8_gather<U>(p, strip, lane_on, par, rid, nxt, bad);
+        h8_rows<U>(p, ident, g0 + 2 * adv, step, it.k1, rid);
       }
+      h8_scatter<U>(cur, sel, cj);
+      cur = nxt;
+      g0 += adv;
     }
     __syncthreads();
-    // flush: the item's shared image ([sub-block][slot][16][G, H] int32)
+    // flush: the item's shared image (per sub-block [slot][16][G, H] int32)
     // leaves as is, one TMA bulk operation per sub-block: a store when the
     // item is its group's only chunk, else a reduce-add into the zeroed
     // group image (exact: the group's int32 sums cannot overflow)
@@ -329,7 +381,7 @@ __global__ void __launch_bounds__(H8_THREADS, 1) k_hist_u8(Hist8Params P) {
       int32_t *img_out = p.partial + it.image * p.image_int4s * 4;
       for (int sb = 0; sb < nsb; ++sb) {
         int32_t *dst = img_out + (int64_t)sb * B * 16 * 2;
-        const int32_t *src = reinterpret_cast<const int32_t *>(hist) + sb * (H8_SB_BYTES / 4);
+        const unsigned char *src = smem + sb * H8_SB_STRIDE;
         if (it.multi) bulk_reduce_add_u32(dst, src, (uint32_t)B * 128u);
         else bulk_store(dst, src, (uint32_t)B * 128u);
       }

@@ -118,6 +118,54 @@ __device__ __forceinline__ float parent_f32(int64_t tg, int64_t th, const SplitP
   return __int_as_float(0x7fc00000);  // NaN: screen_f32 then yields an infinite bound
 }
 
+// Signed 64-bit integer -> float for |x| < 2^45: x = hi * 2^23 + lo with
+// hi = x >> 23 in [-2^22, 2^22) and lo in [0, 2^23), both converted exactly
+// by magic-number constructions (1.5 * 2^23 and 2^23); the FMA rounds once,
+// so the relative error is at most u = 2^-24.
+__device__ __forceinline__ float i45_to_f32(int64_t x) {
+  const int32_t hi = (int32_t)(x >> 23);
+  const uint32_t lo = (uint32_t)x & 0x7FFFFFu;
+  const float fh = __fsub_rn(__int_as_float(0x4B400000 + hi), 12582912.0f);
+  const float fl = __fsub_rn(__int_as_float(0x4B000000u | lo), 8388608.0f);
+  return __fmaf_rn(fh, 8388608.0f, fl);
+}
+
+// Whether every candidate of a strip can use screen_fast: all its quantised
+// sums are below 2^45 in magnitude (|G| sums are bounded by sabs, the sum of
+// |G| over the strip's slots, H sums by th) and every float quantity the
+// screen forms stays within [2^-59, 2^59] or is zero: nonzero |gl| >= inv_sg,
+// denominators in [inv_sh + lambda, th * inv_sh + lambda] (valid candidates
+// have H >= h_min >= 1 on both sides), terms a, b in
+// [inv_sg^2 / dmax, gmax^2 / dmin]. The error analysis of screen_f32 then
+// holds for every candidate without per-candidate checks.
+__device__ __forceinline__ bool strip_fast(int64_t sabs, int64_t th, float Gf2den, const SplitParams &sp) {
+  if (!sp.filter || sabs >= (1LL << 45) || th >= (1LL << 45) || !(Gf2den == Gf2den)) return false;
+  const float rlo = 1.7347234759768071e-18f, rhi = 5.764607523034235e+17f;  // 2^-59, 2^59
+  const float gmax = __fmul_rn(i45_to_f32(sabs), sp.inv_sg_f);
+  const float dmax = __fadd_rn(__fmul_rn(i45_to_f32(th), sp.inv_sh_f), sp.lambda_f);
+  const float dmin = __fadd_rn(sp.inv_sh_f, sp.lambda_f);
+  const float amax = __fdiv_rn(__fmul_rn(gmax, gmax), dmin);
+  const float amin = __fdiv_rn(__fmul_rn(sp.inv_sg_f, sp.inv_sg_f), dmax);
+  return sp.inv_sg_f > rlo && dmin > rlo && gmax < rhi && dmax < rhi && amax < rhi && amin > rlo &&
+         __fadd_rn(__fmul_rn(3.0f, amax), sp.gamma_abs_f) < rhi;
+}
+
+// screen_f32 for a strip that passed strip_fast (same bound, no range checks).
+__device__ __forceinline__ void screen_fast(int64_t GL, int64_t HL, int64_t GR, int64_t HR, float Gf2den,
+                                            const SplitParams &sp, float &up, float &lo) {
+  const float gl = __fmul_rn(i45_to_f32(GL), sp.inv_sg_f);
+  const float hl = __fmul_rn(i45_to_f32(HL), sp.inv_sh_f);
+  const float gr = __fmul_rn(i45_to_f32(GR), sp.inv_sg_f);
+  const float hr = __fmul_rn(i45_to_f32(HR), sp.inv_sh_f);
+  const float a = __fdividef(__fmul_rn(gl, gl), __fadd_rn(hl, sp.lambda_f));
+  const float b = __fdividef(__fmul_rn(gr, gr), __fadd_rn(hr, sp.lambda_f));
+  const float ab = __fadd_rn(a, b);
+  const float g = __fsub_rn(__fmul_rn(0.5f, __fsub_rn(ab, Gf2den)), sp.gamma_f);
+  const float err = __fmul_rn(__fadd_rn(__fadd_rn(ab, Gf2den), sp.gamma_abs_f), 1.9073486328125e-06f);  // 2^-19
+  up = __fadd_rn(g, err);
+  lo = __fsub_rn(g, err);
+}
+
 __device__ __forceinline__ int64_t shfl_i64(int64_t v, int src) {
   return (int64_t)__shfl_sync(0xffffffffu, (long long)v, src);
 }
@@ -145,6 +193,15 @@ __device__ __forceinline__ void warp_sum2(int64_t &a, int64_t &b) {
   for (int o = 16; o > 0; o >>= 1) {
     a += shfl_xor_i64(a, o);
     b += shfl_xor_i64(b, o);
+  }
+}
+
+__device__ __forceinline__ void warp_sum3(int64_t &a, int64_t &b, int64_t &c) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    a += shfl_xor_i64(a, o);
+    b += shfl_xor_i64(b, o);
+    c += shfl_xor_i64(c, o);
   }
 }
 
@@ -248,6 +305,7 @@ struct Surv {
 constexpr int SCAN_THREADS = 256;
 constexpr int SCAN_WARPS = SCAN_THREADS / 32;
 constexpr int SURV_CAP = 256;
+constexpr int SCAN_SPL = 4;  // consecutive slots per lane in the warp scan
 constexpr int STAGE_SLOTS = 256;  // strips with B <= 256 are staged in shared memory
 
 struct ScanShared {
@@ -263,72 +321,90 @@ struct ScanShared {
 };
 
 // Warp scan of one strip of `cells` (shared or global memory; missing cell at
-// n_bins) with totals (tg, th): screens every candidate, keeps a running best
-// lower bound, pushes the candidates that reach it into the CTA pool.
+// n_bins) with totals (tg, th) and sabs = sum of |G| over its slots: screens
+// every candidate and pushes into the CTA pool those whose upper bound reaches
+// the best lower bound seen so far. Lane l takes the SCAN_SPL consecutive
+// slots of each (32 * SCAN_SPL)-slot chunk: prefix sums run in registers,
+// with one warp scan of the lane totals per chunk.
 __device__ __forceinline__ float warp_scan_push(const longlong2 *cells, int n_bins, int64_t tg, int64_t th,
-                                                const SplitParams &sp, int f, int node, ScanShared &sh,
+                                                int64_t sabs, const SplitParams &sp, int f, int node, ScanShared &sh,
                                                 int &overflow) {
   const int lane = threadIdx.x & 31;
   const longlong2 m = cells[n_bins];
   const bool no_missing = (m.x == 0 && m.y == 0);
   const float Gf2den = parent_f32(tg, th, sp);
+  const bool fast = strip_fast(sabs, th, Gf2den, sp);
   float run_lo = -INFINITY;
-  int64_t cg = 0, ch = 0;
-  for (int s0 = 0; s0 < n_bins; s0 += 32) {
-    const int s = s0 + lane;
-    int64_t pg = 0, ph = 0;
-    if (s < n_bins) {
-      const longlong2 c = cells[s];
-      pg = c.x;
-      ph = c.y;
-    }
-    warp_incl_scan(pg, ph);
-    pg += cg;
-    ph += ch;
-    cg = shfl_i64(pg, 31);
-    ch = shfl_i64(ph, 31);
-    float up[2], lo[2];
-    bool valid[2];
+  int64_t carry_g = 0, carry_h = 0;
+  for (int c0 = 0; c0 < n_bins; c0 += 32 * SCAN_SPL) {
+    int64_t pg[SCAN_SPL], ph[SCAN_SPL];
+    int64_t ag = 0, ah = 0;
 #pragma unroll
-    for (int dir = 0; dir < 2; ++dir) {
-      const int64_t GL = pg + (dir ? m.x : 0), HL = ph + (dir ? m.y : 0);
-      const int64_t HR = th - HL;
-      // with an empty missing slot both directions give the same sums, and
-      // missing-right comes first: the left direction can never win
-      valid[dir] = s < n_bins && HL >= sp.h_min && HR >= sp.h_min && !(dir && no_missing);
-      up[dir] = -INFINITY;
-      lo[dir] = -INFINITY;
-      if (valid[dir]) {
-        if (sp.filter) {
-          screen_f32(GL, HL, tg - GL, HR, Gf2den, sp, up[dir], lo[dir]);
-        } else {
-          up[dir] = INFINITY;
+    for (int i = 0; i < SCAN_SPL; ++i) {
+      const int s = c0 + SCAN_SPL * lane + i;
+      longlong2 c = make_longlong2(0, 0);
+      if (s < n_bins) c = cells[s];
+      ag += c.x;
+      ah += c.y;
+      pg[i] = ag;
+      ph[i] = ah;
+    }
+    int64_t eg = ag, eh = ah;
+    warp_incl_scan(eg, eh);
+    const int64_t tot_g = shfl_i64(eg, 31), tot_h = shfl_i64(eh, 31);
+    eg += carry_g - ag;  // exclusive prefix of the lane's first slot
+    eh += carry_h - ah;
+    carry_g += tot_g;
+    carry_h += tot_h;
+    float up[SCAN_SPL][2];
+    uint32_t vmask = 0;
+    float l = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < SCAN_SPL; ++i) {
+      const int s = c0 + SCAN_SPL * lane + i;
+#pragma unroll
+      for (int dir = 0; dir < 2; ++dir) {
+        const int64_t GL = eg + pg[i] + (dir ? m.x : 0), HL = eh + ph[i] + (dir ? m.y : 0);
+        const int64_t HR = th - HL;
+        // with an empty missing slot both directions give the same sums, and
+        // missing-right comes first: the left direction can never win
+        const bool valid = s < n_bins && HL >= sp.h_min && HR >= sp.h_min && !(dir && no_missing);
+        float u = -INFINITY, lw = -INFINITY;
+        if (valid) {
+          if (fast) screen_fast(GL, HL, tg - GL, HR, Gf2den, sp, u, lw);
+          else if (sp.filter) screen_f32(GL, HL, tg - GL, HR, Gf2den, sp, u, lw);
+          else u = INFINITY;
+          vmask |= 1u << (2 * i + dir);
         }
+        up[i][dir] = u;
+        l = fmaxf(l, lw);
       }
     }
-    float l = fmaxf(lo[0], lo[1]);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) l = fmaxf(l, __shfl_xor_sync(0xffffffffu, l, o));
     run_lo = fmaxf(run_lo, l);
 #pragma unroll
-    for (int dir = 0; dir < 2; ++dir) {
-      if (!valid[dir] || up[dir] < run_lo) continue;
-      const int idx = atomicAdd(&sh.n, 1);
-      if (idx >= SURV_CAP) {
-        overflow = 1;
-        continue;
+    for (int i = 0; i < SCAN_SPL; ++i) {
+#pragma unroll
+      for (int dir = 0; dir < 2; ++dir) {
+        if (!((vmask >> (2 * i + dir)) & 1u) || up[i][dir] < run_lo) continue;
+        const int idx = atomicAdd(&sh.n, 1);
+        if (idx >= SURV_CAP) {
+          overflow = 1;
+          continue;
+        }
+        Surv v;
+        v.gl = eg + pg[i] + (dir ? m.x : 0);
+        v.hl = eh + ph[i] + (dir ? m.y : 0);
+        v.tg = tg;
+        v.th = th;
+        v.up = up[i][dir];
+        v.t = c0 + SCAN_SPL * lane + i;
+        v.f = f;
+        v.dir = (int16_t)dir;
+        v.node = (int16_t)node;
+        sh.pool[idx] = v;
       }
-      Surv v;
-      v.gl = pg + (dir ? m.x : 0);
-      v.hl = ph + (dir ? m.y : 0);
-      v.tg = tg;
-      v.th = th;
-      v.up = up[dir];
-      v.t = s;
-      v.f = f;
-      v.dir = (int16_t)dir;
-      v.node = (int16_t)node;
-      sh.pool[idx] = v;
     }
   }
   return run_lo;
@@ -480,7 +556,7 @@ __device__ __forceinline__ void scan_init(ScanShared &sh) {
 // Find: grid (ceil(F / SCAN_WARPS), n_nodes); warp w scans feature
 // blockIdx.x * SCAN_WARPS + w of node blockIdx.y; the last CTA of a node
 // writes its split.
-__global__ void __launch_bounds__(SCAN_THREADS) k_find(const int64_t *__restrict__ hist, int32_t n_features,
+__global__ void __launch_bounds__(SCAN_THREADS, 3) k_find(const int64_t *__restrict__ hist, int32_t n_features,
                                                        int32_t n_bins, SplitParams sp, Cand *__restrict__ cand,
                                                        uint32_t *__restrict__ counters, SplitOut *__restrict__ out) {
   __shared__ ScanShared sh;
@@ -494,16 +570,18 @@ __global__ void __launch_bounds__(SCAN_THREADS) k_find(const int64_t *__restrict
   const longlong2 *cells = staged ? sh.cells[warp] : strip;
   int64_t tg = 0, th = 0;
   if (f < n_features) {
+    int64_t sa = 0;
     for (int s = lane; s < B; s += 32) {
       const longlong2 c = __ldg(strip + s);
       if (staged) sh.cells[warp][s] = c;
       tg += c.x;
       th += c.y;
+      sa += c.x < 0 ? -c.x : c.x;
     }
-    warp_sum2(tg, th);
+    warp_sum3(tg, th, sa);
     __syncwarp();
     int ovf = 0;
-    const float wlo = warp_scan_push(cells, n_bins, tg, th, sp, f, 0, sh, ovf);
+    const float wlo = warp_scan_push(cells, n_bins, tg, th, sa, sp, f, 0, sh, ovf);
     ovf = __any_sync(0xffffffffu, ovf);
     if (lane == 0) {
       sh.warp_lo[warp] = wlo;
@@ -548,7 +626,7 @@ struct SmallSource {
 // Small (written out). Every warp then scans its strip; the last CTA of pair
 // p writes small_out[p] and large_out[p].
 template <bool FROM_PARTIALS>
-__global__ void __launch_bounds__(SCAN_THREADS) k_level_finish(
+__global__ void __launch_bounds__(SCAN_THREADS, 3) k_level_finish(
     SmallSource src, const int64_t *__restrict__ parent, const int32_t *__restrict__ parent_of,
     int64_t *__restrict__ large, int32_t n_features, int32_t n_bins, SplitParams sp, Cand *__restrict__ cand,
     uint32_t *__restrict__ counters, SplitOut *__restrict__ small_out, SplitOut *__restrict__ large_out,
@@ -635,14 +713,16 @@ __global__ void __launch_bounds__(SCAN_THREADS) k_level_finish(
   const longlong2 *cells = staged ? sh.cells[warp] : (side ? L : Sin);
   int64_t tg = 0, th = 0;
   if (active) {
+    int64_t sa = 0;
     for (int s = lane; s < B; s += 32) {
       const longlong2 c = cells[s];
       tg += c.x;
       th += c.y;
+      sa += c.x < 0 ? -c.x : c.x;
     }
-    warp_sum2(tg, th);
+    warp_sum3(tg, th, sa);
     int ovf = 0;
-    const float wlo = warp_scan_push(cells, n_bins, tg, th, sp, f, side, sh, ovf);
+    const float wlo = warp_scan_push(cells, n_bins, tg, th, sa, sp, f, side, sh, ovf);
     ovf = __any_sync(0xffffffffu, ovf);
     if (lane == 0) {
       sh.warp_lo[warp] = wlo;
