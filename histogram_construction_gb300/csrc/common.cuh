@@ -27,6 +27,14 @@ struct DevState {
 };
 
 constexpr int MIRROR_STRIP_BYTES = 64;  // bytes per row per mirror tile of features
+constexpr int MIRROR_ROW_BYTES = 128;   // a tile pair's row: tiles 2p and 2p + 1 side by side
+
+// Byte offset of row `row` of tile `tile` in the mirror [ceil(n_tiles / 2)][N][128]:
+// a gathered row of tile 2p and the same row of tile 2p + 1 share one 128-byte line,
+// so the two items that read them take one line from memory between them.
+__host__ __device__ __forceinline__ int64_t mirror_offset(int64_t tile, int64_t row, int64_t n_rows) {
+  return ((tile >> 1) * n_rows + row) * MIRROR_ROW_BYTES + (tile & 1) * MIRROR_STRIP_BYTES;
+}
 
 __device__ __forceinline__ void raise_err(DevState *st, uint32_t bit) { atomicOr(&st->err, bit); }
 

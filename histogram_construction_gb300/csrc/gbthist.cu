@@ -397,7 +397,7 @@ gbt_status gbt_upload_bins(gbt_ctx *c, const void *bins, int bin_bytes, int64_t 
   }
   const int tf = MIRROR_STRIP_BYTES / bin_bytes;
   const int n_tiles = (n_features + tf - 1) / tf;
-  const size_t mbytes = (size_t)n_tiles * (size_t)n_rows * MIRROR_STRIP_BYTES;
+  const size_t mbytes = (size_t)((n_tiles + 1) / 2) * (size_t)n_rows * MIRROR_ROW_BYTES;
   s = ensure(c, c->mirror, mbytes, "mirror allocation");
   if (s != GBT_OK) return s;
   c->bin_bytes = bin_bytes;

@@ -247,7 +247,7 @@ constexpr int H8_U = 2;                                    // 8-row groups per w
 
 struct Hist8Params {
   LevelParams lv;
-  const uint8_t *mirror;  // [n_tiles][N][64]
+  const uint8_t *mirror;  // tile pairs [ceil(n_tiles / 2)][N][128]
   int32_t n_features;
   int32_t n_slots;        // B
 };
@@ -279,7 +279,7 @@ __device__ __forceinline__ void h8_gather(const LevelParams &p, const unsigned c
     bad |= (r >= 0 && !valid) ? 1u : 0u;
     int2 qv = make_int2(0, 0);
     if (valid) qv = __ldg(p.q + r);
-    st.bw[u] = (valid && lane_on) ? ldg_nc_v4(strip + (int64_t)r * MIRROR_STRIP_BYTES) : make_uint4(0, 0, 0, 0);
+    st.bw[u] = (valid && lane_on) ? ldg_nc_v4(strip + (int64_t)r * MIRROR_ROW_BYTES) : make_uint4(0, 0, 0, 0);
     st.v0[u] = (uint32_t)(par ? qv.y : qv.x);
     st.v1[u] = (uint32_t)(par ? qv.x : qv.y);
   }
@@ -350,7 +350,7 @@ __global__ void __launch_bounds__(H8_THREADS, 1) k_hist_u8(Hist8Params P) {
     }
     __syncthreads();
     const bool lane_on = w < nsb;
-    const unsigned char *strip = P.mirror + (int64_t)it.fgroup * N * MIRROR_STRIP_BYTES + w * 16;
+    const unsigned char *strip = P.mirror + mirror_offset(it.fgroup, 0, N) + w * 16;
     const int64_t step = (int64_t)8 * nwarps;  // rows between a warp's consecutive groups
     const int64_t adv = step * U;              // rows per warp step
     int64_t g0 = it.k0 + 8 * warp + rho;
@@ -405,7 +405,7 @@ constexpr int H16_STAGE_BYTES = H16_STAGE_SLOTS * 8;
 
 struct Hist16Params {
   LevelParams lv;
-  const uint16_t *mirror;  // [n_tiles][N][32]
+  const uint16_t *mirror;  // tile pairs [ceil(n_tiles / 2)][N][2 x 32]
   int32_t n_features;
   int32_t n_slots;         // B
   int32_t n_bins;
@@ -453,7 +453,7 @@ __global__ void __launch_bounds__(H16_THREADS, 1) k_hist_u16(Hist16Params P) {
     const int tile = it.fgroup / GROUPS_PER_TILE;
     const int sub = it.fgroup % GROUPS_PER_TILE;
     const unsigned char *strip =
-        reinterpret_cast<const unsigned char *>(P.mirror) + (int64_t)tile * N * MIRROR_STRIP_BYTES + sub * TS * 2 + wi * 4;
+        reinterpret_cast<const unsigned char *>(P.mirror) + mirror_offset(tile, 0, N) + sub * TS * 2 + wi * 4;
     int32_t mg0 = 0, mh0 = 0, mg1 = 0, mh1 = 0;  // missing-slot partials of features 2wi, 2wi+1
     const int64_t step = (int64_t)RPI * nwarps;
     for (int64_t g0 = it.k0 + RPI * warp; g0 < it.k1; g0 += step * 4) {
@@ -464,7 +464,7 @@ __global__ void __launch_bounds__(H16_THREADS, 1) k_hist_u16(Hist16Params P) {
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         bw[u] = 0;
-        if (rr[u] >= 0) bw[u] = __ldg(reinterpret_cast<const uint32_t *>(strip + (int64_t)rr[u] * MIRROR_STRIP_BYTES));
+        if (rr[u] >= 0) bw[u] = __ldg(reinterpret_cast<const uint32_t *>(strip + (int64_t)rr[u] * MIRROR_ROW_BYTES));
       }
 #pragma unroll
       for (int u = 0; u < 4; ++u) {

@@ -60,7 +60,7 @@ __device__ __forceinline__ int part_flag(const PartParams &p, int64_t k, int32_t
   if (sp.feature < 0 || sp.feature >= p.n_features) return 1;  // no split (or an invalid one): all left
   if (r < 0 || r >= p.n_rows) return 1;
   const int64_t tile = sp.feature / p.tile_feats, fi = sp.feature % p.tile_feats;
-  const unsigned char *strip = p.mirror + (tile * p.n_rows + r) * MIRROR_STRIP_BYTES;
+  const unsigned char *strip = p.mirror + mirror_offset(tile, r, p.n_rows);
   const uint32_t slot = p.bin_bytes == 1 ? (uint32_t)strip[fi] : (uint32_t)reinterpret_cast<const uint16_t *>(strip)[fi];
   if (slot == (uint32_t)p.n_bins) return sp.default_left ? 1 : 0;
   return (int32_t)slot <= sp.bin ? 1 : 0;

@@ -6,8 +6,9 @@
 
 namespace gbt {
 
-// Feature-major [F][N] bins -> tiled row-major mirror [n_tiles][N][64 bytes]
-// holding histogram slots (bin, or n_bins for the missing sentinel).
+// Feature-major [F][N] bins -> tiled row-major mirror: 64-byte strips per
+// (tile, row), tiles paired into 128-byte rows (see mirror_offset), holding
+// histogram slots (bin, or n_bins for the missing sentinel).
 // The mirror is the column tiling of bonsai "E6. The wide-data wall",
 // "Epilogue": each row of a feature tile is one contiguous strip, so a node's
 // gathered rows read whole 64-byte strips instead of one byte per feature.
@@ -48,7 +49,9 @@ __global__ void __launch_bounds__(256) k_mirror(const T *__restrict__ bins, int6
   for (int i = threadIdx.x; i < TF * 64; i += blockDim.x) {
     const int rl = i / TF, fl = i % TF;
     const int64_t r = rl0 + rl;
-    if (r < rows_in_slab) mirror[(gtile * n_rows + row0 + r) * TF + fl] = sm[fl][rl];
+    if (r < rows_in_slab)
+      reinterpret_cast<T *>(reinterpret_cast<unsigned char *>(mirror) + mirror_offset(gtile, row0 + r, n_rows))[fl] =
+          sm[fl][rl];
   }
   if (bad) raise_err(st, ERRBIT_BIN);
 }
