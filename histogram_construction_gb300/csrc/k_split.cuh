@@ -206,13 +206,15 @@ __device__ __forceinline__ void warp_sum3(int64_t &a, int64_t &b, int64_t &c) {
 }
 
 // Candidate record (per CTA and node), 64 bytes, 16-byte aligned so that it
-// can be read back with four 16-byte loads.
+// can be read back with four 16-byte loads. An exact candidate carries its
+// double gain; a bounded one only the FP32 bounds lo <= gain <= up (for an
+// exact one they are the gain rounded down and up).
 struct __align__(16) Cand {
   double gain;
   int32_t t, dir;
-  int32_t f, pad;
+  int32_t f, exact;
   int64_t gl, hl, gr, hr;
-  int64_t pad2;
+  float up, lo;
 };
 static_assert(sizeof(Cand) == 64, "Cand is read as four 16-byte words");
 
@@ -230,10 +232,18 @@ __device__ __forceinline__ Cand no_cand() {
   c.t = INT32_MAX;
   c.dir = 1;
   c.f = INT32_MAX;
-  c.pad = 0;
+  c.exact = 1;
   c.gl = c.hl = c.gr = c.hr = 0;
-  c.pad2 = 0;
+  c.up = c.lo = -INFINITY;
   return c;
+}
+
+// Fills the bounds of an exact candidate from its double gain.
+__device__ __forceinline__ void set_exact(Cand &c, double gain) {
+  c.gain = gain;
+  c.exact = 1;
+  c.lo = __double2float_rd(gain);
+  c.up = __double2float_ru(gain);
 }
 
 // Total order of candidates: gain desc, then (feature, t, dir) asc.
@@ -256,8 +266,9 @@ __device__ __forceinline__ Cand shfl_xor_cand(const Cand &b, int o) {
   c.hl = shfl_xor_i64(b.hl, o);
   c.gr = shfl_xor_i64(b.gr, o);
   c.hr = shfl_xor_i64(b.hr, o);
-  c.pad = 0;
-  c.pad2 = 0;
+  c.exact = __shfl_xor_sync(0xffffffffu, b.exact, o);
+  c.up = __shfl_xor_sync(0xffffffffu, b.up, o);
+  c.lo = __shfl_xor_sync(0xffffffffu, b.lo, o);
   return c;
 }
 
@@ -295,7 +306,7 @@ __device__ __forceinline__ SplitOut cand_to_split(const Cand &best) {
 // A candidate that passed its warp's running screen.
 struct Surv {
   int64_t gl, hl, tg, th;
-  float up;
+  float up, lo;
   int32_t t;
   int32_t f;
   int16_t dir;
@@ -306,6 +317,7 @@ constexpr int SCAN_THREADS = 256;
 constexpr int SCAN_WARPS = SCAN_THREADS / 32;
 constexpr int SURV_CAP = 256;
 constexpr int SCAN_SPL = 4;  // consecutive slots per lane in the warp scan
+constexpr int PUB_K = 2;     // candidates a CTA publishes per node set before it resorts to double
 constexpr int STAGE_SLOTS = 256;  // strips with B <= 256 are staged in shared memory
 
 struct ScanShared {
@@ -315,7 +327,10 @@ struct ScanShared {
   float warp_lo[SCAN_WARPS];
   int warp_overflow[SCAN_WARPS];
   Cand extra[SCAN_WARPS];
-  Cand best[2];
+  Cand pub[2][PUB_K];
+  int sel[2][PUB_K];
+  int cnt[2];
+  float red[SCAN_WARPS];
   int n;
   uint32_t last;
 };
@@ -356,7 +371,7 @@ __device__ __forceinline__ float warp_scan_push(const longlong2 *cells, int n_bi
     eh += carry_h - ah;
     carry_g += tot_g;
     carry_h += tot_h;
-    float up[SCAN_SPL][2];
+    float up[SCAN_SPL][2], lo[SCAN_SPL][2];
     uint32_t vmask = 0;
     float l = -INFINITY;
 #pragma unroll
@@ -377,6 +392,7 @@ __device__ __forceinline__ float warp_scan_push(const longlong2 *cells, int n_bi
           vmask |= 1u << (2 * i + dir);
         }
         up[i][dir] = u;
+        lo[i][dir] = lw;
         l = fmaxf(l, lw);
       }
     }
@@ -399,6 +415,7 @@ __device__ __forceinline__ float warp_scan_push(const longlong2 *cells, int n_bi
         v.tg = tg;
         v.th = th;
         v.up = up[i][dir];
+        v.lo = lo[i][dir];
         v.t = c0 + SCAN_SPL * lane + i;
         v.f = f;
         v.dir = (int16_t)dir;
@@ -452,7 +469,7 @@ __device__ __forceinline__ Cand warp_direct_best(const longlong2 *cells, int n_b
       if (sp.filter) screen_f32(GL, HL, tg - GL, HR, Gf2den, sp, up, lo);
       if (up < thr) continue;
       Cand c;
-      c.gain = surv_gain(GL, HL, tg, th, sp);
+      set_exact(c, surv_gain(GL, HL, tg, th, sp));
       c.t = s;
       c.dir = dir;
       c.f = f;
@@ -460,86 +477,168 @@ __device__ __forceinline__ Cand warp_direct_best(const longlong2 *cells, int n_b
       c.hl = HL;
       c.gr = tg - GL;
       c.hr = th - HL;
-      c.pad = 0;
-      c.pad2 = 0;
       if (cand_better(c, best)) best = c;
     }
   }
   return warp_best_cand(best);
 }
 
-// Evaluate the pool in double (one survivor per thread, only those whose
-// upper bound reaches their node's threshold), then warp `node` forms the
-// CTA's best candidate of its node set (also over the overflow results of
-// the warps with warp_node[w] == node).
-__device__ __forceinline__ void pool_finish(ScanShared &sh, const SplitParams &sp, int n_sets, const float *thr,
-                                            const int *warp_node) {
+__device__ __forceinline__ Cand surv_cand(const Surv &v) {
+  Cand c;
+  c.gain = -INFINITY;
+  c.t = v.t;
+  c.dir = v.dir;
+  c.f = v.f;
+  c.exact = 0;
+  c.gl = v.gl;
+  c.hl = v.hl;
+  c.gr = v.tg - v.gl;
+  c.hr = v.th - v.hl;
+  c.up = v.up;
+  c.lo = v.lo;
+  return c;
+}
+
+// What a CTA publishes for each node set, after the scan and the overflow
+// pass (thr[set]: the set's best lower bound in the CTA). Candidates that can
+// still be the node's best are the pool survivors with up >= thr plus the
+// exact results of warps whose pushes overflowed the pool. Up to PUB_K of
+// them are published with their bounds, with no double work in this CTA;
+// with more, they are evaluated in double and the exact best is published.
+// All threads call it; sh.pub[set][0 .. PUB_K-1] holds the result.
+__device__ __forceinline__ void cta_select(ScanShared &sh, const SplitParams &sp, int n_sets, const float *thr,
+                                           const int *warp_node) {
   const int n = min(sh.n, SURV_CAP);
+  if (threadIdx.x < 2) sh.cnt[threadIdx.x] = 0;
+  __syncthreads();
   for (int i = threadIdx.x; i < n; i += blockDim.x) {
     const Surv &v = sh.pool[i];
-    sh.gain[i] = (v.up >= thr[v.node]) ? surv_gain(v.gl, v.hl, v.tg, v.th, sp) : -INFINITY;
+    if (v.up >= thr[v.node]) {
+      const int k = atomicAdd(&sh.cnt[v.node], 1);
+      if (k < PUB_K) sh.sel[v.node][k] = i;
+    }
+  }
+  if (threadIdx.x < SCAN_WARPS && sh.warp_overflow[threadIdx.x] && sh.extra[threadIdx.x].f != INT32_MAX) {
+    const int set = warp_node[threadIdx.x];
+    const int k = atomicAdd(&sh.cnt[set], 1);
+    if (k < PUB_K) sh.sel[set][k] = -1 - (int)threadIdx.x;
   }
   __syncthreads();
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (warp < n_sets) {
-    Cand best = no_cand();
-    for (int i = lane; i < n; i += 32) {
+  const bool dbl0 = sh.cnt[0] > PUB_K, dbl1 = n_sets > 1 && sh.cnt[1] > PUB_K;
+  if (dbl0 || dbl1) {
+    for (int i = threadIdx.x; i < n; i += blockDim.x) {
       const Surv &v = sh.pool[i];
-      if (v.node != warp || !(v.up >= thr[warp])) continue;
-      Cand c;
-      c.gain = sh.gain[i];
-      c.t = v.t;
-      c.dir = v.dir;
-      c.f = v.f;
-      c.gl = v.gl;
-      c.hl = v.hl;
-      c.gr = v.tg - v.gl;
-      c.hr = v.th - v.hl;
-      c.pad = 0;
-      c.pad2 = 0;
-      if (cand_better(c, best)) best = c;
+      const bool need = (v.node == 0 ? dbl0 : dbl1) && v.up >= thr[v.node];
+      sh.gain[i] = need ? surv_gain(v.gl, v.hl, v.tg, v.th, sp) : -INFINITY;
     }
-    for (int w = lane; w < SCAN_WARPS; w += 32)
-      if (warp_node[w] == warp && cand_better(sh.extra[w], best)) best = sh.extra[w];
-    best = warp_best_cand(best);
-    if (lane == 0) sh.best[warp] = best;
+    __syncthreads();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (warp < n_sets && (warp == 0 ? dbl0 : dbl1)) {
+      Cand best = no_cand();
+      for (int i = lane; i < n; i += 32) {
+        const Surv &v = sh.pool[i];
+        if (v.node != warp || !(v.up >= thr[warp])) continue;
+        Cand c = surv_cand(v);
+        set_exact(c, sh.gain[i]);
+        if (cand_better(c, best)) best = c;
+      }
+      for (int w = lane; w < SCAN_WARPS; w += 32)
+        if (warp_node[w] == warp && sh.warp_overflow[w] && cand_better(sh.extra[w], best)) best = sh.extra[w];
+      best = warp_best_cand(best);
+      if (lane < PUB_K) sh.pub[warp][lane] = lane == 0 ? best : no_cand();
+    }
+  }
+  if (threadIdx.x < n_sets * PUB_K) {
+    const int set = threadIdx.x / PUB_K, k = threadIdx.x % PUB_K;
+    if (!(set == 0 ? dbl0 : dbl1)) {
+      Cand c = no_cand();
+      if (k < sh.cnt[set]) {
+        const int i = sh.sel[set][k];
+        c = i >= 0 ? surv_cand(sh.pool[i]) : sh.extra[-1 - i];
+      }
+      sh.pub[set][k] = c;
+    }
   }
   __syncthreads();
 }
 
-// Reduce the per-CTA candidates of one node (n_cand, written by other CTAs)
-// with one warp and write its split.
-__device__ __forceinline__ void reduce_node_warp(const Cand *cand, int n_cand, SplitOut *out) {
-  const int lane = threadIdx.x & 31;
-  Cand best = no_cand();
-  for (int i = lane; i < n_cand; i += 32) {
-    Cand c;
-    const int4 *src = reinterpret_cast<const int4 *>(cand + i);  // L2 reads: written by other CTAs
-    int4 *dst = reinterpret_cast<int4 *>(&c);
+__device__ __forceinline__ Cand load_cand(const Cand *p) {
+  Cand c;
+  const int4 *src = reinterpret_cast<const int4 *>(p);  // L2 reads: written by other CTAs
+  int4 *dst = reinterpret_cast<int4 *>(&c);
 #pragma unroll
-    for (int k = 0; k < 4; ++k) dst[k] = __ldcg(src + k);
+  for (int k = 0; k < 4; ++k) dst[k] = __ldcg(src + k);
+  return c;
+}
+
+// Order-preserving key of a float (larger float, larger key; 0 is below every
+// finite or infinite value) for atomicMax over lower bounds.
+__device__ __forceinline__ uint32_t lo_key(float f) {
+  const uint32_t b = __float_as_uint(f);
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+__device__ __forceinline__ float key_lo(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
+// Node reduce over the n_ent published candidates of one node, by the `nthr`
+// threads t0 .. t0 + nthr - 1 (whole warps): candidates whose upper bound
+// reaches the node threshold (the best lower bound published for the node)
+// are evaluated in double (unless exact); the best by (gain desc, feature, t,
+// direction asc) becomes the node's split. `slot` (nthr / 32 entries of
+// shared memory) gathers the warp results.
+__device__ __forceinline__ void reduce_node(const Cand *cand, int n_ent, float thr, const SplitParams &sp,
+                                            SplitOut *out, int t0, int nthr, Cand *slot) {
+  const int t = threadIdx.x - t0, lane = threadIdx.x & 31, w = t >> 5;
+  Cand best = no_cand();
+  for (int i = t; i < n_ent; i += nthr) {
+    const int4 w3 = __ldcg(reinterpret_cast<const int4 *>(cand + i) + 3);  // hr, up, lo
+    if (!(__int_as_float(w3.z) >= thr)) continue;
+    Cand c = load_cand(cand + i);
+    if (c.f == INT32_MAX) continue;
+    if (!c.exact) set_exact(c, surv_gain(c.gl, c.hl, c.gl + c.gr, c.hl + c.hr, sp));
     if (cand_better(c, best)) best = c;
   }
   best = warp_best_cand(best);
-  if (lane == 0) *out = cand_to_split(best);
+  if (lane == 0) slot[w] = best;
+  named_sync(1 + t0 / 128, nthr);
+  if (w == 0) {
+    Cand b = lane < nthr / 32 ? slot[lane] : no_cand();
+    b = warp_best_cand(b);
+    if (lane == 0) *out = cand_to_split(b);
+  }
 }
 
-// Thread 0 stores the CTA's candidates and counts the CTA in; returns true in
-// the last CTA of the group (which resets the counter). No CTA waits.
+// Stores the CTA's published candidates (dst[set] + 0 .. PUB_K-1), raises the
+// node thresholds key[set] to the best published lower bound and counts the
+// CTA in; returns true in the last CTA of the group, which gets the node
+// thresholds in thr_out and resets the counter and the keys. No CTA waits.
 __device__ __forceinline__ bool cta_publish(ScanShared &sh, int n_sets, Cand *dst0, Cand *dst1, uint32_t *counter,
-                                            uint32_t group_ctas) {
-  if (threadIdx.x == 0) {
-    *dst0 = sh.best[0];
-    if (n_sets > 1) *dst1 = sh.best[1];
+                                            uint32_t *key0, uint32_t *key1, uint32_t group_ctas, float *thr_out) {
+  if (threadIdx.x < n_sets * PUB_K) {
+    const int set = threadIdx.x / PUB_K, k = threadIdx.x % PUB_K;
+    const Cand c = sh.pub[set][k];
+    (set == 0 ? dst0 : dst1)[k] = c;
+    if (c.f != INT32_MAX) atomicMax(set == 0 ? key0 : key1, lo_key(c.lo));
     __threadfence();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
     const uint32_t done = atomicAdd(counter, 1u);
     sh.last = (done == group_ctas - 1) ? 1u : 0u;
     if (sh.last) {
+      __threadfence();
+      const uint32_t k0 = atomicExch(key0, 0u);
+      const uint32_t k1 = n_sets > 1 ? atomicExch(key1, 0u) : 0u;
+      sh.red[0] = k0 ? key_lo(k0) : -INFINITY;
+      sh.red[1] = k1 ? key_lo(k1) : -INFINITY;
       *counter = 0;
       __threadfence();
     }
   }
   __syncthreads();
+  thr_out[0] = sh.red[0];
+  thr_out[1] = sh.red[1];
   return sh.last != 0;
 }
 
@@ -599,12 +698,14 @@ __global__ void __launch_bounds__(SCAN_THREADS, 3) k_find(const int64_t *__restr
   int warp_node[SCAN_WARPS];
 #pragma unroll
   for (int w = 0; w < SCAN_WARPS; ++w) warp_node[w] = 0;
-  pool_finish(sh, sp, 1, thr, warp_node);
+  cta_select(sh, sp, 1, thr, warp_node);
   const int nfb = gridDim.x;
-  Cand *cn = cand + (int64_t)node * nfb;
-  if (cta_publish(sh, 1, cn + blockIdx.x, nullptr, counters + node, nfb)) {
+  Cand *cn = cand + (int64_t)node * nfb * PUB_K;
+  float nthr[2];
+  uint32_t *key = counters + gridDim.y + node;  // node threshold keys follow the counters
+  if (cta_publish(sh, 1, cn + blockIdx.x * PUB_K, nullptr, counters + node, key, nullptr, nfb, nthr)) {
     __threadfence();
-    if (warp == 0) reduce_node_warp(cn, nfb, out + node);
+    reduce_node(cn, nfb * PUB_K, nthr[0], sp, out + node, 0, SCAN_THREADS, sh.extra);
   }
 }
 
@@ -740,14 +841,18 @@ __global__ void __launch_bounds__(SCAN_THREADS, 3) k_level_finish(
   int warp_node[SCAN_WARPS];
 #pragma unroll
   for (int w = 0; w < SCAN_WARPS; ++w) warp_node[w] = w >> 2;
-  pool_finish(sh, sp, 2, thr, warp_node);
+  cta_select(sh, sp, 2, thr, warp_node);
   const int nfb = gridDim.x;
-  Cand *cs_base = cand + (int64_t)(2 * p) * nfb;
-  Cand *cl_base = cand + (int64_t)(2 * p + 1) * nfb;
-  if (cta_publish(sh, 2, cs_base + blockIdx.x, cl_base + blockIdx.x, counters + p, nfb)) {
+  Cand *cs_base = cand + (int64_t)(2 * p) * nfb * PUB_K;
+  Cand *cl_base = cand + (int64_t)(2 * p + 1) * nfb * PUB_K;
+  float nthr[2];
+  uint32_t *key = counters + gridDim.y + 2 * p;  // node threshold keys follow the counters
+  if (cta_publish(sh, 2, cs_base + blockIdx.x * PUB_K, cl_base + blockIdx.x * PUB_K, counters + p, key, key + 1, nfb,
+                  nthr)) {
     __threadfence();
-    if (warp == 0) reduce_node_warp(cs_base, nfb, small_out + p);
-    if (warp == 1) reduce_node_warp(cl_base, nfb, large_out + p);
+    // warps 0-3 reduce the small sibling, warps 4-7 the large one
+    if (threadIdx.x < 128) reduce_node(cs_base, nfb * PUB_K, nthr[0], sp, small_out + p, 0, 128, sh.extra);
+    else reduce_node(cl_base, nfb * PUB_K, nthr[1], sp, large_out + p, 128, 128, sh.extra + 4);
   }
 }
 

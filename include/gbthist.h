@@ -170,7 +170,7 @@ gbt_status gbt_find_splits(gbt_ctx *ctx, const int64_t *hist, int32_t n_nodes, c
  *   out: DEVICE gbt_split [n_nodes] (no host staging: that would allocate).
  *   scale_g, scale_h: the scales the histogram was quantised with (> 0, finite).
  *   cuda_stream: a cudaStream_t of the calling thread's current device.
- * Scratch: one fixed 2 MiB + 16 KiB array inside the library, present on
+ * Scratch: one fixed 4 MiB + 32 KiB array inside the library, present on
  * every device that loads it until the process exits. Limits per call:
  * n_nodes <= 4096 and n_nodes * ceil(n_features / 8) <= 32768; beyond them
  * the call returns GBT_ERR_UNSUPPORTED before touching the device. The first
