@@ -12,6 +12,7 @@
 #include <map>
 #include <mutex>
 #include <string>
+#include <utility>
 #include <vector>
 
 #include "../../include/gbthist.h"
@@ -124,6 +125,24 @@ gbt_status cuda_fail(gbt_ctx *c, cudaError_t e, const char *what) {
     cudaError_t e_ = (expr);                    \
     if (e_ != cudaSuccess) return cuda_fail(c, e_, what); \
   } while (0)
+
+// Launch with programmatic stream serialization: the kernel may begin while
+// the previous kernel on the stream runs, and waits for it (pdl_wait) before
+// touching its results.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(gbt_ctx *c, void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = c->stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 cudaEvent_t prof_event(gbt_ctx *c) {
   if (!c->prof_pool.empty()) {
@@ -560,12 +579,10 @@ gbt_status run_level_build(gbt_ctx *c, const int32_t *rows, const int64_t *node_
   // image scratch for the largest item count the device plan can produce
   // (there are never more group images than items):
   // items <= n_fgroups * n_nodes + max(target_items, n_fgroups * n_rows / rows_per_chunk_min)
-  const int64_t rc = 2147483647LL / std::max<int64_t>(c->qmax, 1);
-  const int64_t chunk_floor = std::max<int64_t>(1, std::min<int64_t>(rc, CHUNK_MIN_ROWS));
-  const int64_t items_max = (int64_t)lp.n_fgroups * n_nodes +
-                            std::max<int64_t>(lp.target_items, (int64_t)lp.n_fgroups *
-                                                                   ((c->n_rows + chunk_floor - 1) / chunk_floor)) +
-                            lp.n_fgroups;
+  // (a chunk holds at least min(rc, load-balance target) rows, and rc >= 1024 by the quantisation limit)
+  const int64_t rc = std::max<int64_t>(1, 2147483647LL / std::max<int64_t>(c->qmax, 1));
+  const int64_t items_max = (int64_t)lp.n_fgroups * (n_nodes + 1) +
+                            std::max<int64_t>(lp.target_items, (int64_t)lp.n_fgroups * ((c->n_rows + rc - 1) / rc));
   if (items_max > INT32_MAX / 2) return fail(c, GBT_ERR_UNSUPPORTED, "level too large for the work-item plan");
   s = ensure(c, c->partial, (size_t)items_max * lp.image_int4s * 16, "level image scratch");
   if (s != GBT_OK) return s;
@@ -582,7 +599,7 @@ gbt_status run_level_build(gbt_ctx *c, const int32_t *rows, const int64_t *node_
     hp.n_features = c->n_features;
     hp.n_slots = B;
     prof_begin(c);
-    k_hist_u8<<<hist_ctas, H8_THREADS, H8_SMEM, c->stream>>>(hp);
+    launch_pdl(c, k_hist_u8, dim3(hist_ctas), dim3(H8_THREADS), H8_SMEM, hp);
     LAUNCH_CHECK(c, "k_hist_u8");
   } else {
     Hist16Params hp;
@@ -596,11 +613,11 @@ gbt_status run_level_build(gbt_ctx *c, const int32_t *rows, const int64_t *node_
     const int smem = hist_bytes + H16_STAGE_BYTES;
     prof_begin(c);
     switch (c->ts16) {
-      case 32: k_hist_u16<32><<<hist_ctas, H16_THREADS, smem, c->stream>>>(hp); break;
-      case 16: k_hist_u16<16><<<hist_ctas, H16_THREADS, smem, c->stream>>>(hp); break;
-      case 8: k_hist_u16<8><<<hist_ctas, H16_THREADS, smem, c->stream>>>(hp); break;
-      case 4: k_hist_u16<4><<<hist_ctas, H16_THREADS, smem, c->stream>>>(hp); break;
-      default: k_hist_u16<2><<<hist_ctas, H16_THREADS, smem, c->stream>>>(hp); break;
+      case 32: launch_pdl(c, k_hist_u16<32>, dim3(hist_ctas), dim3(H16_THREADS), smem, hp); break;
+      case 16: launch_pdl(c, k_hist_u16<16>, dim3(hist_ctas), dim3(H16_THREADS), smem, hp); break;
+      case 8: launch_pdl(c, k_hist_u16<8>, dim3(hist_ctas), dim3(H16_THREADS), smem, hp); break;
+      case 4: launch_pdl(c, k_hist_u16<4>, dim3(hist_ctas), dim3(H16_THREADS), smem, hp); break;
+      default: launch_pdl(c, k_hist_u16<2>, dim3(hist_ctas), dim3(H16_THREADS), smem, hp); break;
     }
     LAUNCH_CHECK(c, "k_hist_u16");
   }
@@ -639,8 +656,8 @@ gbt_status gbt_build_level(gbt_ctx *c, const int32_t *rows, const int64_t *node_
   if (s != GBT_OK) return s;
   prof_begin(c);
   const int64_t cells = (int64_t)n_nodes * ((c->n_features + 3) / 4) * 4 * (c->n_bins + 1);
-  k_finalize<<<grid_for(c, cells, 256, 8), 256, 0, c->stream>>>(partial_view(lp, c->n_bins + 1), n_nodes,
-                                                                 c->n_features, lp.item_feats, hist_out, c->st);
+  launch_pdl(c, k_finalize, dim3(grid_for(c, cells, 256, 8)), dim3(256), 0, partial_view(lp, c->n_bins + 1), n_nodes,
+             c->n_features, lp.item_feats, hist_out, (const DevState *)c->st);
   LAUNCH_CHECK(c, "k_finalize");
   return GBT_OK;
 }
@@ -743,9 +760,8 @@ gbt_status run_level_finish(gbt_ctx *c, const SmallSource &src, const int64_t *p
   if (s != GBT_OK) return s;
   const SplitParams sp = make_sp(c, params);
   prof_begin(c);
-  k_level_finish<FROM_PARTIALS><<<dim3(nfb, n_pairs), SCAN_THREADS, 0, c->stream>>>(
-      src, parent_hist, po, large_hist, c->n_features, c->n_bins, sp, (Cand *)c->cand.p, (uint32_t *)c->counters.p,
-      da, db, c->st);
+  launch_pdl(c, k_level_finish<FROM_PARTIALS>, dim3(nfb, n_pairs), dim3(SCAN_THREADS), 0, src, parent_hist, po,
+             large_hist, c->n_features, c->n_bins, sp, (Cand *)c->cand.p, (uint32_t *)c->counters.p, da, db, c->st);
   LAUNCH_CHECK(c, FROM_PARTIALS ? "k_level_finish" : "k_subtract_find");
   if (ha)
     CUDA_TRY(c, cudaMemcpyAsync(small_out, da, (size_t)n_pairs * sizeof(gbt_split), cudaMemcpyDeviceToHost, c->stream),

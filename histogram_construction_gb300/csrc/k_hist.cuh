@@ -85,6 +85,7 @@ __device__ __forceinline__ int64_t block_incl_scan(int64_t v, int64_t *s_warp) {
 constexpr int PLAN_THREADS = 1024;
 
 __global__ void __launch_bounds__(PLAN_THREADS) k_level_plan(LevelParams p) {
+  pdl_trigger();  // the histogram kernel may launch now; it waits for this grid to finish
   __shared__ int64_t s_warp[32];
   __shared__ int64_t s_zpre[PLAN_THREADS + 1];  // zero-unit prefix of the batch's nodes
   __shared__ int64_t s_zbase[PLAN_THREADS];     // first zeroed unit of each node of the batch
@@ -313,6 +314,8 @@ __global__ void __launch_bounds__(H8_THREADS, 1) k_hist_u8(Hist8Params P) {
   __shared__ int32_t s_item;
 
   const LevelParams &p = P.lv;
+  pdl_wait();     // the level plan
+  pdl_trigger();  // the consumer kernel may launch; it waits for this grid to finish
   if (!p.st->plan_ok) return;
   const int64_t chunk = p.st->chunk_rows;
   const int32_t cpg = p.st->chunks_per_group;
@@ -424,6 +427,8 @@ __global__ void __launch_bounds__(H16_THREADS, 1) k_hist_u16(Hist16Params P) {
   __shared__ int32_t s_item;
 
   const LevelParams &p = P.lv;
+  pdl_wait();     // the level plan
+  pdl_trigger();  // the consumer kernel may launch; it waits for this grid to finish
   if (!p.st->plan_ok) return;
   const int64_t chunk = p.st->chunk_rows;
   const int32_t cpg = p.st->chunks_per_group;
@@ -552,6 +557,7 @@ __device__ __forceinline__ const int2 *image_cell(const PartialView &v, int32_t 
 __global__ void __launch_bounds__(256) k_finalize(PartialView v, int32_t n_nodes, int32_t n_features,
                                                   int32_t item_feats, int64_t *__restrict__ hist_out,
                                                   const DevState *st) {
+  pdl_wait();  // the histogram kernel
   if (!st->plan_ok) return;
   const int nq = (n_features + 3) >> 2;
   const int64_t units = (int64_t)n_nodes * nq * v.B * 4;

@@ -733,6 +733,7 @@ __global__ void __launch_bounds__(SCAN_THREADS, 3) k_level_finish(
     uint32_t *__restrict__ counters, SplitOut *__restrict__ small_out, SplitOut *__restrict__ large_out,
     DevState *st) {
   __shared__ ScanShared sh;
+  pdl_wait();  // the histogram kernel (or whatever ran before on the stream)
   if (FROM_PARTIALS && !st->plan_ok) return;
   const int p = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
