@@ -219,6 +219,24 @@ def cpu_oracle_timing(w, budget_s=10.0, steps=None, warmup=0):
 
 
 # ----------------------------------------------------------------------------- GPU leg
+def aggregate_ranks(total_ms, e2e_value, world, dist=None, device=None):
+    """Whole-job timing over replicas: the slowest rank's timed total (MAX) and the
+    slowest rank's end-to-end rate (MIN per rank, times world). Every rank calls it."""
+    if dist is None or world == 1:
+        return total_ms, e2e_value
+    import torch
+    t = torch.tensor([total_ms], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    e = torch.tensor([e2e_value / world], device=device, dtype=torch.float64)
+    dist.all_reduce(e, op=dist.ReduceOp.MIN)
+    return float(t.item()), float(e.item()) * world
+
+
+def job_throughput(world, steps, entries_per_rank_step, total_ms):
+    """Units all ranks processed divided by the slowest rank's time (weak scaling)."""
+    return world * steps * entries_per_rank_step / (total_ms / 1e3)
+
+
 def run_gpu(args, rank, world, local_rank):
     import torch
 
@@ -368,20 +386,14 @@ def run_gpu(args, rank, world, local_rank):
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
         sess.close()
 
-    total_ms = sum(ms)
-    if dist is not None:
-        t = torch.tensor([total_ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
-        e = torch.tensor([e2e["value"] / world], device=dev, dtype=torch.float64)
-        dist.all_reduce(e, op=dist.ReduceOp.MIN)
-        e2e["value"] = float(e.item()) * world
+    total_ms, e2e_value = aggregate_ranks(sum(ms), e2e["value"], world, dist, dev)
+    e2e["value"] = e2e_value
     if rank != 0:
         if dist is not None:
             dist.destroy_process_group()
         return
     peak, peak_kind = _peaks()
-    value = world * args.steps * entries / (total_ms / 1e3)
+    value = job_throughput(world, args.steps, entries, total_ms)
     hk_ms, hk_n = snap[hist_kernel]
     hk_avg = hk_ms / max(hk_n, 1)
     achieved = kernel_bytes / (hk_avg / 1e3) / 1e9 if hk_n else None

@@ -53,8 +53,24 @@ def rng_for(name: str, salt: int = 0) -> np.random.Generator:
 
 # ----------------------------------------------------------------------------- bins
 def bins_uniform(rng, n_features, n_rows, n_values=255):
-    """Feature-major [F][N] uint8, uniform over [0, n_values)."""
-    return rng.integers(0, n_values, size=(n_features, n_rows), dtype=np.uint8)
+    """Feature-major [F][N] uint8, uniform over [0, n_values).
+
+    For n_values = 255 each feature row is raw random bytes with every 255
+    redrawn (rejection sampling: exactly uniform over [0, 254], and fast at GB
+    scale)."""
+    if n_values != 255:
+        return rng.integers(0, n_values, size=(n_features, n_rows), dtype=np.uint8)
+    out = np.empty((n_features, n_rows), dtype=np.uint8)
+    per = max(1, (64 << 20) // max(n_rows, 1))  # features per 64 MiB block
+    for f0 in range(0, n_features, per):
+        f1 = min(n_features, f0 + per)
+        blk = np.frombuffer(rng.bytes((f1 - f0) * n_rows), dtype=np.uint8).copy()
+        bad = np.flatnonzero(blk == 255)
+        while bad.size:
+            blk[bad] = np.frombuffer(rng.bytes(bad.size), dtype=np.uint8)
+            bad = bad[blk[bad] == 255]
+        out[f0:f1] = blk.reshape(f1 - f0, n_rows)
+    return out
 
 
 def bins_zipf(rng, n_features, n_rows, s=1.1, n_values=255):
