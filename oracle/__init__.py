@@ -90,6 +90,8 @@ def lib():
         L.oracle_gain.restype = f64
         L.oracle_find_splits.argtypes = [p, i32, i32, i32, f64, f64, f64, f64, f64, p]
         L.oracle_find_splits.restype = ctypes.c_int
+        L.oracle_find_level_split.argtypes = [p, i32, i32, i32, f64, f64, f64, f64, f64, p]
+        L.oracle_find_level_split.restype = ctypes.c_int
         L.oracle_partition.argtypes = [p, ctypes.c_int, i64, i32, ctypes.c_uint32, p, p, i32, p, p, p]
         L.oracle_partition.restype = ctypes.c_int
         _lib = L
@@ -157,6 +159,20 @@ def find_splits(hist: np.ndarray, n_bins: int, lam: float, gamma: float, min_chi
     st = lib().oracle_find_splits(_ptr(hist), n_nodes, F, n_bins, lam, gamma, min_child_weight, inv_sg, inv_sh,
                                   _ptr(out))
     return out, st
+
+
+def find_level_split(hist: np.ndarray, n_bins: int, lam: float, gamma: float, min_child_weight: float,
+                     scale_g: float, scale_h: float):
+    """Oblivious level split: hist [n_nodes][F][n_bins+1][2] int64 -> (one SPLIT_DTYPE record, status)."""
+    hist = np.ascontiguousarray(hist, dtype=np.int64)
+    n_nodes, F, B, _ = hist.shape
+    assert B == n_bins + 1
+    out = np.zeros(1, dtype=SPLIT_DTYPE)
+    inv_sg = 1.0 / float(np.float32(scale_g))
+    inv_sh = 1.0 / float(np.float32(scale_h))
+    st = lib().oracle_find_level_split(_ptr(hist), n_nodes, F, n_bins, lam, gamma, min_child_weight, inv_sg, inv_sh,
+                                       _ptr(out))
+    return out[0], st
 
 
 def partition(bins: np.ndarray, n_bins: int, sentinel: int, rows, node_offsets, splits: np.ndarray):

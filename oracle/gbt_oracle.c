@@ -27,6 +27,10 @@
  *  [P5] hessboost PR #163 "sweep vector-leaf histograms by feature on sparse
  *       indexes" - "Change" (the width's missing sentinel is skipped from the
  *       real bins; here it is routed to its own slot).
+ *  [P1] also: "The device context lifecycle" names find_level_split, the
+ *       oblivious grower's scan of the frontier histograms; [P4] section 5
+ *       defines the oblivious (symmetric) tree: every node of a level uses the
+ *       same feature and the same threshold.
  *
  * Readings where the pages leave a step open (each is also listed in the
  * design notes):
@@ -47,6 +51,13 @@
  *     histogram built from rows every feature's total is the node's total.
  *  R7 after subtraction a negative hessian cell cannot arise from consistent
  *     inputs; the oracle reports it instead of clamping.
+ *  R8 the level split of an oblivious tree: candidate (f, t, direction) scores
+ *     the sum over the level's nodes, ascending, of each node's R6 gain at that
+ *     candidate (node totals of feature f); a node for which the candidate is
+ *     not valid (R4) adds nothing; the candidate is valid iff it is valid for
+ *     at least one node; the sum starts from 0.0 and adds in node order; the
+ *     order and tie-break are R3's. The reported sums are the candidate's
+ *     left/right totals over all nodes.
  */
 #include <stdint.h>
 #include <stddef.h>
@@ -236,6 +247,62 @@ int oracle_find_splits(const int64_t *hist, int32_t n_nodes, int32_t n_features,
     }
     out[n] = best;
   }
+  return OR_OK;
+}
+
+/*
+ * Oblivious level split [P1 "The device context lifecycle": find_level_split;
+ * P4 s5: one feature and threshold for every node of a level], reading R8.
+ * hist: [n_nodes][n_features][n_bins + 1][2]; out: one record.
+ */
+int oracle_find_level_split(const int64_t *hist, int32_t n_nodes, int32_t n_features, int32_t n_bins, double lambda,
+                            double gamma, double min_child_weight, double inv_sg, double inv_sh, oracle_split *out) {
+  if (n_nodes < 0 || n_features < 0 || n_bins < 1 || !out || (n_nodes > 0 && !hist)) return OR_ERR_ARG;
+  const int64_t B = (int64_t)n_bins + 1;
+  const int64_t per_node = (int64_t)n_features * B * 2;
+  oracle_split best;
+  best.feature = -1;
+  best.bin = -1;
+  best.default_left = 0;
+  for (int i = 0; i < 7; ++i) best.pad[i] = 0;
+  best.gain = -INFINITY;
+  best.g_left = best.h_left = best.g_right = best.h_right = 0;
+  for (int32_t f = 0; f < n_features; ++f) {
+    for (int32_t t = 0; t < n_bins; ++t) {
+      for (int dir = 0; dir < 2; ++dir) { /* 0: missing right, 1: missing left */
+        double sum = 0.0;
+        int any = 0;
+        int64_t sgl = 0, shl = 0, sgr = 0, shr = 0;
+        for (int32_t n = 0; n < n_nodes; ++n) {
+          const int64_t *hf = hist + (int64_t)n * per_node + (int64_t)f * B * 2;
+          int64_t G = 0, H = 0, pg = 0, ph = 0;
+          for (int64_t s = 0; s < B; ++s) { G += hf[s * 2]; H += hf[s * 2 + 1]; }
+          for (int64_t s = 0; s <= t; ++s) { pg += hf[s * 2]; ph += hf[s * 2 + 1]; }
+          const int64_t GL = pg + (dir ? hf[(int64_t)n_bins * 2] : 0);
+          const int64_t HL = ph + (dir ? hf[(int64_t)n_bins * 2 + 1] : 0);
+          const int64_t GR = G - GL, HR = H - HL;
+          sgl += GL; shl += HL; sgr += GR; shr += HR;
+          if (!(HL > 0 && HR > 0)) continue;
+          const double gld = (double)GL * inv_sg, hld = (double)HL * inv_sh;
+          const double grd = (double)GR * inv_sg, hrd = (double)HR * inv_sh;
+          if (!(hld >= min_child_weight && hrd >= min_child_weight)) continue;
+          sum = sum + oracle_gain(gld, hld, grd, hrd, (double)G * inv_sg, (double)H * inv_sh, lambda, gamma);
+          any = 1;
+        }
+        if (any && sum > best.gain) {
+          best.feature = f;
+          best.bin = t;
+          best.default_left = (uint8_t)dir;
+          best.gain = sum;
+          best.g_left = sgl;
+          best.h_left = shl;
+          best.g_right = sgr;
+          best.h_right = shr;
+        }
+      }
+    }
+  }
+  *out = best;
   return OR_OK;
 }
 

@@ -287,3 +287,98 @@ def test_synth_is_seeded():
     b = synth.make("root", n_rows=500, n_features=3)
     np.testing.assert_array_equal(a.bins, b.bins)
     np.testing.assert_array_equal(a.gpair, b.gpair)
+
+
+# --------------------------------------------------------------------------- oblivious level split
+def _rand_hist(rng, n_nodes, F, n_bins, miss=True):
+    """Histograms with integer cells: g in [-30, 30], h in [0, 10] (a node may have empty slots)."""
+    B = n_bins + 1
+    h = np.zeros((n_nodes, F, B, 2), np.int64)
+    h[..., 0] = rng.integers(-30, 31, size=(n_nodes, F, B))
+    h[..., 1] = rng.integers(0, 11, size=(n_nodes, F, B))
+    if not miss:
+        h[:, :, n_bins, :] = 0
+    h[..., 0] = np.where(h[..., 1] == 0, 0, h[..., 0])
+    return h
+
+
+def test_level_split_of_one_node_is_its_split(oracle_mod):
+    """With a single node the oblivious level split reduces to the node's own split (same record)."""
+    rng = np.random.default_rng(11)
+    for trial in range(20):
+        hist = _rand_hist(rng, 1, 4, 6, miss=bool(trial % 2))
+        node, st = oracle_mod.find_splits(hist, 6, 1.0, 0.1, 0.0, 1.0, 1.0)
+        lvl, st2 = oracle_mod.find_level_split(hist, 6, 1.0, 0.1, 0.0, 1.0, 1.0)
+        assert st == st2 == oracle_mod.OK
+        for k in ("feature", "bin", "default_left", "g_left", "h_left", "g_right", "h_right"):
+            assert lvl[k] == node[0][k], (trial, k)
+        assert np.float64(lvl["gain"]).tobytes() == np.float64(node[0]["gain"]).tobytes()
+
+
+def test_level_split_of_a_duplicated_node_doubles_the_gain(oracle_mod):
+    """Two identical nodes: the same candidate wins, with twice the gain and twice the sums."""
+    rng = np.random.default_rng(12)
+    for trial in range(10):
+        one = _rand_hist(rng, 1, 3, 5)
+        two = np.concatenate([one, one])
+        a, _ = oracle_mod.find_level_split(one, 5, 1.0, 0.0, 0.0, 1.0, 1.0)
+        b, _ = oracle_mod.find_level_split(two, 5, 1.0, 0.0, 0.0, 1.0, 1.0)
+        assert (a["feature"], a["bin"], a["default_left"]) == (b["feature"], b["bin"], b["default_left"])
+        if a["feature"] >= 0:
+            assert b["gain"] == 2 * a["gain"]
+            assert b["g_left"] == 2 * a["g_left"] and b["h_right"] == 2 * a["h_right"]
+
+
+def test_level_split_hand_case(oracle_mod):
+    """Two nodes, one feature, two bins (lambda = 1): node A cut 0 has gain 1/2 (GL=1,HL=1,GR=-1,HR=1);
+    node B cut 0 has gain 1/10 (GL=2,HL=3,GR=0,HR=1); cut 1 empties both right sides. The level split
+    is cut 0, missing right (no missing mass), gain 3/5, sums (3, 4, -1, 2)."""
+    hist = np.zeros((2, 1, 3, 2), np.int64)
+    hist[0, 0, 0] = (1, 1)
+    hist[0, 0, 1] = (-1, 1)
+    hist[1, 0, 0] = (2, 3)
+    hist[1, 0, 1] = (0, 1)
+    out, st = oracle_mod.find_level_split(hist, 2, 1.0, 0.0, 0.0, 1.0, 1.0)
+    assert st == oracle_mod.OK
+    assert (out["feature"], out["bin"], out["default_left"]) == (0, 0, 0)
+    assert out["gain"] == pytest.approx(0.6, rel=1e-14)
+    assert (out["g_left"], out["h_left"], out["g_right"], out["h_right"]) == (3, 4, -1, 2)
+    # gamma applies once per node that splits: 3/5 - 2 * 0.25
+    out2, _ = oracle_mod.find_level_split(hist, 2, 1.0, 0.25, 0.0, 1.0, 1.0)
+    assert out2["gain"] == pytest.approx(0.1, rel=1e-12)
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_level_split_equals_exact_rational_argmax(oracle_mod, seed):
+    """Brute force in exact rationals: every (feature, cut, direction), the sum over the nodes where it
+    is valid of the node's gain; the first strictly larger sum wins."""
+    rng = np.random.default_rng(900 + seed)
+    n_nodes, F, n_bins = 3, 3, 5
+    hist = _rand_hist(rng, n_nodes, F, n_bins, miss=bool(seed % 2))
+    lam, gamma = Fraction(1), Fraction(1, 20)
+    cands = []
+    for f in range(F):
+        for t in range(n_bins):
+            for d in (0, 1):
+                tot, any_valid = Fraction(0), False
+                for n in range(n_nodes):
+                    c = hist[n, f]
+                    G, H = int(c[:, 0].sum()), int(c[:, 1].sum())
+                    gl = int(c[:t + 1, 0].sum()) + (int(c[n_bins, 0]) if d else 0)
+                    hl = int(c[:t + 1, 1].sum()) + (int(c[n_bins, 1]) if d else 0)
+                    if hl > 0 and H - hl > 0:
+                        tot += _exact_gain(Fraction(gl), hl, Fraction(G - gl), H - hl, lam) - gamma
+                        any_valid = True
+                if any_valid:
+                    cands.append((tot, f, t, d))
+    best = None
+    for c in cands:
+        if best is None or c[0] > best[0]:
+            best = c
+    gains = sorted({c[0] for c in cands}, reverse=True)
+    if len(gains) > 1 and gains[0] - gains[1] < Fraction(1, 10 ** 9):
+        pytest.skip("near-tie between distinct exact gains")
+    out, st = oracle_mod.find_level_split(hist, n_bins, 1.0, 0.05, 0.0, 1.0, 1.0)
+    assert st == oracle_mod.OK
+    assert (out["feature"], out["bin"], out["default_left"]) == best[1:]
+    assert out["gain"] == pytest.approx(float(best[0]), rel=1e-12)
