@@ -345,6 +345,29 @@ def run_gpu(args, rank, world, local_rank):
         ms_warm, _, _, _ = timed_pass(False, flush_l2=False)
         assert sess.sync() == 0
 
+        # ---------------------------------------------------------------- oblivious level split (optional)
+        obl = None
+        if args.oblivious and lv.depth > 0:
+            lvl_h = torch.cat([hs, large])  # every node of the level
+            n_lvl = lvl_h.shape[0]
+            lo_out = torch.empty((1, g.SPLIT_BYTES), dtype=torch.uint8, device=dev)
+            for i in range(3):
+                sess.check(g.gbt_find_level_split(ctx, lvl_h, n_lvl, prm, lo_out))
+            obl_ms = []
+            for i in range(args.steps):
+                flush(i)
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                sess.check(g.gbt_find_level_split(ctx, lvl_h, n_lvl, prm, lo_out))
+                b.record(stream)
+                b.synchronize()
+                obl_ms.append(a.elapsed_time(b))
+            assert sess.sync() == 0
+            obl_bytes = n_lvl * w.n_features * B * 16
+            obl_t = statistics.median(obl_ms)
+            obl = {"nodes": n_lvl, "ms_per_call": obl_t, "algorithmic_bytes": obl_bytes,
+                   "achieved_gbs": obl_bytes / (obl_t / 1e3) / 1e9}
+
         # ---------------------------------------------------------------- e2e through host buffers
         e2e = None
         if lv.depth > 0:
@@ -426,6 +449,10 @@ def run_gpu(args, rank, world, local_rank):
         "cpu_baseline": {"value": cpu_v, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": cpu_sample},
         "wall_s_timed": wall,
     }
+    if obl is not None:
+        peak_v, _ = _peaks()
+        obl["frac"] = obl["achieved_gbs"] / peak_v
+        line["oblivious_split"] = obl
     print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()
@@ -461,6 +488,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOAD_TEXT), default="level5")
     ap.add_argument("--path", choices=["fused", "unfused"], default="fused")
+    ap.add_argument("--oblivious", action="store_true",
+                    help="also time gbt_find_level_split on the level's histograms (reported under oblivious_split)")
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle time for cpu_baseline")
     ap.add_argument("--ref-budget", type=float, default=90.0, help="seconds of oracle time for --impl reference")
     args = ap.parse_args()

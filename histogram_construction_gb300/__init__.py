@@ -27,7 +27,7 @@ EXPORTS = [
     "gbt_suggest_scales", "gbt_build_level", "gbt_subtract_siblings", "gbt_find_splits", "gbt_subtract_and_find",
     "gbt_level_step",
     "gbt_partition_level", "gbt_profile_enable", "gbt_profile_read", "gbt_slots_per_feature",
-    "gbt_kernel_launches", "gbt_find_splits_noalloc",
+    "gbt_kernel_launches", "gbt_find_splits_noalloc", "gbt_find_level_split",
 ]
 
 
@@ -85,6 +85,7 @@ def lib(build_if_missing: bool = True):
         "gbt_slots_per_feature": (i32, [vp]),
         "gbt_kernel_launches": (i64, [vp]),
         "gbt_find_splits_noalloc": (st, [vp, i32, i32, i32, f32, f32, ctypes.POINTER(GbtParams), vp, vp]),
+        "gbt_find_level_split": (st, [vp, vp, i32, ctypes.POINTER(GbtParams), vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(L, name)
@@ -174,6 +175,10 @@ def gbt_subtract_siblings(ctx, parent_hist, parent_of, small_hist, large_hist, n
 
 def gbt_find_splits(ctx, hist, n_nodes, prm, out):
     return lib().gbt_find_splits(ctx, ptr(hist), int(n_nodes), ctypes.byref(prm), ptr(out))
+
+
+def gbt_find_level_split(ctx, hist, n_nodes, prm, out):
+    return lib().gbt_find_level_split(ctx, ptr(hist), int(n_nodes), ctypes.byref(prm), ptr(out))
 
 
 def gbt_find_splits_noalloc(hist, n_nodes, n_features, n_bins, scale_g, scale_h, prm, out, stream=None):

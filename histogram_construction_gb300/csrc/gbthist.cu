@@ -18,6 +18,7 @@
 #include "../../include/gbthist.h"
 #include "common.cuh"
 #include "k_hist.cuh"
+#include "k_level_split.cuh"
 #include "k_partition.cuh"
 #include "k_prep.cuh"
 #include "k_split.cuh"
@@ -91,7 +92,7 @@ struct gbt_ctx {
   DevState *st = nullptr;
   uint32_t *err_host = nullptr;  // pinned: [0] error word copy, [1] max |q| copy
   Buf gp_stage, chunk_prefix, partial, rows_in, offs_in, cand, splits_a, splits_b, parent_of_in, tile_counts, lrank,
-      slab, counters;
+      slab, counters, level_scratch;
   std::string last_error;
   int64_t launches = 0;
   // tuning: work items the level plan aims for (default 2 per SM; GBT_TARGET_ITEMS overrides it for sweeps)
@@ -363,7 +364,7 @@ gbt_status gbt_destroy(gbt_ctx *c) {
   cudaStreamSynchronize(c->stream);
   Buf *bufs[] = {&c->mirror, &c->q, &c->gp_stage, &c->chunk_prefix, &c->partial, &c->rows_in, &c->offs_in,
                  &c->cand, &c->splits_a, &c->splits_b, &c->parent_of_in, &c->tile_counts, &c->lrank, &c->slab,
-                 &c->counters};
+                 &c->counters, &c->level_scratch};
   for (Buf *b : bufs) release(c, *b);
   if (c->st) cudaFreeAsync(c->st, c->stream);
   cudaStreamSynchronize(c->stream);
@@ -731,6 +732,39 @@ gbt_status gbt_find_splits(gbt_ctx *c, const int64_t *hist, int32_t n_nodes, con
   if (host)
     CUDA_TRY(c, cudaMemcpyAsync(out, dout, (size_t)n_nodes * sizeof(gbt_split), cudaMemcpyDeviceToHost, c->stream),
              "splits to host");
+  return GBT_OK;
+}
+
+gbt_status gbt_find_level_split(gbt_ctx *c, const int64_t *hist, int32_t n_nodes, const gbt_params *params,
+                                gbt_split *out) {
+  gbt_status s = check_ctx(c);
+  if (s != GBT_OK) return s;
+  if (!c->tree_ready) return fail(c, GBT_ERR_STATE, "gbt_begin_tree first (scales)");
+  if (!params || n_nodes < 1) return fail(c, GBT_ERR_INVALID_ARG, "params NULL or n_nodes < 1");
+  if (n_nodes > 65535) return fail(c, GBT_ERR_UNSUPPORTED, "n_nodes must be <= 65535");
+  if (ptr_kind(hist) != 1 || !aligned16(hist)) return fail(c, GBT_ERR_INVALID_ARG, "hist must be 16-byte aligned device memory");
+  SplitOut *dout = nullptr;
+  bool host = false;
+  s = split_out_view(c, out, 1, c->splits_a, &dout, &host);
+  if (s != GBT_OK) return s;
+  const int nfb = (c->n_features + SCAN_WARPS - 1) / SCAN_WARPS;
+  s = ensure(c, c->cand, (size_t)nfb * PUB_K * sizeof(Cand), "candidates");
+  if (s != GBT_OK) return s;
+  s = ensure_counters(c, 2);
+  if (s != GBT_OK) return s;
+  // [n_nodes][F] per-(node, feature) totals, then [SCAN_WARPS + nfb][n_nodes] exact-gain buffers
+  const size_t tot_bytes = (size_t)n_nodes * c->n_features * sizeof(LevelTot);
+  s = ensure(c, c->level_scratch, tot_bytes + (size_t)(SCAN_WARPS + nfb) * n_nodes * sizeof(double),
+             "level split scratch");
+  if (s != GBT_OK) return s;
+  const SplitParams sp = make_sp(c, params);
+  prof_begin(c);
+  k_level_split<<<nfb, SCAN_THREADS, 0, c->stream>>>(
+      hist, n_nodes, c->n_features, c->n_bins, sp, (LevelTot *)c->level_scratch.p, (Cand *)c->cand.p,
+      (uint32_t *)c->counters.p, (double *)((char *)c->level_scratch.p + tot_bytes), dout);
+  LAUNCH_CHECK(c, "k_level_split");
+  if (host)
+    CUDA_TRY(c, cudaMemcpyAsync(out, dout, sizeof(gbt_split), cudaMemcpyDeviceToHost, c->stream), "split to host");
   return GBT_OK;
 }
 

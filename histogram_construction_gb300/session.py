@@ -9,7 +9,7 @@ from __future__ import annotations
 import numpy as np
 
 from . import (GBT_OK, SPLIT_BYTES, check, gbt_begin_tree, gbt_build_level, gbt_create, gbt_destroy,
-               gbt_find_splits, gbt_kernel_launches, gbt_level_step, gbt_partition_level, gbt_subtract_and_find,
+               gbt_find_level_split, gbt_find_splits, gbt_kernel_launches, gbt_level_step, gbt_partition_level, gbt_subtract_and_find,
                gbt_subtract_siblings, gbt_sync, gbt_upload_bins, lib, params)
 
 SPLIT_DTYPE = np.dtype([
@@ -123,6 +123,12 @@ class Session:
         n = hist.shape[0]
         out = self.torch.empty((n, SPLIT_BYTES), dtype=self.torch.uint8, device=self.device)
         self.check(gbt_find_splits(self.ctx, hist, n, params(lam, gamma, mcw), out))
+        return out
+
+    def find_level_split(self, hist, lam=1.0, gamma=0.0, mcw=0.0):
+        """One oblivious split for all nodes of `hist` ([n][F][B][2] int64): a [1, 56] uint8 tensor."""
+        out = self.torch.empty((1, SPLIT_BYTES), dtype=self.torch.uint8, device=self.device)
+        self.check(gbt_find_level_split(self.ctx, hist, hist.shape[0], params(lam, gamma, mcw), out))
         return out
 
     def subtract_and_find(self, parent, small, parent_of=None, large=None, lam=1.0, gamma=0.0, mcw=0.0):

@@ -159,6 +159,24 @@ gbt_status gbt_subtract_siblings(gbt_ctx *ctx, const int64_t *parent_hist, const
 gbt_status gbt_find_splits(gbt_ctx *ctx, const int64_t *hist, int32_t n_nodes, const gbt_params *params,
                            gbt_split *out);
 
+/* The split of an oblivious (symmetric) tree level: one feature, cut and
+ * missing direction for every node ["GBDT engine engineering deep-dive",
+ * section 5: an oblivious tree uses the same feature and threshold across a
+ * level; bonsai "10: CUDA histogram backend", "The device context lifecycle":
+ * find_level_split]. The pages give no level gain; this library's reading: a
+ * candidate (feature, t, direction) scores the sum over the nodes, ascending,
+ * of each node's gbt_find_splits gain at that candidate (each node's own
+ * feature totals, gamma included per node), a node for which the candidate
+ * is not valid adding nothing; it is valid when valid for at least one node;
+ * the first strictly larger sum in (feature, t, right-before-left) order wins.
+ * The sum is evaluated in double in node order (bit-identical to the oracle).
+ *   hist: device [n_nodes][n_features][B][2] int64, 16-byte aligned.
+ *   out: host or device, ONE gbt_split: feature, bin, default_left, the level
+ *     gain, and the left/right sums over all nodes. feature = -1 (gain -inf)
+ *     when no candidate is valid for any node. */
+gbt_status gbt_find_level_split(gbt_ctx *ctx, const int64_t *hist, int32_t n_nodes, const gbt_params *params,
+                                gbt_split *out);
+
 /* gbt_find_splits without a context and without any allocation. The paper
  * has no counterpart: this exists for callers that may not allocate device
  * memory themselves or through a library, e.g. a host application that hands
