@@ -747,21 +747,35 @@ gbt_status gbt_find_level_split(gbt_ctx *c, const int64_t *hist, int32_t n_nodes
   bool host = false;
   s = split_out_view(c, out, 1, c->splits_a, &dout, &host);
   if (s != GBT_OK) return s;
-  const int nfb = (c->n_features + SCAN_WARPS - 1) / SCAN_WARPS;
-  s = ensure(c, c->cand, (size_t)nfb * PUB_K * sizeof(Cand), "candidates");
+  const int n_chunks = (c->n_bins + LS_CHUNK - 1) / LS_CHUNK;
+  // warps per feature: enough to share the nodes, the rest of the CTA's 8 warps take more features
+  int wpf = 1;
+  while (wpf < SCAN_WARPS && wpf * 8 <= n_nodes) wpf *= 2;
+  const int fpc = SCAN_WARPS / wpf;
+  const int64_t ctas = (int64_t)((c->n_features + fpc - 1) / fpc) * n_chunks;
+  if (n_chunks > 65535) return fail(c, GBT_ERR_UNSUPPORTED, "too many bins for the level split grid");
+  s = ensure(c, c->cand, (size_t)ctas * PUB_K * sizeof(Cand), "candidates");
   if (s != GBT_OK) return s;
   s = ensure_counters(c, 2);
   if (s != GBT_OK) return s;
-  // [n_nodes][F] per-(node, feature) totals, then [SCAN_WARPS + nfb][n_nodes] exact-gain buffers
-  const size_t tot_bytes = (size_t)n_nodes * c->n_features * sizeof(LevelTot);
-  s = ensure(c, c->level_scratch, tot_bytes + (size_t)(SCAN_WARPS + nfb) * n_nodes * sizeof(double),
+  // [n_nodes][F] totals, [n_nodes][F][n_chunks] carries, [SCAN_WARPS + ctas][n_nodes] exact-gain buffers
+  const size_t nf = (size_t)n_nodes * c->n_features;
+  const size_t tot_bytes = nf * sizeof(LevelTot), carry_bytes = nf * n_chunks * sizeof(longlong2);
+  s = ensure(c, c->level_scratch, tot_bytes + carry_bytes + (size_t)(SCAN_WARPS + ctas) * n_nodes * sizeof(double),
              "level split scratch");
   if (s != GBT_OK) return s;
+  LevelTot *tot = (LevelTot *)c->level_scratch.p;
+  longlong2 *carry = (longlong2 *)((char *)c->level_scratch.p + tot_bytes);
+  double *gbuf = (double *)((char *)c->level_scratch.p + tot_bytes + carry_bytes);
   const SplitParams sp = make_sp(c, params);
   prof_begin(c);
-  k_level_split<<<nfb, SCAN_THREADS, 0, c->stream>>>(
-      hist, n_nodes, c->n_features, c->n_bins, sp, (LevelTot *)c->level_scratch.p, (Cand *)c->cand.p,
-      (uint32_t *)c->counters.p, (double *)((char *)c->level_scratch.p + tot_bytes), dout);
+  k_level_totals<<<(unsigned)((nf * 32 + 255) / 256), 256, 0, c->stream>>>(hist, n_nodes, c->n_features, c->n_bins,
+                                                                          tot, carry);
+  LAUNCH_CHECK(c, "k_level_totals");
+  prof_begin(c);
+  launch_pdl(c, k_level_split, dim3((c->n_features + fpc - 1) / fpc, n_chunks), dim3(SCAN_THREADS), 0, hist, n_nodes,
+             c->n_features, c->n_bins, sp, (const LevelTot *)tot, (const longlong2 *)carry, (Cand *)c->cand.p,
+             (uint32_t *)c->counters.p, gbuf, (int32_t)wpf, dout);
   LAUNCH_CHECK(c, "k_level_split");
   if (host)
     CUDA_TRY(c, cudaMemcpyAsync(out, dout, sizeof(gbt_split), cudaMemcpyDeviceToHost, c->stream), "split to host");
