@@ -92,6 +92,12 @@ def lib():
         L.oracle_find_splits.restype = ctypes.c_int
         L.oracle_find_level_split.argtypes = [p, i32, i32, i32, f64, f64, f64, f64, f64, p]
         L.oracle_find_level_split.restype = ctypes.c_int
+        L.oracle_build_hist_f64.argtypes = [p, ctypes.c_int, i64, i32, i32, ctypes.c_uint32, p, p, p, i32, p, p]
+        L.oracle_build_hist_f64.restype = ctypes.c_int
+        L.oracle_subtract_f64.argtypes = [p, p, p, p, i32, i32, i32]
+        L.oracle_subtract_f64.restype = ctypes.c_int
+        L.oracle_find_splits_f64.argtypes = [p, i32, i32, i32, f64, f64, f64, p]
+        L.oracle_find_splits_f64.restype = ctypes.c_int
         L.oracle_partition.argtypes = [p, ctypes.c_int, i64, i32, ctypes.c_uint32, p, p, i32, p, p, p]
         L.oracle_partition.restype = ctypes.c_int
         _lib = L
@@ -173,6 +179,48 @@ def find_level_split(hist: np.ndarray, n_bins: int, lam: float, gamma: float, mi
     st = lib().oracle_find_level_split(_ptr(hist), n_nodes, F, n_bins, lam, gamma, min_child_weight, inv_sg, inv_sh,
                                        _ptr(out))
     return out[0], st
+
+
+SPLIT_F64_DTYPE = np.dtype([
+    ("feature", "<i4"), ("bin", "<i4"), ("default_left", "u1"), ("pad", "u1", (7,)), ("gain", "<f8"),
+    ("g_left", "<f8"), ("h_left", "<f8"), ("g_right", "<f8"), ("h_right", "<f8"),
+])
+
+
+def build_hist_f64(bins: np.ndarray, n_bins: int, sentinel: int, gpair: np.ndarray, rows, node_offsets):
+    """Float-cell mode: (hist, abs_hist, status), both [n_nodes][F][n_bins+1][2] float64; abs_hist holds the
+    sums of |g|, |h| per cell."""
+    bins = np.ascontiguousarray(bins)
+    F, N = bins.shape
+    gp = np.ascontiguousarray(gpair, dtype=np.float32).reshape(-1, 2)
+    assert gp.shape[0] == N
+    offs = np.ascontiguousarray(node_offsets, dtype=np.int64)
+    n_nodes = offs.shape[0] - 1
+    rows_a = None if rows is None else np.ascontiguousarray(rows, dtype=np.int32)
+    hist = np.empty((n_nodes, F, n_bins + 1, 2), dtype=np.float64)
+    ab = np.empty_like(hist)
+    st = lib().oracle_build_hist_f64(_ptr(bins), bins.dtype.itemsize, N, F, n_bins, sentinel, _ptr(gp), _ptr(rows_a),
+                                     _ptr(offs), n_nodes, _ptr(hist), _ptr(ab))
+    return hist, ab, st
+
+
+def subtract_f64(parent: np.ndarray, parent_of, small: np.ndarray):
+    parent = np.ascontiguousarray(parent, dtype=np.float64)
+    small = np.ascontiguousarray(small, dtype=np.float64)
+    n_pairs, F, B, _ = small.shape
+    po = None if parent_of is None else np.ascontiguousarray(parent_of, dtype=np.int32)
+    large = np.empty_like(small)
+    st = lib().oracle_subtract_f64(_ptr(parent), _ptr(po), _ptr(small), _ptr(large), n_pairs, F, B)
+    return large, st
+
+
+def find_splits_f64(hist: np.ndarray, n_bins: int, lam: float, gamma: float, min_child_weight: float):
+    hist = np.ascontiguousarray(hist, dtype=np.float64)
+    n_nodes, F, B, _ = hist.shape
+    assert B == n_bins + 1
+    out = np.zeros(n_nodes, dtype=SPLIT_F64_DTYPE)
+    st = lib().oracle_find_splits_f64(_ptr(hist), n_nodes, F, n_bins, lam, gamma, min_child_weight, _ptr(out))
+    return out, st
 
 
 def partition(bins: np.ndarray, n_bins: int, sentinel: int, rows, node_offsets, splits: np.ndarray):

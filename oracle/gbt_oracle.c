@@ -51,6 +51,13 @@
  *     histogram built from rows every feature's total is the node's total.
  *  R7 after subtraction a negative hessian cell cannot arise from consistent
  *     inputs; the oracle reports it instead of clamping.
+ *  R9 the float-cell mode [P1 "The kernel": float shared cells merged into
+ *     double global cells; P4 s7 listing; P4 s3: clamp the hessian at zero
+ *     after subtraction]: cells are double sums of the unquantised float32
+ *     g and h, added per bin in the given row order (one chain per bin);
+ *     subtraction clamps a negative H cell to 0 (G is left as is); the split
+ *     find uses R3/R4/R6 on these double cells with inv_s = 1 (values are
+ *     not scaled), prefixes summed left to right.
  *  R8 the level split of an oblivious tree: candidate (f, t, direction) scores
  *     the sum over the level's nodes, ascending, of each node's R6 gain at that
  *     candidate (node totals of feature f); a node for which the candidate is
@@ -232,6 +239,121 @@ int oracle_find_splits(const int64_t *hist, int32_t n_nodes, int32_t n_features,
           double grd = (double)GR * inv_sg, hrd = (double)HR * inv_sh;
           if (!(hld >= min_child_weight && hrd >= min_child_weight)) continue;
           double gain = oracle_gain(gld, hld, grd, hrd, Gd, Hd, lambda, gamma);
+          if (gain > best.gain) {
+            best.feature = f;
+            best.bin = t;
+            best.default_left = (uint8_t)dir;
+            best.gain = gain;
+            best.g_left = GL;
+            best.h_left = HL;
+            best.g_right = GR;
+            best.h_right = HR;
+          }
+        }
+      }
+    }
+    out[n] = best;
+  }
+  return OR_OK;
+}
+
+/*
+ * Float-cell mode (R9). gpair: float32 [n_rows][2]. hist: out
+ * [n_nodes][n_features][n_bins + 1][2] double; abs_out (may be NULL): the same
+ * shape, the sums of |g| and |h| per cell (the tolerance scale).
+ */
+int oracle_build_hist_f64(const void *bins, int bin_bytes, int64_t n_rows, int32_t n_features, int32_t n_bins,
+                          uint32_t sentinel, const float *gpair, const int32_t *rows, const int64_t *node_offsets,
+                          int32_t n_nodes, double *hist, double *abs_out) {
+  if (bin_bytes != 1 && bin_bytes != 2) return OR_ERR_ARG;
+  if (n_rows < 0 || n_features < 0 || n_nodes < 0 || n_bins < 1) return OR_ERR_ARG;
+  if (!node_offsets || (n_nodes > 0 && !hist)) return OR_ERR_ARG;
+  const int64_t B = (int64_t)n_bins + 1;
+  const int64_t per_node = (int64_t)n_features * B * 2;
+  for (int64_t i = 0; i < (int64_t)n_nodes * per_node; ++i) {
+    hist[i] = 0.0;
+    if (abs_out) abs_out[i] = 0.0;
+  }
+  const uint8_t *b8 = (const uint8_t *)bins;
+  const uint16_t *b16 = (const uint16_t *)bins;
+  int st = OR_OK;
+  for (int32_t n = 0; n < n_nodes; ++n) {
+    double *hn = hist + (int64_t)n * per_node;
+    double *an = abs_out ? abs_out + (int64_t)n * per_node : NULL;
+    for (int64_t k = node_offsets[n]; k < node_offsets[n + 1]; ++k) {
+      int64_t r = rows ? (int64_t)rows[k] : k;
+      if (r < 0 || r >= n_rows) { st = OR_ERR_ROW; continue; }
+      const double g = (double)gpair[2 * r], h = (double)gpair[2 * r + 1];
+      for (int32_t f = 0; f < n_features; ++f) {
+        uint32_t b = bin_bytes == 1 ? b8[(int64_t)f * n_rows + r] : b16[(int64_t)f * n_rows + r];
+        int64_t s = slot_of(b, n_bins, sentinel);
+        if (s < 0) { st = OR_ERR_BIN; continue; }
+        hn[((int64_t)f * B + s) * 2 + 0] += g;
+        hn[((int64_t)f * B + s) * 2 + 1] += h;
+        if (an) {
+          an[((int64_t)f * B + s) * 2 + 0] += fabs(g);
+          an[((int64_t)f * B + s) * 2 + 1] += fabs(h);
+        }
+      }
+    }
+  }
+  return st;
+}
+
+/* Float-cell subtraction (R9): large = parent - small, a negative H cell clamped to 0. */
+int oracle_subtract_f64(const double *parent, const int32_t *parent_of, const double *small, double *large,
+                        int32_t n_pairs, int32_t n_features, int32_t n_slots) {
+  if (n_pairs < 0 || n_features < 0 || n_slots < 1) return OR_ERR_ARG;
+  const int64_t per_node = (int64_t)n_features * n_slots * 2;
+  for (int32_t p = 0; p < n_pairs; ++p) {
+    const int64_t pp = parent_of ? parent_of[p] : p;
+    for (int64_t i = 0; i < per_node; i += 2) {
+      large[p * per_node + i] = parent[pp * per_node + i] - small[p * per_node + i];
+      const double h = parent[pp * per_node + i + 1] - small[p * per_node + i + 1];
+      large[p * per_node + i + 1] = h < 0.0 ? 0.0 : h;
+    }
+  }
+  return OR_OK;
+}
+
+typedef struct {
+  int32_t feature;
+  int32_t bin;
+  uint8_t default_left;
+  uint8_t pad[7];
+  double gain;
+  double g_left, h_left, g_right, h_right;
+} oracle_split_f64;
+
+/* Float-cell split find (R9): R3/R4/R6 on double cells, unscaled. */
+int oracle_find_splits_f64(const double *hist, int32_t n_nodes, int32_t n_features, int32_t n_bins, double lambda,
+                           double gamma, double min_child_weight, oracle_split_f64 *out) {
+  if (n_nodes < 0 || n_features < 0 || n_bins < 1 || (n_nodes > 0 && (!hist || !out))) return OR_ERR_ARG;
+  const int64_t B = (int64_t)n_bins + 1;
+  const int64_t per_node = (int64_t)n_features * B * 2;
+  for (int32_t n = 0; n < n_nodes; ++n) {
+    const double *hn = hist + (int64_t)n * per_node;
+    oracle_split_f64 best;
+    best.feature = -1;
+    best.bin = -1;
+    best.default_left = 0;
+    for (int i = 0; i < 7; ++i) best.pad[i] = 0;
+    best.gain = -INFINITY;
+    best.g_left = best.h_left = best.g_right = best.h_right = 0.0;
+    for (int32_t f = 0; f < n_features; ++f) {
+      const double *hf = hn + (int64_t)f * B * 2;
+      double G = 0.0, H = 0.0;
+      for (int64_t s = 0; s < B; ++s) { G += hf[s * 2]; H += hf[s * 2 + 1]; }
+      const double Gm = hf[(int64_t)n_bins * 2], Hm = hf[(int64_t)n_bins * 2 + 1];
+      double pg = 0.0, ph = 0.0;
+      for (int32_t t = 0; t < n_bins; ++t) {
+        pg += hf[(int64_t)t * 2];
+        ph += hf[(int64_t)t * 2 + 1];
+        for (int dir = 0; dir < 2; ++dir) {
+          const double GL = pg + (dir ? Gm : 0.0), HL = ph + (dir ? Hm : 0.0);
+          const double GR = G - GL, HR = H - HL;
+          if (!(HL > 0.0 && HR > 0.0 && HL >= min_child_weight && HR >= min_child_weight)) continue;
+          const double gain = oracle_gain(GL, HL, GR, HR, G, H, lambda, gamma);
           if (gain > best.gain) {
             best.feature = f;
             best.bin = t;

@@ -382,3 +382,66 @@ def test_level_split_equals_exact_rational_argmax(oracle_mod, seed):
     assert st == oracle_mod.OK
     assert (out["feature"], out["bin"], out["default_left"]) == best[1:]
     assert out["gain"] == pytest.approx(float(best[0]), rel=1e-12)
+
+
+# --------------------------------------------------------------------------- float-cell mode
+def test_f64_build_matches_numpy_add_at(oracle_mod):
+    """Float cells: per node, rows in order, each bin one float64 chain; numpy's unbuffered add.at
+    processes the indices in the same order, so the sums agree bit for bit."""
+    rng = np.random.default_rng(21)
+    N, F, n_bins = 200, 4, 9
+    bins = rng.integers(0, n_bins, size=(F, N)).astype(np.uint8)
+    bins[rng.random(bins.shape) < 0.2] = 0xFF
+    gp = np.stack([rng.standard_normal(N), rng.uniform(0.1, 1, N)], 1).astype(np.float32)
+    rows = np.concatenate([np.sort(rng.choice(N, 70, replace=False)), np.sort(rng.choice(N, 40, replace=False))])
+    offs = np.array([0, 70, 110])
+    hist, ab, st = oracle_mod.build_hist_f64(bins, n_bins, 0xFF, gp, rows.astype(np.int32), offs)
+    assert st == oracle_mod.OK
+    for n in range(2):
+        rr = rows[offs[n]:offs[n + 1]]
+        for f in range(F):
+            slot = np.where(bins[f, rr] == 0xFF, n_bins, bins[f, rr]).astype(np.int64)
+            ref = np.zeros((n_bins + 1, 2))
+            np.add.at(ref[:, 0], slot, gp[rr, 0].astype(np.float64))
+            np.add.at(ref[:, 1], slot, gp[rr, 1].astype(np.float64))
+            np.testing.assert_array_equal(hist[n, f], ref)
+            rab = np.zeros(n_bins + 1)
+            np.add.at(rab, slot, np.abs(gp[rr, 0].astype(np.float64)))
+            np.testing.assert_array_equal(ab[n, f, :, 0], rab)
+
+
+def test_f64_constant_h_counts(oracle_mod):
+    """With h = 0.25 every H cell is count * 0.25 exactly (sums of 0.25 are exact)."""
+    rng = np.random.default_rng(22)
+    N, F, n_bins = 500, 3, 16
+    bins = rng.integers(0, n_bins, size=(F, N)).astype(np.uint8)
+    gp = np.stack([rng.standard_normal(N), np.full(N, 0.25)], 1).astype(np.float32)
+    hist, _, st = oracle_mod.build_hist_f64(bins, n_bins, 0xFF, gp, None, np.array([0, N]))
+    for f in range(F):
+        np.testing.assert_array_equal(hist[0, f, :n_bins, 1], np.bincount(bins[f], minlength=n_bins) * 0.25)
+
+
+def test_f64_subtract_clamps_hessian(oracle_mod):
+    """Large = parent - small; a negative H cell (rounding) is clamped to 0, G is kept."""
+    parent = np.zeros((1, 1, 3, 2))
+    small = np.zeros((1, 1, 3, 2))
+    parent[0, 0, :, 0] = [1.0, 2.0, 3.0]
+    parent[0, 0, :, 1] = [0.5, 0.25, 1.0]
+    small[0, 0, :, 0] = [0.5, 2.5, 1.0]
+    small[0, 0, :, 1] = [0.25, 0.25 + 2 ** -40, 0.5]
+    large, st = oracle_mod.subtract_f64(parent, None, small)
+    np.testing.assert_array_equal(large[0, 0, :, 0], [0.5, -0.5, 2.0])
+    np.testing.assert_array_equal(large[0, 0, :, 1], [0.25, 0.0, 0.5])
+
+
+def test_f64_find_on_integer_cells_equals_the_exact_path(oracle_mod):
+    """On integer-valued cells with unit scales the float-cell split find reduces to the fixed-point one."""
+    rng = np.random.default_rng(23)
+    for trial in range(10):
+        hist = _rand_hist(rng, 3, 5, 7, miss=bool(trial % 2))
+        a, _ = oracle_mod.find_splits(hist, 7, 1.0, 0.0, 0.0, 1.0, 1.0)
+        b, _ = oracle_mod.find_splits_f64(hist.astype(np.float64), 7, 1.0, 0.0, 0.0)
+        for k in ("feature", "bin", "default_left"):
+            np.testing.assert_array_equal(a[k], b[k])
+        np.testing.assert_array_equal(a["gain"], b["gain"])
+        np.testing.assert_array_equal(a["g_left"].astype(np.float64), b["g_left"])
