@@ -368,6 +368,40 @@ def run_gpu(args, rank, world, local_rank):
             obl = {"nodes": n_lvl, "ms_per_call": obl_t, "algorithmic_bytes": obl_bytes,
                    "achieved_gbs": obl_bytes / (obl_t / 1e3) / 1e9}
 
+        # ---------------------------------------------------------------- float-cell level (optional)
+        f64 = None
+        if args.f64 and lv.depth > 0:
+            hp64 = sess.build_level_f64(gp_d, torch.from_numpy(par.rows).to(dev), torch.from_numpy(par.offsets).to(dev))
+            hs64 = torch.empty((n_b, w.n_features, B, 2), dtype=torch.float64, device=dev)
+            large64 = torch.empty_like(hs64)
+            so64 = torch.empty_like(so)
+            lo64 = torch.empty_like(so)
+
+            def step64():
+                sess.check(g.gbt_build_level_f64(ctx, gp_d, rows_d, offs_d, n_b, hs64))
+                sess.check(g.gbt_subtract_siblings_f64(ctx, hp64, None, hs64, large64, n_p))
+                sess.check(g.gbt_find_splits_f64(ctx, hs64, n_b, prm, so64))
+                sess.check(g.gbt_find_splits_f64(ctx, large64, n_p, prm, lo64))
+
+            for i in range(3):
+                flush(i)
+                step64()
+            assert sess.sync() == 0
+            f64_ms = []
+            for i in range(args.steps):
+                flush(i)
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                step64()
+                b.record(stream)
+                b.synchronize()
+                f64_ms.append(a.elapsed_time(b))
+            assert sess.sync() == 0
+            f64_t = statistics.median(f64_ms)
+            f64 = {"ms_per_step": f64_t, "entries_per_s": entries / (f64_t / 1e3),
+                   "note": "same level in double cells of the unquantised float32 gpair"}
+            del hp64, hs64, large64
+
         # ---------------------------------------------------------------- e2e through host buffers
         e2e = None
         if lv.depth > 0:
@@ -453,6 +487,8 @@ def run_gpu(args, rank, world, local_rank):
         peak_v, _ = _peaks()
         obl["frac"] = obl["achieved_gbs"] / peak_v
         line["oblivious_split"] = obl
+    if f64 is not None:
+        line["float_cells"] = f64
     print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()
@@ -488,6 +524,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOAD_TEXT), default="level5")
     ap.add_argument("--path", choices=["fused", "unfused"], default="fused")
+    ap.add_argument("--f64", action="store_true",
+                    help="also time the level in float-cell mode (double cells; reported under float_cells)")
     ap.add_argument("--oblivious", action="store_true",
                     help="also time gbt_find_level_split on the level's histograms (reported under oblivious_split)")
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle time for cpu_baseline")

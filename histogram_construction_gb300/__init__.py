@@ -27,7 +27,8 @@ EXPORTS = [
     "gbt_suggest_scales", "gbt_build_level", "gbt_subtract_siblings", "gbt_find_splits", "gbt_subtract_and_find",
     "gbt_level_step",
     "gbt_partition_level", "gbt_profile_enable", "gbt_profile_read", "gbt_slots_per_feature",
-    "gbt_kernel_launches", "gbt_find_splits_noalloc", "gbt_find_level_split",
+    "gbt_kernel_launches", "gbt_find_splits_noalloc", "gbt_find_level_split", "gbt_build_level_f64",
+    "gbt_subtract_siblings_f64", "gbt_find_splits_f64",
 ]
 
 
@@ -86,6 +87,9 @@ def lib(build_if_missing: bool = True):
         "gbt_kernel_launches": (i64, [vp]),
         "gbt_find_splits_noalloc": (st, [vp, i32, i32, i32, f32, f32, ctypes.POINTER(GbtParams), vp, vp]),
         "gbt_find_level_split": (st, [vp, vp, i32, ctypes.POINTER(GbtParams), vp]),
+        "gbt_build_level_f64": (st, [vp, vp, vp, vp, i32, vp]),
+        "gbt_subtract_siblings_f64": (st, [vp, vp, vp, vp, vp, i32]),
+        "gbt_find_splits_f64": (st, [vp, vp, i32, ctypes.POINTER(GbtParams), vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(L, name)
@@ -175,6 +179,19 @@ def gbt_subtract_siblings(ctx, parent_hist, parent_of, small_hist, large_hist, n
 
 def gbt_find_splits(ctx, hist, n_nodes, prm, out):
     return lib().gbt_find_splits(ctx, ptr(hist), int(n_nodes), ctypes.byref(prm), ptr(out))
+
+
+def gbt_build_level_f64(ctx, gpair, rows, node_offsets, n_nodes, hist_out):
+    return lib().gbt_build_level_f64(ctx, ptr(gpair), ptr(rows), ptr(node_offsets), int(n_nodes), ptr(hist_out))
+
+
+def gbt_subtract_siblings_f64(ctx, parent_hist, parent_of, small_hist, large_hist, n_pairs):
+    return lib().gbt_subtract_siblings_f64(ctx, ptr(parent_hist), ptr(parent_of), ptr(small_hist), ptr(large_hist),
+                                           int(n_pairs))
+
+
+def gbt_find_splits_f64(ctx, hist, n_nodes, prm, out):
+    return lib().gbt_find_splits_f64(ctx, ptr(hist), int(n_nodes), ctypes.byref(prm), ptr(out))
 
 
 def gbt_find_level_split(ctx, hist, n_nodes, prm, out):

@@ -17,6 +17,7 @@
 
 #include "../../include/gbthist.h"
 #include "common.cuh"
+#include "k_f64.cuh"
 #include "k_hist.cuh"
 #include "k_level_split.cuh"
 #include "k_partition.cuh"
@@ -27,6 +28,7 @@ using namespace gbt;
 
 static_assert(sizeof(gbt_split) == 56, "gbt_split layout");
 static_assert(sizeof(SplitOut) == sizeof(gbt_split), "device split layout");
+static_assert(sizeof(gbt_split_f64) == sizeof(gbt_split), "float-cell split layout");
 
 namespace {
 
@@ -526,10 +528,26 @@ gbt_status gbt_suggest_scales(int64_t rows_per_partial, float max_abs_g, float m
 
 namespace {
 
+// ts features per float-cell work item: a [B][ts][2] double image within the shared budget.
+int f64_ts_for(int B) {
+  for (int ts = 32; ts >= 2; ts >>= 1)
+    if ((int64_t)ts * B * 16 <= HF_SMEM_MAX) return ts;
+  return 0;
+}
+
+template <typename T, int TS>
+cudaError_t launch_hist_f64(gbt_ctx *c, int ctas, size_t smem, const HistF64Params &hp) {
+  cudaError_t e = cudaFuncSetAttribute(k_hist_f64<T, TS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(c, k_hist_f64<T, TS>, dim3(ctas), dim3(HF_THREADS), smem, hp);
+}
+
 // Validate the level inputs, plan the work items on the device and run the
-// histogram kernel, which leaves exact int32 partials per item in c->partial.
+// histogram kernel, which leaves the group images in c->partial: exact int32
+// sums of the quantised pairs, or, when gpair_f64 (device float (g, h) pairs)
+// is given, double sums of those pairs.
 gbt_status run_level_build(gbt_ctx *c, const int32_t *rows, const int64_t *node_offsets, int32_t n_nodes,
-                           LevelParams *out_lp) {
+                           LevelParams *out_lp, const float2 *gpair_f64 = nullptr) {
   const int B = c->n_bins + 1;
   const void *offs_d = nullptr;
   int64_t R_host = -1;
@@ -556,32 +574,37 @@ gbt_status run_level_build(gbt_ctx *c, const int32_t *rows, const int64_t *node_
   }
   s = ensure(c, c->chunk_prefix, (size_t)2 * (n_nodes + 1) * sizeof(int32_t), "chunk and group prefixes");
   if (s != GBT_OK) return s;
-  if (!c->qmax_known) {
+  const bool f64 = gpair_f64 != nullptr;
+  if (!f64 && !c->qmax_known) {
     CUDA_TRY(c, cudaEventSynchronize(c->ev_q), "wait for max|q|");
     c->qmax = c->err_host[1];
     c->qmax_known = true;
   }
+  const int ts64 = f64 ? f64_ts_for(B) : 0;
+  if (f64 && ts64 == 0) return fail(c, GBT_ERR_UNSUPPORTED, "n_bins too large for the float-cell histogram");
 
   LevelParams lp;
   lp.rows = (const int32_t *)rows_d;
   lp.offs = (const int64_t *)offs_d;
   lp.n_nodes = n_nodes;
-  lp.item_feats = c->bin_bytes == 1 ? 64 : c->ts16;
+  lp.item_feats = f64 ? ts64 : (c->bin_bytes == 1 ? 64 : c->ts16);
   lp.n_fgroups = (c->n_features + lp.item_feats - 1) / lp.item_feats;
   lp.target_items = c->target_items > 0 ? c->target_items : c->n_sm * 2;
   lp.n_rows = c->n_rows;
   lp.q = (const int2 *)c->q.p;
   lp.chunk_prefix = (int32_t *)c->chunk_prefix.p;
   lp.group_prefix = lp.chunk_prefix + (n_nodes + 1);
-  lp.sbw = c->bin_bytes == 1 ? 16 : c->ts16;
-  lp.nsb = c->bin_bytes == 1 ? H8_SB : 1;
-  lp.image_int4s = (int64_t)lp.nsb * lp.sbw * B / 2;  // nsb x B x sbw (G, H) int32 pairs
+  lp.sbw = f64 ? ts64 : (c->bin_bytes == 1 ? 16 : c->ts16);
+  lp.nsb = (!f64 && c->bin_bytes == 1) ? H8_SB : 1;
+  // nsb x B x sbw (G, H) pairs: int32 pairs (8 bytes), or double pairs (16 bytes) for float cells
+  lp.image_int4s = f64 ? (int64_t)lp.sbw * B : (int64_t)lp.nsb * lp.sbw * B / 2;
+  lp.qmax_plan = f64 ? 1u : 0u;  // float cells: any number of rows adds into one image
   lp.st = c->st;
   // image scratch for the largest item count the device plan can produce
   // (there are never more group images than items):
   // items <= n_fgroups * n_nodes + max(target_items, n_fgroups * n_rows / rows_per_chunk_min)
   // (a chunk holds at least min(rc, load-balance target) rows, and rc >= 1024 by the quantisation limit)
-  const int64_t rc = std::max<int64_t>(1, 2147483647LL / std::max<int64_t>(c->qmax, 1));
+  const int64_t rc = std::max<int64_t>(1, 2147483647LL / std::max<int64_t>(f64 ? 1 : c->qmax, 1));
   const int64_t items_max = (int64_t)lp.n_fgroups * (n_nodes + 1) +
                             std::max<int64_t>(lp.target_items, (int64_t)lp.n_fgroups * ((c->n_rows + rc - 1) / rc));
   if (items_max > INT32_MAX / 2) return fail(c, GBT_ERR_UNSUPPORTED, "level too large for the work-item plan");
@@ -593,7 +616,32 @@ gbt_status run_level_build(gbt_ctx *c, const int32_t *rows, const int64_t *node_
   k_level_plan<<<c->n_sm, PLAN_THREADS, 0, c->stream>>>(lp);
   LAUNCH_CHECK(c, "k_level_plan");
   const int hist_ctas = c->n_sm;  // persistent: one resident CTA per SM
-  if (c->bin_bytes == 1) {
+  if (f64) {
+    HistF64Params hp;
+    hp.lv = lp;
+    hp.mirror = (const unsigned char *)c->mirror.p;
+    hp.gpair = gpair_f64;
+    hp.n_features = c->n_features;
+    hp.n_slots = B;
+    hp.n_bins = c->n_bins;
+    hp.tile_feats = c->tile_feats;
+    const size_t smem = (size_t)B * ts64 * 16;
+    cudaError_t e = cudaSuccess;
+    prof_begin(c);
+    if (c->bin_bytes == 1) {
+      e = launch_hist_f64<uint8_t, 32>(c, hist_ctas, smem, hp);
+    } else {
+      switch (ts64) {
+        case 32: e = launch_hist_f64<uint16_t, 32>(c, hist_ctas, smem, hp); break;
+        case 16: e = launch_hist_f64<uint16_t, 16>(c, hist_ctas, smem, hp); break;
+        case 8: e = launch_hist_f64<uint16_t, 8>(c, hist_ctas, smem, hp); break;
+        case 4: e = launch_hist_f64<uint16_t, 4>(c, hist_ctas, smem, hp); break;
+        default: e = launch_hist_f64<uint16_t, 2>(c, hist_ctas, smem, hp); break;
+      }
+    }
+    if (e != cudaSuccess) return cuda_fail(c, e, "k_hist_f64");
+    LAUNCH_CHECK(c, "k_hist_f64");
+  } else if (c->bin_bytes == 1) {
     Hist8Params hp;
     hp.lv = lp;
     hp.mirror = (const uint8_t *)c->mirror.p;
@@ -731,6 +779,82 @@ gbt_status gbt_find_splits(gbt_ctx *c, const int64_t *hist, int32_t n_nodes, con
   LAUNCH_CHECK(c, "k_find");
   if (host)
     CUDA_TRY(c, cudaMemcpyAsync(out, dout, (size_t)n_nodes * sizeof(gbt_split), cudaMemcpyDeviceToHost, c->stream),
+             "splits to host");
+  return GBT_OK;
+}
+
+gbt_status gbt_build_level_f64(gbt_ctx *c, const float *gpair, const int32_t *rows, const int64_t *node_offsets,
+                               int32_t n_nodes, double *hist_out) {
+  gbt_status s = check_ctx(c);
+  if (s != GBT_OK) return s;
+  if (c->n_rows == 0) return fail(c, GBT_ERR_STATE, "gbt_upload_bins first");
+  if (n_nodes < 0 || n_nodes > 65535) return fail(c, GBT_ERR_UNSUPPORTED, "n_nodes must be in [0, 65535]");
+  if (!gpair || !node_offsets || !hist_out) return fail(c, GBT_ERR_INVALID_ARG, "gpair, node_offsets, hist_out required");
+  if (ptr_kind(hist_out) != 1 || !aligned16(hist_out))
+    return fail(c, GBT_ERR_INVALID_ARG, "hist_out must be 16-byte aligned device memory");
+  if (n_nodes == 0) return GBT_OK;
+  const void *gp = nullptr;
+  s = device_view(c, gpair, (size_t)c->n_rows * 2 * sizeof(float), c->gp_stage, &gp, "gpair");
+  if (s != GBT_OK) return s;
+  if ((reinterpret_cast<uintptr_t>(gp) & 7u) != 0) return fail(c, GBT_ERR_INVALID_ARG, "gpair must be 8-byte aligned");
+  LevelParams lp;
+  s = run_level_build(c, rows, node_offsets, n_nodes, &lp, (const float2 *)gp);
+  if (s != GBT_OK) return s;
+  const int B = c->n_bins + 1;
+  const int64_t cells = (int64_t)n_nodes * c->n_features * B;
+  prof_begin(c);
+  launch_pdl(c, k_finalize_f64, dim3(grid_for(c, cells, 256, 8)), dim3(256), 0, (const double *)lp.partial,
+             (const int32_t *)lp.group_prefix, (int64_t)lp.image_int4s * 2, lp.n_fgroups, lp.item_feats, n_nodes,
+             c->n_features, B, hist_out, (const DevState *)c->st);
+  LAUNCH_CHECK(c, "k_finalize_f64");
+  return GBT_OK;
+}
+
+gbt_status gbt_subtract_siblings_f64(gbt_ctx *c, const double *parent_hist, const int32_t *parent_of,
+                                     const double *small_hist, double *large_hist, int32_t n_pairs) {
+  gbt_status s = check_ctx(c);
+  if (s != GBT_OK) return s;
+  if (c->n_rows == 0) return fail(c, GBT_ERR_STATE, "gbt_upload_bins first");
+  if (n_pairs < 0) return fail(c, GBT_ERR_INVALID_ARG, "n_pairs < 0");
+  if (n_pairs == 0) return GBT_OK;
+  for (const void *p : {(const void *)parent_hist, (const void *)small_hist, (const void *)large_hist})
+    if (ptr_kind(p) != 1 || !aligned16(p)) return fail(c, GBT_ERR_INVALID_ARG, "histograms must be 16-byte aligned device memory");
+  const int32_t *po = nullptr;
+  s = parent_of_view(c, parent_of, n_pairs, &po);
+  if (s != GBT_OK) return s;
+  const int64_t cpn = (int64_t)c->n_features * (c->n_bins + 1);
+  prof_begin(c);
+  k_subtract_f64<<<grid_for(c, (int64_t)n_pairs * cpn, 256, 8), 256, 0, c->stream>>>(parent_hist, po, small_hist,
+                                                                                       large_hist, n_pairs, cpn);
+  LAUNCH_CHECK(c, "k_subtract_f64");
+  return GBT_OK;
+}
+
+gbt_status gbt_find_splits_f64(gbt_ctx *c, const double *hist, int32_t n_nodes, const gbt_params *params,
+                               gbt_split_f64 *out) {
+  gbt_status s = check_ctx(c);
+  if (s != GBT_OK) return s;
+  if (c->n_rows == 0) return fail(c, GBT_ERR_STATE, "gbt_upload_bins first");
+  if (!params || n_nodes < 0) return fail(c, GBT_ERR_INVALID_ARG, "params NULL or n_nodes < 0");
+  if (n_nodes == 0) return GBT_OK;
+  if (n_nodes > 65535) return fail(c, GBT_ERR_UNSUPPORTED, "n_nodes must be <= 65535");
+  if (ptr_kind(hist) != 1 || !aligned16(hist)) return fail(c, GBT_ERR_INVALID_ARG, "hist must be 16-byte aligned device memory");
+  SplitOut *dout = nullptr;
+  bool host = false;
+  s = split_out_view(c, reinterpret_cast<gbt_split *>(out), n_nodes, c->splits_a, &dout, &host);
+  if (s != GBT_OK) return s;
+  const int nfb = (c->n_features + SCAN_WARPS - 1) / SCAN_WARPS;
+  s = ensure(c, c->cand, (size_t)n_nodes * nfb * sizeof(Cand), "candidates");
+  if (s != GBT_OK) return s;
+  s = ensure_counters(c, (size_t)n_nodes);
+  if (s != GBT_OK) return s;
+  prof_begin(c);
+  k_find_f64<<<dim3(nfb, n_nodes), SCAN_THREADS, 0, c->stream>>>(hist, c->n_features, c->n_bins, params->lambda,
+                                                                 params->gamma, params->min_child_weight,
+                                                                 (Cand *)c->cand.p, (uint32_t *)c->counters.p, dout);
+  LAUNCH_CHECK(c, "k_find_f64");
+  if (host)
+    CUDA_TRY(c, cudaMemcpyAsync(out, dout, (size_t)n_nodes * sizeof(gbt_split_f64), cudaMemcpyDeviceToHost, c->stream),
              "splits to host");
   return GBT_OK;
 }

@@ -46,6 +46,7 @@ struct LevelParams {
   int64_t image_int4s;    // 16-byte units per image
   int32_t sbw;            // features per sub-block of the image (16 for u8, TS for u16)
   int32_t nsb;            // sub-blocks per image (4 for u8, 1 for u16)
+  uint32_t qmax_plan;     // if nonzero, the plan's exactness bound uses it instead of the tree's max|q|
   DevState *st;
 };
 
@@ -110,7 +111,7 @@ __global__ void __launch_bounds__(PLAN_THREADS) k_level_plan(LevelParams p) {
   }
   if (tid == 0) {
     const int64_t R = p.offs[p.n_nodes];
-    const uint32_t qm = max(p.st->qmax, 1u);
+    const uint32_t qm = max(p.qmax_plan ? p.qmax_plan : p.st->qmax, 1u);
     const int64_t rc = 2147483647LL / (int64_t)qm;  // rows whose int32 partials cannot overflow
     int64_t tgt = (R * p.n_fgroups + p.target_items - 1) / max(p.target_items, 1);
     tgt = max(tgt, (int64_t)CHUNK_MIN_ROWS);

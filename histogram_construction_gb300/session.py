@@ -8,21 +8,28 @@ from __future__ import annotations
 
 import numpy as np
 
-from . import (GBT_OK, SPLIT_BYTES, check, gbt_begin_tree, gbt_build_level, gbt_create, gbt_destroy,
-               gbt_find_level_split, gbt_find_splits, gbt_kernel_launches, gbt_level_step, gbt_partition_level, gbt_subtract_and_find,
-               gbt_subtract_siblings, gbt_sync, gbt_upload_bins, lib, params)
+from . import (GBT_OK, SPLIT_BYTES, check, gbt_begin_tree, gbt_build_level, gbt_build_level_f64, gbt_create,
+               gbt_destroy, gbt_find_level_split, gbt_find_splits, gbt_find_splits_f64, gbt_kernel_launches,
+               gbt_level_step, gbt_partition_level, gbt_subtract_and_find, gbt_subtract_siblings,
+               gbt_subtract_siblings_f64, gbt_sync, gbt_upload_bins, lib, params)
 
 SPLIT_DTYPE = np.dtype([
     ("feature", "<i4"), ("bin", "<i4"), ("default_left", "u1"), ("pad", "u1", (7,)), ("gain", "<f8"),
     ("g_left", "<i8"), ("h_left", "<i8"), ("g_right", "<i8"), ("h_right", "<i8"),
 ])
 assert SPLIT_DTYPE.itemsize == SPLIT_BYTES
+# float-cell mode: the same record with double sums
+SPLIT_F64_DTYPE = np.dtype([
+    ("feature", "<i4"), ("bin", "<i4"), ("default_left", "u1"), ("pad", "u1", (7,)), ("gain", "<f8"),
+    ("g_left", "<f8"), ("h_left", "<f8"), ("g_right", "<f8"), ("h_right", "<f8"),
+])
+assert SPLIT_F64_DTYPE.itemsize == SPLIT_BYTES
 
 
-def splits_to_numpy(t) -> np.ndarray:
+def splits_to_numpy(t, dtype=SPLIT_DTYPE) -> np.ndarray:
     """A [n, 56] uint8 tensor (device or host) -> numpy structured array of splits."""
     a = t.detach().to("cpu").contiguous().numpy()
-    return a.view(SPLIT_DTYPE).reshape(-1)
+    return a.view(dtype).reshape(-1)
 
 
 class Session:
@@ -129,6 +136,38 @@ class Session:
         """One oblivious split for all nodes of `hist` ([n][F][B][2] int64): a [1, 56] uint8 tensor."""
         out = self.torch.empty((1, SPLIT_BYTES), dtype=self.torch.uint8, device=self.device)
         self.check(gbt_find_level_split(self.ctx, hist, hist.shape[0], params(lam, gamma, mcw), out))
+        return out
+
+    # ------------------------------------------------------- float-cell mode
+    def build_level_f64(self, gpair, rows, offsets, hist=None):
+        """Double-cell histogram of the unquantised float32 gpair ([N][2], host or device): [n][F][B][2] float64."""
+        n_nodes = int(len(offsets) - 1)
+        if hist is None:
+            hist = self.torch.empty((n_nodes, self.n_features, self.n_bins + 1, 2), dtype=self.torch.float64,
+                                    device=self.device)
+        r = self.to_dev(rows, self.torch.int32)
+        o = self.to_dev(offsets, self.torch.int64)
+        if isinstance(gpair, np.ndarray):  # host gpair: the library stages it; keep it alive until the copy is done
+            gp = np.ascontiguousarray(gpair, dtype=np.float32)
+            self.check(gbt_build_level_f64(self.ctx, gp, r, o, n_nodes, hist))
+            self.check(self.sync())
+        else:
+            gp = gpair.to(device=self.device, dtype=self.torch.float32).contiguous()
+            self.check(gbt_build_level_f64(self.ctx, gp, r, o, n_nodes, hist))
+        return hist
+
+    def subtract_f64(self, parent, small, parent_of=None, large=None):
+        n_pairs = small.shape[0]
+        if large is None:
+            large = self.torch.empty_like(small)
+        po = self.to_dev(parent_of, self.torch.int32)
+        self.check(gbt_subtract_siblings_f64(self.ctx, parent, po, small, large, n_pairs))
+        return large
+
+    def find_splits_f64(self, hist, lam=1.0, gamma=0.0, mcw=0.0):
+        n = hist.shape[0]
+        out = self.torch.empty((n, SPLIT_BYTES), dtype=self.torch.uint8, device=self.device)
+        self.check(gbt_find_splits_f64(self.ctx, hist, n, params(lam, gamma, mcw), out))
         return out
 
     def subtract_and_find(self, parent, small, parent_of=None, large=None, lam=1.0, gamma=0.0, mcw=0.0):

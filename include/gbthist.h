@@ -61,6 +61,17 @@ typedef struct {
   int64_t g_left, h_left, g_right, h_right;
 } gbt_split; /* 56 bytes */
 
+/* The best split of one node in the float-cell mode: as gbt_split, with the
+ * left/right sums as doubles. */
+typedef struct {
+  int32_t feature;
+  int32_t bin;
+  uint8_t default_left;
+  uint8_t pad[7];
+  double gain;
+  double g_left, h_left, g_right, h_right;
+} gbt_split_f64; /* 56 bytes */
+
 /* lambda: L2 regulariser; gamma: per-split penalty; min_child_weight: minimum
  * converted hessian on each side (0 disables). */
 typedef struct {
@@ -158,6 +169,32 @@ gbt_status gbt_subtract_siblings(gbt_ctx *ctx, const int64_t *parent_hist, const
  *   out: host or device gbt_split [n_nodes] (host: valid after gbt_sync). */
 gbt_status gbt_find_splits(gbt_ctx *ctx, const int64_t *hist, int32_t n_nodes, const gbt_params *params,
                            gbt_split *out);
+
+/* Float-cell mode [bonsai "10: CUDA histogram backend", "The kernel": float
+ * shared-memory cells merged into double global cells; "GBDT engine
+ * engineering deep-dive", section 7 listing; section 3: the hessian is
+ * clamped at zero after subtraction]. Cells are double sums of the
+ * unquantised float32 (g, h); the order of the additions is not fixed, so
+ * cells agree with a serial double sum to rounding (the tests use
+ * |a - b| <= 1e-5 * (sum of |g| over the cell's rows)), not bit for bit.
+ *   gpair: host or device float32 [n_rows][2], read during the call's stream work.
+ *   rows, node_offsets: as gbt_build_level. hist_out: device, 16-byte aligned,
+ *   [n_nodes][n_features][B][2] double, overwritten. Needs gbt_upload_bins
+ *   only (no gbt_begin_tree). Limits: as gbt_build_level; u16 n_bins <= 5119. */
+gbt_status gbt_build_level_f64(gbt_ctx *ctx, const float *gpair, const int32_t *rows, const int64_t *node_offsets,
+                               int32_t n_nodes, double *hist_out);
+
+/* large[p] = parent[parent_of[p]] - small[p] in double, a negative hessian
+ * cell clamped to 0. Histograms: device [..][F][B][2] double, 16-byte aligned. */
+gbt_status gbt_subtract_siblings_f64(gbt_ctx *ctx, const double *parent_hist, const int32_t *parent_of,
+                                     const double *small_hist, double *large_hist, int32_t n_pairs);
+
+/* gbt_find_splits on double cells: the same candidates, gain formula and
+ * tie-break, values used as they are (no scale), a candidate valid iff both
+ * sides' H > 0 and >= min_child_weight; every candidate evaluated in double.
+ *   hist: device [n_nodes][F][B][2] double. out: host or device gbt_split_f64. */
+gbt_status gbt_find_splits_f64(gbt_ctx *ctx, const double *hist, int32_t n_nodes, const gbt_params *params,
+                               gbt_split_f64 *out);
 
 /* The split of an oblivious (symmetric) tree level: one feature, cut and
  * missing direction for every node ["GBDT engine engineering deep-dive",

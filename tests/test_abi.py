@@ -12,7 +12,7 @@ def _declared():
     with open(os.path.join(ROOT, "include", "gbthist.h")) as f:
         text = f.read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(gbt_[a-z_]+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(gbt_[a-z0-9_]+)\s*\(", text)))
 
 
 def test_library_builds_and_exports_header_symbols():

@@ -1,0 +1,235 @@
+"""GPU parity of the float-cell mode (double cells of the unquantised float32
+gpair, clamped subtraction, double split find) against the serial oracle.
+
+Two bars:
+  * dyadic gpair (every g, h a multiple of 2^-10 with |g| < 2^4): every partial
+    sum is exact in double, so the order of the additions cannot matter and
+    histograms, subtraction and splits (gains included) are compared bit for bit;
+  * generic float gpair: a cell summed from n values in any order is within
+    (n - 1) * 2^-53 * (sum of |x|) of the exact sum, so the GPU and the serial
+    oracle differ by at most twice that (the test takes n = the node's rows);
+    the split found on the GPU's histogram is checked against the oracle's
+    split of the same histogram: the same gain within 1e-12 relative, and the
+    same (feature, bin, direction) unless another candidate's gain is that close.
+"""
+import numpy as np
+import pytest
+
+import synth
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+U = 2.0 ** -53
+
+
+@pytest.fixture(scope="module")
+def gb():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import histogram_construction_gb300 as g
+    from histogram_construction_gb300.session import SPLIT_F64_DTYPE, Session, splits_to_numpy
+    g.lib()
+    return g, Session, lambda t: splits_to_numpy(t, SPLIT_F64_DTYPE)
+
+
+@pytest.fixture(scope="module")
+def oracle():
+    import oracle as o
+    return o
+
+
+def dyadic(gp):
+    """Round g to a multiple of 2^-10 and h to a positive multiple of 2^-10."""
+    out = np.empty_like(gp)
+    out[:, 0] = np.round(gp[:, 0] * 1024.0) / 1024.0
+    out[:, 1] = np.maximum(np.round(gp[:, 1] * 1024.0), 1.0) / 1024.0
+    return out
+
+
+def assert_cells_close(got, ref, ab, offsets, where):
+    n_rows = np.diff(np.asarray(offsets, dtype=np.int64)).astype(np.float64)
+    tol = 2.0 * np.maximum(n_rows - 1.0, 0.0)[:, None, None, None] * U * ab
+    err = np.abs(got - ref)
+    bad = err > tol
+    assert not bad.any(), f"{where}: {int(bad.sum())} cells off, worst {float((err - tol).max())}"
+
+
+def assert_splits_bitwise(got, ref, where):
+    for k in ("feature", "bin", "default_left"):
+        np.testing.assert_array_equal(got[k], ref[k], err_msg=f"{where} {k}")
+    for k in ("gain", "g_left", "h_left", "g_right", "h_right"):
+        np.testing.assert_array_equal(got[k].view(np.int64), ref[k].view(np.int64), err_msg=f"{where} {k}")
+
+
+def assert_splits_close(got, ref, hist, n_bins, lam, gamma, mcw, oracle, where):
+    """got: GPU splits of `hist`; ref: oracle splits of the same histogram."""
+    for n in range(got.shape[0]):
+        if ref["feature"][n] < 0:
+            assert got["feature"][n] < 0 or not np.isfinite(got["gain"][n]), f"{where} node {n}"
+            continue
+        g, r = float(got["gain"][n]), float(ref["gain"][n])
+        assert abs(g - r) <= 1e-12 * max(1.0, abs(r)), f"{where} node {n}: gain {g} vs {r}"
+        same = (got["feature"][n], got["bin"][n], got["default_left"][n]) == \
+               (ref["feature"][n], ref["bin"][n], ref["default_left"][n])
+        if not same:
+            # another candidate within rounding of the best: its own oracle gain must be that close too
+            f, t, d = int(got["feature"][n]), int(got["bin"][n]), int(got["default_left"][n])
+            hf = hist[n, f]
+            G, H = hf[:, 0].sum(), hf[:, 1].sum()
+            GL = hf[:t + 1, 0].sum() + (hf[n_bins, 0] if d else 0.0)
+            HL = hf[:t + 1, 1].sum() + (hf[n_bins, 1] if d else 0.0)
+            alt = oracle.gain(GL, HL, G - GL, H - HL, G, H, lam, gamma)
+            assert abs(alt - r) <= 1e-12 * max(1.0, abs(r)), f"{where} node {n}: chose {(f, t, d)} gain {alt} vs {r}"
+        for k in ("g_left", "h_left", "g_right", "h_right"):
+            a, b = float(got[k][n]), float(ref[k][n])
+            if same:
+                assert abs(a - b) <= 1e-9 * max(1.0, abs(b)), f"{where} node {n} {k}: {a} vs {b}"
+
+
+def level_pair(sess, oracle, w, depth, gp, lam=1.0, gamma=0.0, mcw=0.0, exact=True, device_gp=True):
+    """Parents at depth-1 (all their rows), the smaller siblings at depth, subtract, find; compare everything."""
+    par, lv = w.levels[depth - 1], w.levels[depth]
+    gpa = torch.from_numpy(gp).cuda() if device_gp else gp
+    hp = sess.build_level_f64(gpa, par.rows, torch.from_numpy(par.offsets).cuda())
+    hs = sess.build_level_f64(gpa, lv.built_rows, lv.built_offsets)
+    large = sess.subtract_f64(hp, hs)
+    so = sess.find_splits_f64(hs, lam, gamma, mcw)
+    lo = sess.find_splits_f64(large, lam, gamma, mcw)
+    assert sess.sync() == 0
+    ref_hp, ab_p, st = oracle.build_hist_f64(w.bins, w.n_bins, w.sentinel, gp, par.rows, par.offsets)
+    assert st == oracle.OK
+    ref_hs, ab_s, st = oracle.build_hist_f64(w.bins, w.n_bins, w.sentinel, gp, lv.built_rows, lv.built_offsets)
+    assert st == oracle.OK
+    g_hp, g_hs, g_large = hp.cpu().numpy(), hs.cpu().numpy(), large.cpu().numpy()
+    if exact:
+        np.testing.assert_array_equal(g_hp, ref_hp, err_msg="parent hist")
+        np.testing.assert_array_equal(g_hs, ref_hs, err_msg="small hist")
+    else:
+        assert_cells_close(g_hp, ref_hp, ab_p, par.offsets, "parent hist")
+        assert_cells_close(g_hs, ref_hs, ab_s, lv.built_offsets, "small hist")
+    # subtraction: one rounding per cell on the GPU's own operands, so bit-exact against the oracle's
+    ref_large, st = oracle.subtract_f64(g_hp, None, g_hs)
+    assert st == oracle.OK
+    np.testing.assert_array_equal(g_large, ref_large, err_msg="large hist")
+    for name, h, s in (("small", g_hs, so), ("large", g_large, lo)):
+        ref, st = oracle.find_splits_f64(h, w.n_bins, lam, gamma, mcw)
+        assert st == oracle.OK
+        got = gb_split(s)
+        if exact:
+            assert_splits_bitwise(got, ref, f"{name} splits")
+        else:
+            assert_splits_close(got, ref, h, w.n_bins, lam, gamma, mcw, oracle, f"{name} splits")
+    return g_hp, g_hs, g_large
+
+
+gb_split = None
+
+
+@pytest.fixture(autouse=True)
+def _split_reader(gb):
+    global gb_split
+    gb_split = gb[2]
+
+
+def test_level5_dyadic_bitexact(gb, oracle):
+    g, Session, _ = gb
+    w = synth.make("level5", n_rows=120_000, n_features=70, depth=3)
+    gp = dyadic(w.gpair)
+    with Session() as s:
+        s.upload_bins(w.bins, w.n_bins, w.sentinel)
+        for d in (1, 3):
+            level_pair(s, oracle, w, d, gp)
+        level_pair(s, oracle, w, 2, gp, lam=0.5, gamma=0.25, mcw=3.0, device_gp=False)
+
+
+def test_level5_float_within_rounding(gb, oracle):
+    g, Session, _ = gb
+    w = synth.make("level5", n_rows=150_000, n_features=45, depth=3)
+    with Session() as s:
+        s.upload_bins(w.bins, w.n_bins, w.sentinel)
+        for d in (1, 2, 3):
+            level_pair(s, oracle, w, d, w.gpair, exact=False)
+
+
+def test_root_identity_rows(gb, oracle):
+    """rows = None (identity) for the root; one node; tiny feature count."""
+    g, Session, _ = gb
+    w = synth.make("root")
+    gp = dyadic(w.gpair)
+    with Session() as s:
+        s.upload_bins(w.bins, w.n_bins, w.sentinel)
+        offs = np.array([0, w.n_rows], dtype=np.int64)
+        h = s.build_level_f64(torch.from_numpy(gp).cuda(), None, offs)
+        sp = s.find_splits_f64(h, 1.0, 0.0, 1.0)
+        assert s.sync() == 0
+        ref, _, st = oracle.build_hist_f64(w.bins, w.n_bins, w.sentinel, gp, None, offs)
+        np.testing.assert_array_equal(h.cpu().numpy(), ref)
+        rs, _ = oracle.find_splits_f64(ref, w.n_bins, 1.0, 0.0, 1.0)
+        assert_splits_bitwise(gb_split(sp), rs, "root")
+
+
+def test_wide_ragged_feature_groups(gb, oracle):
+    """4133 features: 130 float-cell feature groups of 32, the last holding 5; 2 KB-wide mirror rows."""
+    g, Session, _ = gb
+    w = synth.make("wide", n_rows=8192, n_features=4133)
+    gp = dyadic(w.gpair)
+    with Session() as s:
+        s.upload_bins(w.bins, w.n_bins, w.sentinel)
+        level_pair(s, oracle, w, w.target_depth, gp)
+
+
+def test_u16_missing(gb, oracle):
+    """u16 bins, 4096 bins + missing slot, 40% missing: two features per work item."""
+    g, Session, _ = gb
+    w = synth.make("u16miss", n_rows=60_000, n_features=11, depth=3)
+    gp = dyadic(w.gpair)
+    with Session() as s:
+        s.upload_bins(w.bins, w.n_bins, w.sentinel)
+        level_pair(s, oracle, w, 3, gp)
+        level_pair(s, oracle, w, 2, w.gpair, exact=False, mcw=1.0)
+
+
+def test_empty_nodes_and_clamp(gb, oracle):
+    g, Session, _ = gb
+    w = synth.make("level5", n_rows=20_000, n_features=9, depth=1)
+    gp = dyadic(w.gpair)
+    with Session() as s:
+        s.upload_bins(w.bins, w.n_bins, w.sentinel)
+        rows = w.levels[1].rows
+        n1 = int(w.levels[1].offsets[1])
+        offs = np.array([0, 0, n1, n1, len(rows), len(rows)], dtype=np.int64)  # empty nodes 0, 2, 4
+        h = s.build_level_f64(gp, rows, offs)
+        sp = s.find_splits_f64(h)
+        assert s.sync() == 0
+        ref, _, _ = oracle.build_hist_f64(w.bins, w.n_bins, w.sentinel, gp, rows, offs)
+        np.testing.assert_array_equal(h.cpu().numpy(), ref)
+        got = gb_split(sp)
+        assert (got["feature"][[0, 2, 4]] == -1).all() and np.isneginf(got["gain"][[0, 2, 4]]).all()
+        assert_splits_bitwise(got, oracle.find_splits_f64(ref, w.n_bins, 1.0, 0.0, 0.0)[0], "empty")
+        # clamp: a small sibling whose H exceeds the parent's by rounding-sized amounts
+        rng = np.random.default_rng(7)
+        par = rng.standard_normal((3, 9, w.n_bins + 1, 2))
+        par[..., 1] = np.abs(par[..., 1])
+        small = par.copy()
+        small[..., 1] += rng.choice([0.0, 1e-13, -1e-13], size=small[..., 1].shape)
+        small[..., 0] *= 0.5
+        po = np.array([2, 0, 1], dtype=np.int32)
+        small_p = small[po]
+        d_large = s.subtract_f64(torch.from_numpy(par).cuda(), torch.from_numpy(small_p).cuda(), parent_of=po)
+        assert s.sync() == 0
+        ref_large, st = oracle.subtract_f64(par, po, small_p)
+        assert st == oracle.OK
+        gl = d_large.cpu().numpy()
+        np.testing.assert_array_equal(gl, ref_large)
+        assert (gl[..., 1] >= 0).all() and (gl[..., 1] == 0).any()
+
+
+def test_level5_full_size(gb, oracle):
+    """The full 1M x 100 depth-5 level (16 smaller siblings, 16 parents) in float cells."""
+    g, Session, _ = gb
+    w = synth.make("level5")
+    with Session() as s:
+        s.upload_bins(w.bins, w.n_bins, w.sentinel)
+        level_pair(s, oracle, w, 5, w.gpair, exact=False)
