@@ -301,6 +301,26 @@ SplitParams make_sp(const gbt_ctx *c, const gbt_params *prm) {
   return sp;
 }
 
+// Shared-memory limits of the histogram kernels (once per context).
+bool set_hist_attributes() {
+  const int u16_int = H16_HIST_MAX + H16_STAGE_BYTES + 128, u16_flt = H16_HIST_MAX + FL_STAGE_BYTES + 128;
+  return cudaFuncSetAttribute(k_hist_u8<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, H8_SMEM) == cudaSuccess &&
+         cudaFuncSetAttribute(k_hist_u8<false>, cudaFuncAttributePreferredSharedMemoryCarveout, 100) == cudaSuccess &&
+         cudaFuncSetAttribute(k_hist_u8<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              H8_SMEM + FL_STAGE_BYTES) == cudaSuccess &&
+         cudaFuncSetAttribute(k_hist_u8<true>, cudaFuncAttributePreferredSharedMemoryCarveout, 100) == cudaSuccess &&
+         cudaFuncSetAttribute(k_hist_u16<2, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, u16_int) == cudaSuccess &&
+         cudaFuncSetAttribute(k_hist_u16<4, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, u16_int) == cudaSuccess &&
+         cudaFuncSetAttribute(k_hist_u16<8, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, u16_int) == cudaSuccess &&
+         cudaFuncSetAttribute(k_hist_u16<16, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, u16_int) == cudaSuccess &&
+         cudaFuncSetAttribute(k_hist_u16<32, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, u16_int) == cudaSuccess &&
+         cudaFuncSetAttribute(k_hist_u16<2, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, u16_flt) == cudaSuccess &&
+         cudaFuncSetAttribute(k_hist_u16<4, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, u16_flt) == cudaSuccess &&
+         cudaFuncSetAttribute(k_hist_u16<8, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, u16_flt) == cudaSuccess &&
+         cudaFuncSetAttribute(k_hist_u16<16, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, u16_flt) == cudaSuccess &&
+         cudaFuncSetAttribute(k_hist_u16<32, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, u16_flt) == cudaSuccess;
+}
+
 }  // namespace
 
 extern "C" {
@@ -341,13 +361,7 @@ gbt_status gbt_create(int device, void *cuda_stream, gbt_ctx **out) {
     delete c;
     return GBT_ERR_CUDA;
   }
-  if (cudaFuncSetAttribute(k_hist_u8, cudaFuncAttributeMaxDynamicSharedMemorySize, H8_SMEM) != cudaSuccess ||
-      cudaFuncSetAttribute(k_hist_u8, cudaFuncAttributePreferredSharedMemoryCarveout, 100) != cudaSuccess ||
-      cudaFuncSetAttribute(k_hist_u16<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, H16_HIST_MAX + H16_STAGE_BYTES + 128) != cudaSuccess ||
-      cudaFuncSetAttribute(k_hist_u16<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, H16_HIST_MAX + H16_STAGE_BYTES + 128) != cudaSuccess ||
-      cudaFuncSetAttribute(k_hist_u16<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, H16_HIST_MAX + H16_STAGE_BYTES + 128) != cudaSuccess ||
-      cudaFuncSetAttribute(k_hist_u16<16>, cudaFuncAttributeMaxDynamicSharedMemorySize, H16_HIST_MAX + H16_STAGE_BYTES + 128) != cudaSuccess ||
-      cudaFuncSetAttribute(k_hist_u16<32>, cudaFuncAttributeMaxDynamicSharedMemorySize, H16_HIST_MAX + H16_STAGE_BYTES + 128) != cudaSuccess) {
+  if (!set_hist_attributes()) {
     cudaGetLastError();
     cudaEventDestroy(c->ev_q);
     cudaFreeHost(c->err_host);
@@ -528,19 +542,6 @@ gbt_status gbt_suggest_scales(int64_t rows_per_partial, float max_abs_g, float m
 
 namespace {
 
-// ts features per float-cell work item: a [B][ts][2] double image within the shared budget.
-int f64_ts_for(int B) {
-  for (int ts = 32; ts >= 2; ts >>= 1)
-    if ((int64_t)ts * B * 16 <= HF_SMEM_MAX) return ts;
-  return 0;
-}
-
-template <typename T, int TS>
-cudaError_t launch_hist_f64(gbt_ctx *c, int ctas, size_t smem, const HistF64Params &hp) {
-  cudaError_t e = cudaFuncSetAttribute(k_hist_f64<T, TS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
-  return launch_pdl(c, k_hist_f64<T, TS>, dim3(ctas), dim3(HF_THREADS), smem, hp);
-}
 
 // Validate the level inputs, plan the work items on the device and run the
 // histogram kernel, which leaves the group images in c->partial: exact int32
@@ -580,31 +581,31 @@ gbt_status run_level_build(gbt_ctx *c, const int32_t *rows, const int64_t *node_
     c->qmax = c->err_host[1];
     c->qmax_known = true;
   }
-  const int ts64 = f64 ? f64_ts_for(B) : 0;
-  if (f64 && ts64 == 0) return fail(c, GBT_ERR_UNSUPPORTED, "n_bins too large for the float-cell histogram");
 
   LevelParams lp;
   lp.rows = (const int32_t *)rows_d;
   lp.offs = (const int64_t *)offs_d;
   lp.n_nodes = n_nodes;
-  lp.item_feats = f64 ? ts64 : (c->bin_bytes == 1 ? 64 : c->ts16);
+  lp.item_feats = c->bin_bytes == 1 ? 64 : c->ts16;
   lp.n_fgroups = (c->n_features + lp.item_feats - 1) / lp.item_feats;
   lp.target_items = c->target_items > 0 ? c->target_items : c->n_sm * 2;
   lp.n_rows = c->n_rows;
-  lp.q = (const int2 *)c->q.p;
+  lp.q = f64 ? (const int2 *)gpair_f64 : (const int2 *)c->q.p;  // float cells: the float bit patterns
   lp.chunk_prefix = (int32_t *)c->chunk_prefix.p;
   lp.group_prefix = lp.chunk_prefix + (n_nodes + 1);
-  lp.sbw = f64 ? ts64 : (c->bin_bytes == 1 ? 16 : c->ts16);
-  lp.nsb = (!f64 && c->bin_bytes == 1) ? H8_SB : 1;
+  lp.sbw = c->bin_bytes == 1 ? 16 : c->ts16;
+  lp.nsb = c->bin_bytes == 1 ? H8_SB : 1;
   // nsb x B x sbw (G, H) pairs: int32 pairs (8 bytes), or double pairs (16 bytes) for float cells
-  lp.image_int4s = f64 ? (int64_t)lp.sbw * B : (int64_t)lp.nsb * lp.sbw * B / 2;
-  lp.qmax_plan = f64 ? 1u : 0u;  // float cells: any number of rows adds into one image
+  lp.image_int4s = f64 ? (int64_t)lp.nsb * lp.sbw * B : (int64_t)lp.nsb * lp.sbw * B / 2;
+  lp.qmax_plan = f64 ? 1u : 0u;             // float cells: all chunks of a node merge into one double image
+  lp.chunk_cap = f64 ? FL_CHUNK_CAP : 0;    // ... and each chunk's float sums cover at most 32k rows
   lp.st = c->st;
   // image scratch for the largest item count the device plan can produce
   // (there are never more group images than items):
   // items <= n_fgroups * n_nodes + max(target_items, n_fgroups * n_rows / rows_per_chunk_min)
   // (a chunk holds at least min(rc, load-balance target) rows, and rc >= 1024 by the quantisation limit)
-  const int64_t rc = std::max<int64_t>(1, 2147483647LL / std::max<int64_t>(f64 ? 1 : c->qmax, 1));
+  int64_t rc = std::max<int64_t>(1, 2147483647LL / std::max<int64_t>(f64 ? 1 : c->qmax, 1));
+  if (lp.chunk_cap > 0) rc = std::min<int64_t>(rc, lp.chunk_cap);  // the largest chunk the plan can form
   const int64_t items_max = (int64_t)lp.n_fgroups * (n_nodes + 1) +
                             std::max<int64_t>(lp.target_items, (int64_t)lp.n_fgroups * ((c->n_rows + rc - 1) / rc));
   if (items_max > INT32_MAX / 2) return fail(c, GBT_ERR_UNSUPPORTED, "level too large for the work-item plan");
@@ -616,40 +617,20 @@ gbt_status run_level_build(gbt_ctx *c, const int32_t *rows, const int64_t *node_
   k_level_plan<<<c->n_sm, PLAN_THREADS, 0, c->stream>>>(lp);
   LAUNCH_CHECK(c, "k_level_plan");
   const int hist_ctas = c->n_sm;  // persistent: one resident CTA per SM
-  if (f64) {
-    HistF64Params hp;
-    hp.lv = lp;
-    hp.mirror = (const unsigned char *)c->mirror.p;
-    hp.gpair = gpair_f64;
-    hp.n_features = c->n_features;
-    hp.n_slots = B;
-    hp.n_bins = c->n_bins;
-    hp.tile_feats = c->tile_feats;
-    const size_t smem = (size_t)B * ts64 * 16;
-    cudaError_t e = cudaSuccess;
-    prof_begin(c);
-    if (c->bin_bytes == 1) {
-      e = launch_hist_f64<uint8_t, 32>(c, hist_ctas, smem, hp);
-    } else {
-      switch (ts64) {
-        case 32: e = launch_hist_f64<uint16_t, 32>(c, hist_ctas, smem, hp); break;
-        case 16: e = launch_hist_f64<uint16_t, 16>(c, hist_ctas, smem, hp); break;
-        case 8: e = launch_hist_f64<uint16_t, 8>(c, hist_ctas, smem, hp); break;
-        case 4: e = launch_hist_f64<uint16_t, 4>(c, hist_ctas, smem, hp); break;
-        default: e = launch_hist_f64<uint16_t, 2>(c, hist_ctas, smem, hp); break;
-      }
-    }
-    if (e != cudaSuccess) return cuda_fail(c, e, "k_hist_f64");
-    LAUNCH_CHECK(c, "k_hist_f64");
-  } else if (c->bin_bytes == 1) {
+  if (c->bin_bytes == 1) {
     Hist8Params hp;
     hp.lv = lp;
     hp.mirror = (const uint8_t *)c->mirror.p;
     hp.n_features = c->n_features;
     hp.n_slots = B;
     prof_begin(c);
-    launch_pdl(c, k_hist_u8, dim3(hist_ctas), dim3(H8_THREADS), H8_SMEM, hp);
-    LAUNCH_CHECK(c, "k_hist_u8");
+    if (f64) {
+      launch_pdl(c, k_hist_u8<true>, dim3(hist_ctas), dim3(H8_THREADS), H8_SMEM + FL_STAGE_BYTES, hp);
+      LAUNCH_CHECK(c, "k_hist_u8_f32");
+    } else {
+      launch_pdl(c, k_hist_u8<false>, dim3(hist_ctas), dim3(H8_THREADS), H8_SMEM, hp);
+      LAUNCH_CHECK(c, "k_hist_u8");
+    }
   } else {
     Hist16Params hp;
     hp.lv = lp;
@@ -659,16 +640,27 @@ gbt_status run_level_build(gbt_ctx *c, const int32_t *rows, const int64_t *node_
     hp.n_bins = c->n_bins;
     hp.ts = c->ts16;
     const int hist_bytes = ((B * c->ts16 * 8) + 127) & ~127;
-    const int smem = hist_bytes + H16_STAGE_BYTES;
+    const int smem = hist_bytes + (f64 ? FL_STAGE_BYTES : H16_STAGE_BYTES);
     prof_begin(c);
-    switch (c->ts16) {
-      case 32: launch_pdl(c, k_hist_u16<32>, dim3(hist_ctas), dim3(H16_THREADS), smem, hp); break;
-      case 16: launch_pdl(c, k_hist_u16<16>, dim3(hist_ctas), dim3(H16_THREADS), smem, hp); break;
-      case 8: launch_pdl(c, k_hist_u16<8>, dim3(hist_ctas), dim3(H16_THREADS), smem, hp); break;
-      case 4: launch_pdl(c, k_hist_u16<4>, dim3(hist_ctas), dim3(H16_THREADS), smem, hp); break;
-      default: launch_pdl(c, k_hist_u16<2>, dim3(hist_ctas), dim3(H16_THREADS), smem, hp); break;
+    if (f64) {
+      switch (c->ts16) {
+        case 32: launch_pdl(c, k_hist_u16<32, true>, dim3(hist_ctas), dim3(H16_THREADS), smem, hp); break;
+        case 16: launch_pdl(c, k_hist_u16<16, true>, dim3(hist_ctas), dim3(H16_THREADS), smem, hp); break;
+        case 8: launch_pdl(c, k_hist_u16<8, true>, dim3(hist_ctas), dim3(H16_THREADS), smem, hp); break;
+        case 4: launch_pdl(c, k_hist_u16<4, true>, dim3(hist_ctas), dim3(H16_THREADS), smem, hp); break;
+        default: launch_pdl(c, k_hist_u16<2, true>, dim3(hist_ctas), dim3(H16_THREADS), smem, hp); break;
+      }
+      LAUNCH_CHECK(c, "k_hist_u16_f32");
+    } else {
+      switch (c->ts16) {
+        case 32: launch_pdl(c, k_hist_u16<32, false>, dim3(hist_ctas), dim3(H16_THREADS), smem, hp); break;
+        case 16: launch_pdl(c, k_hist_u16<16, false>, dim3(hist_ctas), dim3(H16_THREADS), smem, hp); break;
+        case 8: launch_pdl(c, k_hist_u16<8, false>, dim3(hist_ctas), dim3(H16_THREADS), smem, hp); break;
+        case 4: launch_pdl(c, k_hist_u16<4, false>, dim3(hist_ctas), dim3(H16_THREADS), smem, hp); break;
+        default: launch_pdl(c, k_hist_u16<2, false>, dim3(hist_ctas), dim3(H16_THREADS), smem, hp); break;
+      }
+      LAUNCH_CHECK(c, "k_hist_u16");
     }
-    LAUNCH_CHECK(c, "k_hist_u16");
   }
   *out_lp = lp;
   return GBT_OK;
@@ -804,8 +796,8 @@ gbt_status gbt_build_level_f64(gbt_ctx *c, const float *gpair, const int32_t *ro
   const int64_t cells = (int64_t)n_nodes * c->n_features * B;
   prof_begin(c);
   launch_pdl(c, k_finalize_f64, dim3(grid_for(c, cells, 256, 8)), dim3(256), 0, (const double *)lp.partial,
-             (const int32_t *)lp.group_prefix, (int64_t)lp.image_int4s * 2, lp.n_fgroups, lp.item_feats, n_nodes,
-             c->n_features, B, hist_out, (const DevState *)c->st);
+             (const int32_t *)lp.group_prefix, (int64_t)lp.image_int4s * 2, lp.n_fgroups, lp.item_feats, lp.sbw,
+             n_nodes, c->n_features, B, hist_out, (const DevState *)c->st);
   LAUNCH_CHECK(c, "k_finalize_f64");
   return GBT_OK;
 }
@@ -849,9 +841,20 @@ gbt_status gbt_find_splits_f64(gbt_ctx *c, const double *hist, int32_t n_nodes, 
   s = ensure_counters(c, (size_t)n_nodes);
   if (s != GBT_OK) return s;
   prof_begin(c);
-  k_find_f64<<<dim3(nfb, n_nodes), SCAN_THREADS, 0, c->stream>>>(hist, c->n_features, c->n_bins, params->lambda,
-                                                                 params->gamma, params->min_child_weight,
-                                                                 (Cand *)c->cand.p, (uint32_t *)c->counters.p, dout);
+  SplitParams sp{};
+  sp.lambda = params->lambda;
+  sp.gamma = params->gamma;
+  sp.inv_sg = sp.inv_sh = 1.0;
+  sp.lambda_f = (float)params->lambda;
+  sp.gamma_f = (float)params->gamma;
+  sp.gamma_abs_f = fabsf(sp.gamma_f);
+  sp.inv_sg_f = sp.inv_sh_f = 1.f;
+  sp.filter = (params->lambda >= 0.0 && params->lambda < 1e30 && isfinite(params->gamma) && fabs(params->gamma) < 1e30)
+                  ? 1
+                  : 0;
+  k_find_f64<<<dim3(nfb, n_nodes), SCAN_THREADS, 0, c->stream>>>(hist, c->n_features, c->n_bins, sp,
+                                                                 params->min_child_weight, (Cand *)c->cand.p,
+                                                                 (uint32_t *)c->counters.p, dout);
   LAUNCH_CHECK(c, "k_find_f64");
   if (host)
     CUDA_TRY(c, cudaMemcpyAsync(out, dout, (size_t)n_nodes * sizeof(gbt_split_f64), cudaMemcpyDeviceToHost, c->stream),

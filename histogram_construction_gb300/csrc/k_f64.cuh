@@ -1,18 +1,15 @@
-// Float-cell mode: histograms of the unquantised (g, h) in double [bonsai "10:
-// CUDA histogram backend", "The kernel": float shared-memory cells merged into
-// double global cells; "GBDT engine engineering deep-dive", section 7 listing;
-// section 3: the hessian is clamped at zero after subtraction].
+// Float-cell mode: histograms of the unquantised (g, h), merged in double
+// [bonsai "10: CUDA histogram backend", "The kernel": float shared-memory
+// cells per chunk of at most 32k rows, merged into double global cells;
+// "GBDT engine engineering deep-dive", section 7 listing; section 3: the
+// hessian is clamped at zero after subtraction].
 //
-// GB300 design: the same device plan and persistent work items as the
-// fixed-point build, with double cells. A work item holds TS features (TS a
-// power of two, 32 for u8) as a [slot][TS][G, H] double image in shared
-// memory; lane l takes feature l % TS of row l / TS of each group of 32/TS
-// rows and adds (g, h) with two 64-bit shared atomics. Missing entries (u16:
-// up to 40%) are summed in registers and added once per item. Items of one
-// node add their images into one double image with TMA bulk reduce-adds (the
-// plan zeroes it), or store it when they are its only chunk. Addition order
-// is not fixed: cells agree with a serial double sum to rounding, not bit for
-// bit.
+// The histogram pass is the fixed-point kernels' float-cell instantiation
+// (k_hist_u8<true>, k_hist_u16<TS, true>): same plan, same shared layouts,
+// red.shared.add.f32 instead of the integer reductions, one double image per
+// (node, feature group). This file holds the passes after it: the images to
+// the [n][F][B][2] double histogram, the clamped subtraction and the split
+// find on double cells.
 #pragma once
 
 #include "common.cuh"
@@ -21,110 +18,14 @@
 
 namespace gbt {
 
-constexpr int HF_THREADS = 512;
-constexpr int HF_SMEM_MAX = 160 * 1024;
-
-__device__ __forceinline__ void bulk_reduce_add_f64(void *gdst, const void *ssrc, uint32_t bytes) {
-  asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f64 [%0], [%1], %2;" ::"l"(gdst),
-               "r"(smem_addr(ssrc)), "r"(bytes)
-               : "memory");
-}
-
-struct HistF64Params {
-  LevelParams lv;
-  const unsigned char *mirror;  // tile pairs (see mirror_offset)
-  const float2 *gpair;          // [n_rows] (g, h)
-  int32_t n_features;
-  int32_t n_slots;              // B
-  int32_t n_bins;
-  int32_t tile_feats;           // features per 64-byte mirror strip (64 u8, 32 u16)
-};
-
-template <typename T, int TS>
-__global__ void __launch_bounds__(HF_THREADS, 1) k_hist_f64(HistF64Params P) {
-  extern __shared__ __align__(128) unsigned char smem[];
-  double *hist = reinterpret_cast<double *>(smem);  // [B][TS][2]
-  __shared__ int32_t s_item;
-  constexpr int RPI = 32 / TS;  // rows per warp instruction
-  const LevelParams &p = P.lv;
-  pdl_wait();
-  pdl_trigger();
-  if (!p.st->plan_ok) return;
-  const int64_t chunk = p.st->chunk_rows;
-  const int32_t cpg = p.st->chunks_per_group;
-  const int32_t n_items = p.st->n_items;
-  const int B = P.n_slots;
-  const int64_t N = p.n_rows;
-  const bool ident = (p.rows == nullptr);
-  const uint32_t miss = (uint32_t)P.n_bins;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
-  const int fl = lane % TS, rho = lane / TS;
-  uint32_t bad = 0;
-  for (;;) {
-    if (threadIdx.x == 0) s_item = (int32_t)atomicAdd(&p.st->work_next, 1u);
-    __syncthreads();
-    const int32_t id = s_item;
-    if (id >= n_items) break;
-    const Item it = decode_item(id, p, chunk, cpg);
-    for (int i = threadIdx.x; i < B * TS * 2; i += blockDim.x) hist[i] = 0.0;
-    __syncthreads();
-    const int f = it.fgroup * TS + fl;
-    const bool f_on = f < P.n_features;
-    const int tile = f / P.tile_feats, ft = f - tile * P.tile_feats;
-    const T *strip = reinterpret_cast<const T *>(P.mirror + mirror_offset(tile, 0, N)) + ft;
-    double mg = 0.0, mh = 0.0;
-    for (int64_t k = it.k0 + (int64_t)warp * RPI + rho; k < it.k1; k += (int64_t)nwarps * RPI) {
-      const int32_t r = ident ? (int32_t)k : __ldg(p.rows + k);
-      if (r < 0 || r >= N) {
-        bad = 1;
-        continue;
-      }
-      if (!f_on) continue;
-      const float2 gh = __ldg(P.gpair + r);
-      const uint32_t slot = __ldg(reinterpret_cast<const T *>(reinterpret_cast<const unsigned char *>(strip) +
-                                                               (int64_t)r * MIRROR_ROW_BYTES));
-      if (slot == miss) {
-        mg += (double)gh.x;
-        mh += (double)gh.y;
-      } else {
-        atomicAdd(&hist[(slot * TS + fl) * 2], (double)gh.x);
-        atomicAdd(&hist[(slot * TS + fl) * 2 + 1], (double)gh.y);
-      }
-    }
-#pragma unroll
-    for (int o = TS; o < 32; o <<= 1) {
-      mg += __shfl_xor_sync(0xffffffffu, mg, o);
-      mh += __shfl_xor_sync(0xffffffffu, mh, o);
-    }
-    if (rho == 0 && f_on) {
-      atomicAdd(&hist[(miss * TS + fl) * 2], mg);
-      atomicAdd(&hist[(miss * TS + fl) * 2 + 1], mh);
-    }
-    fence_proxy_async_smem();
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      unsigned char *dst = reinterpret_cast<unsigned char *>(p.partial + it.image * p.image_int4s * 4);
-      const unsigned char *src = reinterpret_cast<const unsigned char *>(hist);
-      const uint32_t total = (uint32_t)B * TS * 16u;
-      for (uint32_t off = 0; off < total; off += 65536u) {
-        if (it.multi) bulk_reduce_add_f64(dst + off, src + off, min(65536u, total - off));
-        else bulk_store(dst + off, src + off, min(65536u, total - off));
-      }
-      bulk_commit();
-      bulk_wait_read_all();
-    }
-    __syncthreads();
-  }
-  if (bad) raise_err(p.st, ERRBIT_ROW);
-  if (threadIdx.x == 0) bulk_wait_all();
-}
-
-// Group images ([image][slot][TS][2] double) -> hist_out [n][F][B][2] double.
+// Group images ([image][sub-block][slot][sbw][G, H] double; feature fl of an
+// item's group is sub-block fl / sbw, column fl % sbw) -> hist_out
+// [n][F][B][2] double, summing a node's group images.
 __global__ void __launch_bounds__(256) k_finalize_f64(const double *__restrict__ partial,
                                                       const int32_t *__restrict__ group_prefix, int64_t image_doubles,
-                                                      int32_t n_fgroups, int32_t ts, int32_t n_nodes,
-                                                      int32_t n_features, int32_t B, double *__restrict__ hist_out,
-                                                      const DevState *st) {
+                                                      int32_t n_fgroups, int32_t item_feats, int32_t sbw,
+                                                      int32_t n_nodes, int32_t n_features, int32_t B,
+                                                      double *__restrict__ hist_out, const DevState *st) {
   pdl_wait();
   if (!st->plan_ok) return;
   const int64_t units = (int64_t)n_nodes * n_features * B;
@@ -133,12 +34,14 @@ __global__ void __launch_bounds__(256) k_finalize_f64(const double *__restrict__
     int64_t r = u / n_features;
     const int s = (int)(r % B);
     const int n = (int)(r / B);
-    const int fg = f / ts, fl = f - fg * ts;
+    const int fg = f / item_feats, fl = f - fg * item_feats;
+    const int sb = fl / sbw, c = fl - sb * sbw;
+    const int64_t cell = (((int64_t)sb * B + s) * sbw + c) * 2;
     double g = 0.0, h = 0.0;
     for (int32_t k = group_prefix[n]; k < group_prefix[n + 1]; ++k) {
-      const double *c = partial + ((int64_t)k * n_fgroups + fg) * image_doubles + ((int64_t)s * ts + fl) * 2;
-      g += __ldcg(c);
-      h += __ldcg(c + 1);
+      const double *src = partial + ((int64_t)k * n_fgroups + fg) * image_doubles + cell;
+      g += __ldcg(src);
+      h += __ldcg(src + 1);
     }
     double *d = hist_out + (((int64_t)n * n_features + f) * B + s) * 2;
     d[0] = g;
@@ -162,13 +65,56 @@ __global__ void __launch_bounds__(256) k_subtract_f64(const double *__restrict__
   }
 }
 
+// FP32 screen of a float-cell candidate from its double sums: (up, lo) with
+// lo <= gain_fp64 <= up. Each double converts to float with relative error
+// u = 2^-24, within the 4u per input that the fixed-point screen's error
+// budget (screen_f32) assumes, so its bound 2^-19 (a + b + c + |gamma|)
+// holds; values outside [2^-60, 2^60] give an infinite bound (evaluated in
+// double).
+__device__ __forceinline__ void screen_dbl(double GL, double HL, double GR, double HR, float Gf2den,
+                                           const SplitParams &sp, float &up, float &lo) {
+  const float gl = __double2float_rn(GL), hl = __double2float_rn(HL);
+  const float gr = __double2float_rn(GR), hr = __double2float_rn(HR);
+  const float dl = __fadd_rn(hl, sp.lambda_f), dr = __fadd_rn(hr, sp.lambda_f);
+  const float a = __fdividef(__fmul_rn(gl, gl), dl);
+  const float b = __fdividef(__fmul_rn(gr, gr), dr);
+  const float g = __fsub_rn(__fmul_rn(0.5f, __fsub_rn(__fadd_rn(a, b), Gf2den)), sp.gamma_f);
+  const float mag = __fadd_rn(__fadd_rn(__fadd_rn(a, b), Gf2den), sp.gamma_abs_f);
+  const float err = __fmul_rn(mag, 1.9073486328125e-06f);  // 2^-19
+  const float rlo = 8.673617379884035e-19f, rhi = 1.152921504606847e+18f;  // 2^-60, 2^60
+  const float ag = fabsf(gl), ar = fabsf(gr);
+  const bool ok = (ag == 0.f || (ag > rlo && ag < rhi)) && (ar == 0.f || (ar > rlo && ar < rhi)) && dl > rlo &&
+                  dr > rlo && dl < rhi && dr < rhi && mag < rhi && (a == 0.f || a > rlo) && (b == 0.f || b > rlo) &&
+                  g == g;
+  up = ok ? __fadd_rn(g, err) : INFINITY;
+  lo = ok ? __fsub_rn(g, err) : -INFINITY;
+}
+
+// Parent term G^2 / (H + lambda) in FP32 from the double totals; NaN (every
+// candidate then unscreened) outside the checked range.
+__device__ __forceinline__ float parent_dbl(double G, double H, const SplitParams &sp) {
+  const float Gf = __double2float_rn(G), Hf = __double2float_rn(H);
+  const float den = __fadd_rn(Hf, sp.lambda_f);
+  const float rlo = 8.673617379884035e-19f, rhi = 1.152921504606847e+18f;
+  const float ag = fabsf(Gf);
+  if (den > rlo && den < rhi && (ag == 0.f || (ag > rlo && ag < rhi))) {
+    const float c = __fdividef(__fmul_rn(Gf, Gf), den);
+    if (c == 0.f || (c > rlo && c < rhi)) return c;
+  }
+  return __int_as_float(0x7fc00000);
+}
+
 // Split find on double cells: grid (ceil(F / 8), n_nodes), 256 threads; warp w
-// scans feature blockIdx.x * 8 + w of node blockIdx.y, every candidate in
-// double; the CTA's best goes to cand[node][blockIdx.x]; the node's last CTA
-// writes the split. The double sums travel as bit patterns in the candidate's
-// 64-bit fields, so the output record is a gbt_split whose four sums are doubles.
+// scans feature blockIdx.x * 8 + w of node blockIdx.y. Prefix sums are double;
+// each valid candidate is screened in FP32 with a rigorous bound and only
+// those whose upper bound reaches the warp's running best lower bound are
+// evaluated in double (the best candidate and every candidate tied with it
+// always are; FP64 is a small fraction of the FP32 rate on this part). The
+// CTA's best goes to cand[node][blockIdx.x]; the node's last CTA writes the
+// split. The double sums travel as bit patterns in the candidate's 64-bit
+// fields, so the output record is a gbt_split whose four sums are doubles.
 __global__ void __launch_bounds__(SCAN_THREADS) k_find_f64(const double *__restrict__ hist, int32_t n_features,
-                                                           int32_t n_bins, double lambda, double gamma, double mcw,
+                                                           int32_t n_bins, SplitParams sp, double mcw,
                                                            Cand *__restrict__ cand, uint32_t *__restrict__ counters,
                                                            SplitOut *__restrict__ out) {
   __shared__ Cand s_best[SCAN_WARPS];
@@ -193,7 +139,9 @@ __global__ void __launch_bounds__(SCAN_THREADS) k_find_f64(const double *__restr
       H += __shfl_xor_sync(0xffffffffu, H, o);
     }
     const double2 m = __ldg(strip + n_bins);
-    const double parent = __ddiv_rn(__dmul_rn(G, G), __dadd_rn(H, lambda));
+    const double parent = __ddiv_rn(__dmul_rn(G, G), __dadd_rn(H, sp.lambda));
+    const float Gf2den = sp.filter ? parent_dbl(G, H, sp) : 0.f;
+    float run_lo = -INFINITY;
     double cg = 0.0, ch = 0.0;
     for (int c0 = 0; c0 < n_bins; c0 += 32 * SCAN_SPL) {
       double pg[SCAN_SPL], ph[SCAN_SPL], ag = 0.0, ah = 0.0;
@@ -220,21 +168,42 @@ __global__ void __launch_bounds__(SCAN_THREADS) k_find_f64(const double *__restr
       eh = eh - ah + ch;
       cg += tg;
       ch += th;
+      float up[SCAN_SPL][2];
+      uint32_t vmask = 0;
+      float l = -INFINITY;
 #pragma unroll
       for (int i = 0; i < SCAN_SPL; ++i) {
         const int s = c0 + SCAN_SPL * lane + i;
-        if (s >= n_bins) continue;
 #pragma unroll
         for (int dir = 0; dir < 2; ++dir) {
+          up[i][dir] = -INFINITY;
+          if (s >= n_bins) continue;
           const double GL = eg + pg[i] + (dir ? m.x : 0.0), HL = eh + ph[i] + (dir ? m.y : 0.0);
           const double GR = G - GL, HR = H - HL;
           if (!(HL > 0.0 && HR > 0.0 && HL >= mcw && HR >= mcw)) continue;
-          const double l = __ddiv_rn(__dmul_rn(GL, GL), __dadd_rn(HL, lambda));
-          const double r = __ddiv_rn(__dmul_rn(GR, GR), __dadd_rn(HR, lambda));
-          const double gain = __dsub_rn(__dmul_rn(0.5, __dsub_rn(__dadd_rn(l, r), parent)), gamma);
+          float u = INFINITY, lw = -INFINITY;
+          if (sp.filter) screen_dbl(GL, HL, GR, HR, Gf2den, sp, u, lw);
+          up[i][dir] = u;
+          vmask |= 1u << (2 * i + dir);
+          l = fmaxf(l, lw);
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) l = fmaxf(l, __shfl_xor_sync(0xffffffffu, l, o));
+      run_lo = fmaxf(run_lo, l);
+#pragma unroll
+      for (int i = 0; i < SCAN_SPL; ++i) {
+#pragma unroll
+        for (int dir = 0; dir < 2; ++dir) {
+          if (!((vmask >> (2 * i + dir)) & 1u) || up[i][dir] < run_lo) continue;  // invalid, or below a lower bound
+          const double GL = eg + pg[i] + (dir ? m.x : 0.0), HL = eh + ph[i] + (dir ? m.y : 0.0);
+          const double GR = G - GL, HR = H - HL;
+          const double l2 = __ddiv_rn(__dmul_rn(GL, GL), __dadd_rn(HL, sp.lambda));
+          const double r2 = __ddiv_rn(__dmul_rn(GR, GR), __dadd_rn(HR, sp.lambda));
+          const double gain = __dsub_rn(__dmul_rn(0.5, __dsub_rn(__dadd_rn(l2, r2), parent)), sp.gamma);
           Cand c;
           set_exact(c, gain);
-          c.t = s;
+          c.t = c0 + SCAN_SPL * lane + i;
           c.dir = dir;
           c.f = f;
           c.gl = __double_as_longlong(GL);

@@ -25,6 +25,8 @@
 //    kernel, or the fused subtract + split-find kernel).
 #pragma once
 
+#include <type_traits>
+
 #include "common.cuh"
 
 namespace gbt {
@@ -47,6 +49,7 @@ struct LevelParams {
   int32_t sbw;            // features per sub-block of the image (16 for u8, TS for u16)
   int32_t nsb;            // sub-blocks per image (4 for u8, 1 for u16)
   uint32_t qmax_plan;     // if nonzero, the plan's exactness bound uses it instead of the tree's max|q|
+  int32_t chunk_cap;      // if nonzero, no chunk holds more rows (float cells: rounding per chunk)
   DevState *st;
 };
 
@@ -115,7 +118,8 @@ __global__ void __launch_bounds__(PLAN_THREADS) k_level_plan(LevelParams p) {
     const int64_t rc = 2147483647LL / (int64_t)qm;  // rows whose int32 partials cannot overflow
     int64_t tgt = (R * p.n_fgroups + p.target_items - 1) / max(p.target_items, 1);
     tgt = max(tgt, (int64_t)CHUNK_MIN_ROWS);
-    const int64_t chunk = max((int64_t)1, min(rc, tgt));
+    int64_t chunk = max((int64_t)1, min(rc, tgt));
+    if (p.chunk_cap > 0) chunk = min(chunk, (int64_t)p.chunk_cap);
     s_chunk = chunk;
     s_cpg = (int32_t)min(rc / chunk, (int64_t)0x3fffffff);
   }
@@ -222,6 +226,49 @@ __device__ __forceinline__ void load_row(const LevelParams &p, bool ident, int64
 }
 
 // ----------------------------------------------------------------------------
+// Float cells [bonsai "10: CUDA histogram backend", "The kernel": shared
+// accumulation in float with native shared-memory atomics, chunks of at most
+// 32k rows, the cross-chunk merge in double]. The histogram kernels then hold
+// (g, h) as float bit patterns and add them with red.shared.add.f32; the
+// item's float image leaves as doubles, FL_PIECE cells at a time, through two
+// alternating shared staging buffers: converted by the whole block, then
+// stored (the node's only chunk) or reduce-added (cp.reduce.async.bulk .f64)
+// into the node's double image.
+constexpr int FL_PIECE = 4096;                     // floats per staged piece
+constexpr int FL_STAGE_BYTES = 2 * FL_PIECE * 8;   // two double buffers
+constexpr int FL_CHUNK_CAP = 32768;                // rows per float chunk
+
+// nseg float segments of seg_floats floats each (segment i at src + i *
+// seg_stride bytes) -> consecutive double segments at dst. Called by every
+// thread of the block; returns with the staging buffers free again.
+__device__ __forceinline__ void flush_float_image(const unsigned char *src, int nseg, int seg_stride,
+                                                  uint32_t seg_floats, double *dst, bool multi, double *stage) {
+  int idx = 0;
+  for (int sg = 0; sg < nseg; ++sg) {
+    const float *fs = reinterpret_cast<const float *>(src + (size_t)sg * seg_stride);
+    for (uint32_t off = 0; off < seg_floats; off += FL_PIECE, ++idx) {
+      const uint32_t n = min((uint32_t)FL_PIECE, seg_floats - off);
+      double *buf = stage + (idx & 1) * FL_PIECE;
+      if (idx >= 2) {  // the buffer's previous piece must have been read
+        if (threadIdx.x == 0) bulk_wait_read_1();
+        __syncthreads();
+      }
+      for (uint32_t i = threadIdx.x; i < n; i += blockDim.x) buf[i] = (double)fs[off + i];
+      fence_proxy_async_smem();
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        double *d = dst + (size_t)sg * seg_floats + off;
+        if (multi) bulk_reduce_add_f64(d, buf, n * 8u);
+        else bulk_store(d, buf, n * 8u);
+        bulk_commit();
+      }
+    }
+  }
+  if (threadIdx.x == 0) bulk_wait_read_all();
+  __syncthreads();
+}
+
+// ----------------------------------------------------------------------------
 // u8 kernel: items of one 64-feature mirror tile, 16-feature sub-blocks.
 //
 // Shared layout: sub-block sb (features 16 sb .. 16 sb + 15) is a [slot][16]
@@ -287,28 +334,35 @@ __device__ __forceinline__ void h8_gather(const LevelParams &p, const unsigned c
   }
 }
 
-template <int E>
+template <int E, bool FLT>
 __device__ __forceinline__ void h8_word(uint32_t word, const uint32_t (&sel)[4], const uint32_t (&cj)[4], uint32_t v0,
                                         uint32_t v1) {
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
     const uint32_t a = __byte_perm(word, 0u, sel[j]) * 128u + cj[j];
-    asm volatile("red.shared.add.u32 [%0+%2], %1;" ::"r"(a), "r"(v0), "n"(32 * E) : "memory");
-    asm volatile("red.shared.add.u32 [%0+%2], %1;" ::"r"(a ^ 4u), "r"(v1), "n"(32 * E) : "memory");
+    if constexpr (FLT) {
+      asm volatile("red.shared.add.f32 [%0+%2], %1;" ::"r"(a), "f"(__uint_as_float(v0)), "n"(32 * E) : "memory");
+      asm volatile("red.shared.add.f32 [%0+%2], %1;" ::"r"(a ^ 4u), "f"(__uint_as_float(v1)), "n"(32 * E) : "memory");
+    } else {
+      asm volatile("red.shared.add.u32 [%0+%2], %1;" ::"r"(a), "r"(v0), "n"(32 * E) : "memory");
+      asm volatile("red.shared.add.u32 [%0+%2], %1;" ::"r"(a ^ 4u), "r"(v1), "n"(32 * E) : "memory");
+    }
   }
 }
 
-template <int U>
+template <int U, bool FLT>
 __device__ __forceinline__ void h8_scatter(const H8Stage<U> &st, const uint32_t (&sel)[4], const uint32_t (&cj)[4]) {
 #pragma unroll
   for (int u = 0; u < U; ++u) {
-    h8_word<0>(st.bw[u].x, sel, cj, st.v0[u], st.v1[u]);
-    h8_word<1>(st.bw[u].y, sel, cj, st.v0[u], st.v1[u]);
-    h8_word<2>(st.bw[u].z, sel, cj, st.v0[u], st.v1[u]);
-    h8_word<3>(st.bw[u].w, sel, cj, st.v0[u], st.v1[u]);
+    h8_word<0, FLT>(st.bw[u].x, sel, cj, st.v0[u], st.v1[u]);
+    h8_word<1, FLT>(st.bw[u].y, sel, cj, st.v0[u], st.v1[u]);
+    h8_word<2, FLT>(st.bw[u].z, sel, cj, st.v0[u], st.v1[u]);
+    h8_word<3, FLT>(st.bw[u].w, sel, cj, st.v0[u], st.v1[u]);
   }
 }
 
+// FLT: float cells (p.q holds the float (g, h) bit patterns; images are double).
+template <bool FLT>
 __global__ void __launch_bounds__(H8_THREADS, 1) k_hist_u8(Hist8Params P) {
   constexpr int U = H8_U;
   extern __shared__ __align__(128) unsigned char smem[];
@@ -370,11 +424,17 @@ __global__ void __launch_bounds__(H8_THREADS, 1) k_hist_u8(Hist8Params P) {
         h8_gather<U>(p, strip, lane_on, par, rid, nxt, bad);
         h8_rows<U>(p, ident, g0 + 2 * adv, step, it.k1, rid);
       }
-      h8_scatter<U>(cur, sel, cj);
+      h8_scatter<U, FLT>(cur, sel, cj);
       cur = nxt;
       g0 += adv;
     }
     __syncthreads();
+    if constexpr (FLT) {
+      flush_float_image(smem, nsb, H8_SB_STRIDE, (uint32_t)B * 32u,
+                        reinterpret_cast<double *>(p.partial) + it.image * p.image_int4s * 2, it.multi,
+                        reinterpret_cast<double *>(smem + H8_SMEM));
+      continue;
+    }
     // flush: the item's shared image (per sub-block [slot][16][G, H] int32)
     // leaves as is, one TMA bulk operation per sub-block: a store when the
     // item is its group's only chunk, else a reduce-add into the zeroed
@@ -402,6 +462,24 @@ __global__ void __launch_bounds__(H8_THREADS, 1) k_hist_u8(Hist8Params P) {
 // u16 kernel: TS features per item (TS = 2..32), any B with TS * B * 8 within
 // the shared budget. Missing-slot entries are summed in registers and added
 // once per item (40% of entries can be missing; they would all hit one cell).
+template <bool FLT>
+__device__ __forceinline__ typename std::conditional<FLT, float, int32_t>::type h16_val(int32_t bits) {
+  if constexpr (FLT) return __int_as_float(bits);
+  else return bits;
+}
+
+// Adds (g, h) into the (G, H) cell pair c.
+template <bool FLT, typename V>
+__device__ __forceinline__ void h16_add(uint32_t *c, V g, V h) {
+  if constexpr (FLT) {
+    atomicAdd(reinterpret_cast<float *>(c), g);
+    atomicAdd(reinterpret_cast<float *>(c) + 1, h);
+  } else {
+    atomicAdd(c, (uint32_t)g);
+    atomicAdd(c + 1, (uint32_t)h);
+  }
+}
+
 constexpr int H16_THREADS = 512;
 constexpr int H16_HIST_MAX = 160 * 1024;
 constexpr int H16_STAGE_SLOTS = 2048;
@@ -416,8 +494,9 @@ struct Hist16Params {
   int32_t ts;              // features per item
 };
 
-template <int TS>
+template <int TS, bool FLT>
 __global__ void __launch_bounds__(H16_THREADS, 1) k_hist_u16(Hist16Params P) {
+  using V = typename std::conditional<FLT, float, int32_t>::type;  // missing-slot partials
   extern __shared__ __align__(128) unsigned char smem[];
   constexpr int W = TS / 2;        // u32 words per row in an item
   constexpr int RPI = 32 / W;      // rows per warp instruction
@@ -460,7 +539,7 @@ __global__ void __launch_bounds__(H16_THREADS, 1) k_hist_u16(Hist16Params P) {
     const int sub = it.fgroup % GROUPS_PER_TILE;
     const unsigned char *strip =
         reinterpret_cast<const unsigned char *>(P.mirror) + mirror_offset(tile, 0, N) + sub * TS * 2 + wi * 4;
-    int32_t mg0 = 0, mh0 = 0, mg1 = 0, mh1 = 0;  // missing-slot partials of features 2wi, 2wi+1
+    V mg0 = 0, mh0 = 0, mg1 = 0, mh1 = 0;  // missing-slot partials of features 2wi, 2wi+1
     const int64_t step = (int64_t)RPI * nwarps;
     for (int64_t g0 = it.k0 + RPI * warp; g0 < it.k1; g0 += step * 4) {
       int32_t rr[4], vg[4], vh[4];
@@ -476,18 +555,11 @@ __global__ void __launch_bounds__(H16_THREADS, 1) k_hist_u16(Hist16Params P) {
       for (int u = 0; u < 4; ++u) {
         if (rr[u] < 0) continue;
         const uint32_t s0 = bw[u] & 0xffffu, s1 = bw[u] >> 16;
-        if (s0 == miss_slot) { mg0 += vg[u]; mh0 += vh[u]; }
-        else {
-          uint32_t *c = hist + 2 * (s0 * TS + 2 * wi);
-          atomicAdd(c, (uint32_t)vg[u]);
-          atomicAdd(c + 1, (uint32_t)vh[u]);
-        }
-        if (s1 == miss_slot) { mg1 += vg[u]; mh1 += vh[u]; }
-        else {
-          uint32_t *c = hist + 2 * (s1 * TS + 2 * wi + 1);
-          atomicAdd(c, (uint32_t)vg[u]);
-          atomicAdd(c + 1, (uint32_t)vh[u]);
-        }
+        const V g = h16_val<FLT>(vg[u]), h = h16_val<FLT>(vh[u]);
+        if (s0 == miss_slot) { mg0 += g; mh0 += h; }
+        else h16_add<FLT>(hist + 2 * (s0 * TS + 2 * wi), g, h);
+        if (s1 == miss_slot) { mg1 += g; mh1 += h; }
+        else h16_add<FLT>(hist + 2 * (s1 * TS + 2 * wi + 1), g, h);
       }
     }
     // reduce missing partials over lanes sharing wi, add once
@@ -499,14 +571,16 @@ __global__ void __launch_bounds__(H16_THREADS, 1) k_hist_u16(Hist16Params P) {
       mh1 += __shfl_xor_sync(0xffffffffu, mh1, o);
     }
     if (rho == 0) {
-      uint32_t *c0 = hist + 2 * (miss_slot * TS + 2 * wi);
-      atomicAdd(c0, (uint32_t)mg0);
-      atomicAdd(c0 + 1, (uint32_t)mh0);
-      uint32_t *c1 = hist + 2 * (miss_slot * TS + 2 * wi + 1);
-      atomicAdd(c1, (uint32_t)mg1);
-      atomicAdd(c1 + 1, (uint32_t)mh1);
+      h16_add<FLT>(hist + 2 * (miss_slot * TS + 2 * wi), mg0, mh0);
+      h16_add<FLT>(hist + 2 * (miss_slot * TS + 2 * wi + 1), mg1, mh1);
     }
     __syncthreads();
+    if constexpr (FLT) {
+      flush_float_image(smem, 1, 0, (uint32_t)B * TS * 2u,
+                        reinterpret_cast<double *>(p.partial) + it.image * p.image_int4s * 2, it.multi,
+                        reinterpret_cast<double *>(stage));
+      continue;
+    }
     // flush: the item's shared image ([slot][TS][G, H] int32) in bulk stores
     // (or reduce-adds, for a group of several chunks) of <= 64 KB
     fence_proxy_async_smem();
