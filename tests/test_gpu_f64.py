@@ -64,6 +64,9 @@ def assert_cells_close(got, ref, ab, offsets, where):
     err = np.abs(got - ref)
     bad = err > tol
     assert not bad.any(), f"{where}: {int(bad.sum())} cells off, worst {float((err - tol).max())}"
+    # the per-cell bar of the float mode: |a - b| <= 1e-5 * (sum of |x| over the cell)
+    bad = err > 1e-5 * ab
+    assert not bad.any(), f"{where}: {int(bad.sum())} cells beyond 1e-5 of their absolute sum"
 
 
 def assert_splits_bitwise(got, ref, where):
@@ -123,7 +126,8 @@ def level_pair(sess, oracle, w, depth, gp, lam=1.0, gamma=0.0, mcw=0.0, exact=Tr
     ref_large, st = oracle.subtract_f64(g_hp, None, g_hs)
     assert st == oracle.OK
     np.testing.assert_array_equal(g_large, ref_large, err_msg="large hist")
-    for name, h, s in (("small", g_hs, so), ("large", g_large, lo)):
+    ref_large_o, _ = oracle.subtract_f64(ref_hp, None, ref_hs)
+    for name, h, s, h_o in (("small", g_hs, so, ref_hs), ("large", g_large, lo, ref_large_o)):
         ref, st = oracle.find_splits_f64(h, w.n_bins, lam, gamma, mcw)
         assert st == oracle.OK
         got = gb_split(s)
@@ -131,6 +135,17 @@ def level_pair(sess, oracle, w, depth, gp, lam=1.0, gamma=0.0, mcw=0.0, exact=Tr
             assert_splits_bitwise(got, ref, f"{name} splits")
         else:
             assert_splits_close(got, ref, h, w.n_bins, lam, gamma, mcw, oracle, f"{name} splits")
+            # end to end against the oracle's own histograms: best gains within 1e-5 relative
+            ref_o, _ = oracle.find_splits_f64(h_o, w.n_bins, lam, gamma, mcw)
+            fin = np.isfinite(ref_o["gain"])
+            np.testing.assert_array_equal(np.isfinite(got["gain"]), fin, err_msg=f"{name} valid nodes")
+            # 1e-5 relative to the gain's own terms (the gain is a difference of them)
+            r = ref_o[fin]
+            G, H = r["g_left"] + r["g_right"], r["h_left"] + r["h_right"]
+            mag = 0.5 * (r["g_left"] ** 2 / (r["h_left"] + lam) + r["g_right"] ** 2 / (r["h_right"] + lam)
+                         + G ** 2 / (H + lam)) + abs(gamma)
+            err = np.abs(got["gain"][fin] - r["gain"])
+            assert (err <= 1e-5 * np.maximum(np.abs(r["gain"]), mag)).all(), f"{name} gains vs the oracle's histograms"
     return g_hp, g_hs, g_large
 
 
