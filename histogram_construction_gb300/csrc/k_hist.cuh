@@ -367,6 +367,7 @@ __global__ void __launch_bounds__(H8_THREADS, 1) k_hist_u8(Hist8Params P) {
   constexpr int U = H8_U;
   extern __shared__ __align__(128) unsigned char smem[];
   __shared__ int32_t s_item;
+  __shared__ Item s_it;  // the next item, claimed and decoded by thread 0 while the last one flushes
 
   const LevelParams &p = P.lv;
   pdl_wait();     // the level plan
@@ -392,21 +393,17 @@ __global__ void __launch_bounds__(H8_THREADS, 1) k_hist_u8(Hist8Params P) {
   }
   uint32_t bad = 0;
 
+  if (threadIdx.x == 0) {
+    s_item = (int32_t)atomicAdd(&p.st->work_next, 1u);
+    if (s_item < n_items) s_it = decode_item(s_item, p, chunk, cpg);
+  }
+  __syncthreads();
   for (;;) {
-    if (threadIdx.x == 0) s_item = (int32_t)atomicAdd(&p.st->work_next, 1u);
-    __syncthreads();
     const int32_t id = s_item;
     if (id >= n_items) break;
-    const Item it = decode_item(id, p, chunk, cpg);
+    const Item it = s_it;
     const int f_tile0 = it.fgroup * 64;
     const int nsb = min(H8_SB, (P.n_features - f_tile0 + 15) >> 4);
-    // zero the slot rows that will be read back: B rows of each used sub-block
-    // (lanes of unused sub-blocks add into their own, never read, sub-block)
-    for (int sb = 0; sb < nsb; ++sb) {
-      uint4 *h4 = reinterpret_cast<uint4 *>(smem + sb * H8_SB_STRIDE);
-      for (int i = threadIdx.x; i < B * 8; i += blockDim.x) h4[i] = make_uint4(0, 0, 0, 0);
-    }
-    __syncthreads();
     const bool lane_on = w < nsb;
     const unsigned char *strip = P.mirror + mirror_offset(it.fgroup, 0, N) + w * 16;
     const int64_t step = (int64_t)8 * nwarps;  // rows between a warp's consecutive groups
@@ -417,6 +414,17 @@ __global__ void __launch_bounds__(H8_THREADS, 1) k_hist_u8(Hist8Params P) {
     h8_rows<U>(p, ident, g0, step, it.k1, rid);
     h8_gather<U>(p, strip, lane_on, par, rid, cur, bad);
     h8_rows<U>(p, ident, g0 + adv, step, it.k1, rid);
+    // with the first gathers in flight: the previous item's flush must have
+    // read the image before it is zeroed; zero the slot rows that will be read
+    // back, B rows of each used sub-block (lanes of unused sub-blocks add into
+    // their own, never read, sub-block)
+    if (threadIdx.x == 0) bulk_wait_read_all();
+    __syncthreads();
+    for (int sb = 0; sb < nsb; ++sb) {
+      uint4 *h4 = reinterpret_cast<uint4 *>(smem + sb * H8_SB_STRIDE);
+      for (int i = threadIdx.x; i < B * 8; i += blockDim.x) h4[i] = make_uint4(0, 0, 0, 0);
+    }
+    __syncthreads();
     // lanes of a warp run out of rows within one group of each other; any
     // lane with work keeps the warp going (the others add zeros)
     while (__any_sync(0xffffffffu, g0 < it.k1)) {
@@ -433,24 +441,28 @@ __global__ void __launch_bounds__(H8_THREADS, 1) k_hist_u8(Hist8Params P) {
       flush_float_image(smem, nsb, H8_SB_STRIDE, (uint32_t)B * 32u,
                         reinterpret_cast<double *>(p.partial) + it.image * p.image_int4s * 2, it.multi,
                         reinterpret_cast<double *>(smem + H8_SMEM));
-      continue;
-    }
-    // flush: the item's shared image (per sub-block [slot][16][G, H] int32)
-    // leaves as is, one TMA bulk operation per sub-block: a store when the
-    // item is its group's only chunk, else a reduce-add into the zeroed
-    // group image (exact: the group's int32 sums cannot overflow)
-    fence_proxy_async_smem();
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      int32_t *img_out = p.partial + it.image * p.image_int4s * 4;
-      for (int sb = 0; sb < nsb; ++sb) {
-        int32_t *dst = img_out + (int64_t)sb * B * 16 * 2;
-        const unsigned char *src = smem + sb * H8_SB_STRIDE;
-        if (it.multi) bulk_reduce_add_u32(dst, src, (uint32_t)B * 128u);
-        else bulk_store(dst, src, (uint32_t)B * 128u);
+    } else {
+      // flush: the item's shared image (per sub-block [slot][16][G, H] int32)
+      // leaves as is, one TMA bulk operation per sub-block: a store when the
+      // item is its group's only chunk, else a reduce-add into the zeroed
+      // group image (exact: the group's int32 sums cannot overflow). The
+      // next item's claim, decode and first gathers overlap the copy-out.
+      fence_proxy_async_smem();
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        int32_t *img_out = p.partial + it.image * p.image_int4s * 4;
+        for (int sb = 0; sb < nsb; ++sb) {
+          int32_t *dst = img_out + (int64_t)sb * B * 16 * 2;
+          const unsigned char *src = smem + sb * H8_SB_STRIDE;
+          if (it.multi) bulk_reduce_add_u32(dst, src, (uint32_t)B * 128u);
+          else bulk_store(dst, src, (uint32_t)B * 128u);
+        }
+        bulk_commit();
       }
-      bulk_commit();
-      bulk_wait_read_all();
+    }
+    if (threadIdx.x == 0) {
+      s_item = (int32_t)atomicAdd(&p.st->work_next, 1u);
+      if (s_item < n_items) s_it = decode_item(s_item, p, chunk, cpg);
     }
     __syncthreads();
   }
