@@ -831,6 +831,7 @@ gbt_status gbt_find_splits_f64(gbt_ctx *c, const double *hist, int32_t n_nodes, 
   if (n_nodes == 0) return GBT_OK;
   if (n_nodes > 65535) return fail(c, GBT_ERR_UNSUPPORTED, "n_nodes must be <= 65535");
   if (ptr_kind(hist) != 1 || !aligned16(hist)) return fail(c, GBT_ERR_INVALID_ARG, "hist must be 16-byte aligned device memory");
+  if (c->n_bins > F64_MAX_CHUNKS * 32 * SCAN_SPL) return fail(c, GBT_ERR_UNSUPPORTED, "n_bins too large");
   SplitOut *dout = nullptr;
   bool host = false;
   s = split_out_view(c, reinterpret_cast<gbt_split *>(out), n_nodes, c->splits_a, &dout, &host);

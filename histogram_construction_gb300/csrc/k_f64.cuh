@@ -30,10 +30,10 @@ __global__ void __launch_bounds__(256) k_finalize_f64(const double *__restrict__
   if (!st->plan_ok) return;
   const int64_t units = (int64_t)n_nodes * n_features * B;
   for (int64_t u = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; u < units; u += (int64_t)gridDim.x * blockDim.x) {
-    const int f = (int)(u % n_features);  // consecutive threads: consecutive features of one slot
-    int64_t r = u / n_features;
-    const int s = (int)(r % B);
-    const int n = (int)(r / B);
+    const int s = (int)(u % B);  // consecutive threads: consecutive slots of one feature (contiguous writes)
+    const int64_t r = u / B;
+    const int f = (int)(r % n_features);
+    const int n = (int)(r / n_features);
     const int fg = f / item_feats, fl = f - fg * item_feats;
     const int sb = fl / sbw, c = fl - sb * sbw;
     const int64_t cell = (((int64_t)sb * B + s) * sbw + c) * 2;
@@ -65,68 +65,338 @@ __global__ void __launch_bounds__(256) k_subtract_f64(const double *__restrict__
   }
 }
 
-// FP32 screen of a float-cell candidate from its double sums: (up, lo) with
-// lo <= gain_fp64 <= up. Each double converts to float with relative error
-// u = 2^-24, within the 4u per input that the fixed-point screen's error
-// budget (screen_f32) assumes, so its bound 2^-19 (a + b + c + |gamma|)
-// holds; values outside [2^-60, 2^60] give an infinite bound (evaluated in
-// double).
-__device__ __forceinline__ void screen_dbl(double GL, double HL, double GR, double HR, float Gf2den,
-                                           const SplitParams &sp, float &up, float &lo) {
-  const float gl = __double2float_rn(GL), hl = __double2float_rn(HL);
-  const float gr = __double2float_rn(GR), hr = __double2float_rn(HR);
-  const float dl = __fadd_rn(hl, sp.lambda_f), dr = __fadd_rn(hr, sp.lambda_f);
-  const float a = __fdividef(__fmul_rn(gl, gl), dl);
-  const float b = __fdividef(__fmul_rn(gr, gr), dr);
-  const float g = __fsub_rn(__fmul_rn(0.5f, __fsub_rn(__fadd_rn(a, b), Gf2den)), sp.gamma_f);
-  const float mag = __fadd_rn(__fadd_rn(__fadd_rn(a, b), Gf2den), sp.gamma_abs_f);
-  const float err = __fmul_rn(mag, 1.9073486328125e-06f);  // 2^-19
+// ----------------------------------------------------------------------------
+// Split find on double cells. On GB300 an FP64 add has about 65 cycles of
+// latency and about 1/64 of the FP32 throughput, a division about 560 cycles,
+// and a double -> float conversion is as slow as an FP64 add (measured), so
+// the scan screens every candidate with integer and FP32 work and touches
+// FP64 only for the few features whose candidates can still be the best.
+//
+// Screen. Per strip (one feature of one node) the cells are put on a common
+// fixed-point grid, from their bit patterns: with E the largest biased
+// exponent among the strip's g (or h) cells, a cell becomes the int64 number
+// of units 2^-k below it in magnitude (truncation), k = 62 - ceil(log2 B) -
+// (E - 1022), so that every prefix sums exactly in int64. Each of a
+// candidate's sums S (G_L, H_L, G_R, H_R, and the totals) is then known up to
+//   |S_float - S_double| <= 2.02 u |S_float| + B 2^-k + 2 B^2 2^-52 2^(E-1022)
+// (u = 2^-24: the int64 -> float conversion; the truncation of at most B
+// cells; the rounding of the double values that phase 2 uses, with a wide
+// margin), and each gain
+// term x^2 / (d + lambda) is bounded from the endpoints of these intervals,
+// widened by 16u for the float operations that form it; the gain interval is
+// widened by 2^-19 (a + b + c + |gamma|) for the final sums. A candidate is
+// certainly valid when both sides' H intervals lie above 0 and above
+// min_child_weight; only certainly valid candidates lend their lower bound to
+// the threshold; certainly invalid ones are dropped. Strips whose exponents
+// leave the usable range, and quantities outside [2^-60, 2^60], get infinite
+// intervals (evaluated in double).
+constexpr float F64_U = 5.9604644775390625e-08f;  // 2^-24
+constexpr int F64_TOT_U = 8;                       // strip loads in flight per lane in the totals passes
+
+// Units of 2^-k in x, truncated toward zero, from the bit pattern (integer
+// ALU only). Exact for zero; for a normal x with |x| 2^k < 2^61, |result
+// 2^-k - x| < 2^-k; subnormals give 0 (below 2^-1022 <= 2^-k for the k used).
+__device__ __forceinline__ int64_t dbl_to_fixed(double x, int k) {
+  const long long b = __double_as_longlong(x);
+  const int e = (int)((b >> 52) & 0x7ff);
+  if (e == 0) return 0;
+  const long long mant = (b & 0xfffffffffffffLL) | (1LL << 52);
+  const int sh = e - 1075 + k;  // x 2^k = mant 2^sh
+  long long q = 0;
+  if (sh >= 0) q = mant << sh;  // sh <= 8 by the choice of k
+  else if (sh > -63) q = mant >> (-sh);
+  return b < 0 ? -q : q;
+}
+
+// Largest biased exponent of a double (0 for zero and subnormals, 2047 for inf/NaN).
+__device__ __forceinline__ int dbl_exp(double x) { return (int)((__double_as_longlong(x) >> 52) & 0x7ff); }
+
+// Both components exactly zero (either sign), from the bit patterns.
+__device__ __forceinline__ bool dbl2_zero(double2 v) {
+  return ((unsigned long long)(__double_as_longlong(v.x) | __double_as_longlong(v.y)) << 1) == 0ull;
+}
+
+struct F64Screen {
+  float lam, gam, gam_abs, mcw_hi;  // lambda, gamma, |gamma| in float; min_child_weight rounded up
+  int filter;                        // 0: every valid candidate is evaluated in double
+};
+
+// Per-strip fixed-point grid of one component.
+struct FixGrid {
+  int k;       // units of 2^-k
+  float p2;    // 2^-k as a float
+  float eabs;  // absolute part of the error radius of a sum
+};
+
+__device__ __forceinline__ bool make_grid(int E, int B, int L, FixGrid &g) {
+  E = max(E, 1023 - 60);                // all cells below 2^-60 (or zero): the grid of 2^-60 cells
+  if (E > 1022 + 100) return false;     // cells of 2^100 and more (or inf, NaN): no screen
+  g.k = 62 - L - (E - 1022);
+  g.p2 = __int_as_float((127 - g.k) << 23);
+  const float mx = __int_as_float((E - 1022 + 127) << 23);  // 2^(E-1022) >= every |cell|
+  const float fb = (float)B;
+  g.eabs = __fadd_ru(__fadd_ru(__fmul_ru(fb, g.p2), __fmul_ru(__fmul_ru(__fmul_ru(fb, fb), mx), 4.440892098500626e-16f)),
+                     7.52316384526264e-37f);  // B 2^-k + 2 B^2 2^-52 max + 2^-120
+  return true;
+}
+
+// float value of an exact fixed-point sum and its error radius
+__device__ __forceinline__ void fix_to_f32(int64_t q, const FixGrid &g, float &v, float &e) {
+  v = __fmul_rn(i64_to_f32(q), g.p2);
+  e = __fmaf_ru(fabsf(v), 2.02f * F64_U, g.eabs);
+}
+
+// Bounds [lo_t, hi_t] of x^2 / (d + lambda) for x in [xf - ex, xf + ex], d in
+// [df - ed, df + ed]; false when the interval is unusable (denominator not
+// certainly positive, or out of range).
+__device__ __forceinline__ bool term_bounds(float xf, float ex, float df, float ed, float lam, float &lo_t,
+                                            float &hi_t) {
   const float rlo = 8.673617379884035e-19f, rhi = 1.152921504606847e+18f;  // 2^-60, 2^60
-  const float ag = fabsf(gl), ar = fabsf(gr);
-  const bool ok = (ag == 0.f || (ag > rlo && ag < rhi)) && (ar == 0.f || (ar > rlo && ar < rhi)) && dl > rlo &&
-                  dr > rlo && dl < rhi && dr < rhi && mag < rhi && (a == 0.f || a > rlo) && (b == 0.f || b > rlo) &&
-                  g == g;
-  up = ok ? __fadd_rn(g, err) : INFINITY;
-  lo = ok ? __fsub_rn(g, err) : -INFINITY;
+  const float ax = fabsf(xf);
+  const float gmin = fmaxf(0.f, __fsub_rd(ax, ex)), gmax = __fadd_ru(ax, ex);
+  const float dmin = __fsub_rd(__fadd_rd(df, lam), ed), dmax = __fadd_ru(__fadd_ru(df, lam), ed);
+  if (!(dmin > rlo && dmax < rhi && gmax < rhi)) return false;
+  hi_t = __fmul_ru(__fdividef(__fmul_ru(gmax, gmax), dmin), 1.0f + 16.f * F64_U);
+  lo_t = (gmin > rlo) ? __fmul_rd(__fdividef(__fmul_rd(gmin, gmin), dmax), 1.0f - 16.f * F64_U) : 0.f;
+  if (!(hi_t < rhi)) return false;
+  if (lo_t < rlo) lo_t = 0.f;
+  return true;
 }
 
-// Parent term G^2 / (H + lambda) in FP32 from the double totals; NaN (every
-// candidate then unscreened) outside the checked range.
-__device__ __forceinline__ float parent_dbl(double G, double H, const SplitParams &sp) {
-  const float Gf = __double2float_rn(G), Hf = __double2float_rn(H);
-  const float den = __fadd_rn(Hf, sp.lambda_f);
-  const float rlo = 8.673617379884035e-19f, rhi = 1.152921504606847e+18f;
-  const float ag = fabsf(Gf);
-  if (den > rlo && den < rhi && (ag == 0.f || (ag > rlo && ag < rhi))) {
-    const float c = __fdividef(__fmul_rn(Gf, Gf), den);
-    if (c == 0.f || (c > rlo && c < rhi)) return c;
+// One candidate from its fixed-point sums. Returns false when it is certainly
+// invalid; else up (and, when certainly valid, lo) bound its double gain.
+__device__ __forceinline__ bool screen_fix(int64_t GLq, int64_t HLq, int64_t TG, int64_t TH, const FixGrid &gg,
+                                          const FixGrid &gh, float c_lo, float c_hi, bool c_ok, const F64Screen &sc,
+                                          float &up, float &lo) {
+  float GLf, eGL, HLf, eHL, GRf, eGR, HRf, eHR;
+  fix_to_f32(GLq, gg, GLf, eGL);
+  fix_to_f32(HLq, gh, HLf, eHL);
+  fix_to_f32(TG - GLq, gg, GRf, eGR);
+  fix_to_f32(TH - HLq, gh, HRf, eHR);
+  const float hl_lo = __fsub_rd(HLf, eHL), hl_hi = __fadd_ru(HLf, eHL);
+  const float hr_lo = __fsub_rd(HRf, eHR), hr_hi = __fadd_ru(HRf, eHR);
+  if (!(hl_hi > 0.f) || !(hr_hi > 0.f)) return false;
+  const bool sure = hl_lo > 0.f && hr_lo > 0.f && hl_lo >= sc.mcw_hi && hr_lo >= sc.mcw_hi;
+  up = INFINITY;
+  lo = -INFINITY;
+  if (!sc.filter || !c_ok) return true;
+  float a_lo, a_hi, b_lo, b_hi;
+  if (!term_bounds(GLf, eGL, HLf, eHL, sc.lam, a_lo, a_hi) || !term_bounds(GRf, eGR, HRf, eHR, sc.lam, b_lo, b_hi))
+    return true;
+  const float mag = __fadd_ru(__fadd_ru(__fadd_ru(a_hi, b_hi), c_hi), sc.gam_abs);
+  const float slack = __fmul_ru(mag, 1.9073486328125e-06f);  // 2^-19
+  const float g_hi = __fsub_ru(__fmul_ru(0.5f, __fsub_ru(__fadd_ru(a_hi, b_hi), c_lo)), sc.gam);
+  const float g_lo = __fsub_rd(__fmul_rd(0.5f, __fsub_rd(__fadd_rd(a_lo, b_lo), c_hi)), sc.gam);
+  if (!(g_hi == g_hi) || !(g_lo == g_lo) || !(mag < 1.152921504606847e+18f)) return true;
+  up = __fadd_ru(g_hi, slack);
+  if (sure) lo = __fsub_rd(g_lo, slack);
+  return true;
+}
+
+// Fixed-point prefixes of chunk [c0, c0 + 128): lane-local inclusive
+// prefixes and the exclusive prefix of the lane's first slot (carry: the sums
+// before the chunk, updated).
+__device__ __forceinline__ void scan_chunk_fix(const double2 *strip, int n_bins, int c0, int kg, int kh,
+                                               int64_t (&carry)[2], int64_t (&pg)[SCAN_SPL],
+                                               int64_t (&ph)[SCAN_SPL], int64_t &eg, int64_t &eh) {
+  const int lane = threadIdx.x & 31;
+  double2 v[SCAN_SPL];
+#pragma unroll
+  for (int i = 0; i < SCAN_SPL; ++i) {
+    const int s = c0 + SCAN_SPL * lane + i;
+    v[i] = s < n_bins ? __ldg(strip + s) : make_double2(0.0, 0.0);
   }
-  return __int_as_float(0x7fc00000);
+  int64_t ag = 0, ah = 0;
+#pragma unroll
+  for (int i = 0; i < SCAN_SPL; ++i) {
+    ag += dbl_to_fixed(v[i].x, kg);
+    ah += dbl_to_fixed(v[i].y, kh);
+    pg[i] = ag;
+    ph[i] = ah;
+  }
+  int64_t x = ag, y = ah;
+  warp_incl_scan(x, y);
+  const int64_t tx = shfl_i64(x, 31), ty = shfl_i64(y, 31);
+  eg = x - ag + carry[0];
+  eh = y - ah + carry[1];
+  carry[0] += tx;
+  carry[1] += ty;
 }
 
-// Split find on double cells: grid (ceil(F / 8), n_nodes), 256 threads; warp w
-// scans feature blockIdx.x * 8 + w of node blockIdx.y. Prefix sums are double;
-// each valid candidate is screened in FP32 with a rigorous bound and only
-// those whose upper bound reaches the warp's running best lower bound are
-// evaluated in double (the best candidate and every candidate tied with it
-// always are; FP64 is a small fraction of the FP32 rate on this part). The
-// CTA's best goes to cand[node][blockIdx.x]; the node's last CTA writes the
-// split. The double sums travel as bit patterns in the candidate's 64-bit
-// fields, so the output record is a gbt_split whose four sums are doubles.
-__global__ void __launch_bounds__(SCAN_THREADS) k_find_f64(const double *__restrict__ hist, int32_t n_features,
-                                                           int32_t n_bins, SplitParams sp, double mcw,
-                                                           Cand *__restrict__ cand, uint32_t *__restrict__ counters,
-                                                           SplitOut *__restrict__ out) {
+__device__ __forceinline__ float warp_max_f(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// An exact fixed-point sum as a double (one rounding; the scaling by 2^-k is exact).
+__device__ __forceinline__ double fix_to_f64(int64_t q, const FixGrid &g) {
+  return __dmul_rn(__ll2double_rn((long long)q), __longlong_as_double((long long)(1023 - g.k) << 52));
+}
+
+// Validity and gain of one candidate in double; keeps the better of it and best.
+__device__ __forceinline__ void f64_consider(double GL, double HL, double GR, double HR, double parent, double mcw,
+                                             const SplitParams &sp, int f, int t, int dir, Cand &best) {
+  if (!(HL > 0.0 && HR > 0.0 && HL >= mcw && HR >= mcw)) return;
+  const double l2 = __ddiv_rn(__dmul_rn(GL, GL), __dadd_rn(HL, sp.lambda));
+  const double r2 = __ddiv_rn(__dmul_rn(GR, GR), __dadd_rn(HR, sp.lambda));
+  const double gain = __dsub_rn(__dmul_rn(0.5, __dsub_rn(__dadd_rn(l2, r2), parent)), sp.gamma);
+  Cand c;
+  set_exact(c, gain);
+  c.t = t;
+  c.dir = dir;
+  c.f = f;
+  c.gl = __double_as_longlong(GL);
+  c.hl = __double_as_longlong(HL);
+  c.gr = __double_as_longlong(GR);
+  c.hr = __double_as_longlong(HR);
+  if (cand_better(c, best)) best = c;
+}
+
+constexpr int F64_MAX_CHUNKS = 80;  // 128-slot chunks per strip (n_bins <= 10240, the u16 limit)
+
+// What phase 2 needs of a warp's strip.
+struct F64Strip {
+  int64_t TG, TH, mq_g, mq_h;
+  FixGrid gg, gh;
+  float c_lo, c_hi;
+  int c_ok, ok, no_missing;
+};
+
+// grid (ceil(F / 8), n_nodes), 256 threads. Phase 1: warp w screens feature
+// blockIdx.x * 8 + w of node blockIdx.y, keeping its best certain lower bound
+// and, per 128-slot chunk, the largest upper bound and the fixed-point sums
+// before the chunk. The CTA's threshold is the largest lower bound of its
+// warps. Phase 2: every (feature, chunk) whose largest upper bound reaches
+// the threshold is a task; the tasks are dealt round-robin to the CTA's warps,
+// which rescan the chunk and evaluate in double each candidate whose upper
+// bound reaches the threshold. A feature without a usable grid is scanned
+// wholly in double by its own warp. The CTA's best goes to
+// cand[node][blockIdx.x]; the node's last CTA writes the split. The double
+// sums travel as bit patterns in the candidate's 64-bit fields, so the output
+// record is a gbt_split whose four sums are doubles.
+__global__ void __launch_bounds__(SCAN_THREADS, 2) k_find_f64(const double *__restrict__ hist, int32_t n_features,
+                                                              int32_t n_bins, SplitParams sp, double mcw,
+                                                              Cand *__restrict__ cand,
+                                                              uint32_t *__restrict__ counters,
+                                                              SplitOut *__restrict__ out) {
   __shared__ Cand s_best[SCAN_WARPS];
+  __shared__ float s_lo[SCAN_WARPS];
+  __shared__ F64Strip s_strip[SCAN_WARPS];
+  __shared__ float s_cup[SCAN_WARPS][F64_MAX_CHUNKS];
+  __shared__ int64_t s_carry[SCAN_WARPS][F64_MAX_CHUNKS][2];
   __shared__ uint32_t s_last;
   pdl_wait();
   const int node = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int f = blockIdx.x * SCAN_WARPS + warp;
   const int B = n_bins + 1;
+  const int L = 32 - __clz(B - 1);  // ceil(log2 B)
+  const int n_chunks = (n_bins + 32 * SCAN_SPL - 1) / (32 * SCAN_SPL);
+  F64Screen sc;
+  sc.lam = sp.lambda_f;
+  sc.gam = sp.gamma_f;
+  sc.gam_abs = sp.gamma_abs_f;
+  sc.mcw_hi = __double2float_ru(mcw);
+  sc.filter = sp.filter;
+  const bool active = f < n_features;
+  float run_lo = -INFINITY;
   Cand best = no_cand();
-  if (f < n_features) {
+  // ---- phase 1
+  {
     const double2 *strip = reinterpret_cast<const double2 *>(hist) + ((int64_t)node * n_features + f) * B;
+    F64Strip st;
+    st.TG = st.TH = st.mq_g = st.mq_h = 0;
+    st.c_lo = st.c_hi = 0.f;
+    st.c_ok = st.ok = st.no_missing = 0;
+    if (active) {
+      int Eg = 0, Eh = 0;
+      for (int s0 = lane; s0 < B; s0 += 32 * F64_TOT_U) {
+        double2 v[F64_TOT_U];
+#pragma unroll
+        for (int u = 0; u < F64_TOT_U; ++u) {
+          const int s = s0 + 32 * u;
+          v[u] = s < B ? __ldg(strip + s) : make_double2(0.0, 0.0);
+        }
+#pragma unroll
+        for (int u = 0; u < F64_TOT_U; ++u) {
+          Eg = max(Eg, dbl_exp(v[u].x));
+          Eh = max(Eh, dbl_exp(v[u].y));
+        }
+      }
+      Eg = (int)__reduce_max_sync(0xffffffffu, (unsigned)Eg);
+      Eh = (int)__reduce_max_sync(0xffffffffu, (unsigned)Eh);
+      const double2 m = __ldg(strip + n_bins);
+      st.no_missing = dbl2_zero(m);
+      st.ok = make_grid(Eg, B, L, st.gg) && make_grid(Eh, B, L, st.gh) && sc.filter;
+      if (st.ok) {
+        int64_t TG = 0, TH = 0;
+        for (int s0 = lane; s0 < B; s0 += 32 * F64_TOT_U) {
+          double2 v[F64_TOT_U];
+#pragma unroll
+          for (int u = 0; u < F64_TOT_U; ++u) {
+            const int s = s0 + 32 * u;
+            v[u] = s < B ? __ldg(strip + s) : make_double2(0.0, 0.0);
+          }
+#pragma unroll
+          for (int u = 0; u < F64_TOT_U; ++u) {
+            TG += dbl_to_fixed(v[u].x, st.gg.k);
+            TH += dbl_to_fixed(v[u].y, st.gh.k);
+          }
+        }
+        warp_sum2(TG, TH);
+        st.TG = TG;
+        st.TH = TH;
+        st.mq_g = dbl_to_fixed(m.x, st.gg.k);
+        st.mq_h = dbl_to_fixed(m.y, st.gh.k);
+        float Gf, eG, Hf, eH;
+        fix_to_f32(TG, st.gg, Gf, eG);
+        fix_to_f32(TH, st.gh, Hf, eH);
+        st.c_ok = term_bounds(Gf, eG, Hf, eH, sc.lam, st.c_lo, st.c_hi);
+        int64_t carry[2] = {0, 0};
+        for (int c = 0; c < n_chunks; ++c) {
+          const int c0 = c * 32 * SCAN_SPL;
+          if (lane == 0) {
+            s_carry[warp][c][0] = carry[0];
+            s_carry[warp][c][1] = carry[1];
+          }
+          int64_t pg[SCAN_SPL], ph[SCAN_SPL], eg, eh;
+          scan_chunk_fix(strip, n_bins, c0, st.gg.k, st.gh.k, carry, pg, ph, eg, eh);
+          float cup = -INFINITY;
+#pragma unroll
+          for (int i = 0; i < SCAN_SPL; ++i) {
+            if (c0 + SCAN_SPL * lane + i >= n_bins) continue;
+#pragma unroll
+            for (int dir = 0; dir < 2; ++dir) {
+              if (dir && st.no_missing) continue;  // empty missing slot: same sums, missing-right comes first
+              float u, l;
+              if (!screen_fix(eg + pg[i] + (dir ? st.mq_g : 0), eh + ph[i] + (dir ? st.mq_h : 0), TG, TH, st.gg,
+                              st.gh, st.c_lo, st.c_hi, st.c_ok, sc, u, l))
+                continue;
+              cup = fmaxf(cup, u);
+              run_lo = fmaxf(run_lo, l);
+            }
+          }
+          cup = warp_max_f(cup);
+          if (lane == 0) s_cup[warp][c] = cup;
+        }
+        run_lo = warp_max_f(run_lo);
+      }
+    }
+    if (lane == 0) {
+      s_lo[warp] = run_lo;
+      s_strip[warp] = st;
+    }
+  }
+  __syncthreads();
+  float thr = -INFINITY;
+#pragma unroll
+  for (int w = 0; w < SCAN_WARPS; ++w) thr = fmaxf(thr, s_lo[w]);
+  // ---- phase 2a: a strip without a usable grid, wholly in double, by its own warp
+  if (active && !s_strip[warp].ok) {
+    const double2 *strip = reinterpret_cast<const double2 *>(hist) + ((int64_t)node * n_features + f) * B;
+    const double2 m = __ldg(strip + n_bins);
+    const bool no_missing = s_strip[warp].no_missing;
     double G = 0.0, H = 0.0;
     for (int s = lane; s < B; s += 32) {
       const double2 v = __ldg(strip + s);
@@ -138,10 +408,7 @@ __global__ void __launch_bounds__(SCAN_THREADS) k_find_f64(const double *__restr
       G += __shfl_xor_sync(0xffffffffu, G, o);
       H += __shfl_xor_sync(0xffffffffu, H, o);
     }
-    const double2 m = __ldg(strip + n_bins);
     const double parent = __ddiv_rn(__dmul_rn(G, G), __dadd_rn(H, sp.lambda));
-    const float Gf2den = sp.filter ? parent_dbl(G, H, sp) : 0.f;
-    float run_lo = -INFINITY;
     double cg = 0.0, ch = 0.0;
     for (int c0 = 0; c0 < n_bins; c0 += 32 * SCAN_SPL) {
       double pg[SCAN_SPL], ph[SCAN_SPL], ag = 0.0, ah = 0.0;
@@ -168,49 +435,57 @@ __global__ void __launch_bounds__(SCAN_THREADS) k_find_f64(const double *__restr
       eh = eh - ah + ch;
       cg += tg;
       ch += th;
-      float up[SCAN_SPL][2];
-      uint32_t vmask = 0;
-      float l = -INFINITY;
 #pragma unroll
       for (int i = 0; i < SCAN_SPL; ++i) {
-        const int s = c0 + SCAN_SPL * lane + i;
+        if (c0 + SCAN_SPL * lane + i >= n_bins) continue;
 #pragma unroll
         for (int dir = 0; dir < 2; ++dir) {
-          up[i][dir] = -INFINITY;
-          if (s >= n_bins) continue;
+          if (dir && no_missing) continue;
           const double GL = eg + pg[i] + (dir ? m.x : 0.0), HL = eh + ph[i] + (dir ? m.y : 0.0);
-          const double GR = G - GL, HR = H - HL;
-          if (!(HL > 0.0 && HR > 0.0 && HL >= mcw && HR >= mcw)) continue;
-          float u = INFINITY, lw = -INFINITY;
-          if (sp.filter) screen_dbl(GL, HL, GR, HR, Gf2den, sp, u, lw);
-          up[i][dir] = u;
-          vmask |= 1u << (2 * i + dir);
-          l = fmaxf(l, lw);
+          f64_consider(GL, HL, G - GL, H - HL, parent, mcw, sp, f, c0 + SCAN_SPL * lane + i, dir, best);
         }
       }
+    }
+  }
+  // ---- phase 2b: tasks (feature, chunk) whose upper bound reaches the threshold, dealt to the warps. The
+  // candidates' sums are the exact fixed-point sums (cells truncated to the strip's grid, summed without
+  // rounding in int64) rounded once to double: within B 2^-k + 2^-53 |S| of the exact sums of the double
+  // cells, and equal to them whenever the cells lie on the grid.
+  {
+    int task = 0;
+    for (int w = 0; w < SCAN_WARPS; ++w) {
+      if (blockIdx.x * SCAN_WARPS + w >= n_features || !s_strip[w].ok) continue;
+      for (int c = 0; c < n_chunks; ++c) {
+        if (!(s_cup[w][c] >= thr)) continue;
+        if ((task++ % SCAN_WARPS) != warp) continue;
+        const F64Strip &st = s_strip[w];
+        const int fw = blockIdx.x * SCAN_WARPS + w;
+        const double2 *strip = reinterpret_cast<const double2 *>(hist) + ((int64_t)node * n_features + fw) * B;
+        const int c0 = c * 32 * SCAN_SPL;
+        int64_t carry[2] = {s_carry[w][c][0], s_carry[w][c][1]};
+        int64_t pg[SCAN_SPL], ph[SCAN_SPL], eg, eh;
+        scan_chunk_fix(strip, n_bins, c0, st.gg.k, st.gh.k, carry, pg, ph, eg, eh);
+        double G = 0.0, H = 0.0, parent = 0.0;
+        bool have_parent = false;
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) l = fmaxf(l, __shfl_xor_sync(0xffffffffu, l, o));
-      run_lo = fmaxf(run_lo, l);
+        for (int i = 0; i < SCAN_SPL; ++i) {
+          if (c0 + SCAN_SPL * lane + i >= n_bins) continue;
 #pragma unroll
-      for (int i = 0; i < SCAN_SPL; ++i) {
-#pragma unroll
-        for (int dir = 0; dir < 2; ++dir) {
-          if (!((vmask >> (2 * i + dir)) & 1u) || up[i][dir] < run_lo) continue;  // invalid, or below a lower bound
-          const double GL = eg + pg[i] + (dir ? m.x : 0.0), HL = eh + ph[i] + (dir ? m.y : 0.0);
-          const double GR = G - GL, HR = H - HL;
-          const double l2 = __ddiv_rn(__dmul_rn(GL, GL), __dadd_rn(HL, sp.lambda));
-          const double r2 = __ddiv_rn(__dmul_rn(GR, GR), __dadd_rn(HR, sp.lambda));
-          const double gain = __dsub_rn(__dmul_rn(0.5, __dsub_rn(__dadd_rn(l2, r2), parent)), sp.gamma);
-          Cand c;
-          set_exact(c, gain);
-          c.t = c0 + SCAN_SPL * lane + i;
-          c.dir = dir;
-          c.f = f;
-          c.gl = __double_as_longlong(GL);
-          c.hl = __double_as_longlong(HL);
-          c.gr = __double_as_longlong(GR);
-          c.hr = __double_as_longlong(HR);
-          if (cand_better(c, best)) best = c;
+          for (int dir = 0; dir < 2; ++dir) {
+            if (dir && st.no_missing) continue;
+            const int64_t GLq = eg + pg[i] + (dir ? st.mq_g : 0), HLq = eh + ph[i] + (dir ? st.mq_h : 0);
+            float u, l;
+            if (!screen_fix(GLq, HLq, st.TG, st.TH, st.gg, st.gh, st.c_lo, st.c_hi, st.c_ok, sc, u, l) || u < thr)
+              continue;
+            if (!have_parent) {
+              G = fix_to_f64(st.TG, st.gg);
+              H = fix_to_f64(st.TH, st.gh);
+              parent = __ddiv_rn(__dmul_rn(G, G), __dadd_rn(H, sp.lambda));
+              have_parent = true;
+            }
+            f64_consider(fix_to_f64(GLq, st.gg), fix_to_f64(HLq, st.gh), fix_to_f64(st.TG - GLq, st.gg),
+                         fix_to_f64(st.TH - HLq, st.gh), parent, mcw, sp, fw, c0 + SCAN_SPL * lane + i, dir, best);
+          }
         }
       }
     }

@@ -278,3 +278,42 @@ def test_level5_full_size(gb, oracle):
     with Session() as s:
         s.upload_bins(w.bins, w.n_bins, w.sentinel)
         level_pair(s, oracle, w, 5, w.gpair, exact=False)
+
+
+def _dyadic_strip(rng, B, scale_g=1.0, scale_h=1.0):
+    g = np.round(rng.standard_normal(B) * 64.0 * scale_g) / 64.0
+    h = np.maximum(np.round(rng.uniform(0.0, 1.0, B) * 64.0 * scale_h), 1.0) / 64.0
+    return np.stack([g, h], axis=-1)
+
+
+@pytest.mark.parametrize("lam,gamma,mcw,scale", [(1.0, 0.0, 0.0, 1.0), (0.0, 0.5, 2.0, 1.0), (1.0, 0.0, 1.0, 2.0 ** 20),
+                                                 (0.25, 0.0, 0.0, 2.0 ** -8)])
+def test_split_find_near_ties(gb, oracle, lam, gamma, mcw, scale):
+    """Histograms built to stress the FP32 screen: identical features (exact ties: the smallest feature must win),
+    copies perturbed by one 2^-6 step moved between neighbouring bins (gains within ~1e-6 of each other),
+    min_child_weight landing exactly on prefix sums, and large or small magnitudes. Dyadic cells: every sum is
+    exact, so the GPU must match the oracle bit for bit."""
+    g, Session, _ = gb
+    rng = np.random.default_rng(11)
+    n_bins, F, n_nodes = 255, 37, 3
+    B = n_bins + 1
+    hist = np.zeros((n_nodes, F, B, 2))
+    base = _dyadic_strip(rng, B, scale, scale)
+    for n in range(n_nodes):
+        for f in range(F):
+            st = base.copy()
+            if n >= 1 and f % 3:
+                k = (f * 7 + n) % (B - 2)
+                st[k, 0] += 1.0 / 64.0 * scale
+                st[k + 1, 0] -= 1.0 / 64.0 * scale
+            hist[n, f] = st
+    with Session() as s:
+        s.upload_bins(np.zeros((F, 64), dtype=np.uint8), n_bins, 255)
+        d = torch.from_numpy(hist).cuda()
+        sp = s.find_splits_f64(d, lam, gamma, mcw)
+        assert s.sync() == 0
+        ref, st = oracle.find_splits_f64(hist, n_bins, lam, gamma, mcw)
+        assert st == oracle.OK
+        got = gb_split(sp)
+        assert_splits_bitwise(got, ref, "near ties")
+        assert got["feature"][0] == 0  # exact ties across identical features: the first one wins
