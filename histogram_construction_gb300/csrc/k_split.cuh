@@ -581,64 +581,80 @@ __device__ __forceinline__ float key_lo(uint32_t k) {
   return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
 }
 
-// Node reduce over the n_ent published candidates of one node, by the `nthr`
-// threads t0 .. t0 + nthr - 1 (whole warps): candidates whose upper bound
-// reaches the node threshold (the best lower bound published for the node)
-// are evaluated in double (unless exact); the best by (gain desc, feature, t,
-// direction asc) becomes the node's split. `slot` (nthr / 32 entries of
-// shared memory) gathers the warp results.
-__device__ __forceinline__ void reduce_node(const Cand *cand, int n_ent, float thr, const SplitParams &sp,
-                                            SplitOut *out, int t0, int nthr, Cand *slot) {
-  const int t = threadIdx.x - t0, lane = threadIdx.x & 31, w = t >> 5;
-  Cand best = no_cand();
+// Warp argmax in the order of cand_better on the keys alone (gain bits,
+// feature, slot and direction); returns the lane holding the best record.
+__device__ __forceinline__ int warp_argmax_lane(const Cand &best) {
+  double g = best.gain;
+  int f = best.f, td = best.f == INT32_MAX ? INT32_MAX : best.t * 2 + best.dir;
+  const int my_td = td;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const double og = __shfl_xor_sync(0xffffffffu, g, o);
+    const int of = __shfl_xor_sync(0xffffffffu, f, o), otd = __shfl_xor_sync(0xffffffffu, td, o);
+    const bool better = of != INT32_MAX &&
+                        (f == INT32_MAX || (og != g ? og > g : (of != f ? of < f : otd < td)));
+    if (better) {
+      g = og;
+      f = of;
+      td = otd;
+    }
+  }
+  const bool mine = best.f == f && my_td == td && __double_as_longlong(best.gain) == __double_as_longlong(g);
+  return __ffs(__ballot_sync(0xffffffffu, mine)) - 1;
+}
+
+// Node reduce by the nthr threads from t0 (whole warps, named barrier `bar`)
+// over the n_ent published candidates of one node. The node threshold is the
+// best published lower bound; candidates whose upper bound reaches it are
+// evaluated in double (unless exact already) and the best one is written to
+// out. slot: nthr / 32 Cand of shared scratch, sthr: nthr / 32 floats.
+__device__ __forceinline__ void reduce_node(const Cand *cand, int n_ent, const SplitParams &sp, SplitOut *out,
+                                            int t0, int nthr, int bar, Cand *slot, float *sthr) {
+  const int t = threadIdx.x - t0, lane = threadIdx.x & 31, w = t >> 5, nw = nthr >> 5;
+  float thr = -INFINITY;
   for (int i = t; i < n_ent; i += nthr) {
     const int4 w3 = __ldcg(reinterpret_cast<const int4 *>(cand + i) + 3);  // hr, up, lo
+    thr = fmaxf(thr, __int_as_float(w3.w));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) thr = fmaxf(thr, __shfl_xor_sync(0xffffffffu, thr, o));
+  if (lane == 0) sthr[w] = thr;
+  named_sync(bar, nthr);
+  for (int k = 0; k < nw; ++k) thr = fmaxf(thr, sthr[k]);
+  Cand best = no_cand();
+  for (int i = t; i < n_ent; i += nthr) {
+    const int4 w3 = __ldcg(reinterpret_cast<const int4 *>(cand + i) + 3);
     if (!(__int_as_float(w3.z) >= thr)) continue;
     Cand c = load_cand(cand + i);
     if (c.f == INT32_MAX) continue;
     if (!c.exact) set_exact(c, surv_gain(c.gl, c.hl, c.gl + c.gr, c.hl + c.hr, sp));
     if (cand_better(c, best)) best = c;
   }
-  best = warp_best_cand(best);
-  if (lane == 0) slot[w] = best;
-  named_sync(1 + t0 / 128, nthr);
+  if (lane == warp_argmax_lane(best)) slot[w] = best;
+  named_sync(bar, nthr);
   if (w == 0) {
-    Cand b = lane < nthr / 32 ? slot[lane] : no_cand();
-    b = warp_best_cand(b);
-    if (lane == 0) *out = cand_to_split(b);
+    const Cand b = lane < nw ? slot[lane] : no_cand();
+    if (lane == warp_argmax_lane(b)) *out = cand_to_split(b);
   }
 }
 
-// Stores the CTA's published candidates (dst[set] + 0 .. PUB_K-1), raises the
-// node thresholds key[set] to the best published lower bound and counts the
-// CTA in; returns true in the last CTA of the group, which gets the node
-// thresholds in thr_out and resets the counter and the keys. No CTA waits.
+// Stores the CTA's published candidates (dst[set] + 0 .. PUB_K-1) and counts
+// the CTA in; returns true in the last CTA of the group, which resets the
+// counter. No CTA waits.
 __device__ __forceinline__ bool cta_publish(ScanShared &sh, int n_sets, Cand *dst0, Cand *dst1, uint32_t *counter,
-                                            uint32_t *key0, uint32_t *key1, uint32_t group_ctas, float *thr_out) {
+                                            uint32_t group_ctas) {
   if (threadIdx.x < n_sets * PUB_K) {
     const int set = threadIdx.x / PUB_K, k = threadIdx.x % PUB_K;
-    const Cand c = sh.pub[set][k];
-    (set == 0 ? dst0 : dst1)[k] = c;
-    if (c.f != INT32_MAX) atomicMax(set == 0 ? key0 : key1, lo_key(c.lo));
+    (set == 0 ? dst0 : dst1)[k] = sh.pub[set][k];
     __threadfence();
   }
   __syncthreads();
   if (threadIdx.x == 0) {
     const uint32_t done = atomicAdd(counter, 1u);
     sh.last = (done == group_ctas - 1) ? 1u : 0u;
-    if (sh.last) {
-      __threadfence();
-      const uint32_t k0 = atomicExch(key0, 0u);
-      const uint32_t k1 = n_sets > 1 ? atomicExch(key1, 0u) : 0u;
-      sh.red[0] = k0 ? key_lo(k0) : -INFINITY;
-      sh.red[1] = k1 ? key_lo(k1) : -INFINITY;
-      *counter = 0;
-      __threadfence();
-    }
+    if (sh.last) *counter = 0;  // every CTA of the group has counted in
   }
   __syncthreads();
-  thr_out[0] = sh.red[0];
-  thr_out[1] = sh.red[1];
   return sh.last != 0;
 }
 
@@ -701,11 +717,9 @@ __global__ void __launch_bounds__(SCAN_THREADS, 3) k_find(const int64_t *__restr
   cta_select(sh, sp, 1, thr, warp_node);
   const int nfb = gridDim.x;
   Cand *cn = cand + (int64_t)node * nfb * PUB_K;
-  float nthr[2];
-  uint32_t *key = counters + gridDim.y + node;  // node threshold keys follow the counters
-  if (cta_publish(sh, 1, cn + blockIdx.x * PUB_K, nullptr, counters + node, key, nullptr, nfb, nthr)) {
+  if (cta_publish(sh, 1, cn + blockIdx.x * PUB_K, nullptr, counters + node, nfb)) {
     __threadfence();
-    reduce_node(cn, nfb * PUB_K, nthr[0], sp, out + node, 0, SCAN_THREADS, sh.extra);
+    reduce_node(cn, nfb * PUB_K, sp, out + node, 0, SCAN_THREADS, 1, sh.extra, sh.red);
   }
 }
 
@@ -733,24 +747,28 @@ __global__ void __launch_bounds__(SCAN_THREADS, 3) k_level_finish(
     uint32_t *__restrict__ counters, SplitOut *__restrict__ small_out, SplitOut *__restrict__ large_out,
     DevState *st) {
   __shared__ ScanShared sh;
-  pdl_wait();  // the histogram kernel (or whatever ran before on the stream)
-  if (FROM_PARTIALS && !st->plan_ok) return;
   const int p = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int fo = warp & 3, side = warp >> 2;
   const int f = blockIdx.x * 4 + fo;
   const int B = n_bins + 1;
   const bool staged = B <= STAGE_SLOTS;
-  scan_init(sh);
+  const bool active = f < n_features;
   const int64_t pp = parent_of ? (int64_t)parent_of[p] : p;
   const longlong2 *P = reinterpret_cast<const longlong2 *>(parent) + (pp * n_features + f) * B;
+  // The parent strips (and parent_of) were complete before the kernel this one
+  // waits for started, so warps 4-7 stage them while that kernel finishes.
+  if (side == 1 && active && staged)
+    for (int s = lane; s < B; s += 32) sh.cells[warp][s] = __ldg(P + s);
+  pdl_wait();  // the histogram kernel (or whatever ran before on the stream)
+  if (FROM_PARTIALS && !st->plan_ok) return;
+  scan_init(sh);
   longlong2 *L = reinterpret_cast<longlong2 *>(large) + ((int64_t)p * n_features + f) * B;
   longlong2 *Sout = FROM_PARTIALS ? reinterpret_cast<longlong2 *>(src.hist_out) + ((int64_t)p * n_features + f) * B
                                   : nullptr;
   const longlong2 *Sin = FROM_PARTIALS ? Sout
                                        : reinterpret_cast<const longlong2 *>(src.hist) + ((int64_t)p * n_features + f) * B;
-  const bool active = f < n_features;
-  // phase A: small strips (warps 0-3), parent strips (warps 4-7)
+  // phase A: small strips (warps 0-3); the parent strips (warps 4-7) are staged above
   if (side == 0) {
     if (FROM_PARTIALS) {
       // the 128 threads sum the group images of all four features: thread t
@@ -793,8 +811,6 @@ __global__ void __launch_bounds__(SCAN_THREADS, 3) k_level_finish(
     } else if (active && staged) {
       for (int s = lane; s < B; s += 32) sh.cells[warp][s] = __ldg(Sin + s);
     }
-  } else if (active && staged) {
-    for (int s = lane; s < B; s += 32) sh.cells[warp][s] = __ldg(P + s);
   }
   __syncthreads();
   // phase B: large = parent - small
@@ -846,14 +862,11 @@ __global__ void __launch_bounds__(SCAN_THREADS, 3) k_level_finish(
   const int nfb = gridDim.x;
   Cand *cs_base = cand + (int64_t)(2 * p) * nfb * PUB_K;
   Cand *cl_base = cand + (int64_t)(2 * p + 1) * nfb * PUB_K;
-  float nthr[2];
-  uint32_t *key = counters + gridDim.y + 2 * p;  // node threshold keys follow the counters
-  if (cta_publish(sh, 2, cs_base + blockIdx.x * PUB_K, cl_base + blockIdx.x * PUB_K, counters + p, key, key + 1, nfb,
-                  nthr)) {
+  if (cta_publish(sh, 2, cs_base + blockIdx.x * PUB_K, cl_base + blockIdx.x * PUB_K, counters + p, nfb)) {
     __threadfence();
     // warps 0-3 reduce the small sibling, warps 4-7 the large one
-    if (threadIdx.x < 128) reduce_node(cs_base, nfb * PUB_K, nthr[0], sp, small_out + p, 0, 128, sh.extra);
-    else reduce_node(cl_base, nfb * PUB_K, nthr[1], sp, large_out + p, 128, 128, sh.extra + 4);
+    if (threadIdx.x < 128) reduce_node(cs_base, nfb * PUB_K, sp, small_out + p, 0, 128, 1, sh.extra, sh.red);
+    else reduce_node(cl_base, nfb * PUB_K, sp, large_out + p, 128, 128, 2, sh.extra + 4, sh.red + 4);
   }
 }
 
