@@ -336,19 +336,23 @@ struct ScanShared {
 };
 
 // Warp scan of one strip of `cells` (shared or global memory; missing cell at
-// n_bins) with totals (tg, th) and sabs = sum of |G| over its slots: screens
-// every candidate and pushes into the CTA pool those whose upper bound reaches
-// the best lower bound seen so far. Lane l takes the SCAN_SPL consecutive
-// slots of each (32 * SCAN_SPL)-slot chunk: prefix sums run in registers,
-// with one warp scan of the lane totals per chunk.
-__device__ __forceinline__ float warp_scan_push(const longlong2 *cells, int n_bins, int64_t tg, int64_t th,
-                                                int64_t sabs, const SplitParams &sp, int f, int node, ScanShared &sh,
-                                                int &overflow) {
+// n_bins) with totals (tg, th): screens every candidate and pushes into the
+// CTA pool those whose upper bound reaches the best lower bound seen so far.
+// Lane l takes the SCAN_SPL consecutive slots of each (32 * SCAN_SPL)-slot
+// chunk: prefix sums run in registers, with one warp scan of the lane totals
+// per chunk. ND: directions scanned (1 when the missing slot is empty: both
+// directions then give the same sums, and missing-right comes first, so the
+// left direction can never win); mode 0: screen_fast, 1: screen_f32, 2: no
+// screen (every valid candidate pushed with an infinite upper bound); MODE
+// fixes it at compile time, or -1 takes `mode`.
+__device__ __forceinline__ bool no_missing_rt(longlong2 m) { return m.x == 0 && m.y == 0; }
+
+template <int ND, int MODE>
+__device__ __forceinline__ float scan_push_impl(const longlong2 *cells, int n_bins, int64_t tg, int64_t th,
+                                                longlong2 m, float Gf2den, const SplitParams &sp, int f, int node,
+                                                ScanShared &sh, int &overflow, int mode) {
+  if (MODE >= 0) mode = MODE;
   const int lane = threadIdx.x & 31;
-  const longlong2 m = cells[n_bins];
-  const bool no_missing = (m.x == 0 && m.y == 0);
-  const float Gf2den = parent_f32(tg, th, sp);
-  const bool fast = strip_fast(sabs, th, Gf2den, sp);
   float run_lo = -INFINITY;
   int64_t carry_g = 0, carry_h = 0;
   for (int c0 = 0; c0 < n_bins; c0 += 32 * SCAN_SPL) {
@@ -371,23 +375,21 @@ __device__ __forceinline__ float warp_scan_push(const longlong2 *cells, int n_bi
     eh += carry_h - ah;
     carry_g += tot_g;
     carry_h += tot_h;
-    float up[SCAN_SPL][2], lo[SCAN_SPL][2];
+    float up[SCAN_SPL][ND], lo[SCAN_SPL][ND];
     uint32_t vmask = 0;
     float l = -INFINITY;
 #pragma unroll
     for (int i = 0; i < SCAN_SPL; ++i) {
       const int s = c0 + SCAN_SPL * lane + i;
 #pragma unroll
-      for (int dir = 0; dir < 2; ++dir) {
+      for (int dir = 0; dir < ND; ++dir) {
         const int64_t GL = eg + pg[i] + (dir ? m.x : 0), HL = eh + ph[i] + (dir ? m.y : 0);
         const int64_t HR = th - HL;
-        // with an empty missing slot both directions give the same sums, and
-        // missing-right comes first: the left direction can never win
-        const bool valid = s < n_bins && HL >= sp.h_min && HR >= sp.h_min && !(dir && no_missing);
+        const bool valid = s < n_bins && HL >= sp.h_min && HR >= sp.h_min && !(ND == 2 && dir && no_missing_rt(m));
         float u = -INFINITY, lw = -INFINITY;
         if (valid) {
-          if (fast) screen_fast(GL, HL, tg - GL, HR, Gf2den, sp, u, lw);
-          else if (sp.filter) screen_f32(GL, HL, tg - GL, HR, Gf2den, sp, u, lw);
+          if (mode == 0) screen_fast(GL, HL, tg - GL, HR, Gf2den, sp, u, lw);
+          else if (mode == 1) screen_f32(GL, HL, tg - GL, HR, Gf2den, sp, u, lw);
           else u = INFINITY;
           vmask |= 1u << (2 * i + dir);
         }
@@ -402,7 +404,7 @@ __device__ __forceinline__ float warp_scan_push(const longlong2 *cells, int n_bi
 #pragma unroll
     for (int i = 0; i < SCAN_SPL; ++i) {
 #pragma unroll
-      for (int dir = 0; dir < 2; ++dir) {
+      for (int dir = 0; dir < ND; ++dir) {
         if (!((vmask >> (2 * i + dir)) & 1u) || up[i][dir] < run_lo) continue;
         const int idx = atomicAdd(&sh.n, 1);
         if (idx >= SURV_CAP) {
@@ -425,6 +427,20 @@ __device__ __forceinline__ float warp_scan_push(const longlong2 *cells, int n_bi
     }
   }
   return run_lo;
+}
+
+// sabs: the sum of |G| over the strip's slots (for the range check of the fast screen).
+__device__ __forceinline__ float warp_scan_push(const longlong2 *cells, int n_bins, int64_t tg, int64_t th,
+                                                int64_t sabs, const SplitParams &sp, int f, int node, ScanShared &sh,
+                                                int &overflow) {
+  const longlong2 m = cells[n_bins];
+  const bool no_missing = (m.x == 0 && m.y == 0);
+  const float Gf2den = parent_f32(tg, th, sp);
+  const bool fast = strip_fast(sabs, th, Gf2den, sp);
+  // the common case (fast screen, no missing values) gets its own copy
+  if (fast && no_missing) return scan_push_impl<1, 0>(cells, n_bins, tg, th, m, Gf2den, sp, f, node, sh, overflow, 0);
+  return scan_push_impl<2, -1>(cells, n_bins, tg, th, m, Gf2den, sp, f, node, sh, overflow,
+                               fast ? 0 : (sp.filter ? 1 : 2));
 }
 
 __device__ __forceinline__ double surv_gain(int64_t gl, int64_t hl, int64_t tg, int64_t th, const SplitParams &sp) {
