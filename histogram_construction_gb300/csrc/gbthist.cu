@@ -762,7 +762,7 @@ gbt_status gbt_find_splits(gbt_ctx *c, const int64_t *hist, int32_t n_nodes, con
   const int nfb = (c->n_features + SCAN_WARPS - 1) / SCAN_WARPS;
   s = ensure(c, c->cand, (size_t)n_nodes * nfb * PUB_K * sizeof(Cand), "candidates");
   if (s != GBT_OK) return s;
-  s = ensure_counters(c, (size_t)2 * n_nodes);  // arrival counters, then threshold keys
+  s = ensure_counters(c, (size_t)n_nodes);  // arrival counters
   if (s != GBT_OK) return s;
   const SplitParams sp = make_sp(c, params);
   prof_begin(c);
@@ -932,7 +932,7 @@ gbt_status run_level_finish(gbt_ctx *c, const SmallSource &src, const int64_t *p
   const int nfb = (c->n_features + 3) / 4;
   s = ensure(c, c->cand, (size_t)2 * n_pairs * nfb * PUB_K * sizeof(Cand), "candidates");
   if (s != GBT_OK) return s;
-  s = ensure_counters(c, (size_t)3 * n_pairs);  // arrival counters, then two threshold keys per pair
+  s = ensure_counters(c, (size_t)n_pairs);  // arrival counters
   if (s != GBT_OK) return s;
   const SplitParams sp = make_sp(c, params);
   prof_begin(c);
@@ -1125,7 +1125,7 @@ int64_t gbt_kernel_launches(const gbt_ctx *c) { return c ? c->launches : 0; }
 namespace {
 constexpr int NOALLOC_MAX_NODES = 4096;    // nodes per call
 constexpr int NOALLOC_MAX_CANDS = 32768;   // nodes * ceil(n_features / 8) per call
-constexpr size_t NOALLOC_COUNTER_BYTES = (size_t)2 * NOALLOC_MAX_NODES * sizeof(uint32_t);  // counters + keys
+constexpr size_t NOALLOC_COUNTER_BYTES = (size_t)2 * NOALLOC_MAX_NODES * sizeof(uint32_t);  // counters (two words per node reserved)
 constexpr size_t NOALLOC_BYTES =
     NOALLOC_COUNTER_BYTES + (size_t)NOALLOC_MAX_CANDS * PUB_K * sizeof(Cand);  // 4 MiB + 32 KiB
 static_assert(NOALLOC_COUNTER_BYTES % 256 == 0, "candidate area alignment");
@@ -1173,7 +1173,7 @@ gbt_status gbt_find_splits_noalloc(const int64_t *hist, int32_t n_nodes, int32_t
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(cuda_stream);
   uint32_t *counters = static_cast<uint32_t *>(scratch);
   Cand *cand = reinterpret_cast<Cand *>(static_cast<unsigned char *>(scratch) + NOALLOC_COUNTER_BYTES);
-  // the arrival counters and threshold keys must start at zero whatever an earlier call left
+  // the arrival counters must start at zero whatever an earlier call left
   if (cudaMemsetAsync(counters, 0, (size_t)2 * n_nodes * sizeof(uint32_t), stream) != cudaSuccess) {
     cudaGetLastError();
     return GBT_ERR_CUDA;
