@@ -84,6 +84,8 @@ def lib():
         L.oracle_max_abs_q.restype = i64
         L.oracle_build_hist.argtypes = [p, ctypes.c_int, i64, i32, i32, ctypes.c_uint32, p, p, p, i32, p]
         L.oracle_build_hist.restype = ctypes.c_int
+        L.oracle_build_hist_multi.argtypes = [p, ctypes.c_int, i64, i32, i32, ctypes.c_uint32, p, i32, p, p, i32, p]
+        L.oracle_build_hist_multi.restype = ctypes.c_int
         L.oracle_subtract.argtypes = [p, p, p, p, i32, i32, i32]
         L.oracle_subtract.restype = ctypes.c_int
         L.oracle_gain.argtypes = [f64] * 8
@@ -134,6 +136,36 @@ def build_hist(bins: np.ndarray, n_bins: int, sentinel: int, q: np.ndarray, rows
     hist = np.empty((n_nodes, F, n_bins + 1, 2), dtype=np.int64)
     st = lib().oracle_build_hist(_ptr(bins), bins.dtype.itemsize, N, F, n_bins, sentinel, _ptr(q), _ptr(rows_a),
                                  _ptr(offs), n_nodes, _ptr(hist))
+    return hist, st
+
+
+def quantise_multi(gpair: np.ndarray, scales_g, scales_h):
+    """gpair float32 [N][k][2], one scale pair per target -> (q int32 [N][k][2], status): each target's pairs
+    quantised with its own scales."""
+    gp = np.ascontiguousarray(gpair, dtype=np.float32)
+    N, k, _ = gp.shape
+    q = np.empty((N, k, 2), dtype=np.int32)
+    st = OK
+    for t in range(k):
+        qt, s = quantise(gp[:, t, :], scales_g[t], scales_h[t])
+        q[:, t, :] = qt.reshape(N, 2)
+        st = st if st != OK else s
+    return q, st
+
+
+def build_hist_multi(bins: np.ndarray, n_bins: int, sentinel: int, q: np.ndarray, rows, node_offsets):
+    """Multi-output histograms: q int32 [N][k][2] -> (hist [k][n_nodes][F][n_bins+1][2] int64, status)."""
+    bins = np.ascontiguousarray(bins)
+    F, N = bins.shape
+    q = np.ascontiguousarray(q, dtype=np.int32)
+    assert q.ndim == 3 and q.shape[0] == N and q.shape[2] == 2
+    k = q.shape[1]
+    offs = np.ascontiguousarray(node_offsets, dtype=np.int64)
+    n_nodes = offs.shape[0] - 1
+    rows_a = None if rows is None else np.ascontiguousarray(rows, dtype=np.int32)
+    hist = np.empty((k, n_nodes, F, n_bins + 1, 2), dtype=np.int64)
+    st = lib().oracle_build_hist_multi(_ptr(bins), bins.dtype.itemsize, N, F, n_bins, sentinel, _ptr(q), k,
+                                       _ptr(rows_a), _ptr(offs), n_nodes, _ptr(hist))
     return hist, st
 
 

@@ -65,6 +65,12 @@
  *     at least one node; the sum starts from 0.0 and adds in node order; the
  *     order and tie-break are R3's. The reported sums are the candidate's
  *     left/right totals over all nodes.
+ *  R10 multi-output (vector-leaf) histograms [P5 "Summary", "Change": each
+ *     row carries k gradient pairs, one per target, and a bin read serves all
+ *     of them]: target t's histogram is R1-R2's histogram of the t-th pairs;
+ *     each target's pairs are quantised with that target's own scales. The
+ *     pages build vector-leaf cells as f64 chains; here, as for one target,
+ *     the cells are exact int64 sums of the quantised pairs (R1).
  */
 #include <stdint.h>
 #include <stddef.h>
@@ -165,6 +171,45 @@ int oracle_build_hist(const void *bins, int bin_bytes, int64_t n_rows, int32_t n
         if (s < 0) { st = OR_ERR_BIN; continue; }
         hn[((int64_t)f * B + s) * 2 + 0] += qg;
         hn[((int64_t)f * B + s) * 2 + 1] += qh;
+      }
+    }
+  }
+  return st;
+}
+
+/*
+ * Multi-output histograms (R10). q: quantised pairs [n_rows][k][2] (target t
+ * of row r at q[(r * k + t) * 2]). hist: out [k][n_nodes][n_features][n_bins
+ * + 1][2] int64, target-major, overwritten. For each node, rows in the given
+ * order, then features, then targets: add target t's (qg, qh) into the row's
+ * slot of feature f in target t's histogram.
+ */
+int oracle_build_hist_multi(const void *bins, int bin_bytes, int64_t n_rows, int32_t n_features, int32_t n_bins,
+                            uint32_t sentinel, const int32_t *q, int32_t k, const int32_t *rows,
+                            const int64_t *node_offsets, int32_t n_nodes, int64_t *hist) {
+  if (bin_bytes != 1 && bin_bytes != 2) return OR_ERR_ARG;
+  if (n_rows < 0 || n_features < 0 || n_nodes < 0 || n_bins < 1 || k < 1) return OR_ERR_ARG;
+  if (!node_offsets || (n_nodes > 0 && !hist)) return OR_ERR_ARG;
+  const int64_t B = (int64_t)n_bins + 1;
+  const int64_t per_node = (int64_t)n_features * B * 2;
+  const int64_t per_target = (int64_t)n_nodes * per_node;
+  for (int64_t i = 0; i < (int64_t)k * per_target; ++i) hist[i] = 0;
+  const uint8_t *b8 = (const uint8_t *)bins;
+  const uint16_t *b16 = (const uint16_t *)bins;
+  int st = OR_OK;
+  for (int32_t n = 0; n < n_nodes; ++n) {
+    for (int64_t j = node_offsets[n]; j < node_offsets[n + 1]; ++j) {
+      int64_t r = rows ? (int64_t)rows[j] : j;
+      if (r < 0 || r >= n_rows) { st = OR_ERR_ROW; continue; }
+      for (int32_t f = 0; f < n_features; ++f) {
+        uint32_t b = bin_bytes == 1 ? b8[(int64_t)f * n_rows + r] : b16[(int64_t)f * n_rows + r];
+        int64_t s = slot_of(b, n_bins, sentinel);
+        if (s < 0) { st = OR_ERR_BIN; continue; }
+        for (int32_t t = 0; t < k; ++t) {
+          int64_t *cell = hist + t * per_target + (int64_t)n * per_node + ((int64_t)f * B + s) * 2;
+          cell[0] += q[(r * k + t) * 2 + 0];
+          cell[1] += q[(r * k + t) * 2 + 1];
+        }
       }
     }
   }

@@ -445,3 +445,83 @@ def test_f64_find_on_integer_cells_equals_the_exact_path(oracle_mod):
             np.testing.assert_array_equal(a[k], b[k])
         np.testing.assert_array_equal(a["gain"], b["gain"])
         np.testing.assert_array_equal(a["g_left"].astype(np.float64), b["g_left"])
+
+
+# ----------------------------------------------------------------------------- multi-output histograms
+def _brute_hist_multi(bins, n_bins, sentinel, q, rows, offs):
+    """np.add.at over a flattened (feature, slot, target, component) index: the definition, another primitive."""
+    F, N = bins.shape
+    k = q.shape[1]
+    n_nodes = len(offs) - 1
+    out = np.zeros((n_nodes, F, n_bins + 1, k, 2), np.int64)
+    for n in range(n_nodes):
+        rr = np.arange(offs[n], offs[n + 1]) if rows is None else rows[offs[n]:offs[n + 1]]
+        b = bins[:, rr].astype(np.int64)
+        slot = np.where(b == sentinel, n_bins, b)  # [F][rows]
+        flat = out[n].reshape(-1)
+        for t in range(k):
+            for c in range(2):
+                idx = ((np.arange(F)[:, None] * (n_bins + 1) + slot) * k + t) * 2 + c
+                np.add.at(flat, idx.reshape(-1), np.broadcast_to(q[rr, t, c].astype(np.int64), slot.shape).reshape(-1))
+    return np.moveaxis(out, 3, 0)  # target-major [k][n][F][B][2]
+
+
+@pytest.mark.parametrize("width", [1, 2])
+@pytest.mark.parametrize("k", [1, 3, 5])
+def test_multi_build_matches_brute_force(oracle_mod, width, k):
+    rng = np.random.default_rng(300 + 10 * k + width)
+    N, F, n_bins = 80, 5, 9
+    sentinel = 0xFF if width == 1 else 0xFFFF
+    dt = np.uint8 if width == 1 else np.uint16
+    bins = rng.integers(0, n_bins, size=(F, N)).astype(dt)
+    bins[rng.random((F, N)) < 0.25] = sentinel
+    q = rng.integers(-5000, 5000, size=(N, k, 2)).astype(np.int32)
+    rows = rng.permutation(N).astype(np.int32)[:61]
+    offs = np.array([0, 9, 9, 40, 61], np.int64)  # an empty node
+    got, st = oracle_mod.build_hist_multi(bins, n_bins, sentinel, q, rows, offs)
+    assert st == oracle_mod.OK and got.shape == (k, 4, F, n_bins + 1, 2)
+    np.testing.assert_array_equal(got, _brute_hist_multi(bins, n_bins, sentinel, q, rows, offs))
+
+
+def test_multi_build_of_one_target_is_the_single_build(oracle_mod):
+    w = synth.make("level5", n_rows=4000, n_features=6, depth=2)
+    q, _ = oracle_mod.quantise(w.gpair, 1024.0, 1024.0)
+    lv = w.levels[2]
+    one, st = oracle_mod.build_hist(w.bins, w.n_bins, w.sentinel, q, lv.rows, lv.offsets)
+    multi, st2 = oracle_mod.build_hist_multi(w.bins, w.n_bins, w.sentinel, q.reshape(-1, 1, 2), lv.rows, lv.offsets)
+    assert st == st2 == oracle_mod.OK
+    np.testing.assert_array_equal(multi[0], one)
+
+
+def test_multi_build_targets_are_independent(oracle_mod):
+    """Permuting the targets permutes the histograms; a target of zeros has an all-zero histogram; per-feature
+    totals of every target equal that target's node sums."""
+    rng = np.random.default_rng(9)
+    N, F, n_bins, k = 300, 4, 16, 4
+    bins = rng.integers(0, n_bins, size=(F, N)).astype(np.uint8)
+    q = rng.integers(-100, 100, size=(N, k, 2)).astype(np.int32)
+    q[:, 2, :] = 0
+    offs = np.array([0, 120, 300], np.int64)
+    h, st = oracle_mod.build_hist_multi(bins, n_bins, 0xFF, q, None, offs)
+    assert st == oracle_mod.OK
+    perm = np.array([3, 0, 2, 1])
+    hp, _ = oracle_mod.build_hist_multi(bins, n_bins, 0xFF, q[:, perm, :], None, offs)
+    np.testing.assert_array_equal(hp, h[perm])
+    assert not h[2].any()
+    for t in range(k):
+        for n in range(2):
+            tot = q[offs[n]:offs[n + 1], t, :].astype(np.int64).sum(0)
+            np.testing.assert_array_equal(h[t, n].sum(axis=1), np.broadcast_to(tot, (F, 2)))
+
+
+def test_multi_quantise_uses_each_targets_scales(oracle_mod):
+    rng = np.random.default_rng(4)
+    gp = rng.standard_normal((50, 3, 2)).astype(np.float32)
+    sg, sh = [256.0, 1024.0, 4096.0], [512.0, 2048.0, 64.0]
+    q, st = oracle_mod.quantise_multi(gp, sg, sh)
+    assert st == oracle_mod.OK
+    for t in range(3):
+        exp_g = np.rint((gp[:, t, 0] * np.float32(sg[t])).astype(np.float32)).astype(np.int32)
+        exp_h = np.rint((gp[:, t, 1] * np.float32(sh[t])).astype(np.float32)).astype(np.int32)
+        np.testing.assert_array_equal(q[:, t, 0], exp_g)
+        np.testing.assert_array_equal(q[:, t, 1], exp_h)
