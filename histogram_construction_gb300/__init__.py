@@ -28,7 +28,7 @@ EXPORTS = [
     "gbt_level_step",
     "gbt_partition_level", "gbt_profile_enable", "gbt_profile_read", "gbt_slots_per_feature",
     "gbt_kernel_launches", "gbt_find_splits_noalloc", "gbt_find_level_split", "gbt_build_level_f64",
-    "gbt_subtract_siblings_f64", "gbt_find_splits_f64",
+    "gbt_subtract_siblings_f64", "gbt_find_splits_f64", "gbt_begin_tree_multi", "gbt_build_level_multi",
 ]
 
 
@@ -88,6 +88,8 @@ def lib(build_if_missing: bool = True):
         "gbt_find_splits_noalloc": (st, [vp, i32, i32, i32, f32, f32, ctypes.POINTER(GbtParams), vp, vp]),
         "gbt_find_level_split": (st, [vp, vp, i32, ctypes.POINTER(GbtParams), vp]),
         "gbt_build_level_f64": (st, [vp, vp, vp, vp, i32, vp]),
+        "gbt_begin_tree_multi": (st, [vp, vp, i32, vp, vp]),
+        "gbt_build_level_multi": (st, [vp, vp, vp, i32, vp]),
         "gbt_subtract_siblings_f64": (st, [vp, vp, vp, vp, vp, i32]),
         "gbt_find_splits_f64": (st, [vp, vp, i32, ctypes.POINTER(GbtParams), vp]),
     }
@@ -179,6 +181,17 @@ def gbt_subtract_siblings(ctx, parent_hist, parent_of, small_hist, large_hist, n
 
 def gbt_find_splits(ctx, hist, n_nodes, prm, out):
     return lib().gbt_find_splits(ctx, ptr(hist), int(n_nodes), ctypes.byref(prm), ptr(out))
+
+
+def gbt_begin_tree_multi(ctx, gpair, n_targets, scales_g, scales_h):
+    sg = (ctypes.c_float * int(n_targets))(*[float(x) for x in scales_g])
+    sh = (ctypes.c_float * int(n_targets))(*[float(x) for x in scales_h])
+    return lib().gbt_begin_tree_multi(ctx, ptr(gpair), int(n_targets), ctypes.cast(sg, ctypes.c_void_p),
+                                      ctypes.cast(sh, ctypes.c_void_p))
+
+
+def gbt_build_level_multi(ctx, rows, node_offsets, n_nodes, hist_out):
+    return lib().gbt_build_level_multi(ctx, ptr(rows), ptr(node_offsets), int(n_nodes), ptr(hist_out))
 
 
 def gbt_build_level_f64(ctx, gpair, rows, node_offsets, n_nodes, hist_out):

@@ -24,6 +24,7 @@ struct DevState {
   int64_t chunk_rows;  // rows per work item chunk (level plan)
   int32_t n_items;     // work items of the level
   int32_t chunks_per_group;  // consecutive chunks of a node whose int32 sum stays exact (level plan)
+  uint32_t qmax_multi;       // max |q| over the multi-output tree's pairs, all targets
 };
 
 constexpr int MIRROR_STRIP_BYTES = 64;  // bytes per row per mirror tile of features

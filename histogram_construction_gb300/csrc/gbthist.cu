@@ -90,9 +90,15 @@ struct gbt_ctx {
   uint32_t qmax = 0;             // max |q| of the current tree, known on the host after ev_q
   bool qmax_known = false;
   cudaEvent_t ev_q = nullptr;
+  // multi-output tree: k quantised pairs per row
+  Buf qm;
+  int32_t multi_k = 0;
+  uint32_t qmax_multi = 0;       // known on the host after ev_qm
+  bool qmax_multi_known = false;
+  cudaEvent_t ev_qm = nullptr;
   // state + scratch
   DevState *st = nullptr;
-  uint32_t *err_host = nullptr;  // pinned: [0] error word copy, [1] max |q| copy
+  uint32_t *err_host = nullptr;  // pinned: [0] error word copy, [1] max |q| copy, [2] multi-output max |q| copy
   Buf gp_stage, chunk_prefix, partial, rows_in, offs_in, cand, splits_a, splits_b, parent_of_in, tile_counts, lrank,
       slab, counters, level_scratch;
   std::string last_error;
@@ -309,6 +315,10 @@ bool set_hist_attributes() {
          cudaFuncSetAttribute(k_hist_u8<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               H8_SMEM + FL_STAGE_BYTES) == cudaSuccess &&
          cudaFuncSetAttribute(k_hist_u8<true>, cudaFuncAttributePreferredSharedMemoryCarveout, 100) == cudaSuccess &&
+         cudaFuncSetAttribute(k_hist_u8<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, H8_SMEM) ==
+             cudaSuccess &&
+         cudaFuncSetAttribute(k_hist_u8<false, true>, cudaFuncAttributePreferredSharedMemoryCarveout, 100) ==
+             cudaSuccess &&
          cudaFuncSetAttribute(k_hist_u16<2, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, u16_int) == cudaSuccess &&
          cudaFuncSetAttribute(k_hist_u16<4, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, u16_int) == cudaSuccess &&
          cudaFuncSetAttribute(k_hist_u16<8, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, u16_int) == cudaSuccess &&
@@ -347,14 +357,16 @@ gbt_status gbt_create(int device, void *cuda_stream, gbt_ctx **out) {
   }
   c->st = reinterpret_cast<DevState *>(st);
   cudaMemsetAsync(c->st, 0, sizeof(DevState), c->stream);
-  if (alloc_should_fail() || cudaMallocHost(&c->err_host, 2 * sizeof(uint32_t)) != cudaSuccess) {
+  if (alloc_should_fail() || cudaMallocHost(&c->err_host, 3 * sizeof(uint32_t)) != cudaSuccess) {
     cudaFreeAsync(c->st, c->stream);
     cudaStreamSynchronize(c->stream);
     delete c;
     return GBT_ERR_OOM;
   }
-  c->err_host[0] = c->err_host[1] = 0;
-  if (cudaEventCreateWithFlags(&c->ev_q, cudaEventDisableTiming) != cudaSuccess) {
+  c->err_host[0] = c->err_host[1] = c->err_host[2] = 0;
+  if (cudaEventCreateWithFlags(&c->ev_q, cudaEventDisableTiming) != cudaSuccess ||
+      cudaEventCreateWithFlags(&c->ev_qm, cudaEventDisableTiming) != cudaSuccess) {
+    if (c->ev_q) cudaEventDestroy(c->ev_q);
     cudaFreeHost(c->err_host);
     cudaFreeAsync(c->st, c->stream);
     cudaStreamSynchronize(c->stream);
@@ -364,6 +376,7 @@ gbt_status gbt_create(int device, void *cuda_stream, gbt_ctx **out) {
   if (!set_hist_attributes()) {
     cudaGetLastError();
     cudaEventDestroy(c->ev_q);
+    cudaEventDestroy(c->ev_qm);
     cudaFreeHost(c->err_host);
     cudaFreeAsync(c->st, c->stream);
     cudaStreamSynchronize(c->stream);
@@ -380,12 +393,13 @@ gbt_status gbt_destroy(gbt_ctx *c) {
   cudaStreamSynchronize(c->stream);
   Buf *bufs[] = {&c->mirror, &c->q, &c->gp_stage, &c->chunk_prefix, &c->partial, &c->rows_in, &c->offs_in,
                  &c->cand, &c->splits_a, &c->splits_b, &c->parent_of_in, &c->tile_counts, &c->lrank, &c->slab,
-                 &c->counters, &c->level_scratch};
+                 &c->counters, &c->level_scratch, &c->qm};
   for (Buf *b : bufs) release(c, *b);
   if (c->st) cudaFreeAsync(c->st, c->stream);
   cudaStreamSynchronize(c->stream);
   if (c->err_host) cudaFreeHost(c->err_host);
   if (c->ev_q) cudaEventDestroy(c->ev_q);
+  if (c->ev_qm) cudaEventDestroy(c->ev_qm);
   for (auto &r : c->prof_pending) {
     cudaEventDestroy(r.a);
     cudaEventDestroy(r.b);
@@ -517,6 +531,44 @@ gbt_status gbt_begin_tree(gbt_ctx *c, const float *gpair, float scale_g, float s
   return GBT_OK;
 }
 
+gbt_status gbt_begin_tree_multi(gbt_ctx *c, const float *gpair, int32_t n_targets, const float *scales_g,
+                                const float *scales_h) {
+  gbt_status s = check_ctx(c);
+  if (s != GBT_OK) return s;
+  if (c->n_rows == 0) return fail(c, GBT_ERR_STATE, "gbt_upload_bins first");
+  if (n_targets < 1 || n_targets > MULTI_MAX_TARGETS)
+    return fail(c, GBT_ERR_UNSUPPORTED, "n_targets must be in [1, 16]");
+  if (!gpair || !scales_g || !scales_h) return fail(c, GBT_ERR_INVALID_ARG, "gpair and scales are required");
+  MultiScales sc{};
+  sc.k = n_targets;
+  for (int t = 0; t < n_targets; ++t) {
+    const float g = scales_g[t], h = scales_h[t];
+    if (!(g > 0.f) || !(h > 0.f) || !isfinite(g) || !isfinite(h))
+      return fail(c, GBT_ERR_INVALID_ARG, "scales must be finite and > 0");
+    sc.g[t] = g;
+    sc.h[t] = h;
+  }
+  const int64_t n = (int64_t)c->n_rows * n_targets;
+  s = ensure(c, c->qm, (size_t)n * sizeof(int2), "quantised multi-output gpair");
+  if (s != GBT_OK) return s;
+  const void *gp = nullptr;
+  s = device_view(c, gpair, (size_t)n * 2 * sizeof(float), c->gp_stage, &gp, "gpair");
+  if (s != GBT_OK) return s;
+  if ((reinterpret_cast<uintptr_t>(gp) & 7u) != 0) return fail(c, GBT_ERR_INVALID_ARG, "gpair must be 8-byte aligned");
+  CUDA_TRY(c, cudaMemsetAsync(&c->st->qmax_multi, 0, sizeof(uint32_t), c->stream), "reset multi-output qmax");
+  prof_begin(c);
+  k_quantise_multi<<<grid_for(c, n, 1024, 2), 1024, 0, c->stream>>>((const float2 *)gp, n, sc, (int2 *)c->qm.p,
+                                                                    c->st);
+  LAUNCH_CHECK(c, "k_quantise_multi");
+  CUDA_TRY(c, cudaMemcpyAsync(&c->err_host[2], &c->st->qmax_multi, sizeof(uint32_t), cudaMemcpyDeviceToHost,
+                              c->stream),
+           "read multi-output max|q|");
+  CUDA_TRY(c, cudaEventRecord(c->ev_qm, c->stream), "record multi-output max|q| event");
+  c->qmax_multi_known = false;
+  c->multi_k = n_targets;
+  return GBT_OK;
+}
+
 gbt_status gbt_suggest_scales(int64_t rows_per_partial, float max_abs_g, float max_abs_h, float *sg, float *sh) {
   if (!sg || !sh) return GBT_ERR_INVALID_ARG;
   if (!(max_abs_g >= 0.f) || !(max_abs_h >= 0.f) || !isfinite(max_abs_g) || !isfinite(max_abs_h))
@@ -548,7 +600,7 @@ namespace {
 // sums of the quantised pairs, or, when gpair_f64 (device float (g, h) pairs)
 // is given, double sums of those pairs.
 gbt_status run_level_build(gbt_ctx *c, const int32_t *rows, const int64_t *node_offsets, int32_t n_nodes,
-                           LevelParams *out_lp, const float2 *gpair_f64 = nullptr) {
+                           LevelParams *out_lp, const float2 *gpair_f64 = nullptr, bool multi = false) {
   const int B = c->n_bins + 1;
   const void *offs_d = nullptr;
   int64_t R_host = -1;
@@ -576,35 +628,44 @@ gbt_status run_level_build(gbt_ctx *c, const int32_t *rows, const int64_t *node_
   s = ensure(c, c->chunk_prefix, (size_t)2 * (n_nodes + 1) * sizeof(int32_t), "chunk and group prefixes");
   if (s != GBT_OK) return s;
   const bool f64 = gpair_f64 != nullptr;
-  if (!f64 && !c->qmax_known) {
+  if (multi) {
+    if (!c->qmax_multi_known) {
+      CUDA_TRY(c, cudaEventSynchronize(c->ev_qm), "wait for the multi-output max|q|");
+      c->qmax_multi = c->err_host[2];
+      c->qmax_multi_known = true;
+    }
+  } else if (!f64 && !c->qmax_known) {
     CUDA_TRY(c, cudaEventSynchronize(c->ev_q), "wait for max|q|");
     c->qmax = c->err_host[1];
     c->qmax_known = true;
   }
+  const int K = multi ? c->multi_k : 1;
 
   LevelParams lp;
   lp.rows = (const int32_t *)rows_d;
   lp.offs = (const int64_t *)offs_d;
   lp.n_nodes = n_nodes;
-  lp.item_feats = c->bin_bytes == 1 ? 64 : c->ts16;
-  lp.n_fgroups = (c->n_features + lp.item_feats - 1) / lp.item_feats;
+  lp.item_feats = multi ? 16 : (c->bin_bytes == 1 ? 64 : c->ts16);
+  // multi-output: an item is a 16-feature quarter and a group of up to four targets
+  lp.n_fgroups = (c->n_features + lp.item_feats - 1) / lp.item_feats * (multi ? (K + 3) / 4 : 1);
   lp.target_items = c->target_items > 0 ? c->target_items : c->n_sm * 2;
   lp.n_rows = c->n_rows;
-  lp.q = f64 ? (const int2 *)gpair_f64 : (const int2 *)c->q.p;  // float cells: the float bit patterns
+  lp.q = f64 ? (const int2 *)gpair_f64 : (multi ? (const int2 *)c->qm.p : (const int2 *)c->q.p);
   lp.chunk_prefix = (int32_t *)c->chunk_prefix.p;
   lp.group_prefix = lp.chunk_prefix + (n_nodes + 1);
   lp.sbw = c->bin_bytes == 1 ? 16 : c->ts16;
   lp.nsb = c->bin_bytes == 1 ? H8_SB : 1;
   // nsb x B x sbw (G, H) pairs: int32 pairs (8 bytes), or double pairs (16 bytes) for float cells
   lp.image_int4s = f64 ? (int64_t)lp.nsb * lp.sbw * B : (int64_t)lp.nsb * lp.sbw * B / 2;
-  lp.qmax_plan = f64 ? 1u : 0u;             // float cells: all chunks of a node merge into one double image
+  // float cells: all chunks of a node merge into one double image; multi-output: the bound of its own pairs
+  lp.qmax_plan = f64 ? 1u : (multi ? std::max(c->qmax_multi, 1u) : 0u);
   lp.chunk_cap = f64 ? FL_CHUNK_CAP : 0;    // ... and each chunk's float sums cover at most 32k rows
   lp.st = c->st;
   // image scratch for the largest item count the device plan can produce
   // (there are never more group images than items):
   // items <= n_fgroups * n_nodes + max(target_items, n_fgroups * n_rows / rows_per_chunk_min)
   // (a chunk holds at least min(rc, load-balance target) rows, and rc >= 1024 by the quantisation limit)
-  int64_t rc = std::max<int64_t>(1, 2147483647LL / std::max<int64_t>(f64 ? 1 : c->qmax, 1));
+  int64_t rc = std::max<int64_t>(1, 2147483647LL / std::max<int64_t>(f64 ? 1 : (multi ? c->qmax_multi : c->qmax), 1));
   if (lp.chunk_cap > 0) rc = std::min<int64_t>(rc, lp.chunk_cap);  // the largest chunk the plan can form
   const int64_t items_max = (int64_t)lp.n_fgroups * (n_nodes + 1) +
                             std::max<int64_t>(lp.target_items, (int64_t)lp.n_fgroups * ((c->n_rows + rc - 1) / rc));
@@ -623,8 +684,12 @@ gbt_status run_level_build(gbt_ctx *c, const int32_t *rows, const int64_t *node_
     hp.mirror = (const uint8_t *)c->mirror.p;
     hp.n_features = c->n_features;
     hp.n_slots = B;
+    hp.n_targets = K;
     prof_begin(c);
-    if (f64) {
+    if (multi) {
+      launch_pdl(c, k_hist_u8<false, true>, dim3(hist_ctas), dim3(H8_THREADS), H8_SMEM, hp);
+      LAUNCH_CHECK(c, "k_hist_u8_multi");
+    } else if (f64) {
       launch_pdl(c, k_hist_u8<true>, dim3(hist_ctas), dim3(H8_THREADS), H8_SMEM + FL_STAGE_BYTES, hp);
       LAUNCH_CHECK(c, "k_hist_u8_f32");
     } else {
@@ -772,6 +837,29 @@ gbt_status gbt_find_splits(gbt_ctx *c, const int64_t *hist, int32_t n_nodes, con
   if (host)
     CUDA_TRY(c, cudaMemcpyAsync(out, dout, (size_t)n_nodes * sizeof(gbt_split), cudaMemcpyDeviceToHost, c->stream),
              "splits to host");
+  return GBT_OK;
+}
+
+gbt_status gbt_build_level_multi(gbt_ctx *c, const int32_t *rows, const int64_t *node_offsets, int32_t n_nodes,
+                                 int64_t *hist_out) {
+  gbt_status s = check_ctx(c);
+  if (s != GBT_OK) return s;
+  if (c->multi_k == 0) return fail(c, GBT_ERR_STATE, "gbt_begin_tree_multi first");
+  if (c->bin_bytes != 1) return fail(c, GBT_ERR_UNSUPPORTED, "multi-output histograms need u8 bins");
+  if (n_nodes < 0 || n_nodes > 65535) return fail(c, GBT_ERR_UNSUPPORTED, "n_nodes must be in [0, 65535]");
+  if (!node_offsets || !hist_out) return fail(c, GBT_ERR_INVALID_ARG, "node_offsets and hist_out are required");
+  if (ptr_kind(hist_out) != 1 || !aligned16(hist_out))
+    return fail(c, GBT_ERR_INVALID_ARG, "hist_out must be 16-byte aligned device memory");
+  if (n_nodes == 0) return GBT_OK;
+  LevelParams lp;
+  s = run_level_build(c, rows, node_offsets, n_nodes, &lp, nullptr, true);
+  if (s != GBT_OK) return s;
+  const int B = c->n_bins + 1;
+  const int64_t cells = (int64_t)c->multi_k * n_nodes * ((c->n_features + 3) / 4) * 4 * B;
+  prof_begin(c);
+  launch_pdl(c, k_finalize_multi, dim3(grid_for(c, cells, 256, 8)), dim3(256), 0, partial_view(lp, B), c->multi_k,
+             n_nodes, c->n_features, hist_out, (const DevState *)c->st);
+  LAUNCH_CHECK(c, "k_finalize_multi");
   return GBT_OK;
 }
 

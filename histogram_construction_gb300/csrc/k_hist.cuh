@@ -299,6 +299,7 @@ struct Hist8Params {
   const uint8_t *mirror;  // tile pairs [ceil(n_tiles / 2)][N][128]
   int32_t n_features;
   int32_t n_slots;        // B
+  int32_t n_targets;      // multi-output: k pairs per row in lv.q ([N][k]); 1 otherwise
 };
 
 // Gathered operands of U row groups of one lane.
@@ -318,16 +319,22 @@ __device__ __forceinline__ void h8_rows(const LevelParams &p, bool ident, int64_
   }
 }
 
-template <int U>
+// q of row r: lv.q[r] (one target), or target tsel of lv.q[r][k] (multi-output;
+// lanes of targets past k load nothing, lane_on false).
+template <int U, bool MULTI>
 __device__ __forceinline__ void h8_gather(const LevelParams &p, const unsigned char *strip, bool lane_on, int par,
-                                          const int32_t (&rid)[U], H8Stage<U> &st, uint32_t &bad) {
+                                          const int32_t (&rid)[U], H8Stage<U> &st, uint32_t &bad, int k, int tsel) {
 #pragma unroll
   for (int u = 0; u < U; ++u) {
     const int32_t r = rid[u];
     const bool valid = (uint32_t)r < (uint32_t)p.n_rows;
     bad |= (r >= 0 && !valid) ? 1u : 0u;
     int2 qv = make_int2(0, 0);
-    if (valid) qv = __ldg(p.q + r);
+    if (MULTI) {
+      if (valid && lane_on) qv = __ldg(p.q + (int64_t)r * k + tsel);
+    } else if (valid) {
+      qv = __ldg(p.q + r);
+    }
     st.bw[u] = (valid && lane_on) ? ldg_nc_v4(strip + (int64_t)r * MIRROR_ROW_BYTES) : make_uint4(0, 0, 0, 0);
     st.v0[u] = (uint32_t)(par ? qv.y : qv.x);
     st.v1[u] = (uint32_t)(par ? qv.x : qv.y);
@@ -362,7 +369,13 @@ __device__ __forceinline__ void h8_scatter(const H8Stage<U> &st, const uint32_t 
 }
 
 // FLT: float cells (p.q holds the float (g, h) bit patterns; images are double).
-template <bool FLT>
+// MULTI: multi-output (vector-leaf) histograms [hessboost PR #163 "Summary":
+// a bin read serves every target's gradients]. An item is one 16-feature
+// quarter of a mirror tile and up to four targets: sub-block w holds target
+// 4 tg + w, lane quarter w loads that target's pair, and all four lanes of a
+// row read the same 16-byte quarter. The bank map is the same (the sub-block
+// is the target instead of the feature quarter).
+template <bool FLT, bool MULTI = false>
 __global__ void __launch_bounds__(H8_THREADS, 1) k_hist_u8(Hist8Params P) {
   constexpr int U = H8_U;
   extern __shared__ __align__(128) unsigned char smem[];
@@ -402,17 +415,26 @@ __global__ void __launch_bounds__(H8_THREADS, 1) k_hist_u8(Hist8Params P) {
     const int32_t id = s_item;
     if (id >= n_items) break;
     const Item it = s_it;
-    const int f_tile0 = it.fgroup * 64;
-    const int nsb = min(H8_SB, (P.n_features - f_tile0 + 15) >> 4);
+    int nsb, tsel = 0;
+    const unsigned char *strip;
+    if (MULTI) {
+      const int nfq = (P.n_features + 15) >> 4;  // feature quarters
+      const int tg = it.fgroup / nfq, fq = it.fgroup - tg * nfq;
+      nsb = min(H8_SB, P.n_targets - 4 * tg);  // targets of this item
+      tsel = 4 * tg + w;
+      strip = P.mirror + mirror_offset(fq >> 2, 0, N) + (fq & 3) * 16;
+    } else {
+      nsb = min(H8_SB, (P.n_features - it.fgroup * 64 + 15) >> 4);
+      strip = P.mirror + mirror_offset(it.fgroup, 0, N) + w * 16;
+    }
     const bool lane_on = w < nsb;
-    const unsigned char *strip = P.mirror + mirror_offset(it.fgroup, 0, N) + w * 16;
     const int64_t step = (int64_t)8 * nwarps;  // rows between a warp's consecutive groups
     const int64_t adv = step * U;              // rows per warp step
     int64_t g0 = it.k0 + 8 * warp + rho;
     int32_t rid[U];
     H8Stage<U> cur, nxt;
     h8_rows<U>(p, ident, g0, step, it.k1, rid);
-    h8_gather<U>(p, strip, lane_on, par, rid, cur, bad);
+    h8_gather<U, MULTI>(p, strip, lane_on, par, rid, cur, bad, P.n_targets, tsel);
     h8_rows<U>(p, ident, g0 + adv, step, it.k1, rid);
     // with the first gathers in flight: the previous item's flush must have
     // read the image before it is zeroed; zero the slot rows that will be read
@@ -429,7 +451,7 @@ __global__ void __launch_bounds__(H8_THREADS, 1) k_hist_u8(Hist8Params P) {
     // lane with work keeps the warp going (the others add zeros)
     while (__any_sync(0xffffffffu, g0 < it.k1)) {
       if (__any_sync(0xffffffffu, g0 + adv < it.k1)) {
-        h8_gather<U>(p, strip, lane_on, par, rid, nxt, bad);
+        h8_gather<U, MULTI>(p, strip, lane_on, par, rid, nxt, bad, P.n_targets, tsel);
         h8_rows<U>(p, ident, g0 + 2 * adv, step, it.k1, rid);
       }
       h8_scatter<U, FLT>(cur, sel, cj);
@@ -667,6 +689,48 @@ __global__ void __launch_bounds__(256) k_finalize(PartialView v, int32_t n_nodes
       h += x.y;
     }
     reinterpret_cast<longlong2 *>(hist_out)[((int64_t)n * n_features + f) * v.B + s] = make_longlong2(g, h);
+  }
+}
+
+// Multi-output finalize: hist_out [k][n][F][B][2] int64, target-major, from the
+// group images of the MULTI build (feature group = target group * nfq +
+// feature quarter; sub-block = target within its group of four; column = the
+// feature within its quarter). One thread per cell; four consecutive threads
+// take four consecutive features of one slot (one 32-byte sector of an image
+// row).
+__global__ void __launch_bounds__(256) k_finalize_multi(PartialView v, int32_t n_targets, int32_t n_nodes,
+                                                        int32_t n_features, int64_t *__restrict__ hist_out,
+                                                        const DevState *st) {
+  pdl_wait();  // the histogram kernel
+  if (!st->plan_ok) return;
+  const int nq = (n_features + 3) >> 2;
+  const int nfq = (n_features + 15) >> 4;
+  const int64_t units = (int64_t)n_targets * n_nodes * nq * v.B * 4;
+  const int64_t image_stride = v.n_fgroups * v.image_int4s * 2;  // int2 between a node's group images
+  for (int64_t u = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; u < units; u += (int64_t)gridDim.x * blockDim.x) {
+    const int fi = (int)(u & 3);
+    int64_t r = u >> 2;
+    const int s = (int)(r % v.B);
+    r /= v.B;
+    const int qd = (int)(r % nq);
+    r /= nq;
+    const int n = (int)(r % n_nodes);
+    const int t = (int)(r / n_nodes);
+    const int f = qd * 4 + fi;
+    if (f >= n_features) continue;
+    const int fq = f >> 4, fl = f & 15, tg = t >> 2, tl = t & 3;
+    const int32_t g0 = v.group_prefix[n], g1 = v.group_prefix[n + 1];
+    const int64_t image = (int64_t)g0 * v.n_fgroups + (int64_t)tg * nfq + fq;
+    const int2 *cell = reinterpret_cast<const int2 *>(v.partial) + image * v.image_int4s * 2 +
+                       ((int64_t)tl * v.B + s) * 16 + fl;
+    int64_t g = 0, h = 0;
+    for (int32_t k = g0; k < g1; ++k, cell += image_stride) {
+      const int2 x = __ldcg(cell);
+      g += x.x;
+      h += x.y;
+    }
+    reinterpret_cast<longlong2 *>(hist_out)[(((int64_t)t * n_nodes + n) * n_features + f) * v.B + s] =
+        make_longlong2(g, h);
   }
 }
 

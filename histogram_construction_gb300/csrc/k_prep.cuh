@@ -64,33 +64,32 @@ constexpr int QMAX = (1 << 21) - 1;
 // "GBDT engine engineering deep-dive" (ybb.press), section 7: gradients are
 // quantised to fixed point before integer atomics; bonsai "9. Parallelism &
 // determinism", "The idea": int64 cells are exact in any order.
-// Also reduces max |q| into st->qmax (zeroed by the caller).
-__global__ void __launch_bounds__(1024) k_quantise(const float2 *__restrict__ gp, int64_t n, float sg, float sh,
-                                                  int2 *__restrict__ q, DevState *st) {
-  uint32_t mx = 0, bad = 0;
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
-    const float2 v = gp[i];
-    const float pg = __fmul_rn(v.x, sg);
-    const float ph = __fmul_rn(v.y, sh);
-    int qg = 0, qh = 0;
-    if (fabsf(pg) < 2097152.0f) {
-      const int t = __float2int_rn(pg);
-      if (t >= -QMAX && t <= QMAX) qg = t; else bad = 1;
-    } else {
-      bad = 1;
-    }
-    if (fabsf(ph) < 2097152.0f) {
-      const int t = __float2int_rn(ph);
-      if (t >= -QMAX && t <= QMAX) qh = t; else bad = 1;
-    } else {
-      bad = 1;
-    }
-    q[i] = make_int2(qg, qh);
-    const uint32_t ag = qg < 0 ? (uint32_t)(-(int64_t)qg) : (uint32_t)qg;
-    const uint32_t ah = qh < 0 ? (uint32_t)(-(int64_t)qh) : (uint32_t)qh;
-    mx = max(mx, max(ag, ah));
+// One (g, h) pair -> (qg, qh); accumulates max |q| and the overflow flag.
+__device__ __forceinline__ int2 quantise_pair(float2 v, float sg, float sh, uint32_t &mx, uint32_t &bad) {
+  const float pg = __fmul_rn(v.x, sg);
+  const float ph = __fmul_rn(v.y, sh);
+  int qg = 0, qh = 0;
+  if (fabsf(pg) < 2097152.0f) {
+    const int t = __float2int_rn(pg);
+    if (t >= -QMAX && t <= QMAX) qg = t; else bad = 1;
+  } else {
+    bad = 1;
   }
-  // one atomic per block: same-address atomics serialise in L2
+  if (fabsf(ph) < 2097152.0f) {
+    const int t = __float2int_rn(ph);
+    if (t >= -QMAX && t <= QMAX) qh = t; else bad = 1;
+  } else {
+    bad = 1;
+  }
+  const uint32_t ag = qg < 0 ? (uint32_t)(-(int64_t)qg) : (uint32_t)qg;
+  const uint32_t ah = qh < 0 ? (uint32_t)(-(int64_t)qh) : (uint32_t)qh;
+  mx = max(mx, max(ag, ah));
+  return make_int2(qg, qh);
+}
+
+// Block reduction of max |q| into *dst (one atomic per block: same-address
+// atomics serialise in L2) and of the overflow flag into the error word.
+__device__ __forceinline__ void block_qmax(uint32_t mx, uint32_t bad, uint32_t *dst, DevState *st) {
   __shared__ uint32_t s_mx[32];
   __shared__ uint32_t s_bad;
   if (threadIdx.x == 0) s_bad = 0;
@@ -102,9 +101,38 @@ __global__ void __launch_bounds__(1024) k_quantise(const float2 *__restrict__ gp
   if (threadIdx.x == 0) {
     uint32_t m = 0;
     for (int w = 0; w < (int)(blockDim.x >> 5); ++w) m = max(m, s_mx[w]);
-    if (m) atomicMax(&st->qmax, m);
+    if (m) atomicMax(dst, m);
     if (s_bad) raise_err(st, ERRBIT_QUANT);
   }
+}
+
+// Reduces max |q| into st->qmax (zeroed by the caller).
+__global__ void __launch_bounds__(1024) k_quantise(const float2 *__restrict__ gp, int64_t n, float sg, float sh,
+                                                  int2 *__restrict__ q, DevState *st) {
+  uint32_t mx = 0, bad = 0;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
+    q[i] = quantise_pair(gp[i], sg, sh, mx, bad);
+  block_qmax(mx, bad, &st->qmax, st);
+}
+
+// Multi-output gradients [hessboost PR #163 "Change": vector-leaf nodes carry
+// one (g, h) per target]: pairs [n_rows][k], target i % k of element i
+// quantised with that target's scales; max |q| over all targets into
+// st->qmax_multi.
+constexpr int MULTI_MAX_TARGETS = 16;
+struct MultiScales {
+  float g[MULTI_MAX_TARGETS], h[MULTI_MAX_TARGETS];
+  int32_t k;
+};
+
+__global__ void __launch_bounds__(1024) k_quantise_multi(const float2 *__restrict__ gp, int64_t n, MultiScales sc,
+                                                        int2 *__restrict__ q, DevState *st) {
+  uint32_t mx = 0, bad = 0;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+    const int t = (int)(i % sc.k);
+    q[i] = quantise_pair(gp[i], sc.g[t], sc.h[t], mx, bad);
+  }
+  block_qmax(mx, bad, &st->qmax_multi, st);
 }
 
 }  // namespace gbt

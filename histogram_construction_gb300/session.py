@@ -8,7 +8,8 @@ from __future__ import annotations
 
 import numpy as np
 
-from . import (GBT_OK, SPLIT_BYTES, check, gbt_begin_tree, gbt_build_level, gbt_build_level_f64, gbt_create,
+from . import (GBT_OK, SPLIT_BYTES, check, gbt_begin_tree, gbt_begin_tree_multi, gbt_build_level,
+               gbt_build_level_f64, gbt_build_level_multi, gbt_create,
                gbt_destroy, gbt_find_level_split, gbt_find_splits, gbt_find_splits_f64, gbt_kernel_launches,
                gbt_level_step, gbt_partition_level, gbt_subtract_and_find, gbt_subtract_siblings,
                gbt_subtract_siblings_f64, gbt_sync, gbt_upload_bins, lib, params)
@@ -137,6 +138,30 @@ class Session:
         out = self.torch.empty((1, SPLIT_BYTES), dtype=self.torch.uint8, device=self.device)
         self.check(gbt_find_level_split(self.ctx, hist, hist.shape[0], params(lam, gamma, mcw), out))
         return out
+
+    # ------------------------------------------------------- multi-output (vector-leaf) trees
+    def begin_tree_multi(self, gpair, scales_g, scales_h):
+        """gpair: [N][k][2] float32 (numpy host or torch host/device); one scale pair per target."""
+        k = int(len(scales_g))
+        if isinstance(gpair, np.ndarray):
+            arr = np.ascontiguousarray(gpair, dtype=np.float32)
+            self.check(gbt_begin_tree_multi(self.ctx, arr, k, scales_g, scales_h))
+            self.check(self.sync())
+        else:
+            self.check(gbt_begin_tree_multi(self.ctx, gpair.contiguous(), k, scales_g, scales_h))
+        self.n_targets = k
+        return self
+
+    def build_level_multi(self, rows, offsets, hist=None):
+        """Every target's histogram of the level's nodes: [k][n][F][B][2] int64."""
+        n_nodes = int(len(offsets) - 1)
+        if hist is None:
+            hist = self.torch.empty((self.n_targets, n_nodes, self.n_features, self.n_bins + 1, 2),
+                                    dtype=self.torch.int64, device=self.device)
+        r = self.to_dev(rows, self.torch.int32)
+        o = self.to_dev(offsets, self.torch.int64)
+        self.check(gbt_build_level_multi(self.ctx, r, o, n_nodes, hist))
+        return hist
 
     # ------------------------------------------------------- float-cell mode
     def build_level_f64(self, gpair, rows, offsets, hist=None):

@@ -170,6 +170,28 @@ gbt_status gbt_subtract_siblings(gbt_ctx *ctx, const int64_t *parent_hist, const
 gbt_status gbt_find_splits(gbt_ctx *ctx, const int64_t *hist, int32_t n_nodes, const gbt_params *params,
                            gbt_split *out);
 
+/* Multi-output (vector-leaf) trees [hessboost PR #163 "perf(multi): sweep
+ * vector-leaf histograms by feature on sparse indexes", "Summary" and
+ * "Change": each row carries one (g, h) per target and a bin read serves all
+ * of them]. Quantises the k pairs of every row, target t with its own scales:
+ * q = round-half-even(fl32(x * scale)), |q| <= 2^21 - 1 (else
+ * GBT_ERR_QUANT_OVERFLOW at gbt_sync), as gbt_begin_tree does for one target.
+ *   gpair: host or device float32 [n_rows][n_targets][2], read during the call's
+ *   stream work. scales_g, scales_h: host float [n_targets], finite and > 0.
+ *   n_targets: 1 .. 16 (else GBT_ERR_UNSUPPORTED). Independent of gbt_begin_tree. */
+gbt_status gbt_begin_tree_multi(gbt_ctx *ctx, const float *gpair, int32_t n_targets, const float *scales_g,
+                                const float *scales_h);
+
+/* Histograms of every target for the nodes of one level, in one pass over the
+ * bins: hist_out[t] is exactly gbt_build_level's histogram of target t's
+ * quantised pairs (int64 (G, H) cells, bit-identical in any order).
+ *   rows, node_offsets: as gbt_build_level. hist_out: device, 16-byte aligned,
+ *   [n_targets][n_nodes][n_features][n_bins + 1][2] int64, target-major, so each
+ *   target's block is a histogram that gbt_subtract_siblings and
+ *   gbt_find_splits accept. u8 bins only (else GBT_ERR_UNSUPPORTED). */
+gbt_status gbt_build_level_multi(gbt_ctx *ctx, const int32_t *rows, const int64_t *node_offsets, int32_t n_nodes,
+                                 int64_t *hist_out);
+
 /* Float-cell mode [bonsai "10: CUDA histogram backend", "The kernel": float
  * shared-memory cells merged into double global cells; "GBDT engine
  * engineering deep-dive", section 7 listing; section 3: the hessian is

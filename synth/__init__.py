@@ -109,6 +109,11 @@ def gpair(rng, n_rows, h="u0.1"):
     return out
 
 
+def gpair_multi(name: str, n_rows, k, h="u0.1"):
+    """k targets' pairs [N][k][2] float32: target t drawn like `gpair` from its own seeded stream."""
+    return np.stack([gpair(rng_for(name, 100 + t), n_rows, h) for t in range(k)], axis=1)
+
+
 # ----------------------------------------------------------------------------- node structure
 def geometric_partition_ids(rng, n_rows, n_nodes=8, lo=0.05, hi=0.5):
     """Node id of every row for n_nodes nodes with sizes proportional to hi * r^i, r = (lo/hi)^(1/(n-1))."""
