@@ -402,6 +402,56 @@ def run_gpu(args, rank, world, local_rank):
                    "note": "same level in double cells of the unquantised float32 gpair"}
             del hp64, hs64, large64
 
+        # ---------------------------------------------------------------- multi-output level (optional)
+        multi = None
+        if args.multi > 0 and w.width == 1:
+            k = args.multi
+            gpm = synth.gpair_multi(args.workload, w.n_rows, k)
+            msg, msh = [], []
+            for t in range(k):
+                _, a_, b_ = g.gbt_suggest_scales(0, float(np.abs(gpm[:, t, 0]).max()), float(np.abs(gpm[:, t, 1]).max()))
+                msg.append(a_)
+                msh.append(b_)
+            sess.begin_tree_multi(torch.from_numpy(gpm).to(dev), msg, msh)
+            m_rows = rows_d if lv.depth > 0 else None
+            m_offs = offs_d
+            hm = torch.empty((k, n_b, w.n_features, B, 2), dtype=torch.int64, device=dev)
+
+            def step_multi():
+                sess.check(g.gbt_build_level_multi(ctx, m_rows, m_offs, n_b, hm))
+
+            for i in range(3):
+                flush(i)
+                step_multi()
+            assert sess.sync() == 0
+            m_ms = []
+            g.gbt_profile_enable(ctx, True)
+            g.gbt_profile_read(ctx)
+            for i in range(args.steps):
+                flush(i)
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                step_multi()
+                b.record(stream)
+                b.synchronize()
+                m_ms.append(a.elapsed_time(b))
+            mk = {}
+            for name in ("k_level_plan", "k_hist_u8_multi", "k_finalize_multi"):
+                _, t_, n_ = g.gbt_profile_read(ctx, name)
+                if n_:
+                    mk[name] = t_ / n_
+            g.gbt_profile_enable(ctx, False)
+            assert sess.sync() == 0
+            # bins once per target group of four, (row id, k pairs) per row, k partial images written
+            m_kbytes = R * w.n_features * ((k + 3) // 4) + R * (4 + 8 * k) + k * n_b * w.n_features * B * 8
+            m_t = statistics.median(m_ms)
+            hk = mk.get("k_hist_u8_multi")
+            multi = {"targets": k, "ms_per_call": m_t, "target_entries_per_s": k * entries / (m_t / 1e3),
+                     "kernels_ms_per_launch": mk, "hist_kernel_algorithmic_bytes": m_kbytes,
+                     "hist_kernel_achieved_gbs": (m_kbytes / (hk / 1e3) / 1e9) if hk else None,
+                     "note": "gbt_build_level_multi on the level's built nodes: k int64 histograms, one bin pass"}
+            del hm
+
         # ---------------------------------------------------------------- e2e through host buffers
         e2e = None
         if lv.depth > 0:
@@ -489,6 +539,10 @@ def run_gpu(args, rank, world, local_rank):
         line["oblivious_split"] = obl
     if f64 is not None:
         line["float_cells"] = f64
+    if multi is not None:
+        multi["hist_kernel_frac"] = (multi["hist_kernel_achieved_gbs"] / peak
+                                     if multi["hist_kernel_achieved_gbs"] else None)
+        line["multi_output"] = multi
     print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()
@@ -528,6 +582,8 @@ def main():
                     help="also time the level in float-cell mode (double cells; reported under float_cells)")
     ap.add_argument("--oblivious", action="store_true",
                     help="also time gbt_find_level_split on the level's histograms (reported under oblivious_split)")
+    ap.add_argument("--multi", type=int, default=0, metavar="K",
+                    help="also time gbt_build_level_multi with K targets on the level (u8; reported under multi_output)")
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle time for cpu_baseline")
     ap.add_argument("--ref-budget", type=float, default=90.0, help="seconds of oracle time for --impl reference")
     args = ap.parse_args()
