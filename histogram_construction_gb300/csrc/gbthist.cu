@@ -310,12 +310,12 @@ SplitParams make_sp(const gbt_ctx *c, const gbt_params *prm) {
 // Shared-memory limits of the histogram kernels (once per context).
 bool set_hist_attributes() {
   const int u16_int = H16_HIST_MAX + H16_STAGE_BYTES + 128, u16_flt = H16_HIST_MAX + FL_STAGE_BYTES + 128;
-  return cudaFuncSetAttribute(k_hist_u8<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, H8_SMEM) == cudaSuccess &&
+  return cudaFuncSetAttribute(k_hist_u8<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, H8_SMEM_RING) == cudaSuccess &&
          cudaFuncSetAttribute(k_hist_u8<false>, cudaFuncAttributePreferredSharedMemoryCarveout, 100) == cudaSuccess &&
          cudaFuncSetAttribute(k_hist_u8<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               H8_SMEM + FL_STAGE_BYTES) == cudaSuccess &&
          cudaFuncSetAttribute(k_hist_u8<true>, cudaFuncAttributePreferredSharedMemoryCarveout, 100) == cudaSuccess &&
-         cudaFuncSetAttribute(k_hist_u8<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, H8_SMEM) ==
+         cudaFuncSetAttribute(k_hist_u8<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, H8_SMEM_RING) ==
              cudaSuccess &&
          cudaFuncSetAttribute(k_hist_u8<false, true>, cudaFuncAttributePreferredSharedMemoryCarveout, 100) ==
              cudaSuccess &&
@@ -687,13 +687,13 @@ gbt_status run_level_build(gbt_ctx *c, const int32_t *rows, const int64_t *node_
     hp.n_targets = K;
     prof_begin(c);
     if (multi) {
-      launch_pdl(c, k_hist_u8<false, true>, dim3(hist_ctas), dim3(H8_THREADS), H8_SMEM, hp);
+      launch_pdl(c, k_hist_u8<false, true>, dim3(hist_ctas), dim3(H8_THREADS), H8_SMEM_RING, hp);
       LAUNCH_CHECK(c, "k_hist_u8_multi");
     } else if (f64) {
       launch_pdl(c, k_hist_u8<true>, dim3(hist_ctas), dim3(H8_THREADS), H8_SMEM + FL_STAGE_BYTES, hp);
       LAUNCH_CHECK(c, "k_hist_u8_f32");
     } else {
-      launch_pdl(c, k_hist_u8<false>, dim3(hist_ctas), dim3(H8_THREADS), H8_SMEM, hp);
+      launch_pdl(c, k_hist_u8<false>, dim3(hist_ctas), dim3(H8_THREADS), H8_SMEM_RING, hp);
       LAUNCH_CHECK(c, "k_hist_u8");
     }
   } else {

@@ -293,6 +293,14 @@ constexpr int H8_SB_STRIDE = H8_SB_BYTES + 32;             // shared bytes betwe
 constexpr int H8_SMEM = H8_SB * H8_SB_STRIDE;
 constexpr int H8_THREADS = 1024;
 constexpr int H8_U = 2;                                    // 8-row groups per warp step
+// Integer-cell instantiations stage the gathered strips in a shared ring of
+// H8_RING steps per warp (cp.async), so that the gathers of the next
+// H8_RING - 1 steps are in flight while a step's reductions issue; the
+// float-cell instantiation keeps them in registers, one step ahead (its
+// shared memory holds the double staging of the flush instead).
+constexpr int H8_RING = 3;
+constexpr int H8_RING_BYTES = H8_RING * (H8_THREADS / 32) * H8_U * 512;
+constexpr int H8_SMEM_RING = H8_SMEM + H8_RING_BYTES;
 
 struct Hist8Params {
   LevelParams lv;
@@ -341,6 +349,32 @@ __device__ __forceinline__ void h8_gather(const LevelParams &p, const unsigned c
   }
 }
 
+// Ring variant of h8_gather: the lane's 16-byte quarters go straight to its
+// ring slots (ring_dst + 512 u) with cp.async (zero-filled for rows that are
+// past the end, invalid or of an unused sub-block); only (qg, qh) come to
+// registers.
+template <int U, bool MULTI>
+__device__ __forceinline__ void h8_issue(const LevelParams &p, const unsigned char *strip, bool lane_on, int par,
+                                         const int32_t (&rid)[U], uint32_t ring_dst, uint32_t (&v0)[U],
+                                         uint32_t (&v1)[U], uint32_t &bad, int k, int tsel) {
+#pragma unroll
+  for (int u = 0; u < U; ++u) {
+    const int32_t r = rid[u];
+    const bool valid = (uint32_t)r < (uint32_t)p.n_rows;
+    bad |= (r >= 0 && !valid) ? 1u : 0u;
+    int2 qv = make_int2(0, 0);
+    if (MULTI) {
+      if (valid && lane_on) qv = __ldg(p.q + (int64_t)r * k + tsel);
+    } else if (valid) {
+      qv = __ldg(p.q + r);
+    }
+    const bool ld = valid && lane_on;
+    cp_async_16(ring_dst + (uint32_t)u * 512u, ld ? strip + (int64_t)r * MIRROR_ROW_BYTES : strip, ld ? 16u : 0u);
+    v0[u] = (uint32_t)(par ? qv.y : qv.x);
+    v1[u] = (uint32_t)(par ? qv.x : qv.y);
+  }
+}
+
 template <int E, bool FLT>
 __device__ __forceinline__ void h8_word(uint32_t word, const uint32_t (&sel)[4], const uint32_t (&cj)[4], uint32_t v0,
                                         uint32_t v1) {
@@ -375,9 +409,24 @@ __device__ __forceinline__ void h8_scatter(const H8Stage<U> &st, const uint32_t 
 // 4 tg + w, lane quarter w loads that target's pair, and all four lanes of a
 // row read the same 16-byte quarter. The bank map is the same (the sub-block
 // is the target instead of the feature quarter).
+// With the first gathers of an item in flight: the previous item's flush must
+// have read the image before it is zeroed; zero the slot rows that will be
+// read back, B rows of each used sub-block (lanes of unused sub-blocks add into
+// their own, never read, sub-block).
+__device__ __forceinline__ void h8_zero_image(unsigned char *smem, int nsb, int B) {
+  if (threadIdx.x == 0) bulk_wait_read_all();
+  __syncthreads();
+  for (int sb = 0; sb < nsb; ++sb) {
+    uint4 *h4 = reinterpret_cast<uint4 *>(smem + sb * H8_SB_STRIDE);
+    for (int i = threadIdx.x; i < B * 8; i += blockDim.x) h4[i] = make_uint4(0, 0, 0, 0);
+  }
+  __syncthreads();
+}
+
 template <bool FLT, bool MULTI = false>
 __global__ void __launch_bounds__(H8_THREADS, 1) k_hist_u8(Hist8Params P) {
   constexpr int U = H8_U;
+  constexpr bool RING = !FLT;
   extern __shared__ __align__(128) unsigned char smem[];
   __shared__ int32_t s_item;
   __shared__ Item s_it;  // the next item, claimed and decoded by thread 0 while the last one flushes
@@ -405,6 +454,9 @@ __global__ void __launch_bounds__(H8_THREADS, 1) k_hist_u8(Hist8Params P) {
     cj[j] = hist_base + (uint32_t)(w * H8_SB_STRIDE) + (uint32_t)jj * 8u + (par ? 4u : 0u);
   }
   uint32_t bad = 0;
+  // this lane's 16-byte slot of group 0 in ring slot 0 (ring after the image)
+  const uint32_t ring_stage = (uint32_t)nwarps * U * 512u;
+  const uint32_t ring_lane = hist_base + (uint32_t)H8_SMEM + (uint32_t)warp * U * 512u + (uint32_t)lane * 16u;
 
   if (threadIdx.x == 0) {
     s_item = (int32_t)atomicAdd(&p.st->work_next, 1u);
@@ -432,31 +484,64 @@ __global__ void __launch_bounds__(H8_THREADS, 1) k_hist_u8(Hist8Params P) {
     const int64_t adv = step * U;              // rows per warp step
     int64_t g0 = it.k0 + 8 * warp + rho;
     int32_t rid[U];
-    H8Stage<U> cur, nxt;
-    h8_rows<U>(p, ident, g0, step, it.k1, rid);
-    h8_gather<U, MULTI>(p, strip, lane_on, par, rid, cur, bad, P.n_targets, tsel);
-    h8_rows<U>(p, ident, g0 + adv, step, it.k1, rid);
-    // with the first gathers in flight: the previous item's flush must have
-    // read the image before it is zeroed; zero the slot rows that will be read
-    // back, B rows of each used sub-block (lanes of unused sub-blocks add into
-    // their own, never read, sub-block)
-    if (threadIdx.x == 0) bulk_wait_read_all();
-    __syncthreads();
-    for (int sb = 0; sb < nsb; ++sb) {
-      uint4 *h4 = reinterpret_cast<uint4 *>(smem + sb * H8_SB_STRIDE);
-      for (int i = threadIdx.x; i < B * 8; i += blockDim.x) h4[i] = make_uint4(0, 0, 0, 0);
-    }
-    __syncthreads();
-    // lanes of a warp run out of rows within one group of each other; any
-    // lane with work keeps the warp going (the others add zeros)
-    while (__any_sync(0xffffffffu, g0 < it.k1)) {
-      if (__any_sync(0xffffffffu, g0 + adv < it.k1)) {
-        h8_gather<U, MULTI>(p, strip, lane_on, par, rid, nxt, bad, P.n_targets, tsel);
-        h8_rows<U>(p, ident, g0 + 2 * adv, step, it.k1, rid);
+    if constexpr (RING) {
+      // steps j, j + 1, j + 2 of the warp live in ring slots j % 3, ...;
+      // step j's (qg, qh) in q0, the next two in q1, q2
+      uint32_t q0g[U], q0h[U], q1g[U], q1h[U], q2g[U], q2h[U];
+      h8_rows<U>(p, ident, g0, step, it.k1, rid);
+      h8_issue<U, MULTI>(p, strip, lane_on, par, rid, ring_lane, q0g, q0h, bad, P.n_targets, tsel);
+      cp_async_commit();
+      h8_rows<U>(p, ident, g0 + adv, step, it.k1, rid);
+      h8_issue<U, MULTI>(p, strip, lane_on, par, rid, ring_lane + ring_stage, q1g, q1h, bad, P.n_targets, tsel);
+      cp_async_commit();
+      h8_rows<U>(p, ident, g0 + 2 * adv, step, it.k1, rid);
+      h8_zero_image(smem, nsb, B);
+      uint32_t use = 0;  // ring slot of step j
+      while (__any_sync(0xffffffffu, g0 < it.k1)) {
+        const uint32_t nxt2 = use == 0 ? 2u : use - 1;  // slot of step j + 2 (step j - 1's, consumed)
+        if (__any_sync(0xffffffffu, g0 + 2 * adv < it.k1)) {
+          h8_issue<U, MULTI>(p, strip, lane_on, par, rid, ring_lane + nxt2 * ring_stage, q2g, q2h, bad,
+                             P.n_targets, tsel);
+          h8_rows<U>(p, ident, g0 + 3 * adv, step, it.k1, rid);
+        }
+        cp_async_commit();  // possibly empty: one group per step keeps the count
+        cp_async_wait<2>();  // this lane's copies of step j have landed
+        H8Stage<U> cur;
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          cur.bw[u] = lds_v4(ring_lane + use * ring_stage + (uint32_t)u * 512u);
+          cur.v0[u] = q0g[u];
+          cur.v1[u] = q0h[u];
+        }
+        h8_scatter<U, FLT>(cur, sel, cj);
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          q0g[u] = q1g[u];
+          q0h[u] = q1h[u];
+          q1g[u] = q2g[u];
+          q1h[u] = q2h[u];
+        }
+        use = use == 2 ? 0u : use + 1;
+        g0 += adv;
       }
-      h8_scatter<U, FLT>(cur, sel, cj);
-      cur = nxt;
-      g0 += adv;
+      cp_async_wait<0>();  // the prologue's second step may be unused: no copy may land in the next item
+    } else {
+      H8Stage<U> cur, nxt;
+      h8_rows<U>(p, ident, g0, step, it.k1, rid);
+      h8_gather<U, MULTI>(p, strip, lane_on, par, rid, cur, bad, P.n_targets, tsel);
+      h8_rows<U>(p, ident, g0 + adv, step, it.k1, rid);
+      h8_zero_image(smem, nsb, B);
+      // lanes of a warp run out of rows within one group of each other; any
+      // lane with work keeps the warp going (the others add zeros)
+      while (__any_sync(0xffffffffu, g0 < it.k1)) {
+        if (__any_sync(0xffffffffu, g0 + adv < it.k1)) {
+          h8_gather<U, MULTI>(p, strip, lane_on, par, rid, nxt, bad, P.n_targets, tsel);
+          h8_rows<U>(p, ident, g0 + 2 * adv, step, it.k1, rid);
+        }
+        h8_scatter<U, FLT>(cur, sel, cj);
+        cur = nxt;
+        g0 += adv;
+      }
     }
     __syncthreads();
     if constexpr (FLT) {
