@@ -21,10 +21,9 @@ struct DevState {
   uint32_t qmax;       // max |q| over the current tree's rows, both components
   uint32_t work_next;  // dynamic work counter of the histogram kernel
   uint32_t plan_ok;    // 1 when the level plan is valid
-  int64_t chunk_rows;  // rows per work item chunk (level plan)
+  int64_t exact_rows;  // rows whose int32 partial sums cannot overflow (level plan)
   int32_t n_items;     // work items of the level
-  int32_t chunks_per_group;  // consecutive chunks of a node whose int32 sum stays exact (level plan)
-  uint32_t qmax_multi;       // max |q| over the multi-output tree's pairs, all targets
+  uint32_t qmax_multi; // max |q| over the multi-output tree's pairs, all targets
 };
 
 constexpr int MIRROR_STRIP_BYTES = 64;  // bytes per row per mirror tile of features

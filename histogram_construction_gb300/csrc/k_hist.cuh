@@ -78,15 +78,27 @@ __device__ __forceinline__ int64_t block_incl_scan(int64_t v, int64_t *s_warp) {
   return r;
 }
 
-// Level plan. Rows per chunk come from the load-balance target, capped by
-// the int32 exactness bound rc = (2^31 - 1) / max|q|; consecutive chunks of
-// a node form exactness groups of floor(rc / chunk) chunks, whose int32 sum
-// cannot overflow either. Every work item (chunk, feature group) adds its
+// Level plan. With T = target_items / n_fgroups chunks wanted and N' nodes
+// holding rows, the base length is L = ceil(R / max(T - N', ceil(T / 2)))
+// (at least CHUNK_MIN_ROWS, at most the int32 exactness bound
+// rc = (2^31 - 1) / max|q| and the chunk cap): every node rounds its chunk
+// count ceil(rows_n / L) up by less than one, so with T > 2N' the level has at
+// most T chunks and no persistent CTA takes one item more than the others.
+// A node's chunks have equal length ceil(rows_n / c_n) <= L, and its
+// consecutive chunks form exactness groups of floor(rc / length) chunks, whose
+// int32 sum cannot overflow either. Every work item (chunk, feature group) adds its
 // shared-memory image into its group's image; groups of more than one chunk
 // are zeroed here first (every block plans redundantly and zeroes a share;
 // block 0 publishes the plan). Offsets that do not start at 0, descend or
 // leave [0, n_rows] invalidate the plan (no items; GBT_ERR_ROW_RANGE).
 constexpr int PLAN_THREADS = 1024;
+
+// A node of rows_n rows in c equal chunks (ceil(rows_n / c) rows each, the
+// last one shorter): consecutive chunks per exactness group.
+__host__ __device__ __forceinline__ int64_t chunks_per_group(int64_t rows_n, int64_t c, int64_t rc) {
+  const int64_t len = (rows_n + c - 1) / c;
+  return len > 0 ? max((int64_t)1, min(rc / len, (int64_t)0x3fffffff)) : (int64_t)0x3fffffff;
+}
 
 __global__ void __launch_bounds__(PLAN_THREADS) k_level_plan(LevelParams p) {
   pdl_trigger();  // the histogram kernel may launch now; it waits for this grid to finish
@@ -94,8 +106,7 @@ __global__ void __launch_bounds__(PLAN_THREADS) k_level_plan(LevelParams p) {
   __shared__ int64_t s_zpre[PLAN_THREADS + 1];  // zero-unit prefix of the batch's nodes
   __shared__ int64_t s_zbase[PLAN_THREADS];     // first zeroed unit of each node of the batch
   __shared__ int64_t s_tot[2];
-  __shared__ long long s_chunk;
-  __shared__ int32_t s_cpg;
+  __shared__ long long s_chunk, s_rc;
   const int tid = threadIdx.x;
   const bool pub = blockIdx.x == 0;
   bool bad = (tid == 0) && (p.offs[0] != 0);
@@ -112,20 +123,26 @@ __global__ void __launch_bounds__(PLAN_THREADS) k_level_plan(LevelParams p) {
     }
     return;
   }
+  int nonempty = 0;  // N': nodes holding rows
+  for (int base = 0; base < p.n_nodes; base += blockDim.x) {
+    const int n = base + tid;
+    nonempty += __syncthreads_count(n < p.n_nodes && p.offs[n + 1] > p.offs[n]);
+  }
   if (tid == 0) {
     const int64_t R = p.offs[p.n_nodes];
     const uint32_t qm = max(p.qmax_plan ? p.qmax_plan : p.st->qmax, 1u);
     const int64_t rc = 2147483647LL / (int64_t)qm;  // rows whose int32 partials cannot overflow
-    int64_t tgt = (R * p.n_fgroups + p.target_items - 1) / max(p.target_items, 1);
-    tgt = max(tgt, (int64_t)CHUNK_MIN_ROWS);
-    int64_t chunk = max((int64_t)1, min(rc, tgt));
+    const int64_t T = max((int64_t)1, (int64_t)p.target_items / p.n_fgroups);
+    const int64_t denom = max(T - nonempty, (T + 1) / 2);
+    int64_t chunk = max((R + denom - 1) / denom, (int64_t)CHUNK_MIN_ROWS);
+    chunk = max((int64_t)1, min(rc, chunk));
     if (p.chunk_cap > 0) chunk = min(chunk, (int64_t)p.chunk_cap);
     s_chunk = chunk;
-    s_cpg = (int32_t)min(rc / chunk, (int64_t)0x3fffffff);
+    s_rc = rc;
   }
   __syncthreads();
   const int64_t chunk = s_chunk;
-  const int32_t cpg = s_cpg;
+  const int64_t rc = s_rc;
   const int64_t img_group = (int64_t)p.n_fgroups * p.image_int4s;  // units of one group's images
   int4 *zdst = reinterpret_cast<int4 *>(p.partial);
   int64_t carry_c = 0, carry_g = 0;
@@ -135,6 +152,7 @@ __global__ void __launch_bounds__(PLAN_THREADS) k_level_plan(LevelParams p) {
     if (n < p.n_nodes) {
       const int64_t rows_n = p.offs[n + 1] - p.offs[n];
       c = max((int64_t)1, (rows_n + chunk - 1) / chunk);
+      const int64_t cpg = chunks_per_group(rows_n, c, rc);
       g = (c + cpg - 1) / cpg;
       if (cpg > 1) m = c / cpg + ((c % cpg) >= 2 ? 1 : 0);  // groups of >= 2 chunks: the first m
     }
@@ -170,8 +188,7 @@ __global__ void __launch_bounds__(PLAN_THREADS) k_level_plan(LevelParams p) {
     p.chunk_prefix[0] = 0;
     p.group_prefix[0] = 0;
     p.st->plan_ok = 1;
-    p.st->chunk_rows = chunk;
-    p.st->chunks_per_group = cpg;
+    p.st->exact_rows = rc;
     p.st->n_items = (int32_t)(carry_c * p.n_fgroups);
     p.st->work_next = 0;
   }
@@ -186,7 +203,7 @@ struct Item {
   bool multi;     // the group has more than one chunk: reduce-add, else store
 };
 
-__device__ __forceinline__ Item decode_item(int32_t id, const LevelParams &p, int64_t chunk, int32_t cpg) {
+__device__ __forceinline__ Item decode_item(int32_t id, const LevelParams &p, int64_t rc) {
   Item it;
   const int32_t kc = id / p.n_fgroups;
   it.fgroup = id - kc * p.n_fgroups;
@@ -199,8 +216,10 @@ __device__ __forceinline__ Item decode_item(int32_t id, const LevelParams &p, in
   const int32_t c = kc - p.chunk_prefix[lo];
   const int32_t nc = p.chunk_prefix[lo + 1] - p.chunk_prefix[lo];
   const int64_t a = p.offs[lo], b = p.offs[lo + 1];
-  it.k0 = a + (int64_t)c * chunk;
-  it.k1 = min(b, it.k0 + chunk);
+  const int64_t len = (b - a + nc - 1) / nc;
+  it.k0 = a + (int64_t)c * len;
+  it.k1 = min(b, it.k0 + len);
+  const int32_t cpg = (int32_t)chunks_per_group(b - a, nc, rc);
   const int32_t g = c / cpg;
   it.image = (int64_t)(p.group_prefix[lo] + g) * p.n_fgroups + it.fgroup;
   it.multi = min(cpg, nc - g * cpg) > 1;
@@ -435,8 +454,7 @@ __global__ void __launch_bounds__(H8_THREADS, 1) k_hist_u8(Hist8Params P) {
   pdl_wait();     // the level plan
   pdl_trigger();  // the consumer kernel may launch; it waits for this grid to finish
   if (!p.st->plan_ok) return;
-  const int64_t chunk = p.st->chunk_rows;
-  const int32_t cpg = p.st->chunks_per_group;
+  const int64_t rc = p.st->exact_rows;
   const int32_t n_items = p.st->n_items;
   const int B = P.n_slots;
   const int64_t N = p.n_rows;
@@ -460,7 +478,7 @@ __global__ void __launch_bounds__(H8_THREADS, 1) k_hist_u8(Hist8Params P) {
 
   if (threadIdx.x == 0) {
     s_item = (int32_t)atomicAdd(&p.st->work_next, 1u);
-    if (s_item < n_items) s_it = decode_item(s_item, p, chunk, cpg);
+    if (s_item < n_items) s_it = decode_item(s_item, p, rc);
   }
   __syncthreads();
   for (;;) {
@@ -569,7 +587,7 @@ __global__ void __launch_bounds__(H8_THREADS, 1) k_hist_u8(Hist8Params P) {
     }
     if (threadIdx.x == 0) {
       s_item = (int32_t)atomicAdd(&p.st->work_next, 1u);
-      if (s_item < n_items) s_it = decode_item(s_item, p, chunk, cpg);
+      if (s_item < n_items) s_it = decode_item(s_item, p, rc);
     }
     __syncthreads();
   }
@@ -629,8 +647,7 @@ __global__ void __launch_bounds__(H16_THREADS, 1) k_hist_u16(Hist16Params P) {
   pdl_wait();     // the level plan
   pdl_trigger();  // the consumer kernel may launch; it waits for this grid to finish
   if (!p.st->plan_ok) return;
-  const int64_t chunk = p.st->chunk_rows;
-  const int32_t cpg = p.st->chunks_per_group;
+  const int64_t rc = p.st->exact_rows;
   const int32_t n_items = p.st->n_items;
   const int64_t N = p.n_rows;
   const bool ident = (p.rows == nullptr);
@@ -647,7 +664,7 @@ __global__ void __launch_bounds__(H16_THREADS, 1) k_hist_u16(Hist16Params P) {
     __syncthreads();
     const int32_t id = s_item;
     if (id >= n_items) break;
-    const Item it = decode_item(id, p, chunk, cpg);
+    const Item it = decode_item(id, p, rc);
     {
       uint4 *h4 = reinterpret_cast<uint4 *>(hist);
       const int n4 = (B * TS * 8) / 16;
