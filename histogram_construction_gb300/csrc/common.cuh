@@ -21,7 +21,6 @@ struct DevState {
   uint32_t qmax;       // max |q| over the current tree's rows, both components
   uint32_t work_next;  // dynamic work counter of the histogram kernel
   uint32_t plan_ok;    // 1 when the level plan is valid
-  int64_t exact_rows;  // rows whose int32 partial sums cannot overflow (level plan)
   int32_t n_items;     // work items of the level
   uint32_t qmax_multi; // max |q| over the multi-output tree's pairs, all targets
 };

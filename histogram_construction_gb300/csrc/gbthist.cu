@@ -100,10 +100,10 @@ struct gbt_ctx {
   DevState *st = nullptr;
   uint32_t *err_host = nullptr;  // pinned: [0] error word copy, [1] max |q| copy, [2] multi-output max |q| copy
   Buf gp_stage, chunk_prefix, partial, rows_in, offs_in, cand, splits_a, splits_b, parent_of_in, tile_counts, lrank,
-      slab, counters, level_scratch;
+      slab, counters, level_scratch, items;
   std::string last_error;
   int64_t launches = 0;
-  // tuning: work items the level plan aims for (default 2 per SM; GBT_TARGET_ITEMS overrides it for sweeps)
+  // tuning: work items the level plan aims for (default 1 per SM; GBT_TARGET_ITEMS overrides it for sweeps)
   int target_items = 0;
   // diagnostics: per-launch event pairs
   bool prof = false;
@@ -393,7 +393,7 @@ gbt_status gbt_destroy(gbt_ctx *c) {
   cudaStreamSynchronize(c->stream);
   Buf *bufs[] = {&c->mirror, &c->q, &c->gp_stage, &c->chunk_prefix, &c->partial, &c->rows_in, &c->offs_in,
                  &c->cand, &c->splits_a, &c->splits_b, &c->parent_of_in, &c->tile_counts, &c->lrank, &c->slab,
-                 &c->counters, &c->level_scratch, &c->qm};
+                 &c->counters, &c->level_scratch, &c->qm, &c->items};
   for (Buf *b : bufs) release(c, *b);
   if (c->st) cudaFreeAsync(c->st, c->stream);
   cudaStreamSynchronize(c->stream);
@@ -648,7 +648,7 @@ gbt_status run_level_build(gbt_ctx *c, const int32_t *rows, const int64_t *node_
   lp.item_feats = multi ? 16 : (c->bin_bytes == 1 ? 64 : c->ts16);
   // multi-output: an item is a 16-feature quarter and a group of up to four targets
   lp.n_fgroups = (c->n_features + lp.item_feats - 1) / lp.item_feats * (multi ? (K + 3) / 4 : 1);
-  lp.target_items = c->target_items > 0 ? c->target_items : c->n_sm * 2;
+  lp.target_items = c->target_items > 0 ? c->target_items : c->n_sm;
   lp.n_rows = c->n_rows;
   lp.q = f64 ? (const int2 *)gpair_f64 : (multi ? (const int2 *)c->qm.p : (const int2 *)c->q.p);
   lp.chunk_prefix = (int32_t *)c->chunk_prefix.p;
@@ -673,11 +673,15 @@ gbt_status run_level_build(gbt_ctx *c, const int32_t *rows, const int64_t *node_
   s = ensure(c, c->partial, (size_t)items_max * lp.image_int4s * 16, "level image scratch");
   if (s != GBT_OK) return s;
   lp.partial = (int32_t *)c->partial.p;
+  s = ensure(c, c->items, (size_t)items_max * sizeof(Item), "level work items");
+  if (s != GBT_OK) return s;
+  lp.items = (Item *)c->items.p;
+  const int hist_ctas = c->n_sm;  // persistent: one resident CTA per SM
+  lp.first_static = hist_ctas;
 
   prof_begin(c);
   k_level_plan<<<c->n_sm, PLAN_THREADS, 0, c->stream>>>(lp);
   LAUNCH_CHECK(c, "k_level_plan");
-  const int hist_ctas = c->n_sm;  // persistent: one resident CTA per SM
   if (c->bin_bytes == 1) {
     Hist8Params hp;
     hp.lv = lp;

@@ -33,6 +33,17 @@ namespace gbt {
 
 constexpr int CHUNK_MIN_ROWS = 1024;
 
+// A work item: node, feature group, row range [k0, k1) in level order and
+// the group image it adds into. Item ids run chunk-major, feature group
+// fastest; the plan writes every item's record, so that a claim is one load.
+struct Item {
+  int32_t node, fgroup;
+  int64_t k0, k1;
+  int64_t image;  // group image index
+  int32_t multi;  // the group has more than one chunk: reduce-add, else store
+  int32_t pad;
+};
+
 struct LevelParams {
   const int32_t *rows;    // level row list or nullptr (identity)
   const int64_t *offs;    // [n_nodes + 1]
@@ -50,6 +61,8 @@ struct LevelParams {
   int32_t nsb;            // sub-blocks per image (4 for u8, 1 for u16)
   uint32_t qmax_plan;     // if nonzero, the plan's exactness bound uses it instead of the tree's max|q|
   int32_t chunk_cap;      // if nonzero, no chunk holds more rows (float cells: rounding per chunk)
+  Item *items;            // [items] decoded work items (written by the plan)
+  int32_t first_static;   // items 0 .. first_static - 1 go to histogram CTAs by block index
   DevState *st;
 };
 
@@ -78,12 +91,13 @@ __device__ __forceinline__ int64_t block_incl_scan(int64_t v, int64_t *s_warp) {
   return r;
 }
 
-// Level plan. With T = target_items / n_fgroups chunks wanted and N' nodes
-// holding rows, the base length is L = ceil(R / max(T - N', ceil(T / 2)))
-// (at least CHUNK_MIN_ROWS, at most the int32 exactness bound
-// rc = (2^31 - 1) / max|q| and the chunk cap): every node rounds its chunk
-// count ceil(rows_n / L) up by less than one, so with T > 2N' the level has at
-// most T chunks and no persistent CTA takes one item more than the others.
+// Level plan. With T = target_items / n_fgroups chunks wanted, the base
+// length L is the shortest of 16 candidates from ceil(R / T) up to the closed
+// form ceil(R / max(T - N', ceil(T / 2))) (N' nodes holding rows; it keeps the
+// count within T whenever T >= 2N') whose chunk count
+// sum_n max(1, ceil(rows_n / L)) stays within T. L is at least CHUNK_MIN_ROWS and at
+// most the int32 exactness bound rc = (2^31 - 1) / max|q| and the chunk cap.
+// So no persistent CTA takes one item more than the others.
 // A node's chunks have equal length ceil(rows_n / c_n) <= L, and its
 // consecutive chunks form exactness groups of floor(rc / length) chunks, whose
 // int32 sum cannot overflow either. Every work item (chunk, feature group) adds its
@@ -92,6 +106,7 @@ __device__ __forceinline__ int64_t block_incl_scan(int64_t v, int64_t *s_warp) {
 // block 0 publishes the plan). Offsets that do not start at 0, descend or
 // leave [0, n_rows] invalidate the plan (no items; GBT_ERR_ROW_RANGE).
 constexpr int PLAN_THREADS = 1024;
+constexpr int PLAN_CANDS = 16;  // chunk lengths the plan counts in one pass
 
 // A node of rows_n rows in c equal chunks (ceil(rows_n / c) rows each, the
 // last one shorter): consecutive chunks per exactness group.
@@ -105,8 +120,13 @@ __global__ void __launch_bounds__(PLAN_THREADS) k_level_plan(LevelParams p) {
   __shared__ int64_t s_warp[32];
   __shared__ int64_t s_zpre[PLAN_THREADS + 1];  // zero-unit prefix of the batch's nodes
   __shared__ int64_t s_zbase[PLAN_THREADS];     // first zeroed unit of each node of the batch
+  __shared__ int64_t s_a[PLAN_THREADS];         // first level position of each node of the batch
+  __shared__ int32_t s_cpre[PLAN_THREADS + 1];  // chunk prefix within the batch
+  __shared__ int32_t s_rows[PLAN_THREADS], s_len[PLAN_THREADS], s_cpg[PLAN_THREADS], s_gbase[PLAN_THREADS];
   __shared__ int64_t s_tot[2];
   __shared__ long long s_chunk, s_rc;
+  __shared__ uint32_t s_cnt[PLAN_CANDS], s_cand[PLAN_CANDS];
+  __shared__ long long s_T;
   const int tid = threadIdx.x;
   const bool pub = blockIdx.x == 0;
   bool bad = (tid == 0) && (p.offs[0] != 0);
@@ -128,13 +148,52 @@ __global__ void __launch_bounds__(PLAN_THREADS) k_level_plan(LevelParams p) {
     const int n = base + tid;
     nonempty += __syncthreads_count(n < p.n_nodes && p.offs[n + 1] > p.offs[n]);
   }
+  // scalars in one thread (64-bit division is a long software sequence)
   if (tid == 0) {
     const int64_t R = p.offs[p.n_nodes];
+    const int64_t T = max((int64_t)1, (int64_t)p.target_items / p.n_fgroups);
+    // closed form: at most T chunks whenever T >= 2 N'
+    const int64_t denom = max(T - nonempty, (T + 1) / 2);
+    const int64_t hi = max((int64_t)1, (R + denom - 1) / denom);
+    const int64_t lo = min(hi, max((int64_t)1, (R + T - 1) / T));
+    for (int k = 0; k < PLAN_CANDS; ++k)
+      s_cand[k] = (uint32_t)(lo + ((hi - lo) * k + PLAN_CANDS - 2) / (PLAN_CANDS - 1));
+    s_T = T;
+  }
+  if (tid < PLAN_CANDS) s_cnt[tid] = 0;
+  __syncthreads();
+  {
+    // PLAN_CANDS lengths from ceil(R / T) up to the closed form, counted in
+    // one pass; the shortest whose chunk count sum_n max(1, ceil(rows_n / L))
+    // stays within T wins (the closed form when none does)
+    uint32_t cnt[PLAN_CANDS];
+#pragma unroll
+    for (int k = 0; k < PLAN_CANDS; ++k) cnt[k] = 0;
+    for (int n = tid; n < p.n_nodes; n += blockDim.x) {
+      const uint32_t rows_n = (uint32_t)(p.offs[n + 1] - p.offs[n]);
+#pragma unroll
+      for (int k = 0; k < PLAN_CANDS; ++k) cnt[k] += max(1u, (rows_n + s_cand[k] - 1) / s_cand[k]);
+    }
+    if ((tid & ~31) < p.n_nodes) {  // warps holding nodes (warp-uniform)
+#pragma unroll
+      for (int k = 0; k < PLAN_CANDS; ++k) {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) cnt[k] += __shfl_xor_sync(0xffffffffu, cnt[k], o);
+      }
+      if ((tid & 31) == 0) {
+#pragma unroll
+        for (int k = 0; k < PLAN_CANDS; ++k) atomicAdd(&s_cnt[k], cnt[k]);
+      }
+    }
+  }
+  __syncthreads();
+  if (tid == 0) {
+    int64_t len = s_cand[PLAN_CANDS - 1];
+    for (int k = PLAN_CANDS - 1; k >= 0; --k)
+      if ((int64_t)s_cnt[k] <= s_T) len = s_cand[k];
     const uint32_t qm = max(p.qmax_plan ? p.qmax_plan : p.st->qmax, 1u);
     const int64_t rc = 2147483647LL / (int64_t)qm;  // rows whose int32 partials cannot overflow
-    const int64_t T = max((int64_t)1, (int64_t)p.target_items / p.n_fgroups);
-    const int64_t denom = max(T - nonempty, (T + 1) / 2);
-    int64_t chunk = max((R + denom - 1) / denom, (int64_t)CHUNK_MIN_ROWS);
+    int64_t chunk = max(len, (int64_t)CHUNK_MIN_ROWS);
     chunk = max((int64_t)1, min(rc, chunk));
     if (p.chunk_cap > 0) chunk = min(chunk, (int64_t)p.chunk_cap);
     s_chunk = chunk;
@@ -148,11 +207,12 @@ __global__ void __launch_bounds__(PLAN_THREADS) k_level_plan(LevelParams p) {
   int64_t carry_c = 0, carry_g = 0;
   for (int base = 0; base < p.n_nodes; base += blockDim.x) {
     const int n = base + tid;
-    int64_t c = 0, g = 0, m = 0;
+    int64_t c = 0, g = 0, m = 0, cpg = 1, rows_n = 0, a = 0;
     if (n < p.n_nodes) {
-      const int64_t rows_n = p.offs[n + 1] - p.offs[n];
+      a = p.offs[n];
+      rows_n = p.offs[n + 1] - a;
       c = max((int64_t)1, (rows_n + chunk - 1) / chunk);
-      const int64_t cpg = chunks_per_group(rows_n, c, rc);
+      cpg = chunks_per_group(rows_n, c, rc);
       g = (c + cpg - 1) / cpg;
       if (cpg > 1) m = c / cpg + ((c % cpg) >= 2 ? 1 : 0);  // groups of >= 2 chunks: the first m
     }
@@ -165,7 +225,16 @@ __global__ void __launch_bounds__(PLAN_THREADS) k_level_plan(LevelParams p) {
     }
     s_zpre[tid + 1] = iz;
     s_zbase[tid] = (carry_g + ig - g) * img_group;
-    if (tid == 0) s_zpre[0] = 0;
+    s_cpre[tid + 1] = (int32_t)ic;
+    s_a[tid] = a;
+    s_rows[tid] = (int32_t)rows_n;
+    s_len[tid] = (int32_t)((rows_n + c - 1) / max(c, (int64_t)1));
+    s_cpg[tid] = (int32_t)cpg;
+    s_gbase[tid] = (int32_t)(carry_g + ig - g);
+    if (tid == 0) {
+      s_zpre[0] = 0;
+      s_cpre[0] = 0;
+    }
     if (tid == blockDim.x - 1) {
       s_tot[0] = ic;
       s_tot[1] = ig;
@@ -180,6 +249,29 @@ __global__ void __launch_bounds__(PLAN_THREADS) k_level_plan(LevelParams p) {
       }
       zdst[s_zbase[lo] + (u - s_zpre[lo])] = make_int4(0, 0, 0, 0);
     }
+    // the batch's work items, shared out over the grid like the zeroing
+    const int64_t nfg = p.n_fgroups;
+    const int64_t items = (int64_t)s_cpre[blockDim.x] * nfg;
+    for (int64_t u = (int64_t)blockIdx.x * blockDim.x + tid; u < items; u += (int64_t)gridDim.x * blockDim.x) {
+      const int32_t kc = (int32_t)(u / nfg);  // chunk within the batch
+      const int32_t f = (int32_t)(u - (int64_t)kc * nfg);
+      int lo = 0, hi = blockDim.x - 1;  // largest j with s_cpre[j] <= kc
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (s_cpre[mid] <= kc) lo = mid; else hi = mid - 1;
+      }
+      const int32_t cidx = kc - s_cpre[lo], nc = s_cpre[lo + 1] - s_cpre[lo], cpg_n = s_cpg[lo];
+      const int32_t gi = cidx / cpg_n;
+      Item it;
+      it.node = base + lo;
+      it.fgroup = f;
+      it.k0 = s_a[lo] + (int64_t)cidx * s_len[lo];
+      it.k1 = min(s_a[lo] + s_rows[lo], it.k0 + s_len[lo]);
+      it.image = (int64_t)(s_gbase[lo] + gi) * nfg + f;
+      it.multi = min(cpg_n, nc - gi * cpg_n) > 1 ? 1 : 0;
+      it.pad = 0;
+      p.items[(carry_c * nfg) + u] = it;
+    }
     carry_c += s_tot[0];
     carry_g += s_tot[1];
     __syncthreads();
@@ -188,43 +280,11 @@ __global__ void __launch_bounds__(PLAN_THREADS) k_level_plan(LevelParams p) {
     p.chunk_prefix[0] = 0;
     p.group_prefix[0] = 0;
     p.st->plan_ok = 1;
-    p.st->exact_rows = rc;
     p.st->n_items = (int32_t)(carry_c * p.n_fgroups);
-    p.st->work_next = 0;
+    p.st->work_next = (uint32_t)p.first_static;  // dynamic claims start after the static first items
   }
 }
 
-// Decode a work item id (chunk-major, feature group fastest) into node,
-// feature group, row range and the group image it adds into.
-struct Item {
-  int32_t node, fgroup;
-  int64_t k0, k1;
-  int64_t image;  // group image index
-  bool multi;     // the group has more than one chunk: reduce-add, else store
-};
-
-__device__ __forceinline__ Item decode_item(int32_t id, const LevelParams &p, int64_t rc) {
-  Item it;
-  const int32_t kc = id / p.n_fgroups;
-  it.fgroup = id - kc * p.n_fgroups;
-  int lo = 0, hi = p.n_nodes - 1;  // largest n with chunk_prefix[n] <= kc
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (p.chunk_prefix[mid] <= kc) lo = mid; else hi = mid - 1;
-  }
-  it.node = lo;
-  const int32_t c = kc - p.chunk_prefix[lo];
-  const int32_t nc = p.chunk_prefix[lo + 1] - p.chunk_prefix[lo];
-  const int64_t a = p.offs[lo], b = p.offs[lo + 1];
-  const int64_t len = (b - a + nc - 1) / nc;
-  it.k0 = a + (int64_t)c * len;
-  it.k1 = min(b, it.k0 + len);
-  const int32_t cpg = (int32_t)chunks_per_group(b - a, nc, rc);
-  const int32_t g = c / cpg;
-  it.image = (int64_t)(p.group_prefix[lo] + g) * p.n_fgroups + it.fgroup;
-  it.multi = min(cpg, nc - g * cpg) > 1;
-  return it;
-}
 
 // Loads (row id, qg, qh) of level position k; row -1 marks an invalid row.
 __device__ __forceinline__ void load_row(const LevelParams &p, bool ident, int64_t k, int64_t k1, int32_t &r,
@@ -370,27 +430,24 @@ __device__ __forceinline__ void h8_gather(const LevelParams &p, const unsigned c
 
 // Ring variant of h8_gather: the lane's 16-byte quarters go straight to its
 // ring slots (ring_dst + 512 u) with cp.async (zero-filled for rows that are
-// past the end, invalid or of an unused sub-block); only (qg, qh) come to
-// registers.
+// past the end, invalid or of an unused sub-block); only the (qg, qh) pairs
+// come to registers, as loaded (the component order is chosen at use).
 template <int U, bool MULTI>
-__device__ __forceinline__ void h8_issue(const LevelParams &p, const unsigned char *strip, bool lane_on, int par,
-                                         const int32_t (&rid)[U], uint32_t ring_dst, uint32_t (&v0)[U],
-                                         uint32_t (&v1)[U], uint32_t &bad, int k, int tsel) {
+__device__ __forceinline__ void h8_issue(const LevelParams &p, const unsigned char *strip, bool lane_on,
+                                         const int32_t (&rid)[U], uint32_t ring_dst, int2 (&qv)[U], uint32_t &bad,
+                                         int k, int tsel) {
 #pragma unroll
   for (int u = 0; u < U; ++u) {
     const int32_t r = rid[u];
     const bool valid = (uint32_t)r < (uint32_t)p.n_rows;
     bad |= (r >= 0 && !valid) ? 1u : 0u;
-    int2 qv = make_int2(0, 0);
-    if (MULTI) {
-      if (valid && lane_on) qv = __ldg(p.q + (int64_t)r * k + tsel);
-    } else if (valid) {
-      qv = __ldg(p.q + r);
-    }
     const bool ld = valid && lane_on;
+    if (MULTI) {
+      qv[u] = ld ? __ldg(p.q + (int64_t)r * k + tsel) : make_int2(0, 0);
+    } else {
+      qv[u] = valid ? __ldg(p.q + r) : make_int2(0, 0);
+    }
     cp_async_16(ring_dst + (uint32_t)u * 512u, ld ? strip + (int64_t)r * MIRROR_ROW_BYTES : strip, ld ? 16u : 0u);
-    v0[u] = (uint32_t)(par ? qv.y : qv.x);
-    v1[u] = (uint32_t)(par ? qv.x : qv.y);
   }
 }
 
@@ -454,7 +511,6 @@ __global__ void __launch_bounds__(H8_THREADS, 1) k_hist_u8(Hist8Params P) {
   pdl_wait();     // the level plan
   pdl_trigger();  // the consumer kernel may launch; it waits for this grid to finish
   if (!p.st->plan_ok) return;
-  const int64_t rc = p.st->exact_rows;
   const int32_t n_items = p.st->n_items;
   const int B = P.n_slots;
   const int64_t N = p.n_rows;
@@ -476,9 +532,10 @@ __global__ void __launch_bounds__(H8_THREADS, 1) k_hist_u8(Hist8Params P) {
   const uint32_t ring_stage = (uint32_t)nwarps * U * 512u;
   const uint32_t ring_lane = hist_base + (uint32_t)H8_SMEM + (uint32_t)warp * U * 512u + (uint32_t)lane * 16u;
 
-  if (threadIdx.x == 0) {
-    s_item = (int32_t)atomicAdd(&p.st->work_next, 1u);
-    if (s_item < n_items) s_it = decode_item(s_item, p, rc);
+  if (threadIdx.x == 0) {  // the first item by block index, later ones from the counter
+    s_item = (int32_t)blockIdx.x < p.first_static ? (int32_t)blockIdx.x
+                                                   : (int32_t)atomicAdd(&p.st->work_next, 1u);
+    if (s_item < n_items) s_it = p.items[s_item];
   }
   __syncthreads();
   for (;;) {
@@ -503,44 +560,50 @@ __global__ void __launch_bounds__(H8_THREADS, 1) k_hist_u8(Hist8Params P) {
     int64_t g0 = it.k0 + 8 * warp + rho;
     int32_t rid[U];
     if constexpr (RING) {
-      // steps j, j + 1, j + 2 of the warp live in ring slots j % 3, ...;
-      // step j's (qg, qh) in q0, the next two in q1, q2
-      uint32_t q0g[U], q0h[U], q1g[U], q1h[U], q2g[U], q2h[U];
-      h8_rows<U>(p, ident, g0, step, it.k1, rid);
-      h8_issue<U, MULTI>(p, strip, lane_on, par, rid, ring_lane, q0g, q0h, bad, P.n_targets, tsel);
+      // Steps j, j + 1, j + 2 of the warp live in ring slots j % 3, ...; their
+      // (qg, qh) in qa, qb, qc by the same rotation, and the row ids of steps
+      // j + 2, j + 3, j + 4 in xa, xb, xc (step j + 2's set is reloaded with
+      // step j + 5's, three steps ahead of its use). The loop is unrolled three
+      // times so that no register is copied: a copy of a loaded register would
+      // wait for the load.
+      int2 qa[U], qb[U], qc[U];
+      int32_t xa[U], xb[U], xc[U];
+      h8_rows<U>(p, ident, g0, step, it.k1, xa);
+      h8_rows<U>(p, ident, g0 + adv, step, it.k1, xb);
+      h8_rows<U>(p, ident, g0 + 2 * adv, step, it.k1, xc);
+      h8_issue<U, MULTI>(p, strip, lane_on, xa, ring_lane, qa, bad, P.n_targets, tsel);
       cp_async_commit();
-      h8_rows<U>(p, ident, g0 + adv, step, it.k1, rid);
-      h8_issue<U, MULTI>(p, strip, lane_on, par, rid, ring_lane + ring_stage, q1g, q1h, bad, P.n_targets, tsel);
+      h8_issue<U, MULTI>(p, strip, lane_on, xb, ring_lane + ring_stage, qb, bad, P.n_targets, tsel);
       cp_async_commit();
-      h8_rows<U>(p, ident, g0 + 2 * adv, step, it.k1, rid);
+      h8_rows<U>(p, ident, g0 + 3 * adv, step, it.k1, xa);
+      h8_rows<U>(p, ident, g0 + 4 * adv, step, it.k1, xb);
       h8_zero_image(smem, nsb, B);
-      uint32_t use = 0;  // ring slot of step j
-      while (__any_sync(0xffffffffu, g0 < it.k1)) {
-        const uint32_t nxt2 = use == 0 ? 2u : use - 1;  // slot of step j + 2 (step j - 1's, consumed)
+      // one step: consume slot `use` (pairs qcur), issue step j + 2 (row ids
+      // xnew) into slot `nxt2` (pairs qnew: the slot and pairs step j - 1 used)
+      auto one_step = [&](uint32_t use, uint32_t nxt2, const int2(&qcur)[U], int2(&qnew)[U],
+                          int32_t(&xnew)[U]) -> bool {
+        if (!__any_sync(0xffffffffu, g0 < it.k1)) return false;
         if (__any_sync(0xffffffffu, g0 + 2 * adv < it.k1)) {
-          h8_issue<U, MULTI>(p, strip, lane_on, par, rid, ring_lane + nxt2 * ring_stage, q2g, q2h, bad,
-                             P.n_targets, tsel);
-          h8_rows<U>(p, ident, g0 + 3 * adv, step, it.k1, rid);
+          h8_issue<U, MULTI>(p, strip, lane_on, xnew, ring_lane + nxt2 * ring_stage, qnew, bad, P.n_targets, tsel);
+          h8_rows<U>(p, ident, g0 + 5 * adv, step, it.k1, xnew);
         }
-        cp_async_commit();  // possibly empty: one group per step keeps the count
+        cp_async_commit();   // possibly empty: one group per step keeps the count
         cp_async_wait<2>();  // this lane's copies of step j have landed
         H8Stage<U> cur;
 #pragma unroll
         for (int u = 0; u < U; ++u) {
           cur.bw[u] = lds_v4(ring_lane + use * ring_stage + (uint32_t)u * 512u);
-          cur.v0[u] = q0g[u];
-          cur.v1[u] = q0h[u];
+          cur.v0[u] = (uint32_t)(par ? qcur[u].y : qcur[u].x);
+          cur.v1[u] = (uint32_t)(par ? qcur[u].x : qcur[u].y);
         }
         h8_scatter<U, FLT>(cur, sel, cj);
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-          q0g[u] = q1g[u];
-          q0h[u] = q1h[u];
-          q1g[u] = q2g[u];
-          q1h[u] = q2h[u];
-        }
-        use = use == 2 ? 0u : use + 1;
         g0 += adv;
+        return true;
+      };
+      for (;;) {
+        if (!one_step(0, 2, qa, qc, xc)) break;
+        if (!one_step(1, 0, qb, qa, xa)) break;
+        if (!one_step(2, 1, qc, qb, xb)) break;
       }
       cp_async_wait<0>();  // the prologue's second step may be unused: no copy may land in the next item
     } else {
@@ -587,7 +650,7 @@ __global__ void __launch_bounds__(H8_THREADS, 1) k_hist_u8(Hist8Params P) {
     }
     if (threadIdx.x == 0) {
       s_item = (int32_t)atomicAdd(&p.st->work_next, 1u);
-      if (s_item < n_items) s_it = decode_item(s_item, p, rc);
+      if (s_item < n_items) s_it = p.items[s_item];
     }
     __syncthreads();
   }
@@ -647,7 +710,6 @@ __global__ void __launch_bounds__(H16_THREADS, 1) k_hist_u16(Hist16Params P) {
   pdl_wait();     // the level plan
   pdl_trigger();  // the consumer kernel may launch; it waits for this grid to finish
   if (!p.st->plan_ok) return;
-  const int64_t rc = p.st->exact_rows;
   const int32_t n_items = p.st->n_items;
   const int64_t N = p.n_rows;
   const bool ident = (p.rows == nullptr);
@@ -658,13 +720,17 @@ __global__ void __launch_bounds__(H16_THREADS, 1) k_hist_u16(Hist16Params P) {
   const int rho = lane / W, wi = lane % W;
   constexpr int GROUPS_PER_TILE = 32 / TS;
   uint32_t bad = 0;
+  bool first = true;  // the first item by block index, later ones from the counter
 
   for (;;) {
-    if (threadIdx.x == 0) s_item = (int32_t)atomicAdd(&p.st->work_next, 1u);
+    if (threadIdx.x == 0)
+      s_item = first && (int32_t)blockIdx.x < p.first_static ? (int32_t)blockIdx.x
+                                                              : (int32_t)atomicAdd(&p.st->work_next, 1u);
+    first = false;
     __syncthreads();
     const int32_t id = s_item;
     if (id >= n_items) break;
-    const Item it = decode_item(id, p, rc);
+    const Item it = p.items[id];
     {
       uint4 *h4 = reinterpret_cast<uint4 *>(hist);
       const int n4 = (B * TS * 8) / 16;
