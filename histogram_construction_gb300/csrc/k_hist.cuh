@@ -92,10 +92,10 @@ __device__ __forceinline__ int64_t block_incl_scan(int64_t v, int64_t *s_warp) {
 }
 
 // Level plan. With T = target_items / n_fgroups chunks wanted, the base
-// length L is the shortest of 16 candidates from ceil(R / T) up to the closed
-// form ceil(R / max(T - N', ceil(T / 2))) (N' nodes holding rows; it keeps the
-// count within T whenever T >= 2N') whose chunk count
-// sum_n max(1, ceil(rows_n / L)) stays within T. L is at least CHUNK_MIN_ROWS and at
+// length L is the shortest of 16 candidates from ceil(R / T) to
+// ceil(R / ceil(T / 2)) whose chunk count sum_n max(1, ceil(rows_n / L)) stays
+// within T (the longest when none does; the longest keeps the count within T
+// whenever T >= 2 x the nodes holding rows). L is at least CHUNK_MIN_ROWS and at
 // most the int32 exactness bound rc = (2^31 - 1) / max|q| and the chunk cap.
 // So no persistent CTA takes one item more than the others.
 // A node's chunks have equal length ceil(rows_n / c_n) <= L, and its
@@ -110,9 +110,10 @@ constexpr int PLAN_CANDS = 16;  // chunk lengths the plan counts in one pass
 
 // A node of rows_n rows in c equal chunks (ceil(rows_n / c) rows each, the
 // last one shorter): consecutive chunks per exactness group.
-__host__ __device__ __forceinline__ int64_t chunks_per_group(int64_t rows_n, int64_t c, int64_t rc) {
-  const int64_t len = (rows_n + c - 1) / c;
-  return len > 0 ? max((int64_t)1, min(rc / len, (int64_t)0x3fffffff)) : (int64_t)0x3fffffff;
+// (32-bit arithmetic: rows_n, c and rc are below 2^31.)
+__device__ __forceinline__ int64_t chunks_per_group(int64_t rows_n, int64_t c, int64_t rc) {
+  const uint32_t len = ((uint32_t)rows_n + (uint32_t)c - 1) / (uint32_t)c;
+  return len > 0 ? (int64_t)max(1u, min((uint32_t)rc / len, 0x3fffffffu)) : (int64_t)0x3fffffff;
 }
 
 __global__ void __launch_bounds__(PLAN_THREADS) k_level_plan(LevelParams p) {
@@ -124,15 +125,34 @@ __global__ void __launch_bounds__(PLAN_THREADS) k_level_plan(LevelParams p) {
   __shared__ int32_t s_cpre[PLAN_THREADS + 1];  // chunk prefix within the batch
   __shared__ int32_t s_rows[PLAN_THREADS], s_len[PLAN_THREADS], s_cpg[PLAN_THREADS], s_gbase[PLAN_THREADS];
   __shared__ int64_t s_tot[2];
-  __shared__ long long s_chunk, s_rc;
-  __shared__ uint32_t s_cnt[PLAN_CANDS], s_cand[PLAN_CANDS];
-  __shared__ long long s_T;
+  __shared__ uint32_t s_cnt[PLAN_CANDS];
+  __shared__ uint32_t s_qm;
   const int tid = threadIdx.x;
   const bool pub = blockIdx.x == 0;
+  // one read phase: the tree's max|q|, R and every node's offsets
+  uint32_t qm = 1;
+  if (tid == 0) qm = p.qmax_plan ? p.qmax_plan : p.st->qmax;
+  const int64_t R = p.offs[p.n_nodes];
+  // PLAN_CANDS chunk lengths from ceil(R / T) to ceil(R / ceil(T / 2)) (32-bit:
+  // R < 2^31), with T = target_items / n_fgroups chunks wanted
+  const uint32_t T = (uint32_t)max(1, p.target_items / p.n_fgroups);
+  const uint32_t R32 = (R > 0 && R <= p.n_rows) ? (uint32_t)R : 0u;
+  const uint32_t lo = max(1u, (R32 + T - 1) / T), hi = max(lo, (R32 + (T + 1) / 2 - 1) / ((T + 1) / 2));
+  uint32_t cand[PLAN_CANDS], cnt[PLAN_CANDS];
+#pragma unroll
+  for (int k = 0; k < PLAN_CANDS; ++k) {
+    cand[k] = lo + (uint32_t)(((uint64_t)(hi - lo) * k + PLAN_CANDS - 2) / (PLAN_CANDS - 1));
+    cnt[k] = 0;
+  }
+  if (tid < PLAN_CANDS) s_cnt[tid] = 0;
   bool bad = (tid == 0) && (p.offs[0] != 0);
   for (int n = tid; n < p.n_nodes; n += blockDim.x) {
     const int64_t a = p.offs[n], b = p.offs[n + 1];
-    bad |= (a < 0) || (b < a) || (b > p.n_rows);
+    const bool ok = (a >= 0) && (b >= a) && (b <= p.n_rows);
+    bad |= !ok;
+    const uint32_t rows_n = ok ? (uint32_t)(b - a) : 0u;
+#pragma unroll
+    for (int k = 0; k < PLAN_CANDS; ++k) cnt[k] += max(1u, (rows_n + cand[k] - 1) / cand[k]);
   }
   if (__syncthreads_or(bad)) {
     if (pub && tid == 0) {
@@ -143,65 +163,29 @@ __global__ void __launch_bounds__(PLAN_THREADS) k_level_plan(LevelParams p) {
     }
     return;
   }
-  int nonempty = 0;  // N': nodes holding rows
-  for (int base = 0; base < p.n_nodes; base += blockDim.x) {
-    const int n = base + tid;
-    nonempty += __syncthreads_count(n < p.n_nodes && p.offs[n + 1] > p.offs[n]);
-  }
-  // scalars in one thread (64-bit division is a long software sequence)
-  if (tid == 0) {
-    const int64_t R = p.offs[p.n_nodes];
-    const int64_t T = max((int64_t)1, (int64_t)p.target_items / p.n_fgroups);
-    // closed form: at most T chunks whenever T >= 2 N'
-    const int64_t denom = max(T - nonempty, (T + 1) / 2);
-    const int64_t hi = max((int64_t)1, (R + denom - 1) / denom);
-    const int64_t lo = min(hi, max((int64_t)1, (R + T - 1) / T));
-    for (int k = 0; k < PLAN_CANDS; ++k)
-      s_cand[k] = (uint32_t)(lo + ((hi - lo) * k + PLAN_CANDS - 2) / (PLAN_CANDS - 1));
-    s_T = T;
-  }
-  if (tid < PLAN_CANDS) s_cnt[tid] = 0;
-  __syncthreads();
-  {
-    // PLAN_CANDS lengths from ceil(R / T) up to the closed form, counted in
-    // one pass; the shortest whose chunk count sum_n max(1, ceil(rows_n / L))
-    // stays within T wins (the closed form when none does)
-    uint32_t cnt[PLAN_CANDS];
+  // the shortest candidate whose chunk count sum_n max(1, ceil(rows_n / L))
+  // stays within T (the longest when none does)
+  if ((tid & ~31) < p.n_nodes) {  // warps holding nodes (warp-uniform)
 #pragma unroll
-    for (int k = 0; k < PLAN_CANDS; ++k) cnt[k] = 0;
-    for (int n = tid; n < p.n_nodes; n += blockDim.x) {
-      const uint32_t rows_n = (uint32_t)(p.offs[n + 1] - p.offs[n]);
+    for (int k = 0; k < PLAN_CANDS; ++k) {
 #pragma unroll
-      for (int k = 0; k < PLAN_CANDS; ++k) cnt[k] += max(1u, (rows_n + s_cand[k] - 1) / s_cand[k]);
+      for (int o = 16; o > 0; o >>= 1) cnt[k] += __shfl_xor_sync(0xffffffffu, cnt[k], o);
     }
-    if ((tid & ~31) < p.n_nodes) {  // warps holding nodes (warp-uniform)
+    if ((tid & 31) == 0) {
 #pragma unroll
-      for (int k = 0; k < PLAN_CANDS; ++k) {
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) cnt[k] += __shfl_xor_sync(0xffffffffu, cnt[k], o);
-      }
-      if ((tid & 31) == 0) {
-#pragma unroll
-        for (int k = 0; k < PLAN_CANDS; ++k) atomicAdd(&s_cnt[k], cnt[k]);
-      }
+      for (int k = 0; k < PLAN_CANDS; ++k) atomicAdd(&s_cnt[k], cnt[k]);
     }
   }
+  if (tid == 0) s_qm = max(qm, 1u);
   __syncthreads();
-  if (tid == 0) {
-    int64_t len = s_cand[PLAN_CANDS - 1];
-    for (int k = PLAN_CANDS - 1; k >= 0; --k)
-      if ((int64_t)s_cnt[k] <= s_T) len = s_cand[k];
-    const uint32_t qm = max(p.qmax_plan ? p.qmax_plan : p.st->qmax, 1u);
-    const int64_t rc = 2147483647LL / (int64_t)qm;  // rows whose int32 partials cannot overflow
-    int64_t chunk = max(len, (int64_t)CHUNK_MIN_ROWS);
-    chunk = max((int64_t)1, min(rc, chunk));
-    if (p.chunk_cap > 0) chunk = min(chunk, (int64_t)p.chunk_cap);
-    s_chunk = chunk;
-    s_rc = rc;
-  }
-  __syncthreads();
-  const int64_t chunk = s_chunk;
-  const int64_t rc = s_rc;
+  uint32_t len = cand[PLAN_CANDS - 1];
+#pragma unroll
+  for (int k = PLAN_CANDS - 1; k >= 0; --k)
+    if (s_cnt[k] <= T) len = cand[k];
+  const int64_t rc = (int64_t)(0x7fffffffu / s_qm);  // rows whose int32 partials cannot overflow
+  int64_t chunk = max((int64_t)len, (int64_t)CHUNK_MIN_ROWS);
+  chunk = max((int64_t)1, min(rc, chunk));
+  if (p.chunk_cap > 0) chunk = min(chunk, (int64_t)p.chunk_cap);
   const int64_t img_group = (int64_t)p.n_fgroups * p.image_int4s;  // units of one group's images
   int4 *zdst = reinterpret_cast<int4 *>(p.partial);
   int64_t carry_c = 0, carry_g = 0;
@@ -211,7 +195,7 @@ __global__ void __launch_bounds__(PLAN_THREADS) k_level_plan(LevelParams p) {
     if (n < p.n_nodes) {
       a = p.offs[n];
       rows_n = p.offs[n + 1] - a;
-      c = max((int64_t)1, (rows_n + chunk - 1) / chunk);
+      c = max((int64_t)1, (int64_t)(((uint32_t)rows_n + (uint32_t)chunk - 1) / (uint32_t)chunk));
       cpg = chunks_per_group(rows_n, c, rc);
       g = (c + cpg - 1) / cpg;
       if (cpg > 1) m = c / cpg + ((c % cpg) >= 2 ? 1 : 0);  // groups of >= 2 chunks: the first m
