@@ -105,7 +105,7 @@ __device__ __forceinline__ int64_t block_incl_scan(int64_t v, int64_t *s_warp) {
 // are zeroed here first (every block plans redundantly and zeroes a share;
 // block 0 publishes the plan). Offsets that do not start at 0, descend or
 // leave [0, n_rows] invalidate the plan (no items; GBT_ERR_ROW_RANGE).
-constexpr int PLAN_THREADS = 1024;
+constexpr int PLAN_THREADS = 256;  // nodes per planning batch; every block plans redundantly, so keep it small
 constexpr int PLAN_CANDS = 16;  // chunk lengths the plan counts in one pass
 
 // A node of rows_n rows in c equal chunks (ceil(rows_n / c) rows each, the
@@ -212,7 +212,7 @@ __global__ void __launch_bounds__(PLAN_THREADS) k_level_plan(LevelParams p) {
     s_cpre[tid + 1] = (int32_t)ic;
     s_a[tid] = a;
     s_rows[tid] = (int32_t)rows_n;
-    s_len[tid] = (int32_t)((rows_n + c - 1) / max(c, (int64_t)1));
+    s_len[tid] = (int32_t)(((uint32_t)rows_n + (uint32_t)c - 1) / (uint32_t)max(c, (int64_t)1));
     s_cpg[tid] = (int32_t)cpg;
     s_gbase[tid] = (int32_t)(carry_g + ig - g);
     if (tid == 0) {
@@ -225,8 +225,9 @@ __global__ void __launch_bounds__(PLAN_THREADS) k_level_plan(LevelParams p) {
     }
     __syncthreads();
     const int64_t total = s_zpre[blockDim.x];
+    const int last = min(p.n_nodes - base, (int)blockDim.x) - 1;  // the batch's last node
     for (int64_t u = (int64_t)blockIdx.x * blockDim.x + tid; u < total; u += (int64_t)gridDim.x * blockDim.x) {
-      int lo = 0, hi = blockDim.x - 1;  // largest j with s_zpre[j] <= u
+      int lo = 0, hi = last;  // largest j with s_zpre[j] <= u
       while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
         if (s_zpre[mid] <= u) lo = mid; else hi = mid - 1;
@@ -239,7 +240,7 @@ __global__ void __launch_bounds__(PLAN_THREADS) k_level_plan(LevelParams p) {
     for (int64_t u = (int64_t)blockIdx.x * blockDim.x + tid; u < items; u += (int64_t)gridDim.x * blockDim.x) {
       const int32_t kc = (int32_t)(u / nfg);  // chunk within the batch
       const int32_t f = (int32_t)(u - (int64_t)kc * nfg);
-      int lo = 0, hi = blockDim.x - 1;  // largest j with s_cpre[j] <= kc
+      int lo = 0, hi = last;  // largest j with s_cpre[j] <= kc
       while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
         if (s_cpre[mid] <= kc) lo = mid; else hi = mid - 1;
