@@ -347,6 +347,28 @@ struct ScanShared {
 // fixes it at compile time, or -1 takes `mode`.
 __device__ __forceinline__ bool no_missing_rt(longlong2 m) { return m.x == 0 && m.y == 0; }
 
+// Lane partial sums (G, H, |G|) of a strip in global memory, FIN_BATCH loads
+// in flight per lane (a loop that used each load at once would wait for every
+// one of them in turn).
+constexpr int FIN_BATCH = 8;
+__device__ __forceinline__ void strip_totals(const longlong2 *cells, int B, int64_t &tg, int64_t &th, int64_t &sa) {
+  const int lane = threadIdx.x & 31;
+  for (int s0 = lane; s0 < B; s0 += 32 * FIN_BATCH) {
+    longlong2 c[FIN_BATCH];
+#pragma unroll
+    for (int u = 0; u < FIN_BATCH; ++u) {
+      const int s = s0 + 32 * u;
+      c[u] = s < B ? cells[s] : make_longlong2(0, 0);
+    }
+#pragma unroll
+    for (int u = 0; u < FIN_BATCH; ++u) {
+      tg += c[u].x;
+      th += c[u].y;
+      sa += c[u].x < 0 ? -c[u].x : c[u].x;
+    }
+  }
+}
+
 template <int ND, int MODE>
 __device__ __forceinline__ float scan_push_impl(const longlong2 *cells, int n_bins, int64_t tg, int64_t th,
                                                 longlong2 m, float Gf2den, const SplitParams &sp, int f, int node,
@@ -356,6 +378,10 @@ __device__ __forceinline__ float scan_push_impl(const longlong2 *cells, int n_bi
   float run_lo = -INFINITY;
   int64_t carry_g = 0, carry_h = 0;
   for (int c0 = 0; c0 < n_bins; c0 += 32 * SCAN_SPL) {
+    // the next chunk's cells on their way to L1 while this chunk is screened
+    // (strips in global memory: u16 bins)
+    if (c0 + 32 * SCAN_SPL < n_bins && !__isShared(cells))
+      asm volatile("prefetch.global.L1 [%0];" ::"l"(cells + c0 + 32 * SCAN_SPL + SCAN_SPL * lane));
     int64_t pg[SCAN_SPL], ph[SCAN_SPL];
     int64_t ag = 0, ah = 0;
 #pragma unroll
@@ -702,12 +728,16 @@ __global__ void __launch_bounds__(SCAN_THREADS, 3) k_find(const int64_t *__restr
   int64_t tg = 0, th = 0;
   if (f < n_features) {
     int64_t sa = 0;
-    for (int s = lane; s < B; s += 32) {
-      const longlong2 c = __ldg(strip + s);
-      if (staged) sh.cells[warp][s] = c;
-      tg += c.x;
-      th += c.y;
-      sa += c.x < 0 ? -c.x : c.x;
+    if (staged) {
+      for (int s = lane; s < B; s += 32) {
+        const longlong2 c = __ldg(strip + s);
+        sh.cells[warp][s] = c;
+        tg += c.x;
+        th += c.y;
+        sa += c.x < 0 ? -c.x : c.x;
+      }
+    } else {
+      strip_totals(strip, B, tg, th, sa);
     }
     warp_sum3(tg, th, sa);
     __syncwarp();
@@ -832,13 +862,34 @@ __global__ void __launch_bounds__(SCAN_THREADS, 3) k_level_finish(
   // phase B: large = parent - small
   if (active && side == 1) {
     bool neg = false;
-    for (int s = lane; s < B; s += 32) {
-      const longlong2 a = staged ? sh.cells[warp][s] : __ldg(P + s);
-      const longlong2 b = staged ? sh.cells[warp - 4][s] : (FROM_PARTIALS ? __ldcg(Sin + s) : __ldg(Sin + s));
-      const longlong2 d = make_longlong2(a.x - b.x, a.y - b.y);
-      neg |= d.y < 0;
-      L[s] = d;
-      if (staged) sh.cells[warp][s] = d;
+    if (staged) {
+      for (int s = lane; s < B; s += 32) {
+        const longlong2 a = sh.cells[warp][s], b = sh.cells[warp - 4][s];
+        const longlong2 d = make_longlong2(a.x - b.x, a.y - b.y);
+        neg |= d.y < 0;
+        L[s] = d;
+        sh.cells[warp][s] = d;
+      }
+    } else {
+      // FIN_BATCH loads of each operand in flight per lane before the stores
+      for (int s0 = lane; s0 < B; s0 += 32 * FIN_BATCH) {
+        longlong2 a[FIN_BATCH], b[FIN_BATCH];
+#pragma unroll
+        for (int u = 0; u < FIN_BATCH; ++u) {
+          const int s = s0 + 32 * u;
+          a[u] = s < B ? __ldg(P + s) : make_longlong2(0, 0);
+          b[u] = s < B ? (FROM_PARTIALS ? __ldcg(Sin + s) : __ldg(Sin + s)) : make_longlong2(0, 0);
+        }
+#pragma unroll
+        for (int u = 0; u < FIN_BATCH; ++u) {
+          const int s = s0 + 32 * u;
+          if (s < B) {
+            const longlong2 d = make_longlong2(a[u].x - b[u].x, a[u].y - b[u].y);
+            neg |= d.y < 0;
+            L[s] = d;
+          }
+        }
+      }
     }
     if (neg) raise_err(st, ERRBIT_INCONSISTENT);
   }
@@ -848,11 +899,15 @@ __global__ void __launch_bounds__(SCAN_THREADS, 3) k_level_finish(
   int64_t tg = 0, th = 0;
   if (active) {
     int64_t sa = 0;
-    for (int s = lane; s < B; s += 32) {
-      const longlong2 c = cells[s];
-      tg += c.x;
-      th += c.y;
-      sa += c.x < 0 ? -c.x : c.x;
+    if (staged) {
+      for (int s = lane; s < B; s += 32) {
+        const longlong2 c = cells[s];
+        tg += c.x;
+        th += c.y;
+        sa += c.x < 0 ? -c.x : c.x;
+      }
+    } else {
+      strip_totals(cells, B, tg, th, sa);
     }
     warp_sum3(tg, th, sa);
     int ovf = 0;
