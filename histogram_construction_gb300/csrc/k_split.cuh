@@ -463,10 +463,10 @@ __device__ __forceinline__ float warp_scan_push(const longlong2 *cells, int n_bi
   const bool no_missing = (m.x == 0 && m.y == 0);
   const float Gf2den = parent_f32(tg, th, sp);
   const bool fast = strip_fast(sabs, th, Gf2den, sp);
-  // the common case (fast screen, no missing values) gets its own copy
+  // the common cases (fast screen, with or without missing values) get their own copies
   if (fast && no_missing) return scan_push_impl<1, 0>(cells, n_bins, tg, th, m, Gf2den, sp, f, node, sh, overflow, 0);
-  return scan_push_impl<2, -1>(cells, n_bins, tg, th, m, Gf2den, sp, f, node, sh, overflow,
-                               fast ? 0 : (sp.filter ? 1 : 2));
+  if (fast) return scan_push_impl<2, 0>(cells, n_bins, tg, th, m, Gf2den, sp, f, node, sh, overflow, 0);
+  return scan_push_impl<2, -1>(cells, n_bins, tg, th, m, Gf2den, sp, f, node, sh, overflow, sp.filter ? 1 : 2);
 }
 
 __device__ __forceinline__ double surv_gain(int64_t gl, int64_t hl, int64_t tg, int64_t th, const SplitParams &sp) {
