@@ -282,6 +282,49 @@ def test_edge_nodes_empty_single_unsorted(gb, oracle_mod, width):
         assert_splits_equal(s2n(sp), rs)
 
 
+@pytest.mark.parametrize("width", [1, 2])
+@pytest.mark.parametrize("target_items", [None, "7", "1000"])
+def test_many_nodes_and_item_targets(gb, oracle_mod, monkeypatch, width, target_items):
+    """700 nodes (three planning batches of 256), with empty and one-row nodes: the level's histograms,
+    splits and the fused level step. target_items overrides the plan's item target: 7 gives far fewer
+    chunks wanted than nodes, 1000 several items per CTA taken from the counter."""
+    g, Session, s2n = gb
+    if target_items is not None:
+        monkeypatch.setenv("GBT_TARGET_ITEMS", target_items)
+    n_rows = 60_000
+    bins, gp, sentinel = _tiny(width, n_rows=n_rows, n_features=70 if width == 1 else 20, n_bins=50, seed=11)
+    rng = np.random.default_rng(12)
+    sizes = rng.integers(0, 140, size=700)
+    sizes[::37] = 0
+    sizes[5::41] = 1
+    sizes[9] = 4000  # one node larger than a chunk
+    assert sizes.sum() <= n_rows
+    rows = rng.permutation(n_rows)[: int(sizes.sum())].astype(np.int32)
+    offs = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int64)
+    sg, sh = 1024.0, 1000.0
+    q, _ = oracle_mod.quantise(gp, sg, sh)
+    with Session() as s:
+        s.upload_bins(bins, 50, sentinel).begin_tree(gp, sg, sh)
+        h = s.build_level(rows, offs)
+        sp = s.find_splits(h, lam=1.0)
+        assert s.sync() == 0
+        ref, st = oracle_mod.build_hist(bins, 50, sentinel, q, rows, offs)
+        assert st == oracle_mod.OK
+        np.testing.assert_array_equal(h.cpu().numpy(), ref)
+        rs, _ = oracle_mod.find_splits(ref, 50, 1.0, 0.0, 0.0, sg, sh)
+        assert_splits_equal(s2n(sp), rs, "700 nodes")
+        # pairs (2i, 2i + 1): parents hold both children's rows; child 2i is built, 2i + 1 derived
+        hp = s.build_level(rows, offs[::2])
+        small_rows = np.concatenate([rows[offs[2 * i]:offs[2 * i + 1]] for i in range(350)])
+        small_offs = np.concatenate([[0], np.cumsum(sizes[::2])]).astype(np.int64)
+        hs, large, so, lo = s.level_step(small_rows, small_offs, hp, lam=1.0)
+        assert s.sync() == 0
+        np.testing.assert_array_equal(hs.cpu().numpy(), ref[::2], err_msg="level_step small")
+        np.testing.assert_array_equal(large.cpu().numpy(), ref[1::2], err_msg="level_step large")
+        assert_splits_equal(s2n(so), rs[::2], "level_step small splits")
+        assert_splits_equal(s2n(lo), rs[1::2], "level_step large splits")
+
+
 def test_edge_all_rows_one_bin_and_all_missing(gb, oracle_mod):
     g, Session, s2n = gb
     N = 20000
