@@ -728,19 +728,34 @@ __global__ void __launch_bounds__(H16_THREADS, 1) k_hist_u16(Hist16Params P) {
         reinterpret_cast<const unsigned char *>(P.mirror) + mirror_offset(tile, 0, N) + sub * TS * 2 + wi * 4;
     V mg0 = 0, mh0 = 0, mg1 = 0, mh1 = 0;  // missing-slot partials of features 2wi, 2wi+1
     const int64_t step = (int64_t)RPI * nwarps;
-    for (int64_t g0 = it.k0 + RPI * warp; g0 < it.k1; g0 += step * 4) {
-      int32_t rr[4], vg[4], vh[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) load_row(p, ident, g0 + u * step + rho, it.k1, rr[u], vg[u], vh[u], bad);
-      uint32_t bw[4];
+    const int64_t stride = step * 4;  // rows between a warp's consecutive iterations
+    // Iteration j covers rows g0 + j stride + u step + rho (u < 4). Its row ids
+    // are loaded two iterations ahead and its (qg, qh) and bins one iteration
+    // ahead, while iteration j - 1 adds; the loop is unrolled twice so that no
+    // loaded register is copied (a copy would wait for the load). Rows past
+    // the item or invalid add zeros to slot 0, which is never the missing slot.
+    auto rows4 = [&](int64_t gb, int32_t(&R)[4]) {
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
-        bw[u] = 0;
-        if (rr[u] >= 0) bw[u] = __ldg(reinterpret_cast<const uint32_t *>(strip + (int64_t)rr[u] * MIRROR_ROW_BYTES));
+        const int64_t k = gb + u * step + rho;
+        R[u] = k < it.k1 ? (ident ? (int32_t)k : __ldg(p.rows + k)) : -1;
       }
+    };
+    auto gather4 = [&](const int32_t(&R)[4], int32_t(&vg)[4], int32_t(&vh)[4], uint32_t(&bw)[4]) {
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
-        if (rr[u] < 0) continue;
+        const int32_t r = R[u];
+        const bool valid = (uint32_t)r < (uint32_t)N;
+        bad |= (r >= 0 && !valid) ? 1u : 0u;
+        const int2 qv = valid ? __ldg(p.q + r) : make_int2(0, 0);
+        vg[u] = qv.x;
+        vh[u] = qv.y;
+        bw[u] = valid ? __ldg(reinterpret_cast<const uint32_t *>(strip + (int64_t)r * MIRROR_ROW_BYTES)) : 0u;
+      }
+    };
+    auto scatter4 = [&](const int32_t(&vg)[4], const int32_t(&vh)[4], const uint32_t(&bw)[4]) {
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
         const uint32_t s0 = bw[u] & 0xffffu, s1 = bw[u] >> 16;
         const V g = h16_val<FLT>(vg[u]), h = h16_val<FLT>(vh[u]);
         if (s0 == miss_slot) { mg0 += g; mh0 += h; }
@@ -748,6 +763,25 @@ __global__ void __launch_bounds__(H16_THREADS, 1) k_hist_u16(Hist16Params P) {
         if (s1 == miss_slot) { mg1 += g; mh1 += h; }
         else h16_add<FLT>(hist + 2 * (s1 * TS + 2 * wi + 1), g, h);
       }
+    };
+    int64_t g0 = it.k0 + RPI * warp;
+    int32_t ra[4], rb[4], ga[4], ha[4], gb4[4], hb4[4];
+    uint32_t ba[4], bb[4];
+    rows4(g0, ra);
+    rows4(g0 + stride, rb);
+    gather4(ra, ga, ha, ba);
+    rows4(g0 + 2 * stride, ra);
+    for (;;) {
+      if (g0 >= it.k1) break;
+      gather4(rb, gb4, hb4, bb);      // iteration j + 1
+      rows4(g0 + 3 * stride, rb);     // iteration j + 3
+      scatter4(ga, ha, ba);           // iteration j
+      g0 += stride;
+      if (g0 >= it.k1) break;
+      gather4(ra, ga, ha, ba);        // iteration j + 2
+      rows4(g0 + 3 * stride, ra);     // iteration j + 4
+      scatter4(gb4, hb4, bb);         // iteration j + 1
+      g0 += stride;
     }
     // reduce missing partials over lanes sharing wi, add once
 #pragma unroll
