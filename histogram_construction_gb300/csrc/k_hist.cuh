@@ -10,8 +10,11 @@
 //
 // GB300 design (differs from the pages' (feature, node, row-chunk) grid with
 // float shared cells and double global atomics):
-//  * work items (node, 64-feature tile, row chunk) go to a persistent grid
-//    (one 1024-thread CTA per SM) through an atomic counter;
+//  * work items (node, 64-feature tile, row chunk), about one per SM and
+//    decoded by the level plan, go to a persistent grid (one 1024-thread CTA
+//    per SM): the first by block index, later ones through an atomic counter;
+//  * each warp streams its rows' 16-byte strip quarters into a shared ring
+//    with cp.async, two steps ahead of the step whose reductions it issues;
 //  * a CTA holds the tile's histogram as int32 (G, H) pairs in shared memory,
 //    in 16-feature sub-blocks of [256 slots][16 features]; each lane adds
 //    (qg, qh) with two 32-bit shared atomics, and lanes are assigned to
@@ -19,10 +22,11 @@
 //    instruction hit 32 different banks whatever the bin values;
 //  * a chunk never holds more rows than keep every int32 partial exact
 //    (rows * max|q| < 2^31);
-//  * the item's shared image leaves as is with TMA bulk stores (no
-//    transposition, no zeroing of global memory, no global atomics); the
-//    images of a node's chunks are added in int64 afterwards (finalize
-//    kernel, or the fused subtract + split-find kernel).
+//  * the item's shared image leaves as is with TMA bulk stores, or bulk
+//    reduce-adds into a group image the plan zeroed when several chunks of a
+//    node share it (no transposition, no global atomics); the images of a
+//    node's groups are added in int64 afterwards (finalize kernel, or the
+//    fused subtract + split-find kernel).
 #pragma once
 
 #include <type_traits>
@@ -270,24 +274,6 @@ __global__ void __launch_bounds__(PLAN_THREADS) k_level_plan(LevelParams p) {
   }
 }
 
-
-// Loads (row id, qg, qh) of level position k; row -1 marks an invalid row.
-__device__ __forceinline__ void load_row(const LevelParams &p, bool ident, int64_t k, int64_t k1, int32_t &r,
-                                         int32_t &vg, int32_t &vh, uint32_t &bad) {
-  r = -1;
-  vg = 0;
-  vh = 0;
-  if (k >= k1) return;
-  const int32_t rr = ident ? (int32_t)k : __ldg(p.rows + k);
-  if (rr < 0 || rr >= p.n_rows) {
-    bad = 1;
-    return;
-  }
-  const int2 qv = __ldg(p.q + rr);
-  r = rr;
-  vg = qv.x;
-  vh = qv.y;
-}
 
 // ----------------------------------------------------------------------------
 // Float cells [bonsai "10: CUDA histogram backend", "The kernel": shared
