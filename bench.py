@@ -506,6 +506,7 @@ def run_gpu(args, rank, world, local_rank):
     achieved = kernel_bytes / (hk_avg / 1e3) / 1e9 if hk_n else None
     traffic = _profile_traffic(args.workload) if w.width == 1 else None
     step_ms = total_ms / args.steps
+    level_entries = int(lv.offsets[-1]) * w.n_features
     level_gbs = level_bytes / (step_ms / 1e3) / 1e9
     cpu_v, cpu_sample, _ = cpu_oracle_timing(w, budget_s=args.cpu_budget)
     line = {
@@ -527,6 +528,9 @@ def run_gpu(args, rank, world, local_rank):
         "profiled_pass_ms_per_step": sum(ms_prof) / len(ms_prof),
         "warm_l2": {"ms_per_step": sum(ms_warm) / len(ms_warm),
                     "value": world * entries / (sum(ms_warm) / len(ms_warm) / 1e3)},
+        # every row of the level (built and derived siblings) x F over the same step time
+        "effective": {"entries_per_step": level_entries,
+                      "value": world * level_entries / (step_ms / 1e3)},
         "e2e": e2e,
         "gpu_launches": int(launches),
         "clocks": clk,
