@@ -511,7 +511,8 @@ def run_gpu(args, rank, world, local_rank):
     cpu_v, cpu_sample, _ = cpu_oracle_timing(w, budget_s=args.cpu_budget)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
+        "warmup": args.warmup, "ms_per_step": step_ms, "median_ms_per_step": statistics.median(ms),
+        "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "int64", "data": "synthetic",
         "config": {"workload": WORKLOAD_TEXT[args.workload], "rows_built": R, "features": w.n_features,
                    "bin_bytes": w.width, "slots_per_feature": B, "nodes_built": n_b, "nodes_derived": n_p,
