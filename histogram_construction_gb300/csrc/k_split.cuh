@@ -380,8 +380,9 @@ __device__ __forceinline__ float scan_push_impl(const longlong2 *cells, int n_bi
   for (int c0 = 0; c0 < n_bins; c0 += 32 * SCAN_SPL) {
     // the next chunk's cells on their way to L1 while this chunk is screened
     // (strips in global memory: u16 bins)
+    // (clamped to the strip's missing slot: the address stays inside the strip)
     if (c0 + 32 * SCAN_SPL < n_bins && !__isShared(cells))
-      asm volatile("prefetch.global.L1 [%0];" ::"l"(cells + c0 + 32 * SCAN_SPL + SCAN_SPL * lane));
+      asm volatile("prefetch.global.L1 [%0];" ::"l"(cells + min(c0 + 32 * SCAN_SPL + SCAN_SPL * lane, n_bins)));
     int64_t pg[SCAN_SPL], ph[SCAN_SPL];
     int64_t ag = 0, ah = 0;
 #pragma unroll
