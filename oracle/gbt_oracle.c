@@ -35,8 +35,9 @@
  * Readings where the pages leave a step open (each is also listed in the
  * design notes):
  *  R1 cells are int64 fixed point: q = round-half-even(x * s) of the float32
- *     product, |q| <= 2^21 - 1 per row (a design limit that lets any 1024 rows
- *     be summed exactly in 32 bits), cell = exact int64 sum.
+ *     product, an error unless |x * s| < 2^31 (so q fits the 32 bits per
+ *     component that the pages' packed atomics give each of g and h), cell =
+ *     exact int64 sum (no overflow: fewer than 2^31 rows of |q| < 2^31).
  *  R2 slot(b) = b for a real bin b < n_bins, slot(sentinel) = n_bins (the
  *     missing slot); any other value is an error.
  *  R3 a cut t in [0, n_bins-1] sends slots <= t left; missing goes wholly left
@@ -92,14 +93,12 @@ typedef struct {
   int64_t g_left, h_left, g_right, h_right;
 } oracle_split;
 
-#define OR_QMAX 2097151LL /* 2^21 - 1 */
-
 /* [P4 s7], [P2 "The idea"]: quantise one float to fixed point, R1. */
 static int quantise_one(float x, float s, int32_t *q) {
   float p = x * s; /* one IEEE float32 multiply, round to nearest even */
-  if (!(fabsf(p) < 2097152.0f)) return OR_ERR_QUANT; /* |p| < 2^21; also catches NaN/inf */
+  if (!(fabsf(p) < 2147483648.0f)) return OR_ERR_QUANT; /* |p| < 2^31; also catches NaN/inf */
   long long r = llrintf(p); /* current mode: round to nearest, ties to even */
-  if (r < -OR_QMAX || r > OR_QMAX) return OR_ERR_QUANT;
+  if (r <= -2147483648LL || r >= 2147483648LL) return OR_ERR_QUANT;
   *q = (int32_t)r;
   return OR_OK;
 }

@@ -27,9 +27,10 @@ def _load(name):
     [
         (0.5, 1.0, 0), (1.5, 1.0, 2), (2.5, 1.0, 2), (-0.5, 1.0, 0), (-1.5, 1.0, -2), (-2.5, 1.0, -2),
         (3.25, 4.0, 13), (0.1, 1024.0, 102), (-0.1, 1024.0, -102),
-        (2097151.0, 1.0, 2097151),  # largest admissible |q| = 2^21 - 1
-        (-2097151.0, 1.0, -2097151),
-        (2097151.25, 1.0, 2097151),  # rounds down to the limit
+        (2147483520.0, 1.0, 2147483520),  # largest float32 below 2^31
+        (-2147483520.0, 1.0, -2147483520),
+        (2097151.25, 1.0, 2097151),
+        (16777215.0, 1.0, 16777215),  # beyond the library's per-row limit, inside the definition's domain
     ],
 )
 def test_quantise_round_half_even(oracle_mod, x, s, q):
@@ -40,9 +41,10 @@ def test_quantise_round_half_even(oracle_mod, x, s, q):
     assert out[0, 0] == q and out[0, 1] == q
 
 
-@pytest.mark.parametrize("x", [2097152.0, -2097152.0, 2097151.75, float("inf"), float("nan"), 3.0e9])
+@pytest.mark.parametrize("x", [2147483648.0, -2147483648.0, float("inf"), float("nan"), 3.0e9])
 def test_quantise_overflow_is_an_error(oracle_mod, x):
-    """|q| must stay within 2^21 - 1 (2097151.75 rounds to 2^21: out of range)."""
+    """|x * s| must stay below 2^31: q is one 32-bit half of the pages' packed (g, h) word ('GBDT engine
+    engineering deep-dive', section 7)."""
     _, st = oracle_mod.quantise(np.array([[x, 0.0]], np.float32), 1.0, 1.0)
     assert st == oracle_mod.ERR_QUANT
 
@@ -75,14 +77,16 @@ def _brute_hist(bins, n_bins, sentinel, q, rows, offs):
 
 @pytest.mark.parametrize("width", [1, 2])
 @pytest.mark.parametrize("seed", [0, 1, 2])
-def test_build_matches_brute_force(oracle_mod, width, seed):
+@pytest.mark.parametrize("qmag", [1000, 2 ** 31 - 1])
+def test_build_matches_brute_force(oracle_mod, width, seed, qmag):
+    """qmag 2^31 - 1: every per-row value of the definition's domain; int64 cells stay exact."""
     rng = np.random.default_rng(100 + seed)
     N, F, n_bins = 64, 4, 8
     sentinel = 0xFF if width == 1 else 0xFFFF
     dt = np.uint8 if width == 1 else np.uint16
     bins = rng.integers(0, n_bins, size=(F, N)).astype(dt)
     bins[rng.random((F, N)) < 0.2] = sentinel
-    q = rng.integers(-1000, 1000, size=(N, 2)).astype(np.int32)
+    q = rng.integers(-qmag, qmag + 1, size=(N, 2)).astype(np.int32)
     perm = rng.permutation(N).astype(np.int32)
     rows = perm[:50]
     offs = np.array([0, 7, 7, 30, 50], np.int64)  # includes an empty node
@@ -128,6 +132,8 @@ def test_build_reports_bad_bin_and_row(oracle_mod):
     _, st = oracle_mod.build_hist(bins, 4, 0xFF, q, None, np.array([0, 3]))
     assert st == oracle_mod.ERR_BIN
     _, st = oracle_mod.build_hist(bins[:, :2], 4, 0xFF, q[:2], np.array([0, 5], np.int32), np.array([0, 2]))
+    assert st == oracle_mod.ERR_ROW
+    _, st = oracle_mod.build_hist(bins[:, :2], 4, 0xFF, q[:2], np.array([-5, 1], np.int32), np.array([0, 2]))
     assert st == oracle_mod.ERR_ROW
 
 
