@@ -154,9 +154,8 @@ def entries_and_bytes(w, lv, B):
 
 
 def scales_for(w):
-    import histogram_construction_gb300 as g
-    _, sg, sh = g.gbt_suggest_scales(0, float(np.abs(w.gpair[:, 0]).max()), float(np.abs(w.gpair[:, 1]).max()))
-    return sg, sh
+    """The workload's fixed-point scales (equal to gbt_suggest_scales on the same data; tests/test_abi.py)."""
+    return synth.fixed_point_scales(w.gpair)
 
 
 # ----------------------------------------------------------------------------- CPU oracle leg

@@ -27,6 +27,7 @@ each of its rows goes left with probability p; children of node i are 2i
 """
 from __future__ import annotations
 
+import math
 from dataclasses import dataclass, field
 
 import numpy as np
@@ -107,6 +108,26 @@ def gpair(rng, n_rows, h="u0.1"):
     else:
         out[:, 1] = np.float32(float(h[1:]))
     return out
+
+
+def fixed_point_scales(gpair_arr, rows_per_partial=65536):
+    """The fixed-point scales a workload is run with (an input of the method, chosen from the data):
+    for g and h, the largest power of two s with max|x| * s * rows_per_partial <= 2^31 - 1 (1.0 when
+    max|x| = 0), clamped to [2^-126, 2^126]."""
+    lim = (2 ** 31 - 1) / float(rows_per_partial)
+    out = []
+    for c in range(2):
+        m = float(np.abs(np.asarray(gpair_arr, dtype=np.float32)[..., c]).max()) if np.size(gpair_arr) else 0.0
+        if m == 0.0:
+            out.append(1.0)
+            continue
+        e = max(-126, min(126, math.floor(math.log2(lim / m))))
+        while e > -126 and m * 2.0 ** e > lim:
+            e -= 1
+        while e < 126 and m * 2.0 ** (e + 1) <= lim:
+            e += 1
+        out.append(2.0 ** e)
+    return out[0], out[1]
 
 
 def gpair_multi(name: str, n_rows, k, h="u0.1"):

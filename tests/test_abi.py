@@ -47,6 +47,23 @@ def test_suggest_scales_is_largest_power_of_two_within_bound(rows, mg, mh):
         assert m * (2 * s) * r > 2 ** 31 - 1
 
 
+@pytest.mark.parametrize("name", ["root", "level5", "u16miss"])
+def test_workload_scales_equal_the_library_suggestion(name):
+    """The benchmark and tests run every workload with synth.fixed_point_scales (so its CPU legs never
+    load the library); that is exactly what gbt_suggest_scales returns for the same data."""
+    import numpy as np
+
+    import histogram_construction_gb300 as g
+    import synth
+    rng = np.random.default_rng(7)
+    for gp in (synth.make(name, n_rows=5000, n_features=3).gpair,
+               (rng.standard_normal((100, 2)) * [1e-3, 7e4]).astype(np.float32),
+               np.zeros((4, 2), np.float32)):
+        st, sg, sh = g.gbt_suggest_scales(0, float(np.abs(gp[:, 0]).max()), float(np.abs(gp[:, 1]).max()))
+        assert st == 0
+        assert synth.fixed_point_scales(gp) == (sg, sh)
+
+
 def test_suggest_scales_rejects_bad_input():
     import histogram_construction_gb300 as g
     assert g.gbt_suggest_scales(0, float("nan"), 1.0)[0] == g.GBT_ERR_INVALID_ARG
