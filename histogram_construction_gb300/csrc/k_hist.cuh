@@ -378,15 +378,19 @@ __device__ __forceinline__ void h8_rows(const LevelParams &p, bool ident, int64_
 }
 
 // q of row r: lv.q[r] (one target), or target tsel of lv.q[r][k] (multi-output;
-// lanes of targets past k load nothing, lane_on false).
+// lanes of targets past k load nothing, lane_on false). Rows rid[u] sit at
+// level positions kb + u * step; a position before k1 whose id is outside
+// [0, n_rows) is a caller error (negative ids included), positions past k1
+// are the loop's padding.
 template <int U, bool MULTI>
 __device__ __forceinline__ void h8_gather(const LevelParams &p, const unsigned char *strip, bool lane_on, int par,
-                                          const int32_t (&rid)[U], H8Stage<U> &st, uint32_t &bad, int k, int tsel) {
+                                          const int32_t (&rid)[U], int64_t kb, int64_t step, int64_t k1,
+                                          H8Stage<U> &st, uint32_t &bad, int k, int tsel) {
 #pragma unroll
   for (int u = 0; u < U; ++u) {
     const int32_t r = rid[u];
     const bool valid = (uint32_t)r < (uint32_t)p.n_rows;
-    bad |= (r >= 0 && !valid) ? 1u : 0u;
+    bad |= (kb + u * step < k1 && !valid) ? 1u : 0u;
     int2 qv = make_int2(0, 0);
     if (MULTI) {
       if (valid && lane_on) qv = __ldg(p.q + (int64_t)r * k + tsel);
@@ -405,13 +409,13 @@ __device__ __forceinline__ void h8_gather(const LevelParams &p, const unsigned c
 // come to registers, as loaded (the component order is chosen at use).
 template <int U, bool MULTI>
 __device__ __forceinline__ void h8_issue(const LevelParams &p, const unsigned char *strip, bool lane_on,
-                                         const int32_t (&rid)[U], uint32_t ring_dst, int2 (&qv)[U], uint32_t &bad,
-                                         int k, int tsel) {
+                                         const int32_t (&rid)[U], int64_t kb, int64_t step, int64_t k1,
+                                         uint32_t ring_dst, int2 (&qv)[U], uint32_t &bad, int k, int tsel) {
 #pragma unroll
   for (int u = 0; u < U; ++u) {
     const int32_t r = rid[u];
     const bool valid = (uint32_t)r < (uint32_t)p.n_rows;
-    bad |= (r >= 0 && !valid) ? 1u : 0u;
+    bad |= (kb + u * step < k1 && !valid) ? 1u : 0u;
     const bool ld = valid && lane_on;
     if (MULTI) {
       qv[u] = ld ? __ldg(p.q + (int64_t)r * k + tsel) : make_int2(0, 0);
@@ -542,9 +546,10 @@ __global__ void __launch_bounds__(H8_THREADS, 1) k_hist_u8(Hist8Params P) {
       h8_rows<U>(p, ident, g0, step, it.k1, xa);
       h8_rows<U>(p, ident, g0 + adv, step, it.k1, xb);
       h8_rows<U>(p, ident, g0 + 2 * adv, step, it.k1, xc);
-      h8_issue<U, MULTI>(p, strip, lane_on, xa, ring_lane, qa, bad, P.n_targets, tsel);
+      h8_issue<U, MULTI>(p, strip, lane_on, xa, g0, step, it.k1, ring_lane, qa, bad, P.n_targets, tsel);
       cp_async_commit();
-      h8_issue<U, MULTI>(p, strip, lane_on, xb, ring_lane + ring_stage, qb, bad, P.n_targets, tsel);
+      h8_issue<U, MULTI>(p, strip, lane_on, xb, g0 + adv, step, it.k1, ring_lane + ring_stage, qb, bad, P.n_targets,
+                         tsel);
       cp_async_commit();
       h8_rows<U>(p, ident, g0 + 3 * adv, step, it.k1, xa);
       h8_rows<U>(p, ident, g0 + 4 * adv, step, it.k1, xb);
@@ -555,7 +560,8 @@ __global__ void __launch_bounds__(H8_THREADS, 1) k_hist_u8(Hist8Params P) {
                           int32_t(&xnew)[U]) -> bool {
         if (!__any_sync(0xffffffffu, g0 < it.k1)) return false;
         if (__any_sync(0xffffffffu, g0 + 2 * adv < it.k1)) {
-          h8_issue<U, MULTI>(p, strip, lane_on, xnew, ring_lane + nxt2 * ring_stage, qnew, bad, P.n_targets, tsel);
+          h8_issue<U, MULTI>(p, strip, lane_on, xnew, g0 + 2 * adv, step, it.k1, ring_lane + nxt2 * ring_stage, qnew,
+                             bad, P.n_targets, tsel);
           h8_rows<U>(p, ident, g0 + 5 * adv, step, it.k1, xnew);
         }
         cp_async_commit();   // possibly empty: one group per step keeps the count
@@ -580,14 +586,14 @@ __global__ void __launch_bounds__(H8_THREADS, 1) k_hist_u8(Hist8Params P) {
     } else {
       H8Stage<U> cur, nxt;
       h8_rows<U>(p, ident, g0, step, it.k1, rid);
-      h8_gather<U, MULTI>(p, strip, lane_on, par, rid, cur, bad, P.n_targets, tsel);
+      h8_gather<U, MULTI>(p, strip, lane_on, par, rid, g0, step, it.k1, cur, bad, P.n_targets, tsel);
       h8_rows<U>(p, ident, g0 + adv, step, it.k1, rid);
       h8_zero_image(smem, nsb, B);
       // lanes of a warp run out of rows within one group of each other; any
       // lane with work keeps the warp going (the others add zeros)
       while (__any_sync(0xffffffffu, g0 < it.k1)) {
         if (__any_sync(0xffffffffu, g0 + adv < it.k1)) {
-          h8_gather<U, MULTI>(p, strip, lane_on, par, rid, nxt, bad, P.n_targets, tsel);
+          h8_gather<U, MULTI>(p, strip, lane_on, par, rid, g0 + adv, step, it.k1, nxt, bad, P.n_targets, tsel);
           h8_rows<U>(p, ident, g0 + 2 * adv, step, it.k1, rid);
         }
         h8_scatter<U, FLT>(cur, sel, cj);
@@ -727,12 +733,15 @@ __global__ void __launch_bounds__(H16_THREADS, 1) k_hist_u16(Hist16Params P) {
         R[u] = k < it.k1 ? (ident ? (int32_t)k : __ldg(p.rows + k)) : -1;
       }
     };
-    auto gather4 = [&](const int32_t(&R)[4], int32_t(&vg)[4], int32_t(&vh)[4], uint32_t(&bw)[4]) {
+    // rows R[u] sit at level positions gb + u * step + rho: an id outside [0, N)
+    // at a position before the item's end is a caller error (negative ids
+    // included); positions past the end are the loop's padding
+    auto gather4 = [&](const int32_t(&R)[4], int64_t gb, int32_t(&vg)[4], int32_t(&vh)[4], uint32_t(&bw)[4]) {
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const int32_t r = R[u];
         const bool valid = (uint32_t)r < (uint32_t)N;
-        bad |= (r >= 0 && !valid) ? 1u : 0u;
+        bad |= (gb + u * step + rho < it.k1 && !valid) ? 1u : 0u;
         const int2 qv = valid ? __ldg(p.q + r) : make_int2(0, 0);
         vg[u] = qv.x;
         vh[u] = qv.y;
@@ -755,16 +764,16 @@ __global__ void __launch_bounds__(H16_THREADS, 1) k_hist_u16(Hist16Params P) {
     uint32_t ba[4], bb[4];
     rows4(g0, ra);
     rows4(g0 + stride, rb);
-    gather4(ra, ga, ha, ba);
+    gather4(ra, g0, ga, ha, ba);
     rows4(g0 + 2 * stride, ra);
     for (;;) {
       if (g0 >= it.k1) break;
-      gather4(rb, gb4, hb4, bb);      // iteration j + 1
-      rows4(g0 + 3 * stride, rb);     // iteration j + 3
-      scatter4(ga, ha, ba);           // iteration j
+      gather4(rb, g0 + stride, gb4, hb4, bb);  // iteration j + 1
+      rows4(g0 + 3 * stride, rb);              // iteration j + 3
+      scatter4(ga, ha, ba);                    // iteration j
       g0 += stride;
       if (g0 >= it.k1) break;
-      gather4(ra, ga, ha, ba);        // iteration j + 2
+      gather4(ra, g0 + stride, ga, ha, ba);    // iteration j + 2
       rows4(g0 + 3 * stride, ra);     // iteration j + 4
       scatter4(gb4, hb4, bb);         // iteration j + 1
       g0 += stride;

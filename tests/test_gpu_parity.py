@@ -362,9 +362,40 @@ def test_edge_quantisation_limit_forces_minimum_chunks(gb, oracle_mod):
         ref, _ = oracle_mod.build_hist(bins, 40, sentinel, q, None, offs)
         np.testing.assert_array_equal(h.cpu().numpy(), ref)
         bad = gp.copy()
-        bad[3, 0] = 1.5  # 1.5 * (2^21 - 1) is beyond the limit
+        bad[3, 0] = 1.5  # 1.5 * (2^21 - 1): inside the definition's domain, beyond the library's per-row limit
+        qb, st = oracle_mod.quantise(bad, scale, 1.0e6)
+        assert st == oracle_mod.OK and oracle_mod.max_abs_q(qb) > 2097151
+        ref_b, st = oracle_mod.build_hist(bins, 40, sentinel, qb, None, offs)
+        assert st == oracle_mod.OK
         assert g.gbt_begin_tree(s.ctx, bad, scale, 1.0e6) == 0
         assert s.sync() == g.GBT_ERR_QUANT_OVERFLOW
+
+
+@pytest.mark.parametrize("qbig", [2 ** 21, 2 ** 24 + 2, 2 ** 31 - 128])
+def test_library_refuses_what_the_oracle_accepts(gb, oracle_mod, qbig):
+    """|q| in [2^21, 2^31): the definition's domain, beyond the library's documented per-row limit. The
+    oracle builds the histogram; the library reports GBT_ERR_QUANT_OVERFLOW at sync, and its level calls
+    then build nothing that could be mistaken for a result."""
+    g, Session, s2n = gb
+    bins, gp, sentinel = _tiny(1, n_rows=3000, n_features=9, n_bins=30)
+    gp[:, 0] = np.clip(gp[:, 0], -1.0, 1.0)
+    gp[17, 0] = float(qbig)
+    q, st = oracle_mod.quantise(gp, 1.0, 1.0e4)
+    assert st == oracle_mod.OK and oracle_mod.max_abs_q(q) == qbig
+    offs = np.array([0, 3000], np.int64)
+    ref, st = oracle_mod.build_hist(bins, 30, sentinel, q, None, offs)
+    assert st == oracle_mod.OK and ref[0, :, :, 0].sum(axis=1).max() >= qbig - 3000
+    with Session() as s:
+        s.upload_bins(bins, 30, sentinel)
+        assert g.gbt_begin_tree(s.ctx, gp, 1.0, 1.0e4) == 0
+        assert s.sync() == g.GBT_ERR_QUANT_OVERFLOW
+        assert s.sync() == 0  # the word was cleared; the context stays usable
+        s.begin_tree(np.clip(gp, -1.0, 1.0), 1.0, 1.0e4)
+        h = s.build_level(None, offs)
+        assert s.sync() == 0
+        q2, _ = oracle_mod.quantise(np.clip(gp, -1.0, 1.0), 1.0, 1.0e4)
+        ref2, _ = oracle_mod.build_hist(bins, 30, sentinel, q2, None, offs)
+        np.testing.assert_array_equal(h.cpu().numpy(), ref2)
 
 
 def test_determinism_bytes_identical(gb):
@@ -430,6 +461,42 @@ def test_error_bad_row_and_quant(gb):
         assert s.sync() == g.GBT_ERR_ROW_RANGE
         # host offsets are validated synchronously
         assert g.gbt_build_level(s.ctx, rows, np.array([0, 5, 3], np.int64), 2, s.hist_tensor(2)) == g.GBT_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("width", [1, 2])
+@pytest.mark.parametrize("bad_row", [-5, -1, -2 ** 31, 5000])
+def test_error_row_outside_range_any_sign(gb, oracle_mod, width, bad_row):
+    """A row id outside [0, n_rows), negative ones included, is GBT_ERR_ROW_RANGE at gbt_sync, as the
+    oracle reports its row error, through gbt_build_level and gbt_level_step, wherever the id sits in its
+    node (first row, last row of a ragged chunk)."""
+    g, Session, s2n = gb
+    bins, gp, sentinel = _tiny(width, n_rows=5000, n_features=70 if width == 1 else 20, n_bins=40, seed=4)
+    rng = np.random.default_rng(5)
+    rows = rng.permutation(5000)[:3001].astype(np.int32)
+    offs = np.array([0, 1200, 3001], np.int64)
+    q, _ = oracle_mod.quantise(gp, 1024.0, 1024.0)
+    for pos in (0, 1199, 3000):
+        bad = rows.copy()
+        bad[pos] = bad_row
+        _, st = oracle_mod.build_hist(bins, 40, sentinel, q, bad, offs)
+        assert st == oracle_mod.ERR_ROW
+        with Session() as s:
+            s.upload_bins(bins, 40, sentinel).begin_tree(gp, 1024.0, 1024.0)
+            hp = s.build_level(None, np.array([0, 2500, 5000], np.int64))
+            assert s.sync() == 0
+            assert g.gbt_build_level(s.ctx, torch.from_numpy(bad).cuda(), torch.from_numpy(offs).cuda(), 2,
+                                     s.hist_tensor(2)) == 0
+            assert s.sync() == g.GBT_ERR_ROW_RANGE, (pos, "build")
+            hs, large = s.hist_tensor(2), s.hist_tensor(2)
+            so = torch.empty((2, g.SPLIT_BYTES), dtype=torch.uint8, device="cuda")
+            lo = torch.empty_like(so)
+            assert g.gbt_level_step(s.ctx, torch.from_numpy(bad).cuda(), torch.from_numpy(offs).cuda(), 2, hp, None,
+                                    hs, large, g.params(1.0, 0.0, 0.0), so, lo) == 0
+            assert s.sync() == g.GBT_ERR_ROW_RANGE, (pos, "level step")
+            # and the same call on valid rows is clean
+            assert g.gbt_build_level(s.ctx, torch.from_numpy(rows).cuda(), torch.from_numpy(offs).cuda(), 2,
+                                     s.hist_tensor(2)) == 0
+            assert s.sync() == 0
 
 
 def test_error_inconsistent_subtraction(gb):
