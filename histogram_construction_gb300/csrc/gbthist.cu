@@ -1,5 +1,6 @@
 // gbthist C-ABI: context, uploads, level build, subtraction, split find and
 // row partition on one GB300 (sm_103a). See include/gbthist.h for the contract.
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 #include <math.h>
@@ -1230,7 +1231,37 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[NOALLOC_BYTES];
 
 namespace {
 std::mutex g_noalloc_mu;
-void *g_noalloc_addr[NOALLOC_MAX_DEVICES] = {};  // device address of g_noalloc_scratch per device, once known
+// Device address of g_noalloc_scratch per device, with the id of the context it was taken in: a context
+// destroyed and created again (cudaDeviceReset, or the caller switching contexts) loads the module
+// again, so the address is looked up again whenever the current context's id differs.
+void *g_noalloc_addr[NOALLOC_MAX_DEVICES] = {};
+unsigned long long g_noalloc_ctx[NOALLOC_MAX_DEVICES] = {};
+
+// The calling thread's current context's process-unique id, or 0 when it cannot be read. The two
+// driver entry points are looked up through the runtime, so the library links no driver library.
+unsigned long long current_ctx_id() {
+  static std::once_flag once;
+  static CUresult (*get_current)(CUcontext *) = nullptr;
+  static CUresult (*get_id)(CUcontext, unsigned long long *) = nullptr;
+  std::call_once(once, [] {
+    void *f = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<CUresult (*)(CUcontext *)>(f);
+    f = nullptr;
+    q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<CUresult (*)(CUcontext, unsigned long long *)>(f);
+    cudaGetLastError();
+  });
+  if (!get_current || !get_id) return 0;
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (get_current(&ctx) != CUDA_SUCCESS || !ctx || get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
 }  // namespace
 
 extern "C" {
@@ -1251,7 +1282,8 @@ gbt_status gbt_find_splits_noalloc(const int64_t *hist, int32_t n_nodes, int32_t
   void *scratch = nullptr;
   {
     std::lock_guard<std::mutex> lock(g_noalloc_mu);
-    if (!g_noalloc_addr[dev]) {
+    const unsigned long long ctx_id = current_ctx_id();
+    if (!g_noalloc_addr[dev] || ctx_id == 0 || ctx_id != g_noalloc_ctx[dev]) {
       void *p = nullptr;
       const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
       if (e != cudaSuccess || !p) {
@@ -1259,6 +1291,7 @@ gbt_status gbt_find_splits_noalloc(const int64_t *hist, int32_t n_nodes, int32_t
         return GBT_ERR_CUDA;
       }
       g_noalloc_addr[dev] = p;
+      g_noalloc_ctx[dev] = current_ctx_id();  // the lookup may have made the primary context current
     }
     scratch = g_noalloc_addr[dev];
   }

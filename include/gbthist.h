@@ -43,7 +43,7 @@ typedef enum {
   GBT_ERR_CUDA = 4,           /* a CUDA runtime call failed; gbt_last_error has the text */
   GBT_ERR_BIN_RANGE = 5,      /* device: a bin value was neither < n_bins nor the sentinel */
   GBT_ERR_ROW_RANGE = 6,      /* device: a row index was outside [0, n_rows), or offsets not ascending */
-  GBT_ERR_QUANT_OVERFLOW = 7, /* device: a quantised value outside [-(2^21-1), 2^21-1], or not finite */
+  GBT_ERR_QUANT_OVERFLOW = 7, /* device: a quantised value beyond this library's limit |q| <= 2^21-1, or not finite */
   GBT_ERR_UNSUPPORTED = 8,    /* a size beyond this build's limits */
   GBT_ERR_TIMEOUT = 9,        /* device: a bounded wait ran out */
   GBT_ERR_INCONSISTENT = 10   /* device: subtraction produced a negative hessian cell */
@@ -116,10 +116,13 @@ gbt_status gbt_upload_bins(gbt_ctx *ctx, const void *bins, int bin_bytes, int64_
  * deep-dive", section 7: gradients are quantised to fixed point for integer
  * atomics].
  *   gpair: host or device, packed float32 (g, h) pairs [n_rows][2].
- *   scale_g, scale_h: fixed-point scales; q = round-half-even(float32(x * s)),
- *     |q| <= 2^21 - 1 (else GBT_ERR_QUANT_OVERFLOW on the device word). The
- *     limit lets the kernels sum any 1024 rows exactly in 32-bit partials;
- *     histogram cells are exact int64 sums.
+ *   scale_g, scale_h: fixed-point scales; q = round-half-even(float32(x * s)).
+ *     The definition admits any q with |x * s| < 2^31 (one 32-bit half of
+ *     the page's packed (g, h) word); this library accepts |q| <= 2^21 - 1
+ *     per row and reports GBT_ERR_QUANT_OVERFLOW on the device word for
+ *     larger (or non-finite) values. That limit is the kernels' own: it lets
+ *     them sum any 1024 rows exactly in 32-bit shared-memory partials.
+ *     Histogram cells are exact int64 sums.
  * Read only during the call's stream work. The call also brings max|q| back
  * to the host (asynchronously) to size the build's scratch. */
 gbt_status gbt_begin_tree(gbt_ctx *ctx, const float *gpair, float scale_g, float scale_h);
@@ -252,7 +255,11 @@ gbt_status gbt_find_level_split(gbt_ctx *ctx, const int64_t *hist, int32_t n_nod
  * n_nodes <= 4096 and n_nodes * ceil(n_features / 8) <= 32768; beyond them
  * the call returns GBT_ERR_UNSUPPORTED before touching the device. The first
  * call on each device looks up that array's device address (make it before
- * any stream capture). Every call uses the same array and clears only its
+ * any stream capture); the address is looked up again when the calling
+ * thread's current context is another one than at the last lookup, e.g.
+ * after cudaDeviceReset created the device's primary context anew (make the
+ * first call after such a change outside stream capture too). Every call uses
+ * the same array and clears only its
  * arrival counters: calls whose work overlaps on the GPU (other streams,
  * other threads) race on it, so order them on one stream or synchronise.
  * Errors: GBT_ERR_INVALID_ARG (NULL, bad sizes or scales, host or misaligned

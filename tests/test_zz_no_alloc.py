@@ -1,11 +1,10 @@
-"""The allocation-free split find against the context's split find.
+"""The allocation-free split find, against the oracle and against the context's split find.
 
-Some callers cannot allocate device memory. One example is a host application
-that hands out all device memory from its own pool. Another is code that keeps
-work stream-ordered, where a cudaMalloc would synchronise the device.
-gbt_find_splits_noalloc serves them: its scratch is a fixed array inside the
-library. This file is collected last, so a failure here cannot hide another
-GPU test from a run that stops at the first failure.
+Some callers cannot allocate device memory. One example is a host application that hands out all device
+memory from its own pool. Another is code that keeps work stream-ordered, where a cudaMalloc would
+synchronise the device. gbt_find_splits_noalloc serves them: its scratch is a fixed array inside the
+library. This file is collected last, so a failure here cannot hide another GPU test from a run that
+stops at the first failure.
 """
 import numpy as np
 import pytest
@@ -28,44 +27,79 @@ def _same(a, b, where):
     np.testing.assert_array_equal(a["gain"].view(np.int64), b["gain"].view(np.int64), err_msg=f"{where} gain")
 
 
-def test_noalloc_matches_context_find_two_calls_in_a_row():
+def _oracle_hists(oracle, w, depths, sg, sh):
+    """The oracle's own histograms of the given levels (inputs that never pass through the library)."""
+    q, st = oracle.quantise(w.gpair, sg, sh)
+    assert st == oracle.OK
+    out = []
+    for d in depths:
+        lv = w.levels[d]
+        h, st = oracle.build_hist(w.bins, w.n_bins, w.sentinel, q, lv.rows, lv.offsets)
+        assert st == oracle.OK
+        out.append(h)
+    return out
+
+
+@pytest.mark.parametrize("name,n_rows,n_features,depths", [
+    ("level5", 30_000, 70, (2, 3)),     # u8: 256 slots, strips staged in shared memory
+    ("u16miss", 20_000, 11, (3, 2)),    # u16: 4097 slots with 40% missing, strips read from global memory
+])
+def test_noalloc_matches_oracle_and_context_find_two_calls_in_a_row(oracle_mod, name, n_rows, n_features, depths):
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     import histogram_construction_gb300 as g
     from histogram_construction_gb300.session import Session
 
-    w = synth.make("level5", n_rows=30_000, n_features=70, depth=3)
-    mg = float(np.abs(w.gpair[:, 0]).max())
-    mh = float(np.abs(w.gpair[:, 1]).max())
-    s, sg, sh = g.gbt_suggest_scales(0, mg, mh)
-    assert s == 0
+    w = synth.make(name, n_rows=n_rows, n_features=n_features, depth=max(depths))
+    sg, sh = synth.fixed_point_scales(w.gpair)
     lam, gamma, mcw = 1.0, 0.5, 1e-3
+    hists = _oracle_hists(oracle_mod, w, depths, sg, sh)
+    refs = [oracle_mod.find_splits(h, w.n_bins, lam, gamma, mcw, sg, sh)[0] for h in hists]
     with Session(0) as sess:
         sess.upload_bins(w.bins, w.n_bins, w.sentinel)
         sess.begin_tree(w.gpair, sg, sh)
-        # two different inputs: 4 nodes, then 8 nodes (the second call runs on
-        # whatever the first left in the shared scratch)
-        hists = []
-        for depth in (2, 3):
-            lv = w.levels[depth]
-            hists.append(sess.build_level(lv.rows, torch.from_numpy(lv.offsets).cuda()))
-        refs = [_splits(sess.find_splits(h, lam, gamma, mcw)) for h in hists]
+        dev = [torch.from_numpy(h).cuda() for h in hists]
+        ctx_refs = [_splits(sess.find_splits(h, lam, gamma, mcw)) for h in dev]
         assert sess.sync() == 0
+        for r, c in zip(refs, ctx_refs):
+            _same(c, r, "context find vs oracle")
         stream = sess.stream.cuda_stream
         prm = g.params(lam, gamma, mcw)
-        for call, h in enumerate(hists):
-            n = h.shape[0]
+        # two different inputs in a row (the second call runs on whatever the first left in the shared
+        # scratch), then the first again
+        for call, k in enumerate((0, 1, 0)):
+            n = dev[k].shape[0]
             out = torch.zeros((n, g.SPLIT_BYTES), dtype=torch.uint8, device=sess.device)
-            st = g.gbt_find_splits_noalloc(h, n, w.n_features, w.n_bins, sg, sh, prm, out, stream)
+            st = g.gbt_find_splits_noalloc(dev[k], n, w.n_features, w.n_bins, sg, sh, prm, out, stream)
             assert st == g.GBT_OK, st
             torch.cuda.synchronize()
-            _same(_splits(out), refs[call], f"call {call}")
-        # the same input again after a larger call: the counters were cleared
-        out = torch.zeros((hists[0].shape[0], g.SPLIT_BYTES), dtype=torch.uint8, device=sess.device)
-        assert g.gbt_find_splits_noalloc(hists[0], hists[0].shape[0], w.n_features, w.n_bins, sg, sh, prm, out,
-                                         stream) == g.GBT_OK
-        torch.cuda.synchronize()
-        _same(_splits(out), refs[0], "repeat")
+            _same(_splits(out), refs[k], f"call {call} vs oracle")
+            _same(_splits(out), ctx_refs[k], f"call {call} vs context find")
+
+
+def test_noalloc_allocates_no_device_memory(oracle_mod):
+    """After a first call (which may load the library's module on this device), further calls leave the
+    device's free memory unchanged."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import histogram_construction_gb300 as g
+
+    w = synth.make("u16miss", n_rows=8_000, n_features=5, depth=2)
+    sg, sh = synth.fixed_point_scales(w.gpair)
+    (h,) = _oracle_hists(oracle_mod, w, (2,), sg, sh)
+    ref, _ = oracle_mod.find_splits(h, w.n_bins, 1.0, 0.0, 0.0, sg, sh)
+    hd = torch.from_numpy(h).cuda()
+    out = torch.zeros((h.shape[0], g.SPLIT_BYTES), dtype=torch.uint8, device="cuda")
+    prm = g.params(1.0, 0.0, 0.0)
+    assert g.gbt_find_splits_noalloc(hd, h.shape[0], w.n_features, w.n_bins, sg, sh, prm, out) == g.GBT_OK
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info()
+    for _ in range(5):
+        assert g.gbt_find_splits_noalloc(hd, h.shape[0], w.n_features, w.n_bins, sg, sh, prm, out) == g.GBT_OK
+    torch.cuda.synchronize()
+    free1, _ = torch.cuda.mem_get_info()
+    assert free1 == free0, (free0, free1)
+    _same(_splits(out), ref, "after repeated calls")
 
 
 def test_noalloc_rejects_sizes_beyond_its_scratch_and_host_outputs():
