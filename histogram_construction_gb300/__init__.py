@@ -29,6 +29,7 @@ EXPORTS = [
     "gbt_partition_level", "gbt_profile_enable", "gbt_profile_read", "gbt_slots_per_feature",
     "gbt_kernel_launches", "gbt_find_splits_noalloc", "gbt_find_level_split", "gbt_build_level_f64",
     "gbt_subtract_siblings_f64", "gbt_find_splits_f64", "gbt_begin_tree_multi", "gbt_build_level_multi",
+    "gbt_partition_level_pairs", "gbt_advance_level",
 ]
 
 
@@ -81,6 +82,8 @@ def lib(build_if_missing: bool = True):
         "gbt_subtract_and_find": (st, [vp, vp, vp, vp, vp, i32, ctypes.POINTER(GbtParams), vp, vp]),
         "gbt_level_step": (st, [vp, vp, vp, i32, vp, vp, vp, vp, ctypes.POINTER(GbtParams), vp, vp]),
         "gbt_partition_level": (st, [vp, vp, vp, i32, vp, vp, vp]),
+        "gbt_partition_level_pairs": (st, [vp, vp, vp, i32, vp, vp, vp, vp, vp, vp]),
+        "gbt_advance_level": (st, [vp, vp, vp, vp, i32, vp, vp, ctypes.POINTER(GbtParams), vp]),
         "gbt_profile_enable": (st, [vp, ctypes.c_int]),
         "gbt_profile_read": (st, [vp, ctypes.c_char_p, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(i64)]),
         "gbt_slots_per_feature": (i32, [vp]),
@@ -231,6 +234,19 @@ def gbt_level_step(ctx, rows, node_offsets, n_pairs, parent_hist, parent_of, sma
 def gbt_partition_level(ctx, rows, node_offsets, n_nodes, splits, out_rows, out_offsets):
     return lib().gbt_partition_level(ctx, ptr(rows), ptr(node_offsets), int(n_nodes), ptr(splits), ptr(out_rows),
                                      ptr(out_offsets))
+
+
+def gbt_partition_level_pairs(ctx, rows, node_offsets, n_nodes, splits, out_rows, out_offsets, small_rows,
+                              small_offsets, small_side):
+    return lib().gbt_partition_level_pairs(ctx, ptr(rows), ptr(node_offsets), int(n_nodes), ptr(splits),
+                                           ptr(out_rows), ptr(out_offsets), ptr(small_rows), ptr(small_offsets),
+                                           ptr(small_side))
+
+
+def gbt_advance_level(ctx, small_rows, small_offsets, small_side, n_pairs, parent_hist, level_hist, prm,
+                      level_splits):
+    return lib().gbt_advance_level(ctx, ptr(small_rows), ptr(small_offsets), ptr(small_side), int(n_pairs),
+                                   ptr(parent_hist), ptr(level_hist), ctypes.byref(prm), ptr(level_splits))
 
 
 def gbt_profile_enable(ctx, on=True):

@@ -101,7 +101,7 @@ struct gbt_ctx {
   DevState *st = nullptr;
   uint32_t *err_host = nullptr;  // pinned: [0] error word copy, [1] max |q| copy, [2] multi-output max |q| copy
   Buf gp_stage, chunk_prefix, partial, rows_in, offs_in, cand, splits_a, splits_b, parent_of_in, tile_counts, lrank,
-      slab, counters, level_scratch, items;
+      slab, counters, level_scratch, items, side_in;
   std::string last_error;
   int64_t launches = 0;
   // tuning: work items the level plan aims for (default 1 per SM; GBT_TARGET_ITEMS overrides it for sweeps)
@@ -394,7 +394,7 @@ gbt_status gbt_destroy(gbt_ctx *c) {
   cudaStreamSynchronize(c->stream);
   Buf *bufs[] = {&c->mirror, &c->q, &c->gp_stage, &c->chunk_prefix, &c->partial, &c->rows_in, &c->offs_in,
                  &c->cand, &c->splits_a, &c->splits_b, &c->parent_of_in, &c->tile_counts, &c->lrank, &c->slab,
-                 &c->counters, &c->level_scratch, &c->qm, &c->items};
+                 &c->counters, &c->level_scratch, &c->qm, &c->items, &c->side_in};
   for (Buf *b : bufs) release(c, *b);
   if (c->st) cudaFreeAsync(c->st, c->stream);
   cudaStreamSynchronize(c->stream);
@@ -1012,16 +1012,22 @@ namespace {
 template <bool FROM_PARTIALS>
 gbt_status run_level_finish(gbt_ctx *c, const SmallSource &src, const int64_t *parent_hist, const int32_t *parent_of,
                             int64_t *large_hist, int32_t n_pairs, const gbt_params *params, gbt_split *small_out,
-                            gbt_split *large_out) {
+                            gbt_split *large_out, const uint8_t *side = nullptr) {
   const int32_t *po = nullptr;
   gbt_status s = parent_of_view(c, parent_of, n_pairs, &po);
   if (s != GBT_OK) return s;
   SplitOut *da = nullptr, *db = nullptr;
   bool ha = false, hb = false;
-  s = split_out_view(c, small_out, n_pairs, c->splits_a, &da, &ha);
+  // node order (side given): one array of 2 n_pairs splits, small and large interleaved by pair
+  const int32_t n_out = side ? 2 * n_pairs : n_pairs;
+  s = split_out_view(c, small_out, n_out, c->splits_a, &da, &ha);
   if (s != GBT_OK) return s;
-  s = split_out_view(c, large_out, n_pairs, c->splits_b, &db, &hb);
-  if (s != GBT_OK) return s;
+  if (side) {
+    db = da;
+  } else {
+    s = split_out_view(c, large_out, n_pairs, c->splits_b, &db, &hb);
+    if (s != GBT_OK) return s;
+  }
   const int nfb = (c->n_features + 3) / 4;
   s = ensure(c, c->cand, (size_t)2 * n_pairs * nfb * PUB_K * sizeof(Cand), "candidates");
   if (s != GBT_OK) return s;
@@ -1030,10 +1036,11 @@ gbt_status run_level_finish(gbt_ctx *c, const SmallSource &src, const int64_t *p
   const SplitParams sp = make_sp(c, params);
   prof_begin(c);
   launch_pdl(c, k_level_finish<FROM_PARTIALS>, dim3(nfb, n_pairs), dim3(SCAN_THREADS), 0, src, parent_hist, po,
-             large_hist, c->n_features, c->n_bins, sp, (Cand *)c->cand.p, (uint32_t *)c->counters.p, da, db, c->st);
+             large_hist, c->n_features, c->n_bins, sp, (Cand *)c->cand.p, (uint32_t *)c->counters.p, da, db, c->st,
+             side);
   LAUNCH_CHECK(c, FROM_PARTIALS ? "k_level_finish" : "k_subtract_find");
   if (ha)
-    CUDA_TRY(c, cudaMemcpyAsync(small_out, da, (size_t)n_pairs * sizeof(gbt_split), cudaMemcpyDeviceToHost, c->stream),
+    CUDA_TRY(c, cudaMemcpyAsync(small_out, da, (size_t)n_out * sizeof(gbt_split), cudaMemcpyDeviceToHost, c->stream),
              "splits to host");
   if (hb)
     CUDA_TRY(c, cudaMemcpyAsync(large_out, db, (size_t)n_pairs * sizeof(gbt_split), cudaMemcpyDeviceToHost, c->stream),
@@ -1089,8 +1096,14 @@ gbt_status gbt_level_step(gbt_ctx *c, const int32_t *rows, const int64_t *node_o
   return run_level_finish<true>(c, src, parent_hist, parent_of, large_hist, n_pairs, params, small_out, large_out);
 }
 
-gbt_status gbt_partition_level(gbt_ctx *c, const int32_t *rows, const int64_t *node_offsets, int32_t n_nodes,
-                               const gbt_split *splits, int32_t *out_rows, int64_t *out_offsets) {
+}  // extern "C"
+
+namespace {
+
+// Shared body of gbt_partition_level and gbt_partition_level_pairs (small_* NULL: no smaller-child list).
+gbt_status partition_impl(gbt_ctx *c, const int32_t *rows, const int64_t *node_offsets, int32_t n_nodes,
+                          const gbt_split *splits, int32_t *out_rows, int64_t *out_offsets, int32_t *small_rows,
+                          int64_t *small_offsets, uint8_t *small_side) {
   gbt_status s = check_ctx(c);
   if (s != GBT_OK) return s;
   if (c->n_rows == 0) return fail(c, GBT_ERR_STATE, "gbt_upload_bins first");
@@ -1099,6 +1112,9 @@ gbt_status gbt_partition_level(gbt_ctx *c, const int32_t *rows, const int64_t *n
   if (!node_offsets || !splits || !out_rows || !out_offsets) return fail(c, GBT_ERR_INVALID_ARG, "NULL argument");
   if (ptr_kind(out_rows) != 1 || ptr_kind(out_offsets) != 1)
     return fail(c, GBT_ERR_INVALID_ARG, "out_rows and out_offsets must be device memory");
+  const bool pairs = small_rows != nullptr || small_offsets != nullptr || small_side != nullptr;
+  if (pairs && (ptr_kind(small_rows) != 1 || ptr_kind(small_offsets) != 1 || ptr_kind(small_side) != 1))
+    return fail(c, GBT_ERR_INVALID_ARG, "small_rows, small_offsets and small_side must all be device memory");
   int64_t R_host = -1;
   if (ptr_kind(node_offsets) == 0) {
     if (node_offsets[0] != 0) return fail(c, GBT_ERR_INVALID_ARG, "node_offsets[0] must be 0");
@@ -1145,6 +1161,9 @@ gbt_status gbt_partition_level(gbt_ctx *c, const int32_t *rows, const int64_t *n
   pp.tile_counts = (int64_t *)c->tile_counts.p;
   pp.out_rows = out_rows;
   pp.out_offs = out_offsets;
+  pp.small_rows = pairs ? small_rows : nullptr;
+  pp.small_offs = pairs ? small_offsets : nullptr;
+  pp.small_side = pairs ? small_side : nullptr;
   pp.st = c->st;
   int64_t *lrank = (int64_t *)c->lrank.p;
   prof_begin(c);
@@ -1163,6 +1182,57 @@ gbt_status gbt_partition_level(gbt_ctx *c, const int32_t *rows, const int64_t *n
   k_part_scatter<<<(unsigned)n_tiles, PART_THREADS, 0, c->stream>>>(pp, lrank);
   LAUNCH_CHECK(c, "k_part_scatter");
   return GBT_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+gbt_status gbt_advance_level(gbt_ctx *c, const int32_t *small_rows, const int64_t *small_offsets,
+                             const uint8_t *small_side, int32_t n_pairs, const int64_t *parent_hist,
+                             int64_t *level_hist, const gbt_params *params, gbt_split *level_splits) {
+  gbt_status s = check_ctx(c);
+  if (s != GBT_OK) return s;
+  if (!small_offsets) return fail(c, GBT_ERR_INVALID_ARG, "small_offsets is required");
+  if (n_pairs == 0 && params) return GBT_OK;
+  s = check_pair_args(c, params, n_pairs, {parent_hist, level_hist});
+  if (s != GBT_OK) return s;
+  if (!level_splits) return fail(c, GBT_ERR_INVALID_ARG, "level_splits is required");
+  const void *side_d = nullptr;
+  if (small_side) {
+    s = device_view(c, small_side, (size_t)n_pairs, c->side_in, &side_d, "small_side");
+    if (s != GBT_OK) return s;
+  } else {
+    s = ensure(c, c->side_in, (size_t)n_pairs, "small_side zeros");
+    if (s != GBT_OK) return s;
+    CUDA_TRY(c, cudaMemsetAsync(c->side_in.p, 0, (size_t)n_pairs, c->stream), "small_side zeros");
+    side_d = c->side_in.p;
+  }
+  LevelParams lp;
+  s = run_level_build(c, small_rows, small_offsets, n_pairs, &lp);
+  if (s != GBT_OK) return s;
+  SmallSource src{};
+  src.view = partial_view(lp, c->n_bins + 1);
+  src.item_feats = lp.item_feats;
+  src.hist_out = level_hist;
+  return run_level_finish<true>(c, src, parent_hist, nullptr, level_hist, n_pairs, params, level_splits, level_splits,
+                                (const uint8_t *)side_d);
+}
+
+gbt_status gbt_partition_level(gbt_ctx *c, const int32_t *rows, const int64_t *node_offsets, int32_t n_nodes,
+                               const gbt_split *splits, int32_t *out_rows, int64_t *out_offsets) {
+  return partition_impl(c, rows, node_offsets, n_nodes, splits, out_rows, out_offsets, nullptr, nullptr, nullptr);
+}
+
+gbt_status gbt_partition_level_pairs(gbt_ctx *c, const int32_t *rows, const int64_t *node_offsets, int32_t n_nodes,
+                                     const gbt_split *splits, int32_t *out_rows, int64_t *out_offsets,
+                                     int32_t *small_rows, int64_t *small_offsets, uint8_t *small_side) {
+  if (!small_rows || !small_offsets || !small_side) {
+    if (c) c->last_error = "small_rows, small_offsets and small_side are required";
+    return GBT_ERR_INVALID_ARG;
+  }
+  return partition_impl(c, rows, node_offsets, n_nodes, splits, out_rows, out_offsets, small_rows, small_offsets,
+                        small_side);
 }
 
 gbt_status gbt_profile_enable(gbt_ctx *c, int on) {

@@ -10,6 +10,14 @@
 // Three kernels over the flat level list in tiles of PART_TILE positions:
 // per-tile left counts, one-block scan of the tile counts, then per-tile
 // recompute + block scan + scatter.
+//
+// Optionally the scatter also writes every pair's smaller child (fewer rows;
+// the left one on a tie) into a compact list: small_rows holds, in pair
+// order, the rows of child 2n + small_side[n], in their order, with pair n's
+// segment at [small_offs[n], small_offs[n+1]). This is the input of the next
+// level's smaller-sibling build [bonsai "10: CUDA histogram backend", "The
+// device context lifecycle": advance_level builds the smaller siblings in one
+// pass].
 #pragma once
 
 #include "common.cuh"
@@ -35,6 +43,9 @@ struct PartParams {
   int64_t *tile_counts;  // [n_tiles + 1]
   int32_t *out_rows;
   int64_t *out_offs;     // [2 n_nodes + 1]
+  int32_t *small_rows;   // optional: rows of each pair's smaller child, pair order
+  int64_t *small_offs;   // [n_nodes + 1] with small_rows
+  uint8_t *small_side;   // [n_nodes] with small_rows: 0 = child 2n is the smaller, 1 = child 2n + 1
   DevState *st;
 };
 
@@ -210,10 +221,19 @@ __global__ void __launch_bounds__(32) k_part_offsets(PartParams p, int64_t *lran
     next = lrank_at[n];
   }
   p.out_offs[0] = 0;
+  int64_t small_total = 0;
+  if (p.small_rows) p.small_offs[0] = 0;
   for (int n = 0; n < p.n_nodes; ++n) {
     const int64_t left = lrank_at[n + 1] - lrank_at[n];
+    const int64_t right = (p.offs[n + 1] - p.offs[n]) - left;
     p.out_offs[2 * n + 1] = p.offs[n] + left;
     p.out_offs[2 * n + 2] = p.offs[n + 1];
+    if (p.small_rows) {
+      const bool right_smaller = right < left;  // ties go to the left child
+      p.small_side[n] = right_smaller ? 1 : 0;
+      small_total += right_smaller ? right : left;
+      p.small_offs[n + 1] = small_total;
+    }
   }
 }
 
@@ -260,10 +280,14 @@ __global__ void __launch_bounds__(PART_THREADS) k_part_scatter(PartParams p, con
     const int64_t a = p.offs[n];
     const int64_t left_before = lr - lrank_at[n];  // left rows of node n before k
     const int64_t left_n = lrank_at[n + 1] - lrank_at[n];
-    int64_t dst;
-    if (flags[j]) dst = a + left_before;
-    else dst = a + left_n + ((k - a) - left_before);
-    if (dst >= 0 && dst < R) p.out_rows[dst] = (rows[j] >= 0 && rows[j] < p.n_rows) ? rows[j] : 0;
+    const int64_t rank = flags[j] ? left_before : (k - a) - left_before;  // position within its child
+    const int64_t dst = flags[j] ? a + rank : a + left_n + rank;
+    const int32_t row = (rows[j] >= 0 && rows[j] < p.n_rows) ? rows[j] : 0;
+    if (dst >= 0 && dst < R) p.out_rows[dst] = row;
+    if (p.small_rows && (flags[j] ? 0 : 1) == (int)p.small_side[n]) {
+      const int64_t sd = p.small_offs[n] + rank;
+      if (sd >= 0 && sd < p.small_offs[p.n_nodes]) p.small_rows[sd] = row;
+    }
     lr += flags[j];
   }
 }

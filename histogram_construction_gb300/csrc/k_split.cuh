@@ -786,13 +786,16 @@ struct SmallSource {
 // sibling's strip (read, or summed from the build's chunk partials and
 // written out), warps 4-7 load the parent strip and form Large = Parent -
 // Small (written out). Every warp then scans its strip; the last CTA of pair
-// p writes small_out[p] and large_out[p].
+// p writes small_out[p] and large_out[p]. With node_side (node order), pair
+// p's outputs go to node 2p + node_side[p] (small) and 2p + 1 - node_side[p] (large) of
+// one level array instead (the small histogram's own index, small_out and
+// hist_out, and large / large_out then name the same arrays).
 template <bool FROM_PARTIALS>
 __global__ void __launch_bounds__(SCAN_THREADS, 3) k_level_finish(
     SmallSource src, const int64_t *__restrict__ parent, const int32_t *__restrict__ parent_of,
     int64_t *__restrict__ large, int32_t n_features, int32_t n_bins, SplitParams sp, Cand *__restrict__ cand,
     uint32_t *__restrict__ counters, SplitOut *__restrict__ small_out, SplitOut *__restrict__ large_out,
-    DevState *st) {
+    DevState *st, const uint8_t *__restrict__ node_side) {
   __shared__ ScanShared sh;
   const int p = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -810,8 +813,14 @@ __global__ void __launch_bounds__(SCAN_THREADS, 3) k_level_finish(
   pdl_wait();  // the histogram kernel (or whatever ran before on the stream)
   if (FROM_PARTIALS && !st->plan_ok) return;
   scan_init(sh);
-  longlong2 *L = reinterpret_cast<longlong2 *>(large) + ((int64_t)p * n_features + f) * B;
-  longlong2 *Sout = FROM_PARTIALS ? reinterpret_cast<longlong2 *>(src.hist_out) + ((int64_t)p * n_features + f) * B
+  int64_t si = p, li = p;  // output indices of the small and the large sibling
+  if (node_side) {
+    const int sd = node_side[p] & 1;
+    si = 2 * (int64_t)p + sd;
+    li = 2 * (int64_t)p + 1 - sd;
+  }
+  longlong2 *L = reinterpret_cast<longlong2 *>(large) + (li * n_features + f) * B;
+  longlong2 *Sout = FROM_PARTIALS ? reinterpret_cast<longlong2 *>(src.hist_out) + (si * n_features + f) * B
                                   : nullptr;
   const longlong2 *Sin = FROM_PARTIALS ? Sout
                                        : reinterpret_cast<const longlong2 *>(src.hist) + ((int64_t)p * n_features + f) * B;
@@ -827,7 +836,7 @@ __global__ void __launch_bounds__(SCAN_THREADS, 3) k_level_finish(
         const int64_t stride = src.view.n_fgroups * src.view.image_int4s * 2;
         const int2 *img0 = image_cell(src.view, g0, ff, src.item_feats, 0);
         const int64_t sstride = src.view.sbw;  // int2 between slots
-        longlong2 *So = reinterpret_cast<longlong2 *>(src.hist_out) + ((int64_t)p * n_features + ff) * B;
+        longlong2 *So = reinterpret_cast<longlong2 *>(src.hist_out) + (si * n_features + ff) * B;
         for (int s0 = t >> 2; s0 < B; s0 += 128) {
           int64_t ag[4] = {0, 0, 0, 0}, ah[4] = {0, 0, 0, 0};
           const int2 *img = img0;
@@ -937,8 +946,8 @@ __global__ void __launch_bounds__(SCAN_THREADS, 3) k_level_finish(
   if (cta_publish(sh, 2, cs_base + blockIdx.x * PUB_K, cl_base + blockIdx.x * PUB_K, counters + p, nfb)) {
     __threadfence();
     // warps 0-3 reduce the small sibling, warps 4-7 the large one
-    if (threadIdx.x < 128) reduce_node(cs_base, nfb * PUB_K, sp, small_out + p, 0, 128, 1, sh.extra, sh.red);
-    else reduce_node(cl_base, nfb * PUB_K, sp, large_out + p, 128, 128, 2, sh.extra + 4, sh.red + 4);
+    if (threadIdx.x < 128) reduce_node(cs_base, nfb * PUB_K, sp, small_out + si, 0, 128, 1, sh.extra, sh.red);
+    else reduce_node(cl_base, nfb * PUB_K, sp, large_out + li, 128, 128, 2, sh.extra + 4, sh.red + 4);
   }
 }
 

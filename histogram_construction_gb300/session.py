@@ -8,8 +8,8 @@ from __future__ import annotations
 
 import numpy as np
 
-from . import (GBT_OK, SPLIT_BYTES, check, gbt_begin_tree, gbt_begin_tree_multi, gbt_build_level,
-               gbt_build_level_f64, gbt_build_level_multi, gbt_create,
+from . import (GBT_OK, SPLIT_BYTES, check, gbt_advance_level, gbt_begin_tree, gbt_begin_tree_multi, gbt_build_level,
+               gbt_build_level_f64, gbt_build_level_multi, gbt_create, gbt_partition_level_pairs,
                gbt_destroy, gbt_find_level_split, gbt_find_splits, gbt_find_splits_f64, gbt_kernel_launches,
                gbt_level_step, gbt_partition_level, gbt_subtract_and_find, gbt_subtract_siblings,
                gbt_subtract_siblings_f64, gbt_sync, gbt_upload_bins, lib, params)
@@ -234,3 +234,35 @@ class Session:
         out_offs = torch.empty(2 * n_nodes + 1, dtype=torch.int64, device=self.device)
         self.check(gbt_partition_level(self.ctx, r, o, n_nodes, splits, out_rows, out_offs))
         return out_rows[:R], out_offs
+
+    def partition_pairs(self, rows, offsets, splits, n_rows_level=None):
+        """gbt_partition_level_pairs: returns (rows, offsets [2n+1], small_rows, small_offsets [n+1],
+        small_side [n]) device tensors. n_rows_level: the level's row count (read from offsets if None)."""
+        torch = self.torch
+        n_nodes = int(len(offsets) - 1)
+        R = int(offsets[-1]) if n_rows_level is None else int(n_rows_level)
+        r = self.to_dev(rows, torch.int32)
+        o = self.to_dev(offsets, torch.int64)
+        if isinstance(splits, np.ndarray):
+            splits = torch.from_numpy(np.ascontiguousarray(splits).view(np.uint8).reshape(-1, SPLIT_BYTES)).to(
+                self.device)
+        out_rows = torch.empty(max(R, 1), dtype=torch.int32, device=self.device)
+        out_offs = torch.empty(2 * n_nodes + 1, dtype=torch.int64, device=self.device)
+        small_rows = torch.empty(max(R // 2, 1), dtype=torch.int32, device=self.device)
+        small_offs = torch.empty(n_nodes + 1, dtype=torch.int64, device=self.device)
+        small_side = torch.empty(n_nodes, dtype=torch.uint8, device=self.device)
+        self.check(gbt_partition_level_pairs(self.ctx, r, o, n_nodes, splits, out_rows, out_offs, small_rows,
+                                             small_offs, small_side))
+        return out_rows[:R], out_offs, small_rows, small_offs, small_side
+
+    def advance_level(self, small_rows, small_offsets, small_side, parent, level_hist=None, lam=1.0, gamma=0.0,
+                      mcw=0.0, splits=None):
+        """gbt_advance_level: the next level's histograms and splits in node order ([2 n_pairs] each)."""
+        n_pairs = parent.shape[0]
+        if level_hist is None:
+            level_hist = self.hist_tensor(2 * n_pairs)
+        if splits is None:
+            splits = self.torch.empty((2 * n_pairs, SPLIT_BYTES), dtype=self.torch.uint8, device=self.device)
+        self.check(gbt_advance_level(self.ctx, small_rows, small_offsets, small_side, n_pairs, parent, level_hist,
+                                     params(lam, gamma, mcw), splits))
+        return level_hist, splits

@@ -308,6 +308,42 @@ gbt_status gbt_subtract_and_find(gbt_ctx *ctx, const int64_t *parent_hist, const
 gbt_status gbt_partition_level(gbt_ctx *ctx, const int32_t *rows, const int64_t *node_offsets, int32_t n_nodes,
                                const gbt_split *splits, int32_t *out_rows, int64_t *out_offsets);
 
+/* gbt_partition_level that also lists every pair's smaller child for the
+ * next level's build [bonsai "10: CUDA histogram backend", "The device
+ * context lifecycle": partition_level, then advance_level builds the smaller
+ * siblings in one pass]. Outputs as gbt_partition_level, plus:
+ *   small_side: device uint8 [n_nodes]: 0 when child 2i (left) has no more
+ *     rows than child 2i + 1, else 1 (the smaller sibling; ties go left).
+ *   small_offsets: device int64 [n_nodes + 1]: small_offsets[0] = 0,
+ *     small_offsets[i + 1] - small_offsets[i] = rows of node i's smaller child.
+ *   small_rows: device int32 [small_offsets[n_nodes]] (at most half the
+ *     level's rows): node i's smaller child's rows in their order, node by
+ *     node. All three must be device memory (else GBT_ERR_INVALID_ARG). */
+gbt_status gbt_partition_level_pairs(gbt_ctx *ctx, const int32_t *rows, const int64_t *node_offsets, int32_t n_nodes,
+                                     const gbt_split *splits, int32_t *out_rows, int64_t *out_offsets,
+                                     int32_t *small_rows, int64_t *small_offsets, uint8_t *small_side);
+
+/* One level of a depth-wise grower in node order [bonsai "10: CUDA histogram
+ * backend", "The device context lifecycle": advance_level builds the smaller
+ * siblings in one pass, derives the larger by subtraction and flips the
+ * buffers so that the children become the next frontier]. Pair p is nodes
+ * (2p, 2p + 1) with parent p: its smaller child 2p + small_side[p] is built
+ * from segment p of small_rows / small_offsets (as gbt_build_level), the
+ * other is parent_hist[p] minus it (as gbt_subtract_siblings), and both
+ * splits are found (as gbt_find_splits). Results are written in node order,
+ * so that level_hist is the next level's parent_hist and level_splits the
+ * next gbt_partition_level_pairs's splits.
+ *   small_rows, small_offsets, small_side: as gbt_partition_level_pairs
+ *     writes them (host or device; small_side NULL = all 0).
+ *   parent_hist: device [n_pairs][F][B][2] int64 (the previous level).
+ *   level_hist: device [2 n_pairs][F][B][2] int64, written; must not alias
+ *     parent_hist.
+ *   level_splits: host or device gbt_split [2 n_pairs], written.
+ * Limits: n_pairs <= 32767. */
+gbt_status gbt_advance_level(gbt_ctx *ctx, const int32_t *small_rows, const int64_t *small_offsets,
+                             const uint8_t *small_side, int32_t n_pairs, const int64_t *parent_hist,
+                             int64_t *level_hist, const gbt_params *params, gbt_split *level_splits);
+
 /* Per-kernel device-time accounting for diagnostics. When enabled, every
  * kernel this context launches is bracketed by a pair of CUDA events on the
  * context stream. gbt_profile_read synchronises the stream, adds up the

@@ -139,46 +139,6 @@ def test_wide_full_size(gb, oracle_mod):
         run_level(s, oracle_mod, w, 3, sg, sh)
 
 
-def test_dense_full_size_two_levels(gb, oracle_mod):
-    """10,000,000 x 500 u8 with constant h: the root histogram and split, the device partition by
-    that split, then level 1's smaller sibling, subtraction and splits, all compared in full."""
-    g, Session, s2n = gb
-    w = synth.make("dense", depth=1)
-    sg, sh = _scales(w)
-    q, _ = oracle_mod.quantise(w.gpair, sg, sh)
-    with Session() as s:
-        s.upload_bins(torch.from_numpy(w.bins).cuda(), w.n_bins, w.sentinel)
-        s.begin_tree(torch.from_numpy(w.gpair).cuda(), sg, sh)
-        offs = np.array([0, w.n_rows], np.int64)
-        h = s.build_level(None, torch.from_numpy(offs).cuda())
-        sp = s.find_splits(h)
-        ref_h, st = oracle_mod.build_hist(w.bins, w.n_bins, w.sentinel, q, None, offs)
-        assert st == oracle_mod.OK and s.sync() == 0
-        np.testing.assert_array_equal(h.cpu().numpy(), ref_h, err_msg="root")
-        ref_sp, _ = oracle_mod.find_splits(ref_h, w.n_bins, 1.0, 0.0, 0.0, sg, sh)
-        assert_splits_equal(s2n(sp), ref_sp, "root")
-        d_rows, d_offs = s.partition(None, offs, sp)
-        ref_rows, ref_offs, st = oracle_mod.partition(w.bins, w.n_bins, w.sentinel, None, offs, ref_sp)
-        assert st == oracle_mod.OK and s.sync() == 0
-        np.testing.assert_array_equal(d_rows.cpu().numpy(), ref_rows)
-        np.testing.assert_array_equal(d_offs.cpu().numpy(), ref_offs)
-        sizes = np.diff(ref_offs)
-        small = 1 if sizes[1] < sizes[0] else 0
-        b_rows = ref_rows[ref_offs[small]:ref_offs[small + 1]].astype(np.int32)
-        b_offs = np.array([0, sizes[small]], np.int64)
-        hs = s.build_level(torch.from_numpy(b_rows).cuda(), torch.from_numpy(b_offs).cuda())
-        large, so, lo = s.subtract_and_find(h, hs)
-        ref_hs, _ = oracle_mod.build_hist(w.bins, w.n_bins, w.sentinel, q, b_rows, b_offs)
-        ref_large, _ = oracle_mod.subtract(ref_h, None, ref_hs)
-        assert s.sync() == 0
-        np.testing.assert_array_equal(hs.cpu().numpy(), ref_hs, err_msg="small")
-        np.testing.assert_array_equal(large.cpu().numpy(), ref_large, err_msg="large")
-        rs, _ = oracle_mod.find_splits(ref_hs, w.n_bins, 1.0, 0.0, 0.0, sg, sh)
-        rl, _ = oracle_mod.find_splits(ref_large, w.n_bins, 1.0, 0.0, 0.0, sg, sh)
-        assert_splits_equal(s2n(so), rs, "level 1 small")
-        assert_splits_equal(s2n(lo), rl, "level 1 large")
-
-
 def test_u16_missing_reduced(gb, oracle_mod):
     g, Session, s2n = gb
     w = synth.make("u16miss", n_rows=100_000, n_features=20, depth=5)
