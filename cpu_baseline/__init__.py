@@ -54,6 +54,16 @@ def threads() -> int:
     return int(lib().omp_threads())
 
 
+def quantise(gpair, scale_g, scale_h):
+    """The quantised pairs the baseline fills with: round-half-even of the float32 product, int32 [N][2]
+    (inputs must keep |x * s| < 2^31)."""
+    gp = np.ascontiguousarray(gpair, dtype=np.float32).reshape(-1, 2)
+    prod = gp * np.array([scale_g, scale_h], dtype=np.float32)
+    if not np.all(np.abs(prod) < 2.0 ** 31):
+        raise ValueError("quantised value out of the int32 range")
+    return np.rint(prod).astype(np.int32)
+
+
 def _p(a):
     return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
 
