@@ -19,7 +19,8 @@ enum : uint32_t {
 struct DevState {
   uint32_t err;        // error bits
   uint32_t qmax;       // max |q| over the current tree's rows, both components
-  uint32_t work_next;  // dynamic work counter of the histogram kernel
+  uint32_t work_next;  // dynamic work counter of the histogram kernel (0 between launches)
+  uint32_t work_done;  // CTAs of the histogram kernel that have finished (0 between launches)
   uint32_t plan_ok;    // 1 when the level plan is valid
   int32_t n_items;     // work items of the level
   uint32_t qmax_multi; // max |q| over the multi-output tree's pairs, all targets

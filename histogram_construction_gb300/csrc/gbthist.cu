@@ -106,6 +106,11 @@ struct gbt_ctx {
   int64_t launches = 0;
   // tuning: work items the level plan aims for (default 1 per SM; GBT_TARGET_ITEMS overrides it for sweeps)
   int target_items = 0;
+  bool plan_kernel = false;  // GBT_PLAN_KERNEL=1: always plan levels with the plan kernel (comparisons)
+  // group images: bytes at the start of `partial` known to be zero (the reduce region must be, when a
+  // level's histogram kernel starts); img_r_pending: this level's reduce region, zero again once the
+  // level's consumer kernel (which zeroes what it reads) is launched
+  size_t img_clean = 0, img_r_pending = 0;
   // diagnostics: per-launch event pairs
   bool prof = false;
   struct ProfRec {
@@ -350,6 +355,7 @@ gbt_status gbt_create(int device, void *cuda_stream, gbt_ctx **out) {
   cudaDeviceGetAttribute(&c->n_sm, cudaDevAttrMultiProcessorCount, device);
   cudaDeviceGetAttribute(&c->smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device);
   if (const char *e = getenv("GBT_TARGET_ITEMS")) c->target_items = std::max(0, atoi(e));
+  if (const char *e = getenv("GBT_PLAN_KERNEL")) c->plan_kernel = atoi(e) != 0;
   void *st = nullptr;
   e = dev_alloc(&st, sizeof(DevState), c->stream);
   if (e != cudaSuccess) {
@@ -626,7 +632,7 @@ gbt_status run_level_build(gbt_ctx *c, const int32_t *rows, const int64_t *node_
       rows_d = rows;
     }
   }
-  s = ensure(c, c->chunk_prefix, (size_t)2 * (n_nodes + 1) * sizeof(int32_t), "chunk and group prefixes");
+  s = ensure(c, c->chunk_prefix, (size_t)(2 * n_nodes + 1) * sizeof(int32_t), "group prefixes and first images");
   if (s != GBT_OK) return s;
   const bool f64 = gpair_f64 != nullptr;
   if (multi) {
@@ -652,8 +658,8 @@ gbt_status run_level_build(gbt_ctx *c, const int32_t *rows, const int64_t *node_
   lp.target_items = c->target_items > 0 ? c->target_items : c->n_sm;
   lp.n_rows = c->n_rows;
   lp.q = f64 ? (const int2 *)gpair_f64 : (multi ? (const int2 *)c->qm.p : (const int2 *)c->q.p);
-  lp.chunk_prefix = (int32_t *)c->chunk_prefix.p;
-  lp.group_prefix = lp.chunk_prefix + (n_nodes + 1);
+  lp.group_prefix = (int32_t *)c->chunk_prefix.p;
+  lp.img_first = lp.group_prefix + (n_nodes + 1);
   lp.sbw = c->bin_bytes == 1 ? 16 : c->ts16;
   lp.nsb = c->bin_bytes == 1 ? H8_SB : 1;
   // nsb x B x sbw (G, H) pairs: int32 pairs (8 bytes), or double pairs (16 bytes) for float cells
@@ -671,18 +677,34 @@ gbt_status run_level_build(gbt_ctx *c, const int32_t *rows, const int64_t *node_
   const int64_t items_max = (int64_t)lp.n_fgroups * (n_nodes + 1) +
                             std::max<int64_t>(lp.target_items, (int64_t)lp.n_fgroups * ((c->n_rows + rc - 1) / rc));
   if (items_max > INT32_MAX / 2) return fail(c, GBT_ERR_UNSUPPORTED, "level too large for the work-item plan");
-  s = ensure(c, c->partial, (size_t)items_max * lp.image_int4s * 16, "level image scratch");
+  // group images: the reduce region (at most one group per chunk, chunks <= items_max / n_fgroups) and one
+  // store image group per node after it
+  const int64_t r_cap = (items_max + lp.n_fgroups - 1) / lp.n_fgroups;
+  const size_t group_bytes = (size_t)lp.n_fgroups * lp.image_int4s * 16;
+  const size_t r_bytes = (size_t)r_cap * group_bytes;
+  const size_t old_cap = c->partial.cap;
+  s = ensure(c, c->partial, r_bytes + (size_t)n_nodes * group_bytes, "level image scratch");
   if (s != GBT_OK) return s;
+  if (c->partial.cap != old_cap) c->img_clean = 0;  // a new allocation holds anything
+  if (r_bytes > c->img_clean)
+    CUDA_TRY(c, cudaMemsetAsync((char *)c->partial.p + c->img_clean, 0, r_bytes - c->img_clean, c->stream),
+             "zero the reduce images");
+  c->img_clean = 0;  // in use until this level's consumer is launched
+  c->img_r_pending = r_bytes;
+  lp.r_cap_groups = r_cap;
   lp.partial = (int32_t *)c->partial.p;
   s = ensure(c, c->items, (size_t)items_max * sizeof(Item), "level work items");
   if (s != GBT_OK) return s;
   lp.items = (Item *)c->items.p;
   const int hist_ctas = c->n_sm;  // persistent: one resident CTA per SM
-  lp.first_static = hist_ctas;
-
-  prof_begin(c);
-  k_level_plan<<<c->n_sm, PLAN_THREADS, 0, c->stream>>>(lp);
-  LAUNCH_CHECK(c, "k_level_plan");
+  // levels of few nodes are planned by the histogram kernel itself (GBT_PLAN_KERNEL=1 forces the plan kernel)
+  lp.fold = (n_nodes <= FOLD_MAX_NODES && !c->plan_kernel) ? 1 : 0;
+  lp.pad_ = 0;
+  if (!lp.fold) {
+    prof_begin(c);
+    k_level_plan<<<1, PLAN_THREADS, 0, c->stream>>>(lp);
+    LAUNCH_CHECK(c, "k_level_plan");
+  }
   if (c->bin_bytes == 1) {
     Hist8Params hp;
     hp.lv = lp;
@@ -740,6 +762,8 @@ PartialView partial_view(const LevelParams &lp, int B) {
   PartialView v;
   v.partial = lp.partial;
   v.group_prefix = lp.group_prefix;
+  v.img_first = lp.img_first;
+  v.r_cap = lp.r_cap_groups;
   v.image_int4s = lp.image_int4s;
   v.n_fgroups = lp.n_fgroups;
   v.sbw = lp.sbw;
@@ -770,6 +794,7 @@ gbt_status gbt_build_level(gbt_ctx *c, const int32_t *rows, const int64_t *node_
   launch_pdl(c, k_finalize, dim3(grid_for(c, cells, 256, 8)), dim3(256), 0, partial_view(lp, c->n_bins + 1), n_nodes,
              c->n_features, lp.item_feats, hist_out, (const DevState *)c->st);
   LAUNCH_CHECK(c, "k_finalize");
+  c->img_clean = c->img_r_pending;
   return GBT_OK;
 }
 
@@ -865,6 +890,7 @@ gbt_status gbt_build_level_multi(gbt_ctx *c, const int32_t *rows, const int64_t 
   launch_pdl(c, k_finalize_multi, dim3(grid_for(c, cells, 256, 8)), dim3(256), 0, partial_view(lp, B), c->multi_k,
              n_nodes, c->n_features, hist_out, (const DevState *)c->st);
   LAUNCH_CHECK(c, "k_finalize_multi");
+  c->img_clean = c->img_r_pending;
   return GBT_OK;
 }
 
@@ -888,10 +914,12 @@ gbt_status gbt_build_level_f64(gbt_ctx *c, const float *gpair, const int32_t *ro
   const int B = c->n_bins + 1;
   const int64_t cells = (int64_t)n_nodes * c->n_features * B;
   prof_begin(c);
-  launch_pdl(c, k_finalize_f64, dim3(grid_for(c, cells, 256, 8)), dim3(256), 0, (const double *)lp.partial,
-             (const int32_t *)lp.group_prefix, (int64_t)lp.image_int4s * 2, lp.n_fgroups, lp.item_feats, lp.sbw,
-             n_nodes, c->n_features, B, hist_out, (const DevState *)c->st);
+  launch_pdl(c, k_finalize_f64, dim3(grid_for(c, cells, 256, 8)), dim3(256), 0, (double *)lp.partial,
+             (const int32_t *)lp.group_prefix, (const int32_t *)lp.img_first, (int64_t)lp.r_cap_groups,
+             (int64_t)lp.image_int4s * 2, lp.n_fgroups, lp.item_feats, lp.sbw, n_nodes, c->n_features, B, hist_out,
+             (const DevState *)c->st);
   LAUNCH_CHECK(c, "k_finalize_f64");
+  c->img_clean = c->img_r_pending;
   return GBT_OK;
 }
 
@@ -1039,6 +1067,7 @@ gbt_status run_level_finish(gbt_ctx *c, const SmallSource &src, const int64_t *p
              large_hist, c->n_features, c->n_bins, sp, (Cand *)c->cand.p, (uint32_t *)c->counters.p, da, db, c->st,
              side);
   LAUNCH_CHECK(c, FROM_PARTIALS ? "k_level_finish" : "k_subtract_find");
+  if (FROM_PARTIALS) c->img_clean = c->img_r_pending;
   if (ha)
     CUDA_TRY(c, cudaMemcpyAsync(small_out, da, (size_t)n_out * sizeof(gbt_split), cudaMemcpyDeviceToHost, c->stream),
              "splits to host");

@@ -21,8 +21,10 @@ namespace gbt {
 // Group images ([image][sub-block][slot][sbw][G, H] double; feature fl of an
 // item's group is sub-block fl / sbw, column fl % sbw) -> hist_out
 // [n][F][B][2] double, summing a node's group images.
-__global__ void __launch_bounds__(256) k_finalize_f64(const double *__restrict__ partial,
-                                                      const int32_t *__restrict__ group_prefix, int64_t image_doubles,
+__global__ void __launch_bounds__(256) k_finalize_f64(double *__restrict__ partial,
+                                                      const int32_t *__restrict__ group_prefix,
+                                                      const int32_t *__restrict__ img_first, int64_t r_cap,
+                                                      int64_t image_doubles,
                                                       int32_t n_fgroups, int32_t item_feats, int32_t sbw,
                                                       int32_t n_nodes, int32_t n_features, int32_t B,
                                                       double *__restrict__ hist_out, const DevState *st) {
@@ -38,10 +40,14 @@ __global__ void __launch_bounds__(256) k_finalize_f64(const double *__restrict__
     const int sb = fl / sbw, c = fl - sb * sbw;
     const int64_t cell = (((int64_t)sb * B + s) * sbw + c) * 2;
     double g = 0.0, h = 0.0;
+    const int32_t i0 = img_first[n];
+    const bool zero = i0 < r_cap;  // reduce-region images are zeroed as they are read
     for (int32_t k = group_prefix[n]; k < group_prefix[n + 1]; ++k) {
-      const double *src = partial + ((int64_t)k * n_fgroups + fg) * image_doubles + cell;
-      g += __ldcg(src);
-      h += __ldcg(src + 1);
+      double *src = partial + ((int64_t)(i0 + k - group_prefix[n]) * n_fgroups + fg) * image_doubles + cell;
+      const double2 x = __ldcg(reinterpret_cast<const double2 *>(src));
+      if (zero) __stcg(reinterpret_cast<double2 *>(src), make_double2(0.0, 0.0));
+      g += x.x;
+      h += x.y;
     }
     double *d = hist_out + (((int64_t)n * n_features + f) * B + s) * 2;
     d[0] = g;

@@ -57,16 +57,18 @@ struct LevelParams {
   int32_t item_feats;     // features per work item (64 for u8, TS for u16)
   int64_t n_rows;
   const int2 *q;          // quantised gpair [n_rows]
-  int32_t *chunk_prefix;  // [n_nodes + 1] chunks before each node
-  int32_t *group_prefix;  // [n_nodes + 1] exactness groups before each node
+  int32_t *group_prefix;  // [n_nodes + 1] exactness groups before each node (written by the plan)
+  int32_t *img_first;     // [n_nodes] first group image of each node (written by the plan)
+  int64_t r_cap_groups;   // size of the reduce region in group images; store node n owns r_cap_groups + n
   int32_t *partial;       // int32 group images (see PartialView)
   int64_t image_int4s;    // 16-byte units per image
   int32_t sbw;            // features per sub-block of the image (16 for u8, TS for u16)
   int32_t nsb;            // sub-blocks per image (4 for u8, 1 for u16)
   uint32_t qmax_plan;     // if nonzero, the plan's exactness bound uses it instead of the tree's max|q|
   int32_t chunk_cap;      // if nonzero, no chunk holds more rows (float cells: rounding per chunk)
-  Item *items;            // [items] decoded work items (written by the plan)
-  int32_t first_static;   // items 0 .. first_static - 1 go to histogram CTAs by block index
+  Item *items;            // [items] decoded work items (written by the plan kernel)
+  int32_t fold;           // 1: the histogram kernel plans the level itself (n_nodes <= FOLD_MAX_NODES)
+  int32_t pad_;
   DevState *st;
 };
 
@@ -95,8 +97,8 @@ __device__ __forceinline__ int64_t block_incl_scan(int64_t v, int64_t *s_warp) {
   return r;
 }
 
-// Level plan. With T = target_items / n_fgroups chunks wanted, the base
-// length L is the shortest of 16 candidates from ceil(R / T) to
+// Level plan (one block). With T = target_items / n_fgroups chunks wanted,
+// the base length L is the shortest of 16 candidates from ceil(R / T) to
 // ceil(R / ceil(T / 2)) whose chunk count sum_n max(1, ceil(rows_n / L)) stays
 // within T (the longest when none does; the longest keeps the count within T
 // whenever T >= 2 x the nodes holding rows). L is at least CHUNK_MIN_ROWS and at
@@ -104,13 +106,19 @@ __device__ __forceinline__ int64_t block_incl_scan(int64_t v, int64_t *s_warp) {
 // So no persistent CTA takes one item more than the others.
 // A node's chunks have equal length ceil(rows_n / c_n) <= L, and its
 // consecutive chunks form exactness groups of floor(rc / length) chunks, whose
-// int32 sum cannot overflow either. Every work item (chunk, feature group) adds its
-// shared-memory image into its group's image; groups of more than one chunk
-// are zeroed here first (every block plans redundantly and zeroes a share;
-// block 0 publishes the plan). Offsets that do not start at 0, descend or
-// leave [0, n_rows] invalidate the plan (no items; GBT_ERR_ROW_RANGE).
-constexpr int PLAN_THREADS = 256;  // nodes per planning batch; every block plans redundantly, so keep it small
-constexpr int PLAN_CANDS = 16;  // chunk lengths the plan counts in one pass
+// int32 sum cannot overflow either. Every work item (chunk, feature group) adds
+// its shared-memory image into its group's image.
+//
+// Group images live in two regions. A node of one chunk ("store" node) owns
+// group image r_cap + n, which its item overwrites with a bulk store. The
+// groups of a node of several chunks ("reduce" nodes) are numbered from 0 in
+// node order; their items bulk reduce-add into them. The reduce region is kept
+// zero between calls (the host zeroes it once; every consumer zeroes the
+// reduce images it reads), so nothing is zeroed here and one block plans the
+// level. Offsets that do not start at 0, descend or leave [0, n_rows]
+// invalidate the plan (no items; GBT_ERR_ROW_RANGE).
+constexpr int PLAN_THREADS = 512;  // nodes per planning batch
+constexpr int PLAN_CANDS = 16;     // chunk lengths the plan counts in one pass
 
 // A node of rows_n rows in c equal chunks (ceil(rows_n / c) rows each, the
 // last one shorter): consecutive chunks per exactness group.
@@ -123,19 +131,15 @@ __device__ __forceinline__ int64_t chunks_per_group(int64_t rows_n, int64_t c, i
 __global__ void __launch_bounds__(PLAN_THREADS) k_level_plan(LevelParams p) {
   pdl_trigger();  // the histogram kernel may launch now; it waits for this grid to finish
   __shared__ int64_t s_warp[32];
-  __shared__ int64_t s_zpre[PLAN_THREADS + 1];  // zero-unit prefix of the batch's nodes
-  __shared__ int64_t s_zbase[PLAN_THREADS];     // first zeroed unit of each node of the batch
   __shared__ int64_t s_a[PLAN_THREADS];         // first level position of each node of the batch
   __shared__ int32_t s_cpre[PLAN_THREADS + 1];  // chunk prefix within the batch
-  __shared__ int32_t s_rows[PLAN_THREADS], s_len[PLAN_THREADS], s_cpg[PLAN_THREADS], s_gbase[PLAN_THREADS];
-  __shared__ int64_t s_tot[2];
+  __shared__ int32_t s_rows[PLAN_THREADS], s_len[PLAN_THREADS], s_cpg[PLAN_THREADS], s_img[PLAN_THREADS];
+  __shared__ int32_t s_red[PLAN_THREADS];       // 1: a reduce node
+  __shared__ int64_t s_tot[3];
   __shared__ uint32_t s_cnt[PLAN_CANDS];
-  __shared__ uint32_t s_qm;
   const int tid = threadIdx.x;
-  const bool pub = blockIdx.x == 0;
   // one read phase: the tree's max|q|, R and every node's offsets
-  uint32_t qm = 1;
-  if (tid == 0) qm = p.qmax_plan ? p.qmax_plan : p.st->qmax;
+  const uint32_t qm = max(p.qmax_plan ? p.qmax_plan : p.st->qmax, 1u);
   const int64_t R = p.offs[p.n_nodes];
   // PLAN_CANDS chunk lengths from ceil(R / T) to ceil(R / ceil(T / 2)) (32-bit:
   // R < 2^31), with T = target_items / n_fgroups chunks wanted
@@ -159,10 +163,9 @@ __global__ void __launch_bounds__(PLAN_THREADS) k_level_plan(LevelParams p) {
     for (int k = 0; k < PLAN_CANDS; ++k) cnt[k] += max(1u, (rows_n + cand[k] - 1) / cand[k]);
   }
   if (__syncthreads_or(bad)) {
-    if (pub && tid == 0) {
+    if (tid == 0) {
       p.st->plan_ok = 0;
       p.st->n_items = 0;
-      p.st->work_next = 0;
       raise_err(p.st, ERRBIT_ROW);
     }
     return;
@@ -180,97 +183,258 @@ __global__ void __launch_bounds__(PLAN_THREADS) k_level_plan(LevelParams p) {
       for (int k = 0; k < PLAN_CANDS; ++k) atomicAdd(&s_cnt[k], cnt[k]);
     }
   }
-  if (tid == 0) s_qm = max(qm, 1u);
   __syncthreads();
   uint32_t len = cand[PLAN_CANDS - 1];
 #pragma unroll
   for (int k = PLAN_CANDS - 1; k >= 0; --k)
     if (s_cnt[k] <= T) len = cand[k];
-  const int64_t rc = (int64_t)(0x7fffffffu / s_qm);  // rows whose int32 partials cannot overflow
+  const int64_t rc = (int64_t)(0x7fffffffu / qm);  // rows whose int32 partials cannot overflow
   int64_t chunk = max((int64_t)len, (int64_t)CHUNK_MIN_ROWS);
   chunk = max((int64_t)1, min(rc, chunk));
   if (p.chunk_cap > 0) chunk = min(chunk, (int64_t)p.chunk_cap);
-  const int64_t img_group = (int64_t)p.n_fgroups * p.image_int4s;  // units of one group's images
-  int4 *zdst = reinterpret_cast<int4 *>(p.partial);
-  int64_t carry_c = 0, carry_g = 0;
+  int64_t carry_c = 0, carry_g = 0, carry_r = 0;
   for (int base = 0; base < p.n_nodes; base += blockDim.x) {
     const int n = base + tid;
-    int64_t c = 0, g = 0, m = 0, cpg = 1, rows_n = 0, a = 0;
+    int64_t c = 0, g = 0, cpg = 1, rows_n = 0, a = 0;
+    bool red = false;
     if (n < p.n_nodes) {
       a = p.offs[n];
       rows_n = p.offs[n + 1] - a;
       c = max((int64_t)1, (int64_t)(((uint32_t)rows_n + (uint32_t)chunk - 1) / (uint32_t)chunk));
       cpg = chunks_per_group(rows_n, c, rc);
       g = (c + cpg - 1) / cpg;
-      if (cpg > 1) m = c / cpg + ((c % cpg) >= 2 ? 1 : 0);  // groups of >= 2 chunks: the first m
+      red = c >= 2;
     }
     const int64_t ic = block_incl_scan(c, s_warp);
     const int64_t ig = block_incl_scan(g, s_warp);
-    const int64_t iz = block_incl_scan(m * img_group, s_warp);
-    if (n < p.n_nodes && pub) {
-      p.chunk_prefix[n + 1] = (int32_t)(carry_c + ic);
+    const int64_t ir = block_incl_scan(red ? g : 0, s_warp);
+    const int64_t img = red ? carry_r + ir - g : p.r_cap_groups + n;
+    if (n < p.n_nodes) {
       p.group_prefix[n + 1] = (int32_t)(carry_g + ig);
+      p.img_first[n] = (int32_t)img;
     }
-    s_zpre[tid + 1] = iz;
-    s_zbase[tid] = (carry_g + ig - g) * img_group;
     s_cpre[tid + 1] = (int32_t)ic;
     s_a[tid] = a;
     s_rows[tid] = (int32_t)rows_n;
     s_len[tid] = (int32_t)(((uint32_t)rows_n + (uint32_t)c - 1) / (uint32_t)max(c, (int64_t)1));
     s_cpg[tid] = (int32_t)cpg;
-    s_gbase[tid] = (int32_t)(carry_g + ig - g);
-    if (tid == 0) {
-      s_zpre[0] = 0;
-      s_cpre[0] = 0;
-    }
+    s_img[tid] = (int32_t)img;
+    s_red[tid] = red ? 1 : 0;
+    if (tid == 0) s_cpre[0] = 0;
     if (tid == blockDim.x - 1) {
       s_tot[0] = ic;
       s_tot[1] = ig;
+      s_tot[2] = ir;
     }
     __syncthreads();
-    const int64_t total = s_zpre[blockDim.x];
     const int last = min(p.n_nodes - base, (int)blockDim.x) - 1;  // the batch's last node
-    for (int64_t u = (int64_t)blockIdx.x * blockDim.x + tid; u < total; u += (int64_t)gridDim.x * blockDim.x) {
-      int lo = 0, hi = last;  // largest j with s_zpre[j] <= u
-      while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (s_zpre[mid] <= u) lo = mid; else hi = mid - 1;
-      }
-      zdst[s_zbase[lo] + (u - s_zpre[lo])] = make_int4(0, 0, 0, 0);
-    }
-    // the batch's work items, shared out over the grid like the zeroing
+    // the batch's work items
     const int64_t nfg = p.n_fgroups;
     const int64_t items = (int64_t)s_cpre[blockDim.x] * nfg;
-    for (int64_t u = (int64_t)blockIdx.x * blockDim.x + tid; u < items; u += (int64_t)gridDim.x * blockDim.x) {
+    for (int64_t u = tid; u < items; u += blockDim.x) {
       const int32_t kc = (int32_t)(u / nfg);  // chunk within the batch
       const int32_t f = (int32_t)(u - (int64_t)kc * nfg);
-      int lo = 0, hi = last;  // largest j with s_cpre[j] <= kc
-      while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (s_cpre[mid] <= kc) lo = mid; else hi = mid - 1;
+      int lo2 = 0, hi2 = last;  // largest j with s_cpre[j] <= kc
+      while (lo2 < hi2) {
+        const int mid = (lo2 + hi2 + 1) >> 1;
+        if (s_cpre[mid] <= kc) lo2 = mid; else hi2 = mid - 1;
       }
-      const int32_t cidx = kc - s_cpre[lo], nc = s_cpre[lo + 1] - s_cpre[lo], cpg_n = s_cpg[lo];
+      const int32_t cidx = kc - s_cpre[lo2], cpg_n = s_cpg[lo2];
       const int32_t gi = cidx / cpg_n;
       Item it;
-      it.node = base + lo;
+      it.node = base + lo2;
       it.fgroup = f;
-      it.k0 = s_a[lo] + (int64_t)cidx * s_len[lo];
-      it.k1 = min(s_a[lo] + s_rows[lo], it.k0 + s_len[lo]);
-      it.image = (int64_t)(s_gbase[lo] + gi) * nfg + f;
-      it.multi = min(cpg_n, nc - gi * cpg_n) > 1 ? 1 : 0;
+      it.k0 = s_a[lo2] + (int64_t)cidx * s_len[lo2];
+      it.k1 = min(s_a[lo2] + s_rows[lo2], it.k0 + s_len[lo2]);
+      it.image = (int64_t)(s_img[lo2] + gi) * nfg + f;
+      it.multi = s_red[lo2];
       it.pad = 0;
       p.items[(carry_c * nfg) + u] = it;
     }
     carry_c += s_tot[0];
     carry_g += s_tot[1];
+    carry_r += s_tot[2];
     __syncthreads();
   }
-  if (pub && tid == 0) {
-    p.chunk_prefix[0] = 0;
+  if (tid == 0) {
     p.group_prefix[0] = 0;
     p.st->plan_ok = 1;
     p.st->n_items = (int32_t)(carry_c * p.n_fgroups);
-    p.st->work_next = (uint32_t)p.first_static;  // dynamic claims start after the static first items
+  }
+}
+
+// ----------------------------------------------------------------------------
+// The same plan, computed by every CTA of the histogram kernel itself for a
+// level of at most FOLD_MAX_NODES nodes: no plan launch on the critical path.
+// Each CTA keeps the chunk prefix and the first group image of every node in
+// shared memory and decodes an item when it claims it (the node's offsets are
+// read again, from L1 or L2). CTA 0 publishes group_prefix, img_first and
+// plan_ok for the consumer kernels.
+constexpr int FOLD_MAX_NODES = 256;
+
+struct FoldPlan {
+  int32_t cpre[FOLD_MAX_NODES + 1];  // chunk prefix over the nodes
+  int32_t img[FOLD_MAX_NODES];       // first group image of each node
+  int32_t wtot[3][FOLD_MAX_NODES / 32];
+  uint32_t cnt[PLAN_CANDS], cand[PLAN_CANDS];
+  int64_t chunk, rc;
+  int64_t R;                         // level rows
+  uint32_t qm;                       // max |q| bound of the plan
+  int32_t n_items;
+};
+
+// Returns false (and, in CTA 0, reports GBT_ERR_ROW_RANGE) when the offsets are
+// invalid. Called by every thread; blockDim.x >= FOLD_MAX_NODES and >= 32 *
+// PLAN_CANDS. Warp k counts the chunks of candidate length k over all nodes
+// (their offsets read again, from L1), so the sixteen counts take one pass.
+// (The u8 kernels leave under 1 KB of shared memory for this record.)
+__device__ __noinline__ bool plan_fold(const LevelParams &p, FoldPlan &fp) {
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  const bool has = tid < p.n_nodes;
+  // every load of the plan in one round trip: the node's offsets, and R and
+  // max|q| by one thread (152 CTAs x 32 warps reading one word would queue at its L2 slice)
+  if (tid == 0) {
+    fp.R = p.offs[p.n_nodes];
+    fp.qm = max(p.qmax_plan ? p.qmax_plan : p.st->qmax, 1u);
+  }
+  bool ok = true;
+  uint32_t rows_n = 0;
+  if (has) {
+    const int64_t a = __ldg(p.offs + tid), b = __ldg(p.offs + tid + 1);
+    ok = (a >= 0) && (b >= a) && (b <= p.n_rows) && (tid > 0 || a == 0);
+    rows_n = ok ? (uint32_t)(b - a) : 0u;
+  }
+  if (__syncthreads_or(!ok)) {
+    if (blockIdx.x == 0 && tid == 0) {
+      p.st->plan_ok = 0;
+      raise_err(p.st, ERRBIT_ROW);
+    }
+    return false;
+  }
+  const int64_t R = fp.R;
+  const uint32_t qm = fp.qm;
+  const uint32_t T = (uint32_t)max(1, p.target_items / p.n_fgroups);
+  const uint32_t R32 = (R > 0 && R <= p.n_rows) ? (uint32_t)R : 0u;
+  const uint32_t lo = max(1u, (R32 + T - 1) / T), hi = max(lo, (R32 + (T + 1) / 2 - 1) / ((T + 1) / 2));
+  if (w < PLAN_CANDS) {
+    const uint32_t cand = lo + (uint32_t)(((uint64_t)(hi - lo) * w + PLAN_CANDS - 2) / (PLAN_CANDS - 1));
+    uint32_t cnt = 0;
+    for (int n = lane; n < p.n_nodes; n += 32) {
+      const uint32_t r = (uint32_t)(__ldg(p.offs + n + 1) - __ldg(p.offs + n));  // valid: checked above
+      cnt += max(1u, (r + cand - 1) / cand);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+    if (lane == 0) {
+      fp.cnt[w] = cnt;
+      fp.cand[w] = cand;
+    }
+  }
+  __syncthreads();
+  // the shortest candidate whose chunk count stays within T (the longest when none does)
+  uint32_t len = fp.cand[PLAN_CANDS - 1];
+#pragma unroll
+  for (int k = PLAN_CANDS - 1; k >= 0; --k)
+    if (fp.cnt[k] <= T) len = fp.cand[k];
+  const int64_t rc = (int64_t)(0x7fffffffu / qm);
+  int64_t chunk = max((int64_t)len, (int64_t)CHUNK_MIN_ROWS);
+  chunk = max((int64_t)1, min(rc, chunk));
+  if (p.chunk_cap > 0) chunk = min(chunk, (int64_t)p.chunk_cap);
+  // per node: chunks, groups, reduce flag; inclusive scans of (chunks, groups, reduce groups)
+  int32_t c = 0, g = 0, rg = 0;
+  if (has) {
+    c = (int32_t)max((uint32_t)1, (rows_n + (uint32_t)chunk - 1) / (uint32_t)chunk);
+    const int64_t cpg = chunks_per_group(rows_n, c, rc);
+    g = (int32_t)((c + cpg - 1) / cpg);
+    rg = c >= 2 ? g : 0;
+  }
+  int32_t ic = c, ig = g, ir = rg;
+  if (w < FOLD_MAX_NODES / 32) {
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int32_t yc = __shfl_up_sync(0xffffffffu, ic, o), yg = __shfl_up_sync(0xffffffffu, ig, o),
+                    yr = __shfl_up_sync(0xffffffffu, ir, o);
+      if (lane >= o) {
+        ic += yc;
+        ig += yg;
+        ir += yr;
+      }
+    }
+    if (lane == 31) {
+      fp.wtot[0][w] = ic;
+      fp.wtot[1][w] = ig;
+      fp.wtot[2][w] = ir;
+    }
+  }
+  __syncthreads();
+  if (w < FOLD_MAX_NODES / 32) {
+    for (int k = 0; k < w; ++k) {
+      ic += fp.wtot[0][k];
+      ig += fp.wtot[1][k];
+      ir += fp.wtot[2][k];
+    }
+    if (has) {
+      fp.cpre[tid + 1] = ic;
+      const int32_t img = c >= 2 ? ir - rg : (int32_t)(p.r_cap_groups + tid);
+      fp.img[tid] = img;
+      if (blockIdx.x == 0) {
+        p.group_prefix[tid + 1] = ig;
+        p.img_first[tid] = img;
+      }
+    }
+    if (tid == p.n_nodes - 1) fp.n_items = ic * p.n_fgroups;
+  }
+  if (tid == 0) {
+    fp.cpre[0] = 0;
+    fp.chunk = chunk;
+    fp.rc = rc;
+    if (blockIdx.x == 0) {
+      p.group_prefix[0] = 0;
+      p.st->plan_ok = 1;
+    }
+  }
+  __syncthreads();
+  return true;
+}
+
+// Work item `id` of a folded plan (one thread).
+__device__ __forceinline__ Item fold_item(const LevelParams &p, const FoldPlan &fp, int32_t id) {
+  const int32_t nfg = p.n_fgroups;
+  const int32_t kc = id / nfg, f = id - kc * nfg;
+  int lo = 0, hi = p.n_nodes - 1;  // largest node with cpre[node] <= kc
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (fp.cpre[mid] <= kc) lo = mid; else hi = mid - 1;
+  }
+  const int64_t a = __ldg(p.offs + lo), rows_n = __ldg(p.offs + lo + 1) - a;
+  const int32_t c = fp.cpre[lo + 1] - fp.cpre[lo], cidx = kc - fp.cpre[lo];
+  const int64_t len = ((uint32_t)rows_n + (uint32_t)c - 1) / (uint32_t)c;
+  const int32_t gi = cidx / (int32_t)chunks_per_group(rows_n, c, fp.rc);
+  Item it;
+  it.node = lo;
+  it.fgroup = f;
+  it.k0 = a + (int64_t)cidx * len;
+  it.k1 = min(a + rows_n, it.k0 + len);
+  it.image = (int64_t)(fp.img[lo] + gi) * nfg + f;
+  it.multi = c >= 2 ? 1 : 0;
+  it.pad = 0;
+  return it;
+}
+
+// The next item of a CTA (one thread): the first by block index, later ones from the launch's counter.
+__device__ __forceinline__ int32_t claim_item(const LevelParams &p, bool first) {
+  return first ? (int32_t)blockIdx.x : (int32_t)(gridDim.x + atomicAdd(&p.st->work_next, 1u));
+}
+
+// At the end of every CTA that claimed items: the last one resets the counters for the next launch
+// (every other CTA has made its last claim before counting itself done).
+__device__ __forceinline__ void claims_done(const LevelParams &p) {
+  if (threadIdx.x == 0) {
+    __threadfence();
+    if (atomicAdd(&p.st->work_done, 1u) == gridDim.x - 1) {
+      p.st->work_next = 0;
+      p.st->work_done = 0;
+    }
   }
 }
 
@@ -474,6 +638,20 @@ __device__ __forceinline__ void h8_zero_image(unsigned char *smem, int nsb, int 
   __syncthreads();
 }
 
+// The mirror pads the features past the last one with bin 0, so the slot-0
+// cells of those pad columns received the item's gradients; they are cleared
+// before the flush, so that group images hold nothing but real features (the
+// reduce region of the images must stay zero wherever no consumer reads).
+// Columns valid .. 15 of sub-blocks sb0 .. sb1 - 1 (cells of 8 bytes).
+__device__ __forceinline__ void h8_zero_pad(unsigned char *smem, int sb0, int sb1, int valid) {
+  const int pad = 16 - valid;
+  if (pad <= 0) return;
+  for (int i = threadIdx.x; i < (sb1 - sb0) * pad; i += blockDim.x) {
+    const int sb = sb0 + i / pad, col = valid + i % pad;
+    *reinterpret_cast<uint2 *>(smem + sb * H8_SB_STRIDE + col * 8) = make_uint2(0u, 0u);
+  }
+}
+
 template <bool FLT, bool MULTI = false>
 __global__ void __launch_bounds__(H8_THREADS, 1) k_hist_u8(Hist8Params P) {
   constexpr int U = H8_U;
@@ -481,12 +659,19 @@ __global__ void __launch_bounds__(H8_THREADS, 1) k_hist_u8(Hist8Params P) {
   extern __shared__ __align__(128) unsigned char smem[];
   __shared__ int32_t s_item;
   __shared__ Item s_it;  // the next item, claimed and decoded by thread 0 while the last one flushes
+  __shared__ FoldPlan s_fp;
 
   const LevelParams &p = P.lv;
-  pdl_wait();     // the level plan
+  pdl_wait();     // the level plan (or whatever produced the row lists)
   pdl_trigger();  // the consumer kernel may launch; it waits for this grid to finish
-  if (!p.st->plan_ok) return;
-  const int32_t n_items = p.st->n_items;
+  int32_t n_items;
+  if (p.fold) {
+    if (!plan_fold(p, s_fp)) return;
+    n_items = s_fp.n_items;
+  } else {
+    if (!p.st->plan_ok) return;
+    n_items = p.st->n_items;
+  }
   const int B = P.n_slots;
   const int64_t N = p.n_rows;
   const bool ident = (p.rows == nullptr);
@@ -508,9 +693,8 @@ __global__ void __launch_bounds__(H8_THREADS, 1) k_hist_u8(Hist8Params P) {
   const uint32_t ring_lane = hist_base + (uint32_t)H8_SMEM + (uint32_t)warp * U * 512u + (uint32_t)lane * 16u;
 
   if (threadIdx.x == 0) {  // the first item by block index, later ones from the counter
-    s_item = (int32_t)blockIdx.x < p.first_static ? (int32_t)blockIdx.x
-                                                   : (int32_t)atomicAdd(&p.st->work_next, 1u);
-    if (s_item < n_items) s_it = p.items[s_item];
+    s_item = claim_item(p, true);
+    if (s_item < n_items) s_it = p.fold ? fold_item(p, s_fp, s_item) : p.items[s_item];
   }
   __syncthreads();
   for (;;) {
@@ -602,7 +786,16 @@ __global__ void __launch_bounds__(H8_THREADS, 1) k_hist_u8(Hist8Params P) {
       }
     }
     __syncthreads();
+    if (MULTI) {
+      const int nfq = (P.n_features + 15) >> 4;
+      const int fq = it.fgroup % nfq;
+      h8_zero_pad(smem, 0, nsb, min(16, P.n_features - 16 * fq));
+    } else {
+      const int nf = P.n_features - it.fgroup * 64;
+      if (nf < 64) h8_zero_pad(smem, nsb - 1, nsb, nf - 16 * (nsb - 1));
+    }
     if constexpr (FLT) {
+      __syncthreads();
       flush_float_image(smem, nsb, H8_SB_STRIDE, (uint32_t)B * 32u,
                         reinterpret_cast<double *>(p.partial) + it.image * p.image_int4s * 2, it.multi,
                         reinterpret_cast<double *>(smem + H8_SMEM));
@@ -626,12 +819,13 @@ __global__ void __launch_bounds__(H8_THREADS, 1) k_hist_u8(Hist8Params P) {
       }
     }
     if (threadIdx.x == 0) {
-      s_item = (int32_t)atomicAdd(&p.st->work_next, 1u);
-      if (s_item < n_items) s_it = p.items[s_item];
+      s_item = claim_item(p, false);
+      if (s_item < n_items) s_it = p.fold ? fold_item(p, s_fp, s_item) : p.items[s_item];
     }
     __syncthreads();
   }
   if (bad) raise_err(p.st, ERRBIT_ROW);
+  claims_done(p);
   if (threadIdx.x == 0) bulk_wait_all();
 }
 
@@ -682,12 +876,20 @@ __global__ void __launch_bounds__(H16_THREADS, 1) k_hist_u16(Hist16Params P) {
   const int hist_bytes = ((B * TS * 8) + 127) & ~127;
   unsigned char *stage = smem + hist_bytes;
   __shared__ int32_t s_item;
+  __shared__ Item s_it;
+  __shared__ FoldPlan s_fp;
 
   const LevelParams &p = P.lv;
-  pdl_wait();     // the level plan
+  pdl_wait();     // the level plan (or whatever produced the row lists)
   pdl_trigger();  // the consumer kernel may launch; it waits for this grid to finish
-  if (!p.st->plan_ok) return;
-  const int32_t n_items = p.st->n_items;
+  int32_t n_items;
+  if (p.fold) {
+    if (!plan_fold(p, s_fp)) return;
+    n_items = s_fp.n_items;
+  } else {
+    if (!p.st->plan_ok) return;
+    n_items = p.st->n_items;
+  }
   const int64_t N = p.n_rows;
   const bool ident = (p.rows == nullptr);
   const uint32_t miss_slot = (uint32_t)P.n_bins;
@@ -700,14 +902,15 @@ __global__ void __launch_bounds__(H16_THREADS, 1) k_hist_u16(Hist16Params P) {
   bool first = true;  // the first item by block index, later ones from the counter
 
   for (;;) {
-    if (threadIdx.x == 0)
-      s_item = first && (int32_t)blockIdx.x < p.first_static ? (int32_t)blockIdx.x
-                                                              : (int32_t)atomicAdd(&p.st->work_next, 1u);
+    if (threadIdx.x == 0) {
+      s_item = claim_item(p, first);
+      if (s_item < n_items) s_it = p.fold ? fold_item(p, s_fp, s_item) : p.items[s_item];
+    }
     first = false;
     __syncthreads();
     const int32_t id = s_item;
     if (id >= n_items) break;
-    const Item it = p.items[id];
+    const Item it = s_it;
     {
       uint4 *h4 = reinterpret_cast<uint4 *>(hist);
       const int n4 = (B * TS * 8) / 16;
@@ -791,6 +994,13 @@ __global__ void __launch_bounds__(H16_THREADS, 1) k_hist_u16(Hist16Params P) {
       h16_add<FLT>(hist + 2 * (miss_slot * TS + 2 * wi + 1), mg1, mh1);
     }
     __syncthreads();
+    {
+      // pad features past the last one (mirror bin 0): clear their slot-0 cells
+      const int valid = P.n_features - it.fgroup * TS;
+      if (valid < TS && (int)threadIdx.x < TS - valid)
+        *reinterpret_cast<uint2 *>(hist + 2 * (valid + (int)threadIdx.x)) = make_uint2(0u, 0u);
+      __syncthreads();
+    }
     if constexpr (FLT) {
       flush_float_image(smem, 1, 0, (uint32_t)B * TS * 2u,
                         reinterpret_cast<double *>(p.partial) + it.image * p.image_int4s * 2, it.multi,
@@ -815,6 +1025,7 @@ __global__ void __launch_bounds__(H16_THREADS, 1) k_hist_u16(Hist16Params P) {
     __syncthreads();
   }
   if (bad) raise_err(p.st, ERRBIT_ROW);
+  claims_done(p);
   if (threadIdx.x == 0) bulk_wait_all();
 }
 
@@ -826,25 +1037,27 @@ __global__ void __launch_bounds__(H16_THREADS, 1) k_hist_u16(Hist16Params P) {
 // s) * sbw + fl % sbw. The images of node n are groups group_prefix[n] ..
 // group_prefix[n+1]-1, image (group * n_fgroups + feature group).
 struct PartialView {
-  const int32_t *partial;
-  const int32_t *group_prefix;
+  int32_t *partial;
+  const int32_t *group_prefix;  // groups of node n: group_prefix[n + 1] - group_prefix[n]
+  const int32_t *img_first;     // the first group image of node n (the node's images are consecutive)
+  int64_t r_cap;                // images below r_cap (in groups) are in the reduce region: zeroed once read
   int64_t image_int4s;
   int32_t n_fgroups, sbw, nsb, B;
 };
 
-// Cell (slot s) of feature f of the first group image of a node; the next
-// group's image is image_stride int2 further.
-__device__ __forceinline__ const int2 *image_cell(const PartialView &v, int32_t group, int f, int item_feats,
-                                                  int s) {
+// Cell (slot s) of feature f of group image `group` (a node's first is
+// img_first[n]); the next group's image is image_stride int2 further.
+__device__ __forceinline__ int2 *image_cell(const PartialView &v, int32_t group, int f, int item_feats, int s) {
   const int fg = f / item_feats, fl = f - fg * item_feats;
   const int sb = fl / v.sbw, c = fl - sb * v.sbw;
   const int64_t image = (int64_t)group * v.n_fgroups + fg;
-  return reinterpret_cast<const int2 *>(v.partial) + image * v.image_int4s * 2 + ((int64_t)sb * v.B + s) * v.sbw + c;
+  return reinterpret_cast<int2 *>(v.partial) + image * v.image_int4s * 2 + ((int64_t)sb * v.B + s) * v.sbw + c;
 }
 
 // Finalize: the int64 histogram of every (node, feature, slot) is the sum of
-// the node's group images. One thread per cell; four consecutive threads take
-// four consecutive features of one slot (one 32-byte sector of an image row).
+// the node's group images (reduce-region images are zeroed as they are read).
+// One thread per cell; four consecutive threads take four consecutive
+// features of one slot (one 32-byte sector of an image row).
 __global__ void __launch_bounds__(256) k_finalize(PartialView v, int32_t n_nodes, int32_t n_features,
                                                   int32_t item_feats, int64_t *__restrict__ hist_out,
                                                   const DevState *st) {
@@ -862,11 +1075,13 @@ __global__ void __launch_bounds__(256) k_finalize(PartialView v, int32_t n_nodes
     const int n = (int)(r / nq);
     const int f = qd * 4 + fi;
     if (f >= n_features) continue;
-    const int32_t g0 = v.group_prefix[n], g1 = v.group_prefix[n + 1];
-    const int2 *cell = image_cell(v, g0, f, item_feats, s);
+    const int32_t g0 = v.group_prefix[n], g1 = v.group_prefix[n + 1], i0 = v.img_first[n];
+    const bool zero = i0 < v.r_cap;
+    int2 *cell = image_cell(v, i0, f, item_feats, s);
     int64_t g = 0, h = 0;
     for (int32_t k = g0; k < g1; ++k, cell += image_stride) {
       const int2 x = __ldcg(cell);
+      if (zero) __stcg(cell, make_int2(0, 0));
       g += x.x;
       h += x.y;
     }
@@ -901,13 +1116,14 @@ __global__ void __launch_bounds__(256) k_finalize_multi(PartialView v, int32_t n
     const int f = qd * 4 + fi;
     if (f >= n_features) continue;
     const int fq = f >> 4, fl = f & 15, tg = t >> 2, tl = t & 3;
-    const int32_t g0 = v.group_prefix[n], g1 = v.group_prefix[n + 1];
-    const int64_t image = (int64_t)g0 * v.n_fgroups + (int64_t)tg * nfq + fq;
-    const int2 *cell = reinterpret_cast<const int2 *>(v.partial) + image * v.image_int4s * 2 +
-                       ((int64_t)tl * v.B + s) * 16 + fl;
+    const int32_t g0 = v.group_prefix[n], g1 = v.group_prefix[n + 1], i0 = v.img_first[n];
+    const bool zero = i0 < v.r_cap;
+    const int64_t image = (int64_t)i0 * v.n_fgroups + (int64_t)tg * nfq + fq;
+    int2 *cell = reinterpret_cast<int2 *>(v.partial) + image * v.image_int4s * 2 + ((int64_t)tl * v.B + s) * 16 + fl;
     int64_t g = 0, h = 0;
     for (int32_t k = g0; k < g1; ++k, cell += image_stride) {
       const int2 x = __ldcg(cell);
+      if (zero) __stcg(cell, make_int2(0, 0));
       g += x.x;
       h += x.y;
     }

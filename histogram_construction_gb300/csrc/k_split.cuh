@@ -369,6 +369,10 @@ __device__ __forceinline__ void strip_totals(const longlong2 *cells, int B, int6
   }
 }
 
+// A cut t > 0 whose own cell is empty has the sums of cut t - 1 (in both
+// missing directions), so its gain equals that earlier candidate's and the
+// serial order never picks it: such cuts are skipped (runs of empty bins would
+// otherwise flood the survivor pool with exact ties).
 template <int ND, int MODE>
 __device__ __forceinline__ float scan_push_impl(const longlong2 *cells, int n_bins, int64_t tg, int64_t th,
                                                 longlong2 m, float Gf2den, const SplitParams &sp, int f, int node,
@@ -385,6 +389,7 @@ __device__ __forceinline__ float scan_push_impl(const longlong2 *cells, int n_bi
       asm volatile("prefetch.global.L1 [%0];" ::"l"(cells + min(c0 + 32 * SCAN_SPL + SCAN_SPL * lane, n_bins)));
     int64_t pg[SCAN_SPL], ph[SCAN_SPL];
     int64_t ag = 0, ah = 0;
+    uint32_t nzmask = 0;  // slots of the lane whose cell is not empty
 #pragma unroll
     for (int i = 0; i < SCAN_SPL; ++i) {
       const int s = c0 + SCAN_SPL * lane + i;
@@ -394,6 +399,7 @@ __device__ __forceinline__ float scan_push_impl(const longlong2 *cells, int n_bi
       ah += c.y;
       pg[i] = ag;
       ph[i] = ah;
+      nzmask |= ((c.x | c.y) != 0 || s == 0) ? (1u << i) : 0u;  // cut 0 has no earlier twin
     }
     int64_t eg = ag, eh = ah;
     warp_incl_scan(eg, eh);
@@ -412,7 +418,8 @@ __device__ __forceinline__ float scan_push_impl(const longlong2 *cells, int n_bi
       for (int dir = 0; dir < ND; ++dir) {
         const int64_t GL = eg + pg[i] + (dir ? m.x : 0), HL = eh + ph[i] + (dir ? m.y : 0);
         const int64_t HR = th - HL;
-        const bool valid = s < n_bins && HL >= sp.h_min && HR >= sp.h_min && !(ND == 2 && dir && no_missing_rt(m));
+        const bool valid = s < n_bins && ((nzmask >> i) & 1u) && HL >= sp.h_min && HR >= sp.h_min &&
+                           !(ND == 2 && dir && no_missing_rt(m));
         float u = -INFINITY, lw = -INFINITY;
         if (valid) {
           if (mode == 0) screen_fast(GL, HL, tg - GL, HR, Gf2den, sp, u, lw);
@@ -654,10 +661,17 @@ __device__ __forceinline__ int warp_argmax_lane(const Cand &best) {
 __device__ __forceinline__ void reduce_node(const Cand *cand, int n_ent, const SplitParams &sp, SplitOut *out,
                                             int t0, int nthr, int bar, Cand *slot, float *sthr) {
   const int t = threadIdx.x - t0, lane = threadIdx.x & 31, w = t >> 5, nw = nthr >> 5;
+  constexpr int RB = 8;  // loads in flight per thread
   float thr = -INFINITY;
-  for (int i = t; i < n_ent; i += nthr) {
-    const int4 w3 = __ldcg(reinterpret_cast<const int4 *>(cand + i) + 3);  // hr, up, lo
-    thr = fmaxf(thr, __int_as_float(w3.w));
+  for (int i0 = t; i0 < n_ent; i0 += nthr * RB) {
+    float v[RB];
+#pragma unroll
+    for (int u = 0; u < RB; ++u) {
+      const int i = i0 + u * nthr;
+      v[u] = i < n_ent ? __int_as_float(__ldcg(reinterpret_cast<const int4 *>(cand + i) + 3).w) : -INFINITY;  // lo
+    }
+#pragma unroll
+    for (int u = 0; u < RB; ++u) thr = fmaxf(thr, v[u]);
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) thr = fmaxf(thr, __shfl_xor_sync(0xffffffffu, thr, o));
@@ -665,13 +679,23 @@ __device__ __forceinline__ void reduce_node(const Cand *cand, int n_ent, const S
   named_sync(bar, nthr);
   for (int k = 0; k < nw; ++k) thr = fmaxf(thr, sthr[k]);
   Cand best = no_cand();
-  for (int i = t; i < n_ent; i += nthr) {
-    const int4 w3 = __ldcg(reinterpret_cast<const int4 *>(cand + i) + 3);
-    if (!(__int_as_float(w3.z) >= thr)) continue;
-    Cand c = load_cand(cand + i);
-    if (c.f == INT32_MAX) continue;
-    if (!c.exact) set_exact(c, surv_gain(c.gl, c.hl, c.gl + c.gr, c.hl + c.hr, sp));
-    if (cand_better(c, best)) best = c;
+  for (int i0 = t; i0 < n_ent; i0 += nthr * RB) {
+    float up[RB];
+#pragma unroll
+    for (int u = 0; u < RB; ++u) {
+      const int i = i0 + u * nthr;
+      // past the node's entries: NaN, which never passes the test below (no load beyond the entries)
+      up[u] = i < n_ent ? __int_as_float(__ldcg(reinterpret_cast<const int4 *>(cand + i) + 3).z)
+                        : __int_as_float(0x7fc00000);
+    }
+#pragma unroll
+    for (int u = 0; u < RB; ++u) {
+      if (!(up[u] >= thr)) continue;
+      Cand c = load_cand(cand + i0 + u * nthr);
+      if (c.f == INT32_MAX) continue;
+      if (!c.exact) set_exact(c, surv_gain(c.gl, c.hl, c.gl + c.gr, c.hl + c.hr, sp));
+      if (cand_better(c, best)) best = c;
+    }
   }
   if (lane == warp_argmax_lane(best)) slot[w] = best;
   named_sync(bar, nthr);
@@ -832,20 +856,26 @@ __global__ void __launch_bounds__(SCAN_THREADS, 3) k_level_finish(
       // covers 8 slots x 4 features (whole 32-byte sectors)
       const int t = threadIdx.x, fi = t & 3, ff = blockIdx.x * 4 + fi;
       if (ff < n_features) {
-        const int32_t g0 = src.view.group_prefix[p], g1 = src.view.group_prefix[p + 1];
+        const int32_t g0 = src.view.group_prefix[p], g1 = src.view.group_prefix[p + 1], i0 = src.view.img_first[p];
+        const bool zero = i0 < src.view.r_cap;  // reduce-region images are zeroed as they are read
         const int64_t stride = src.view.n_fgroups * src.view.image_int4s * 2;
-        const int2 *img0 = image_cell(src.view, g0, ff, src.item_feats, 0);
+        int2 *img0 = image_cell(src.view, i0, ff, src.item_feats, 0);
         const int64_t sstride = src.view.sbw;  // int2 between slots
         longlong2 *So = reinterpret_cast<longlong2 *>(src.hist_out) + (si * n_features + ff) * B;
         for (int s0 = t >> 2; s0 < B; s0 += 128) {
           int64_t ag[4] = {0, 0, 0, 0}, ah[4] = {0, 0, 0, 0};
-          const int2 *img = img0;
+          int2 *img = img0;
           for (int32_t k = g0; k < g1; ++k, img += stride) {
             int2 x[4];
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
               const int s = s0 + 32 * u;
               x[u] = s < B ? __ldcg(img + s * sstride) : make_int2(0, 0);
+            }
+            if (zero) {
+#pragma unroll
+              for (int u = 0; u < 4; ++u)
+                if (s0 + 32 * u < B) __stcg(img + (s0 + 32 * u) * sstride, make_int2(0, 0));
             }
 #pragma unroll
             for (int u = 0; u < 4; ++u) {

@@ -229,3 +229,43 @@ def test_near_tie_cases_are_what_they_claim(oracle_mod):
         ref, st = oracle_mod.find_splits(case.h, n_bins, lam, 0.0, 0.0, 1.0, 1.0)
         assert st == oracle_mod.OK
         _check_designed(case, ref, "oracle")
+
+
+def _empty_first_cut_case(n_bins):
+    """One node, one feature: slot 0 empty, 100 real slots of (G -1, H 1), missing (G 100, H 10). Sending only
+    the missing rows left (cut 0, missing left) ties exactly with cut n_bins - 1, missing right (the same two
+    sides swapped); the serial order picks cut 0."""
+    B = n_bins + 1
+    h = np.zeros((1, 1, B, 2), np.int64)
+    h[0, 0, 1:101] = (-1, 1)
+    h[0, 0, n_bins] = (100, 10)
+    return h
+
+
+def test_empty_first_cut_oracle_pin(oracle_mod):
+    for n_bins in (255, 4096):
+        ref, st = oracle_mod.find_splits(_empty_first_cut_case(n_bins), n_bins, 1.0, 0.0, 0.0, 1.0, 1.0)
+        assert st == oracle_mod.OK
+        assert (int(ref["feature"][0]), int(ref["bin"][0]), int(ref["default_left"][0])) == (0, 0, 1)
+        expect = 0.5 * ((100.0 * 100.0 / 11.0 + 100.0 * 100.0 / 101.0) - 0.0)
+        assert ref["gain"][0] == expect
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("n_bins", [255, 4096])
+def test_empty_first_cut_on_gpu(gb, oracle_mod, n_bins):
+    """Cuts over empty cells repeat the previous cut and are skipped by the scan, except cut 0."""
+    g, Session, s2n = gb
+    h = _empty_first_cut_case(n_bins)
+    ref, _ = oracle_mod.find_splits(h, n_bins, 1.0, 0.0, 0.0, 1.0, 1.0)
+    s = _session(Session, n_bins, 1)
+    try:
+        got = s2n(s.find_splits(torch.from_numpy(h).cuda()))
+        parent = np.concatenate([h, h]).sum(axis=0, keepdims=True)
+        large, so, lo = s.subtract_and_find(torch.from_numpy(parent).cuda(), torch.from_numpy(h).cuda())
+        assert s.sync() == 0
+    finally:
+        s.close()
+    _same(got, ref, "find")
+    _same(s2n(so), ref, "finish small")
+    _same(s2n(lo), ref, "finish large")

@@ -97,9 +97,13 @@ def test_root_full_size(gb, oracle_mod):
         assert_splits_equal(s2n(out), rs, "root")
 
 
+@pytest.mark.parametrize("plan_kernel", [False, True])
 @pytest.mark.parametrize("n_rows,host_offsets", [(60_000, False), (200_000, True)])
-def test_level5_reduced(gb, oracle_mod, n_rows, host_offsets):
+def test_level5_reduced(gb, oracle_mod, monkeypatch, n_rows, host_offsets, plan_kernel):
+    """plan_kernel: the level planned by the plan kernel instead of by the histogram kernel itself."""
     g, Session, s2n = gb
+    if plan_kernel:
+        monkeypatch.setenv("GBT_PLAN_KERNEL", "1")
     w = synth.make("level5", n_rows=n_rows)
     sg, sh = _scales(w)
     with Session() as s:
@@ -139,8 +143,11 @@ def test_wide_full_size(gb, oracle_mod):
         run_level(s, oracle_mod, w, 3, sg, sh)
 
 
-def test_u16_missing_reduced(gb, oracle_mod):
+@pytest.mark.parametrize("plan_kernel", [False, True])
+def test_u16_missing_reduced(gb, oracle_mod, monkeypatch, plan_kernel):
     g, Session, s2n = gb
+    if plan_kernel:
+        monkeypatch.setenv("GBT_PLAN_KERNEL", "1")
     w = synth.make("u16miss", n_rows=100_000, n_features=20, depth=5)
     sg, sh = _scales(w)
     with Session() as s:
