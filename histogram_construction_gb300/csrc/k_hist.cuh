@@ -332,10 +332,35 @@ __device__ __noinline__ bool plan_fold(const LevelParams &p, FoldPlan &fp) {
   }
   __syncthreads();
   // the shortest candidate whose chunk count stays within T (the longest when none does)
-  uint32_t len = fp.cand[PLAN_CANDS - 1];
+  int kb = PLAN_CANDS - 1;
 #pragma unroll
   for (int k = PLAN_CANDS - 1; k >= 0; --k)
-    if (fp.cnt[k] <= T) len = fp.cand[k];
+    if (fp.cnt[k] <= T) kb = k;
+  uint32_t len = fp.cand[kb];
+  if (kb > 0 && fp.cnt[kb] <= T && fp.cand[kb] > fp.cand[kb - 1] + 1) {
+    // a second pass over the lengths between the last count above T and the first within it
+    const uint32_t lo2 = fp.cand[kb - 1] + 1, hi2 = fp.cand[kb];
+    __syncthreads();  // every thread has read the first pass
+    if (w < PLAN_CANDS) {
+      const uint32_t cand = lo2 + (uint32_t)(((uint64_t)(hi2 - lo2) * w + PLAN_CANDS - 2) / (PLAN_CANDS - 1));
+      uint32_t cnt = 0;
+      for (int n = lane; n < p.n_nodes; n += 32) {
+        const uint32_t r = (uint32_t)(__ldg(p.offs + n + 1) - __ldg(p.offs + n));
+        cnt += max(1u, (r + cand - 1) / cand);
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+      if (lane == 0) {
+        fp.cnt[w] = cnt;
+        fp.cand[w] = cand;
+      }
+    }
+    __syncthreads();
+    len = hi2;
+#pragma unroll
+    for (int k = PLAN_CANDS - 1; k >= 0; --k)
+      if (fp.cnt[k] <= T) len = fp.cand[k];
+  }
   const int64_t rc = (int64_t)(0x7fffffffu / qm);
   int64_t chunk = max((int64_t)len, (int64_t)CHUNK_MIN_ROWS);
   chunk = max((int64_t)1, min(rc, chunk));

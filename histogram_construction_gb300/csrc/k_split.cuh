@@ -320,6 +320,12 @@ constexpr int SCAN_SPL = 4;  // consecutive slots per lane in the warp scan
 constexpr int PUB_K = 2;     // candidates a CTA publishes per node set before it resorts to double
 constexpr int STAGE_SLOTS = 256;  // strips with B <= 256 are staged in shared memory
 
+// Position of slot s in a staged strip: slots are permuted within aligned
+// blocks of 8 cells (16 bytes each) so that both shared-memory access
+// patterns of a warp are free of bank conflicts: lane l reading slot 4l + i
+// (the scan: four consecutive slots per lane) and lane l reading slot l + 32k.
+__device__ __forceinline__ int swz(int s) { return (s & ~7) | ((s & 7) ^ ((s >> 3) & 7)); }
+
 struct ScanShared {
   longlong2 cells[SCAN_WARPS][STAGE_SLOTS];
   Surv pool[SURV_CAP];
@@ -374,7 +380,7 @@ __device__ __forceinline__ void strip_totals(const longlong2 *cells, int B, int6
 // serial order never picks it: such cuts are skipped (runs of empty bins would
 // otherwise flood the survivor pool with exact ties).
 template <int ND, int MODE>
-__device__ __forceinline__ float scan_push_impl(const longlong2 *cells, int n_bins, int64_t tg, int64_t th,
+__device__ __forceinline__ float scan_push_impl(const longlong2 *cells, bool sw, int n_bins, int64_t tg, int64_t th,
                                                 longlong2 m, float Gf2den, const SplitParams &sp, int f, int node,
                                                 ScanShared &sh, int &overflow, int mode) {
   if (MODE >= 0) mode = MODE;
@@ -394,7 +400,7 @@ __device__ __forceinline__ float scan_push_impl(const longlong2 *cells, int n_bi
     for (int i = 0; i < SCAN_SPL; ++i) {
       const int s = c0 + SCAN_SPL * lane + i;
       longlong2 c = make_longlong2(0, 0);
-      if (s < n_bins) c = cells[s];
+      if (s < n_bins) c = cells[sw ? swz(s) : s];
       ag += c.x;
       ah += c.y;
       pg[i] = ag;
@@ -464,17 +470,19 @@ __device__ __forceinline__ float scan_push_impl(const longlong2 *cells, int n_bi
 }
 
 // sabs: the sum of |G| over the strip's slots (for the range check of the fast screen).
-__device__ __forceinline__ float warp_scan_push(const longlong2 *cells, int n_bins, int64_t tg, int64_t th,
+// sw: a staged strip (shared memory, slot s at swz(s)).
+__device__ __forceinline__ float warp_scan_push(const longlong2 *cells, bool sw, int n_bins, int64_t tg, int64_t th,
                                                 int64_t sabs, const SplitParams &sp, int f, int node, ScanShared &sh,
                                                 int &overflow) {
-  const longlong2 m = cells[n_bins];
+  const longlong2 m = cells[sw ? swz(n_bins) : n_bins];
   const bool no_missing = (m.x == 0 && m.y == 0);
   const float Gf2den = parent_f32(tg, th, sp);
   const bool fast = strip_fast(sabs, th, Gf2den, sp);
   // the common cases (fast screen, with or without missing values) get their own copies
-  if (fast && no_missing) return scan_push_impl<1, 0>(cells, n_bins, tg, th, m, Gf2den, sp, f, node, sh, overflow, 0);
-  if (fast) return scan_push_impl<2, 0>(cells, n_bins, tg, th, m, Gf2den, sp, f, node, sh, overflow, 0);
-  return scan_push_impl<2, -1>(cells, n_bins, tg, th, m, Gf2den, sp, f, node, sh, overflow, sp.filter ? 1 : 2);
+  if (fast && no_missing)
+    return scan_push_impl<1, 0>(cells, sw, n_bins, tg, th, m, Gf2den, sp, f, node, sh, overflow, 0);
+  if (fast) return scan_push_impl<2, 0>(cells, sw, n_bins, tg, th, m, Gf2den, sp, f, node, sh, overflow, 0);
+  return scan_push_impl<2, -1>(cells, sw, n_bins, tg, th, m, Gf2den, sp, f, node, sh, overflow, sp.filter ? 1 : 2);
 }
 
 __device__ __forceinline__ double surv_gain(int64_t gl, int64_t hl, int64_t tg, int64_t th, const SplitParams &sp) {
@@ -490,10 +498,10 @@ __device__ __forceinline__ double surv_gain(int64_t gl, int64_t hl, int64_t tg, 
 // Overflow path (more pushes than the pool holds, e.g. very many exact
 // ties): the warp re-scans its strip and evaluates every candidate whose
 // upper bound reaches thr in double itself.
-__device__ __forceinline__ Cand warp_direct_best(const longlong2 *cells, int n_bins, int64_t tg, int64_t th,
-                                                 const SplitParams &sp, float thr, int f) {
+__device__ __noinline__ Cand warp_direct_best(const longlong2 *cells, bool sw, int n_bins, int64_t tg, int64_t th,
+                                              const SplitParams &sp, float thr, int f) {
   const int lane = threadIdx.x & 31;
-  const longlong2 m = cells[n_bins];
+  const longlong2 m = cells[sw ? swz(n_bins) : n_bins];
   const float Gf2den = parent_f32(tg, th, sp);
   Cand best = no_cand();
   int64_t cg = 0, ch = 0;
@@ -501,7 +509,7 @@ __device__ __forceinline__ Cand warp_direct_best(const longlong2 *cells, int n_b
     const int s = s0 + lane;
     int64_t pg = 0, ph = 0;
     if (s < n_bins) {
-      const longlong2 c = cells[s];
+      const longlong2 c = cells[sw ? swz(s) : s];
       pg = c.x;
       ph = c.y;
     }
@@ -556,7 +564,7 @@ __device__ __forceinline__ Cand surv_cand(const Surv &v) {
 // them are published with their bounds, with no double work in this CTA;
 // with more, they are evaluated in double and the exact best is published.
 // All threads call it; sh.pub[set][0 .. PUB_K-1] holds the result.
-__device__ __forceinline__ void cta_select(ScanShared &sh, const SplitParams &sp, int n_sets, const float *thr,
+__device__ __noinline__ void cta_select(ScanShared &sh, const SplitParams &sp, int n_sets, const float *thr,
                                            const int *warp_node) {
   const int n = min(sh.n, SURV_CAP);
   if (threadIdx.x < 2) sh.cnt[threadIdx.x] = 0;
@@ -756,7 +764,7 @@ __global__ void __launch_bounds__(SCAN_THREADS, 3) k_find(const int64_t *__restr
     if (staged) {
       for (int s = lane; s < B; s += 32) {
         const longlong2 c = __ldg(strip + s);
-        sh.cells[warp][s] = c;
+        sh.cells[warp][swz(s)] = c;
         tg += c.x;
         th += c.y;
         sa += c.x < 0 ? -c.x : c.x;
@@ -767,7 +775,7 @@ __global__ void __launch_bounds__(SCAN_THREADS, 3) k_find(const int64_t *__restr
     warp_sum3(tg, th, sa);
     __syncwarp();
     int ovf = 0;
-    const float wlo = warp_scan_push(cells, n_bins, tg, th, sa, sp, f, 0, sh, ovf);
+    const float wlo = warp_scan_push(cells, staged, n_bins, tg, th, sa, sp, f, 0, sh, ovf);
     ovf = __any_sync(0xffffffffu, ovf);
     if (lane == 0) {
       sh.warp_lo[warp] = wlo;
@@ -778,7 +786,7 @@ __global__ void __launch_bounds__(SCAN_THREADS, 3) k_find(const int64_t *__restr
   float thr[2] = {-INFINITY, -INFINITY};
   for (int w = 0; w < SCAN_WARPS; ++w) thr[0] = fmaxf(thr[0], sh.warp_lo[w]);
   if (f < n_features && sh.warp_overflow[warp]) {
-    const Cand d = warp_direct_best(cells, n_bins, tg, th, sp, thr[0], f);
+    const Cand d = warp_direct_best(cells, staged, n_bins, tg, th, sp, thr[0], f);
     if (lane == 0) sh.extra[warp] = d;
   }
   __syncthreads();
@@ -833,7 +841,7 @@ __global__ void __launch_bounds__(SCAN_THREADS, 3) k_level_finish(
   // The parent strips (and parent_of) were complete before the kernel this one
   // waits for started, so warps 4-7 stage them while that kernel finishes.
   if (side == 1 && active && staged)
-    for (int s = lane; s < B; s += 32) sh.cells[warp][s] = __ldg(P + s);
+    for (int s = lane; s < B; s += 32) sh.cells[warp][swz(s)] = __ldg(P + s);
   pdl_wait();  // the histogram kernel (or whatever ran before on the stream)
   if (FROM_PARTIALS && !st->plan_ok) return;
   scan_init(sh);
@@ -848,55 +856,56 @@ __global__ void __launch_bounds__(SCAN_THREADS, 3) k_level_finish(
                                   : nullptr;
   const longlong2 *Sin = FROM_PARTIALS ? Sout
                                        : reinterpret_cast<const longlong2 *>(src.hist) + ((int64_t)p * n_features + f) * B;
-  // phase A: small strips (warps 0-3); the parent strips (warps 4-7) are staged above
-  if (side == 0) {
-    if (FROM_PARTIALS) {
-      // the 128 threads sum the group images of all four features: thread t
-      // takes feature t & 3 and slots (t >> 2) + 32 i, so each warp load
-      // covers 8 slots x 4 features (whole 32-byte sectors)
-      const int t = threadIdx.x, fi = t & 3, ff = blockIdx.x * 4 + fi;
-      if (ff < n_features) {
-        const int32_t g0 = src.view.group_prefix[p], g1 = src.view.group_prefix[p + 1], i0 = src.view.img_first[p];
-        const bool zero = i0 < src.view.r_cap;  // reduce-region images are zeroed as they are read
-        const int64_t stride = src.view.n_fgroups * src.view.image_int4s * 2;
-        int2 *img0 = image_cell(src.view, i0, ff, src.item_feats, 0);
-        const int64_t sstride = src.view.sbw;  // int2 between slots
-        longlong2 *So = reinterpret_cast<longlong2 *>(src.hist_out) + (si * n_features + ff) * B;
-        for (int s0 = t >> 2; s0 < B; s0 += 128) {
-          int64_t ag[4] = {0, 0, 0, 0}, ah[4] = {0, 0, 0, 0};
-          int2 *img = img0;
-          for (int32_t k = g0; k < g1; ++k, img += stride) {
-            int2 x[4];
+  // phase A: small strips; the parent strips (warps 4-7) are staged above
+  if (FROM_PARTIALS) {
+    // all 256 threads sum the group images of the four features: thread t
+    // takes feature t & 3 and slots (t >> 2) + 64 u, eight loads in flight,
+    // so each warp load covers 8 slots x 4 features (whole 32-byte sectors)
+    constexpr int PA = 8;
+    const int t = threadIdx.x, fi = t & 3, ff = blockIdx.x * 4 + fi;
+    if (ff < n_features) {
+      const int32_t g0 = src.view.group_prefix[p], g1 = src.view.group_prefix[p + 1], i0 = src.view.img_first[p];
+      const bool zero = i0 < src.view.r_cap;  // reduce-region images are zeroed as they are read
+      const int64_t stride = src.view.n_fgroups * src.view.image_int4s * 2;
+      int2 *img0 = image_cell(src.view, i0, ff, src.item_feats, 0);
+      const int64_t sstride = src.view.sbw;  // int2 between slots
+      longlong2 *So = reinterpret_cast<longlong2 *>(src.hist_out) + (si * n_features + ff) * B;
+      for (int s0 = t >> 2; s0 < B; s0 += 64 * PA) {
+        int64_t ag[PA], ah[PA];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              const int s = s0 + 32 * u;
-              x[u] = s < B ? __ldcg(img + s * sstride) : make_int2(0, 0);
-            }
-            if (zero) {
+        for (int u = 0; u < PA; ++u) ag[u] = ah[u] = 0;
+        int2 *img = img0;
+        for (int32_t k = g0; k < g1; ++k, img += stride) {
+          int2 x[PA];
 #pragma unroll
-              for (int u = 0; u < 4; ++u)
-                if (s0 + 32 * u < B) __stcg(img + (s0 + 32 * u) * sstride, make_int2(0, 0));
-            }
+          for (int u = 0; u < PA; ++u) {
+            const int s = s0 + 64 * u;
+            x[u] = s < B ? __ldcg(img + s * sstride) : make_int2(0, 0);
+          }
+          if (zero) {
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              ag[u] += x[u].x;
-              ah[u] += x[u].y;
-            }
+            for (int u = 0; u < PA; ++u)
+              if (s0 + 64 * u < B) __stcg(img + (s0 + 64 * u) * sstride, make_int2(0, 0));
           }
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int s = s0 + 32 * u;
-            if (s < B) {
-              const longlong2 c = make_longlong2(ag[u], ah[u]);
-              So[s] = c;
-              if (staged) sh.cells[fi][s] = c;
-            }
+          for (int u = 0; u < PA; ++u) {
+            ag[u] += x[u].x;
+            ah[u] += x[u].y;
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < PA; ++u) {
+          const int s = s0 + 64 * u;
+          if (s < B) {
+            const longlong2 c = make_longlong2(ag[u], ah[u]);
+            So[s] = c;
+            if (staged) sh.cells[fi][swz(s)] = c;
           }
         }
       }
-    } else if (active && staged) {
-      for (int s = lane; s < B; s += 32) sh.cells[warp][s] = __ldg(Sin + s);
     }
+  } else if (side == 0 && active && staged) {
+    for (int s = lane; s < B; s += 32) sh.cells[warp][swz(s)] = __ldg(Sin + s);
   }
   __syncthreads();
   // phase B: large = parent - small
@@ -904,11 +913,12 @@ __global__ void __launch_bounds__(SCAN_THREADS, 3) k_level_finish(
     bool neg = false;
     if (staged) {
       for (int s = lane; s < B; s += 32) {
-        const longlong2 a = sh.cells[warp][s], b = sh.cells[warp - 4][s];
+        const int q = swz(s);
+        const longlong2 a = sh.cells[warp][q], b = sh.cells[warp - 4][q];
         const longlong2 d = make_longlong2(a.x - b.x, a.y - b.y);
         neg |= d.y < 0;
         L[s] = d;
-        sh.cells[warp][s] = d;
+        sh.cells[warp][q] = d;
       }
     } else {
       // FIN_BATCH loads of each operand in flight per lane before the stores
@@ -941,7 +951,7 @@ __global__ void __launch_bounds__(SCAN_THREADS, 3) k_level_finish(
     int64_t sa = 0;
     if (staged) {
       for (int s = lane; s < B; s += 32) {
-        const longlong2 c = cells[s];
+        const longlong2 c = cells[swz(s)];
         tg += c.x;
         th += c.y;
         sa += c.x < 0 ? -c.x : c.x;
@@ -951,7 +961,7 @@ __global__ void __launch_bounds__(SCAN_THREADS, 3) k_level_finish(
     }
     warp_sum3(tg, th, sa);
     int ovf = 0;
-    const float wlo = warp_scan_push(cells, n_bins, tg, th, sa, sp, f, side, sh, ovf);
+    const float wlo = warp_scan_push(cells, staged, n_bins, tg, th, sa, sp, f, side, sh, ovf);
     ovf = __any_sync(0xffffffffu, ovf);
     if (lane == 0) {
       sh.warp_lo[warp] = wlo;
@@ -962,7 +972,7 @@ __global__ void __launch_bounds__(SCAN_THREADS, 3) k_level_finish(
   float thr[2] = {-INFINITY, -INFINITY};
   for (int w = 0; w < SCAN_WARPS; ++w) thr[w >> 2] = fmaxf(thr[w >> 2], sh.warp_lo[w]);
   if (active && sh.warp_overflow[warp]) {
-    const Cand d = warp_direct_best(cells, n_bins, tg, th, sp, thr[side], f);
+    const Cand d = warp_direct_best(cells, staged, n_bins, tg, th, sp, thr[side], f);
     if (lane == 0) sh.extra[warp] = d;
   }
   __syncthreads();
