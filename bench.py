@@ -365,7 +365,7 @@ def level_summary(ms, entries, level_bytes, peak):
 
 
 KERNELS = ["k_hist_u8", "k_hist_u16", "k_level_plan", "k_subtract_find", "k_level_finish", "k_finalize", "k_find",
-           "k_part_count", "k_part_scan", "k_part_rank", "k_part_offsets", "k_part_scatter"]
+           "k_part_flags", "k_part_scan", "k_part_scatter"]
 
 
 def run_config_level(name, torch, g, dev, stream, args, peak, peak_kind):
@@ -495,6 +495,8 @@ def run_dense_tree(torch, g, dev, stream, args, peak, peak_kind):
             if d > 0:
                 pms, _, _ = tm.run(lambda d=d: part_step(d), K, warmup=1)
                 e["partition_ms"] = statistics.mean(pms)
+                _, _, pk = tm.run(lambda d=d: part_step(d), K, warmup=0, profile_kernels=KERNELS)
+                e["partition_kernels_ms_per_launch"] = pk
             levels.append(e)
         tms, tl, _ = tm.run(tree_step, max(2, K // 2), warmup=1)
         assert sess.sync() == 0

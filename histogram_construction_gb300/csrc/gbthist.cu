@@ -101,7 +101,7 @@ struct gbt_ctx {
   DevState *st = nullptr;
   uint32_t *err_host = nullptr;  // pinned: [0] error word copy, [1] max |q| copy, [2] multi-output max |q| copy
   Buf gp_stage, chunk_prefix, partial, rows_in, offs_in, cand, splits_a, splits_b, parent_of_in, tile_counts, lrank,
-      slab, counters, level_scratch, items, side_in;
+      slab, counters, level_scratch, items, side_in, pflags;
   std::string last_error;
   int64_t launches = 0;
   // tuning: work items the level plan aims for (default 1 per SM; GBT_TARGET_ITEMS overrides it for sweeps)
@@ -400,7 +400,7 @@ gbt_status gbt_destroy(gbt_ctx *c) {
   cudaStreamSynchronize(c->stream);
   Buf *bufs[] = {&c->mirror, &c->q, &c->gp_stage, &c->chunk_prefix, &c->partial, &c->rows_in, &c->offs_in,
                  &c->cand, &c->splits_a, &c->splits_b, &c->parent_of_in, &c->tile_counts, &c->lrank, &c->slab,
-                 &c->counters, &c->level_scratch, &c->qm, &c->items, &c->side_in};
+                 &c->counters, &c->level_scratch, &c->qm, &c->items, &c->side_in, &c->pflags};
   for (Buf *b : bufs) release(c, *b);
   if (c->st) cudaFreeAsync(c->st, c->stream);
   cudaStreamSynchronize(c->stream);
@@ -1175,6 +1175,8 @@ gbt_status partition_impl(gbt_ctx *c, const int32_t *rows, const int64_t *node_o
   if (s != GBT_OK) return s;
   s = ensure(c, c->lrank, (size_t)(n_nodes + 1) * sizeof(int64_t), "partition node ranks");
   if (s != GBT_OK) return s;
+  s = ensure(c, c->pflags, (size_t)n_tiles * (PART_TILE / 8) + 16, "partition flags");
+  if (s != GBT_OK) return s;
   PartParams pp;
   pp.rows = (const int32_t *)rows_d;
   pp.offs = (const int64_t *)offs_d;
@@ -1188,27 +1190,22 @@ gbt_status partition_impl(gbt_ctx *c, const int32_t *rows, const int64_t *node_o
   pp.mirror = (const unsigned char *)c->mirror.p;
   pp.splits = (const SplitOut *)sp_d;
   pp.tile_counts = (int64_t *)c->tile_counts.p;
+  pp.flags = (uint8_t *)c->pflags.p;
+  pp.lrank = (int64_t *)c->lrank.p;
   pp.out_rows = out_rows;
   pp.out_offs = out_offsets;
   pp.small_rows = pairs ? small_rows : nullptr;
   pp.small_offs = pairs ? small_offsets : nullptr;
   pp.small_side = pairs ? small_side : nullptr;
   pp.st = c->st;
-  int64_t *lrank = (int64_t *)c->lrank.p;
   prof_begin(c);
-  k_part_count<<<(unsigned)n_tiles, PART_THREADS, 0, c->stream>>>(pp);
-  LAUNCH_CHECK(c, "k_part_count");
+  k_part_flags<<<(unsigned)n_tiles, PART_THREADS, 0, c->stream>>>(pp);
+  LAUNCH_CHECK(c, "k_part_flags");
   prof_begin(c);
   k_part_scan<<<1, 1024, 0, c->stream>>>(pp, n_tiles);
   LAUNCH_CHECK(c, "k_part_scan");
   prof_begin(c);
-  k_part_rank<<<(unsigned)n_tiles, PART_THREADS, 0, c->stream>>>(pp, lrank);
-  LAUNCH_CHECK(c, "k_part_rank");
-  prof_begin(c);
-  k_part_offsets<<<1, 32, 0, c->stream>>>(pp, lrank, n_tiles);
-  LAUNCH_CHECK(c, "k_part_offsets");
-  prof_begin(c);
-  k_part_scatter<<<(unsigned)n_tiles, PART_THREADS, 0, c->stream>>>(pp, lrank);
+  k_part_scatter<<<(unsigned)n_tiles, PART_THREADS, 0, c->stream>>>(pp);
   LAUNCH_CHECK(c, "k_part_scatter");
   return GBT_OK;
 }

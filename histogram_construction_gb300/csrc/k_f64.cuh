@@ -42,13 +42,16 @@ __global__ void __launch_bounds__(256) k_finalize_f64(double *__restrict__ parti
     double g = 0.0, h = 0.0;
     const int32_t i0 = img_first[n];
     const bool zero = i0 < r_cap;  // reduce-region images are zeroed as they are read
-    for (int32_t k = group_prefix[n]; k < group_prefix[n + 1]; ++k) {
-      double *src = partial + ((int64_t)(i0 + k - group_prefix[n]) * n_fgroups + fg) * image_doubles + cell;
-      const double2 x = __ldcg(reinterpret_cast<const double2 *>(src));
-      if (zero) __stcg(reinterpret_cast<double2 *>(src), make_double2(0.0, 0.0));
+    const int32_t ng = group_prefix[n + 1] - group_prefix[n];
+    double *src0 = partial + ((int64_t)i0 * n_fgroups + fg) * image_doubles + cell;
+    const int64_t gstride = (int64_t)n_fgroups * image_doubles;
+    for (int32_t k = 0; k < ng; ++k) {  // loads first, then the zeroing stores
+      const double2 x = __ldcg(reinterpret_cast<const double2 *>(src0 + k * gstride));
       g += x.x;
       h += x.y;
     }
+    if (zero)
+      for (int32_t k = 0; k < ng; ++k) __stcg(reinterpret_cast<double2 *>(src0 + k * gstride), make_double2(0.0, 0.0));
     double *d = hist_out + (((int64_t)n * n_features + f) * B + s) * 2;
     d[0] = g;
     d[1] = h;

@@ -1104,12 +1104,16 @@ __global__ void __launch_bounds__(256) k_finalize(PartialView v, int32_t n_nodes
     const bool zero = i0 < v.r_cap;
     int2 *cell = image_cell(v, i0, f, item_feats, s);
     int64_t g = 0, h = 0;
-    for (int32_t k = g0; k < g1; ++k, cell += image_stride) {
-      const int2 x = __ldcg(cell);
-      if (zero) __stcg(cell, make_int2(0, 0));
+    // the loads first, then the zeroing stores (a store between two loads
+    // would keep the next load from being issued before the store)
+    int2 *c = cell;
+    for (int32_t k = g0; k < g1; ++k, c += image_stride) {
+      const int2 x = __ldcg(c);
       g += x.x;
       h += x.y;
     }
+    if (zero)
+      for (int32_t k = g0; k < g1; ++k, cell += image_stride) __stcg(cell, make_int2(0, 0));
     reinterpret_cast<longlong2 *>(hist_out)[((int64_t)n * n_features + f) * v.B + s] = make_longlong2(g, h);
   }
 }
@@ -1146,12 +1150,14 @@ __global__ void __launch_bounds__(256) k_finalize_multi(PartialView v, int32_t n
     const int64_t image = (int64_t)i0 * v.n_fgroups + (int64_t)tg * nfq + fq;
     int2 *cell = reinterpret_cast<int2 *>(v.partial) + image * v.image_int4s * 2 + ((int64_t)tl * v.B + s) * 16 + fl;
     int64_t g = 0, h = 0;
-    for (int32_t k = g0; k < g1; ++k, cell += image_stride) {
-      const int2 x = __ldcg(cell);
-      if (zero) __stcg(cell, make_int2(0, 0));
+    int2 *c = cell;
+    for (int32_t k = g0; k < g1; ++k, c += image_stride) {  // loads first, then the zeroing stores
+      const int2 x = __ldcg(c);
       g += x.x;
       h += x.y;
     }
+    if (zero)
+      for (int32_t k = g0; k < g1; ++k, cell += image_stride) __stcg(cell, make_int2(0, 0));
     reinterpret_cast<longlong2 *>(hist_out)[(((int64_t)t * n_nodes + n) * n_features + f) * v.B + s] =
         make_longlong2(g, h);
   }

@@ -882,15 +882,18 @@ __global__ void __launch_bounds__(SCAN_THREADS, 3) k_level_finish(
             const int s = s0 + 64 * u;
             x[u] = s < B ? __ldcg(img + s * sstride) : make_int2(0, 0);
           }
-          if (zero) {
-#pragma unroll
-            for (int u = 0; u < PA; ++u)
-              if (s0 + 64 * u < B) __stcg(img + (s0 + 64 * u) * sstride, make_int2(0, 0));
-          }
 #pragma unroll
           for (int u = 0; u < PA; ++u) {
             ag[u] += x[u].x;
             ah[u] += x[u].y;
+          }
+        }
+        if (zero) {  // after all the loads (a store would hold back the loads after it)
+          img = img0;
+          for (int32_t k = g0; k < g1; ++k, img += stride) {
+#pragma unroll
+            for (int u = 0; u < PA; ++u)
+              if (s0 + 64 * u < B) __stcg(img + (s0 + 64 * u) * sstride, make_int2(0, 0));
           }
         }
 #pragma unroll
