@@ -1057,15 +1057,21 @@ gbt_status run_level_finish(gbt_ctx *c, const SmallSource &src, const int64_t *p
     if (s != GBT_OK) return s;
   }
   const int nfb = (c->n_features + 3) / 4;
-  s = ensure(c, c->cand, (size_t)2 * n_pairs * nfb * PUB_K * sizeof(Cand), "candidates");
+  // candidate records, then their bounds (lo, up) as float2 (16-byte aligned: the records are 64 bytes)
+  const size_t n_ent = (size_t)2 * n_pairs * nfb * PUB_K;
+  s = ensure(c, c->cand, n_ent * (sizeof(Cand) + sizeof(float2)), "candidates");
   if (s != GBT_OK) return s;
+  float2 *cbounds = reinterpret_cast<float2 *>((Cand *)c->cand.p + n_ent);
   s = ensure_counters(c, (size_t)n_pairs);  // arrival counters
   if (s != GBT_OK) return s;
   const SplitParams sp = make_sp(c, params);
   prof_begin(c);
-  launch_pdl(c, k_level_finish<FROM_PARTIALS>, dim3(nfb, n_pairs), dim3(SCAN_THREADS), 0, src, parent_hist, po,
-             large_hist, c->n_features, c->n_bins, sp, (Cand *)c->cand.p, (uint32_t *)c->counters.p, da, db, c->st,
-             side);
+  // staged strips: the 4-CTA register budget when the grid is more than one wave of 3 CTAs per SM
+  auto kern = c->n_bins + 1 > STAGE_SLOTS                  ? k_level_finish<FROM_PARTIALS, false, 3>
+               : (int64_t)nfb * n_pairs > 3 * (int64_t)c->n_sm ? k_level_finish<FROM_PARTIALS, true, 4>
+                                                              : k_level_finish<FROM_PARTIALS, true, 3>;
+  launch_pdl(c, kern, dim3(nfb, n_pairs), dim3(SCAN_THREADS), 0, src, parent_hist, po, large_hist, c->n_features,
+             c->n_bins, sp, (Cand *)c->cand.p, cbounds, (uint32_t *)c->counters.p, da, db, c->st, side);
   LAUNCH_CHECK(c, FROM_PARTIALS ? "k_level_finish" : "k_subtract_find");
   if (FROM_PARTIALS) c->img_clean = c->img_r_pending;
   if (ha)

@@ -166,6 +166,26 @@ __device__ __forceinline__ void screen_fast(int64_t GL, int64_t HL, int64_t GR, 
   lo = __fsub_rn(g, err);
 }
 
+// Upper bound on the gain of every valid candidate (HL, HR >= h_min) of a run
+// of consecutive cuts of one missing direction in a strip that passed
+// strip_fast: gl_mn, gl_mx bound GL over the run (int64, the missing slot
+// already added for missing-left), HL rises from hl_a to hl_b. The gain
+// term GL^2/(HL + lambda) is largest at the largest |GL| and the smallest
+// valid HL, the right term likewise at the largest |G - GL| and the
+// smallest valid HR, so screen_fast's upper bound of that (possibly
+// unreal) corner candidate bounds every candidate of the run: its inputs
+// are sums of subsets of the strip's slots, within strip_fast's ranges.
+__device__ __forceinline__ float run_bound(int64_t gl_mn, int64_t gl_mx, int64_t hl_a, int64_t hl_b, int64_t tg,
+                                           int64_t th, float Gf2den, const SplitParams &sp) {
+  const int64_t ga = max(gl_mn < 0 ? -gl_mn : gl_mn, gl_mx < 0 ? -gl_mx : gl_mx);
+  const int64_t r1 = tg - gl_mn, r2 = tg - gl_mx;
+  const int64_t gb = max(r1 < 0 ? -r1 : r1, r2 < 0 ? -r2 : r2);
+  const int64_t hl = max(hl_a, sp.h_min), hr = max(th - hl_b, sp.h_min);
+  float up, lo;
+  screen_fast(ga, hl, gb, hr, Gf2den, sp, up, lo);
+  return up;
+}
+
 __device__ __forceinline__ int64_t shfl_i64(int64_t v, int src) {
   return (int64_t)__shfl_sync(0xffffffffu, (long long)v, src);
 }
@@ -379,12 +399,21 @@ __device__ __forceinline__ void strip_totals(const longlong2 *cells, int B, int6
 // missing directions), so its gain equals that earlier candidate's and the
 // serial order never picks it: such cuts are skipped (runs of empty bins would
 // otherwise flood the survivor pool with exact ties).
-template <int ND, int MODE>
+//
+// SKIP (long strips under the fast screen): a chunk is skipped whole when an
+// upper bound on all its candidates (run_bound) lies below the best lower
+// bound found so far by the warps of the same node set in this CTA
+// (set_warps warps from the set's first, each publishing its running bound
+// in sh.warp_lo). Every skipped candidate's gain is then strictly below
+// another candidate's, so it cannot be chosen.
+template <int ND, int MODE, bool SKIP>
 __device__ __forceinline__ float scan_push_impl(const longlong2 *cells, bool sw, int n_bins, int64_t tg, int64_t th,
                                                 longlong2 m, float Gf2den, const SplitParams &sp, int f, int node,
-                                                ScanShared &sh, int &overflow, int mode) {
+                                                ScanShared &sh, int &overflow, int mode, int set_warps) {
   if (MODE >= 0) mode = MODE;
-  const int lane = threadIdx.x & 31;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int sw0 = warp - warp % set_warps;
+  volatile float *vlo = sh.warp_lo;
   float run_lo = -INFINITY;
   int64_t carry_g = 0, carry_h = 0;
   for (int c0 = 0; c0 < n_bins; c0 += 32 * SCAN_SPL) {
@@ -412,8 +441,29 @@ __device__ __forceinline__ float scan_push_impl(const longlong2 *cells, bool sw,
     const int64_t tot_g = shfl_i64(eg, 31), tot_h = shfl_i64(eh, 31);
     eg += carry_g - ag;  // exclusive prefix of the lane's first slot
     eh += carry_h - ah;
+    const int64_t h_a = carry_h;  // HL over the chunk's cuts lies in [h_a, h_b]
     carry_g += tot_g;
     carry_h += tot_h;
+    if (SKIP && MODE == 0) {
+      float sthr = run_lo;
+      for (int w = 0; w < set_warps; ++w) sthr = fmaxf(sthr, vlo[sw0 + w]);
+      if (sthr > -INFINITY) {
+        int64_t mn = eg + pg[0], mx = mn;
+#pragma unroll
+        for (int i = 1; i < SCAN_SPL; ++i) {
+          mn = min(mn, eg + pg[i]);
+          mx = max(mx, eg + pg[i]);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          mn = min(mn, shfl_xor_i64(mn, o));
+          mx = max(mx, shfl_xor_i64(mx, o));
+        }
+        float ub = run_bound(mn, mx, h_a, carry_h, tg, th, Gf2den, sp);
+        if (ND == 2) ub = fmaxf(ub, run_bound(mn + m.x, mx + m.x, h_a + m.y, carry_h + m.y, tg, th, Gf2den, sp));
+        if (ub < sthr) continue;  // no candidate of the chunk can reach the set's best
+      }
+    }
     float up[SCAN_SPL][ND], lo[SCAN_SPL][ND];
     uint32_t vmask = 0;
     float l = -INFINITY;
@@ -440,7 +490,10 @@ __device__ __forceinline__ float scan_push_impl(const longlong2 *cells, bool sw,
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) l = fmaxf(l, __shfl_xor_sync(0xffffffffu, l, o));
-    run_lo = fmaxf(run_lo, l);
+    if (l > run_lo) {
+      run_lo = l;
+      if (SKIP && MODE == 0 && lane == 0) vlo[warp] = run_lo;  // the other warps of the set may skip by it
+    }
 #pragma unroll
     for (int i = 0; i < SCAN_SPL; ++i) {
 #pragma unroll
@@ -473,16 +526,25 @@ __device__ __forceinline__ float scan_push_impl(const longlong2 *cells, bool sw,
 // sw: a staged strip (shared memory, slot s at swz(s)).
 __device__ __forceinline__ float warp_scan_push(const longlong2 *cells, bool sw, int n_bins, int64_t tg, int64_t th,
                                                 int64_t sabs, const SplitParams &sp, int f, int node, ScanShared &sh,
-                                                int &overflow) {
+                                                int &overflow, int set_warps) {
   const longlong2 m = cells[sw ? swz(n_bins) : n_bins];
   const bool no_missing = (m.x == 0 && m.y == 0);
   const float Gf2den = parent_f32(tg, th, sp);
   const bool fast = strip_fast(sabs, th, Gf2den, sp);
-  // the common cases (fast screen, with or without missing values) get their own copies
-  if (fast && no_missing)
-    return scan_push_impl<1, 0>(cells, sw, n_bins, tg, th, m, Gf2den, sp, f, node, sh, overflow, 0);
-  if (fast) return scan_push_impl<2, 0>(cells, sw, n_bins, tg, th, m, Gf2den, sp, f, node, sh, overflow, 0);
-  return scan_push_impl<2, -1>(cells, sw, n_bins, tg, th, m, Gf2den, sp, f, node, sh, overflow, sp.filter ? 1 : 2);
+  // the common cases (fast screen, with or without missing values) get their own copies; chunk
+  // skipping only pays on long strips (in global memory): a staged strip has two chunks
+  if (fast && no_missing) {
+    if (sw) return scan_push_impl<1, 0, false>(cells, sw, n_bins, tg, th, m, Gf2den, sp, f, node, sh, overflow, 0,
+                                               set_warps);
+    return scan_push_impl<1, 0, true>(cells, sw, n_bins, tg, th, m, Gf2den, sp, f, node, sh, overflow, 0, set_warps);
+  }
+  if (fast) {
+    if (sw) return scan_push_impl<2, 0, false>(cells, sw, n_bins, tg, th, m, Gf2den, sp, f, node, sh, overflow, 0,
+                                               set_warps);
+    return scan_push_impl<2, 0, true>(cells, sw, n_bins, tg, th, m, Gf2den, sp, f, node, sh, overflow, 0, set_warps);
+  }
+  return scan_push_impl<2, -1, false>(cells, sw, n_bins, tg, th, m, Gf2den, sp, f, node, sh, overflow,
+                                      sp.filter ? 1 : 2, set_warps);
 }
 
 __device__ __forceinline__ double surv_gain(int64_t gl, int64_t hl, int64_t tg, int64_t th, const SplitParams &sp) {
@@ -713,14 +775,73 @@ __device__ __forceinline__ void reduce_node(const Cand *cand, int n_ent, const S
   }
 }
 
-// Stores the CTA's published candidates (dst[set] + 0 .. PUB_K-1) and counts
-// the CTA in; returns true in the last CTA of the group, which resets the
+// reduce_node for published entries whose bounds are also stored compactly,
+// cb[i] = (lo, up) of entry i (n_ent even, cb 16-byte aligned): both passes
+// read 8 bytes per entry, two entries per 16-byte load, and only the entries
+// whose upper bound reaches the threshold are read in full.
+__device__ __forceinline__ void reduce_node_cb(const Cand *cand, const float2 *cb, int n_ent, const SplitParams &sp,
+                                               SplitOut *out, int t0, int nthr, int bar, Cand *slot, float *sthr) {
+  const int t = threadIdx.x - t0, lane = threadIdx.x & 31, w = t >> 5, nw = nthr >> 5;
+  constexpr int RB = 8;  // 16-byte loads in flight per thread
+  const float4 *cb4 = reinterpret_cast<const float4 *>(cb);
+  const int n4 = n_ent >> 1;
+  float thr = -INFINITY;
+  for (int i0 = t; i0 < n4; i0 += nthr * RB) {
+    float4 v[RB];
+#pragma unroll
+    for (int u = 0; u < RB; ++u) {
+      const int i = i0 + u * nthr;
+      v[u] = i < n4 ? __ldcg(cb4 + i) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+    }
+#pragma unroll
+    for (int u = 0; u < RB; ++u) thr = fmaxf(thr, fmaxf(v[u].x, v[u].z));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) thr = fmaxf(thr, __shfl_xor_sync(0xffffffffu, thr, o));
+  if (lane == 0) sthr[w] = thr;
+  named_sync(bar, nthr);
+  for (int k = 0; k < nw; ++k) thr = fmaxf(thr, sthr[k]);
+  Cand best = no_cand();
+  for (int i0 = t; i0 < n4; i0 += nthr * RB) {
+    uint32_t pass = 0;  // bit 2u + e: entry 2 (i0 + u nthr) + e reaches the threshold
+#pragma unroll
+    for (int u = 0; u < RB; ++u) {
+      const int i = i0 + u * nthr;
+      if (i < n4) {
+        const float4 x = __ldcg(cb4 + i);
+        pass |= (x.y >= thr ? 1u : 0u) << (2 * u);
+        pass |= (x.w >= thr ? 1u : 0u) << (2 * u + 1);
+      }
+    }
+    // one copy of the evaluation, however many entries pass
+    while (pass) {
+      const int b = __ffs(pass) - 1;
+      pass &= pass - 1u;
+      Cand c = load_cand(cand + 2 * (i0 + (b >> 1) * nthr) + (b & 1));
+      if (c.f == INT32_MAX) continue;
+      if (!c.exact) set_exact(c, surv_gain(c.gl, c.hl, c.gl + c.gr, c.hl + c.hr, sp));
+      if (cand_better(c, best)) best = c;
+    }
+  }
+  if (lane == warp_argmax_lane(best)) slot[w] = best;
+  named_sync(bar, nthr);
+  if (w == 0) {
+    const Cand b = lane < nw ? slot[lane] : no_cand();
+    if (lane == warp_argmax_lane(b)) *out = cand_to_split(b);
+  }
+}
+
+// Stores the CTA's published candidates (dst[set] + 0 .. PUB_K-1), and their
+// bounds (lo, up) in cb[set] + 0 .. PUB_K-1 when cb0 is given, and counts the
+// CTA in; returns true in the last CTA of the group, which resets the
 // counter. No CTA waits.
 __device__ __forceinline__ bool cta_publish(ScanShared &sh, int n_sets, Cand *dst0, Cand *dst1, uint32_t *counter,
-                                            uint32_t group_ctas) {
+                                            uint32_t group_ctas, float2 *cb0 = nullptr, float2 *cb1 = nullptr) {
   if (threadIdx.x < n_sets * PUB_K) {
     const int set = threadIdx.x / PUB_K, k = threadIdx.x % PUB_K;
-    (set == 0 ? dst0 : dst1)[k] = sh.pub[set][k];
+    const Cand &c = sh.pub[set][k];
+    (set == 0 ? dst0 : dst1)[k] = c;
+    if (cb0) (set == 0 ? cb0 : cb1)[k] = make_float2(c.lo, c.up);
     __threadfence();
   }
   __syncthreads();
@@ -775,7 +896,7 @@ __global__ void __launch_bounds__(SCAN_THREADS, 3) k_find(const int64_t *__restr
     warp_sum3(tg, th, sa);
     __syncwarp();
     int ovf = 0;
-    const float wlo = warp_scan_push(cells, staged, n_bins, tg, th, sa, sp, f, 0, sh, ovf);
+    const float wlo = warp_scan_push(cells, staged, n_bins, tg, th, sa, sp, f, 0, sh, ovf, SCAN_WARPS);
     ovf = __any_sync(0xffffffffu, ovf);
     if (lane == 0) {
       sh.warp_lo[warp] = wlo;
@@ -822,19 +943,23 @@ struct SmallSource {
 // p's outputs go to node 2p + node_side[p] (small) and 2p + 1 - node_side[p] (large) of
 // one level array instead (the small histogram's own index, small_out and
 // hist_out, and large / large_out then name the same arrays).
-template <bool FROM_PARTIALS>
-__global__ void __launch_bounds__(SCAN_THREADS, 3) k_level_finish(
+// STAGED: the instance for B <= STAGE_SLOTS (strips in shared memory), compiled
+// without the long-strip paths. CTAS: resident CTAs per SM the registers are
+// budgeted for (4 pays when the grid is several waves: more warps hide the
+// latency of each CTA's chain; 3 keeps a one-wave grid's chains shorter).
+template <bool FROM_PARTIALS, bool STAGED, int CTAS>
+__global__ void __launch_bounds__(SCAN_THREADS, CTAS) k_level_finish(
     SmallSource src, const int64_t *__restrict__ parent, const int32_t *__restrict__ parent_of,
     int64_t *__restrict__ large, int32_t n_features, int32_t n_bins, SplitParams sp, Cand *__restrict__ cand,
-    uint32_t *__restrict__ counters, SplitOut *__restrict__ small_out, SplitOut *__restrict__ large_out,
-    DevState *st, const uint8_t *__restrict__ node_side) {
+    float2 *__restrict__ cbounds, uint32_t *__restrict__ counters, SplitOut *__restrict__ small_out,
+    SplitOut *__restrict__ large_out, DevState *st, const uint8_t *__restrict__ node_side) {
   __shared__ ScanShared sh;
   const int p = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int fo = warp & 3, side = warp >> 2;
   const int f = blockIdx.x * 4 + fo;
   const int B = n_bins + 1;
-  const bool staged = B <= STAGE_SLOTS;
+  const bool staged = STAGED;  // B <= STAGE_SLOTS (the host picks the instance)
   const bool active = f < n_features;
   const int64_t pp = parent_of ? (int64_t)parent_of[p] : p;
   const longlong2 *P = reinterpret_cast<const longlong2 *>(parent) + (pp * n_features + f) * B;
@@ -964,7 +1089,7 @@ __global__ void __launch_bounds__(SCAN_THREADS, 3) k_level_finish(
     }
     warp_sum3(tg, th, sa);
     int ovf = 0;
-    const float wlo = warp_scan_push(cells, staged, n_bins, tg, th, sa, sp, f, side, sh, ovf);
+    const float wlo = warp_scan_push(cells, staged, n_bins, tg, th, sa, sp, f, side, sh, ovf, 4);
     ovf = __any_sync(0xffffffffu, ovf);
     if (lane == 0) {
       sh.warp_lo[warp] = wlo;
@@ -984,13 +1109,15 @@ __global__ void __launch_bounds__(SCAN_THREADS, 3) k_level_finish(
   for (int w = 0; w < SCAN_WARPS; ++w) warp_node[w] = w >> 2;
   cta_select(sh, sp, 2, thr, warp_node);
   const int nfb = gridDim.x;
-  Cand *cs_base = cand + (int64_t)(2 * p) * nfb * PUB_K;
-  Cand *cl_base = cand + (int64_t)(2 * p + 1) * nfb * PUB_K;
-  if (cta_publish(sh, 2, cs_base + blockIdx.x * PUB_K, cl_base + blockIdx.x * PUB_K, counters + p, nfb)) {
+  const int64_t es = (int64_t)(2 * p) * nfb * PUB_K, el = es + (int64_t)nfb * PUB_K;  // the siblings' first entries
+  if (cta_publish(sh, 2, cand + es + blockIdx.x * PUB_K, cand + el + blockIdx.x * PUB_K, counters + p, nfb,
+                  cbounds + es + blockIdx.x * PUB_K, cbounds + el + blockIdx.x * PUB_K)) {
     __threadfence();
     // warps 0-3 reduce the small sibling, warps 4-7 the large one
-    if (threadIdx.x < 128) reduce_node(cs_base, nfb * PUB_K, sp, small_out + si, 0, 128, 1, sh.extra, sh.red);
-    else reduce_node(cl_base, nfb * PUB_K, sp, large_out + li, 128, 128, 2, sh.extra + 4, sh.red + 4);
+    if (threadIdx.x < 128)
+      reduce_node_cb(cand + es, cbounds + es, nfb * PUB_K, sp, small_out + si, 0, 128, 1, sh.extra, sh.red);
+    else
+      reduce_node_cb(cand + el, cbounds + el, nfb * PUB_K, sp, large_out + li, 128, 128, 2, sh.extra + 4, sh.red + 4);
   }
 }
 
