@@ -1066,8 +1066,9 @@ gbt_status run_level_finish(gbt_ctx *c, const SmallSource &src, const int64_t *p
   if (s != GBT_OK) return s;
   const SplitParams sp = make_sp(c, params);
   prof_begin(c);
-  // staged strips: the 4-CTA register budget when the grid is more than one wave of 3 CTAs per SM
-  auto kern = c->n_bins + 1 > STAGE_SLOTS                  ? k_level_finish<FROM_PARTIALS, false, 3>
+  // staged strips: the 4-CTA register budget when the grid is more than one wave of 3 CTAs per SM;
+  // long strips: two CTAs per SM, whose register budget holds the long scan without spills
+  auto kern = c->n_bins + 1 > STAGE_SLOTS                  ? k_level_finish<FROM_PARTIALS, false, 2>
                : (int64_t)nfb * n_pairs > 3 * (int64_t)c->n_sm ? k_level_finish<FROM_PARTIALS, true, 4>
                                                               : k_level_finish<FROM_PARTIALS, true, 3>;
   launch_pdl(c, kern, dim3(nfb, n_pairs), dim3(SCAN_THREADS), 0, src, parent_hist, po, large_hist, c->n_features,

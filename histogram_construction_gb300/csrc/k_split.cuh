@@ -150,13 +150,21 @@ __device__ __forceinline__ bool strip_fast(int64_t sabs, int64_t th, float Gf2de
          __fadd_rn(__fmul_rn(3.0f, amax), sp.gamma_abs_f) < rhi;
 }
 
+// Integer -> float, rounded once (relative error at most u): a 32-bit value
+// by the conversion instruction, a 64-bit one below 2^45 by i45_to_f32.
+__device__ __forceinline__ float to_f32(int32_t x) { return __int2float_rn(x); }
+__device__ __forceinline__ float to_f32(int64_t x) { return i45_to_f32(x); }
+
 // screen_f32 for a strip that passed strip_fast (same bound, no range checks).
-__device__ __forceinline__ void screen_fast(int64_t GL, int64_t HL, int64_t GR, int64_t HR, float Gf2den,
-                                            const SplitParams &sp, float &up, float &lo) {
-  const float gl = __fmul_rn(i45_to_f32(GL), sp.inv_sg_f);
-  const float hl = __fmul_rn(i45_to_f32(HL), sp.inv_sh_f);
-  const float gr = __fmul_rn(i45_to_f32(GR), sp.inv_sg_f);
-  const float hr = __fmul_rn(i45_to_f32(HR), sp.inv_sh_f);
+// I: the integer type of the sums (int32_t when every partial sum of the
+// strip fits, which the caller has checked).
+template <typename I>
+__device__ __forceinline__ void screen_fast(I GL, I HL, I GR, I HR, float Gf2den, const SplitParams &sp, float &up,
+                                            float &lo) {
+  const float gl = __fmul_rn(to_f32(GL), sp.inv_sg_f);
+  const float hl = __fmul_rn(to_f32(HL), sp.inv_sh_f);
+  const float gr = __fmul_rn(to_f32(GR), sp.inv_sg_f);
+  const float hr = __fmul_rn(to_f32(HR), sp.inv_sh_f);
   const float a = __fdividef(__fmul_rn(gl, gl), __fadd_rn(hl, sp.lambda_f));
   const float b = __fdividef(__fmul_rn(gr, gr), __fadd_rn(hr, sp.lambda_f));
   const float ab = __fadd_rn(a, b);
@@ -175,14 +183,16 @@ __device__ __forceinline__ void screen_fast(int64_t GL, int64_t HL, int64_t GR, 
 // smallest valid HR, so screen_fast's upper bound of that (possibly
 // unreal) corner candidate bounds every candidate of the run: its inputs
 // are sums of subsets of the strip's slots, within strip_fast's ranges.
-__device__ __forceinline__ float run_bound(int64_t gl_mn, int64_t gl_mx, int64_t hl_a, int64_t hl_b, int64_t tg,
-                                           int64_t th, float Gf2den, const SplitParams &sp) {
-  const int64_t ga = max(gl_mn < 0 ? -gl_mn : gl_mn, gl_mx < 0 ? -gl_mx : gl_mx);
-  const int64_t r1 = tg - gl_mn, r2 = tg - gl_mx;
-  const int64_t gb = max(r1 < 0 ? -r1 : r1, r2 < 0 ? -r2 : r2);
-  const int64_t hl = max(hl_a, sp.h_min), hr = max(th - hl_b, sp.h_min);
+// I as in screen_fast; hm: h_min in I.
+template <typename I>
+__device__ __forceinline__ float run_bound(I gl_mn, I gl_mx, I hl_a, I hl_b, I tg, I th, I hm, float Gf2den,
+                                           const SplitParams &sp) {
+  const I ga = max(gl_mn < 0 ? -gl_mn : gl_mn, gl_mx < 0 ? -gl_mx : gl_mx);
+  const I r1 = tg - gl_mn, r2 = tg - gl_mx;
+  const I gb = max(r1 < 0 ? -r1 : r1, r2 < 0 ? -r2 : r2);
+  const I hl = max(hl_a, hm), hr = max(th - hl_b, hm);
   float up, lo;
-  screen_fast(ga, hl, gb, hr, Gf2den, sp, up, lo);
+  screen_fast<I>(ga, hl, gb, hr, Gf2den, sp, up, lo);
   return up;
 }
 
@@ -196,11 +206,16 @@ __device__ __forceinline__ int64_t shfl_xor_i64(int64_t v, int m) {
   return (int64_t)__shfl_xor_sync(0xffffffffu, (long long)v, m);
 }
 
-__device__ __forceinline__ void warp_incl_scan(int64_t &pg, int64_t &ph) {
+__device__ __forceinline__ int32_t shfl_i64(int32_t v, int src) { return __shfl_sync(0xffffffffu, v, src); }
+__device__ __forceinline__ int32_t shfl_up_i64(int32_t v, int d) { return __shfl_up_sync(0xffffffffu, v, d); }
+__device__ __forceinline__ int32_t shfl_xor_i64(int32_t v, int m) { return __shfl_xor_sync(0xffffffffu, v, m); }
+
+template <typename I>
+__device__ __forceinline__ void warp_incl_scan(I &pg, I &ph) {
   const int lane = threadIdx.x & 31;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    const int64_t yg = shfl_up_i64(pg, o), yh = shfl_up_i64(ph, o);
+    const I yg = shfl_up_i64(pg, o), yh = shfl_up_i64(ph, o);
     if (lane >= o) {
       pg += yg;
       ph += yh;
@@ -377,7 +392,8 @@ __device__ __forceinline__ bool no_missing_rt(longlong2 m) { return m.x == 0 && 
 // in flight per lane (a loop that used each load at once would wait for every
 // one of them in turn).
 constexpr int FIN_BATCH = 8;
-__device__ __forceinline__ void strip_totals(const longlong2 *cells, int B, int64_t &tg, int64_t &th, int64_t &sa) {
+__device__ __forceinline__ void strip_totals(const longlong2 *cells, int B, int64_t &tg, int64_t &th, int64_t &sa,
+                                             bool &hneg) {
   const int lane = threadIdx.x & 31;
   for (int s0 = lane; s0 < B; s0 += 32 * FIN_BATCH) {
     longlong2 c[FIN_BATCH];
@@ -391,6 +407,7 @@ __device__ __forceinline__ void strip_totals(const longlong2 *cells, int B, int6
       tg += c[u].x;
       th += c[u].y;
       sa += c[u].x < 0 ? -c[u].x : c[u].x;
+      hneg |= c[u].y < 0;
     }
   }
 }
@@ -406,49 +423,56 @@ __device__ __forceinline__ void strip_totals(const longlong2 *cells, int B, int6
 // (set_warps warps from the set's first, each publishing its running bound
 // in sh.warp_lo). Every skipped candidate's gain is then strictly below
 // another candidate's, so it cannot be chosen.
-template <int ND, int MODE, bool SKIP>
-__device__ __forceinline__ float scan_push_impl(const longlong2 *cells, bool sw, int n_bins, int64_t tg, int64_t th,
-                                                longlong2 m, float Gf2den, const SplitParams &sp, int f, int node,
+// I: the integer type of the prefix sums (int32_t only under the fast screen,
+// when every partial sum of the strip fits: fewer instructions per cut).
+template <int ND, int MODE, bool SKIP, typename I>
+__device__ __forceinline__ float scan_push_impl(const longlong2 *cells, bool sw, int n_bins, int64_t tg64, int64_t th64,
+                                                longlong2 m64, float Gf2den, const SplitParams &sp, int f, int node,
                                                 ScanShared &sh, int &overflow, int mode, int set_warps) {
   if (MODE >= 0) mode = MODE;
+  const I tg = (I)tg64, th = (I)th64, h_min = (I)sp.h_min;  // exact: the caller checked the range for int32_t
+  struct {
+    I x, y;
+  } m = {(I)m64.x, (I)m64.y};
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int sw0 = warp - warp % set_warps;
   volatile float *vlo = sh.warp_lo;
   float run_lo = -INFINITY;
-  int64_t carry_g = 0, carry_h = 0;
+  I carry_g = 0, carry_h = 0;
   for (int c0 = 0; c0 < n_bins; c0 += 32 * SCAN_SPL) {
     // the next chunk's cells on their way to L1 while this chunk is screened
     // (strips in global memory: u16 bins)
     // (clamped to the strip's missing slot: the address stays inside the strip)
     if (c0 + 32 * SCAN_SPL < n_bins && !__isShared(cells))
       asm volatile("prefetch.global.L1 [%0];" ::"l"(cells + min(c0 + 32 * SCAN_SPL + SCAN_SPL * lane, n_bins)));
-    int64_t pg[SCAN_SPL], ph[SCAN_SPL];
-    int64_t ag = 0, ah = 0;
+    I pg[SCAN_SPL], ph[SCAN_SPL];
+    I ag = 0, ah = 0;
     uint32_t nzmask = 0;  // slots of the lane whose cell is not empty
 #pragma unroll
     for (int i = 0; i < SCAN_SPL; ++i) {
       const int s = c0 + SCAN_SPL * lane + i;
       longlong2 c = make_longlong2(0, 0);
       if (s < n_bins) c = cells[sw ? swz(s) : s];
-      ag += c.x;
-      ah += c.y;
+      const I cx = (I)c.x, cy = (I)c.y;
+      ag += cx;
+      ah += cy;
       pg[i] = ag;
       ph[i] = ah;
-      nzmask |= ((c.x | c.y) != 0 || s == 0) ? (1u << i) : 0u;  // cut 0 has no earlier twin
+      nzmask |= ((cx | cy) != 0 || s == 0) ? (1u << i) : 0u;  // cut 0 has no earlier twin
     }
-    int64_t eg = ag, eh = ah;
-    warp_incl_scan(eg, eh);
-    const int64_t tot_g = shfl_i64(eg, 31), tot_h = shfl_i64(eh, 31);
+    I eg = ag, eh = ah;
+    warp_incl_scan<I>(eg, eh);
+    const I tot_g = shfl_i64(eg, 31), tot_h = shfl_i64(eh, 31);
     eg += carry_g - ag;  // exclusive prefix of the lane's first slot
     eh += carry_h - ah;
-    const int64_t h_a = carry_h;  // HL over the chunk's cuts lies in [h_a, h_b]
+    const I h_a = carry_h;  // HL over the chunk's cuts lies in [h_a, h_b]
     carry_g += tot_g;
     carry_h += tot_h;
     if (SKIP && MODE == 0) {
       float sthr = run_lo;
       for (int w = 0; w < set_warps; ++w) sthr = fmaxf(sthr, vlo[sw0 + w]);
       if (sthr > -INFINITY) {
-        int64_t mn = eg + pg[0], mx = mn;
+        I mn = eg + pg[0], mx = mn;
 #pragma unroll
         for (int i = 1; i < SCAN_SPL; ++i) {
           mn = min(mn, eg + pg[i]);
@@ -459,8 +483,9 @@ __device__ __forceinline__ float scan_push_impl(const longlong2 *cells, bool sw,
           mn = min(mn, shfl_xor_i64(mn, o));
           mx = max(mx, shfl_xor_i64(mx, o));
         }
-        float ub = run_bound(mn, mx, h_a, carry_h, tg, th, Gf2den, sp);
-        if (ND == 2) ub = fmaxf(ub, run_bound(mn + m.x, mx + m.x, h_a + m.y, carry_h + m.y, tg, th, Gf2den, sp));
+        float ub = run_bound<I>(mn, mx, h_a, carry_h, tg, th, h_min, Gf2den, sp);
+        if (ND == 2)
+          ub = fmaxf(ub, run_bound<I>(mn + m.x, mx + m.x, h_a + m.y, carry_h + m.y, tg, th, h_min, Gf2den, sp));
         if (ub < sthr) continue;  // no candidate of the chunk can reach the set's best
       }
     }
@@ -472,13 +497,13 @@ __device__ __forceinline__ float scan_push_impl(const longlong2 *cells, bool sw,
       const int s = c0 + SCAN_SPL * lane + i;
 #pragma unroll
       for (int dir = 0; dir < ND; ++dir) {
-        const int64_t GL = eg + pg[i] + (dir ? m.x : 0), HL = eh + ph[i] + (dir ? m.y : 0);
-        const int64_t HR = th - HL;
-        const bool valid = s < n_bins && ((nzmask >> i) & 1u) && HL >= sp.h_min && HR >= sp.h_min &&
-                           !(ND == 2 && dir && no_missing_rt(m));
+        const I GL = eg + pg[i] + (dir ? m.x : 0), HL = eh + ph[i] + (dir ? m.y : 0);
+        const I HR = th - HL;
+        const bool valid = s < n_bins && ((nzmask >> i) & 1u) && HL >= h_min && HR >= h_min &&
+                           !(ND == 2 && dir && m.x == 0 && m.y == 0);
         float u = -INFINITY, lw = -INFINITY;
         if (valid) {
-          if (mode == 0) screen_fast(GL, HL, tg - GL, HR, Gf2den, sp, u, lw);
+          if (mode == 0) screen_fast<I>(GL, HL, tg - GL, HR, Gf2den, sp, u, lw);
           else if (mode == 1) screen_f32(GL, HL, tg - GL, HR, Gf2den, sp, u, lw);
           else u = INFINITY;
           vmask |= 1u << (2 * i + dir);
@@ -505,10 +530,10 @@ __device__ __forceinline__ float scan_push_impl(const longlong2 *cells, bool sw,
           continue;
         }
         Surv v;
-        v.gl = eg + pg[i] + (dir ? m.x : 0);
-        v.hl = eh + ph[i] + (dir ? m.y : 0);
-        v.tg = tg;
-        v.th = th;
+        v.gl = (int64_t)(eg + pg[i] + (dir ? m.x : 0));
+        v.hl = (int64_t)(eh + ph[i] + (dir ? m.y : 0));
+        v.tg = tg64;
+        v.th = th64;
         v.up = up[i][dir];
         v.lo = lo[i][dir];
         v.t = c0 + SCAN_SPL * lane + i;
@@ -524,27 +549,31 @@ __device__ __forceinline__ float scan_push_impl(const longlong2 *cells, bool sw,
 
 // sabs: the sum of |G| over the strip's slots (for the range check of the fast screen).
 // sw: a staged strip (shared memory, slot s at swz(s)).
+// h_ok: no H cell of the strip is negative (then every partial sum of H lies
+// in [0, th] and of G in [-sabs, sabs], and the 32-bit scan is exact when
+// th, sabs and h_min are below 2^31).
 __device__ __forceinline__ float warp_scan_push(const longlong2 *cells, bool sw, int n_bins, int64_t tg, int64_t th,
-                                                int64_t sabs, const SplitParams &sp, int f, int node, ScanShared &sh,
-                                                int &overflow, int set_warps) {
+                                                int64_t sabs, bool h_ok, const SplitParams &sp, int f, int node,
+                                                ScanShared &sh, int &overflow, int set_warps) {
   const longlong2 m = cells[sw ? swz(n_bins) : n_bins];
   const bool no_missing = (m.x == 0 && m.y == 0);
   const float Gf2den = parent_f32(tg, th, sp);
   const bool fast = strip_fast(sabs, th, Gf2den, sp);
+  const bool i32 = h_ok && sabs < (1LL << 31) && th < (1LL << 31) && sp.h_min < (1LL << 31);
   // the common cases (fast screen, with or without missing values) get their own copies; chunk
   // skipping only pays on long strips (in global memory): a staged strip has two chunks
+#define GBT_SCAN(ND, MODE, SKIP, I, mode) \
+  scan_push_impl<ND, MODE, SKIP, I>(cells, sw, n_bins, tg, th, m, Gf2den, sp, f, node, sh, overflow, mode, set_warps)
   if (fast && no_missing) {
-    if (sw) return scan_push_impl<1, 0, false>(cells, sw, n_bins, tg, th, m, Gf2den, sp, f, node, sh, overflow, 0,
-                                               set_warps);
-    return scan_push_impl<1, 0, true>(cells, sw, n_bins, tg, th, m, Gf2den, sp, f, node, sh, overflow, 0, set_warps);
+    if (sw) return i32 ? GBT_SCAN(1, 0, false, int32_t, 0) : GBT_SCAN(1, 0, false, int64_t, 0);
+    return i32 ? GBT_SCAN(1, 0, true, int32_t, 0) : GBT_SCAN(1, 0, true, int64_t, 0);
   }
   if (fast) {
-    if (sw) return scan_push_impl<2, 0, false>(cells, sw, n_bins, tg, th, m, Gf2den, sp, f, node, sh, overflow, 0,
-                                               set_warps);
-    return scan_push_impl<2, 0, true>(cells, sw, n_bins, tg, th, m, Gf2den, sp, f, node, sh, overflow, 0, set_warps);
+    if (sw) return i32 ? GBT_SCAN(2, 0, false, int32_t, 0) : GBT_SCAN(2, 0, false, int64_t, 0);
+    return i32 ? GBT_SCAN(2, 0, true, int32_t, 0) : GBT_SCAN(2, 0, true, int64_t, 0);
   }
-  return scan_push_impl<2, -1, false>(cells, sw, n_bins, tg, th, m, Gf2den, sp, f, node, sh, overflow,
-                                      sp.filter ? 1 : 2, set_warps);
+  return GBT_SCAN(2, -1, false, int64_t, sp.filter ? 1 : 2);
+#undef GBT_SCAN
 }
 
 __device__ __forceinline__ double surv_gain(int64_t gl, int64_t hl, int64_t tg, int64_t th, const SplitParams &sp) {
@@ -625,21 +654,24 @@ __device__ __forceinline__ Cand surv_cand(const Surv &v) {
 // exact results of warps whose pushes overflowed the pool. Up to PUB_K of
 // them are published with their bounds, with no double work in this CTA;
 // with more, they are evaluated in double and the exact best is published.
-// All threads call it; sh.pub[set][0 .. PUB_K-1] holds the result.
-__device__ __noinline__ void cta_select(ScanShared &sh, const SplitParams &sp, int n_sets, const float *thr,
-                                           const int *warp_node) {
+// All threads call it; sh.pub[set][0 .. PUB_K-1] holds the result. Warp w
+// scanned a strip of set w >> set_shift. The thresholds come by value: an
+// array whose address a call takes lives in local memory, whose lines the
+// long strips' streaming evicts (each access then a DRAM round trip).
+__device__ __noinline__ void cta_select(ScanShared &sh, const SplitParams &sp, int n_sets, float thr0, float thr1,
+                                        int set_shift) {
   const int n = min(sh.n, SURV_CAP);
   if (threadIdx.x < 2) sh.cnt[threadIdx.x] = 0;
   __syncthreads();
   for (int i = threadIdx.x; i < n; i += blockDim.x) {
     const Surv &v = sh.pool[i];
-    if (v.up >= thr[v.node]) {
+    if (v.up >= (v.node == 0 ? thr0 : thr1)) {
       const int k = atomicAdd(&sh.cnt[v.node], 1);
       if (k < PUB_K) sh.sel[v.node][k] = i;
     }
   }
   if (threadIdx.x < SCAN_WARPS && sh.warp_overflow[threadIdx.x] && sh.extra[threadIdx.x].f != INT32_MAX) {
-    const int set = warp_node[threadIdx.x];
+    const int set = (int)threadIdx.x >> set_shift;
     const int k = atomicAdd(&sh.cnt[set], 1);
     if (k < PUB_K) sh.sel[set][k] = -1 - (int)threadIdx.x;
   }
@@ -648,7 +680,7 @@ __device__ __noinline__ void cta_select(ScanShared &sh, const SplitParams &sp, i
   if (dbl0 || dbl1) {
     for (int i = threadIdx.x; i < n; i += blockDim.x) {
       const Surv &v = sh.pool[i];
-      const bool need = (v.node == 0 ? dbl0 : dbl1) && v.up >= thr[v.node];
+      const bool need = (v.node == 0 ? dbl0 : dbl1) && v.up >= (v.node == 0 ? thr0 : thr1);
       sh.gain[i] = need ? surv_gain(v.gl, v.hl, v.tg, v.th, sp) : -INFINITY;
     }
     __syncthreads();
@@ -657,13 +689,13 @@ __device__ __noinline__ void cta_select(ScanShared &sh, const SplitParams &sp, i
       Cand best = no_cand();
       for (int i = lane; i < n; i += 32) {
         const Surv &v = sh.pool[i];
-        if (v.node != warp || !(v.up >= thr[warp])) continue;
+        if (v.node != warp || !(v.up >= (warp == 0 ? thr0 : thr1))) continue;
         Cand c = surv_cand(v);
         set_exact(c, sh.gain[i]);
         if (cand_better(c, best)) best = c;
       }
       for (int w = lane; w < SCAN_WARPS; w += 32)
-        if (warp_node[w] == warp && sh.warp_overflow[w] && cand_better(sh.extra[w], best)) best = sh.extra[w];
+        if ((w >> set_shift) == warp && sh.warp_overflow[w] && cand_better(sh.extra[w], best)) best = sh.extra[w];
       best = warp_best_cand(best);
       if (lane < PUB_K) sh.pub[warp][lane] = lane == 0 ? best : no_cand();
     }
@@ -882,6 +914,7 @@ __global__ void __launch_bounds__(SCAN_THREADS, 3) k_find(const int64_t *__restr
   int64_t tg = 0, th = 0;
   if (f < n_features) {
     int64_t sa = 0;
+    bool hneg = false;
     if (staged) {
       for (int s = lane; s < B; s += 32) {
         const longlong2 c = __ldg(strip + s);
@@ -889,14 +922,16 @@ __global__ void __launch_bounds__(SCAN_THREADS, 3) k_find(const int64_t *__restr
         tg += c.x;
         th += c.y;
         sa += c.x < 0 ? -c.x : c.x;
+        hneg |= c.y < 0;
       }
     } else {
-      strip_totals(strip, B, tg, th, sa);
+      strip_totals(strip, B, tg, th, sa, hneg);
     }
     warp_sum3(tg, th, sa);
+    const bool h_ok = !__any_sync(0xffffffffu, hneg);
     __syncwarp();
     int ovf = 0;
-    const float wlo = warp_scan_push(cells, staged, n_bins, tg, th, sa, sp, f, 0, sh, ovf, SCAN_WARPS);
+    const float wlo = warp_scan_push(cells, staged, n_bins, tg, th, sa, h_ok, sp, f, 0, sh, ovf, SCAN_WARPS);
     ovf = __any_sync(0xffffffffu, ovf);
     if (lane == 0) {
       sh.warp_lo[warp] = wlo;
@@ -904,17 +939,15 @@ __global__ void __launch_bounds__(SCAN_THREADS, 3) k_find(const int64_t *__restr
     }
   }
   __syncthreads();
-  float thr[2] = {-INFINITY, -INFINITY};
-  for (int w = 0; w < SCAN_WARPS; ++w) thr[0] = fmaxf(thr[0], sh.warp_lo[w]);
+  float thr0 = -INFINITY;
+#pragma unroll
+  for (int w = 0; w < SCAN_WARPS; ++w) thr0 = fmaxf(thr0, sh.warp_lo[w]);
   if (f < n_features && sh.warp_overflow[warp]) {
-    const Cand d = warp_direct_best(cells, staged, n_bins, tg, th, sp, thr[0], f);
+    const Cand d = warp_direct_best(cells, staged, n_bins, tg, th, sp, thr0, f);
     if (lane == 0) sh.extra[warp] = d;
   }
   __syncthreads();
-  int warp_node[SCAN_WARPS];
-#pragma unroll
-  for (int w = 0; w < SCAN_WARPS; ++w) warp_node[w] = 0;
-  cta_select(sh, sp, 1, thr, warp_node);
+  cta_select(sh, sp, 1, thr0, -INFINITY, 3);
   const int nfb = gridDim.x;
   Cand *cn = cand + (int64_t)node * nfb * PUB_K;
   if (cta_publish(sh, 1, cn + blockIdx.x * PUB_K, nullptr, counters + node, nfb)) {
@@ -1077,19 +1110,22 @@ __global__ void __launch_bounds__(SCAN_THREADS, CTAS) k_level_finish(
   int64_t tg = 0, th = 0;
   if (active) {
     int64_t sa = 0;
+    bool hneg = false;
     if (staged) {
       for (int s = lane; s < B; s += 32) {
         const longlong2 c = cells[swz(s)];
         tg += c.x;
         th += c.y;
         sa += c.x < 0 ? -c.x : c.x;
+        hneg |= c.y < 0;
       }
     } else {
-      strip_totals(cells, B, tg, th, sa);
+      strip_totals(cells, B, tg, th, sa, hneg);
     }
     warp_sum3(tg, th, sa);
+    const bool h_ok = !__any_sync(0xffffffffu, hneg);
     int ovf = 0;
-    const float wlo = warp_scan_push(cells, staged, n_bins, tg, th, sa, sp, f, side, sh, ovf, 4);
+    const float wlo = warp_scan_push(cells, staged, n_bins, tg, th, sa, h_ok, sp, f, side, sh, ovf, 4);
     ovf = __any_sync(0xffffffffu, ovf);
     if (lane == 0) {
       sh.warp_lo[warp] = wlo;
@@ -1097,17 +1133,18 @@ __global__ void __launch_bounds__(SCAN_THREADS, CTAS) k_level_finish(
     }
   }
   __syncthreads();
-  float thr[2] = {-INFINITY, -INFINITY};
-  for (int w = 0; w < SCAN_WARPS; ++w) thr[w >> 2] = fmaxf(thr[w >> 2], sh.warp_lo[w]);
+  float thr0 = -INFINITY, thr1 = -INFINITY;  // the small and the large set's best lower bound
+#pragma unroll
+  for (int w = 0; w < SCAN_WARPS / 2; ++w) {
+    thr0 = fmaxf(thr0, sh.warp_lo[w]);
+    thr1 = fmaxf(thr1, sh.warp_lo[w + SCAN_WARPS / 2]);
+  }
   if (active && sh.warp_overflow[warp]) {
-    const Cand d = warp_direct_best(cells, staged, n_bins, tg, th, sp, thr[side], f);
+    const Cand d = warp_direct_best(cells, staged, n_bins, tg, th, sp, side ? thr1 : thr0, f);
     if (lane == 0) sh.extra[warp] = d;
   }
   __syncthreads();
-  int warp_node[SCAN_WARPS];
-#pragma unroll
-  for (int w = 0; w < SCAN_WARPS; ++w) warp_node[w] = w >> 2;
-  cta_select(sh, sp, 2, thr, warp_node);
+  cta_select(sh, sp, 2, thr0, thr1, 2);
   const int nfb = gridDim.x;
   const int64_t es = (int64_t)(2 * p) * nfb * PUB_K, el = es + (int64_t)nfb * PUB_K;  // the siblings' first entries
   if (cta_publish(sh, 2, cand + es + blockIdx.x * PUB_K, cand + el + blockIdx.x * PUB_K, counters + p, nfb,

@@ -54,10 +54,9 @@ def _pick(G, H, GL, lam, d, start):
     raise AssertionError("no candidate pair found")
 
 
-def _flat_start(G, H, GL, lam):
-    """A hessian HL on the rising side of the gain's minimum over HL (the gain is convex in HL: a sum of
-    x^2 / y terms) where one unit of HL moves the gain by about a quarter ulp, so that nearby candidates
-    differ by a few ulps."""
+def _gain_min(G, H, GL, lam):
+    """The hessian HL at which the gain is smallest over HL (the gain is convex in HL: a sum of x^2 / y
+    terms)."""
     f = lambda h: float(_gains(np.array([GL]), np.array([h]), G, H, lam)[0])  # noqa: E731
     lo, hi = 1, H - 1
     while hi - lo > 3:
@@ -66,6 +65,13 @@ def _flat_start(G, H, GL, lam):
             hi = m2
         else:
             lo = m1
+    return lo
+
+
+def _flat_start(G, H, GL, lam):
+    """A hessian HL on the rising side of the gain's minimum over HL where one unit of HL moves the gain by
+    about a quarter ulp, so that nearby candidates differ by a few ulps."""
+    lo = _gain_min(G, H, GL, lam)
     delta = 1 << 16
     while True:
         b = _gains(np.full(2, GL, np.int64), np.array([lo + delta, lo + delta + 4096], np.int64), G, H,
@@ -102,6 +108,8 @@ class Case:
 
 
 def _build(n_bins, G, H, GL, lam):
+    if H < (1 << 31):
+        return _build_near_min(n_bins, G, H, GL, lam)
     F = 24
     c = Case(6, F, n_bins, G, H)
     h0 = _flat_start(G, H, GL, lam)
@@ -126,6 +134,49 @@ def _build(n_bins, G, H, GL, lam):
     c.expect[4] = (21, t0 + 3, 0)
     # (d) one cut of feature 9 whose missing rows (G 0, H m) make missing-left 1 ulp higher than missing-right
     ha, hb = _pick(G, H, GL, lam, 1, h0 + 1300)
+    c.strip(5, 9, [(t0, GL, ha)], miss=(0, hb - ha))
+    c.expect[5] = (9, t0, 1)
+    return c
+
+
+def _build_near_min(n_bins, G, H, GL, lam):
+    """The cases of _build for sums below 2^31, where every partial sum of a strip fits in 32 bits. One unit
+    of HL then moves the gain by many ulps except near its minimum over HL, where the gain is flat to within
+    its rounding: every pair comes from a window of hessians around the minimum, each partner found for the
+    given first hessian."""
+    F = 24
+    c = Case(6, F, n_bins, G, H)
+    m = _gain_min(G, H, GL, lam)
+    HL = np.arange(m - 3000, m + 3000, dtype=np.int64)
+    bits = _gains(np.full(HL.shape, GL, np.int64), HL, G, H, lam).view(np.int64)
+
+    def partner(i, d, above=False):
+        """An index j (j > i when above) whose gain is exactly d ulps above gain i, or None."""
+        j = np.flatnonzero(bits - bits[i] == d)
+        j = j[(j > i) if above else (j != i)]
+        return int(j[0]) if j.size else None
+
+    def first(ds, above=False, start=0):
+        for i in range(start, len(HL)):
+            js = [partner(i, d, above) for d in ds]
+            if all(j is not None for j in js):
+                return [int(HL[i])] + [int(HL[j]) for j in js]
+        raise AssertionError("no candidate set found")
+
+    t0 = min(40, n_bins - 3)
+    for n, d, win in ((0, 1, 13), (1, -2, 3), (2, 0, 3)):
+        ha, hb = first([d], start=97 * n)
+        c.strip(n, 3, [(t0, GL, ha)])
+        c.strip(n, 13, [(t0 + 1, GL, hb)])
+        c.expect[n] = (win, t0 if win == 3 else t0 + 1, 0)
+    ha, hb1, hb3, hb2 = first([1, 3, 2], start=500)
+    for f, hl in zip((16, 17, 18, 19), (ha, hb1, hb3, hb2)):
+        c.strip(3, f, [(t0 + f - 16, GL, hl)])
+    c.expect[3] = (18, t0 + 2, 0)
+    ha, hb = first([2], above=True, start=900)
+    c.strip(4, 21, [(t0, GL, ha), (t0 + 3, GL, hb)])
+    c.expect[4] = (21, t0 + 3, 0)
+    ha, hb = first([1], above=True, start=1300)
     c.strip(5, 9, [(t0, GL, ha)], miss=(0, hb - ha))
     c.expect[5] = (9, t0, 1)
     return c
@@ -169,6 +220,10 @@ SETTINGS = [
     (4096, 3 << 36, 1 << 44, 5 << 40, 1.0),
     (4096, 3 << 40, 1 << 47, 5 << 44, 0.5),
     (4096, 3 << 36, 1 << 44, 5 << 40, -0.25),
+    # sums below 2^31 (the scan's 32-bit instantiation), staged and in global memory
+    (255, 3 << 26, 1 << 30, 5 << 26, 1.0),
+    (255, 3 << 26, 1 << 30, 5 << 26, 0.5),
+    (4096, 3 << 26, 1 << 30, 5 << 26, 1.0),
 ]
 
 
@@ -226,6 +281,13 @@ def test_near_tie_cases_are_what_they_claim(oracle_mod):
             assert _ulps(ga, gb_) == d and ha != hb
         case = _build(n_bins, G, H, GL, lam)
         assert (case.h[..., 1] >= 0).all()
+        ref, st = oracle_mod.find_splits(case.h, n_bins, lam, 0.0, 0.0, 1.0, 1.0)
+        assert st == oracle_mod.OK
+        _check_designed(case, ref, "oracle")
+    for n_bins, G, H, GL, lam in SETTINGS[6:]:
+        case = _build(n_bins, G, H, GL, lam)
+        assert (case.h[..., 1] >= 0).all()
+        assert np.abs(case.h[..., 0]).sum(axis=2).max() < 2 ** 31 and case.h[..., 1].sum(axis=2).max() < 2 ** 31
         ref, st = oracle_mod.find_splits(case.h, n_bins, lam, 0.0, 0.0, 1.0, 1.0)
         assert st == oracle_mod.OK
         _check_designed(case, ref, "oracle")
