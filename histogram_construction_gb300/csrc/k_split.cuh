@@ -549,6 +549,15 @@ __device__ __forceinline__ float scan_push_impl(const longlong2 *cells, bool sw,
 
 // sabs: the sum of |G| over the strip's slots (for the range check of the fast screen).
 // sw: a staged strip (shared memory, slot s at swz(s)).
+// The checked screen and the unscreened scan (rare: extreme ranges, lambda < 0), out of line so that
+// their registers do not weigh on the common copies.
+__device__ __noinline__ float scan_push_checked(const longlong2 *cells, bool sw, int n_bins, int64_t tg, int64_t th,
+                                                longlong2 m, float Gf2den, const SplitParams &sp, int f, int node,
+                                                ScanShared &sh, int &overflow, int set_warps) {
+  return scan_push_impl<2, -1, false, int64_t>(cells, sw, n_bins, tg, th, m, Gf2den, sp, f, node, sh, overflow,
+                                               sp.filter ? 1 : 2, set_warps);
+}
+
 // h_ok: no H cell of the strip is negative (then every partial sum of H lies
 // in [0, th] and of G in [-sabs, sabs], and the 32-bit scan is exact when
 // th, sabs and h_min are below 2^31).
@@ -572,7 +581,7 @@ __device__ __forceinline__ float warp_scan_push(const longlong2 *cells, bool sw,
     if (sw) return i32 ? GBT_SCAN(2, 0, false, int32_t, 0) : GBT_SCAN(2, 0, false, int64_t, 0);
     return i32 ? GBT_SCAN(2, 0, true, int32_t, 0) : GBT_SCAN(2, 0, true, int64_t, 0);
   }
-  return GBT_SCAN(2, -1, false, int64_t, sp.filter ? 1 : 2);
+  return scan_push_checked(cells, sw, n_bins, tg, th, m, Gf2den, sp, f, node, sh, overflow, set_warps);
 #undef GBT_SCAN
 }
 
@@ -811,8 +820,12 @@ __device__ __forceinline__ void reduce_node(const Cand *cand, int n_ent, const S
 // cb[i] = (lo, up) of entry i (n_ent even, cb 16-byte aligned): both passes
 // read 8 bytes per entry, two entries per 16-byte load, and only the entries
 // whose upper bound reaches the threshold are read in full.
+// BAR, the named barrier, is a compile-time constant so that a kernel reserves only the barriers it
+// uses, also when the call stays out of line (reduce_node_cb_ool).
+template <int BAR>
 __device__ __forceinline__ void reduce_node_cb(const Cand *cand, const float2 *cb, int n_ent, const SplitParams &sp,
-                                               SplitOut *out, int t0, int nthr, int bar, Cand *slot, float *sthr) {
+                                               SplitOut *out, int t0, int nthr, Cand *slot, float *sthr) {
+  constexpr int bar = BAR;
   const int t = threadIdx.x - t0, lane = threadIdx.x & 31, w = t >> 5, nw = nthr >> 5;
   constexpr int RB = 8;  // 16-byte loads in flight per thread
   const float4 *cb4 = reinterpret_cast<const float4 *>(cb);
@@ -861,6 +874,15 @@ __device__ __forceinline__ void reduce_node_cb(const Cand *cand, const float2 *c
     const Cand b = lane < nw ? slot[lane] : no_cand();
     if (lane == warp_argmax_lane(b)) *out = cand_to_split(b);
   }
+}
+
+// reduce_node_cb out of line: only the last CTA of a node runs it, so in a kernel budgeted for many
+// CTAs per SM its registers need not weigh on the other CTAs (a one-wave grid keeps it inline: the
+// call would lengthen the critical path).
+template <int BAR>
+__device__ __noinline__ void reduce_node_cb_ool(const Cand *cand, const float2 *cb, int n_ent, const SplitParams &sp,
+                                                SplitOut *out, int t0, int nthr, Cand *slot, float *sthr) {
+  reduce_node_cb<BAR>(cand, cb, n_ent, sp, out, t0, nthr, slot, sthr);
 }
 
 // Stores the CTA's published candidates (dst[set] + 0 .. PUB_K-1), and their
@@ -1019,7 +1041,7 @@ __global__ void __launch_bounds__(SCAN_THREADS, CTAS) k_level_finish(
     // all 256 threads sum the group images of the four features: thread t
     // takes feature t & 3 and slots (t >> 2) + 64 u, eight loads in flight,
     // so each warp load covers 8 slots x 4 features (whole 32-byte sectors)
-    constexpr int PA = 8;
+    constexpr int PA = STAGED ? STAGE_SLOTS / 64 : 8;  // a staged strip has at most 4 slots per thread
     const int t = threadIdx.x, fi = t & 3, ff = blockIdx.x * 4 + fi;
     if (ff < n_features) {
       const int32_t g0 = src.view.group_prefix[p], g1 = src.view.group_prefix[p + 1], i0 = src.view.img_first[p];
@@ -1151,10 +1173,19 @@ __global__ void __launch_bounds__(SCAN_THREADS, CTAS) k_level_finish(
                   cbounds + es + blockIdx.x * PUB_K, cbounds + el + blockIdx.x * PUB_K)) {
     __threadfence();
     // warps 0-3 reduce the small sibling, warps 4-7 the large one
-    if (threadIdx.x < 128)
-      reduce_node_cb(cand + es, cbounds + es, nfb * PUB_K, sp, small_out + si, 0, 128, 1, sh.extra, sh.red);
-    else
-      reduce_node_cb(cand + el, cbounds + el, nfb * PUB_K, sp, large_out + li, 128, 128, 2, sh.extra + 4, sh.red + 4);
+    if (CTAS >= 4) {
+      if (threadIdx.x < 128)
+        reduce_node_cb_ool<1>(cand + es, cbounds + es, nfb * PUB_K, sp, small_out + si, 0, 128, sh.extra, sh.red);
+      else
+        reduce_node_cb_ool<2>(cand + el, cbounds + el, nfb * PUB_K, sp, large_out + li, 128, 128, sh.extra + 4,
+                              sh.red + 4);
+    } else {
+      if (threadIdx.x < 128)
+        reduce_node_cb<1>(cand + es, cbounds + es, nfb * PUB_K, sp, small_out + si, 0, 128, sh.extra, sh.red);
+      else
+        reduce_node_cb<2>(cand + el, cbounds + el, nfb * PUB_K, sp, large_out + li, 128, 128, sh.extra + 4,
+                          sh.red + 4);
+    }
   }
 }
 
