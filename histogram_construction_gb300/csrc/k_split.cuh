@@ -372,6 +372,7 @@ struct ScanShared {
   int sel[2][PUB_K];
   int cnt[2];
   float red[SCAN_WARPS];
+  int rcnt[2];  // candidates evaluated by each half's node reduce
   int n;
   uint32_t last;
 };
@@ -824,50 +825,89 @@ __device__ __forceinline__ void reduce_node(const Cand *cand, int n_ent, const S
 // uses, also when the call stays out of line (reduce_node_cb_ool).
 template <int BAR>
 __device__ __forceinline__ void reduce_node_cb(const Cand *cand, const float2 *cb, int n_ent, const SplitParams &sp,
-                                               SplitOut *out, int t0, int nthr, Cand *slot, float *sthr) {
+                                               SplitOut *out, int t0, int nthr, Cand *slot, float *sthr, int *rcnt) {
   constexpr int bar = BAR;
   const int t = threadIdx.x - t0, lane = threadIdx.x & 31, w = t >> 5, nw = nthr >> 5;
   constexpr int RB = 8;  // 16-byte loads in flight per thread
   const float4 *cb4 = reinterpret_cast<const float4 *>(cb);
   const int n4 = n_ent >> 1;
+  const bool one = n4 <= nthr;  // each thread holds at most one pair of entries: kept in registers
   float thr = -INFINITY;
-  for (int i0 = t; i0 < n4; i0 += nthr * RB) {
-    float4 v[RB];
+  float4 v1 = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+  if (one) {
+    if (t < n4) v1 = __ldcg(cb4 + t);
+    thr = fmaxf(v1.x, v1.z);
+  } else {
+    for (int i0 = t; i0 < n4; i0 += nthr * RB) {
+      float4 v[RB];
 #pragma unroll
-    for (int u = 0; u < RB; ++u) {
-      const int i = i0 + u * nthr;
-      v[u] = i < n4 ? __ldcg(cb4 + i) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+      for (int u = 0; u < RB; ++u) {
+        const int i = i0 + u * nthr;
+        v[u] = i < n4 ? __ldcg(cb4 + i) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+      }
+#pragma unroll
+      for (int u = 0; u < RB; ++u) thr = fmaxf(thr, fmaxf(v[u].x, v[u].z));
     }
-#pragma unroll
-    for (int u = 0; u < RB; ++u) thr = fmaxf(thr, fmaxf(v[u].x, v[u].z));
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) thr = fmaxf(thr, __shfl_xor_sync(0xffffffffu, thr, o));
+  // the entry of this pair with the larger upper bound, read in full already if it reaches the warp's
+  // best lower bound (the node's threshold is at least that): the load overlaps the barrier
+  const int se = v1.w > v1.y ? 1 : 0;
+  const bool spec = one && t < n4 && (se ? v1.w : v1.y) >= thr;
+  Cand cs;
+  if (spec) cs = load_cand(cand + 2 * t + se);
   if (lane == 0) sthr[w] = thr;
+  if (t == 0) *rcnt = 0;
   named_sync(bar, nthr);
   for (int k = 0; k < nw; ++k) thr = fmaxf(thr, sthr[k]);
   Cand best = no_cand();
-  for (int i0 = t; i0 < n4; i0 += nthr * RB) {
-    uint32_t pass = 0;  // bit 2u + e: entry 2 (i0 + u nthr) + e reaches the threshold
+  auto consider = [&](Cand c) {
+    if (c.f == INT32_MAX) return;
+    if (!c.exact) set_exact(c, surv_gain(c.gl, c.hl, c.gl + c.gr, c.hl + c.hr, sp));
+    if (cand_better(c, best)) best = c;
+  };
+  if (one) {
+    if (t < n4)
+      for (int e = 0; e < 2; ++e)
+        if ((e ? v1.w : v1.y) >= thr) consider(spec && e == se ? cs : load_cand(cand + 2 * t + e));
+  } else {
+    for (int i0 = t; i0 < n4; i0 += nthr * RB) {
+      uint32_t pass = 0;  // bit 2u + e: entry 2 (i0 + u nthr) + e reaches the threshold
 #pragma unroll
-    for (int u = 0; u < RB; ++u) {
-      const int i = i0 + u * nthr;
-      if (i < n4) {
-        const float4 x = __ldcg(cb4 + i);
-        pass |= (x.y >= thr ? 1u : 0u) << (2 * u);
-        pass |= (x.w >= thr ? 1u : 0u) << (2 * u + 1);
+      for (int u = 0; u < RB; ++u) {
+        const int i = i0 + u * nthr;
+        if (i < n4) {
+          const float4 x = __ldcg(cb4 + i);
+          pass |= (x.y >= thr ? 1u : 0u) << (2 * u);
+          pass |= (x.w >= thr ? 1u : 0u) << (2 * u + 1);
+        }
+      }
+      // one copy of the evaluation, however many entries pass
+      while (pass) {
+        const int b = __ffs(pass) - 1;
+        pass &= pass - 1u;
+        consider(load_cand(cand + 2 * (i0 + (b >> 1) * nthr) + (b & 1)));
       }
     }
-    // one copy of the evaluation, however many entries pass
-    while (pass) {
-      const int b = __ffs(pass) - 1;
-      pass &= pass - 1u;
-      Cand c = load_cand(cand + 2 * (i0 + (b >> 1) * nthr) + (b & 1));
-      if (c.f == INT32_MAX) continue;
-      if (!c.exact) set_exact(c, surv_gain(c.gl, c.hl, c.gl + c.gr, c.hl + c.hr, sp));
-      if (cand_better(c, best)) best = c;
-    }
   }
+  // the argmax: a short list when few candidates were evaluated (the usual case), else warp shuffles
+  if (best.f != INT32_MAX) {
+    const int k = atomicAdd(rcnt, 1);
+    if (k < nw) slot[k] = best;
+  }
+  named_sync(bar, nthr);
+  const int nc = *rcnt;
+  if (nc <= nw) {
+    if (t == 0) {
+      Cand b = no_cand();
+      for (int k = 0; k < nc; ++k)
+        if (cand_better(slot[k], b)) b = slot[k];
+      *out = cand_to_split(b);
+    }
+    return;
+  }
+  named_sync(bar, nthr);  // every thread has read the count before the list is overwritten
   if (lane == warp_argmax_lane(best)) slot[w] = best;
   named_sync(bar, nthr);
   if (w == 0) {
@@ -881,14 +921,18 @@ __device__ __forceinline__ void reduce_node_cb(const Cand *cand, const float2 *c
 // call would lengthen the critical path).
 template <int BAR>
 __device__ __noinline__ void reduce_node_cb_ool(const Cand *cand, const float2 *cb, int n_ent, const SplitParams &sp,
-                                                SplitOut *out, int t0, int nthr, Cand *slot, float *sthr) {
-  reduce_node_cb<BAR>(cand, cb, n_ent, sp, out, t0, nthr, slot, sthr);
+                                                SplitOut *out, int t0, int nthr, Cand *slot, float *sthr, int *rcnt) {
+  reduce_node_cb<BAR>(cand, cb, n_ent, sp, out, t0, nthr, slot, sthr, rcnt);
 }
 
 // Stores the CTA's published candidates (dst[set] + 0 .. PUB_K-1), and their
 // bounds (lo, up) in cb[set] + 0 .. PUB_K-1 when cb0 is given, and counts the
 // CTA in; returns true in the last CTA of the group, which resets the
-// counter. No CTA waits.
+// counter. No CTA waits. Ordering: the stores precede the block barrier,
+// which precedes thread 0's acquire-release increment (a release that covers
+// what the barrier ordered before it); in the last CTA that increment
+// acquires every other CTA's release, and the second barrier orders the
+// block's later reads after it.
 __device__ __forceinline__ bool cta_publish(ScanShared &sh, int n_sets, Cand *dst0, Cand *dst1, uint32_t *counter,
                                             uint32_t group_ctas, float2 *cb0 = nullptr, float2 *cb1 = nullptr) {
   if (threadIdx.x < n_sets * PUB_K) {
@@ -896,11 +940,11 @@ __device__ __forceinline__ bool cta_publish(ScanShared &sh, int n_sets, Cand *ds
     const Cand &c = sh.pub[set][k];
     (set == 0 ? dst0 : dst1)[k] = c;
     if (cb0) (set == 0 ? cb0 : cb1)[k] = make_float2(c.lo, c.up);
-    __threadfence();
   }
   __syncthreads();
   if (threadIdx.x == 0) {
-    const uint32_t done = atomicAdd(counter, 1u);
+    uint32_t done;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(done) : "l"(counter) : "memory");
     sh.last = (done == group_ctas - 1) ? 1u : 0u;
     if (sh.last) *counter = 0;  // every CTA of the group has counted in
   }
@@ -973,7 +1017,6 @@ __global__ void __launch_bounds__(SCAN_THREADS, 3) k_find(const int64_t *__restr
   const int nfb = gridDim.x;
   Cand *cn = cand + (int64_t)node * nfb * PUB_K;
   if (cta_publish(sh, 1, cn + blockIdx.x * PUB_K, nullptr, counters + node, nfb)) {
-    __threadfence();
     reduce_node(cn, nfb * PUB_K, sp, out + node, 0, SCAN_THREADS, 1, sh.extra, sh.red);
   }
 }
@@ -1171,20 +1214,21 @@ __global__ void __launch_bounds__(SCAN_THREADS, CTAS) k_level_finish(
   const int64_t es = (int64_t)(2 * p) * nfb * PUB_K, el = es + (int64_t)nfb * PUB_K;  // the siblings' first entries
   if (cta_publish(sh, 2, cand + es + blockIdx.x * PUB_K, cand + el + blockIdx.x * PUB_K, counters + p, nfb,
                   cbounds + es + blockIdx.x * PUB_K, cbounds + el + blockIdx.x * PUB_K)) {
-    __threadfence();
     // warps 0-3 reduce the small sibling, warps 4-7 the large one
     if (CTAS >= 4) {
       if (threadIdx.x < 128)
-        reduce_node_cb_ool<1>(cand + es, cbounds + es, nfb * PUB_K, sp, small_out + si, 0, 128, sh.extra, sh.red);
+        reduce_node_cb_ool<1>(cand + es, cbounds + es, nfb * PUB_K, sp, small_out + si, 0, 128, sh.extra, sh.red,
+                              sh.rcnt);
       else
         reduce_node_cb_ool<2>(cand + el, cbounds + el, nfb * PUB_K, sp, large_out + li, 128, 128, sh.extra + 4,
-                              sh.red + 4);
+                              sh.red + 4, sh.rcnt + 1);
     } else {
       if (threadIdx.x < 128)
-        reduce_node_cb<1>(cand + es, cbounds + es, nfb * PUB_K, sp, small_out + si, 0, 128, sh.extra, sh.red);
+        reduce_node_cb<1>(cand + es, cbounds + es, nfb * PUB_K, sp, small_out + si, 0, 128, sh.extra, sh.red,
+                          sh.rcnt);
       else
         reduce_node_cb<2>(cand + el, cbounds + el, nfb * PUB_K, sp, large_out + li, 128, 128, sh.extra + 4,
-                          sh.red + 4);
+                          sh.red + 4, sh.rcnt + 1);
     }
   }
 }
