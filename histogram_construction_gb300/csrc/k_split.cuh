@@ -440,12 +440,14 @@ __device__ __forceinline__ float scan_push_impl(const longlong2 *cells, bool sw,
   volatile float *vlo = sh.warp_lo;
   float run_lo = -INFINITY;
   I carry_g = 0, carry_h = 0;
+  if (!__isShared(cells))
+    asm volatile("prefetch.global.L1 [%0];" ::"l"(cells + min(32 * SCAN_SPL + SCAN_SPL * lane, n_bins)));
   for (int c0 = 0; c0 < n_bins; c0 += 32 * SCAN_SPL) {
     // the next chunk's cells on their way to L1 while this chunk is screened
     // (strips in global memory: u16 bins)
     // (clamped to the strip's missing slot: the address stays inside the strip)
     if (c0 + 32 * SCAN_SPL < n_bins && !__isShared(cells))
-      asm volatile("prefetch.global.L1 [%0];" ::"l"(cells + min(c0 + 32 * SCAN_SPL + SCAN_SPL * lane, n_bins)));
+      asm volatile("prefetch.global.L1 [%0];" ::"l"(cells + min(c0 + 2 * 32 * SCAN_SPL + SCAN_SPL * lane, n_bins)));
     I pg[SCAN_SPL], ph[SCAN_SPL];
     I ag = 0, ah = 0;
     uint32_t nzmask = 0;  // slots of the lane whose cell is not empty
