@@ -373,6 +373,7 @@ struct ScanShared {
   int cnt[2];
   float red[SCAN_WARPS];
   int rcnt[2];  // candidates evaluated by each half's node reduce
+  int64_t ptot[SCAN_WARPS][4][4];  // long strips: each warp's share of the small strips' (G, H, |G|, H < 0)
   int n;
   uint32_t last;
 };
@@ -1088,6 +1089,8 @@ __global__ void __launch_bounds__(SCAN_THREADS, CTAS) k_level_finish(
     // so each warp load covers 8 slots x 4 features (whole 32-byte sectors)
     constexpr int PA = STAGED ? STAGE_SLOTS / 64 : 8;  // a staged strip has at most 4 slots per thread
     const int t = threadIdx.x, fi = t & 3, ff = blockIdx.x * 4 + fi;
+    int64_t pg = 0, ph = 0, pa = 0;  // long strips: this thread's part of feature fi's totals
+    bool pn = false;
     if (ff < n_features) {
       const int32_t g0 = src.view.group_prefix[p], g1 = src.view.group_prefix[p + 1], i0 = src.view.img_first[p];
       const bool zero = i0 < src.view.r_cap;  // reduce-region images are zeroed as they are read
@@ -1127,9 +1130,31 @@ __global__ void __launch_bounds__(SCAN_THREADS, CTAS) k_level_finish(
           if (s < B) {
             const longlong2 c = make_longlong2(ag[u], ah[u]);
             So[s] = c;
-            if (staged) sh.cells[fi][swz(s)] = c;
+            if (staged) {
+              sh.cells[fi][swz(s)] = c;
+            } else {
+              pg += c.x;
+              ph += c.y;
+              pa += c.x < 0 ? -c.x : c.x;
+              pn |= c.y < 0;
+            }
           }
         }
+      }
+    }
+    if (!staged) {  // the small strips' totals as they are written: the scan then reads each strip once
+#pragma unroll
+      for (int o = 4; o < 32; o <<= 1) {  // lanes of equal fi
+        pg += shfl_xor_i64(pg, o);
+        ph += shfl_xor_i64(ph, o);
+        pa += shfl_xor_i64(pa, o);
+        pn |= __shfl_xor_sync(0xffffffffu, (int)pn, o) != 0;
+      }
+      if (lane < 4) {
+        sh.ptot[warp][lane][0] = pg;
+        sh.ptot[warp][lane][1] = ph;
+        sh.ptot[warp][lane][2] = pa;
+        sh.ptot[warp][lane][3] = pn ? 1 : 0;
       }
     }
   } else if (side == 0 && active && staged) {
@@ -1137,6 +1162,8 @@ __global__ void __launch_bounds__(SCAN_THREADS, CTAS) k_level_finish(
   }
   __syncthreads();
   // phase B: large = parent - small
+  int64_t bg = 0, bh = 0, ba = 0;  // long strips: this lane's part of the large strip's totals as it is written
+  bool bn = false;
   if (active && side == 1) {
     bool neg = false;
     if (staged) {
@@ -1165,11 +1192,15 @@ __global__ void __launch_bounds__(SCAN_THREADS, CTAS) k_level_finish(
             const longlong2 d = make_longlong2(a[u].x - b[u].x, a[u].y - b[u].y);
             neg |= d.y < 0;
             L[s] = d;
+            bg += d.x;
+            bh += d.y;
+            ba += d.x < 0 ? -d.x : d.x;
           }
         }
       }
     }
     if (neg) raise_err(st, ERRBIT_INCONSISTENT);
+    bn = neg;
   }
   __syncwarp();
   // phase C: scan
@@ -1186,10 +1217,24 @@ __global__ void __launch_bounds__(SCAN_THREADS, CTAS) k_level_finish(
         sa += c.x < 0 ? -c.x : c.x;
         hneg |= c.y < 0;
       }
+      warp_sum3(tg, th, sa);
+    } else if (side == 1) {  // summed by this warp in phase B
+      tg = bg;
+      th = bh;
+      sa = ba;
+      hneg = bn;
+      warp_sum3(tg, th, sa);
+    } else if (FROM_PARTIALS) {  // summed by the block in phase A
+      for (int w = 0; w < SCAN_WARPS; ++w) {
+        tg += sh.ptot[w][fo][0];
+        th += sh.ptot[w][fo][1];
+        sa += sh.ptot[w][fo][2];
+        hneg |= sh.ptot[w][fo][3] != 0;
+      }
     } else {
       strip_totals(cells, B, tg, th, sa, hneg);
+      warp_sum3(tg, th, sa);
     }
-    warp_sum3(tg, th, sa);
     const bool h_ok = !__any_sync(0xffffffffu, hneg);
     int ovf = 0;
     const float wlo = warp_scan_push(cells, staged, n_bins, tg, th, sa, h_ok, sp, f, side, sh, ovf, 4);
