@@ -63,6 +63,18 @@ __device__ __forceinline__ float i64_to_f32(int64_t x) {
   return x < 0 ? -f : f;
 }
 
+// Signed 64-bit integer -> float for |x| < 2^45: x = hi * 2^23 + lo with
+// hi = x >> 23 in [-2^22, 2^22) and lo in [0, 2^23), both converted exactly
+// by magic-number constructions (1.5 * 2^23 and 2^23); the FMA rounds once,
+// so the relative error is at most u = 2^-24.
+__device__ __forceinline__ float i45_to_f32(int64_t x) {
+  const int32_t hi = (int32_t)(x >> 23);
+  const uint32_t lo = (uint32_t)x & 0x7FFFFFu;
+  const float fh = __fsub_rn(__int_as_float(0x4B400000 + hi), 12582912.0f);
+  const float fl = __fsub_rn(__int_as_float(0x4B000000u | lo), 8388608.0f);
+  return __fmaf_rn(fh, 8388608.0f, fl);
+}
+
 // FP32 screen of one candidate: returns (up, lo) with lo <= gain_fp64 <= up.
 // Error budget (u = 2^-24): an int64 value converts with relative error 2u,
 // the scale product adds u and the float scale u, so each converted value is
@@ -106,8 +118,9 @@ __device__ __forceinline__ void screen_f32(int64_t GL, int64_t HL, int64_t GR, i
 // range it is NaN, which gives every candidate of the strip an infinite bound
 // (all of them are then evaluated in double).
 __device__ __forceinline__ float parent_f32(int64_t tg, int64_t th, const SplitParams &sp) {
-  const float Gf = __fmul_rn(i64_to_f32(tg), sp.inv_sg_f);
-  const float Hf = __fmul_rn(i64_to_f32(th), sp.inv_sh_f);
+  const bool small = tg > -(1LL << 45) && tg < (1LL << 45) && th > -(1LL << 45) && th < (1LL << 45);
+  const float Gf = __fmul_rn(small ? i45_to_f32(tg) : i64_to_f32(tg), sp.inv_sg_f);  // both round once
+  const float Hf = __fmul_rn(small ? i45_to_f32(th) : i64_to_f32(th), sp.inv_sh_f);
   const float den = __fadd_rn(Hf, sp.lambda_f);
   const float rlo = 8.673617379884035e-19f, rhi = 1.152921504606847e+18f;
   const float ag = fabsf(Gf);
@@ -118,17 +131,6 @@ __device__ __forceinline__ float parent_f32(int64_t tg, int64_t th, const SplitP
   return __int_as_float(0x7fc00000);  // NaN: screen_f32 then yields an infinite bound
 }
 
-// Signed 64-bit integer -> float for |x| < 2^45: x = hi * 2^23 + lo with
-// hi = x >> 23 in [-2^22, 2^22) and lo in [0, 2^23), both converted exactly
-// by magic-number constructions (1.5 * 2^23 and 2^23); the FMA rounds once,
-// so the relative error is at most u = 2^-24.
-__device__ __forceinline__ float i45_to_f32(int64_t x) {
-  const int32_t hi = (int32_t)(x >> 23);
-  const uint32_t lo = (uint32_t)x & 0x7FFFFFu;
-  const float fh = __fsub_rn(__int_as_float(0x4B400000 + hi), 12582912.0f);
-  const float fl = __fsub_rn(__int_as_float(0x4B000000u | lo), 8388608.0f);
-  return __fmaf_rn(fh, 8388608.0f, fl);
-}
 
 // Whether every candidate of a strip can use screen_fast: all its quantised
 // sums are below 2^45 in magnitude (|G| sums are bounded by sabs, the sum of
@@ -144,8 +146,10 @@ __device__ __forceinline__ bool strip_fast(int64_t sabs, int64_t th, float Gf2de
   const float gmax = __fmul_rn(i45_to_f32(sabs), sp.inv_sg_f);
   const float dmax = __fadd_rn(__fmul_rn(i45_to_f32(th), sp.inv_sh_f), sp.lambda_f);
   const float dmin = __fadd_rn(sp.inv_sh_f, sp.lambda_f);
-  const float amax = __fdiv_rn(__fmul_rn(gmax, gmax), dmin);
-  const float amin = __fdiv_rn(__fmul_rn(sp.inv_sg_f, sp.inv_sg_f), dmax);
+  // range checks with a factor 2 of margin: the approximate division (2 ulp for denominators in
+  // [2^-126, 2^126]; a larger dmax already fails its own check) decides nothing differently
+  const float amax = __fdividef(__fmul_rn(gmax, gmax), dmin);
+  const float amin = __fdividef(__fmul_rn(sp.inv_sg_f, sp.inv_sg_f), dmax);
   return sp.inv_sg_f > rlo && dmin > rlo && gmax < rhi && dmax < rhi && amax < rhi && amin > rlo &&
          __fadd_rn(__fmul_rn(3.0f, amax), sp.gamma_abs_f) < rhi;
 }
