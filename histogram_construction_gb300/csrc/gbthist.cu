@@ -101,7 +101,7 @@ struct gbt_ctx {
   DevState *st = nullptr;
   uint32_t *err_host = nullptr;  // pinned: [0] error word copy, [1] max |q| copy, [2] multi-output max |q| copy
   Buf gp_stage, chunk_prefix, partial, rows_in, offs_in, cand, splits_a, splits_b, parent_of_in, tile_counts, lrank,
-      slab, counters, level_scratch, items, side_in, pflags;
+      slab, counters, level_scratch, items, side_in, pflags, cols;
   std::string last_error;
   int64_t launches = 0;
   // tuning: work items the level plan aims for (default 1 per SM; GBT_TARGET_ITEMS overrides it for sweeps)
@@ -400,7 +400,7 @@ gbt_status gbt_destroy(gbt_ctx *c) {
   cudaStreamSynchronize(c->stream);
   Buf *bufs[] = {&c->mirror, &c->q, &c->gp_stage, &c->chunk_prefix, &c->partial, &c->rows_in, &c->offs_in,
                  &c->cand, &c->splits_a, &c->splits_b, &c->parent_of_in, &c->tile_counts, &c->lrank, &c->slab,
-                 &c->counters, &c->level_scratch, &c->qm, &c->items, &c->side_in, &c->pflags};
+                 &c->counters, &c->level_scratch, &c->qm, &c->items, &c->side_in, &c->pflags, &c->cols};
   for (Buf *b : bufs) release(c, *b);
   if (c->st) cudaFreeAsync(c->st, c->stream);
   cudaStreamSynchronize(c->stream);
@@ -457,6 +457,8 @@ gbt_status gbt_upload_bins(gbt_ctx *c, const void *bins, int bin_bytes, int64_t 
   const size_t mbytes = (size_t)((n_tiles + 1) / 2) * (size_t)n_rows * MIRROR_ROW_BYTES;
   s = ensure(c, c->mirror, mbytes, "mirror allocation");
   if (s != GBT_OK) return s;
+  s = ensure(c, c->cols, (size_t)n_features * (size_t)n_rows * bin_bytes, "slot columns");
+  if (s != GBT_OK) return s;
   c->bin_bytes = bin_bytes;
   c->n_rows = n_rows;
   c->n_features = n_features;
@@ -473,10 +475,12 @@ gbt_status gbt_upload_bins(gbt_ctx *c, const void *bins, int bin_bytes, int64_t 
     prof_begin(c);
     if (bin_bytes == 1)
       k_mirror<uint8_t><<<grid, block, 0, c->stream>>>((const uint8_t *)bins, n_rows, 0, n_rows, 0, n_features,
-                                                       n_bins, sentinel, n_rows, (uint8_t *)c->mirror.p, c->st);
+                                                       n_bins, sentinel, n_rows, (uint8_t *)c->mirror.p,
+                                                       (uint8_t *)c->cols.p, c->st);
     else
       k_mirror<uint16_t><<<grid, block, 0, c->stream>>>((const uint16_t *)bins, n_rows, 0, n_rows, 0, n_features,
-                                                        n_bins, sentinel, n_rows, (uint16_t *)c->mirror.p, c->st);
+                                                        n_bins, sentinel, n_rows, (uint16_t *)c->mirror.p,
+                                                        (uint16_t *)c->cols.p, c->st);
     LAUNCH_CHECK(c, "k_mirror");
   } else {
     // host input: one feature tile (tf feature rows, contiguous) per copy + kernel
@@ -494,11 +498,12 @@ gbt_status gbt_upload_bins(gbt_ctx *c, const void *bins, int bin_bytes, int64_t 
       if (bin_bytes == 1)
         k_mirror<uint8_t><<<grid, block, 0, c->stream>>>((const uint8_t *)c->slab.p, n_rows, 0, n_rows, f0,
                                                          n_features, n_bins, sentinel, n_rows,
-                                                         (uint8_t *)c->mirror.p, c->st);
+                                                         (uint8_t *)c->mirror.p, (uint8_t *)c->cols.p, c->st);
       else
         k_mirror<uint16_t><<<grid, block, 0, c->stream>>>((const uint16_t *)c->slab.p, n_rows, 0, n_rows, f0,
                                                           n_features, n_bins, sentinel, n_rows,
-                                                          (uint16_t *)c->mirror.p, c->st);
+                                                          (uint16_t *)c->mirror.p, (uint16_t *)c->cols.p,
+                                                          c->st);
       LAUNCH_CHECK(c, "k_mirror");
     }
     // the slab is only needed during the upload
@@ -1194,7 +1199,7 @@ gbt_status partition_impl(gbt_ctx *c, const int32_t *rows, const int64_t *node_o
   pp.n_features = c->n_features;
   pp.pad = 0;
   pp.n_rows = c->n_rows;
-  pp.mirror = (const unsigned char *)c->mirror.p;
+  pp.cols = (const unsigned char *)c->cols.p;
   pp.splits = (const SplitOut *)sp_d;
   pp.tile_counts = (int64_t *)c->tile_counts.p;
   pp.flags = (uint8_t *)c->pflags.p;

@@ -41,7 +41,7 @@ struct PartParams {
   int32_t n_features;
   int32_t pad;
   int64_t n_rows;       // also the bound on the level length
-  const unsigned char *mirror;
+  const unsigned char *cols;  // slots feature-major [n_features][n_rows], bin_bytes each
   const SplitOut *splits;
   int64_t *tile_counts;  // [n_tiles + 1] left rows per tile, then their exclusive prefix
   uint8_t *flags;        // [ceil(R / 8)] bit j of byte k / 8: position k (8-aligned k) goes left
@@ -81,9 +81,8 @@ __device__ __forceinline__ NodeRoute node_route(const PartParams &p, int n) {
 __device__ __forceinline__ int route_left(const PartParams &p, const NodeRoute &nr, int32_t r) {
   if (nr.feature < 0 || nr.feature >= p.n_features) return 1;  // no split (or an invalid one): all left
   if (r < 0 || r >= p.n_rows) return 1;
-  const int64_t tile = nr.feature / p.tile_feats, fi = nr.feature % p.tile_feats;
-  const unsigned char *strip = p.mirror + mirror_offset(tile, r, p.n_rows);
-  const uint32_t slot = p.bin_bytes == 1 ? (uint32_t)strip[fi] : (uint32_t)reinterpret_cast<const uint16_t *>(strip)[fi];
+  const int64_t at = (int64_t)nr.feature * p.n_rows + r;
+  const uint32_t slot = p.bin_bytes == 1 ? (uint32_t)p.cols[at] : (uint32_t)reinterpret_cast<const uint16_t *>(p.cols)[at];
   if (slot == (uint32_t)p.n_bins) return nr.dleft ? 1 : 0;
   return (int32_t)slot <= nr.bin ? 1 : 0;
 }

@@ -12,12 +12,15 @@ namespace gbt {
 // The mirror is the column tiling of bonsai "E6. The wide-data wall",
 // "Epilogue": each row of a feature tile is one contiguous strip, so a node's
 // gathered rows read whole 64-byte strips instead of one byte per feature.
-// grid (ceil(rows/64), n_tiles), block 256. Validates every value.
+// grid (ceil(rows/64), n_tiles), block 256. Validates every value. The slots
+// are also written feature-major into cols [n_features][n_rows]: the row
+// partition reads one feature of consecutive rows there (rows that are
+// close share a sector) instead of one 32-byte sector of the mirror per row.
 template <typename T>
 __global__ void __launch_bounds__(256) k_mirror(const T *__restrict__ bins, int64_t n_rows, int64_t row0,
                                                 int64_t rows_in_slab, int32_t f_base, int32_t n_features,
                                                 int32_t n_bins, uint32_t sentinel, int64_t bins_stride,
-                                                T *__restrict__ mirror, DevState *st) {
+                                                T *__restrict__ mirror, T *__restrict__ cols, DevState *st) {
   constexpr int TF = MIRROR_STRIP_BYTES / sizeof(T);  // features per tile
   __shared__ T sm[TF][64 + 2];
   const int tile = blockIdx.y;
@@ -41,6 +44,7 @@ __global__ void __launch_bounds__(256) k_mirror(const T *__restrict__ bins, int6
         bad = 1;
       }
       v = (T)slot;
+      cols[(int64_t)(f_base + f) * n_rows + row0 + r] = v;
     }
     sm[fl][rl] = v;
   }

@@ -105,7 +105,9 @@ gbt_status gbt_sync(gbt_ctx *ctx);
  *     (0xFF / 0xFFFF usually); must be >= n_bins and fit the width.
  * The library copies the data into its own tiled row-major mirror (64-byte
  * row strips per tile of features), validating every value on the device
- * (GBT_ERR_BIN_RANGE). The caller may free `bins` after the call returns
+ * (GBT_ERR_BIN_RANGE), and keeps a feature-major copy of the validated slots
+ * for the row partition (device memory: about 2 x n_rows x n_features x
+ * bin_bytes in all). The caller may free `bins` after the call returns
  * (device pointer) or after gbt_sync (host pointer).
  * Limits: n_rows < 2^31, n_features < 2^24. */
 gbt_status gbt_upload_bins(gbt_ctx *ctx, const void *bins, int bin_bytes, int64_t n_rows, int32_t n_features,
