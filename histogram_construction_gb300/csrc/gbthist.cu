@@ -1071,13 +1071,21 @@ gbt_status run_level_finish(gbt_ctx *c, const SmallSource &src, const int64_t *p
   if (s != GBT_OK) return s;
   const SplitParams sp = make_sp(c, params);
   prof_begin(c);
-  // staged strips: the 4-CTA register budget when the grid is more than one wave of 3 CTAs per SM;
-  // long strips: two CTAs per SM, whose register budget holds the long scan without spills
-  auto kern = c->n_bins + 1 > STAGE_SLOTS                  ? k_level_finish<FROM_PARTIALS, false, 2>
-               : (int64_t)nfb * n_pairs > 3 * (int64_t)c->n_sm ? k_level_finish<FROM_PARTIALS, true, 4>
-                                                              : k_level_finish<FROM_PARTIALS, true, 3>;
-  launch_pdl(c, kern, dim3(nfb, n_pairs), dim3(SCAN_THREADS), 0, src, parent_hist, po, large_hist, c->n_features,
-             c->n_bins, sp, (Cand *)c->cand.p, cbounds, (uint32_t *)c->counters.p, da, db, c->st, side);
+  // staged strips: when the grid is more than one wave of 3 CTAs per SM, the 4-CTA register budget
+  // and FIN_PASSES groups of four features per CTA (its selection, publication and node-reduce
+  // entries paid once for all); long strips: two CTAs per SM, whose register budget holds the long
+  // scan without spills
+#ifndef GBT_FIN_PASSES
+#define GBT_FIN_PASSES 4
+#endif
+  constexpr int FIN_PASSES = GBT_FIN_PASSES;
+  const bool many = c->n_bins + 1 <= STAGE_SLOTS && (int64_t)nfb * n_pairs > 3 * (int64_t)c->n_sm;
+  const int nfb_launch = many ? (c->n_features + 4 * FIN_PASSES - 1) / (4 * FIN_PASSES) : nfb;
+  auto kern = c->n_bins + 1 > STAGE_SLOTS ? k_level_finish<FROM_PARTIALS, false, 2, 1>
+               : many                    ? k_level_finish<FROM_PARTIALS, true, 4, FIN_PASSES>
+                                         : k_level_finish<FROM_PARTIALS, true, 3, 1>;
+  launch_pdl(c, kern, dim3(nfb_launch, n_pairs), dim3(SCAN_THREADS), 0, src, parent_hist, po, large_hist,
+             c->n_features, c->n_bins, sp, (Cand *)c->cand.p, cbounds, (uint32_t *)c->counters.p, da, db, c->st, side);
   LAUNCH_CHECK(c, FROM_PARTIALS ? "k_level_finish" : "k_subtract_find");
   if (FROM_PARTIALS) c->img_clean = c->img_r_pending;
   if (ha)

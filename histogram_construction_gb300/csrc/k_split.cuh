@@ -434,7 +434,7 @@ __device__ __forceinline__ void strip_totals(const longlong2 *cells, int B, int6
 template <int ND, int MODE, bool SKIP, typename I>
 __device__ __forceinline__ float scan_push_impl(const longlong2 *cells, bool sw, int n_bins, int64_t tg64, int64_t th64,
                                                 longlong2 m64, float Gf2den, const SplitParams &sp, int f, int node,
-                                                ScanShared &sh, int &overflow, int mode, int set_warps) {
+                                                ScanShared &sh, int &overflow, int mode, int set_warps, float lo0) {
   if (MODE >= 0) mode = MODE;
   const I tg = (I)tg64, th = (I)th64, h_min = (I)sp.h_min;  // exact: the caller checked the range for int32_t
   struct {
@@ -443,7 +443,7 @@ __device__ __forceinline__ float scan_push_impl(const longlong2 *cells, bool sw,
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int sw0 = warp - warp % set_warps;
   volatile float *vlo = sh.warp_lo;
-  float run_lo = -INFINITY;
+  float run_lo = lo0;  // a lower bound of a candidate of the same node set, found earlier (or -inf)
   I carry_g = 0, carry_h = 0;
   if (!__isShared(cells))
     asm volatile("prefetch.global.L1 [%0];" ::"l"(cells + min(32 * SCAN_SPL + SCAN_SPL * lane, n_bins)));
@@ -561,9 +561,9 @@ __device__ __forceinline__ float scan_push_impl(const longlong2 *cells, bool sw,
 // their registers do not weigh on the common copies.
 __device__ __noinline__ float scan_push_checked(const longlong2 *cells, bool sw, int n_bins, int64_t tg, int64_t th,
                                                 longlong2 m, float Gf2den, const SplitParams &sp, int f, int node,
-                                                ScanShared &sh, int &overflow, int set_warps) {
+                                                ScanShared &sh, int &overflow, int set_warps, float lo0) {
   return scan_push_impl<2, -1, false, int64_t>(cells, sw, n_bins, tg, th, m, Gf2den, sp, f, node, sh, overflow,
-                                               sp.filter ? 1 : 2, set_warps);
+                                               sp.filter ? 1 : 2, set_warps, lo0);
 }
 
 // h_ok: no H cell of the strip is negative (then every partial sum of H lies
@@ -571,7 +571,8 @@ __device__ __noinline__ float scan_push_checked(const longlong2 *cells, bool sw,
 // th, sabs and h_min are below 2^31).
 __device__ __forceinline__ float warp_scan_push(const longlong2 *cells, bool sw, int n_bins, int64_t tg, int64_t th,
                                                 int64_t sabs, bool h_ok, const SplitParams &sp, int f, int node,
-                                                ScanShared &sh, int &overflow, int set_warps) {
+                                                ScanShared &sh, int &overflow, int set_warps,
+                                                float lo0 = -INFINITY) {
   const longlong2 m = cells[sw ? swz(n_bins) : n_bins];
   const bool no_missing = (m.x == 0 && m.y == 0);
   const float Gf2den = parent_f32(tg, th, sp);
@@ -580,7 +581,8 @@ __device__ __forceinline__ float warp_scan_push(const longlong2 *cells, bool sw,
   // the common cases (fast screen, with or without missing values) get their own copies; chunk
   // skipping only pays on long strips (in global memory): a staged strip has two chunks
 #define GBT_SCAN(ND, MODE, SKIP, I, mode) \
-  scan_push_impl<ND, MODE, SKIP, I>(cells, sw, n_bins, tg, th, m, Gf2den, sp, f, node, sh, overflow, mode, set_warps)
+  scan_push_impl<ND, MODE, SKIP, I>(cells, sw, n_bins, tg, th, m, Gf2den, sp, f, node, sh, overflow, mode, set_warps, \
+                                    lo0)
   if (fast && no_missing) {
     if (sw) return i32 ? GBT_SCAN(1, 0, false, int32_t, 0) : GBT_SCAN(1, 0, false, int64_t, 0);
     return i32 ? GBT_SCAN(1, 0, true, int32_t, 0) : GBT_SCAN(1, 0, true, int64_t, 0);
@@ -589,7 +591,7 @@ __device__ __forceinline__ float warp_scan_push(const longlong2 *cells, bool sw,
     if (sw) return i32 ? GBT_SCAN(2, 0, false, int32_t, 0) : GBT_SCAN(2, 0, false, int64_t, 0);
     return i32 ? GBT_SCAN(2, 0, true, int32_t, 0) : GBT_SCAN(2, 0, true, int64_t, 0);
   }
-  return scan_push_checked(cells, sw, n_bins, tg, th, m, Gf2den, sp, f, node, sh, overflow, set_warps);
+  return scan_push_checked(cells, sw, n_bins, tg, th, m, Gf2den, sp, f, node, sh, overflow, set_warps, lo0);
 #undef GBT_SCAN
 }
 
@@ -1052,7 +1054,7 @@ struct SmallSource {
 // without the long-strip paths. CTAS: resident CTAs per SM the registers are
 // budgeted for (4 pays when the grid is several waves: more warps hide the
 // latency of each CTA's chain; 3 keeps a one-wave grid's chains shorter).
-template <bool FROM_PARTIALS, bool STAGED, int CTAS>
+template <bool FROM_PARTIALS, bool STAGED, int CTAS, int PASSES>
 __global__ void __launch_bounds__(SCAN_THREADS, CTAS) k_level_finish(
     SmallSource src, const int64_t *__restrict__ parent, const int32_t *__restrict__ parent_of,
     int64_t *__restrict__ large, int32_t n_features, int32_t n_bins, SplitParams sp, Cand *__restrict__ cand,
@@ -1062,16 +1064,16 @@ __global__ void __launch_bounds__(SCAN_THREADS, CTAS) k_level_finish(
   const int p = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int fo = warp & 3, side = warp >> 2;
-  const int f = blockIdx.x * 4 + fo;
   const int B = n_bins + 1;
   const bool staged = STAGED;  // B <= STAGE_SLOTS (the host picks the instance)
-  const bool active = f < n_features;
   const int64_t pp = parent_of ? (int64_t)parent_of[p] : p;
-  const longlong2 *P = reinterpret_cast<const longlong2 *>(parent) + (pp * n_features + f) * B;
+  const int fcta = blockIdx.x * 4 * PASSES;  // the CTA's first feature: PASSES groups of four, one per pass
   // The parent strips (and parent_of) were complete before the kernel this one
-  // waits for started, so warps 4-7 stage them while that kernel finishes.
-  if (side == 1 && active && staged)
-    for (int s = lane; s < B; s += 32) sh.cells[warp][swz(s)] = __ldg(P + s);
+  // waits for started, so warps 4-7 stage the first pass's while that kernel finishes.
+  if (side == 1 && fcta + fo < n_features && staged) {
+    const longlong2 *P0 = reinterpret_cast<const longlong2 *>(parent) + (pp * n_features + fcta + fo) * B;
+    for (int s = lane; s < B; s += 32) sh.cells[warp][swz(s)] = __ldg(P0 + s);
+  }
   pdl_wait();  // the histogram kernel (or whatever ran before on the stream)
   if (FROM_PARTIALS && !st->plan_ok) return;
   scan_init(sh);
@@ -1080,6 +1082,37 @@ __global__ void __launch_bounds__(SCAN_THREADS, CTAS) k_level_finish(
     const int sd = node_side[p] & 1;
     si = 2 * (int64_t)p + sd;
     li = 2 * (int64_t)p + 1 - sd;
+  }
+  int32_t g0 = 0, g1 = 0, i0 = 0;  // the small sibling's exclusive groups and first group image
+  if (FROM_PARTIALS) {
+    g0 = src.view.group_prefix[p];
+    g1 = src.view.group_prefix[p + 1];
+    i0 = src.view.img_first[p];
+  }
+  float wlo = -INFINITY;  // this warp's best lower bound over its passes
+  int ovf_any = 0;        // some pass of this warp overflowed the pool
+  for (int pass = 0; pass < PASSES; ++pass) {
+  const int f = fcta + 4 * pass + fo;
+  const bool active = f < n_features;
+  const longlong2 *P = reinterpret_cast<const longlong2 *>(parent) + (pp * n_features + f) * B;
+  if (pass > 0) {
+    __syncthreads();  // every warp is done with the previous pass's staged strips
+    if (side == 1 && active && staged)
+      for (int s = lane; s < B; s += 32) sh.cells[warp][swz(s)] = __ldg(P + s);
+  }
+  if (STAGED && pass + 1 < PASSES && fcta + 4 * pass + 4 < n_features) {
+    // the next pass's parent strips (four strips of 16-byte cells, one 128-byte line per thread) and
+    // group image rows (one sector per slot and group) on their way to L2 while this pass runs
+    const int fn = fcta + 4 * pass + 4;
+    const int64_t ncells = (int64_t)min(4, n_features - fn) * B;
+    if ((int64_t)threadIdx.x * 8 < ncells)
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<const longlong2 *>(parent) +
+                                                    (pp * n_features + fn) * B + threadIdx.x * 8));
+    if (FROM_PARTIALS && (int)threadIdx.x < B) {
+      const int2 *img = image_cell(src.view, i0, fn, src.item_feats, (int)threadIdx.x);
+      const int64_t stride = src.view.n_fgroups * src.view.image_int4s * 2;
+      for (int32_t k = g0; k < g1; ++k, img += stride) asm volatile("prefetch.global.L2 [%0];" ::"l"(img));
+    }
   }
   longlong2 *L = reinterpret_cast<longlong2 *>(large) + (li * n_features + f) * B;
   longlong2 *Sout = FROM_PARTIALS ? reinterpret_cast<longlong2 *>(src.hist_out) + (si * n_features + f) * B
@@ -1092,11 +1125,10 @@ __global__ void __launch_bounds__(SCAN_THREADS, CTAS) k_level_finish(
     // takes feature t & 3 and slots (t >> 2) + 64 u, eight loads in flight,
     // so each warp load covers 8 slots x 4 features (whole 32-byte sectors)
     constexpr int PA = STAGED ? STAGE_SLOTS / 64 : 8;  // a staged strip has at most 4 slots per thread
-    const int t = threadIdx.x, fi = t & 3, ff = blockIdx.x * 4 + fi;
+    const int t = threadIdx.x, fi = t & 3, ff = fcta + 4 * pass + fi;
     int64_t pg = 0, ph = 0, pa = 0;  // long strips: this thread's part of feature fi's totals
     bool pn = false;
     if (ff < n_features) {
-      const int32_t g0 = src.view.group_prefix[p], g1 = src.view.group_prefix[p + 1], i0 = src.view.img_first[p];
       const bool zero = i0 < src.view.r_cap;  // reduce-region images are zeroed as they are read
       const int64_t stride = src.view.n_fgroups * src.view.image_int4s * 2;
       int2 *img0 = image_cell(src.view, i0, ff, src.item_feats, 0);
@@ -1241,25 +1273,34 @@ __global__ void __launch_bounds__(SCAN_THREADS, CTAS) k_level_finish(
     }
     const bool h_ok = !__any_sync(0xffffffffu, hneg);
     int ovf = 0;
-    const float wlo = warp_scan_push(cells, staged, n_bins, tg, th, sa, h_ok, sp, f, side, sh, ovf, 4);
+    wlo = warp_scan_push(cells, staged, n_bins, tg, th, sa, h_ok, sp, f, side, sh, ovf, 4, wlo);
     ovf = __any_sync(0xffffffffu, ovf);
+    ovf_any |= ovf;
     if (lane == 0) {
       sh.warp_lo[warp] = wlo;
       sh.warp_overflow[warp] = ovf;
     }
   }
   __syncthreads();
-  float thr0 = -INFINITY, thr1 = -INFINITY;  // the small and the large set's best lower bound
+  float thr0 = -INFINITY, thr1 = -INFINITY;  // the small and the large set's best lower bound so far
 #pragma unroll
   for (int w = 0; w < SCAN_WARPS / 2; ++w) {
     thr0 = fmaxf(thr0, sh.warp_lo[w]);
     thr1 = fmaxf(thr1, sh.warp_lo[w + SCAN_WARPS / 2]);
   }
-  if (active && sh.warp_overflow[warp]) {
+  if (active && sh.warp_overflow[warp]) {  // this pass's strip overflowed: the warp rescans it now
     const Cand d = warp_direct_best(cells, staged, n_bins, tg, th, sp, side ? thr1 : thr0, f);
-    if (lane == 0) sh.extra[warp] = d;
+    if (lane == 0 && cand_better(d, sh.extra[warp])) sh.extra[warp] = d;
   }
+  }  // passes
+  if (lane == 0) sh.warp_overflow[warp] = ovf_any;  // the select takes sh.extra of every warp that overflowed
   __syncthreads();
+  float thr0 = -INFINITY, thr1 = -INFINITY;
+#pragma unroll
+  for (int w = 0; w < SCAN_WARPS / 2; ++w) {
+    thr0 = fmaxf(thr0, sh.warp_lo[w]);
+    thr1 = fmaxf(thr1, sh.warp_lo[w + SCAN_WARPS / 2]);
+  }
   cta_select(sh, sp, 2, thr0, thr1, 2);
   const int nfb = gridDim.x;
   const int64_t es = (int64_t)(2 * p) * nfb * PUB_K, el = es + (int64_t)nfb * PUB_K;  // the siblings' first entries

@@ -270,6 +270,43 @@ def test_level_finish_near_ties(gb, oracle_mod, n_bins, G, H, GL, lam):
         s.close()
 
 
+def _widened(case, n_features=700, moves=((13, 301), (9, 450), (17, 602))):
+    """The case's histograms with features appended (copies of features 0-2, weak in every node) up to
+    n_features, and some designed features moved far away (swapped with appended ones), so that the
+    near-tied candidates fall in different CTAs and in different passes of one CTA of a grid of many
+    waves."""
+    h = case.h
+    extra = np.tile(h[:, 0:3], (1, (n_features - h.shape[1] + 2) // 3, 1, 1))[:, : n_features - h.shape[1]]
+    h = np.concatenate([h, extra], axis=1)
+    for a, b in moves:
+        h[:, [a, b]] = h[:, [b, a]]
+    return np.ascontiguousarray(h)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("n_bins,G,H,GL,lam", [x for x in SETTINGS if x[0] == 255])
+def test_level_finish_near_ties_many_waves(gb, oracle_mod, n_bins, G, H, GL, lam):
+    """test_level_finish_near_ties on 700 features: the fused finish runs its many-wave form (several
+    groups of four features per CTA, in passes)."""
+    g, Session, s2n = gb
+    small = _widened(_build(n_bins, G, H, GL, lam))
+    large = small[::-1].copy()
+    parent = small + large
+    ref_s, _ = oracle_mod.find_splits(small, n_bins, lam, 0.0, 0.0, 1.0, 1.0)
+    ref_l, _ = oracle_mod.find_splits(large, n_bins, lam, 0.0, 0.0, 1.0, 1.0)
+    assert set(int(x) for x in ref_s["feature"]) <= {3, 301, 450, 16, 602, 18, 19, 21}
+    s = _session(Session, n_bins, small.shape[1])
+    try:
+        got_large, so, lo = s.subtract_and_find(torch.from_numpy(parent).cuda(), torch.from_numpy(small).cuda(),
+                                                lam=lam)
+        assert s.sync() == 0
+        np.testing.assert_array_equal(got_large.cpu().numpy(), large)
+        _same(s2n(so), ref_s, f"finish small many waves lam={lam}")
+        _same(s2n(lo), ref_l, f"finish large many waves lam={lam}")
+    finally:
+        s.close()
+
+
 def test_near_tie_cases_are_what_they_claim(oracle_mod):
     """CPU check of the case builder against the oracle's gain: each designed pair differs by the stated
     number of ulps (runs without a GPU)."""
