@@ -866,8 +866,8 @@ gbt_status gbt_find_splits(gbt_ctx *c, const int64_t *hist, int32_t n_nodes, con
   if (s != GBT_OK) return s;
   const SplitParams sp = make_sp(c, params);
   prof_begin(c);
-  k_find<<<dim3(nfb, n_nodes), SCAN_THREADS, 0, c->stream>>>(hist, c->n_features, c->n_bins, sp, (Cand *)c->cand.p,
-                                                             (uint32_t *)c->counters.p, dout);
+  launch_pdl(c, k_find, dim3(nfb, n_nodes), dim3(SCAN_THREADS), 0, hist, c->n_features, c->n_bins, sp,
+             (Cand *)c->cand.p, (uint32_t *)c->counters.p, dout);
   LAUNCH_CHECK(c, "k_find");
   if (host)
     CUDA_TRY(c, cudaMemcpyAsync(out, dout, (size_t)n_nodes * sizeof(gbt_split), cudaMemcpyDeviceToHost, c->stream),
@@ -1080,9 +1080,13 @@ gbt_status run_level_finish(gbt_ctx *c, const SmallSource &src, const int64_t *p
 #endif
   constexpr int FIN_PASSES = GBT_FIN_PASSES;
   const bool many = c->n_bins + 1 <= STAGE_SLOTS && (int64_t)nfb * n_pairs > 3 * (int64_t)c->n_sm;
-  const int nfb_launch = many ? (c->n_features + 4 * FIN_PASSES - 1) / (4 * FIN_PASSES) : nfb;
+  // passes only while the grid of passes still fills three waves of four CTAs per SM (fewer, longer
+  // chains would leave SMs idle)
+  const bool passes = many && (int64_t)nfb * n_pairs / FIN_PASSES >= 3 * 4 * (int64_t)c->n_sm;
+  const int nfb_launch = passes ? (c->n_features + 4 * FIN_PASSES - 1) / (4 * FIN_PASSES) : nfb;
   auto kern = c->n_bins + 1 > STAGE_SLOTS ? k_level_finish<FROM_PARTIALS, false, 2, 1>
-               : many                    ? k_level_finish<FROM_PARTIALS, true, 4, FIN_PASSES>
+               : passes                  ? k_level_finish<FROM_PARTIALS, true, 4, FIN_PASSES>
+               : many                    ? k_level_finish<FROM_PARTIALS, true, 4, 1>
                                          : k_level_finish<FROM_PARTIALS, true, 3, 1>;
   launch_pdl(c, kern, dim3(nfb_launch, n_pairs), dim3(SCAN_THREADS), 0, src, parent_hist, po, large_hist,
              c->n_features, c->n_bins, sp, (Cand *)c->cand.p, cbounds, (uint32_t *)c->counters.p, da, db, c->st, side);

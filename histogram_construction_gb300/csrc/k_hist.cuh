@@ -1086,7 +1086,8 @@ __device__ __forceinline__ int2 *image_cell(const PartialView &v, int32_t group,
 __global__ void __launch_bounds__(256) k_finalize(PartialView v, int32_t n_nodes, int32_t n_features,
                                                   int32_t item_feats, int64_t *__restrict__ hist_out,
                                                   const DevState *st) {
-  pdl_wait();  // the histogram kernel
+  pdl_wait();     // the histogram kernel
+  pdl_trigger();  // the split find may launch; it waits for this grid to finish
   if (!st->plan_ok) return;
   const int nq = (n_features + 3) >> 2;
   const int64_t units = (int64_t)n_nodes * nq * v.B * 4;

@@ -978,6 +978,7 @@ __global__ void __launch_bounds__(SCAN_THREADS, 3) k_find(const int64_t *__restr
                                                        int32_t n_bins, SplitParams sp, Cand *__restrict__ cand,
                                                        uint32_t *__restrict__ counters, SplitOut *__restrict__ out) {
   __shared__ ScanShared sh;
+  pdl_wait();  // the kernel that wrote hist, when launched as its dependent (a no-op otherwise)
   const int node = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int f = blockIdx.x * SCAN_WARPS + warp;
