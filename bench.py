@@ -364,7 +364,7 @@ def level_summary(ms, entries, level_bytes, peak):
                                "frac": level_bytes / (t / 1e3) / 1e9 / peak, "peak": peak}}
 
 
-KERNELS = ["k_hist_u8", "k_hist_u16", "k_level_plan", "k_subtract_find", "k_level_finish", "k_finalize", "k_find",
+KERNELS = ["k_gather_q", "k_hist_u8", "k_hist_u16", "k_level_plan", "k_subtract_find", "k_level_finish", "k_finalize", "k_find",
            "k_part_flags", "k_part_scan", "k_part_scatter"]
 
 

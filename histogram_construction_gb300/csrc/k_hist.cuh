@@ -70,7 +70,25 @@ struct LevelParams {
   int32_t fold;           // 1: the histogram kernel plans the level itself (n_nodes <= FOLD_MAX_NODES)
   int32_t pad_;
   DevState *st;
+  const int2 *qpos = nullptr;  // if set: q of the level's rows in level order, qpos[k] = q[rows[k]] (k_gather_q)
 };
+
+// The level's (qg, qh) pairs in level order, qpos[k] = q[rows[k]] (zero for an
+// id outside [0, n_rows), which the histogram kernel reports). With many
+// feature tiles every work item of a row would otherwise gather its pair by
+// row id, one sector per row and tile; in level order eight rows share one
+// 64-byte load. Grid-stride over the level's positions.
+__global__ void __launch_bounds__(256) k_gather_q(const int32_t *__restrict__ rows, const int64_t *__restrict__ offs,
+                                                  int32_t n_nodes, int64_t n_rows, const int2 *__restrict__ q,
+                                                  int2 *__restrict__ qpos) {
+  pdl_wait();  // the kernel that wrote the row list
+  pdl_trigger();
+  const int64_t R = min(max(offs[n_nodes], (int64_t)0), n_rows);
+  for (int64_t k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; k < R; k += (int64_t)gridDim.x * blockDim.x) {
+    const int32_t r = rows[k];
+    qpos[k] = (uint32_t)r < (uint32_t)n_rows ? __ldg(q + r) : make_int2(0, 0);
+  }
+}
 
 // Block-wide inclusive scan of one int64 per thread (every thread calls it).
 __device__ __forceinline__ int64_t block_incl_scan(int64_t v, int64_t *s_warp) {
@@ -609,7 +627,7 @@ __device__ __forceinline__ void h8_issue(const LevelParams &p, const unsigned ch
     if (MULTI) {
       qv[u] = ld ? __ldg(p.q + (int64_t)r * k + tsel) : make_int2(0, 0);
     } else {
-      qv[u] = valid ? __ldg(p.q + r) : make_int2(0, 0);
+      qv[u] = valid ? __ldg(p.qpos ? p.qpos + kb + u * step : p.q + r) : make_int2(0, 0);
     }
     cp_async_16(ring_dst + (uint32_t)u * 512u, ld ? strip + (int64_t)r * MIRROR_ROW_BYTES : strip, ld ? 16u : 0u);
   }
@@ -970,7 +988,7 @@ __global__ void __launch_bounds__(H16_THREADS, 1) k_hist_u16(Hist16Params P) {
         const int32_t r = R[u];
         const bool valid = (uint32_t)r < (uint32_t)N;
         bad |= (gb + u * step + rho < it.k1 && !valid) ? 1u : 0u;
-        const int2 qv = valid ? __ldg(p.q + r) : make_int2(0, 0);
+        const int2 qv = valid ? __ldg(p.qpos ? p.qpos + gb + u * step + rho : p.q + r) : make_int2(0, 0);
         vg[u] = qv.x;
         vh[u] = qv.y;
         bw[u] = valid ? __ldg(reinterpret_cast<const uint32_t *>(strip + (int64_t)r * MIRROR_ROW_BYTES)) : 0u;
