@@ -231,6 +231,20 @@ int ptr_kind(const void *p) {
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// The device's address of pinned (page-locked) host memory, or nullptr for any other pointer. Kernels
+// read and write such memory in place (over the host link), which for small buffers costs less than a
+// copy's launch and completion.
+void *pinned_device_ptr(const void *p) {
+  if (!p) return nullptr;
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  return a.type == cudaMemoryTypeHost ? a.devicePointer : nullptr;
+}
+constexpr size_t ZERO_COPY_MAX_BYTES = 64 << 10;  // small pinned inputs are read in place
+
 // Return a device pointer holding `bytes` of `src` (copied into `stage` when src is host memory).
 gbt_status device_view(gbt_ctx *c, const void *src, size_t bytes, Buf &stage, const void **out, const char *what) {
   const int k = ptr_kind(src);
@@ -238,6 +252,12 @@ gbt_status device_view(gbt_ctx *c, const void *src, size_t bytes, Buf &stage, co
   if (k == 1) {
     *out = src;
     return GBT_OK;
+  }
+  if (bytes <= ZERO_COPY_MAX_BYTES) {
+    if (void *d = pinned_device_ptr(src)) {
+      *out = d;
+      return GBT_OK;
+    }
   }
   gbt_status s = ensure(c, stage, bytes, what);
   if (s != GBT_OK) return s;
@@ -852,6 +872,11 @@ static gbt_status split_out_view(gbt_ctx *c, gbt_split *out, int32_t n, Buf &sta
   *host = (k == 0);
   if (k == 1) {
     *dev = reinterpret_cast<SplitOut *>(out);
+    return GBT_OK;
+  }
+  if (void *d = pinned_device_ptr(out)) {  // the kernels write the pinned host records in place
+    *dev = reinterpret_cast<SplitOut *>(d);
+    *host = false;
     return GBT_OK;
   }
   gbt_status s = ensure(c, stage, (size_t)n * sizeof(SplitOut), "split staging");

@@ -97,6 +97,40 @@ def test_root_full_size(gb, oracle_mod):
         assert_splits_equal(s2n(out), rs, "root")
 
 
+@pytest.mark.parametrize("n_rows", [30_000, 60_000])
+def test_level_step_pinned_host_buffers(gb, oracle_mod, n_rows):
+    """gbt_level_step with page-locked host buffers: the offsets and the split records are read and written
+    in place by the kernels; the row list in place too when small (30,000 rows: about 11,000 built rows),
+    else copied (60,000 rows)."""
+    g, Session, s2n = gb
+    w = synth.make("level5", n_rows=n_rows)
+    sg, sh = _scales(w)
+    q, _ = oracle_mod.quantise(w.gpair, sg, sh)
+    par, lv = w.levels[4], w.levels[5]
+    ref_hp, _ = oracle_mod.build_hist(w.bins, w.n_bins, w.sentinel, q, par.rows, par.offsets)
+    ref_hs, _ = oracle_mod.build_hist(w.bins, w.n_bins, w.sentinel, q, lv.built_rows, lv.built_offsets)
+    ref_large, _ = oracle_mod.subtract(ref_hp, None, ref_hs)
+    ref_so, _ = oracle_mod.find_splits(ref_hs, w.n_bins, 1.0, 0.0, 0.0, sg, sh)
+    ref_lo, _ = oracle_mod.find_splits(ref_large, w.n_bins, 1.0, 0.0, 0.0, sg, sh)
+    with Session() as s:
+        s.upload_bins(w.bins, w.n_bins, w.sentinel).begin_tree(w.gpair, sg, sh)
+        hp = s.build_level(par.rows, torch.from_numpy(par.offsets).cuda())
+        n_p = len(lv.built_offsets) - 1
+        rows_h = torch.from_numpy(lv.built_rows).pin_memory()
+        offs_h = torch.from_numpy(lv.built_offsets).pin_memory()
+        so_h = torch.zeros((n_p, g.SPLIT_BYTES), dtype=torch.uint8).pin_memory()
+        lo_h = torch.zeros((n_p, g.SPLIT_BYTES), dtype=torch.uint8).pin_memory()
+        hs = s.hist_tensor(n_p)
+        large = torch.empty_like(hs)
+        s.check(g.gbt_level_step(s.ctx, rows_h, offs_h, n_p, hp, None, hs, large, g.params(1.0, 0.0, 0.0), so_h,
+                                 lo_h))
+        assert s.sync() == 0
+        np.testing.assert_array_equal(hs.cpu().numpy(), ref_hs, err_msg="small hist")
+        np.testing.assert_array_equal(large.cpu().numpy(), ref_large, err_msg="large hist")
+        assert_splits_equal(s2n(so_h), ref_so, "pinned small splits")
+        assert_splits_equal(s2n(lo_h), ref_lo, "pinned large splits")
+
+
 @pytest.mark.parametrize("plan_kernel", [False, True])
 @pytest.mark.parametrize("n_rows,host_offsets", [(60_000, False), (200_000, True)])
 def test_level5_reduced(gb, oracle_mod, monkeypatch, n_rows, host_offsets, plan_kernel):
