@@ -14,7 +14,7 @@
  * cudaPointerGetAttributes: device (or managed) memory is read in place, host
  * memory is copied on the context stream first (pinned host memory keeps that
  * copy asynchronous; pageable host memory makes it synchronous). Pinned host
- * inputs of up to 64 KiB, and pinned host split outputs, are read and written
+ * inputs of up to 4 MiB, and pinned host split outputs, are read and written
  * in place by the kernels instead (keep them unchanged, or unread, until
  * gbt_sync, as for a copy). Arguments documented "device" must be device
  * memory.

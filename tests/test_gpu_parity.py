@@ -99,9 +99,8 @@ def test_root_full_size(gb, oracle_mod):
 
 @pytest.mark.parametrize("n_rows", [30_000, 60_000])
 def test_level_step_pinned_host_buffers(gb, oracle_mod, n_rows):
-    """gbt_level_step with page-locked host buffers: the offsets and the split records are read and written
-    in place by the kernels; the row list in place too when small (30,000 rows: about 11,000 built rows),
-    else copied (60,000 rows)."""
+    """gbt_level_step with page-locked host buffers: the row list, the offsets and the split records are
+    read and written in place by the kernels (pageable host buffers, copied first, are the other tests')."""
     g, Session, s2n = gb
     w = synth.make("level5", n_rows=n_rows)
     sg, sh = _scales(w)
