@@ -1042,12 +1042,13 @@ struct SmallSource {
   int64_t *hist_out;
 };
 
-// Level finish: grid (ceil(F / 4), n_pairs), 8 warps. Warp w takes feature
-// blockIdx.x * 4 + (w & 3) of pair blockIdx.y; warps 0-3 form the small
-// sibling's strip (read, or summed from the build's chunk partials and
-// written out), warps 4-7 load the parent strip and form Large = Parent -
-// Small (written out). Every warp then scans its strip; the last CTA of pair
-// p writes small_out[p] and large_out[p]. With node_side (node order), pair
+// Level finish: grid (ceil(F / (4 PASSES)), n_pairs), 8 warps. In pass k,
+// warp w takes feature (blockIdx.x * PASSES + k) * 4 + (w & 3) of pair
+// blockIdx.y; warps 0-3 form the small sibling's strip (read, or summed from
+// the build's chunk partials and written out), warps 4-7 load the parent
+// strip and form Large = Parent - Small (written out). Every warp then scans
+// its strip; after the last pass the CTA selects and publishes once, and the
+// last CTA of pair p writes small_out[p] and large_out[p]. With node_side (node order), pair
 // p's outputs go to node 2p + node_side[p] (small) and 2p + 1 - node_side[p] (large) of
 // one level array instead (the small histogram's own index, small_out and
 // hist_out, and large / large_out then name the same arrays).
@@ -1055,6 +1056,8 @@ struct SmallSource {
 // without the long-strip paths. CTAS: resident CTAs per SM the registers are
 // budgeted for (4 pays when the grid is several waves: more warps hide the
 // latency of each CTA's chain; 3 keeps a one-wave grid's chains shorter).
+// PASSES: groups of four features per CTA, taken one after the other (the
+// selection, publication and node-reduce entries are then paid once for all).
 template <bool FROM_PARTIALS, bool STAGED, int CTAS, int PASSES>
 __global__ void __launch_bounds__(SCAN_THREADS, CTAS) k_level_finish(
     SmallSource src, const int64_t *__restrict__ parent, const int32_t *__restrict__ parent_of,
