@@ -1079,19 +1079,23 @@ __global__ void __launch_bounds__(SCAN_THREADS, CTAS) k_level_finish(
     for (int s = lane; s < B; s += 32) sh.cells[warp][swz(s)] = __ldg(P0 + s);
   }
   pdl_wait();  // the histogram kernel (or whatever ran before on the stream)
-  if (FROM_PARTIALS && !st->plan_ok) return;
+  // the plan's verdict and this pair's groups in one round trip (the arrays exist whatever the verdict;
+  // no image address is formed from them unless the plan is valid)
+  int32_t g0 = 0, g1 = 0, i0 = 0;  // the small sibling's exclusive groups and first group image
+  uint32_t plan_ok = 1;
+  if (FROM_PARTIALS) {
+    plan_ok = st->plan_ok;
+    g0 = src.view.group_prefix[p];
+    g1 = src.view.group_prefix[p + 1];
+    i0 = src.view.img_first[p];
+  }
+  if (!plan_ok) return;
   scan_init(sh);
   int64_t si = p, li = p;  // output indices of the small and the large sibling
   if (node_side) {
     const int sd = node_side[p] & 1;
     si = 2 * (int64_t)p + sd;
     li = 2 * (int64_t)p + 1 - sd;
-  }
-  int32_t g0 = 0, g1 = 0, i0 = 0;  // the small sibling's exclusive groups and first group image
-  if (FROM_PARTIALS) {
-    g0 = src.view.group_prefix[p];
-    g1 = src.view.group_prefix[p + 1];
-    i0 = src.view.img_first[p];
   }
   float wlo = -INFINITY;  // this warp's best lower bound over its passes
   int ovf_any = 0;        // some pass of this warp overflowed the pool
