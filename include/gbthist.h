@@ -47,7 +47,7 @@ typedef enum {
   GBT_ERR_BIN_RANGE = 5,      /* device: a bin value was neither < n_bins nor the sentinel */
   GBT_ERR_ROW_RANGE = 6,      /* device: a row index was outside [0, n_rows), or offsets not ascending */
   GBT_ERR_QUANT_OVERFLOW = 7, /* device: a quantised value beyond this library's limit |q| <= 2^21-1, or not finite */
-  GBT_ERR_UNSUPPORTED = 8,    /* a size beyond this build's limits */
+  GBT_ERR_UNSUPPORTED = 8,    /* a size beyond this library's limits */
   GBT_ERR_TIMEOUT = 9,        /* device: a bounded wait ran out */
   GBT_ERR_INCONSISTENT = 10   /* device: subtraction produced a negative hessian cell */
 } gbt_status;
