@@ -392,7 +392,6 @@ struct ScanShared {
 // left direction can never win); mode 0: screen_fast, 1: screen_f32, 2: no
 // screen (every valid candidate pushed with an infinite upper bound); MODE
 // fixes it at compile time, or -1 takes `mode`.
-__device__ __forceinline__ bool no_missing_rt(longlong2 m) { return m.x == 0 && m.y == 0; }
 
 // Lane partial sums (G, H, |G|) of a strip in global memory, FIN_BATCH loads
 // in flight per lane (a loop that used each load at once would wait for every
