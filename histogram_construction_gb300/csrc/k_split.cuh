@@ -778,9 +778,47 @@ __device__ __forceinline__ int warp_argmax_lane(const Cand &best) {
 // best published lower bound; candidates whose upper bound reaches it are
 // evaluated in double (unless exact already) and the best one is written to
 // out. slot: nthr / 32 Cand of shared scratch, sthr: nthr / 32 floats.
+// With rcnt (a shared counter) and at most one entry per thread, each thread reads its record once, the
+// block settles the threshold, and a short list takes the argmax of the few evaluated records.
 __device__ __forceinline__ void reduce_node(const Cand *cand, int n_ent, const SplitParams &sp, SplitOut *out,
-                                            int t0, int nthr, int bar, Cand *slot, float *sthr) {
+                                            int t0, int nthr, int bar, Cand *slot, float *sthr, int *rcnt = nullptr) {
   const int t = threadIdx.x - t0, lane = threadIdx.x & 31, w = t >> 5, nw = nthr >> 5;
+  if (rcnt && n_ent <= nthr) {
+    Cand c = t < n_ent ? load_cand(cand + t) : no_cand();
+    float thr = c.lo;  // -inf for no record
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) thr = fmaxf(thr, __shfl_xor_sync(0xffffffffu, thr, o));
+    if (lane == 0) sthr[w] = thr;
+    if (t == 0) *rcnt = 0;
+    named_sync(bar, nthr);
+    for (int k = 0; k < nw; ++k) thr = fmaxf(thr, sthr[k]);
+    const bool take = c.f != INT32_MAX && c.up >= thr;
+    if (take) {
+      if (!c.exact) set_exact(c, surv_gain(c.gl, c.hl, c.gl + c.gr, c.hl + c.hr, sp));
+      const int k = atomicAdd(rcnt, 1);
+      if (k < nw) slot[k] = c;
+    }
+    named_sync(bar, nthr);
+    const int nc = *rcnt;
+    if (nc <= nw) {
+      if (t == 0) {
+        Cand b = no_cand();
+        for (int k = 0; k < nc; ++k)
+          if (cand_better(slot[k], b)) b = slot[k];
+        *out = cand_to_split(b);
+      }
+      return;
+    }
+    named_sync(bar, nthr);  // every thread has read the count before the list is overwritten
+    const Cand best = take ? c : no_cand();
+    if (lane == warp_argmax_lane(best)) slot[w] = best;
+    named_sync(bar, nthr);
+    if (w == 0) {
+      const Cand b = lane < nw ? slot[lane] : no_cand();
+      if (lane == warp_argmax_lane(b)) *out = cand_to_split(b);
+    }
+    return;
+  }
   constexpr int RB = 8;  // loads in flight per thread
   float thr = -INFINITY;
   for (int i0 = t; i0 < n_ent; i0 += nthr * RB) {
@@ -1026,7 +1064,7 @@ __global__ void __launch_bounds__(SCAN_THREADS, 3) k_find(const int64_t *__restr
   const int nfb = gridDim.x;
   Cand *cn = cand + (int64_t)node * nfb * PUB_K;
   if (cta_publish(sh, 1, cn + blockIdx.x * PUB_K, nullptr, counters + node, nfb)) {
-    reduce_node(cn, nfb * PUB_K, sp, out + node, 0, SCAN_THREADS, 1, sh.extra, sh.red);
+    reduce_node(cn, nfb * PUB_K, sp, out + node, 0, SCAN_THREADS, 1, sh.extra, sh.red, sh.rcnt);
   }
 }
 
