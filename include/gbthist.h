@@ -259,12 +259,10 @@ gbt_status gbt_find_level_split(gbt_ctx *ctx, const int64_t *hist, int32_t n_nod
  * every device that loads it until the process exits. Limits per call:
  * n_nodes <= 4096 and n_nodes * ceil(n_features / 8) <= 32768; beyond them
  * the call returns GBT_ERR_UNSUPPORTED before touching the device. The first
- * call on each device looks up that array's device address (make it before
- * any stream capture); the address is looked up again when the calling
- * thread's current context is another one than at the last lookup, e.g.
- * after cudaDeviceReset created the device's primary context anew (make the
- * first call after such a change outside stream capture too). Every call uses
- * the same array and clears only its
+ * call on each device looks up that array's device address; the address is
+ * looked up again when the calling thread's current context is another one
+ * than at the last lookup, e.g. after cudaDeviceReset created the device's
+ * primary context anew. Every call uses the same array and clears only its
  * arrival counters: calls whose work overlaps on the GPU (other streams,
  * other threads) race on it, so order them on one stream or synchronise.
  * Errors: GBT_ERR_INVALID_ARG (NULL, bad sizes or scales, host or misaligned
